@@ -1,0 +1,190 @@
+"""FP64 CPU oracle for convolution forward and input gradient.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the package smoke check
+and by the benchmark's CPU-baseline leg, never by the product path.  It shares
+no code with the CUDA library; the only thing both sides take is the seeded
+input generator in ``synth``.
+
+The arithmetic lives in ``conv_oracle.c`` (plain nested loops, double
+accumulation); this module compiles it with gcc when needed and marshals numpy
+arrays through ctypes.  See that file's header for the definitions it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in (
+        "n", "c_in", "c_out", "groups", "in_h", "in_w", "k_h", "k_w",
+        "s_h", "s_w", "p_h", "p_w", "d_h", "d_w")] + [
+        ("nhwc", ctypes.c_int32), ("w_ohwi", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class Conv:
+    """Shape of one convolution as the oracle sees it.
+
+    ``spatial_dims`` is 1 for conv1d (NCL / NLC; ``in_hw = (1, L)``) and 2 for
+    conv2d.  ``nhwc`` selects channels-last activations, ``w_ohwi`` selects the
+    [C_out, KH, KW, C_in/G] weight order instead of [C_out, C_in/G, KH, KW].
+    """
+    n: int
+    c_in: int
+    c_out: int
+    in_hw: tuple
+    k: tuple
+    stride: tuple = (1, 1)
+    pad: tuple = (0, 0)
+    dil: tuple = (1, 1)
+    groups: int = 1
+    nhwc: bool = False
+    w_ohwi: bool = False
+    spatial_dims: int = 2
+
+    def _c(self) -> _Desc:
+        return _Desc(self.n, self.c_in, self.c_out, self.groups, self.in_hw[0], self.in_hw[1],
+                     self.k[0], self.k[1], self.stride[0], self.stride[1], self.pad[0], self.pad[1],
+                     self.dil[0], self.dil[1], int(self.nhwc), int(self.w_ohwi))
+
+    def out_hw(self):
+        oh = out_size(self.in_hw[0], self.k[0], self.stride[0], self.pad[0], self.dil[0])
+        ow = out_size(self.in_hw[1], self.k[1], self.stride[1], self.pad[1], self.dil[1])
+        return oh, ow
+
+    def x_shape(self):
+        return _act_shape(self, self.c_in, self.in_hw)
+
+    def y_shape(self):
+        return _act_shape(self, self.c_out, self.out_hw())
+
+    def w_shape(self):
+        cpg = self.c_in // self.groups
+        if self.spatial_dims == 1:
+            return (self.c_out, self.k[1], cpg) if self.w_ohwi else (self.c_out, cpg, self.k[1])
+        if self.w_ohwi:
+            return (self.c_out, self.k[0], self.k[1], cpg)
+        return (self.c_out, cpg, self.k[0], self.k[1])
+
+
+def _act_shape(c: Conv, ch: int, hw):
+    if c.spatial_dims == 1:
+        return (c.n, hw[1], ch) if c.nhwc else (c.n, ch, hw[1])
+    return (c.n, hw[0], hw[1], ch) if c.nhwc else (c.n, ch, hw[0], hw[1])
+
+
+def build(force: bool = False) -> str:
+    """Compile conv_oracle.c into liboracle.so next to it (plain -O2, no tuning)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + ".tmp.%d" % os.getpid()
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.POINTER
+        f32p, f64p, i64p = P(ctypes.c_float), P(ctypes.c_double), P(ctypes.c_int64)
+        lib.oracle_out_size.argtypes = [ctypes.c_int64] * 5 + [i64p]
+        lib.oracle_out_size.restype = ctypes.c_int
+        lib.oracle_check.argtypes = [P(_Desc), i64p, i64p]
+        lib.oracle_check.restype = ctypes.c_int
+        for name in ("oracle_conv_fwd",):
+            getattr(lib, name).argtypes = [P(_Desc), f32p, f32p, f32p, f64p]
+            getattr(lib, name).restype = ctypes.c_int
+        for name in ("oracle_conv_dgrad", "oracle_conv_dgrad_scatter"):
+            getattr(lib, name).argtypes = [P(_Desc), f32p, f32p, f64p]
+            getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_conv_fwd_points.argtypes = [P(_Desc), f32p, f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_fwd_points.restype = None
+        lib.oracle_conv_dgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_dgrad_points.restype = None
+        _lib = lib
+    return _lib
+
+
+def _f32(a, shape=None):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    if shape is not None and a.size != int(np.prod(shape)):
+        raise ValueError("array has %d elements, expected shape %s" % (a.size, shape))
+    return a
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def out_size(in_: int, k: int, s: int, p: int, d: int):
+    """Output length along one axis, or None when the shape is rejected."""
+    out = ctypes.c_int64(0)
+    rc = _load().oracle_out_size(in_, k, s, p, d, ctypes.byref(out))
+    return None if rc != 0 else out.value
+
+
+def check(c: Conv) -> bool:
+    """True when the oracle accepts the shape (nonzero extents, divisibility, kernel fits)."""
+    oh, ow = ctypes.c_int64(0), ctypes.c_int64(0)
+    return _load().oracle_check(ctypes.byref(c._c()), ctypes.byref(oh), ctypes.byref(ow)) == 0
+
+
+def conv_fwd(c: Conv, x, w, bias=None) -> np.ndarray:
+    """Whole forward output in fp64, shaped like the layout ``c`` names."""
+    x, w = _f32(x, c.x_shape()), _f32(w, c.w_shape())
+    b = None if bias is None else _f32(bias, (c.c_out,))
+    y = np.empty(c.y_shape(), dtype=np.float64)
+    rc = _load().oracle_conv_fwd(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float),
+                                 _ptr(b, ctypes.c_float), _ptr(y, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return y
+
+
+def conv_dgrad(c: Conv, dy, w, scatter: bool = False) -> np.ndarray:
+    """Whole input gradient in fp64 (gather form, or the scatter form when asked)."""
+    dy, w = _f32(dy, c.y_shape()), _f32(w, c.w_shape())
+    dx = np.empty(c.x_shape(), dtype=np.float64)
+    fn = _load().oracle_conv_dgrad_scatter if scatter else _load().oracle_conv_dgrad
+    rc = fn(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(dx, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return dx
+
+
+def conv_fwd_points(c: Conv, x, w, bias, idx) -> np.ndarray:
+    """Forward outputs at an (count, 4) array of (n, c_out, oh, ow) indices."""
+    x, w = _f32(x, c.x_shape()), _f32(w, c.w_shape())
+    b = None if bias is None else _f32(bias, (c.c_out,))
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(idx.shape[0], dtype=np.float64)
+    _load().oracle_conv_fwd_points(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float),
+                                   _ptr(b, ctypes.c_float), _ptr(idx, ctypes.c_int64), idx.shape[0],
+                                   _ptr(out, ctypes.c_double))
+    return out
+
+
+def conv_dgrad_points(c: Conv, dy, w, idx) -> np.ndarray:
+    """Input-gradient elements at an (count, 4) array of (n, c_in, ih, iw) indices."""
+    dy, w = _f32(dy, c.y_shape()), _f32(w, c.w_shape())
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(idx.shape[0], dtype=np.float64)
+    _load().oracle_conv_dgrad_points(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(w, ctypes.c_float),
+                                     _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
+    return out

@@ -1,0 +1,220 @@
+/*
+ * Convolution oracle: the plain, slow, FP64 definition of N-D (1-D and 2-D)
+ * convolution forward and of its input gradient (dgrad).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * Inputs arrive as float32 arrays (bf16 and f32 values are both exactly
+ * representable in float32), every product and sum is taken in double, and
+ * results are returned as double.  Loops are plain nested loops in the order
+ * the definitions below state them; there is no blocking, no reordering and
+ * no fusion.
+ *
+ * Definitions followed (cited by page title and item):
+ *  - Output size: oarust 0.8.6 `src/rs/ml/matrix/conv.rs`,
+ *    `Conv1dGeometry::resolve` (effective kernel = (k-1)*dil + 1, reject a
+ *    padded input shorter than it, out = (in + 2*pad - eff) / stride + 1 with
+ *    integer floor division).  The 2-D rule is the same per spatial axis.
+ *  - Index map: burn-cubecl `src/kernel/conv/im2col.rs`, doc of `im2col`
+ *    (input position = out*stride + k*dilation - padding, zero outside the
+ *    image; no kernel flip: cross-correlation).
+ *  - Groups: teeny-kernels `src/nn/conv/conv2d.rs`, `conv2d_forward`
+ *    (c_in_per_group = C_IN/G, group = c_out / (C_OUT/G), weight
+ *    [C_OUT, C_IN/G, KH, KW]).
+ *  - Bias: teeny-kernels `conv2d_bias_forward` (bias[c_out] added once, after
+ *    the reduction).
+ *  - Data gradient, scatter form: teeny-kernels `conv2d_backward_dx`
+ *    (dx[b, c_in, oh*S + kh - P, ow*S + kw - P] += dy[b, c_out, oh, ow] *
+ *    w[c_out, c_in_local, kh, kw], out-of-image positions skipped).
+ *  - Data gradient, gather form: oarust `conv_2d_backward` dispatches its
+ *    input-gradient pass over input elements; the gather form here is the
+ *    exact transpose of the scatter form above.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+
+typedef struct {
+  int64_t n, c_in, c_out, groups;
+  int64_t in_h, in_w;    /* 1-D convolution: in_h = 1, k_h = 1, s_h = 1, p_h = 0, d_h = 1 */
+  int64_t k_h, k_w;
+  int64_t s_h, s_w;
+  int64_t p_h, p_w;
+  int64_t d_h, d_w;
+  int32_t nhwc;          /* 0: NCHW / NCL activations, 1: NHWC / NLC activations */
+  int32_t w_ohwi;        /* 0: OIHW / OIK weight [C_out, C_in/G, KH, KW], 1: OHWI [C_out, KH, KW, C_in/G] */
+} oracle_conv;
+
+/* Output length along one axis, or ORACLE_EINVAL when the effective kernel
+ * does not fit the padded input (oarust Conv1dGeometry::resolve). */
+int oracle_out_size(int64_t in, int64_t k, int64_t s, int64_t p, int64_t d, int64_t *out) {
+  if (in <= 0 || k <= 0 || s <= 0 || d <= 0 || p < 0) return ORACLE_EINVAL;
+  int64_t eff = (k - 1) * d + 1;
+  int64_t padded = in + 2 * p;
+  if (padded < eff) return ORACLE_EINVAL;
+  *out = (padded - eff) / s + 1;
+  return ORACLE_OK;
+}
+
+/* Shape checks of oarust Conv1dGeometry / Conv2dGeometry::resolve: nonzero
+ * extents, nonzero stride, dilation and groups, channels divisible by groups. */
+int oracle_check(const oracle_conv *c, int64_t *oh, int64_t *ow) {
+  if (c->n <= 0 || c->c_in <= 0 || c->c_out <= 0 || c->groups <= 0) return ORACLE_EINVAL;
+  if (c->c_in % c->groups != 0 || c->c_out % c->groups != 0) return ORACLE_EINVAL;
+  if (oracle_out_size(c->in_h, c->k_h, c->s_h, c->p_h, c->d_h, oh) != ORACLE_OK) return ORACLE_EINVAL;
+  if (oracle_out_size(c->in_w, c->k_w, c->s_w, c->p_w, c->d_w, ow) != ORACLE_OK) return ORACLE_EINVAL;
+  return ORACLE_OK;
+}
+
+/* Offset of activation element (n, c, h, w) in a tensor of C channels and
+ * H x W spatial extent, in the layout the descriptor names. */
+static int64_t act_index(const oracle_conv *c, int64_t C, int64_t H, int64_t W,
+                         int64_t n, int64_t ch, int64_t h, int64_t w) {
+  if (c->nhwc) return ((n * H + h) * W + w) * C + ch;
+  return ((n * C + ch) * H + h) * W + w;
+}
+
+/* Offset of weight element (co, c_local, kh, kw). */
+static int64_t w_index(const oracle_conv *c, int64_t co, int64_t cl, int64_t kh, int64_t kw) {
+  int64_t cpg = c->c_in / c->groups;
+  if (c->w_ohwi) return ((co * c->k_h + kh) * c->k_w + kw) * cpg + cl;
+  return ((co * cpg + cl) * c->k_h + kh) * c->k_w + kw;
+}
+
+/* One forward output y[n, co, oh, ow]:
+ *   bias[co] + sum over c_local < C_in/G, kh < KH, kw < KW of
+ *   x[n, g*C_in/G + c_local, oh*s_h + kh*d_h - p_h, ow*s_w + kw*d_w - p_w] * w[co, c_local, kh, kw]
+ * with g = co / (C_out/G) and out-of-image x taken as zero. */
+double oracle_conv_fwd_at(const oracle_conv *c, const float *x, const float *w, const float *bias,
+                          int64_t n, int64_t co, int64_t oh, int64_t ow) {
+  int64_t cpg = c->c_in / c->groups;
+  int64_t g = co / (c->c_out / c->groups);
+  double acc = 0.0;
+  for (int64_t cl = 0; cl < cpg; ++cl) {
+    int64_t ci = g * cpg + cl;
+    for (int64_t kh = 0; kh < c->k_h; ++kh) {
+      int64_t ih = oh * c->s_h + kh * c->d_h - c->p_h;
+      if (ih < 0 || ih >= c->in_h) continue;
+      for (int64_t kw = 0; kw < c->k_w; ++kw) {
+        int64_t iw = ow * c->s_w + kw * c->d_w - c->p_w;
+        if (iw < 0 || iw >= c->in_w) continue;
+        double xv = (double)x[act_index(c, c->c_in, c->in_h, c->in_w, n, ci, ih, iw)];
+        double wv = (double)w[w_index(c, co, cl, kh, kw)];
+        acc += xv * wv;
+      }
+    }
+  }
+  if (bias) acc += (double)bias[co];
+  return acc;
+}
+
+/* Whole forward output, written in the descriptor's activation layout. */
+int oracle_conv_fwd(const oracle_conv *c, const float *x, const float *w, const float *bias, double *y) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return ORACLE_EINVAL;
+  for (int64_t n = 0; n < c->n; ++n)
+    for (int64_t co = 0; co < c->c_out; ++co)
+      for (int64_t oh = 0; oh < OH; ++oh)
+        for (int64_t ow = 0; ow < OW; ++ow)
+          y[act_index(c, c->c_out, OH, OW, n, co, oh, ow)] = oracle_conv_fwd_at(c, x, w, bias, n, co, oh, ow);
+  return ORACLE_OK;
+}
+
+/* One input-gradient element dx[n, ci, ih, iw], gather form:
+ *   sum over co in ci's group, kh, kw of dy[n, co, oh, ow] * w[co, ci - g*C_in/G, kh, kw]
+ * over the taps where oh = (ih + p_h - kh*d_h) / s_h is an exact integer in
+ * [0, OH) (and likewise ow).  These are exactly the (oh, ow, kh, kw) whose
+ * forward read lands on (ih, iw). */
+double oracle_conv_dgrad_at(const oracle_conv *c, const float *dy, const float *w,
+                            int64_t n, int64_t ci, int64_t ih, int64_t iw) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return 0.0;
+  int64_t cpg = c->c_in / c->groups;
+  int64_t opg = c->c_out / c->groups;
+  int64_t g = ci / cpg;
+  int64_t cl = ci - g * cpg;
+  double acc = 0.0;
+  for (int64_t co = g * opg; co < (g + 1) * opg; ++co) {
+    for (int64_t kh = 0; kh < c->k_h; ++kh) {
+      int64_t th = ih + c->p_h - kh * c->d_h;
+      if (th < 0 || th % c->s_h != 0) continue;
+      int64_t oh = th / c->s_h;
+      if (oh >= OH) continue;
+      for (int64_t kw = 0; kw < c->k_w; ++kw) {
+        int64_t tw = iw + c->p_w - kw * c->d_w;
+        if (tw < 0 || tw % c->s_w != 0) continue;
+        int64_t ow = tw / c->s_w;
+        if (ow >= OW) continue;
+        double gv = (double)dy[act_index(c, c->c_out, OH, OW, n, co, oh, ow)];
+        double wv = (double)w[w_index(c, co, cl, kh, kw)];
+        acc += gv * wv;
+      }
+    }
+  }
+  return acc;
+}
+
+/* Whole input gradient, gather form, in the descriptor's activation layout. */
+int oracle_conv_dgrad(const oracle_conv *c, const float *dy, const float *w, double *dx) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return ORACLE_EINVAL;
+  for (int64_t n = 0; n < c->n; ++n)
+    for (int64_t ci = 0; ci < c->c_in; ++ci)
+      for (int64_t ih = 0; ih < c->in_h; ++ih)
+        for (int64_t iw = 0; iw < c->in_w; ++iw)
+          dx[act_index(c, c->c_in, c->in_h, c->in_w, n, ci, ih, iw)] = oracle_conv_dgrad_at(c, dy, w, n, ci, ih, iw);
+  return ORACLE_OK;
+}
+
+/* Whole input gradient, scatter form: the loop structure of teeny-kernels
+ * `conv2d_backward_dx`, run serially in double.  Walks the output gradient
+ * and adds dy * w into every in-image input position the forward read from. */
+int oracle_conv_dgrad_scatter(const oracle_conv *c, const float *dy, const float *w, double *dx) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return ORACLE_EINVAL;
+  int64_t cpg = c->c_in / c->groups;
+  int64_t opg = c->c_out / c->groups;
+  int64_t total = c->n * c->c_in * c->in_h * c->in_w;
+  for (int64_t i = 0; i < total; ++i) dx[i] = 0.0;
+  for (int64_t n = 0; n < c->n; ++n)
+    for (int64_t co = 0; co < c->c_out; ++co) {
+      int64_t g = co / opg;
+      for (int64_t oh = 0; oh < OH; ++oh)
+        for (int64_t ow = 0; ow < OW; ++ow) {
+          double gv = (double)dy[act_index(c, c->c_out, OH, OW, n, co, oh, ow)];
+          for (int64_t cl = 0; cl < cpg; ++cl)
+            for (int64_t kh = 0; kh < c->k_h; ++kh) {
+              int64_t ih = oh * c->s_h + kh * c->d_h - c->p_h;
+              if (ih < 0 || ih >= c->in_h) continue;
+              for (int64_t kw = 0; kw < c->k_w; ++kw) {
+                int64_t iw = ow * c->s_w + kw * c->d_w - c->p_w;
+                if (iw < 0 || iw >= c->in_w) continue;
+                dx[act_index(c, c->c_in, c->in_h, c->in_w, n, g * cpg + cl, ih, iw)] +=
+                    gv * (double)w[w_index(c, co, cl, kh, kw)];
+              }
+            }
+        }
+    }
+  return ORACLE_OK;
+}
+
+/* Batched point queries: out[i] = fwd (or dgrad) at the i-th (n, c, h, w)
+ * quadruple of idx.  Used for sampled checks at sizes where a whole pass
+ * would take too long. */
+void oracle_conv_fwd_points(const oracle_conv *c, const float *x, const float *w, const float *bias,
+                            const int64_t *idx, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_conv_fwd_at(c, x, w, bias, idx[4 * i], idx[4 * i + 1], idx[4 * i + 2], idx[4 * i + 3]);
+}
+
+void oracle_conv_dgrad_points(const oracle_conv *c, const float *dy, const float *w,
+                              const int64_t *idx, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_conv_dgrad_at(c, dy, w, idx[4 * i], idx[4 * i + 1], idx[4 * i + 2], idx[4 * i + 3]);
+}

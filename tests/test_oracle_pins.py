@@ -1,0 +1,256 @@
+"""Pins for the FP64 oracle, checked against things other than the oracle itself.
+
+Each test ties the oracle to a fact the pages or the mathematics fix:
+hand-worked examples (tests/golden), the output-size rule, the 1x1 = matmul
+identity, delta kernels, constant-input closed forms, an independent library
+convolution (PyTorch CPU, float64), the adjoint identity between forward and
+input gradient, scatter == gather, and rejection of degenerate shapes.
+A plausible slip in the oracle (dropped bias, a flipped kernel, a wrong group
+window, a sign or stride error in the gather) fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import Conv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- golden cases
+
+def test_golden_conv1d_dilated_padded():
+    g = _golden("conv1d_dilated_padded.json")
+    s = g["shape"]
+    c = Conv(n=1, c_in=1, c_out=1, in_hw=(1, s["length"]), k=(1, s["k"]), stride=(1, s["stride"]),
+             pad=(0, s["pad"]), dil=(1, s["dil"]), spatial_dims=1)
+    y = oracle.conv_fwd(c, np.array(g["x"]).reshape(1, 1, 5), np.array(g["w"]).reshape(1, 1, 3), g["bias"])
+    assert y.reshape(-1).tolist() == g["y"]
+
+
+def test_golden_conv2d_grouped_strided():
+    g = _golden("conv2d_grouped_strided.json")
+    s = g["shape"]
+    c = Conv(n=1, c_in=2, c_out=2, in_hw=(3, 3), k=(2, 2), stride=(2, 2), pad=(1, 1), groups=2)
+    y = oracle.conv_fwd(c, np.array(g["x_nchw"], dtype=np.float32)[None], np.array(g["w_oihw"]))
+    assert y[0].tolist() == g["y_nchw"]
+
+
+def test_golden_conv1d_dgrad_strided():
+    g = _golden("conv1d_dgrad_strided.json")
+    c = Conv(n=1, c_in=1, c_out=1, in_hw=(1, 5), k=(1, 3), stride=(1, 2), pad=(0, 1), spatial_dims=1)
+    dx = oracle.conv_dgrad(c, np.array(g["dy"]).reshape(1, 1, 3), np.array(g["w"]).reshape(1, 1, 3))
+    assert dx.reshape(-1).tolist() == g["dx"]
+    dxs = oracle.conv_dgrad(c, np.array(g["dy"]).reshape(1, 1, 3), np.array(g["w"]).reshape(1, 1, 3), scatter=True)
+    assert dxs.reshape(-1).tolist() == g["dx"]
+
+
+# ------------------------------------------------------------ output-size rule
+
+@pytest.mark.parametrize("in_,k,s,p,d,expect", [
+    (32, 3, 1, 2, 2, 32),     # conv1d NCL fp32 workload: eff 5, (32+4-5)/1+1
+    (56, 1, 1, 0, 1, 56),     # pointwise 1x1
+    (56, 3, 1, 1, 1, 56),     # dense 3x3 pad 1
+    (112, 3, 2, 1, 1, 56),    # depthwise 3x3 stride 2: (112+2-3)//2+1
+    (64, 3, 2, 1, 1, 32),     # dgrad forward shape
+    (63, 3, 2, 1, 1, 32),     # ... and a different input giving the same output
+    (5, 5, 1, 0, 1, 1),       # kernel exactly fills the input
+    (4, 3, 1, 0, 2, None),    # eff 5 > 4: rejected
+    (1, 3, 1, 1, 1, 1),       # padding makes it fit
+    (7, 3, 3, 0, 1, 2),       # floor: last input position never read
+    (10, 4, 3, 2, 3, 2),      # eff 10, (10+4-10)//3+1 = 2
+    (0, 1, 1, 0, 1, None),
+    (8, 0, 1, 0, 1, None),
+    (8, 3, 0, 0, 1, None),
+    (8, 3, 1, 0, 0, None),
+])
+def test_out_size_table(in_, k, s, p, d, expect):
+    assert oracle.out_size(in_, k, s, p, d) == expect
+
+
+# --------------------------------------------------------- 1x1 conv == matmul
+
+@pytest.mark.parametrize("nhwc", [True, False])
+def test_pointwise_is_matmul(nhwc):
+    n, h, w, ci, co = 2, 5, 3, 12, 7
+    c = Conv(n=n, c_in=ci, c_out=co, in_hw=(h, w), k=(1, 1), nhwc=nhwc, w_ohwi=True)
+    x = synth.normal(11, c.x_shape()).astype(np.float32)
+    wt = synth.normal(12, c.w_shape()).astype(np.float32)
+    y = oracle.conv_fwd(c, x, wt)
+    xm = x.astype(np.float64)
+    if not nhwc:
+        xm = xm.transpose(0, 2, 3, 1)
+    ref = xm.reshape(-1, ci) @ wt.astype(np.float64).reshape(co, ci).T
+    got = y if nhwc else y.transpose(0, 2, 3, 1)
+    np.testing.assert_allclose(got.reshape(-1, co), ref, rtol=1e-12, atol=1e-12)
+    # data gradient of the same 1x1: dy[M, C_out] @ W[C_out, C_in]
+    dy = synth.normal(13, c.y_shape()).astype(np.float32)
+    dx = oracle.conv_dgrad(c, dy, wt)
+    dym = dy.astype(np.float64) if nhwc else dy.astype(np.float64).transpose(0, 2, 3, 1)
+    refdx = dym.reshape(-1, co) @ wt.astype(np.float64).reshape(co, ci)
+    gotdx = dx if nhwc else dx.transpose(0, 2, 3, 1)
+    np.testing.assert_allclose(gotdx.reshape(-1, ci), refdx, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- delta kernels
+
+@pytest.mark.parametrize("k,d", [(3, 1), (5, 1), (3, 2), (3, 3)])
+@pytest.mark.parametrize("nhwc", [False, True])
+def test_delta_kernel_reproduces_input(k, d, nhwc):
+    ch, kc = 4, (k - 1) // 2
+    c = Conv(n=2, c_in=ch, c_out=ch, in_hw=(6, 7), k=(k, k), pad=(d * kc, d * kc), dil=(d, d), nhwc=nhwc)
+    w = np.zeros(c.w_shape())
+    for i in range(ch):
+        w[i, i, kc, kc] = 1.0
+    x = synth.normal(21, c.x_shape())
+    y = oracle.conv_fwd(c, x, w)
+    np.testing.assert_array_equal(y, x.astype(np.float32).astype(np.float64))
+
+
+def test_delta_kernel_depthwise():
+    ch = 5
+    c = Conv(n=1, c_in=ch, c_out=ch, in_hw=(4, 9), k=(3, 3), pad=(1, 1), groups=ch)
+    w = np.zeros(c.w_shape())
+    w[:, 0, 1, 1] = 1.0
+    x = synth.normal(22, c.x_shape())
+    np.testing.assert_array_equal(oracle.conv_fwd(c, x, w), x.astype(np.float32).astype(np.float64))
+
+
+@pytest.mark.parametrize("k0,s,p,d", [(0, 1, 2, 2), (2, 1, 2, 2), (1, 2, 1, 3), (2, 3, 0, 2)])
+def test_delta_tap_1d_shift(k0, s, p, d):
+    L, K = 13, 3
+    c = Conv(n=1, c_in=1, c_out=1, in_hw=(1, L), k=(1, K), stride=(1, s), pad=(0, p), dil=(1, d), spatial_dims=1)
+    w = np.zeros((1, 1, K))
+    w[0, 0, k0] = 1.0
+    x = np.arange(1, L + 1, dtype=np.float64).reshape(1, 1, L)
+    y = oracle.conv_fwd(c, x, w).reshape(-1)
+    lout = oracle.out_size(L, K, s, p, d)
+    for l in range(lout):
+        src = l * s + k0 * d - p
+        assert y[l] == (src + 1 if 0 <= src < L else 0.0)
+
+
+# ---------------------------------------------------- closed form, constants
+
+def test_constant_input_border_counts():
+    # x = 1, w = 1, 3x3 pad 1 stride 1: each output is bias + (C_in/G) * (taps inside the image):
+    # 4 at corners, 6 on edges, 9 inside.
+    g, ci, co = 2, 6, 4
+    c = Conv(n=1, c_in=ci, c_out=co, in_hw=(5, 6), k=(3, 3), pad=(1, 1), groups=g, nhwc=True, w_ohwi=True)
+    b = np.array([0.25, -1.0, 2.0, 0.0])
+    y = oracle.conv_fwd(c, np.ones(c.x_shape()), np.ones(c.w_shape()), b)
+    cpg = ci // g
+    taps = np.full((5, 6), 9.0)
+    taps[0, :] = taps[-1, :] = 6.0
+    taps[:, 0] = taps[:, -1] = 6.0
+    taps[0, 0] = taps[0, -1] = taps[-1, 0] = taps[-1, -1] = 4.0
+    for o in range(co):
+        np.testing.assert_array_equal(y[0, :, :, o], b[o] + cpg * taps)
+
+
+# ------------------------------------------- independent library convolution
+
+torch = pytest.importorskip("torch")
+
+
+def _to_nchw(a, c):
+    return a.transpose(0, 3, 1, 2) if (c.nhwc and c.spatial_dims == 2) else (
+        a.transpose(0, 2, 1) if (c.nhwc and c.spatial_dims == 1) else a)
+
+
+def _w_to_oihw(w, c):
+    if not c.w_ohwi:
+        return w
+    return w.transpose(0, 3, 1, 2) if c.spatial_dims == 2 else w.transpose(0, 2, 1)
+
+
+CASES = [
+    Conv(n=2, c_in=4, c_out=8, in_hw=(1, 32), k=(1, 3), stride=(1, 1), pad=(0, 2), dil=(1, 2), spatial_dims=1),
+    Conv(n=1, c_in=6, c_out=4, in_hw=(1, 17), k=(1, 4), stride=(1, 3), pad=(0, 1), dil=(1, 2), groups=2,
+         spatial_dims=1, nhwc=True, w_ohwi=True),
+    Conv(n=2, c_in=6, c_out=9, in_hw=(7, 9), k=(3, 2), stride=(2, 1), pad=(1, 0), dil=(1, 2), groups=3),
+    Conv(n=1, c_in=8, c_out=8, in_hw=(9, 8), k=(3, 3), stride=(2, 2), pad=(1, 1), groups=8, nhwc=True, w_ohwi=True),
+    Conv(n=2, c_in=4, c_out=6, in_hw=(6, 5), k=(5, 3), stride=(1, 2), pad=(2, 1), dil=(1, 1), nhwc=True),
+    Conv(n=1, c_in=3, c_out=2, in_hw=(10, 10), k=(3, 3), stride=(3, 3), pad=(0, 0), dil=(2, 2), w_ohwi=True),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_matches_torch_float64(ci):
+    c = CASES[ci]
+    F = torch.nn.functional
+    x = synth.normal(31 + ci, c.x_shape()).astype(np.float32)
+    w = synth.normal(41 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(51 + ci, (c.c_out,)).astype(np.float32)
+    xt = torch.from_numpy(_to_nchw(x, c).astype(np.float64).copy())
+    wt = torch.from_numpy(_w_to_oihw(w, c).astype(np.float64).copy())
+    bt = torch.from_numpy(b.astype(np.float64))
+    if c.spatial_dims == 1:
+        ref = F.conv1d(xt, wt, bt, stride=c.stride[1], padding=c.pad[1], dilation=c.dil[1], groups=c.groups)
+    else:
+        ref = F.conv2d(xt, wt, bt, stride=c.stride, padding=c.pad, dilation=c.dil, groups=c.groups)
+    y = oracle.conv_fwd(c, x, w, b)
+    np.testing.assert_allclose(_to_nchw(y, c), ref.numpy(), rtol=1e-12, atol=1e-12)
+    # input gradient against torch's own backward-data routine
+    dy = synth.normal(61 + ci, c.y_shape()).astype(np.float32)
+    dyt = torch.from_numpy(_to_nchw(dy, c).astype(np.float64).copy())
+    if c.spatial_dims == 1:
+        refdx = torch.nn.grad.conv1d_input(xt.shape, wt, dyt, stride=c.stride[1], padding=c.pad[1],
+                                           dilation=c.dil[1], groups=c.groups)
+    else:
+        refdx = torch.nn.grad.conv2d_input(xt.shape, wt, dyt, stride=c.stride, padding=c.pad,
+                                           dilation=c.dil, groups=c.groups)
+    dx = oracle.conv_dgrad(c, dy, w)
+    np.testing.assert_allclose(_to_nchw(dx, c), refdx.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------- adjoint and scatter == gather
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_adjoint_identity(ci):
+    # <conv(x, w), dy> == <x, dgrad(dy, w)> for the bias-free convolution
+    c = CASES[ci]
+    x = synth.normal(71 + ci, c.x_shape())
+    w = synth.normal(72 + ci, c.w_shape())
+    dy = synth.normal(73 + ci, c.y_shape())
+    lhs = float(np.sum(oracle.conv_fwd(c, x, w) * dy.astype(np.float32)))
+    rhs = float(np.sum(x.astype(np.float32).astype(np.float64) * oracle.conv_dgrad(c, dy, w)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs)) * 10
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_scatter_equals_gather(ci):
+    c = CASES[ci]
+    dy = synth.normal(81 + ci, c.y_shape())
+    w = synth.normal(82 + ci, c.w_shape())
+    np.testing.assert_allclose(oracle.conv_dgrad(c, dy, w), oracle.conv_dgrad(c, dy, w, scatter=True),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_unreached_input_has_zero_gradient():
+    # in=7, k=3, s=3, p=0: out=2 reads positions 0..5; position 6 gets no gradient.
+    c = Conv(n=1, c_in=2, c_out=3, in_hw=(1, 7), k=(1, 3), stride=(1, 3), spatial_dims=1)
+    dx = oracle.conv_dgrad(c, synth.normal(91, c.y_shape()), synth.normal(92, c.w_shape()))
+    assert np.all(dx[:, :, 6] == 0.0) and np.all(dx[:, :, :6] != 0.0)
+
+
+# ------------------------------------------------------- degenerate rejection
+
+@pytest.mark.parametrize("kw", [
+    dict(n=0), dict(c_in=0), dict(c_out=0), dict(groups=0), dict(groups=3),
+    dict(stride=(0, 1)), dict(dil=(1, 0)), dict(k=(9, 3)), dict(in_hw=(0, 5)),
+])
+def test_degenerate_shapes_rejected(kw):
+    base = dict(n=1, c_in=4, c_out=4, in_hw=(6, 5), k=(3, 3), stride=(1, 1), pad=(1, 1), dil=(1, 1), groups=2)
+    base.update(kw)
+    c = Conv(**base)
+    assert not oracle.check(c)
