@@ -1,0 +1,205 @@
+// The C ABI: argument checks, shape resolution, choice of kernel family and
+// the device status word.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "problem.h"
+
+namespace gbconv {
+
+namespace {
+
+// Bounded-wait failures of any kernel of this library on this device set bits here.
+__device__ unsigned int g_status_word;
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+bool device_context(Launch* l, void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    g_num_sms[dev] = sms;
+  }
+  l->stream = stream;
+  l->status = g_status_ptr[dev];
+  l->num_sms = g_num_sms[dev];
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMax32 = 2147483647;
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+gbconv_status resolve(const gbconv_desc* d, Problem* p) {
+  if (!d || !p) return GBCONV_EINVAL;
+  if (d->spatial_dims != 1 && d->spatial_dims != 2) return GBCONV_EINVAL;
+  if (d->layout != GBCONV_NCHW && d->layout != GBCONV_NHWC) return GBCONV_EINVAL;
+  if (d->wlayout != GBCONV_W_OIHW && d->wlayout != GBCONV_W_OHWI) return GBCONV_EINVAL;
+  if (d->dtype != GBCONV_F32 && d->dtype != GBCONV_BF16) return GBCONV_EINVAL;
+  Problem q{};
+  q.N = d->n;
+  q.Cin = d->c_in;
+  q.Cout = d->c_out;
+  q.G = d->groups;
+  if (d->spatial_dims == 1) {  // the length axis is carried as the width
+    q.H = 1; q.KH = 1; q.SH = 1; q.PH = 0; q.DH = 1;
+    q.W = d->in[0]; q.KW = d->k[0]; q.SW = d->stride[0]; q.PW = d->pad[0]; q.DW = d->dil[0];
+  } else {
+    q.H = d->in[0]; q.KH = d->k[0]; q.SH = d->stride[0]; q.PH = d->pad[0]; q.DH = d->dil[0];
+    q.W = d->in[1]; q.KW = d->k[1]; q.SW = d->stride[1]; q.PW = d->pad[1]; q.DW = d->dil[1];
+  }
+  if (q.N <= 0 || q.Cin <= 0 || q.Cout <= 0 || q.G <= 0) return GBCONV_EINVAL;
+  if (q.H <= 0 || q.W <= 0 || q.KH <= 0 || q.KW <= 0) return GBCONV_EINVAL;
+  if (q.SH <= 0 || q.SW <= 0 || q.DH <= 0 || q.DW <= 0 || q.PH < 0 || q.PW < 0) return GBCONV_EINVAL;
+  if (q.Cin % q.G != 0 || q.Cout % q.G != 0) return GBCONV_EINVAL;
+  // Keep every intermediate well inside int64 before multiplying.
+  const int64_t lim = int64_t(1) << 31;
+  if (q.N >= lim || q.Cin >= lim || q.Cout >= lim || q.H >= lim || q.W >= lim || q.KH >= lim || q.KW >= lim ||
+      q.SH >= lim || q.SW >= lim || q.PH >= lim || q.PW >= lim || q.DH >= lim || q.DW >= lim)
+    return GBCONV_EUNSUPPORTED;
+  const int64_t effh = (q.KH - 1) * q.DH + 1, effw = (q.KW - 1) * q.DW + 1;
+  if (q.H + 2 * q.PH < effh || q.W + 2 * q.PW < effw) return GBCONV_EINVAL;
+  q.OH = (q.H + 2 * q.PH - effh) / q.SH + 1;
+  q.OW = (q.W + 2 * q.PW - effw) / q.SW + 1;
+  q.nhwc = d->layout == GBCONV_NHWC;
+  q.ohwi = d->wlayout == GBCONV_W_OHWI;
+  q.bf16 = d->dtype == GBCONV_BF16;
+  // 32-bit device indexing: element counts and the farthest coordinate read.
+  auto fits = [](int64_t a, int64_t b, int64_t c, int64_t e) -> bool {
+    __int128 v = static_cast<__int128>(a) * b * c * e;
+    return v <= kMax32;
+  };
+  if (!fits(q.N, q.Cin, q.H, q.W) || !fits(q.N, q.Cout, q.OH, q.OW) || !fits(q.Cout, q.cpg(), q.KH, q.KW))
+    return GBCONV_EUNSUPPORTED;
+  if ((q.OH - 1) * q.SH + (q.KH - 1) * q.DH > kMax32 || (q.OW - 1) * q.SW + (q.KW - 1) * q.DW > kMax32)
+    return GBCONV_EUNSUPPORTED;
+  *p = q;
+  return GBCONV_OK;
+}
+
+namespace {
+
+int32_t select_fwd(const Problem& p, bool aligned) {
+  if (aligned && depthwise_supported(p)) return GBCONV_K_DEPTHWISE;
+  if (aligned && pointwise_supported(p)) return GBCONV_K_POINTWISE;
+  if (aligned && implicit_fwd_supported(p)) return GBCONV_K_IMPLICIT;
+  return GBCONV_K_DIRECT;
+}
+
+int32_t select_dgrad(const Problem& p, bool aligned) {
+  if (aligned && implicit_dgrad_supported(p)) return GBCONV_K_DGRAD;
+  return GBCONV_K_DIRECT_DGRAD;
+}
+
+}  // namespace
+}  // namespace gbconv
+
+using namespace gbconv;
+
+extern "C" {
+
+gbconv_status gbconv_out_shape(const gbconv_desc* desc, int64_t out[2]) {
+  if (!out) return GBCONV_EINVAL;
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (desc->spatial_dims == 1) {
+    out[0] = p.OW;
+    out[1] = 1;
+  } else {
+    out[0] = p.OH;
+    out[1] = p.OW;
+  }
+  return GBCONV_OK;
+}
+
+gbconv_status gbconv_select(const gbconv_desc* desc, int32_t op, int32_t* kernel) {
+  if (!kernel || (op != GBCONV_OP_FWD && op != GBCONV_OP_BWD_DATA)) return GBCONV_EINVAL;
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  *kernel = op == GBCONV_OP_FWD ? select_fwd(p, true) : select_dgrad(p, true);
+  return GBCONV_OK;
+}
+
+gbconv_status gbconv_fwd(const gbconv_desc* desc, const void* x, const void* w, const float* bias, void* y,
+                         void* stream) {
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (!x || !w || !y) return GBCONV_EINVAL;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  const bool aligned = aligned16(x) && aligned16(w) && aligned16(y);
+  switch (select_fwd(p, aligned)) {
+    case GBCONV_K_DEPTHWISE: return launch_depthwise_fwd(p, x, w, bias, y, l);
+    case GBCONV_K_POINTWISE: return launch_pointwise_fwd(p, x, w, bias, y, l);
+    case GBCONV_K_IMPLICIT: return launch_implicit_fwd(p, x, w, bias, y, l);
+    default: return launch_direct_fwd(p, x, w, bias, y, l);
+  }
+}
+
+gbconv_status gbconv_bwd_data(const gbconv_desc* desc, const void* dy, const void* w, void* dx, void* stream) {
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (!dy || !w || !dx) return GBCONV_EINVAL;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  const bool aligned = aligned16(dy) && aligned16(w) && aligned16(dx);
+  if (select_dgrad(p, aligned) == GBCONV_K_DGRAD) return launch_implicit_dgrad(p, dy, w, dx, l);
+  return launch_direct_dgrad(p, dy, w, dx, l);
+}
+
+gbconv_status gbconv_pack_weight(const gbconv_desc* desc, const void* w_oihw, void* w_ohwi, void* stream) {
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (!w_oihw || !w_ohwi) return GBCONV_EINVAL;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  return launch_pack_weight(p, w_oihw, w_ohwi, l);
+}
+
+gbconv_status gbconv_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GBCONV_ECUDA;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return GBCONV_ECUDA;
+  if (word != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return GBCONV_ECUDA;
+  return word ? GBCONV_ETIMEOUT : GBCONV_OK;
+}
+
+uint64_t gbconv_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* gbconv_status_string(gbconv_status status) {
+  switch (status) {
+    case GBCONV_OK: return "ok";
+    case GBCONV_EINVAL: return "invalid argument or shape";
+    case GBCONV_EUNSUPPORTED: return "shape beyond the library's 32-bit indexing";
+    case GBCONV_ECUDA: return "CUDA runtime error";
+    case GBCONV_ETIMEOUT: return "a kernel's bounded internal wait expired";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+// Depthwise convolution forward (G = C_in = C_out, channel multiplier 1),
+// NHWC bf16, on CUDA cores.  The regime is bandwidth bound (about two flops
+// per byte), so the kernel is organised around the memory system, not the
+// arithmetic: each thread owns 8 consecutive channels (one 16-byte vector)
+// of one output column and walks a strip of output rows; a warp covers 32
+// channel vectors of one pixel, so every load and store of a warp is one
+// contiguous 512-byte run.  Rows shared by vertically adjacent outputs are
+// re-read through L1, columns shared by horizontally adjacent outputs are
+// read by neighbouring warps of the same block at the same time.
+//
+// Definition: teeny-kernels `src/nn/conv/conv2d.rs`, `conv2d_forward` with
+// G = C_IN = C_OUT (the depthwise case its doc names): output channel c reads
+// only input channel c through weight [C, 1, KH, KW].
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "problem.h"
+
+namespace gbconv {
+namespace {
+
+struct DwArgs {
+  int N, C, H, W, OH, OW, KH, KW, SH, SW, PH, PW, DH, DW;
+  int rows_per_thread;  // output rows walked by one thread
+  int cv_per_block;     // channel vectors (of 8) per block along x
+  int cv_chunks;        // C/8 / cv_per_block
+};
+
+constexpr int kThreads = 256;
+constexpr int kMaxTaps = 25;  // up to 5x5 kernels: taps x 256 channels x 4 bytes of shared memory
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int KH_, int KW_>
+__global__ void __launch_bounds__(kThreads) depthwise_fwd_kernel(DwArgs a, const __nv_bfloat16* __restrict__ x,
+                                                                 const __nv_bfloat16* __restrict__ w,
+                                                                 const float* __restrict__ bias,
+                                                                 __nv_bfloat16* __restrict__ y) {
+  const int KH = KH_ > 0 ? KH_ : a.KH;
+  const int KW = KW_ > 0 ? KW_ : a.KW;
+  const int taps = KH * KW;
+  // Weights of this block's channels as fp32, laid out [tap][channel].
+  extern __shared__ __align__(16) float ws[];
+  const int cpb = a.cv_per_block * 8;
+  const int chunk = blockIdx.x % a.cv_chunks;
+  const int c0 = chunk * cpb;
+  for (int i = threadIdx.y * blockDim.x + threadIdx.x; i < taps * cpb; i += kThreads) {
+    const int t = i / cpb, c = i % cpb;
+    ws[t * cpb + c] = __bfloat162float(w[(c0 + c) * taps + t]);
+  }
+  __syncthreads();
+
+  const int ow = (blockIdx.x / a.cv_chunks) * blockDim.y + threadIdx.y;
+  const int cv = threadIdx.x;
+  const int n = blockIdx.z;
+  if (ow >= a.OW) return;
+  const int oh0 = blockIdx.y * a.rows_per_thread;
+  const int oh1 = min(a.OH, oh0 + a.rows_per_thread);
+  const int c = c0 + cv * 8;
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = bias ? __ldg(bias + c + j) : 0.f;
+
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* yv = reinterpret_cast<uint4*>(y);
+  const int cvec = a.C / 8;
+  for (int oh = oh0; oh < oh1; ++oh) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = b[j];
+#pragma unroll
+    for (int kh = 0; kh < KH; ++kh) {
+      const int ih = oh * a.SH + kh * a.DH - a.PH;
+      if (ih < 0 || ih >= a.H) continue;
+      const int row = (n * a.H + ih) * a.W;
+#pragma unroll
+      for (int kw = 0; kw < KW; ++kw) {
+        const int iw = ow * a.SW + kw * a.DW - a.PW;
+        if (iw < 0 || iw >= a.W) continue;
+        float xf[8];
+        unpack8(__ldg(xv + (size_t)(row + iw) * cvec + (c >> 3)), xf);
+        const float* wt = ws + (kh * KW + kw) * cpb + cv * 8;
+        const float4 w0 = *reinterpret_cast<const float4*>(wt);
+        const float4 w1 = *reinterpret_cast<const float4*>(wt + 4);
+        acc[0] = fmaf(xf[0], w0.x, acc[0]);
+        acc[1] = fmaf(xf[1], w0.y, acc[1]);
+        acc[2] = fmaf(xf[2], w0.z, acc[2]);
+        acc[3] = fmaf(xf[3], w0.w, acc[3]);
+        acc[4] = fmaf(xf[4], w1.x, acc[4]);
+        acc[5] = fmaf(xf[5], w1.y, acc[5]);
+        acc[6] = fmaf(xf[6], w1.z, acc[6]);
+        acc[7] = fmaf(xf[7], w1.w, acc[7]);
+      }
+    }
+    uint4 o;
+    o.x = pack2(acc[0], acc[1]);
+    o.y = pack2(acc[2], acc[3]);
+    o.z = pack2(acc[4], acc[5]);
+    o.w = pack2(acc[6], acc[7]);
+    yv[(size_t)((n * a.OH + oh) * a.OW + ow) * cvec + (c >> 3)] = o;
+  }
+}
+
+}  // namespace
+
+bool depthwise_supported(const Problem& p) {
+  return p.bf16 && p.nhwc && p.G == p.Cin && p.Cin == p.Cout && p.Cin % 8 == 0 && p.KH * p.KW <= kMaxTaps;
+}
+
+gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                   const Launch& l) {
+  DwArgs a;
+  a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.KH = int(p.KH); a.KW = int(p.KW); a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.DH = int(p.DH); a.DW = int(p.DW);
+  const int cvec = a.C / 8;
+  // Largest power-of-two divisor of C/8 up to 32 channel vectors per block row.
+  int cvb = 1;
+  while (cvb < 32 && cvec % (cvb * 2) == 0) cvb *= 2;
+  a.cv_per_block = cvb;
+  a.cv_chunks = cvec / cvb;
+  const int ty = kThreads / cvb;
+  a.rows_per_thread = 4;
+  dim3 block(cvb, ty);
+  const int64_t gx = ((p.OW + ty - 1) / ty) * a.cv_chunks;
+  const int64_t gy = (p.OH + a.rows_per_thread - 1) / a.rows_per_thread;
+  if (gx > 0x7FFFFFFF || gy > 65535 || p.N > 65535) return GBCONV_EUNSUPPORTED;
+  dim3 grid(unsigned(gx), unsigned(gy), unsigned(p.N));
+  const size_t smem = size_t(p.KH * p.KW) * cvb * 8 * sizeof(float);
+  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
+  auto xb = static_cast<const __nv_bfloat16*>(x);
+  auto wb = static_cast<const __nv_bfloat16*>(w);
+  auto yb = static_cast<__nv_bfloat16*>(y);
+  if (p.KH == 3 && p.KW == 3)
+    depthwise_fwd_kernel<3, 3><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
+  else
+    depthwise_fwd_kernel<0, 0><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+}  // namespace gbconv

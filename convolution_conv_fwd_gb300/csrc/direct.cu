@@ -1,0 +1,199 @@
+// Generic direct convolution on CUDA cores: any layout, element type, group
+// count, stride, padding and dilation.  One thread per output element, fp32
+// accumulation.  This family serves the conv1d fp32 NCL workload and every
+// shape the specialised families do not take.
+//
+// Forward follows teeny-kernels `src/nn/conv/conv2d.rs`, `conv2d_forward`
+// (group window, per-tap read position oh*stride + kh*dil - pad, zero
+// outside, bias after the reduction as in `conv2d_bias_forward`), with
+// dilation per oarust `Conv1dGeometry`.  The input gradient is the gather
+// form: each thread owns one dx element and sums the (dy, w) products whose
+// forward read lands on it, so nothing is accumulated atomically.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "problem.h"
+
+namespace gbconv {
+namespace {
+
+struct DirectArgs {
+  int N, Cin, Cout, G, H, W, KH, KW, SH, SW, PH, PW, DH, DW, OH, OW;
+  int nhwc, ohwi;
+};
+
+template <typename T> __device__ __forceinline__ float ld(const T* p, int i);
+template <> __device__ __forceinline__ float ld<float>(const float* p, int i) { return __ldg(p + i); }
+template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p, int i) {
+  return __bfloat162float(p[i]);
+}
+template <typename T> __device__ __forceinline__ T cvt(float v);
+template <> __device__ __forceinline__ float cvt<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 cvt<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ int act_off(const DirectArgs& a, int C, int H, int W, int n, int c, int h, int w) {
+  return a.nhwc ? ((n * H + h) * W + w) * C + c : ((n * C + c) * H + h) * W + w;
+}
+
+__device__ __forceinline__ int w_off(const DirectArgs& a, int co, int cl, int kh, int kw) {
+  const int cpg = a.Cin / a.G;
+  return a.ohwi ? ((co * a.KH + kh) * a.KW + kw) * cpg + cl : ((co * cpg + cl) * a.KH + kh) * a.KW + kw;
+}
+
+template <typename T>
+__global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T* __restrict__ w,
+                                  const float* __restrict__ bias, T* __restrict__ y) {
+  const int total = a.N * a.Cout * a.OH * a.OW;
+  const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    int n, co, oh, ow;
+    if (a.nhwc) {  // channel fastest, so a warp writes contiguous channels
+      co = i % a.Cout;
+      int r = i / a.Cout;
+      ow = r % a.OW; r /= a.OW;
+      oh = r % a.OH; n = r / a.OH;
+    } else {
+      ow = i % a.OW;
+      int r = i / a.OW;
+      oh = r % a.OH; r /= a.OH;
+      co = r % a.Cout; n = r / a.Cout;
+    }
+    const int g = co / opg;
+    float acc = 0.f;
+    for (int cl = 0; cl < cpg; ++cl) {
+      const int ci = g * cpg + cl;
+      for (int kh = 0; kh < a.KH; ++kh) {
+        const int ih = oh * a.SH + kh * a.DH - a.PH;
+        if (ih < 0 || ih >= a.H) continue;
+        for (int kw = 0; kw < a.KW; ++kw) {
+          const int iw = ow * a.SW + kw * a.DW - a.PW;
+          if (iw < 0 || iw >= a.W) continue;
+          acc = fmaf(ld(x, act_off(a, a.Cin, a.H, a.W, n, ci, ih, iw)), ld(w, w_off(a, co, cl, kh, kw)), acc);
+        }
+      }
+    }
+    if (bias) acc += __ldg(bias + co);
+    y[act_off(a, a.Cout, a.OH, a.OW, n, co, oh, ow)] = cvt<T>(acc);
+  }
+}
+
+template <typename T>
+__global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, const T* __restrict__ w,
+                                    T* __restrict__ dx) {
+  const int total = a.N * a.Cin * a.H * a.W;
+  const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    int n, ci, ih, iw;
+    if (a.nhwc) {
+      ci = i % a.Cin;
+      int r = i / a.Cin;
+      iw = r % a.W; r /= a.W;
+      ih = r % a.H; n = r / a.H;
+    } else {
+      iw = i % a.W;
+      int r = i / a.W;
+      ih = r % a.H; r /= a.H;
+      ci = r % a.Cin; n = r / a.Cin;
+    }
+    const int g = ci / cpg, cl = ci - g * cpg;
+    float acc = 0.f;
+    for (int co = g * opg; co < (g + 1) * opg; ++co) {
+      for (int kh = 0; kh < a.KH; ++kh) {
+        const int th = ih + a.PH - kh * a.DH;
+        if (th < 0 || th % a.SH != 0) continue;
+        const int oh = th / a.SH;
+        if (oh >= a.OH) continue;
+        for (int kw = 0; kw < a.KW; ++kw) {
+          const int tw = iw + a.PW - kw * a.DW;
+          if (tw < 0 || tw % a.SW != 0) continue;
+          const int ow = tw / a.SW;
+          if (ow >= a.OW) continue;
+          acc = fmaf(ld(dy, act_off(a, a.Cout, a.OH, a.OW, n, co, oh, ow)), ld(w, w_off(a, co, cl, kh, kw)), acc);
+        }
+      }
+    }
+    dx[act_off(a, a.Cin, a.H, a.W, n, ci, ih, iw)] = cvt<T>(acc);
+  }
+}
+
+// [C_out, C_in/G, KH, KW] -> [C_out, KH, KW, C_in/G]; one thread per destination element.
+template <typename T>
+__global__ void pack_ohwi_kernel(int Cout, int cpg, int KH, int KW, const T* __restrict__ src, T* __restrict__ dst) {
+  const int total = Cout * cpg * KH * KW;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int cl = i % cpg;
+    int r = i / cpg;
+    const int kw = r % KW; r /= KW;
+    const int kh = r % KH;
+    const int co = r / KH;
+    dst[i] = src[((co * cpg + cl) * KH + kh) * KW + kw];
+  }
+}
+
+DirectArgs make_args(const Problem& p) {
+  DirectArgs a;
+  a.N = int(p.N); a.Cin = int(p.Cin); a.Cout = int(p.Cout); a.G = int(p.G);
+  a.H = int(p.H); a.W = int(p.W); a.KH = int(p.KH); a.KW = int(p.KW);
+  a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.DH = int(p.DH); a.DW = int(p.DW); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.nhwc = p.nhwc; a.ohwi = p.ohwi;
+  return a;
+}
+
+int grid_for(int64_t total, int threads, int num_sms) {
+  const int64_t want = (total + threads - 1) / threads;
+  return int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(num_sms) * 32)));
+}
+
+}  // namespace
+
+gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                const Launch& l) {
+  const DirectArgs a = make_args(p);
+  const int threads = 256, blocks = grid_for(p.y_elems(), threads, l.num_sms);
+  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
+  if (p.bf16)
+    direct_fwd_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+        a, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), bias,
+        static_cast<__nv_bfloat16*>(y));
+  else
+    direct_fwd_kernel<float><<<blocks, threads, 0, s>>>(a, static_cast<const float*>(x),
+                                                        static_cast<const float*>(w), bias, static_cast<float*>(y));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
+  const DirectArgs a = make_args(p);
+  const int threads = 256, blocks = grid_for(p.x_elems(), threads, l.num_sms);
+  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
+  if (p.bf16)
+    direct_dgrad_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+        a, static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(w),
+        static_cast<__nv_bfloat16*>(dx));
+  else
+    direct_dgrad_kernel<float><<<blocks, threads, 0, s>>>(a, static_cast<const float*>(dy),
+                                                          static_cast<const float*>(w), static_cast<float*>(dx));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_ohwi, const Launch& l) {
+  const int threads = 256, blocks = grid_for(p.w_elems(), threads, l.num_sms);
+  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
+  const int Cout = int(p.Cout), cpg = int(p.cpg()), KH = int(p.KH), KW = int(p.KW);
+  if (p.bf16)
+    pack_ohwi_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(Cout, cpg, KH, KW,
+                                                               static_cast<const __nv_bfloat16*>(w_oihw),
+                                                               static_cast<__nv_bfloat16*>(w_ohwi));
+  else
+    pack_ohwi_kernel<float><<<blocks, threads, 0, s>>>(Cout, cpg, KH, KW, static_cast<const float*>(w_oihw),
+                                                       static_cast<float*>(w_ohwi));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+}  // namespace gbconv

@@ -1,0 +1,269 @@
+// Pointwise (1x1, unit stride, no padding, no dilation, one group) forward as
+// a plain TMA-fed GEMM on tcgen05.  burn-cubecl `src/kernel/conv/im2col.rs`
+// (doc of `check_pointwise`) states the identity used: every output pixel
+// reads only the input pixel under it, so im2col is the identity and the
+// convolution is the per-pixel matmul y[(n,h,w), co] = sum_ci x[(n,h,w), ci] *
+// w[co, ci].  NHWC x is already the K-major [M = N*H*W, K = C_in] matrix and
+// the [C_out, C_in] weight is already the K-major B operand, so both are read
+// by TMA straight from the caller's tensors (burn-cubecl's `reshape_input` /
+// `reshape_weight` reach the same views by metadata alone).
+//
+// Roles: warps 0-3 epilogue (TMEM -> bias -> bf16 -> NHWC stores), warp 4
+// TMEM allocation + MMA issue (lane 0), warp 5 TMA producer (lane 0).  Tiles
+// are 128 rows of M; the weight stays resident in shared memory; A tiles
+// stream through a ring of 128-byte-swizzled stages; two TMEM accumulators
+// let the epilogue of one tile overlap the MMAs of the next.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "problem.h"
+#include "ptx.cuh"
+
+namespace gbconv {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kThreads = 6 * 32;
+constexpr int kBM = 128, kBK = 64;
+constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxStages = 8;
+
+struct PwArgs {
+  const float* bias;
+  bf16* out;
+  unsigned int* status;
+  int M, Cout, K;
+  int kb_count, m_tiles, stages;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    pointwise_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                          const __grid_constant__ PwArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte swizzled tiles must start on 1024-byte boundaries.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kBTileBytes = BN * kBK * 2;
+  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BN);
+
+  uint8_t* b_base = smem;                                      // kb_count tiles of [BN][64] bf16
+  uint8_t* a_base = b_base + size_t(a.kb_count) * kBTileBytes;  // stages x [128][64] bf16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(a_base + size_t(a.stages) * kATileBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + a.stages;
+  uint64_t* tfull = empty + a.stages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* bfull = tempty + 2;
+  uint64_t* fin = bfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.stages; ++i) { ptx::mbar_init(full + i, 1); ptx::mbar_init(empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, 128); }
+    ptx::mbar_init(bfull, 1);
+    ptx::mbar_init(fin, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 4) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_a);
+      ptx::prefetch_tmap(&tmap_b);
+      ptx::mbar_arrive_expect_tx(bfull, uint32_t(a.kb_count) * kBTileBytes);
+      for (int kb = 0; kb < a.kb_count; ++kb)
+        ptx::tma_load_2d(ptx::smem_addr(b_base + size_t(kb) * kBTileBytes), &tmap_b, bfull, kb * kBK, 0);
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < a.m_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < a.kb_count; ++kb) {
+          if (!(ok = ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 8u))) break;
+          ptx::mbar_arrive_expect_tx(full + st, kATileBytes);
+          ptx::tma_load_2d(ptx::smem_addr(a_base + size_t(st) * kATileBytes), &tmap_a, full + st, kb * kBK,
+                           tile * kBM);
+          if (++st == a.stages) { st = 0; ph ^= 1; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = ptx::mbar_wait(bfull, 0, abort_flag, a.status, 8u);
+      int st = 0, it = 0;
+      uint32_t ph = 0;
+      for (int tile = blockIdx.x; ok && tile < a.m_tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        if (!(ok = ptx::mbar_wait(tempty + buf, ((it >> 1) & 1) ^ 1, abort_flag, a.status, 8u))) break;
+        ptx::tc_fence_after();
+        const uint32_t acc = tmem + uint32_t(buf * BN);
+        for (int kb = 0; kb < a.kb_count; ++kb) {
+          if (!(ok = ptx::mbar_wait(full + st, ph, abort_flag, a.status, 8u))) break;
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_addr(a_base + size_t(st) * kATileBytes);
+          const uint32_t b_addr = ptx::smem_addr(b_base + size_t(kb) * kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            ptx::mma_bf16(acc, ptx::desc_kmajor_sw128(a_addr + k * 32), ptx::desc_kmajor_sw128(b_addr + k * 32),
+                          kIdesc, (kb | k) != 0);
+          ptx::mma_commit(empty + st);
+          if (++st == a.stages) { st = 0; ph ^= 1; }
+        }
+        ptx::mma_commit(tfull + buf);
+      }
+      ptx::mma_commit(fin);
+      ptx::mbar_wait(fin, 0, abort_flag, a.status, 8u);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    int it = 0;
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    for (int tile = blockIdx.x; tile < a.m_tiles; tile += gridDim.x, ++it) {
+      const int buf = it & 1;
+      if (!ptx::mbar_wait(tfull + buf, (it >> 1) & 1, abort_flag, a.status, 8u)) break;
+      ptx::tc_fence_after();
+      const int row = tile * kBM + warp * 32 + lane;
+      bf16* dst = a.out + size_t(row) * a.Cout;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * BN + c * 32), v);
+        ptx::tmem_ld_wait();
+        if (row < a.M) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
+            if (a.bias) {
+              lo += __ldg(a.bias + c * 32 + 2 * j);
+              hi += __ldg(a.bias + c * 32 + 2 * j + 1);
+            }
+            pk[j] = ptx::pack_bf16x2(lo, hi);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty + buf);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 4) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] bf16 matrix, box [box_rows, 64 columns], 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {uint32_t(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_bn(int64_t cout) {
+  for (int bn : {256, 128, 64, 32})
+    if (cout == bn) return bn;
+  return 0;
+}
+
+int stages_for(int bn, int kb_count) {
+  const size_t fixed = size_t(kb_count) * bn * kBK * 2 + 1024 + 8 * (2 * kMaxStages + 8);
+  if (fixed >= size_t(kSmemLimit)) return 0;
+  const int s = int((size_t(kSmemLimit) - fixed) / kATileBytes);
+  return std::min(s, kMaxStages);
+}
+
+template <int BN>
+gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a, int grid, const Launch& l) {
+  const size_t smem = size_t(a.kb_count) * BN * kBK * 2 + size_t(a.stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8);
+  auto kern = pointwise_gemm_kernel<BN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return GBCONV_ECUDA;
+  kern<<<grid, kThreads, smem, static_cast<cudaStream_t>(l.stream)>>>(ta, tb, a);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+}  // namespace
+
+bool pointwise_supported(const Problem& p) {
+  if (!(p.bf16 && p.nhwc && p.G == 1 && p.KH == 1 && p.KW == 1 && p.SH == 1 && p.SW == 1 && p.PH == 0 && p.PW == 0))
+    return false;
+  if (p.Cin % 8 != 0) return false;  // TMA row pitch must be a multiple of 16 bytes
+  const int bn = pick_bn(p.Cout);
+  if (!bn) return false;
+  const int kb_count = int((p.Cin + kBK - 1) / kBK);
+  return stages_for(bn, kb_count) >= 3 && encode_fn() != nullptr;
+}
+
+gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                   const Launch& l) {
+  if (!pointwise_supported(p)) return GBCONV_EUNSUPPORTED;
+  PwArgs a;
+  a.bias = bias;
+  a.out = static_cast<bf16*>(y);
+  a.status = l.status;
+  a.M = int(p.N * p.H * p.W);
+  a.Cout = int(p.Cout);
+  a.K = int(p.Cin);
+  a.kb_count = int((p.Cin + kBK - 1) / kBK);
+  a.m_tiles = (a.M + kBM - 1) / kBM;
+  const int bn = pick_bn(p.Cout);
+  a.stages = stages_for(bn, a.kb_count);
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, x, uint64_t(a.M), uint64_t(a.K), kBM)) return GBCONV_ECUDA;
+  if (!make_map(&tb, w, uint64_t(p.Cout), uint64_t(a.K), uint32_t(bn))) return GBCONV_ECUDA;
+  const int grid = std::max(1, std::min(a.m_tiles, l.num_sms));
+  switch (bn) {
+    case 256: return run<256>(ta, tb, a, grid, l);
+    case 128: return run<128>(ta, tb, a, grid, l);
+    case 64: return run<64>(ta, tb, a, grid, l);
+    default: return run<32>(ta, tb, a, grid, l);
+  }
+}
+
+}  // namespace gbconv

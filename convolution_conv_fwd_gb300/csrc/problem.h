@@ -1,0 +1,61 @@
+// Resolved convolution geometry shared by the host dispatcher and the kernel
+// launchers.  A 1-D convolution is carried as a 2-D one with H = KH = 1.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/gbconv.h"
+
+namespace gbconv {
+
+struct Problem {
+  int64_t N, Cin, Cout, G;
+  int64_t H, W, KH, KW, SH, SW, PH, PW, DH, DW;
+  int64_t OH, OW;
+  bool nhwc;   // activations channels-last
+  bool ohwi;   // weight [C_out, KH, KW, C_in/G]
+  bool bf16;   // element type bf16 (else f32)
+  int64_t cpg() const { return Cin / G; }   // input channels per group
+  int64_t opg() const { return Cout / G; }  // output channels per group
+  int64_t x_elems() const { return N * Cin * H * W; }
+  int64_t y_elems() const { return N * Cout * OH * OW; }
+  int64_t w_elems() const { return Cout * cpg() * KH * KW; }
+  int elem_bytes() const { return bf16 ? 2 : 4; }
+};
+
+// Fills `p` from `d` and checks it the way oarust's geometry resolvers do:
+// nonzero extents, stride, dilation and groups, channels divisible by groups,
+// the effective kernel fitting the padded input.  Element counts must fit the
+// kernels' 32-bit indexing.  Returns GBCONV_OK, GBCONV_EINVAL or GBCONV_EUNSUPPORTED.
+gbconv_status resolve(const gbconv_desc* d, Problem* p);
+
+// ---- launchers (each enqueues exactly one kernel) ----
+struct Launch {
+  void* stream;
+  unsigned int* status;  // device status word for bounded-wait failures
+  int num_sms;
+};
+
+gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                const Launch& l);
+gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
+gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_ohwi, const Launch& l);
+
+bool depthwise_supported(const Problem& p);
+gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                   const Launch& l);
+
+bool pointwise_supported(const Problem& p);
+gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                   const Launch& l);
+
+bool implicit_fwd_supported(const Problem& p);
+bool implicit_dgrad_supported(const Problem& p);
+gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                  const Launch& l);
+gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
+
+// Counts one enqueued kernel.
+void note_launch();
+
+}  // namespace gbconv

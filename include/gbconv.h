@@ -1,0 +1,132 @@
+/*
+ * gbconv: convolution forward and input gradient (dgrad) on one NVIDIA GB300
+ * (sm_103a), exposed as a plain C ABI.
+ *
+ * Operations (definitions as the source pages state them):
+ *
+ *   forward   y[n, co, o] = bias[co] + sum_{cl < C_in/G, k} x[n, g*C_in/G + cl, o*stride + k*dil - pad] * w[co, cl, k]
+ *             with g = co / (C_out/G), x taken as zero outside the input (cross-correlation, no kernel flip).
+ *             Sources: burn-cubecl `src/kernel/conv/im2col.rs`, doc of `im2col` (read position
+ *             out*stride + k*dilation - padding, zero outside); teeny-kernels `src/nn/conv/conv2d.rs`,
+ *             `conv2d_forward` (group window, weight [C_OUT, C_IN/G, KH, KW]) and `conv2d_bias_forward`
+ *             (bias added once after the reduction); oarust `src/rs/ml/matrix/conv.rs`, `conv_1d` and
+ *             `conv_2d` (NCL / NCHW inputs, OIK / OIHW weights).
+ *
+ *   dgrad     dx = the gradient of sum(y * dy) with respect to x for the bias-free forward above:
+ *             dx[n, ci, i] = sum over co in ci's group, k, and output positions o with o*stride + k*dil - pad == i
+ *             of dy[n, co, o] * w[co, ci - g*C_in/G, k].
+ *             Sources: teeny-kernels `conv2d_backward_dx` (the scatter form), oarust `conv_2d_backward`
+ *             (an input-gradient pass over input elements, i.e. the gather form).  The library computes the
+ *             gather form: every dx element is written once, with no atomics, so results are deterministic.
+ *
+ *   out size  out = (in + 2*pad - dil*(k - 1) - 1) / stride + 1 (floor), rejected when in + 2*pad < dil*(k-1) + 1.
+ *             Source: oarust `Conv1dGeometry::resolve`.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are dense and contiguous in the layouts named by the descriptor.  Activation layouts:
+ *    GBCONV_NCHW (NCL for 1-D) or GBCONV_NHWC (NLC for 1-D).  Weight layouts: GBCONV_W_OIHW
+ *    [C_out, C_in/G, KH, KW] (OIK for 1-D; the pages' canonical order) or GBCONV_W_OHWI
+ *    [C_out, KH, KW, C_in/G] (the channels-last weight order burn-cubecl's im2col column axis uses).
+ *  - Data pointers are DEVICE pointers owned by the caller; the library never allocates, frees or
+ *    retains them.  `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls only enqueue work: they return after the launch, not after the kernel finishes.
+ *  - Element types: GBCONV_F32 (x, w, y all float) or GBCONV_BF16 (x, w, y all bf16, accumulation in
+ *    fp32, one round-to-nearest-even at the store).  bias, when given, is always float [C_out].
+ *  - Errors: shape errors return GBCONV_EINVAL before anything is launched; shapes whose 32-bit device
+ *    indexing would overflow return GBCONV_EUNSUPPORTED; launch failures return GBCONV_ECUDA.  A kernel
+ *    whose internal wait gave up (it never should) records it on the device; gbconv_device_status reads it.
+ *  - Every valid shape is served on the GPU.  Which kernel family serves it is reported by gbconv_select.
+ */
+#ifndef GBCONV_H
+#define GBCONV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GBCONV_OK = 0,
+  GBCONV_EINVAL = 1,          /* invalid shape or argument (degenerate extent, kernel larger than padded input ...) */
+  GBCONV_EUNSUPPORTED = 2,    /* valid, but beyond this library's limits (32-bit element indexing) */
+  GBCONV_ECUDA = 3,           /* a CUDA runtime call failed; cudaGetLastError has the detail */
+  GBCONV_ETIMEOUT = 4         /* a kernel's bounded internal wait expired (reported by gbconv_device_status) */
+} gbconv_status;
+
+typedef enum { GBCONV_NCHW = 0, GBCONV_NHWC = 1 } gbconv_layout;
+typedef enum { GBCONV_W_OIHW = 0, GBCONV_W_OHWI = 1 } gbconv_wlayout;
+typedef enum { GBCONV_F32 = 0, GBCONV_BF16 = 1 } gbconv_dtype;
+
+/* Kernel families, as reported by gbconv_select. */
+typedef enum {
+  GBCONV_K_DIRECT = 0,        /* generic direct kernel on CUDA cores (any layout, dtype, groups, stride, dilation) */
+  GBCONV_K_DEPTHWISE = 1,     /* NHWC bf16 depthwise direct kernel, bandwidth bound */
+  GBCONV_K_POINTWISE = 2,     /* NHWC bf16 1x1: TMA-fed tcgen05 GEMM */
+  GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
+  GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 */
+  GBCONV_K_DIRECT_DGRAD = 5   /* generic gather dgrad on CUDA cores */
+} gbconv_kernel;
+
+typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1 } gbconv_op;
+
+/* One convolution.  For spatial_dims == 1 only index 0 of in/k/stride/pad/dil is read (the length
+ * axis); index 1 is ignored.  For spatial_dims == 2 index 0 is height and index 1 is width.
+ * Padding is symmetric: pad[i] zeros on both sides of axis i. */
+typedef struct {
+  int32_t spatial_dims;       /* 1 or 2 */
+  int32_t layout;             /* gbconv_layout of x, y, dy, dx */
+  int32_t wlayout;            /* gbconv_wlayout of w */
+  int32_t dtype;              /* gbconv_dtype of x, w, y, dy, dx */
+  int64_t n, c_in, c_out, groups;
+  int64_t in[2], k[2], stride[2], pad[2], dil[2];
+} gbconv_desc;
+
+/* Output spatial extent of the forward convolution (oarust Conv1dGeometry::resolve applied per axis).
+ * out[0] = OH (or L_out for 1-D), out[1] = OW (1 for 1-D).  Launches nothing.
+ * Returns GBCONV_EINVAL for a NULL argument or any shape the forward would reject. */
+gbconv_status gbconv_out_shape(const gbconv_desc *desc, int64_t out[2]);
+
+/* Which kernel family would serve `op` for this descriptor (pointers assumed 16-byte aligned).
+ * Launches nothing. */
+gbconv_status gbconv_select(const gbconv_desc *desc, int32_t op, int32_t *kernel);
+
+/* Forward convolution, y = conv(x, w) (+ bias).
+ *   x    : device, [N, C_in, in...] or [N, in..., C_in] per desc->layout, desc->dtype
+ *   w    : device, per desc->wlayout, desc->dtype
+ *   bias : device float [C_out], or NULL for no bias
+ *   y    : device, [N, C_out, out...] or [N, out..., C_out], desc->dtype; fully overwritten
+ * Enqueues exactly one kernel on `stream`.  y must not overlap x, w or bias. */
+gbconv_status gbconv_fwd(const gbconv_desc *desc, const void *x, const void *w, const float *bias,
+                         void *y, void *stream);
+
+/* Input gradient of the forward convolution described by desc (desc is the FORWARD descriptor: its
+ * input extent fixes dx's shape, which the output extent alone does not, see burn-cubecl
+ * `dgrad_im2col_1x1`, which takes the input shape for the same reason).
+ *   dy : device, forward-output shape, desc->dtype
+ *   w  : device, forward weight, per desc->wlayout
+ *   dx : device, forward-input shape, desc->dtype; fully overwritten (no need to zero it first)
+ * Enqueues exactly one kernel on `stream`.  Deterministic: the same inputs give bitwise-equal dx. */
+gbconv_status gbconv_bwd_data(const gbconv_desc *desc, const void *dy, const void *w, void *dx, void *stream);
+
+/* Re-lays a weight from [C_out, C_in/G, KH, KW] (OIHW) into [C_out, KH, KW, C_in/G] (OHWI), the order the
+ * NHWC tensor-core kernels read.  desc->dtype gives the element type; desc->wlayout is ignored.
+ * w_oihw and w_ohwi are device pointers that must not overlap.  Enqueues one kernel. */
+gbconv_status gbconv_pack_weight(const gbconv_desc *desc, const void *w_oihw, void *w_ohwi, void *stream);
+
+/* Synchronises `stream`, then returns GBCONV_ETIMEOUT if any kernel of this library on the current
+ * device recorded an expired internal wait since the last call (and clears the record), else GBCONV_OK
+ * (or GBCONV_ECUDA if the synchronisation itself failed). */
+gbconv_status gbconv_device_status(void *stream);
+
+/* Number of kernels this library has enqueued in this process (all devices, all streams). */
+uint64_t gbconv_kernels_launched(void);
+
+/* Static, human-readable name of a status code. */
+const char *gbconv_status_string(gbconv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBCONV_H */
