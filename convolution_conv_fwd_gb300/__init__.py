@@ -1,0 +1,264 @@
+"""Python binding of the gbconv C ABI (include/gbconv.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libgbconv.so.  The raw entry points keep the C names
+(``gbconv_fwd``, ``gbconv_bwd_data`` ...) and take integer device addresses;
+``conv_fwd`` / ``conv_bwd_data`` wrap them for torch tensors (device memory
+and the current stream come from PyTorch; nothing else does).
+
+Importing this module loads libgbconv.so and fails loudly if it has not been
+built (``python -m convolution_conv_fwd_gb300.build``): there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgbconv.so")
+
+# status codes
+GBCONV_OK, GBCONV_EINVAL, GBCONV_EUNSUPPORTED, GBCONV_ECUDA, GBCONV_ETIMEOUT = range(5)
+# layouts / dtypes
+GBCONV_NCHW, GBCONV_NHWC = 0, 1
+GBCONV_W_OIHW, GBCONV_W_OHWI = 0, 1
+GBCONV_F32, GBCONV_BF16 = 0, 1
+# kernel families
+KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad"}
+GBCONV_OP_FWD, GBCONV_OP_BWD_DATA = 0, 1
+
+EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
+           "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
+
+
+class Desc(ctypes.Structure):
+    """Mirror of gbconv_desc."""
+    _fields_ = [("spatial_dims", ctypes.c_int32), ("layout", ctypes.c_int32), ("wlayout", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("n", ctypes.c_int64), ("c_in", ctypes.c_int64),
+                ("c_out", ctypes.c_int64), ("groups", ctypes.c_int64), ("in_", ctypes.c_int64 * 2),
+                ("k", ctypes.c_int64 * 2), ("stride", ctypes.c_int64 * 2), ("pad", ctypes.c_int64 * 2),
+                ("dil", ctypes.c_int64 * 2)]
+
+
+class GbconvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libgbconv.so is not built at %s; run `python -m convolution_conv_fwd_gb300.build`"
+                          % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    vp, st = ctypes.c_void_p, ctypes.c_int
+    lib.gbconv_out_shape.argtypes = [P(Desc), P(ctypes.c_int64)]
+    lib.gbconv_select.argtypes = [P(Desc), ctypes.c_int32, P(ctypes.c_int32)]
+    lib.gbconv_fwd.argtypes = [P(Desc), vp, vp, vp, vp, vp]
+    lib.gbconv_bwd_data.argtypes = [P(Desc), vp, vp, vp, vp]
+    lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
+    lib.gbconv_device_status.argtypes = [vp]
+    for f in ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
+              "gbconv_device_status"):
+        getattr(lib, f).restype = st
+    lib.gbconv_kernels_launched.argtypes = []
+    lib.gbconv_kernels_launched.restype = ctypes.c_uint64
+    lib.gbconv_status_string.argtypes = [st]
+    lib.gbconv_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+# ---------------------------------------------------------------- raw C entry points
+
+def gbconv_out_shape(desc: Desc):
+    out = (ctypes.c_int64 * 2)()
+    s = _lib.gbconv_out_shape(ctypes.byref(desc), out)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_out_shape")
+    return int(out[0]), int(out[1])
+
+
+def gbconv_select(desc: Desc, op: int) -> str:
+    k = ctypes.c_int32(-1)
+    s = _lib.gbconv_select(ctypes.byref(desc), op, ctypes.byref(k))
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_select")
+    return KERNELS[k.value]
+
+
+def gbconv_fwd(desc: Desc, x: int, w: int, bias: int | None, y: int, stream: int) -> int:
+    return _lib.gbconv_fwd(ctypes.byref(desc), x, w, bias or None, y, stream or None)
+
+
+def gbconv_bwd_data(desc: Desc, dy: int, w: int, dx: int, stream: int) -> int:
+    return _lib.gbconv_bwd_data(ctypes.byref(desc), dy, w, dx, stream or None)
+
+
+def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int:
+    return _lib.gbconv_pack_weight(ctypes.byref(desc), w_oihw, w_ohwi, stream or None)
+
+
+def gbconv_device_status(stream: int) -> int:
+    return _lib.gbconv_device_status(stream or None)
+
+
+def gbconv_kernels_launched() -> int:
+    return int(_lib.gbconv_kernels_launched())
+
+
+def status_string(status: int) -> str:
+    return _lib.gbconv_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- descriptors
+
+def make_desc(n, c_in, c_out, in_size, k, stride=1, pad=0, dil=1, groups=1, *, spatial_dims=2,
+              layout="nhwc", wlayout="ohwi", dtype="bf16") -> Desc:
+    """Build a gbconv_desc.  Sizes are ints (1-D) or pairs (2-D)."""
+    def pair(v):
+        if isinstance(v, (tuple, list)):
+            return (int(v[0]), int(v[1]) if len(v) > 1 else 1)
+        return (int(v), int(v)) if spatial_dims == 2 else (int(v), 1)
+    d = Desc()
+    d.spatial_dims = spatial_dims
+    d.layout = {"nchw": GBCONV_NCHW, "ncl": GBCONV_NCHW, "nhwc": GBCONV_NHWC, "nlc": GBCONV_NHWC}[layout]
+    d.wlayout = {"oihw": GBCONV_W_OIHW, "oik": GBCONV_W_OIHW, "ohwi": GBCONV_W_OHWI, "oki": GBCONV_W_OHWI}[wlayout]
+    d.dtype = {"f32": GBCONV_F32, "bf16": GBCONV_BF16}[dtype]
+    d.n, d.c_in, d.c_out, d.groups = int(n), int(c_in), int(c_out), int(groups)
+    for name, v in (("in_", in_size), ("k", k), ("stride", stride), ("pad", pad), ("dil", dil)):
+        a, b = pair(v)
+        getattr(d, name)[0] = a
+        getattr(d, name)[1] = b
+    return d
+
+
+def desc_shapes(d: Desc):
+    """(x_shape, w_shape, y_shape) in the layouts the descriptor names."""
+    oh, ow = gbconv_out_shape(d)
+    cpg = d.c_in // d.groups
+    if d.spatial_dims == 1:
+        L, K = d.in_[0], d.k[0]
+        x = (d.n, L, d.c_in) if d.layout == GBCONV_NHWC else (d.n, d.c_in, L)
+        y = (d.n, oh, d.c_out) if d.layout == GBCONV_NHWC else (d.n, d.c_out, oh)
+        w = (d.c_out, K, cpg) if d.wlayout == GBCONV_W_OHWI else (d.c_out, cpg, K)
+        return x, w, y
+    H, W, KH, KW = d.in_[0], d.in_[1], d.k[0], d.k[1]
+    x = (d.n, H, W, d.c_in) if d.layout == GBCONV_NHWC else (d.n, d.c_in, H, W)
+    y = (d.n, oh, ow, d.c_out) if d.layout == GBCONV_NHWC else (d.n, d.c_out, oh, ow)
+    w = (d.c_out, KH, KW, cpg) if d.wlayout == GBCONV_W_OHWI else (d.c_out, cpg, KH, KW)
+    return x, w, y
+
+
+# ---------------------------------------------------------------- torch helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(t, shape, dtype, name):
+    torch = _torch()
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+    return t
+
+
+def _dtype(d: Desc):
+    torch = _torch()
+    return torch.bfloat16 if d.dtype == GBCONV_BF16 else torch.float32
+
+
+def conv_fwd(d: Desc, x, w, bias=None, y=None):
+    """y = conv(x, w) (+ bias) on the current CUDA stream.
+
+    x, w (and y if given) are contiguous CUDA tensors in the descriptor's
+    layouts and dtype; bias is a float32 CUDA tensor [C_out] or None.  Host
+    (CPU) tensors are copied to the current device first and the result is
+    copied back, so the same call serves device-resident and host data.
+    """
+    torch = _torch()
+    host = not x.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        x = x.to(dev, non_blocking=True)
+        w = w.to(dev, non_blocking=True)
+        bias = None if bias is None else bias.to(dev, non_blocking=True)
+    xs, ws, ys = desc_shapes(d)
+    dt = _dtype(d)
+    _check(x, xs, dt, "x")
+    _check(w, ws, dt, "w")
+    if bias is not None:
+        _check(bias, (d.c_out,), torch.float32, "bias")
+    out = y if (y is not None and not host) else torch.empty(ys, dtype=dt, device=x.device)
+    _check(out, ys, dt, "y")
+    s = gbconv_fwd(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
+                   torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_fwd")
+    if host:
+        res = torch.empty(ys, dtype=dt, pin_memory=True) if y is None else y
+        res.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return res
+    return out
+
+
+def conv_bwd_data(d: Desc, dy, w, dx=None):
+    """Input gradient of the forward convolution ``d`` on the current CUDA stream.
+
+    dy has the forward output's shape, w the forward weight's; the result has
+    the forward input's shape (the descriptor fixes it).  Host tensors are
+    staged through the device as in ``conv_fwd``.
+    """
+    torch = _torch()
+    host = not dy.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        dy = dy.to(dev, non_blocking=True)
+        w = w.to(dev, non_blocking=True)
+    xs, ws, ys = desc_shapes(d)
+    dt = _dtype(d)
+    _check(dy, ys, dt, "dy")
+    _check(w, ws, dt, "w")
+    out = dx if (dx is not None and not host) else torch.empty(xs, dtype=dt, device=dy.device)
+    _check(out, xs, dt, "dx")
+    s = gbconv_bwd_data(d, dy.data_ptr(), w.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_bwd_data")
+    if host:
+        res = torch.empty(xs, dtype=dt, pin_memory=True) if dx is None else dx
+        res.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return res
+    return out
+
+
+def pack_weight(d: Desc, w_oihw):
+    """OIHW -> OHWI copy of a weight, on the device."""
+    torch = _torch()
+    dt = _dtype(d)
+    cpg = d.c_in // d.groups
+    if d.spatial_dims == 1:
+        src_shape, dst_shape = (d.c_out, cpg, d.k[0]), (d.c_out, d.k[0], cpg)
+    else:
+        src_shape, dst_shape = (d.c_out, cpg, d.k[0], d.k[1]), (d.c_out, d.k[0], d.k[1], cpg)
+    _check(w_oihw, src_shape, dt, "w_oihw")
+    out = torch.empty(dst_shape, dtype=dt, device=w_oihw.device)
+    s = gbconv_pack_weight(d, w_oihw.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_pack_weight")
+    return out
+
+
+def device_status():
+    """Raise if a kernel of this library recorded an expired internal wait."""
+    torch = _torch()
+    s = gbconv_device_status(torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_device_status")

@@ -1,0 +1,100 @@
+"""The five benchmark workloads: tensor shapes and value recipes, nothing else.
+
+Shapes are stated explicitly (including the output-gradient shape of the dgrad
+workload, which its description gives); no convolution arithmetic lives here.
+Values come from ``synth`` with seed ``1000 + index`` unless a caller passes
+another seed; bf16 workloads round the drawn values to bf16 (RNE) and hand the
+same bits to the GPU and the oracle.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import as_bf16, normal, uniform
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    op: str                 # "fwd" or "dgrad"
+    dtype: str              # "f32" or "bf16"
+    spatial_dims: int
+    layout: str             # "ncl" / "nhwc"
+    wlayout: str            # "oik" / "ohwi"
+    n: int
+    c_in: int
+    c_out: int
+    in_size: tuple          # (L,) or (H, W)
+    k: tuple
+    stride: tuple
+    pad: tuple
+    dil: tuple
+    groups: int
+    bias: bool
+    x_shape: tuple          # forward input (fwd) -- or dx shape (dgrad)
+    w_shape: tuple
+    g_shape: tuple          # output gradient shape (dgrad only)
+    recipe: dict = field(default_factory=dict)
+    describe: str = ""
+
+
+WORKLOADS = [
+    Workload("conv1d_ncl_f32", 0, "fwd", "f32", 1, "ncl", "oik", 2, 4, 8, (32,), (3,), (1,), (2,), (2,), 1, True,
+             (2, 4, 32), (8, 4, 3), (),
+             {"x": ("uniform", -1, 1), "w": ("uniform", -1, 1), "b": ("uniform", -1, 1)},
+             "conv1d NCL fp32, N=2, C_in=4, C_out=8, L=32, K=3, stride 1, pad 2, dilation 2, bias"),
+    Workload("pointwise_1x1_nhwc_bf16", 1, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 256, 64, (56, 56), (1, 1), (1, 1),
+             (0, 0), (1, 1), 1, False, (32, 56, 56, 256), (64, 1, 1, 256), (),
+             {"x": ("normal", 1.0), "w": ("normal", (1.0 / 256) ** 0.5)},
+             "pointwise 1x1 conv2d NHWC bf16, N=32, 56x56, C 256->64, no bias"),
+    Workload("dense3x3_nhwc_bf16", 2, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 64, 64, (56, 56), (3, 3), (1, 1),
+             (1, 1), (1, 1), 1, True, (32, 56, 56, 64), (64, 3, 3, 64), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 9)) ** 0.5), "b": ("normal", 0.1)},
+             "dense 3x3 conv2d NHWC bf16, N=32, 56x56, C 64->64, stride 1, pad 1, fp32 bias"),
+    Workload("depthwise3x3_s2_nhwc_bf16", 3, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 256, 256, (112, 112), (3, 3),
+             (2, 2), (1, 1), (1, 1), 256, False, (32, 112, 112, 256), (256, 3, 3, 1), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / 9) ** 0.5)},
+             "depthwise 3x3 conv2d NHWC bf16, N=32, 112x112, C=G=256, stride 2, pad 1, no bias"),
+    Workload("dgrad3x3_s2_nhwc_bf16", 4, "dgrad", "bf16", 2, "nhwc", "ohwi", 16, 128, 256, (64, 64), (3, 3),
+             (2, 2), (1, 1), (1, 1), 1, False, (16, 64, 64, 128), (256, 3, 3, 128), (16, 32, 32, 256),
+             {"g": ("normal", 1.0), "w": ("normal", (2.0 / (128 * 9)) ** 0.5)},
+             "conv2d backward-data NHWC bf16, 3x3 stride 2 pad 1, x 16x64x64x128, dy 16x32x32x256"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _draw(spec, seed, shape):
+    kind = spec[0]
+    if kind == "uniform":
+        return uniform(seed, shape, spec[1], spec[2])
+    if kind == "normal":
+        return normal(seed, shape, spec[1])
+    raise ValueError(kind)
+
+
+def make_inputs(wl: Workload, seed: int | None = None) -> dict:
+    """Draw the workload's inputs.
+
+    Returns float32 arrays ``x``/``g`` (input or output gradient), ``w`` and,
+    when the workload has one, float32 ``b``; for bf16 workloads also the
+    uint16 bit patterns ``x_bits``/``g_bits`` and ``w_bits`` of the same values.
+    """
+    base = 1000 + wl.index if seed is None else seed
+    out = {}
+    names = [("g", wl.g_shape)] if wl.op == "dgrad" else [("x", wl.x_shape)]
+    names.append(("w", wl.w_shape))
+    for i, (name, shape) in enumerate(names):
+        v = _draw(wl.recipe[name], base * 16 + i, shape)
+        if wl.dtype == "bf16":
+            bits, f = as_bf16(v)
+            out[name + "_bits"] = bits
+            out[name] = f
+        else:
+            out[name] = v.astype(np.float32)
+    if wl.bias:
+        out["b"] = _draw(wl.recipe["b"], base * 16 + 7, (wl.c_out,)).astype(np.float32)
+    return out

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library is built here (nvcc cross-compiles for sm_103a), loaded through
+ctypes, and checked for: every function include/gbconv.h declares is
+exported; output sizes agree with the oracle; invalid shapes and arguments are
+rejected before anything is launched; the kernel family chosen per workload.
+"""
+import os
+import re
+
+import pytest
+
+import oracle
+from synth.workloads import WORKLOADS
+from tests.helpers import lib_desc, oracle_conv, shape_kw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gb():
+    from convolution_conv_fwd_gb300 import build
+    build.build()
+    import convolution_conv_fwd_gb300 as gb
+    return gb
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gbconv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gbconv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(gb):
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(gb._lib, name), name
+    assert set(names) == set(gb.EXPORTS)
+
+
+@pytest.mark.parametrize("kw", [
+    shape_kw(),
+    shape_kw(in_size=(112, 112), c_in=256, c_out=256, groups=256, stride=(2, 2)),
+    shape_kw(in_size=(63, 64), stride=(2, 2), k=(3, 3), pad=(1, 1)),
+    shape_kw(in_size=(10, 7), k=(4, 2), stride=(3, 2), pad=(2, 0), dil=(3, 2)),
+    shape_kw(spatial_dims=1, in_size=(32,), k=(3,), stride=(1,), pad=(2,), dil=(2,), layout="ncl", wlayout="oik",
+             dtype="f32"),
+    shape_kw(spatial_dims=1, in_size=(17,), k=(4,), stride=(3,), pad=(1,), dil=(2,)),
+])
+def test_out_shape_matches_oracle(gb, kw):
+    d = lib_desc(gb, kw)
+    c = oracle_conv(kw)
+    oh, ow = gb.gbconv_out_shape(d)
+    if kw["spatial_dims"] == 1:
+        assert (oh, ow) == (c.out_hw()[1], 1)
+    else:
+        assert (oh, ow) == c.out_hw()
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=0), dict(c_in=0), dict(c_out=0), dict(groups=0), dict(groups=5), dict(stride=(0, 1)),
+    dict(dil=(1, 0)), dict(k=(11, 3)), dict(in_size=(0, 8)), dict(pad=(-1, 0)),
+])
+def test_degenerate_shapes_rejected(gb, bad):
+    kw = shape_kw(c_in=12, c_out=12, groups=2)
+    kw.update(bad)
+    d = lib_desc(gb, kw)
+    with pytest.raises(gb.GbconvError) as e:
+        gb.gbconv_out_shape(d)
+    assert e.value.status == gb.GBCONV_EINVAL
+    # the enqueuing entry points reject the same shape before touching the device
+    assert gb.gbconv_fwd(d, 16, 16, None, 16, 0) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_data(d, 16, 16, 16, 0) == gb.GBCONV_EINVAL
+    assert not oracle.check(oracle_conv(kw))  # the oracle rejects the same shapes
+
+
+def test_enum_fields_and_null_pointers_rejected(gb):
+    d = lib_desc(gb, shape_kw())
+    assert gb.gbconv_fwd(d, 0, 16, None, 16, 0) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd(d, 16, 0, None, 16, 0) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd(d, 16, 16, None, 0, 0) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_data(d, 0, 16, 16, 0) == gb.GBCONV_EINVAL
+    assert gb.gbconv_pack_weight(d, 0, 16, 0) == gb.GBCONV_EINVAL
+    for field, value in (("spatial_dims", 3), ("layout", 7), ("wlayout", -1), ("dtype", 5)):
+        d2 = lib_desc(gb, shape_kw())
+        setattr(d2, field, value)
+        assert gb.gbconv_fwd(d2, 16, 16, None, 16, 0) == gb.GBCONV_EINVAL
+
+
+def test_index_overflow_is_unsupported(gb):
+    d = lib_desc(gb, shape_kw(n=4096, in_size=(1024, 1024), c_in=64, c_out=64))
+    assert gb.gbconv_fwd(d, 16, 16, None, 16, 0) == gb.GBCONV_EUNSUPPORTED
+    with pytest.raises(gb.GbconvError) as e:
+        gb.gbconv_out_shape(d)
+    assert e.value.status == gb.GBCONV_EUNSUPPORTED
+
+
+def test_status_strings(gb):
+    for s in range(5):
+        assert gb.status_string(s)
+    assert gb.status_string(99) == "unknown status"
+
+
+EXPECTED_FAMILY = {
+    "conv1d_ncl_f32": {"direct"},
+    "pointwise_1x1_nhwc_bf16": {"pointwise", "implicit"},  # pointwise needs the driver's TMA encoder
+    "dense3x3_nhwc_bf16": {"implicit"},
+    "depthwise3x3_s2_nhwc_bf16": {"depthwise"},
+    "dgrad3x3_s2_nhwc_bf16": {"dgrad"},
+}
+
+
+@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_workload_kernel_family(gb, wl):
+    d = lib_desc(gb, wl)
+    op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
+    assert gb.gbconv_select(d, op) in EXPECTED_FAMILY[wl.name]
+
+
+def test_generic_families_for_other_layouts(gb):
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(layout="nchw", wlayout="oihw")), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(dtype="f32")), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(groups=2)), 1) == "direct_dgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), c_in=32, c_out=32)), 1) == "dgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 1) == "direct_dgrad"  # C_in=16: no 32-wide N tile

