@@ -7,7 +7,7 @@ kernels of libgbconv.so.  The raw entry points keep the C names
 and the current stream come from PyTorch; nothing else does).
 
 Importing this module loads libgbconv.so and fails loudly if it has not been
-built (``python -m convolution_conv_fwd_gb300.build``): there is no fallback.
+built (``python convolution_conv_fwd_gb300/build.py``): there is no fallback.
 """
 from __future__ import annotations
 
@@ -48,7 +48,7 @@ class GbconvError(RuntimeError):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libgbconv.so is not built at %s; run `python -m convolution_conv_fwd_gb300.build`"
+        raise ImportError("libgbconv.so is not built at %s; run `python convolution_conv_fwd_gb300/build.py`"
                           % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER

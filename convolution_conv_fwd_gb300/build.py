@@ -2,7 +2,9 @@
 
 Each translation unit is compiled by its own nvcc process (in parallel), then
 linked into one shared library next to this file.  Objects go to _build/.
-Run as ``python -m convolution_conv_fwd_gb300.build`` or call ``build()``.
+Run as ``python convolution_conv_fwd_gb300/build.py`` or load this file and
+call ``build()``; it imports nothing from the package (whose import needs the
+library this file builds).
 """
 from __future__ import annotations
 

@@ -19,8 +19,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def gb():
-    from convolution_conv_fwd_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import convolution_conv_fwd_gb300 as gb
     return gb
 
