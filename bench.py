@@ -1,0 +1,428 @@
+"""Benchmark: the convolution hot path on GB300, one JSON line on stdout.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+each of the five workloads (conv1d fp32 NCL, 1x1 NHWC bf16, dense 3x3 NHWC
+bf16, depthwise 3x3 stride-2 NHWC bf16, 3x3 stride-2 dgrad NHWC bf16) is run
+once through the C ABI, inputs resident in HBM.  L2 is flushed (a write larger
+than L2) before every kernel, and each kernel is timed with CUDA events on the
+stream it runs on.  ``value`` is the step's aggregate TFLOP/s (algorithmic
+flops / summed kernel time); per-workload TFLOP/s, GB/s and roofline
+fractions are in ``per_config``; ``roofline`` describes the kernel that takes
+the largest share of the step.
+
+``--impl reference`` times the FP64 CPU oracle instead (the reference arm: a
+bounded sample of every workload per step, on the host cores).
+
+Multi-GPU (torchrun): each rank runs the same step on its own GPU (replicas,
+weak scaling, no collective on the data path); the step time is the max over
+ranks and ``value`` the work of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "conv fwd/dgrad TFLOP/s (or GB/s) per config and % of roofline on 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD_NAME = "conv hot path: 5 workloads per step (conv1d f32, 1x1, dense 3x3, depthwise 3x3 s2, dgrad 3x3 s2)"
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    return p
+
+
+def out_hw(wl):
+    """Output extent of a workload (the forward's), from the output-size rule."""
+    res = []
+    for i in range(wl.spatial_dims):
+        eff = (wl.k[i] - 1) * wl.dil[i] + 1
+        res.append((wl.in_size[i] + 2 * wl.pad[i] - eff) // wl.stride[i] + 1)
+    return res
+
+
+def work(wl):
+    """(algorithmic flops, compulsory bytes) of one launch of a workload."""
+    o = int(np.prod(out_hw(wl)))
+    taps = int(np.prod(wl.k))
+    flops = 2 * wl.n * o * wl.c_out * (wl.c_in // wl.groups) * taps
+    es = 4 if wl.dtype == "f32" else 2
+    x = wl.n * int(np.prod(wl.in_size)) * wl.c_in * es
+    y = wl.n * o * wl.c_out * es
+    w = wl.c_out * (wl.c_in // wl.groups) * taps * es
+    b = 4 * wl.c_out if wl.bias else 0
+    return flops, x + y + w + b
+
+
+def desc_for(gb, wl):
+    one = (lambda t: t[0]) if wl.spatial_dims == 1 else (lambda t: tuple(t))
+    return gb.make_desc(wl.n, wl.c_in, wl.c_out, one(wl.in_size), one(wl.k), one(wl.stride), one(wl.pad),
+                        one(wl.dil), wl.groups, spatial_dims=wl.spatial_dims, layout=wl.layout,
+                        wlayout=wl.wlayout, dtype=wl.dtype)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "convolution_conv_fwd_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        # | kernel file | source sha256[:16] | dram bytes per launch | ...
+        parts = [p.strip() for p in line.split("|")]
+        if len(parts) > 4 and parts[1] == kernel_file and parts[2] == digest:
+            try:
+                return float(parts[3])
+            except ValueError:
+                return None
+    return None
+
+
+KERNEL_FILE = {"direct": "direct.cu", "depthwise": "depthwise.cu", "pointwise": "pointwise.cu",
+               "implicit": "implicit.cu", "dgrad": "implicit.cu", "direct_dgrad": "direct.cu"}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import convolution_conv_fwd_gb300 as gb
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    cases = []
+    for wl in WORKLOADS:
+        inp = make_inputs(wl)
+        d = desc_for(gb, wl)
+        xs, ws, ys = gb.desc_shapes(d)
+        if wl.dtype == "bf16":
+            def t(bits):
+                return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+            src = t(inp["g_bits"] if wl.op == "dgrad" else inp["x_bits"])
+            w = t(inp["w_bits"])
+            dt = torch.bfloat16
+        else:
+            src = torch.from_numpy(inp["x"]).to(dev)
+            w = torch.from_numpy(inp["w"]).to(dev)
+            dt = torch.float32
+        b = torch.from_numpy(inp["b"]).to(dev) if "b" in inp else None
+        out = torch.empty(xs if wl.op == "dgrad" else ys, dtype=dt, device=dev)
+        op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
+        family = gb.gbconv_select(d, op)
+        flops, nbytes = work(wl)
+        cases.append(dict(wl=wl, d=d, src=src, w=w, b=b, out=out, family=family, flops=flops, bytes=nbytes,
+                          host=inp))
+
+    def launch(c):
+        s = stream.cuda_stream
+        if c["wl"].op == "dgrad":
+            rc = gb.gbconv_bwd_data(c["d"], c["src"].data_ptr(), c["w"].data_ptr(), c["out"].data_ptr(), s)
+        else:
+            rc = gb.gbconv_fwd(c["d"], c["src"].data_ptr(), c["w"].data_ptr(),
+                               None if c["b"] is None else c["b"].data_ptr(), c["out"].data_ptr(), s)
+        if rc != gb.GBCONV_OK:
+            raise gb.GbconvError(rc, c["wl"].name)
+
+    def step(events=None):
+        for i, c in enumerate(cases):
+            flush.zero_()
+            if events is not None:
+                events[i][0].record(stream)
+            launch(c)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    gb.device_status()
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cases]
+           for _ in range(args.steps)]
+    launches0 = gb.gbconv_kernels_launched()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    launches = gb.gbconv_kernels_launched() - launches0
+    gb.device_status()
+    per_kernel_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
+                     for i in range(len(cases))]
+    step_ms = sum(per_kernel_ms)
+    if world > 1:
+        tt = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    # ---------------------------------------------------------------- end to end through the public API
+    e2e_ms, h2d, d2h = None, 0, 0
+    host_cases = []
+    for c in cases:
+        hs = c["src"].cpu().pin_memory()
+        hw = c["w"].cpu().pin_memory()
+        hb = None if c["b"] is None else c["b"].cpu().pin_memory()
+        host_cases.append((c, hs, hw, hb))
+        h2d += hs.numel() * hs.element_size() + hw.numel() * hw.element_size() + (0 if hb is None else hb.numel() * 4)
+        d2h += c["out"].numel() * c["out"].element_size()
+    def e2e_step():
+        for c, hs, hw, hb in host_cases:
+            if c["wl"].op == "dgrad":
+                gb.conv_bwd_data(c["d"], hs, hw)
+            else:
+                gb.conv_fwd(c["d"], hs, hw, hb)
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    total_flops = sum(c["flops"] for c in cases)
+    per = []
+    for c, ms in zip(cases, per_kernel_ms):
+        t_f = c["flops"] / (pk["bf16_tflops"] * 1e12)
+        t_b = c["bytes"] / (pk["hbm_gbs"] * 1e9)
+        t_roof = max(t_f, t_b)
+        per.append({"workload": c["wl"].name, "kernel": c["family"], "us": round(ms * 1e3, 3),
+                    "tflops": round(c["flops"] / (ms * 1e-3) / 1e12, 2),
+                    "gbs": round(c["bytes"] / (ms * 1e-3) / 1e9, 1),
+                    "bound": "tensor" if t_f >= t_b else "hbm", "t_roof_us": round(t_roof * 1e6, 3),
+                    "roofline_frac": round(t_roof / (ms * 1e-3), 4)})
+    dom = max(range(len(cases)), key=lambda i: per_kernel_ms[i])
+    dc, dms = cases[dom], per_kernel_ms[dom]
+    if per[dom]["bound"] == "hbm":
+        achieved, peak, unit = dc["bytes"] / (dms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = dc["flops"] / (dms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    roof = {"bound": per[dom]["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic_record(KERNEL_FILE[dc["family"]]),
+            "kernel": dc["family"], "workload": dc["wl"].name,
+            "algorithmic_bytes": dc["bytes"], "algorithmic_flops": dc["flops"],
+            "peak_source": pk["source"] + " (burst)"}
+    value = world * total_flops / (step_ms * 1e-3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "l2": "flushed before every kernel (write of 2x L2)",
+                   "inputs": "seeded SplitMix64/Box-Muller, bf16 RNE; conv1d workload fp32",
+                   "step_roofline_frac": round(sum(p["t_roof_us"] for p in per) / (step_ms * 1e3), 4),
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "per_config": per,
+        "roofline": roof,
+        "e2e": {"value": round(world * total_flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    return res, cases
+
+
+def cpu_sample(target_s: float, cases_host):
+    """Time the FP64 oracle on a bounded, strided sample of every workload's outputs."""
+    import oracle
+    from tests.helpers import oracle_conv  # the same shape mapping the tests use
+    oracle.build()
+    per_point = []
+    for wl, inp in cases_host:
+        c = oracle_conv(wl)
+        if wl.op == "dgrad":
+            n, ch, h, w = wl.n, wl.c_in, wl.in_size[0], wl.in_size[1]
+            iters = (wl.c_out // wl.groups) * int(np.prod(wl.k))
+        else:
+            oh = out_hw(wl)
+            n, ch = wl.n, wl.c_out
+            h, w = (oh[0], oh[1]) if wl.spatial_dims == 2 else (1, oh[0])
+            iters = (wl.c_in // wl.groups) * int(np.prod(wl.k))
+        per_point.append((wl, inp, c, (n, ch, h, w), iters))
+    # calibrate: a small sample of the heaviest workload
+    budget_iters = None
+    wl, inp, c, shp, iters = max(per_point, key=lambda p: p[4])
+    probe = 2000
+    t = _time_points(wl, inp, c, shp, probe)
+    rate = probe * iters / max(t, 1e-6)  # inner iterations per second
+    budget_iters = rate * target_s
+    total_flops, total_s, points = 0.0, 0.0, {}
+    for wl, inp, c, shp, iters in per_point:
+        outputs = int(np.prod(shp))
+        count = int(min(outputs, max(256, budget_iters / len(per_point) / iters)))
+        dt = _time_points(wl, inp, c, shp, count)
+        flops, _ = work(wl)
+        total_flops += flops * count / outputs
+        total_s += dt
+        points[wl.name] = count
+    return total_flops, total_s, points
+
+
+def _time_points(wl, inp, c, shp, count):
+    import oracle
+    n, ch, h, w = shp
+    total = n * ch * h * w
+    stride = max(1, total // count)
+    flat = (np.arange(count, dtype=np.int64) * stride) % total
+    idx = np.stack(np.unravel_index(flat, (n, ch, h, w)), axis=1).astype(np.int64)
+    t0 = time.perf_counter()
+    if wl.op == "dgrad":
+        oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
+    else:
+        oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    """The reference arm: the FP64 oracle on the host cores, one bounded sample per step."""
+    cases_host = [(wl, make_inputs(wl)) for wl in WORKLOADS]
+    for _ in range(args.warmup):
+        cpu_sample(0.5, cases_host)
+    flops, secs = 0.0, 0.0
+    points = {}
+    for _ in range(args.steps):
+        f, s, points = cpu_sample(args.ref_seconds_per_step, cases_host)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    sample = "strided sample of every workload's outputs per step, %s points" % json.dumps(points)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME}, "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gbconv", choices=["gbconv", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work for the cpu_baseline sample")
+    ap.add_argument("--ref-seconds-per-step", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gbconv":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res, cases = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        host = [(c["wl"], c["host"]) for c in cases]
+        flops, secs, points = cpu_sample(args.cpu_seconds, host)
+        res["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+                               "sample": "strided sample of every workload's outputs, %s points, %.1f s"
+                                         % (json.dumps(points), secs)}
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
