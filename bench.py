@@ -225,6 +225,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         t0 = time.perf_counter()
+        # A spin kernel first, so every later launch is queued before the GPU reaches it: the events
+        # then bracket device time only, with no gaps from host-side launch latency.
+        torch.cuda._sleep(int(3e8))
         for k in range(args.steps):
             step(evs[k])
         torch.cuda.synchronize()

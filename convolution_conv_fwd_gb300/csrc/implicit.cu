@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "problem.h"
@@ -568,8 +569,15 @@ bool plan_dgrad(const Problem& p, Plan& pl) {
 template <int BN, int NSUB, bool DGRAD, bool BRES>
 gbconv_status run(const Plan& pl, const Launch& l) {
   auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem)) != cudaSuccess)
-    return GBCONV_ECUDA;
+  // The shared-memory opt-in is a per-device function attribute: set it once per device and size.
+  static std::atomic<uint64_t> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  if (done[dev].load(std::memory_order_acquire) < uint64_t(pl.smem)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem)) != cudaSuccess)
+      return GBCONV_ECUDA;
+    done[dev].store(uint64_t(pl.smem), std::memory_order_release);
+  }
   kern<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(l.stream)>>>(pl.a);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;

@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -221,8 +222,15 @@ template <int BN>
 gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a, int grid, const Launch& l) {
   const size_t smem = size_t(a.kb_count) * BN * kBK * 2 + size_t(a.stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8);
   auto kern = pointwise_gemm_kernel<BN>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-    return GBCONV_ECUDA;
+  // The shared-memory opt-in is a per-device function attribute: set it once per device and size.
+  static std::atomic<uint64_t> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  if (done[dev].load(std::memory_order_acquire) < uint64_t(smem)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+      return GBCONV_ECUDA;
+    done[dev].store(uint64_t(smem), std::memory_order_release);
+  }
   kern<<<grid, kThreads, smem, static_cast<cudaStream_t>(l.stream)>>>(ta, tb, a);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
