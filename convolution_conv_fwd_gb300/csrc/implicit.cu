@@ -4,41 +4,48 @@
 //
 //  * dense forward at unit stride (the 3x3 workload): y = sum over taps of a
 //    shifted window of x times the tap's [C_out, C_in] weight slice;
-//  * the input gradient at any stride up to 2x2, in gather form: dx is split
-//    into stride phases (ih % s_h, iw % s_w); inside one phase every tap that
-//    reaches it does so at a fixed integer shift of dy, so each phase is again
-//    a sum of shifted windows, now of dy, times transposed weight slices.
+//  * the input gradient at strides up to 2x2, in gather form: dx is split into
+//    stride phases (ih % s_h, iw % s_w); inside one phase every tap that reaches
+//    it does so at a fixed integer shift of dy, so each phase is again a sum of
+//    shifted windows, now of dy, times the tap's weight slice read transposed.
 //    Each dx element is produced by exactly one accumulator and written once;
 //    there are no atomics and the result is deterministic.
 //
 // No im2col matrix is materialised (burn-cubecl `im2col.rs` notes that the
 // column matrix holds every pixel once per tap that reads it, nine times for
-// a 3x3).  Instead, a tile of 128 * NSUB consecutive positions of a "virtual
-// grid" (the output rows, each widened by the kernel's horizontal reach) is
-// computed from one halo tile in shared memory: position q of the tile reads
-// tap t at halo row q + off(t), so every tap's A operand is the same halo
-// tile with a different start address.  The halo is stored in the no-swizzle
-// K-major core-matrix layout ([8-channel chunk][halo row][16 bytes]) whose
-// rows are 16 bytes apart, so a shift by any number of rows is a plain
-// descriptor offset.
+// a 3x3).  Positions are laid out on a per-image "virtual grid": R rows of P
+// columns, P being the valid output width plus the kernel's horizontal reach.
+// A tile of 128*NSUB consecutive positions reads, for every tap t, the window
+// that starts off(t) rows later in one halo block held in shared memory; the
+// halo block is a single 4-D TMA box of whole virtual rows (zero fill supplies
+// the padding), stored as 128-byte swizzled K-major rows, and because the
+// swizzle follows absolute shared-memory addresses a tap is only a different
+// descriptor start address.
+//
+// Weights are TMA boxes of the caller's OHWI tensor: K-major [C_out, C_in]
+// slices for the forward, and for the gradient the same bytes read as an
+// MN-major operand (C_in is the GEMM N dimension and is contiguous), so no
+// transposed copy of the weight is ever made.
 //
 // Roles (warp specialised, one CTA per SM, persistent over work items):
-//   warps 0-3  epilogue: TMEM -> registers, + bias, -> bf16, NHWC stores
-//   warp  4    TMEM allocation; lane 0 issues every tcgen05.mma and commit
-//   warps 5-8  producers: cp.async halo fill (zero fill covers the padding)
-//              and weight tiles (transposed in registers for the gradient)
+//   warps 0-7  epilogue: TMEM -> registers, + bias, -> bf16, NHWC stores
+//   warp  8    TMEM allocation; lane 0 issues every tcgen05.mma and commit
+//   warp  9    lane 0 issues every TMA load
 //
 // Definitions followed: forward as teeny-kernels `conv2d_forward` (read
 // position oh*stride + kh*dil - pad, zero outside) with bias added once after
 // the reduction as in `conv2d_bias_forward`; gradient as the exact transpose
 // of teeny-kernels `conv2d_backward_dx` (scatter), evaluated per input
 // element as oarust `conv_2d_backward` dispatches it.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "problem.h"
 #include "ptx.cuh"
@@ -50,93 +57,111 @@ using bf16 = __nv_bfloat16;
 
 constexpr int kMaxPhases = 4;
 constexpr int kMaxTapsPerPhase = 32;
-constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarps = 4;
-constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kThreads = (kEpiWarps + 1 + kProdWarps) * 32;
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kKB = 64;  // channels per k-block: one 128-byte swizzled row
 
 struct Phase {
   int ntaps;
-  int R;       // output rows of the virtual grid per image
-  int RS;      // virtual rows per image (R plus the vertical reach of the taps)
-  int P;       // virtual grid pitch: valid columns plus the horizontal reach
-  int OWv;     // valid columns
-  int rmin, cmin;             // input coordinate of virtual (0, 0)
+  int R;        // output rows of the virtual grid (per image)
+  int P;        // virtual grid pitch: valid columns plus the horizontal reach
+  int OWv;      // valid columns
+  int rmin, cmin;                      // input coordinate of virtual (0, 0)
   int out_sh, out_sw, out_ph, out_pw;  // output pixel = (r*out_sh + out_ph, c*out_sw + out_pw)
-  int tiles;   // m-tiles of this phase
-  int item0;   // first work item of this phase
+  int bh;       // rows in one halo box
+  int a_bytes;  // bytes of one halo box (64 channels x P x bh)
+  int tiles;    // m-tiles per image
+  int item0;    // first work item of this phase
   int tap_off[kMaxTapsPerPhase];  // halo row offset of tap t
   int tap_w[kMaxTapsPerPhase];    // weight tap index kh*KW + kw
 };
 
 struct Args {
-  const bf16* in;     // gathered tensor, NHWC [N, Hi, Wi, Ck]: x (forward) or dy (gradient)
-  const bf16* w;      // weight, OHWI [C_out, KH, KW, C_in]
   const float* bias;  // [Cn] or null
   bf16* out;          // NHWC [N, Ho, Wo, Cn]: y or dx
   unsigned int* status;
-  int N, Hi, Wi, Ck;  // gathered side; Ck is the reduction channel count
-  int Cn;             // output channels (the GEMM N extent)
-  int Ho, Wo;
+  int N, Cn, Ho, Wo;
   int T;              // KH*KW
-  int Cw;             // innermost extent of the weight (the convolution's C_in)
-  int kbc, kb_count;  // channels per k-block and k-blocks per tap
+  int kb_count;       // 64-channel k-blocks of the reduction
   int n_tiles;
-  int halo, hp;       // halo rows of a tile, rows per halo slab (hp % 8 == 1)
-  int a_stage_bytes, b_tile_bytes, sa, sb;  // stage sizes and ring depths
+  int a_stage_bytes, b_tile_bytes, sa, sb;
   int nphase, total_items;
   Phase ph[kMaxPhases];
 };
 
-// B tile layout: [k chunk of 8][row group of 8][row % 8][16 bytes].
-template <bool DGRAD>
-struct BLayout {
-  static constexpr uint32_t sbo = DGRAD ? 144 : 128;  // padded for the transposed stores
-  __host__ __device__ static constexpr uint32_t lbo(int bn) { return uint32_t(bn / 8) * sbo + 16; }
+struct Maps {
+  CUtensorMap a[kMaxPhases];  // gathered activations, one box shape per phase
+  CUtensorMap b;              // weight viewed as [C_out][KH*KW][C_in]
 };
 
-__device__ __forceinline__ void decode_item(const Args& a, int item, int& phase, int& mtile, int& ntile) {
+struct Item {
+  int phase, n, m, ntile;
+};
+
+__device__ __forceinline__ Item decode_item(const Args& a, int item) {
   int p = 0;
   while (p + 1 < a.nphase && item >= a.ph[p + 1].item0) ++p;
-  phase = p;
-  const int local = item - a.ph[p].item0;
-  mtile = local / a.n_tiles;
-  ntile = local - mtile * a.n_tiles;
+  Item it;
+  it.phase = p;
+  int local = item - a.ph[p].item0;
+  it.ntile = local % a.n_tiles;
+  local /= a.n_tiles;
+  it.n = local / a.ph[p].tiles;
+  it.m = local - it.n * a.ph[p].tiles;
+  return it;
 }
 
-// 8x8 transpose of bf16: r[j] holds row j (8 values), out[i] receives column i.
-__device__ __forceinline__ void transpose8x8(const uint4 (&r)[8], uint4 (&o)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-    uint32_t c[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t v = (i >> 1) == 0 ? r[j].x : (i >> 1) == 1 ? r[j].y : (i >> 1) == 2 ? r[j].z : r[j].w;
-      c[j] = v;
-    }
-    o[i].x = __byte_perm(c[0], c[1], sel);
-    o[i].y = __byte_perm(c[2], c[3], sel);
-    o[i].z = __byte_perm(c[4], c[5], sel);
-    o[i].w = __byte_perm(c[6], c[7], sel);
-  }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+      "%6}], [%2];" ::"r"(dst),
+      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+// K-major operand, 128-byte swizzle, 8-row atoms of 1024 bytes.
+__device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) { return ptx::desc_kmajor_sw128(saddr); }
+
+// MN-major operand, 128-byte swizzle: `mn_stride` bytes between 64-element
+// atoms along N, 1024 bytes between 8-row atoms along K.
+__device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
 }
 
 template <int BN, int NSUB, bool DGRAD, bool BRES>
-__global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid_constant__ Args a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  using BL = BLayout<DGRAD>;
-  constexpr uint32_t kTmemCols = (2 * NSUB * BN) <= 32 ? 32 : (2 * NSUB * BN);
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BN);
-  const uint32_t lbo_b = BL::lbo(BN);
-  const int KC = a.kbc / 8;
+__global__ void __launch_bounds__(kThreads, 1)
+    implicit_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Swizzled TMA destinations and operands sit on 1024-byte boundaries.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kCols = 2 * NSUB * BN;
+  constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BN) | (DGRAD ? (1u << 16) : 0u);
+  constexpr int kBTile = BN * kKB * 2;
 
   uint8_t* a_base = smem;
   uint8_t* b_base = a_base + size_t(a.sa) * a.a_stage_bytes;
-  const int b_tiles = BRES ? a.T * a.kb_count : a.sb;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(b_base + size_t(b_tiles) * a.b_tile_bytes);
+  const int b_tiles = BRES ? a.T : a.sb;
+  float* bias_s = reinterpret_cast<float*>(b_base + size_t(b_tiles) * kBTile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bias_s + ((a.Cn + 1) & ~1));
   uint64_t* fullA = bars;
   uint64_t* emptyA = fullA + a.sa;
   uint64_t* fullB = emptyA + a.sa;
@@ -149,16 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.sa; ++i) { ptx::mbar_init(fullA + i, kProdThreads); ptx::mbar_init(emptyA + i, 1); }
-    for (int i = 0; i < a.sb; ++i) { ptx::mbar_init(fullB + i, kProdThreads); ptx::mbar_init(emptyB + i, 1); }
+    for (int i = 0; i < a.sa; ++i) { ptx::mbar_init(fullA + i, 1); ptx::mbar_init(emptyA + i, 1); }
+    for (int i = 0; i < a.sb; ++i) { ptx::mbar_init(fullB + i, 1); ptx::mbar_init(emptyB + i, 1); }
     for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, kEpiWarps * 32); }
-    ptx::mbar_init(bres, kProdThreads);
+    ptx::mbar_init(bres, 1);
     ptx::mbar_init(fin, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  if (warp < kEpiWarps)
+    for (int i = threadIdx.x; i < a.Cn; i += kEpiWarps * 32) bias_s[i] = a.bias ? a.bias[i] : 0.f;
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
@@ -168,143 +194,67 @@ __global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= kEpiWarps + 1) {
-    // ------------------------------------------------------------ producers
-    const int pt = threadIdx.x - (kEpiWarps + 1) * 32;
-    uint64_t* pending = nullptr;  // full barrier of the last committed, not yet signalled cp.async group
-    auto flush = [&]() {
-      if (pending) {
-        ptx::cp_async_wait_all();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(pending);
-        pending = nullptr;
-      }
-    };
-    auto push = [&](uint64_t* bar) {
-      ptx::cp_async_commit();
-      if (pending) {
-        ptx::cp_async_wait_group<1>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(pending);
-      }
-      pending = bar;
-    };
-    auto wait_empty = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-      flush();
-      return ptx::mbar_wait(bar, parity, abort_flag, a.status, 1u);
-    };
-    // Forward weight tile: rows = output channels n0.., K = input channels of k-block kb, tap wt.
-    auto fill_b_fwd = [&](uint8_t* tile, int wt, int kb, int n0) {
-      const uint32_t dst0 = ptx::smem_addr(tile);
-      for (int c = pt; c < BN * KC; c += kProdThreads) {
-        const int kc = c % KC, row = c / KC;
-        const bf16* src = a.w + (size_t(n0 + row) * a.T + wt) * a.Cw + kb * a.kbc + kc * 8;
-        ptx::cp_async_16(dst0 + kc * lbo_b + (row >> 3) * BL::sbo + (row & 7) * 16, src, 16);
-      }
-    };
-    // Gradient weight tile: rows = input channels n0.., K = output channels of k-block kb, tap wt.
-    auto fill_b_dgrad = [&](uint8_t* tile, int wt, int kb, int n0) {
-      const uint32_t dst0 = ptx::smem_addr(tile);
-      const int rbs = BN / 8;
-      for (int u = pt; u < rbs * KC; u += kProdThreads) {
-        const int rb = u % rbs, kc = u / rbs;
-        uint4 r[8], o[8];
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int p = 0; p < a.nphase; ++p) ptx::prefetch_tmap(&maps.a[p]);
+      ptx::prefetch_tmap(&maps.b);
+      auto load_b = [&](uint8_t* dst, uint64_t* bar, int wt, int kb, int n0) {
+        const uint32_t d = ptx::smem_addr(dst);
+        if (DGRAD) {  // MN-major: 64 input channels x 64 output channels per box
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int co = kb * a.kbc + kc * 8 + j;
-          r[j] = __ldg(reinterpret_cast<const uint4*>(a.w + (size_t(co) * a.T + wt) * a.Cw + n0 + rb * 8));
+          for (int h = 0; h < BN / 64; ++h) tma_load_3d(d + h * 8192, &maps.b, bar, n0 + h * 64, wt, kb * kKB);
+        } else {      // K-major: BN output channels x 64 input channels
+          tma_load_3d(d, &maps.b, bar, kb * kKB, wt, n0);
         }
-        transpose8x8(r, o);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t d = dst0 + kc * lbo_b + rb * BL::sbo + i * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(o[i].x), "r"(o[i].y), "r"(o[i].z),
-                       "r"(o[i].w)
-                       : "memory");
-        }
+      };
+      bool ok = true;
+      if (BRES) {
+        ptx::mbar_arrive_expect_tx(bres, uint32_t(a.T) * kBTile);
+        for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(wt) * kBTile, bres, wt, 0, 0);
       }
-    };
-
-    bool ok = true;
-    if (BRES) {  // the whole weight stays resident; only one n-tile exists in this mode
-      for (int wt = 0; wt < a.T; ++wt)
-        for (int kb = 0; kb < a.kb_count; ++kb) fill_b_fwd(b_base + size_t(wt * a.kb_count + kb) * a.b_tile_bytes, wt, kb, 0);
-      ptx::cp_async_commit();
-      ptx::cp_async_wait_all();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bres);
-    }
-    int sa = 0, sb = 0;
-    uint32_t pa = 0, pb = 0;
-    const int hs = kProdThreads / KC;  // halo rows advanced per pass of the producer threads
-    for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
-      int phase, mtile, ntile;
-      decode_item(a, item, phase, mtile, ntile);
-      const Phase& ph = a.ph[phase];
-      if (ph.ntaps == 0) continue;
-      const int q0 = mtile * 128 * NSUB;
-      const int n0 = ntile * BN;
-      const int img = ph.RS * ph.P;
-      for (int kb = 0; ok && kb < a.kb_count; ++kb) {
-        if (!(ok = wait_empty(emptyA + sa, pa ^ 1))) break;
-        {
-          const uint32_t dst0 = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
-          const int kc = pt % KC;
-          int h = pt / KC;
-          int q = q0 + h;
-          int n = q / img, rem = q - n * img;
-          int r = rem / ph.P, col = rem - r * ph.P;
-          const bf16* chan = a.in + kb * a.kbc + kc * 8;
-          for (; h < a.halo; h += hs) {
-            const int ih = r + ph.rmin, iw = col + ph.cmin;
-            const bool valid = n < a.N && ih >= 0 && ih < a.Hi && iw >= 0 && iw < a.Wi;
-            const bf16* src = valid ? chan + (size_t(n * a.Hi + ih) * a.Wi + iw) * a.Ck : a.in;
-            ptx::cp_async_16(dst0 + kc * (a.hp * 16) + h * 16, src, valid ? 16u : 0u);
-            col += hs;
-            while (col >= ph.P) {
-              col -= ph.P;
-              if (++r == ph.RS) { r = 0; ++n; }
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+        const Item it = decode_item(a, item);
+        const Phase& ph = a.ph[it.phase];
+        if (ph.ntaps == 0) continue;
+        const int ra = (it.m * 128 * NSUB) / ph.P;
+        for (int kb = 0; ok && kb < a.kb_count; ++kb) {
+          if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
+          ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
+          tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                      kb * kKB, ph.cmin, ra + ph.rmin, it.n);
+          if (++sa == a.sa) { sa = 0; pa ^= 1; }
+          if (!BRES) {
+            for (int t = 0; ok && t < ph.ntaps; ++t) {
+              if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
+              ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
+              load_b(b_base + size_t(sb) * kBTile, fullB + sb, ph.tap_w[t], kb, it.ntile * BN);
+              if (++sb == a.sb) { sb = 0; pb ^= 1; }
             }
-          }
-        }
-        push(fullA + sa);
-        if (++sa == a.sa) { sa = 0; pa ^= 1; }
-        if (!BRES) {
-          for (int t = 0; ok && t < ph.ntaps; ++t) {
-            if (!(ok = wait_empty(emptyB + sb, pb ^ 1))) break;
-            uint8_t* tile = b_base + size_t(sb) * a.b_tile_bytes;
-            if (DGRAD) {
-              fill_b_dgrad(tile, ph.tap_w[t], kb, n0);
-              ptx::fence_proxy_async_smem();
-              ptx::mbar_arrive(fullB + sb);
-            } else {
-              fill_b_fwd(tile, ph.tap_w[t], kb, n0);
-              push(fullB + sb);
-            }
-            if (++sb == a.sb) { sb = 0; pb ^= 1; }
           }
         }
       }
     }
-    flush();
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
       if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, a.status, 2u);
-      int sa = 0, sb = 0, it = 0;
+      int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
-      const uint32_t a_lbo = uint32_t(a.hp) * 16;
-      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x, ++it) {
-        int phase, mtile, ntile;
-        decode_item(a, item, phase, mtile, ntile);
-        const Phase& ph = a.ph[phase];
-        const int buf = it & 1;
-        if (!(ok = ptx::mbar_wait(tempty + buf, ((it >> 1) & 1) ^ 1, abort_flag, a.status, 2u))) break;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x, ++iter) {
+        const Item it = decode_item(a, item);
+        const Phase& ph = a.ph[it.phase];
+        const int buf = iter & 1;
+        if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, a.status, 2u))) break;
         ptx::tc_fence_after();
         const uint32_t acc = tmem + uint32_t(buf * NSUB * BN);
         if (ph.ntaps > 0) {
+          const int q0 = it.m * 128 * NSUB;
+          const int row0 = q0 - (q0 / ph.P) * ph.P;  // tile start inside the halo block
           for (int kb = 0; ok && kb < a.kb_count; ++kb) {
             if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
             ptx::tc_fence_after();
@@ -312,21 +262,21 @@ __global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid
             for (int t = 0; t < ph.ntaps; ++t) {
               uint32_t b_addr;
               if (BRES) {
-                b_addr = ptx::smem_addr(b_base + size_t(ph.tap_w[t] * a.kb_count + kb) * a.b_tile_bytes);
+                b_addr = ptx::smem_addr(b_base + size_t(ph.tap_w[t]) * kBTile);
               } else {
                 if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
                 ptx::tc_fence_after();
-                b_addr = ptx::smem_addr(b_base + size_t(sb) * a.b_tile_bytes);
+                b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
               }
-              for (int j = 0; j < a.kbc / 16; ++j) {
-                const uint64_t bdesc = ptx::desc_kmajor_noswizzle(b_addr + 2 * j * lbo_b, lbo_b, BL::sbo);
+              const uint32_t arow = a_addr + uint32_t(row0 + ph.tap_off[t]) * 128;
 #pragma unroll
-                for (int s = 0; s < NSUB; ++s) {
-                  const uint32_t arow = uint32_t(s * 128 + ph.tap_off[t]);
-                  const uint64_t adesc =
-                      ptx::desc_kmajor_noswizzle(a_addr + 2 * j * a_lbo + arow * 16, a_lbo, 128);
-                  ptx::mma_bf16(acc + s * BN, adesc, bdesc, kIdesc, (kb | t | j) != 0);
-                }
+              for (int j = 0; j < kKB / 16; ++j) {
+                const uint64_t bdesc = DGRAD ? desc_sw128_mnmajor(b_addr + j * 2048, 8192)
+                                             : desc_sw128_kmajor(b_addr + j * 32);
+#pragma unroll
+                for (int s = 0; s < NSUB; ++s)
+                  ptx::mma_bf16(acc + s * BN, desc_sw128_kmajor(arow + s * 128 * 128 + j * 32), bdesc, kIdesc,
+                                (kb | t | j) != 0);
               }
               if (!BRES) {
                 ptx::mma_commit(emptyB + sb);
@@ -345,49 +295,44 @@ __global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    int it = 0;
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++it) {
-      int phase, mtile, ntile;
-      decode_item(a, item, phase, mtile, ntile);
-      const Phase& ph = a.ph[phase];
-      const int buf = it & 1;
-      if (!ptx::mbar_wait(tfull + buf, (it >> 1) & 1, abort_flag, a.status, 4u)) break;
+    const int quad = warp & 3, half = warp >> 2;
+    const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    int iter = 0;
+    for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
+      const Item it = decode_item(a, item);
+      const Phase& ph = a.ph[it.phase];
+      const int buf = iter & 1;
+      if (!ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u)) break;
       ptx::tc_fence_after();
-      const int n0 = ntile * BN;
-      const int img = ph.RS * ph.P;
+      const int n0 = it.ntile * BN;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
-        const int q = mtile * 128 * NSUB + s * 128 + warp * 32 + lane;
-        const int n = q / img, rem = q - n * img;
-        const int r = rem / ph.P, col = rem - r * ph.P;
-        const bool valid = n < a.N && r < ph.R && col < ph.OWv;
-        bf16* dst = a.out + (size_t(n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + col * ph.out_sw + ph.out_pw) *
-                                a.Cn + n0;
+        const int q = it.m * 128 * NSUB + s * 128 + quad * 32 + lane;
+        const int r = q / ph.P, col = q - r * ph.P;
+        const bool valid = r < ph.R && col < ph.OWv;
+        bf16* dst = a.out + (size_t(it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + col * ph.out_sw + ph.out_pw) *
+                                a.Cn;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           uint32_t v[32];
           if (ph.ntaps > 0) {
-            ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + c * 32), v);
+            ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + c), v);
             ptx::tmem_ld_wait();
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0u;
           }
-          if (valid) {
+          const int co = n0 + c;
+          if (valid && co < a.Cn) {
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
-              if (a.bias) {
-                lo += __ldg(a.bias + n0 + c * 32 + 2 * j);
-                hi += __ldg(a.bias + n0 + c * 32 + 2 * j + 1);
-              }
-              pk[j] = ptx::pack_bf16x2(lo, hi);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            for (int j = 0; j < 16; ++j)
+              pk[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) + bias_s[min(co + 2 * j, a.Cn - 1)],
+                                       __uint_as_float(v[2 * j + 1]) + bias_s[min(co + 2 * j + 1, a.Cn - 1)]);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + co);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int g = 0; g < 4; ++g)
+              if (co + 8 * g < a.Cn) d4[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
           }
         }
       }
@@ -406,40 +351,157 @@ __global__ void __launch_bounds__(kThreads, 1) implicit_gemm_kernel(const __grid
 
 struct Plan {
   Args a;
+  Maps maps;
   int bn, nsub;
-  bool bres;
+  bool bres, dgrad;
   size_t smem;
   int grid;
+  // geometry kept for the tensor maps
+  int N, Hi, Wi, Ck, Cw;
 };
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int floordiv(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
 int pick_bn(int64_t cn) {
-  for (int bn : {256, 128, 64, 32})
-    if (cn % bn == 0) return bn;
-  return 0;
+  int best = 0, best_cols = 0;
+  for (int bn : {256, 192, 128, 64}) {
+    const int64_t cols = ((cn + bn - 1) / bn) * bn;
+    if (!best || cols < best_cols) { best = bn; best_cols = int(cols); }
+  }
+  return best;
 }
 
-int pick_kbc(int64_t ck) {
-  for (int k : {64, 32, 16})
-    if (ck % k == 0) return k;
-  return 0;
+struct PhaseSpec {
+  Phase ph;
+  int maxoff;
+};
+
+// Fills the per-phase box geometry and counts for a tile of 128*nsub positions.
+bool finish_phase(PhaseSpec& s, int nsub, int N) {
+  Phase& ph = s.ph;
+  const int mt = 128 * nsub;
+  ph.bh = (ph.P - 1 + mt + s.maxoff + ph.P - 1) / ph.P;
+  if (ph.P > 256 || ph.bh > 256) return false;  // TMA box extent limit
+  ph.a_bytes = 128 * ph.P * ph.bh;
+  const int64_t per_img = int64_t(ph.R) * ph.P;
+  ph.tiles = int((per_img + mt - 1) / mt);
+  return int64_t(N) * ph.tiles < (int64_t(1) << 30);
 }
 
-int floordiv(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
-
-// Fills the stage sizes and checks the shared-memory budget.
-bool size_plan(Plan& pl, bool dgrad, int maxoff) {
+bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
+  if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
+  if (!dgrad && (p.SH != 1 || p.SW != 1)) return false;
+  if (dgrad && p.SH * p.SW > kMaxPhases) return false;
+  if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides and vector stores
+  if (p.KH * p.KW > kMaxTapsPerPhase) return false;
+  pl = Plan{};
+  pl.dgrad = dgrad;
   Args& a = pl.a;
-  const int KC = a.kbc / 8;
-  a.halo = 128 * pl.nsub + maxoff;
-  a.hp = a.halo + ((1 - a.halo % 8) + 8) % 8;  // hp % 8 == 1 keeps the 8 chunk slabs on distinct banks
-  a.a_stage_bytes = KC * a.hp * 16;
-  const uint32_t sbo = dgrad ? 144 : 128;
-  a.b_tile_bytes = KC * int((pl.bn / 8) * sbo + 16);
-  const int bars = 8 * (2 * 8 + 2 * 8 + 4 + 2) + 16;
-  for (int sa = 4; sa >= 2; --sa) {
-    for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 2); --sb) {
-      const size_t b_bytes = size_t(pl.bres ? a.T * a.kb_count : sb) * a.b_tile_bytes;
-      const size_t total = size_t(sa) * a.a_stage_bytes + b_bytes + bars;
+  const int64_t Ck = dgrad ? p.Cout : p.Cin, Cn = dgrad ? p.Cin : p.Cout;
+  pl.bn = pick_bn(Cn);
+  pl.nsub = pl.bn <= 128 ? 2 : 1;
+  a.N = int(p.N);
+  a.Cn = int(Cn);
+  a.Ho = int(p.H);
+  a.Wo = int(p.W);
+  if (!dgrad) { a.Ho = int(p.OH); a.Wo = int(p.OW); }
+  a.T = int(p.KH * p.KW);
+  a.kb_count = int((Ck + kKB - 1) / kKB);
+  a.n_tiles = int((Cn + pl.bn - 1) / pl.bn);
+  pl.N = int(p.N);
+  pl.Hi = int(dgrad ? p.OH : p.H);
+  pl.Wi = int(dgrad ? p.OW : p.W);
+  pl.Ck = int(Ck);
+  pl.Cw = int(p.Cin);
+
+  PhaseSpec specs[kMaxPhases];
+  int nph = 0;
+  if (!dgrad) {
+    PhaseSpec s{};
+    Phase& ph = s.ph;
+    const int rmin = -int(p.PH), rmax = int((p.KH - 1) * p.DH - p.PH);
+    const int cmin = -int(p.PW), cmax = int((p.KW - 1) * p.DW - p.PW);
+    ph.ntaps = a.T;
+    ph.R = int(p.OH); ph.OWv = int(p.OW);
+    ph.P = int(p.OW) + (cmax - cmin);
+    ph.rmin = rmin; ph.cmin = cmin;
+    ph.out_sh = 1; ph.out_sw = 1;
+    for (int kh = 0; kh < p.KH; ++kh)
+      for (int kw = 0; kw < p.KW; ++kw) {
+        const int t = int(kh * p.KW + kw);
+        ph.tap_off[t] = (int(kh * p.DH - p.PH) - rmin) * ph.P + (int(kw * p.DW - p.PW) - cmin);
+        ph.tap_w[t] = t;
+      }
+    s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+    specs[nph++] = s;
+  } else {
+    for (int ah = 0; ah < p.SH; ++ah)
+      for (int aw = 0; aw < p.SW; ++aw) {
+        PhaseSpec s{};
+        Phase& ph = s.ph;
+        ph.R = int((p.H - ah + p.SH - 1) / p.SH);
+        ph.OWv = int((p.W - aw + p.SW - 1) / p.SW);
+        if (ph.R <= 0 || ph.OWv <= 0) continue;
+        int khs[kMaxTapsPerPhase], drs[kMaxTapsPerPhase], nkh = 0;
+        int kws[kMaxTapsPerPhase], dcs[kMaxTapsPerPhase], nkw = 0;
+        for (int kh = 0; kh < p.KH; ++kh) {
+          const int num = int(ah + p.PH - kh * p.DH);
+          if (((num % p.SH) + p.SH) % p.SH == 0) { khs[nkh] = kh; drs[nkh] = floordiv(num, int(p.SH)); ++nkh; }
+        }
+        for (int kw = 0; kw < p.KW; ++kw) {
+          const int num = int(aw + p.PW - kw * p.DW);
+          if (((num % p.SW) + p.SW) % p.SW == 0) { kws[nkw] = kw; dcs[nkw] = floordiv(num, int(p.SW)); ++nkw; }
+        }
+        int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
+        for (int i = 0; i < nkh; ++i) { rmin = i ? std::min(rmin, drs[i]) : drs[i]; rmax = i ? std::max(rmax, drs[i]) : drs[i]; }
+        for (int i = 0; i < nkw; ++i) { cmin = i ? std::min(cmin, dcs[i]) : dcs[i]; cmax = i ? std::max(cmax, dcs[i]) : dcs[i]; }
+        ph.ntaps = nkh * nkw;
+        ph.P = ph.OWv + (cmax - cmin);
+        ph.rmin = rmin; ph.cmin = cmin;
+        ph.out_sh = int(p.SH); ph.out_sw = int(p.SW); ph.out_ph = ah; ph.out_pw = aw;
+        for (int i = 0; i < nkh; ++i)
+          for (int j = 0; j < nkw; ++j) {
+            const int t = i * nkw + j;
+            ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
+            ph.tap_w[t] = int(khs[i] * p.KW + kws[j]);
+          }
+        s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+        specs[nph++] = s;
+      }
+    // Longest phases first, so the persistent CTAs finish together.
+    std::stable_sort(specs, specs + nph, [](const PhaseSpec& x, const PhaseSpec& y) { return x.ph.ntaps > y.ph.ntaps; });
+  }
+  if (nph == 0) return false;
+  int item = 0, a_max = 0;
+  for (int i = 0; i < nph; ++i) {
+    if (!finish_phase(specs[i], pl.nsub, a.N)) return false;
+    specs[i].ph.item0 = item;
+    item += a.N * specs[i].ph.tiles * a.n_tiles;
+    a.ph[i] = specs[i].ph;
+    a_max = std::max(a_max, specs[i].ph.a_bytes);
+  }
+  a.nphase = nph;
+  a.total_items = item;
+  a.a_stage_bytes = (a_max + 1023) & ~1023;
+  a.b_tile_bytes = pl.bn * kKB * 2;
+  pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
+  const size_t fixed = 1024 + size_t(a.Cn + 2) * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
+  for (int sa = 3; sa >= 2; --sa) {
+    for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
+      const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
       if (total <= size_t(kSmemLimit)) {
         a.sa = sa;
         a.sb = pl.bres ? 1 : sb;
@@ -451,193 +513,97 @@ bool size_plan(Plan& pl, bool dgrad, int maxoff) {
   return false;
 }
 
-// Forward at unit stride: one phase, taps at (kh*dh - ph, kw*dw - pw).
-bool plan_fwd(const Problem& p, Plan& pl) {
-  if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1 && p.SH == 1 && p.SW == 1)) return false;
-  if (p.Cin % 16 != 0 || p.KH * p.KW > kMaxTapsPerPhase) return false;
-  const int bn = pick_bn(p.Cout), kbc = pick_kbc(p.Cin);
-  if (!bn || !kbc) return false;
-  Args& a = pl.a;
-  a = Args{};
-  a.N = int(p.N); a.Hi = int(p.H); a.Wi = int(p.W); a.Ck = int(p.Cin);
-  a.Cn = int(p.Cout); a.Ho = int(p.OH); a.Wo = int(p.OW);
-  a.T = int(p.KH * p.KW); a.Cw = int(p.Cin);
-  a.kbc = kbc; a.kb_count = int(p.Cin / kbc);
-  a.n_tiles = int(p.Cout / bn);
-  pl.bn = bn;
-  pl.nsub = bn == 256 ? 1 : 2;
-  Phase& ph = a.ph[0];
-  ph = Phase{};
-  const int rmin = -int(p.PH), rmax = int((p.KH - 1) * p.DH - p.PH);
-  const int cmin = -int(p.PW), cmax = int((p.KW - 1) * p.DW - p.PW);
-  ph.ntaps = a.T;
-  ph.R = int(p.OH); ph.OWv = int(p.OW);
-  ph.P = int(p.OW) + (cmax - cmin);
-  ph.RS = int(p.OH) + (rmax - rmin);
-  ph.rmin = rmin; ph.cmin = cmin;
-  ph.out_sh = 1; ph.out_sw = 1; ph.out_ph = 0; ph.out_pw = 0;
-  for (int kh = 0; kh < p.KH; ++kh)
-    for (int kw = 0; kw < p.KW; ++kw) {
-      const int t = int(kh * p.KW + kw);
-      ph.tap_off[t] = (int(kh * p.DH) - int(p.PH) - rmin) * ph.P + (int(kw * p.DW) - int(p.PW) - cmin);
-      ph.tap_w[t] = t;
-    }
-  const int maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
-  const int64_t positions = int64_t(p.N) * ph.RS * ph.P;
-  if (positions + maxoff + 256 > 0x7FFFFFFF) return false;
-  ph.tiles = int((positions + 128 * pl.nsub - 1) / (128 * pl.nsub));
-  ph.item0 = 0;
-  a.nphase = 1;
-  a.total_items = ph.tiles * a.n_tiles;
-  pl.bres = a.n_tiles == 1 && size_t(a.T) * a.kb_count * (size_t(a.kbc / 8) * (bn / 8 * 128 + 16)) <= 110 * 1024;
-  if (!size_plan(pl, false, maxoff)) {
-    pl.bres = false;
-    if (!size_plan(pl, false, maxoff)) return false;
+bool encode_maps(Plan& pl, const void* in, const void* w) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const Args& a = pl.a;
+  for (int i = 0; i < a.nphase; ++i) {
+    const Phase& ph = a.ph[i];
+    cuuint64_t dims[4] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N)};
+    cuuint64_t strides[3] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Wi) * pl.Ck * 2, cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2};
+    cuuint32_t box[4] = {cuuint32_t(kKB), cuuint32_t(ph.P), cuuint32_t(ph.bh), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fn(&pl.maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(in), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
   }
-  return true;
-}
-
-// Gradient: one phase per (ih % s_h, iw % s_w); each tap that reaches the
-// phase does so at row shift (a + p_h - kh*d_h) / s_h of dy (exact division).
-bool plan_dgrad(const Problem& p, Plan& pl) {
-  if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
-  if (p.SH * p.SW > kMaxPhases || p.Cout % 16 != 0) return false;
-  const int bn = pick_bn(p.Cin), kbc = pick_kbc(p.Cout);
-  if (!bn || !kbc) return false;
-  Args& a = pl.a;
-  a = Args{};
-  a.N = int(p.N); a.Hi = int(p.OH); a.Wi = int(p.OW); a.Ck = int(p.Cout);
-  a.Cn = int(p.Cin); a.Ho = int(p.H); a.Wo = int(p.W);
-  a.T = int(p.KH * p.KW); a.Cw = int(p.Cin);
-  a.kbc = kbc; a.kb_count = int(p.Cout / kbc);
-  a.n_tiles = int(p.Cin / bn);
-  pl.bn = bn;
-  pl.nsub = bn == 256 ? 1 : 2;
-  pl.bres = false;
-  Phase phs[kMaxPhases];
-  int nph = 0, maxoff = 0;
-  for (int ah = 0; ah < p.SH; ++ah)
-    for (int aw = 0; aw < p.SW; ++aw) {
-      Phase ph{};
-      const int R = int((p.H - ah + p.SH - 1) / p.SH), OWv = int((p.W - aw + p.SW - 1) / p.SW);
-      if (R <= 0 || OWv <= 0) continue;
-      int khs[64], drs[64], nkh = 0, kws[64], dcs[64], nkw = 0;
-      for (int kh = 0; kh < p.KH; ++kh) {
-        const int num = int(ah + p.PH - kh * p.DH);
-        if (((num % p.SH) + p.SH) % p.SH == 0 && nkh < 64) { khs[nkh] = kh; drs[nkh] = floordiv(num, int(p.SH)); ++nkh; }
-      }
-      for (int kw = 0; kw < p.KW; ++kw) {
-        const int num = int(aw + p.PW - kw * p.DW);
-        if (((num % p.SW) + p.SW) % p.SW == 0 && nkw < 64) { kws[nkw] = kw; dcs[nkw] = floordiv(num, int(p.SW)); ++nkw; }
-      }
-      if (nkh * nkw > kMaxTapsPerPhase) return false;
-      int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
-      for (int i = 0; i < nkh; ++i) { rmin = i ? std::min(rmin, drs[i]) : drs[i]; rmax = i ? std::max(rmax, drs[i]) : drs[i]; }
-      for (int i = 0; i < nkw; ++i) { cmin = i ? std::min(cmin, dcs[i]) : dcs[i]; cmax = i ? std::max(cmax, dcs[i]) : dcs[i]; }
-      ph.ntaps = nkh * nkw;
-      ph.R = R; ph.OWv = OWv;
-      ph.P = OWv + (cmax - cmin);
-      ph.RS = R + (rmax - rmin);
-      ph.rmin = rmin; ph.cmin = cmin;
-      ph.out_sh = int(p.SH); ph.out_sw = int(p.SW); ph.out_ph = ah; ph.out_pw = aw;
-      for (int i = 0; i < nkh; ++i)
-        for (int j = 0; j < nkw; ++j) {
-          const int t = i * nkw + j;
-          ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
-          ph.tap_w[t] = int(khs[i] * p.KW + kws[j]);
-        }
-      const int off = (rmax - rmin) * ph.P + (cmax - cmin);
-      maxoff = std::max(maxoff, off);
-      const int64_t positions = int64_t(p.N) * ph.RS * ph.P;
-      if (positions + off + 256 > 0x7FFFFFFF) return false;
-      ph.tiles = int((positions + 128 * pl.nsub - 1) / (128 * pl.nsub));
-      phs[nph++] = ph;
-    }
-  // Longest phases first, so the persistent CTAs finish together.
-  std::stable_sort(phs, phs + nph, [](const Phase& x, const Phase& y) { return x.ntaps > y.ntaps; });
-  int item = 0;
-  for (int i = 0; i < nph; ++i) {
-    phs[i].item0 = item;
-    item += phs[i].tiles * a.n_tiles;
-    a.ph[i] = phs[i];
-  }
-  a.nphase = nph;
-  a.total_items = item;
-  return nph > 0 && size_plan(pl, true, maxoff);
+  const int Cout = pl.dgrad ? pl.Ck : a.Cn;
+  cuuint64_t dims[3] = {cuuint64_t(pl.Cw), cuuint64_t(a.T), cuuint64_t(Cout)};
+  cuuint64_t strides[2] = {cuuint64_t(pl.Cw) * 2, cuuint64_t(a.T) * pl.Cw * 2};
+  cuuint32_t box[3] = {cuuint32_t(kKB), 1, cuuint32_t(pl.dgrad ? kKB : pl.bn)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(&pl.maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int NSUB, bool DGRAD, bool BRES>
 gbconv_status run(const Plan& pl, const Launch& l) {
   auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES>;
-  // The shared-memory opt-in is a per-device function attribute: set it once per device and size.
+  // The shared-memory opt-in is a per-device function attribute: raise it once per device.
   static std::atomic<uint64_t> done[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
   if (done[dev].load(std::memory_order_acquire) < uint64_t(pl.smem)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemLimit)) != cudaSuccess)
       return GBCONV_ECUDA;
-    done[dev].store(uint64_t(pl.smem), std::memory_order_release);
+    done[dev].store(uint64_t(kSmemLimit), std::memory_order_release);
   }
-  kern<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(l.stream)>>>(pl.a);
+  kern<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(l.stream)>>>(pl.maps, pl.a);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
 template <bool DGRAD>
 gbconv_status dispatch(const Plan& pl, const Launch& l) {
-  if (pl.bres) {
-    if constexpr (!DGRAD) {
-      switch (pl.bn) {
-        case 256: return run<256, 1, false, true>(pl, l);
-        case 128: return run<128, 2, false, true>(pl, l);
-        case 64: return run<64, 2, false, true>(pl, l);
-        default: return run<32, 2, false, true>(pl, l);
-      }
+  if (!DGRAD && pl.bres) {
+    switch (pl.bn) {
+      case 256: return run<256, 1, false, true>(pl, l);
+      case 192: return run<192, 1, false, true>(pl, l);
+      case 128: return run<128, 2, false, true>(pl, l);
+      default: return run<64, 2, false, true>(pl, l);
     }
-    return GBCONV_EUNSUPPORTED;
   }
   switch (pl.bn) {
     case 256: return run<256, 1, DGRAD, false>(pl, l);
+    case 192: return run<192, 1, DGRAD, false>(pl, l);
     case 128: return run<128, 2, DGRAD, false>(pl, l);
-    case 64: return run<64, 2, DGRAD, false>(pl, l);
-    default: return run<32, 2, DGRAD, false>(pl, l);
+    default: return run<64, 2, DGRAD, false>(pl, l);
   }
 }
 
-void finish_plan(Plan& pl, const void* in, const void* w, const float* bias, void* out, const Launch& l) {
-  pl.a.in = static_cast<const bf16*>(in);
-  pl.a.w = static_cast<const bf16*>(w);
+gbconv_status launch(const Problem& p, bool dgrad, const void* in, const void* w, const float* bias, void* out,
+                     const Launch& l) {
+  Plan pl;
+  if (!plan_geometry(p, dgrad, pl)) return GBCONV_EUNSUPPORTED;
   pl.a.bias = bias;
   pl.a.out = static_cast<bf16*>(out);
   pl.a.status = l.status;
   pl.grid = std::max(1, std::min(pl.a.total_items, l.num_sms));
+  if (!encode_maps(pl, in, w)) return GBCONV_ECUDA;
+  return dgrad ? dispatch<true>(pl, l) : dispatch<false>(pl, l);
 }
 
 }  // namespace
 
 bool implicit_fwd_supported(const Problem& p) {
   Plan pl;
-  return plan_fwd(p, pl);
+  return plan_geometry(p, false, pl);
 }
 
 bool implicit_dgrad_supported(const Problem& p) {
   Plan pl;
-  return plan_dgrad(p, pl);
+  return plan_geometry(p, true, pl);
 }
 
 gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                   const Launch& l) {
-  Plan pl;
-  if (!plan_fwd(p, pl)) return GBCONV_EUNSUPPORTED;
-  finish_plan(pl, x, w, bias, y, l);
-  return dispatch<false>(pl, l);
+  return launch(p, false, x, w, bias, y, l);
 }
 
 gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
-  Plan pl;
-  if (!plan_dgrad(p, pl)) return GBCONV_EUNSUPPORTED;
-  finish_plan(pl, dy, w, nullptr, dx, l);
-  return dispatch<true>(pl, l);
+  return launch(p, true, dy, w, nullptr, dx, l);
 }
 
 }  // namespace gbconv

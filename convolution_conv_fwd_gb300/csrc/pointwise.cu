@@ -245,7 +245,7 @@ bool pointwise_supported(const Problem& p) {
   const int bn = pick_bn(p.Cout);
   if (!bn) return false;
   const int kb_count = int((p.Cin + kBK - 1) / kBK);
-  return stages_for(bn, kb_count) >= 3 && encode_fn() != nullptr;
+  return stages_for(bn, kb_count) >= 3;
 }
 
 gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,

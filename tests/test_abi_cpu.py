@@ -104,7 +104,7 @@ def test_status_strings(gb):
 
 EXPECTED_FAMILY = {
     "conv1d_ncl_f32": {"direct"},
-    "pointwise_1x1_nhwc_bf16": {"pointwise", "implicit"},  # pointwise needs the driver's TMA encoder
+    "pointwise_1x1_nhwc_bf16": {"pointwise"},
     "dense3x3_nhwc_bf16": {"implicit"},
     "depthwise3x3_s2_nhwc_bf16": {"depthwise"},
     "dgrad3x3_s2_nhwc_bf16": {"dgrad"},
@@ -124,4 +124,7 @@ def test_generic_families_for_other_layouts(gb):
     assert gb.gbconv_select(lib_desc(gb, shape_kw(groups=2)), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), c_in=32, c_out=32)), 1) == "dgrad"
-    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 1) == "direct_dgrad"  # C_in=16: no 32-wide N tile
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 1) == "dgrad"
+    # channel counts that are not a multiple of 8 break the 16-byte TMA row pitch
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 1) == "direct_dgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 0) == "direct"

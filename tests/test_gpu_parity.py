@@ -80,6 +80,9 @@ SMALL = [
     (shape_kw(n=2, in_size=(9, 9), c_in=64, c_out=96, k=(1, 1), pad=(0, 0)), "fwd", "implicit"),
     (shape_kw(spatial_dims=1, n=3, in_size=(37,), c_in=32, c_out=64, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="nlc", wlayout="oki", bias=True), "fwd", "implicit"),
+    # channel tails: 80 input channels (second 64-block zero-filled by TMA), 72 outputs (masked N columns)
+    (shape_kw(n=2, in_size=(7, 9), c_in=80, c_out=72, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(6, 7), c_in=64, c_out=192, bias=True), "fwd", "implicit"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(13, 13), c_in=72, c_out=128, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
@@ -95,6 +98,8 @@ SMALL = [
     (shape_kw(n=1, in_size=(8, 8), c_in=32, c_out=32, k=(1, 1), pad=(0, 0), stride=(2, 2)), "dgrad", "dgrad"),
     (shape_kw(n=1, in_size=(11, 9), c_in=64, c_out=32, k=(4, 4), stride=(2, 2), pad=(1, 1)), "dgrad", "dgrad"),
     (shape_kw(n=1, in_size=(7, 7), c_in=96, c_out=48, dil=(2, 2), pad=(1, 1)), "dgrad", "dgrad"),
+    (shape_kw(n=2, in_size=(9, 9), c_in=72, c_out=40, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(8, 6), c_in=192, c_out=64), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
