@@ -116,6 +116,87 @@ __global__ void __launch_bounds__(kThreads) depthwise_fwd_kernel(DwArgs a, const
   }
 }
 
+
+// 3x3, dilation 1, stride S in {1, 2}: the nine weights of the thread's 8
+// channels live in registers, and each input row a thread loads is kept in
+// registers for every output row of its strip that reads it (rows overlap by
+// 3 - S), so a strip of R output rows loads (R*S + 3 - S) input rows instead
+// of 3R.  No shared memory is touched in the loop.
+template <int S>
+__global__ void __launch_bounds__(kThreads, 2) depthwise3x3_kernel(DwArgs a, const __nv_bfloat16* __restrict__ x,
+                                                                  const __nv_bfloat16* __restrict__ w,
+                                                                  const float* __restrict__ bias,
+                                                                  __nv_bfloat16* __restrict__ y) {
+  constexpr int kKeep = 3 - S;  // input rows shared by consecutive output rows
+  const int cpb = a.cv_per_block * 8;
+  const int chunk = blockIdx.x % a.cv_chunks;
+  const int ow = (blockIdx.x / a.cv_chunks) * blockDim.y + threadIdx.y;
+  const int c = chunk * cpb + threadIdx.x * 8;
+  const int n = blockIdx.z;
+  if (ow >= a.OW) return;
+  float wr[9][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(c + j) * 9 + t]);
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = bias ? __ldg(bias + c + j) : 0.f;
+
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* yv = reinterpret_cast<uint4*>(y);
+  const int cvec = a.C / 8, cv = c >> 3;
+  int iw[3];
+  bool okw[3];
+#pragma unroll
+  for (int kw = 0; kw < 3; ++kw) {
+    iw[kw] = ow * S + kw - a.PW;
+    okw[kw] = iw[kw] >= 0 && iw[kw] < a.W;
+  }
+  auto load_row = [&](int ih, uint4 (&r)[3]) {
+    const bool okh = ih >= 0 && ih < a.H;
+#pragma unroll
+    for (int kw = 0; kw < 3; ++kw)
+      r[kw] = (okh && okw[kw]) ? __ldg(xv + (size_t(n * a.H + ih) * a.W + iw[kw]) * cvec + cv) : make_uint4(0, 0, 0, 0);
+  };
+  const int oh0 = blockIdx.y * a.rows_per_thread;
+  const int oh1 = min(a.OH, oh0 + a.rows_per_thread);
+  uint4 keep[kKeep][3];
+#pragma unroll
+  for (int k = 0; k < kKeep; ++k) load_row(oh0 * S - a.PH + k, keep[k]);
+  for (int oh = oh0; oh < oh1; ++oh) {
+    uint4 rows[3][3];
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k)
+#pragma unroll
+      for (int kw = 0; kw < 3; ++kw) rows[k][kw] = keep[k][kw];
+#pragma unroll
+    for (int k = kKeep; k < 3; ++k) load_row(oh * S - a.PH + k, rows[k]);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = b[j];
+#pragma unroll
+    for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+      for (int kw = 0; kw < 3; ++kw) {
+        float xf[8];
+        unpack8(rows[kh][kw], xf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(xf[j], wr[kh * 3 + kw][j], acc[j]);
+      }
+    uint4 o;
+    o.x = pack2(acc[0], acc[1]);
+    o.y = pack2(acc[2], acc[3]);
+    o.z = pack2(acc[4], acc[5]);
+    o.w = pack2(acc[6], acc[7]);
+    yv[(size_t(n * a.OH + oh) * a.OW + ow) * cvec + cv] = o;
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k)
+#pragma unroll
+      for (int kw = 0; kw < 3; ++kw) keep[k][kw] = rows[3 - kKeep + k][kw];
+  }
+}
+
 }  // namespace
 
 bool depthwise_supported(const Problem& p) {
@@ -146,10 +227,18 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
   auto xb = static_cast<const __nv_bfloat16*>(x);
   auto wb = static_cast<const __nv_bfloat16*>(w);
   auto yb = static_cast<__nv_bfloat16*>(y);
-  if (p.KH == 3 && p.KW == 3)
+  if (p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2)) {
+    a.rows_per_thread = 8;
+    grid.y = unsigned((p.OH + a.rows_per_thread - 1) / a.rows_per_thread);
+    if (p.SH == 1)
+      depthwise3x3_kernel<1><<<grid, block, 0, s>>>(a, xb, wb, bias, yb);
+    else
+      depthwise3x3_kernel<2><<<grid, block, 0, s>>>(a, xb, wb, bias, yb);
+  } else if (p.KH == 3 && p.KW == 3) {
     depthwise_fwd_kernel<3, 3><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
-  else
+  } else {
     depthwise_fwd_kernel<0, 0><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
+  }
   note_launch();
   return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
