@@ -176,7 +176,7 @@ def run_gpu(args, rank, world, local_rank):
         # Write a buffer twice the size of L2, then read another one: L2 ends up holding only clean lines
         # of the read buffer, so no write-back of the flush lands inside the next timed kernel.
         flush.zero_()
-        torch.sum(flush_read, dtype=torch.float32, out=flush_sink)
+        torch.sum(flush_read, dim=0, out=flush_sink)
 
     cases = []
     for wl in WORKLOADS:
