@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_base = smem;
   uint8_t* b_base = a_base + size_t(a.sa) * a.a_stage_bytes;
   const int b_tiles = BRES ? a.T : a.sb;
-  float* bias_s = reinterpret_cast<float*>(b_base + size_t(b_tiles) * kBTile);
+  uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;  // 128 rows x (staging group * 2 + 16) bytes
+  float* bias_s = reinterpret_cast<float*>(stage_base + 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16));
   uint64_t* bars = reinterpret_cast<uint64_t*>(bias_s + ((a.Cn + 1) & ~1));
   uint64_t* fullA = bars;
   uint64_t* emptyA = fullA + a.sa;
@@ -295,8 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Warps w and w+4 share TMEM lanes 32*(w%4).. (32 positions) and split the
+    // columns of each 128-column group.  Each converts its accumulators to
+    // bf16 into a padded shared-memory staging block; then the pair stores the
+    // 32 rows so that consecutive threads write consecutive 16-byte pieces of
+    // the same output pixel (whole pixels per warp instruction).
+    constexpr int kG = BN % 128 == 0 ? 128 : 64;  // columns per staging group
+    constexpr int kPitch = kG * 2 + 16;         // padded row pitch of the staging block, bytes
+    constexpr int kParts = kG / 8;              // 16-byte pieces per staged row
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    uint8_t* stage = stage_base + quad * 32 * kPitch;
+    const uint32_t stage_s = ptx::smem_addr(stage);
+    const int tp = half * 32 + lane;            // thread index within the pair
     int iter = 0;
     for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
       const Item it = decode_item(a, item);
@@ -307,33 +319,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = it.ntile * BN;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
-        const int q = it.m * 128 * NSUB + s * 128 + quad * 32 + lane;
-        const int r = q / ph.P, col = q - r * ph.P;
-        const bool valid = r < ph.R && col < ph.OWv;
-        bf16* dst = a.out + (size_t(it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + col * ph.out_sw + ph.out_pw) *
-                                a.Cn;
+        const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
 #pragma unroll 1
-        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-          uint32_t v[32];
-          if (ph.ntaps > 0) {
-            ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + c), v);
-            ptx::tmem_ld_wait();
-          } else {
+        for (int g = 0; g < BN / kG; ++g) {
+          // 1. this warp's half of the group: TMEM -> + bias -> bf16 -> staging row `lane`
+#pragma unroll 1
+          for (int c = half * (kG / 2); c < (half + 1) * (kG / 2); c += 32) {
+            const int col = g * kG + c;
+            uint32_t v[32];
+            if (ph.ntaps > 0) {
+              ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + col), v);
+              ptx::tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
-          }
-          const int co = n0 + c;
-          if (valid && co < a.Cn) {
+              for (int j = 0; j < 32; ++j) v[j] = 0u;
+            }
+            const int co = n0 + col;
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               pk[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) + bias_s[min(co + 2 * j, a.Cn - 1)],
                                        __uint_as_float(v[2 * j + 1]) + bias_s[min(co + 2 * j + 1, a.Cn - 1)]);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + co);
+            const uint32_t d = stage_s + uint32_t(lane * kPitch + c * 2);
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-              if (co + 8 * g < a.Cn) d4[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            for (int q = 0; q < 4; ++q)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + q * 16), "r"(pk[4 * q]),
+                           "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                           : "memory");
           }
+          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+          // 2. the pair stores the 32 staged rows: whole pixels per instruction
+#pragma unroll 1
+          for (int k = tp; k < 32 * kParts; k += 64) {
+            const int row = k / kParts, part = k - row * kParts;
+            const int q = qbase + row;
+            const int r = q / ph.P, colv = q - r * ph.P;
+            const int co = n0 + g * kG + part * 8;
+            if (r < ph.R && colv < ph.OWv && co < a.Cn) {
+              uint4 val;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                           : "r"(stage_s + uint32_t(row * kPitch + part * 16))
+                           : "memory");
+              bf16* dst = a.out + (size_t(it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw +
+                                   ph.out_pw) * a.Cn + co;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
       }
       ptx::tc_fence_before();
@@ -498,7 +531,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
-  const size_t fixed = 1024 + size_t(a.Cn + 2) * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
+  const size_t staging = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
+  const size_t fixed = 1024 + staging + size_t(a.Cn + 2) * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
   for (int sa = 3; sa >= 2; --sa) {
     for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
       const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
