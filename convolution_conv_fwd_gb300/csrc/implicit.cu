@@ -162,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b_tiles = BRES ? a.T : a.sb;
   uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;  // 128 rows x (staging group * 2 + 16) bytes
   float* bias_s = reinterpret_cast<float*>(stage_base + 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(bias_s + ((a.Cn + 1) & ~1));
+  // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
+  // parameter reads are slow next to shared-memory reads in the MMA loop.
+  int* taps_s = reinterpret_cast<int*>(bias_s + ((a.Cn + 1) & ~1));  // [phase][off, w][kMaxTapsPerPhase]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(taps_s + kMaxPhases * 2 * kMaxTapsPerPhase);
   uint64_t* fullA = bars;
   uint64_t* emptyA = fullA + a.sa;
   uint64_t* fullB = emptyA + a.sa;
@@ -184,8 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp < kEpiWarps)
+  if (warp < kEpiWarps) {
     for (int i = threadIdx.x; i < a.Cn; i += kEpiWarps * 32) bias_s[i] = a.bias ? a.bias[i] : 0.f;
+    for (int i = threadIdx.x; i < a.nphase * kMaxTapsPerPhase; i += kEpiWarps * 32) {
+      const int p = i / kMaxTapsPerPhase, t = i % kMaxTapsPerPhase;
+      taps_s[(p * 2 + 0) * kMaxTapsPerPhase + t] = a.ph[p].tap_off[t];
+      taps_s[(p * 2 + 1) * kMaxTapsPerPhase + t] = a.ph[p].tap_w[t];
+    }
+  }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
@@ -231,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; ok && t < ph.ntaps; ++t) {
               if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
               ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
-              load_b(b_base + size_t(sb) * kBTile, fullB + sb, ph.tap_w[t], kb, it.ntile * BN);
+              load_b(b_base + size_t(sb) * kBTile, fullB + sb, taps_s[(it.phase * 2 + 1) * kMaxTapsPerPhase + t], kb,
+                     it.ntile * BN);
               if (++sb == a.sb) { sb = 0; pb ^= 1; }
             }
           }
@@ -256,20 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ph.ntaps > 0) {
           const int q0 = it.m * 128 * NSUB;
           const int row0 = q0 - (q0 / ph.P) * ph.P;  // tile start inside the halo block
-          for (int kb = 0; ok && kb < a.kb_count; ++kb) {
+          const int ntaps = ph.ntaps, kbn = a.kb_count;
+          const int* toff = taps_s + (it.phase * 2 + 0) * kMaxTapsPerPhase;
+          const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
+          for (int kb = 0; ok && kb < kbn; ++kb) {
             if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
             ptx::tc_fence_after();
             const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
-            for (int t = 0; t < ph.ntaps; ++t) {
+            for (int t = 0; t < ntaps; ++t) {
               uint32_t b_addr;
               if (BRES) {
-                b_addr = ptx::smem_addr(b_base + size_t(ph.tap_w[t]) * kBTile);
+                b_addr = ptx::smem_addr(b_base + size_t(tw[t]) * kBTile);
               } else {
                 if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
                 ptx::tc_fence_after();
                 b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
               }
-              const uint32_t arow = a_addr + uint32_t(row0 + ph.tap_off[t]) * 128;
+              const uint32_t arow = a_addr + uint32_t(row0 + toff[t]) * 128;
 #pragma unroll
               for (int j = 0; j < kKB / 16; ++j) {
                 const uint64_t bdesc = DGRAD ? desc_sw128_mnmajor(b_addr + j * 2048, 8192)
@@ -532,7 +545,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
   const size_t staging = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
-  const size_t fixed = 1024 + staging + size_t(a.Cn + 2) * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
+  const size_t fixed = 1024 + staging + size_t(a.Cn + 2) * 4 + size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 +
+                       8 * (2 * 4 + 2 * 8 + 6) + 16;
   for (int sa = 3; sa >= 2; --sa) {
     for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
       const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
