@@ -55,22 +55,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended in hardware for up to
+// `hint_ns` while the phase is incomplete, instead of returning at once:
+// waiting threads then stop polling the barrier (each poll is a shared-memory
+// access, and shared-memory bandwidth is what the tensor core's operand
+// fetch runs on).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after kWaitLimitNs, or as soon as another role of the CTA has given up
 // (*abort != 0); on giving up it records bit `why` in *status and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status, unsigned int why) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicOr(status, why);
-        return false;
-      }
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicOr(status, why);
+      return false;
     }
   }
 }
