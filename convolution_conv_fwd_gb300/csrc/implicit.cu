@@ -230,18 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Phase& ph = a.ph[it.phase];
         if (ph.ntaps == 0) continue;
         const int ra = (it.m * 128 * NSUB) / ph.P;
-        for (int kb = 0; ok && kb < a.kb_count; ++kb) {
+        const int kb_rot = item % a.kb_count, t_rot = item % ph.ntaps;
+        const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
+        for (int kbi = 0; ok && kbi < a.kb_count; ++kbi) {
+          const int kb = kbi + kb_rot < a.kb_count ? kbi + kb_rot : kbi + kb_rot - a.kb_count;
           if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
           ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
           tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
                       kb * kKB, ph.cmin, ra + ph.rmin, it.n);
           if (++sa == a.sa) { sa = 0; pa ^= 1; }
           if (!BRES) {
-            for (int t = 0; ok && t < ph.ntaps; ++t) {
+            for (int ti = 0, t = t_rot; ok && ti < ph.ntaps; ++ti, t = (t + 1 == ph.ntaps ? 0 : t + 1)) {
               if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
               ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
-              load_b(b_base + size_t(sb) * kBTile, fullB + sb, taps_s[(it.phase * 2 + 1) * kMaxTapsPerPhase + t], kb,
-                     it.ntile * BN);
+              load_b(b_base + size_t(sb) * kBTile, fullB + sb, tw[t], kb, it.ntile * BN);
               if (++sb == a.sb) { sb = 0; pb ^= 1; }
             }
           }
@@ -269,20 +271,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ntaps = ph.ntaps, kbn = a.kb_count;
           const int* toff = taps_s + (it.phase * 2 + 0) * kMaxTapsPerPhase;
           const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
-          for (int kb = 0; ok && kb < kbn; ++kb) {
+          // k-blocks and taps are walked in an order rotated by the item index (the producer
+          // walks the same order): CTAs working at the same time then read different weight
+          // tiles, which spreads the L2 traffic of the streamed weights.
+          const int t_rot = item % ntaps;
+          for (int kbi = 0; ok && kbi < kbn; ++kbi) {
             if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
             ptx::tc_fence_after();
             const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
-            for (int t = 0; t < ntaps; ++t) {
+            int tc = t_rot;
+            int off_c = toff[tc], w_c = tw[tc];
+            for (int ti = 0; ti < ntaps; ++ti) {
+              // fetch the next tap's table entries before this tap's MMAs are issued
+              const int tn = tc + 1 == ntaps ? 0 : tc + 1;
+              const int off_n = toff[tn], w_n = tw[tn];
               uint32_t b_addr;
               if (BRES) {
-                b_addr = ptx::smem_addr(b_base + size_t(tw[t]) * kBTile);
+                b_addr = ptx::smem_addr(b_base + size_t(w_c) * kBTile);
               } else {
                 if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
                 ptx::tc_fence_after();
                 b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
               }
-              const uint32_t arow = a_addr + uint32_t(row0 + toff[t]) * 128;
+              const uint32_t arow = a_addr + uint32_t(row0 + off_c) * 128;
 #pragma unroll
               for (int j = 0; j < kKB / 16; ++j) {
                 const uint64_t bdesc = DGRAD ? desc_sw128_mnmajor(b_addr + j * 2048, 8192)
@@ -290,12 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int s = 0; s < NSUB; ++s)
                   ptx::mma_bf16(acc + s * BN, desc_sw128_kmajor(arow + s * 128 * 128 + j * 32), bdesc, kIdesc,
-                                (kb | t | j) != 0);
+                                (kbi | ti | j) != 0);
               }
               if (!BRES) {
                 ptx::mma_commit(emptyB + sb);
                 if (++sb == a.sb) { sb = 0; pb ^= 1; }
               }
+              tc = tn;
+              off_c = off_n;
+              w_c = w_n;
             }
             ptx::mma_commit(emptyA + sa);
             if (++sa == a.sa) { sa = 0; pa ^= 1; }
