@@ -293,15 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
               }
-              const uint32_t arow = a_addr + uint32_t(row0 + off_c) * 128;
+              // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
+              // per-MMA operand offsets (K step j, sub-tile s) are compile-time adds on it.
+              const uint64_t ad0 = desc_sw128_kmajor(a_addr + uint32_t(row0 + off_c) * 128);
+              const uint64_t bd0 = DGRAD ? desc_sw128_mnmajor(b_addr, 8192) : desc_sw128_kmajor(b_addr);
+              const uint32_t a_lo = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
+              const uint32_t b_lo = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+              const uint32_t first = uint32_t(kbi | ti);
 #pragma unroll
               for (int j = 0; j < kKB / 16; ++j) {
-                const uint64_t bdesc = DGRAD ? desc_sw128_mnmajor(b_addr + j * 2048, 8192)
-                                             : desc_sw128_kmajor(b_addr + j * 32);
+                const uint32_t b_off = DGRAD ? uint32_t(j * 2048 >> 4) : uint32_t(j * 32 >> 4);
 #pragma unroll
                 for (int s = 0; s < NSUB; ++s)
-                  ptx::mma_bf16(acc + s * BN, desc_sw128_kmajor(arow + s * 128 * 128 + j * 32), bdesc, kIdesc,
-                                (kbi | ti | j) != 0);
+                  ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((s * 128 * 128 + j * 32) >> 4), a_hi, b_lo + b_off,
+                                     b_hi, kIdesc, j == 0 ? first : 1u);
               }
               if (!BRES) {
                 ptx::mma_commit(emptyB + sb);
