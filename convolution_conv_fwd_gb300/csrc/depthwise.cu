@@ -17,7 +17,14 @@
 #include <algorithm>
 #include <cstdint>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
 #include "problem.h"
+#include "ptx.cuh"
 
 namespace gbconv {
 namespace {
@@ -197,6 +204,187 @@ __global__ void __launch_bounds__(kThreads, 2) depthwise3x3_kernel(DwArgs a, con
   }
 }
 
+
+// ---------------------------------------------------------------- TMA-fed 3x3
+// Persistent kernel for the 3x3 / stride 1 or 2 / dilation 1 case with 64-channel
+// chunks.  A producer lane streams halo tiles (kTR x kTC outputs need
+// ((kTR-1)S+3) x ((kTC-1)S+3) input pixels x 64 channels, zero fill supplying the
+// padding) through a ring of shared-memory stages with TMA; 256 compute threads
+// each own 8 channels of two output pixels per tile, keep their 72 weights in
+// registers, and read the taps from shared memory.  DRAM sees each input byte
+// once per tile (halo overlap between tiles comes from L2).
+constexpr int kTR = 4, kTC = 16;            // output tile: rows x columns
+constexpr int kDwStages = 4;
+constexpr int kDwCompute = 256;             // compute threads (8 warps)
+constexpr int kDwThreads = kDwCompute + 32; // + one producer warp
+
+struct DwTmaArgs {
+  const float* bias;
+  __nv_bfloat16* y;
+  unsigned int* status;
+  int N, C, H, W, OH, OW, PH, PW;
+  int nchunk, tiles_h, tiles_w, tiles_per_chunk;
+  int ir, ic, stage_bytes;
+};
+
+template <int S>
+__global__ void __launch_bounds__(kDwThreads, 1)
+    depthwise3x3_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ DwTmaArgs a,
+                            const __nv_bfloat16* __restrict__ w) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDwStages * a.stage_bytes);
+  uint64_t* empty = full + kDwStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDwStages);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDwStages; ++i) { ptx::mbar_init(full + i, 1); ptx::mbar_init(empty + i, kDwCompute); }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // CTAs are split evenly over the channel chunks, so each keeps one chunk's weights.
+  const int chunk = blockIdx.x % a.nchunk;
+  const int ctas_per_chunk = gridDim.x / a.nchunk;
+  const int first = blockIdx.x / a.nchunk;
+  if (warp == kDwCompute / 32) {
+    if ((threadIdx.x & 31) == 0) {
+      ptx::prefetch_tmap(&xmap);
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
+        const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
+        if (!ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 16u)) break;
+        ptx::mbar_arrive_expect_tx(full + st, uint32_t(a.stage_bytes));
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+            "%6}], [%2];" ::"r"(ptx::smem_addr(smem + st * a.stage_bytes)),
+            "l"(&xmap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC * S - a.PW),
+            "r"(th * kTR * S - a.PH), "r"(n)
+            : "memory");
+        if (++st == kDwStages) { st = 0; ph ^= 1; }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+  // ------------------------------------------------------------ compute threads
+  const int cv = threadIdx.x & 7;     // 8-channel vector inside the 64-channel chunk
+  const int pix = threadIdx.x >> 3;   // 0..31: output pixels pix and pix + 32 of the tile
+  const int c = chunk * 64 + cv * 8;
+  float wr[9][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(c + j) * 9 + t]);
+  float b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + c + j) : 0.f;
+  uint4* yv = reinterpret_cast<uint4*>(a.y);
+  const int cvec = a.C / 8;
+  int st = 0;
+  uint32_t ph = 0;
+  for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
+    const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
+    if (!ptx::mbar_wait(full + st, ph, abort_flag, a.status, 16u)) break;
+    const uint32_t base = ptx::smem_addr(smem + st * a.stage_bytes) + cv * 16;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int p = pix + half * 32;
+      const int r = p / kTC, col = p % kTC;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = b[j];
+#pragma unroll
+      for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+        for (int kw = 0; kw < 3; ++kw) {
+          uint4 v;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(base + uint32_t(((r * S + kh) * a.ic + col * S + kw) * 128)));
+          float xf[8];
+          unpack8(v, xf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = fmaf(xf[j], wr[kh * 3 + kw][j], acc[j]);
+        }
+      const int oh = th * kTR + r, ow = tw * kTC + col;
+      if (oh < a.OH && ow < a.OW) {
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        yv[(size_t(n * a.OH + oh) * a.OW + ow) * cvec + (c >> 3)] = o;
+      }
+    }
+    ptx::mbar_arrive(empty + st);
+    if (++st == kDwStages) { st = 0; ph ^= 1; }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool dw_tma_supported(const Problem& p) {
+  return p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2) &&
+         p.Cin % 64 == 0;
+}
+
+template <int S>
+gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                            const Launch& l) {
+  auto fn = dw_encode_fn();
+  if (!fn) return GBCONV_ECUDA;
+  DwTmaArgs a{};
+  a.bias = bias;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.status = l.status;
+  a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.PH = int(p.PH); a.PW = int(p.PW);
+  a.nchunk = a.C / 64;
+  a.tiles_h = (a.OH + kTR - 1) / kTR;
+  a.tiles_w = (a.OW + kTC - 1) / kTC;
+  a.tiles_per_chunk = a.N * a.tiles_h * a.tiles_w;
+  a.ir = (kTR - 1) * S + 3;
+  a.ic = (kTC - 1) * S + 3;
+  a.stage_bytes = a.ir * a.ic * 128;
+  CUtensorMap map;
+  cuuint64_t dims[4] = {cuuint64_t(a.C), cuuint64_t(a.W), cuuint64_t(a.H), cuuint64_t(a.N)};
+  cuuint64_t strides[3] = {cuuint64_t(a.C) * 2, cuuint64_t(a.W) * a.C * 2, cuuint64_t(a.H) * a.W * a.C * 2};
+  cuuint32_t box[4] = {64, cuuint32_t(a.ic), cuuint32_t(a.ir), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return GBCONV_ECUDA;
+  const size_t smem = size_t(kDwStages) * a.stage_bytes + 8 * 2 * kDwStages + 16;
+  auto kern = depthwise3x3_tma_kernel<S>;
+  static std::atomic<uint64_t> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  if (done[dev].load(std::memory_order_acquire) == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+      return GBCONV_ECUDA;
+    done[dev].store(1, std::memory_order_release);
+  }
+  // A multiple of the chunk count, at most one CTA per SM and per tile column of work.
+  int grid = std::max(a.nchunk, (l.num_sms / a.nchunk) * a.nchunk);
+  grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
+  kern<<<grid, kDwThreads, smem, static_cast<cudaStream_t>(l.stream)>>>(map, a, static_cast<const __nv_bfloat16*>(w));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
 }  // namespace
 
 bool depthwise_supported(const Problem& p) {
@@ -227,6 +415,7 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
   auto xb = static_cast<const __nv_bfloat16*>(x);
   auto wb = static_cast<const __nv_bfloat16*>(w);
   auto yb = static_cast<__nv_bfloat16*>(y);
+  if (dw_tma_supported(p)) return p.SH == 1 ? launch_dw_tma<1>(p, x, w, bias, y, l) : launch_dw_tma<2>(p, x, w, bias, y, l);
   if (p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2)) {
     a.rows_per_thread = 8;
     grid.y = unsigned((p.OH + a.rows_per_thread - 1) / a.rows_per_thread);

@@ -95,6 +95,11 @@ SMALL = [
     (shape_kw(n=2, in_size=(11, 10), c_in=32, c_out=32, groups=32, bias=True), "fwd", "depthwise"),
     (shape_kw(n=1, in_size=(10, 9), c_in=16, c_out=16, groups=16, stride=(2, 2), pad=(0, 0)), "fwd", "depthwise"),
     (shape_kw(n=1, in_size=(21, 19), c_in=40, c_out=40, groups=40, stride=(2, 2), pad=(2, 2)), "fwd", "depthwise"),
+    # TMA-fed 3x3 path (64-channel chunks): stride 1 and 2, several tiles, ragged tile edges, wide padding
+    (shape_kw(n=2, in_size=(13, 37), c_in=128, c_out=128, groups=128, bias=True), "fwd", "depthwise"),
+    (shape_kw(n=3, in_size=(19, 35), c_in=64, c_out=64, groups=64, stride=(2, 2), pad=(0, 0)), "fwd", "depthwise"),
+    (shape_kw(n=1, in_size=(10, 41), c_in=192, c_out=192, groups=192, stride=(2, 2), pad=(2, 2), bias=True),
+     "fwd", "depthwise"),
     # stride-phase dgrad (tcgen05): one phase, four uneven phases, zero-tap phases, even kernel, N tiles
     (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64), "dgrad", "dgrad"),
     (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad", "dgrad"),
