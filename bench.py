@@ -397,6 +397,31 @@ def run_reference(args):
     }
 
 
+def profile_workload(name: str, reps: int):
+    """Run one workload `reps` times through the C ABI (no timing, no oracle): the target of ncu captures."""
+    import torch
+    import convolution_conv_fwd_gb300 as gb
+    from synth.workloads import BY_NAME
+    wl = BY_NAME[name]
+    inp = make_inputs(wl)
+    d = desc_for(gb, wl)
+
+    def dev(key):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(inp[key + "_bits"]).view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(inp[key]).cuda()
+    w = dev("w")
+    b = torch.from_numpy(inp["b"]).cuda() if "b" in inp else None
+    src = dev("g" if wl.op == "dgrad" else "x")
+    for _ in range(reps):
+        if wl.op == "dgrad":
+            gb.conv_bwd_data(d, src, w)
+        else:
+            gb.conv_fwd(d, src, w, b)
+    gb.device_status()
+    print("ran", name, reps, "times")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,7 +430,12 @@ def main():
     ap.add_argument("--impl", default="gbconv", choices=["gbconv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle work for the cpu_baseline sample")
     ap.add_argument("--ref-seconds-per-step", type=float, default=3.0)
+    ap.add_argument("--profile-workload", default=None,
+                    help="run only this workload --steps times through the C ABI and exit (for ncu captures)")
     args = ap.parse_args()
+    if args.profile_workload:
+        profile_workload(args.profile_workload, args.steps)
+        return
     if args.warmup < 3 and args.impl == "gbconv":
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
