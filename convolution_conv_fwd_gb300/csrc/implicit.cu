@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* bias_s = reinterpret_cast<float*>(stage_base + 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16));
   // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
   // parameter reads are slow next to shared-memory reads in the MMA loop.
-  int* taps_s = reinterpret_cast<int*>(bias_s + ((a.Cn + 1) & ~1));  // [phase][off, w][kMaxTapsPerPhase]
+  int* taps_s = reinterpret_cast<int*>(bias_s + a.n_tiles * BN);  // [phase][off, w][kMaxTapsPerPhase]
   uint64_t* bars = reinterpret_cast<uint64_t*>(taps_s + kMaxPhases * 2 * kMaxTapsPerPhase);
   uint64_t* fullA = bars;
   uint64_t* emptyA = fullA + a.sa;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp < kEpiWarps) {
-    for (int i = threadIdx.x; i < a.Cn; i += kEpiWarps * 32) bias_s[i] = a.bias ? a.bias[i] : 0.f;
+    for (int i = threadIdx.x; i < a.n_tiles * BN; i += kEpiWarps * 32) bias_s[i] = (a.bias && i < a.Cn) ? a.bias[i] : 0.f;
     for (int i = threadIdx.x; i < a.nphase * kMaxTapsPerPhase; i += kEpiWarps * 32) {
       const int p = i / kMaxTapsPerPhase, t = i % kMaxTapsPerPhase;
       taps_s[(p * 2 + 0) * kMaxTapsPerPhase + t] = a.ph[p].tap_off[t];
@@ -349,53 +349,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u)) break;
       ptx::tc_fence_after();
       const int n0 = it.ntile * BN;
+      const bool has_bias = a.bias != nullptr;
+      // Store-phase geometry: thread tp always writes 16-byte piece (tp % kParts) of rows
+      // tp / kParts + i * kRowStep, so only the row advances between its stores.
+      constexpr int kRowStep = 64 / kParts;
+      const int part = tp % kParts;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
 #pragma unroll 1
         for (int g = 0; g < BN / kG; ++g) {
-          // 1. this warp's half of the group: TMEM -> + bias -> bf16 -> staging row `lane`
-#pragma unroll 1
-          for (int c = half * (kG / 2); c < (half + 1) * (kG / 2); c += 32) {
-            const int col = g * kG + c;
-            uint32_t v[32];
-            if (ph.ntaps > 0) {
-              ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + col), v);
-              ptx::tmem_ld_wait();
-            } else {
+          // 1. this warp's half of the group: TMEM -> (+ bias) -> bf16 -> staging row `lane`
+          constexpr int kChunks = kG / 64;  // 32-column TMEM loads per warp per group
+          uint32_t v[kChunks][32];
+          const int c0 = g * kG + half * (kG / 2);
+          if (ph.ntaps > 0) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = 0u;
+            for (int ch = 0; ch < kChunks; ++ch)
+              ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + c0 + ch * 32), v[ch]);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[ch][j] = 0u;
+          }
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) {
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[ch][j]);
+            if (has_bias) {
+              const float4* b4 = reinterpret_cast<const float4*>(bias_s + n0 + c0 + ch * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 bb = b4[q];
+                f[4 * q] += bb.x; f[4 * q + 1] += bb.y; f[4 * q + 2] += bb.z; f[4 * q + 3] += bb.w;
+              }
             }
-            const int co = n0 + col;
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) + bias_s[min(co + 2 * j, a.Cn - 1)],
-                                       __uint_as_float(v[2 * j + 1]) + bias_s[min(co + 2 * j + 1, a.Cn - 1)]);
-            const uint32_t d = stage_s + uint32_t(lane * kPitch + c * 2);
+            const uint32_t d = stage_s + uint32_t(lane * kPitch + (half * (kG / 2) + ch * 32) * 2);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + q * 16), "r"(pk[4 * q]),
-                           "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + q * 16),
+                           "r"(ptx::pack_bf16x2(f[8 * q], f[8 * q + 1])), "r"(ptx::pack_bf16x2(f[8 * q + 2], f[8 * q + 3])),
+                           "r"(ptx::pack_bf16x2(f[8 * q + 4], f[8 * q + 5])), "r"(ptx::pack_bf16x2(f[8 * q + 6], f[8 * q + 7]))
                            : "memory");
           }
           asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-          // 2. the pair stores the 32 staged rows: whole pixels per instruction
-#pragma unroll 1
-          for (int k = tp; k < 32 * kParts; k += 64) {
-            const int row = k / kParts, part = k - row * kParts;
-            const int q = qbase + row;
-            const int r = q / ph.P, colv = q - r * ph.P;
-            const int co = n0 + g * kG + part * 8;
-            if (r < ph.R && colv < ph.OWv && co < a.Cn) {
-              uint4 val;
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                           : "r"(stage_s + uint32_t(row * kPitch + part * 16))
-                           : "memory");
-              bf16* dst = a.out + (size_t(it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw +
-                                   ph.out_pw) * a.Cn + co;
-              *reinterpret_cast<uint4*>(dst) = val;
+          // 2. the pair stores the 32 staged rows: whole pixels per warp instruction
+          const int co = n0 + g * kG + part * 8;
+          if (co < a.Cn) {
+            int row = tp / kParts;
+            int q = qbase + row;
+            int r = q / ph.P, colv = q - r * ph.P;
+#pragma unroll
+            for (int i = 0; i < 32 / kRowStep; ++i) {
+              if (r < ph.R && colv < ph.OWv) {
+                uint4 val;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                             : "r"(stage_s + uint32_t(row * kPitch + part * 16))
+                             : "memory");
+                const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
+                *reinterpret_cast<uint4*>(a.out + size_t(pix) * a.Cn + co) = val;
+              }
+              row += kRowStep;
+              colv += kRowStep;
+              while (colv >= ph.P) { colv -= ph.P; ++r; }
             }
           }
           asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
@@ -564,7 +584,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
   const size_t staging = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
-  const size_t fixed = 1024 + staging + size_t(a.Cn + 2) * 4 + size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 +
+  const size_t fixed = 1024 + staging + size_t(a.n_tiles) * pl.bn * 4 + size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 +
                        8 * (2 * 4 + 2 * 8 + 6) + 16;
   for (int sa = 3; sa >= 2; --sa) {
     for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
