@@ -335,12 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the same output pixel (whole pixels per warp instruction).
     constexpr int kG = BN % 128 == 0 ? 128 : 64;  // columns per staging group
     constexpr int kPitch = kG * 2 + 16;         // padded row pitch of the staging block, bytes
-    constexpr int kParts = kG / 8;              // 16-byte pieces per staged row
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
     uint8_t* stage = stage_base + quad * 32 * kPitch;
     const uint32_t stage_s = ptx::smem_addr(stage);
-    const int tp = half * 32 + lane;            // thread index within the pair
     int iter = 0;
     for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
       const Item it = decode_item(a, item);
@@ -350,10 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int n0 = it.ntile * BN;
       const bool has_bias = a.bias != nullptr;
-      // Store-phase geometry: thread tp always writes 16-byte piece (tp % kParts) of rows
-      // tp / kParts + i * kRowStep, so only the row advances between its stores.
-      constexpr int kRowStep = 64 / kParts;
-      const int part = tp % kParts;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
@@ -395,28 +389,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                            "r"(ptx::pack_bf16x2(f[8 * q + 4], f[8 * q + 5])), "r"(ptx::pack_bf16x2(f[8 * q + 6], f[8 * q + 7]))
                            : "memory");
           }
+          // make the staged rows visible to the TMA engine, then let the pair see each other's halves
+          ptx::fence_proxy_async_smem();
           asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-          // 2. the pair stores the 32 staged rows: whole pixels per warp instruction
-          const int co = n0 + g * kG + part * 8;
-          if (co < a.Cn) {
-            int row = tp / kParts;
-            int q = qbase + row;
-            int r = q / ph.P, colv = q - r * ph.P;
-#pragma unroll
-            for (int i = 0; i < 32 / kRowStep; ++i) {
-              if (r < ph.R && colv < ph.OWv) {
-                uint4 val;
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                             : "r"(stage_s + uint32_t(row * kPitch + part * 16))
-                             : "memory");
-                const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
-                *reinterpret_cast<uint4*>(a.out + size_t(pix) * a.Cn + co) = val;
-              }
-              row += kRowStep;
-              colv += kRowStep;
-              while (colv >= ph.P) { colv -= ph.P; ++r; }
+          // 2. each staged row is one bulk copy to its output pixel (16 rows per warp of the pair)
+          if (lane < 16) {
+            const int row = half * 16 + lane;
+            const int q = qbase + row;
+            const int r = q / ph.P, colv = q - r * ph.P;
+            const int co = n0 + g * kG;
+            if (r < ph.R && colv < ph.OWv && co < a.Cn) {
+              const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
+              const uint32_t bytes = uint32_t(min(kG, a.Cn - co) * 2);
+              asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(a.out + size_t(pix) * a.Cn + co),
+                           "r"(stage_s + uint32_t(row * kPitch)), "r"(bytes)
+                           : "memory");
             }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            // the staging block may be rewritten only after the copies have read it
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           }
           asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
@@ -424,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty + buf);
     }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   ptx::tc_fence_before();
