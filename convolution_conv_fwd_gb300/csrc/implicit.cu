@@ -88,6 +88,7 @@ struct Args {
   int kb_count;       // 64-channel k-blocks of the reduction
   int n_tiles;
   int a_stage_bytes, b_tile_bytes, sa, sb;
+  int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int nphase, total_items;
   Phase ph[kMaxPhases];
 };
@@ -160,8 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_base = smem;
   uint8_t* b_base = a_base + size_t(a.sa) * a.a_stage_bytes;
   const int b_tiles = BRES ? a.T : a.sb;
-  uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;  // 128 rows x (staging group * 2 + 16) bytes
-  float* bias_s = reinterpret_cast<float*>(stage_base + 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16));
+  // two staging blocks of 128 rows x (staging group * 2 + 16) bytes
+  uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;
+  constexpr int kStageBlock = 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16);
+  float* bias_s = reinterpret_cast<float*>(stage_base + a.stage_bufs * kStageBlock);
   // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
   // parameter reads are slow next to shared-memory reads in the MMA loop.
   int* taps_s = reinterpret_cast<int*>(bias_s + a.n_tiles * BN);  // [phase][off, w][kMaxTapsPerPhase]
@@ -337,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kPitch = kG * 2 + 16;         // padded row pitch of the staging block, bytes
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    uint8_t* stage = stage_base + quad * 32 * kPitch;
-    const uint32_t stage_s = ptx::smem_addr(stage);
+    const uint32_t stage0 = ptx::smem_addr(stage_base + quad * 32 * kPitch);
+    int sbuf = 0;  // staging block used next
     int iter = 0;
     for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
       const Item it = decode_item(a, item);
@@ -353,6 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
 #pragma unroll 1
         for (int g = 0; g < BN / kG; ++g) {
+          // The staging block is reused every second sub-tile: its previous bulk copies (the group
+          // before the most recent one) must have finished reading it first.
+          const uint32_t stage_s = stage0 + uint32_t(sbuf * kStageBlock);
+          if (a.stage_bufs == 2) {
+            sbuf ^= 1;
+            if (lane < 16) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          } else {
+            if (lane < 16) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          }
+          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
           // 1. this warp's half of the group: TMEM -> (+ bias) -> bf16 -> staging row `lane`
           constexpr int kChunks = kG / 64;  // 32-column TMEM loads per warp per group
           uint32_t v[kChunks][32];
@@ -406,10 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : "memory");
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            // the staging block may be rewritten only after the copies have read it
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           }
-          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
       }
       ptx::tc_fence_before();
@@ -575,17 +585,20 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
-  const size_t staging = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
-  const size_t fixed = 1024 + staging + size_t(a.n_tiles) * pl.bn * 4 + size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 +
-                       8 * (2 * 4 + 2 * 8 + 6) + 16;
-  for (int sa = 3; sa >= 2; --sa) {
-    for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
-      const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
-      if (total <= size_t(kSmemLimit)) {
-        a.sa = sa;
-        a.sb = pl.bres ? 1 : sb;
-        pl.smem = total;
-        return true;
+  const size_t block = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
+  for (int bufs = 2; bufs >= 1; --bufs) {
+    const size_t fixed = 1024 + bufs * block + size_t(a.n_tiles) * pl.bn * 4 +
+                         size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
+    for (int sa = 3; sa >= 2; --sa) {
+      for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
+        const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
+        if (total <= size_t(kSmemLimit)) {
+          a.sa = sa;
+          a.sb = pl.bres ? 1 : sb;
+          a.stage_bufs = bufs;
+          pl.smem = total;
+          return true;
+        }
       }
     }
   }
