@@ -356,16 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
 #pragma unroll 1
         for (int g = 0; g < BN / kG; ++g) {
-          // The staging block is reused every second sub-tile: its previous bulk copies (the group
-          // before the most recent one) must have finished reading it first.
+          // With two staging blocks the barrier after the writes also proves that both warps
+          // finished reading the block they are about to overwrite (two sub-tiles ago).
           const uint32_t stage_s = stage0 + uint32_t(sbuf * kStageBlock);
-          if (a.stage_bufs == 2) {
-            sbuf ^= 1;
-            if (lane < 16) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          } else {
-            if (lane < 16) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          }
-          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+          if (a.stage_bufs == 2) sbuf ^= 1;
           // 1. this warp's half of the group: TMEM -> (+ bias) -> bf16 -> staging row `lane`
           constexpr int kChunks = kG / 64;  // 32-column TMEM loads per warp per group
           uint32_t v[kChunks][32];
@@ -402,30 +396,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                            "r"(ptx::pack_bf16x2(f[8 * q + 4], f[8 * q + 5])), "r"(ptx::pack_bf16x2(f[8 * q + 6], f[8 * q + 7]))
                            : "memory");
           }
-          // make the staged rows visible to the TMA engine, then let the pair see each other's halves
-          ptx::fence_proxy_async_smem();
           asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-          // 2. each staged row is one bulk copy to its output pixel (16 rows per warp of the pair)
-          if (lane < 16) {
-            const int row = half * 16 + lane;
-            const int q = qbase + row;
-            const int r = q / ph.P, colv = q - r * ph.P;
-            const int co = n0 + g * kG;
-            if (r < ph.R && colv < ph.OWv && co < a.Cn) {
-              const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
-              const uint32_t bytes = uint32_t(min(kG, a.Cn - co) * 2);
-              asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(a.out + size_t(pix) * a.Cn + co),
-                           "r"(stage_s + uint32_t(row * kPitch)), "r"(bytes)
-                           : "memory");
+          // 2. the pair stores the 32 staged rows: consecutive threads write consecutive 16-byte
+          //    pieces of the same output pixel, so each warp store covers whole pixels.
+          {
+            constexpr int kParts = kG / 8;        // 16-byte pieces per staged row
+            constexpr int kRowStep = 64 / kParts; // rows advanced per pass of the pair
+            const int tp = half * 32 + lane;
+            const int part = tp % kParts;
+            const int co = n0 + g * kG + part * 8;
+            if (co < a.Cn) {
+              int row = tp / kParts;
+              const int q = qbase + row;
+              int r = q / ph.P, colv = q - r * ph.P;
+#pragma unroll
+              for (int i = 0; i < 32 / kRowStep; ++i) {
+                if (r < ph.R && colv < ph.OWv) {
+                  uint4 val;
+                  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                               : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                               : "r"(stage_s + uint32_t(row * kPitch + part * 16))
+                               : "memory");
+                  const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
+                  *reinterpret_cast<uint4*>(a.out + size_t(pix) * a.Cn + co) = val;
+                }
+                row += kRowStep;
+                colv += kRowStep;
+                while (colv >= ph.P) { colv -= ph.P; ++r; }
+              }
             }
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
+          if (a.stage_bufs == 1) asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty + buf);
     }
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   ptx::tc_fence_before();
