@@ -64,7 +64,7 @@ constexpr int kThreads = 10 * 32;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kKB = 64;  // channels per k-block: one 128-byte swizzled row
 
-struct Phase {
+struct PhaseHdr {
   int ntaps;
   int R;        // output rows of the virtual grid (per image)
   int P;        // virtual grid pitch: valid columns plus the horizontal reach
@@ -75,6 +75,9 @@ struct Phase {
   int a_bytes;  // bytes of one halo box (64 channels x P x bh)
   int tiles;    // m-tiles per image
   int item0;    // first work item of this phase
+};
+
+struct Phase : PhaseHdr {
   int tap_off[kMaxTapsPerPhase];  // halo row offset of tap t
   int tap_w[kMaxTapsPerPhase];    // weight tap index kh*KW + kw
 };
@@ -102,16 +105,16 @@ struct Item {
   int phase, n, m, ntile;
 };
 
-__device__ __forceinline__ Item decode_item(const Args& a, int item) {
+__device__ __forceinline__ Item decode_item(const PhaseHdr* ph, int nphase, int n_tiles, int item) {
   int p = 0;
-  while (p + 1 < a.nphase && item >= a.ph[p + 1].item0) ++p;
+  while (p + 1 < nphase && item >= ph[p + 1].item0) ++p;
   Item it;
   it.phase = p;
-  int local = item - a.ph[p].item0;
-  it.ntile = local % a.n_tiles;
-  local /= a.n_tiles;
-  it.n = local / a.ph[p].tiles;
-  it.m = local - it.n * a.ph[p].tiles;
+  int local = item - ph[p].item0;
+  it.ntile = local % n_tiles;
+  local /= n_tiles;
+  it.n = local / ph[p].tiles;
+  it.m = local - it.n * ph[p].tiles;
   return it;
 }
 
@@ -168,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
   // parameter reads are slow next to shared-memory reads in the MMA loop.
   int* taps_s = reinterpret_cast<int*>(bias_s + a.n_tiles * BN);  // [phase][off, w][kMaxTapsPerPhase]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(taps_s + kMaxPhases * 2 * kMaxTapsPerPhase);
+  PhaseHdr* phase_s = reinterpret_cast<PhaseHdr*>(taps_s + kMaxPhases * 2 * kMaxTapsPerPhase);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(phase_s + kMaxPhases);
   uint64_t* fullA = bars;
   uint64_t* emptyA = fullA + a.sa;
   uint64_t* fullB = emptyA + a.sa;
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp < kEpiWarps) {
-    for (int i = threadIdx.x; i < a.n_tiles * BN; i += kEpiWarps * 32) bias_s[i] = (a.bias && i < a.Cn) ? a.bias[i] : 0.f;
+    if (threadIdx.x < a.nphase) phase_s[threadIdx.x] = a.ph[threadIdx.x];
     for (int i = threadIdx.x; i < a.nphase * kMaxTapsPerPhase; i += kEpiWarps * 32) {
       const int p = i / kMaxTapsPerPhase, t = i % kMaxTapsPerPhase;
       taps_s[(p * 2 + 0) * kMaxTapsPerPhase + t] = a.ph[p].tap_off[t];
@@ -229,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
-        const Item it = decode_item(a, item);
-        const Phase& ph = a.ph[it.phase];
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+        const PhaseHdr& ph = phase_s[it.phase];
         if (ph.ntaps == 0) continue;
         const int ra = (it.m * 128 * NSUB) / ph.P;
         const int kb_rot = item % a.kb_count, t_rot = item % ph.ntaps;
@@ -262,8 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
       for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x, ++iter) {
-        const Item it = decode_item(a, item);
-        const Phase& ph = a.ph[it.phase];
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+        const PhaseHdr& ph = phase_s[it.phase];
         const int buf = iter & 1;
         if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, a.status, 2u))) break;
         ptx::tc_fence_after();
@@ -340,12 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kPitch = kG * 2 + 16;         // padded row pitch of the staging block, bytes
     const int quad = warp & 3, half = warp >> 2;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    // The bias comes from global memory: copied here, after the block-wide barrier, so the
+    // producer and MMA warps start without waiting for it.
+    for (int i = threadIdx.x; i < a.n_tiles * BN; i += kEpiWarps * 32) bias_s[i] = (a.bias && i < a.Cn) ? a.bias[i] : 0.f;
+    asm volatile("bar.sync 5, %0;" ::"n"(kEpiWarps * 32) : "memory");
     const uint32_t stage0 = ptx::smem_addr(stage_base + quad * 32 * kPitch);
     int sbuf = 0;  // staging block used next
     int iter = 0;
     for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
-      const Item it = decode_item(a, item);
-      const Phase& ph = a.ph[it.phase];
+      const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+      const PhaseHdr& ph = phase_s[it.phase];
       const int buf = iter & 1;
       if (!ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u)) break;
       ptx::tc_fence_after();
@@ -594,7 +602,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   const size_t block = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
   for (int bufs = 2; bufs >= 1; --bufs) {
     const size_t fixed = 1024 + bufs * block + size_t(a.n_tiles) * pl.bn * 4 +
-                         size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + 8 * (2 * 4 + 2 * 8 + 6) + 16;
+                         size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
+                         8 * (2 * 4 + 2 * 8 + 6) + 16;
     for (int sa = 3; sa >= 2; --sa) {
       for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
         const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;

@@ -58,7 +58,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* b_base = smem;                                      // kb_count tiles of [BN][64] bf16
   uint8_t* a_base = b_base + size_t(a.kb_count) * kBTileBytes;  // stages x [128][64] bf16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(a_base + size_t(a.stages) * kATileBytes);
+  // epilogue staging: 4 warps x 32 rows x (BN*2 + 16) bytes (padded rows: conflict-free 16-byte stores)
+  constexpr int kPitch = BN * 2 + 16;
+  uint8_t* stage_base = a_base + size_t(a.stages) * kATileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base + 128 * kPitch);
   uint64_t* full = bars;
   uint64_t* empty = full + a.stages;
   uint64_t* tfull = empty + a.stages;
@@ -145,31 +148,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = it & 1;
       if (!ptx::mbar_wait(tfull + buf, (it >> 1) & 1, abort_flag, a.status, 8u)) break;
       ptx::tc_fence_after();
-      const int row = tile * kBM + warp * 32 + lane;
-      bf16* dst = a.out + size_t(row) * a.Cout;
+      // TMEM -> (+ bias) -> bf16 -> this warp's staging rows, then whole-row coalesced stores:
+      // consecutive lanes write consecutive 16-byte pieces of the same output pixel.
+      const uint32_t stage_s = ptx::smem_addr(stage_base + warp * 32 * kPitch);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * BN + c * 32), v);
         ptx::tmem_ld_wait();
-        if (row < a.M) {
-          uint32_t pk[16];
+        float f[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float lo = __uint_as_float(v[2 * j]), hi = __uint_as_float(v[2 * j + 1]);
-            if (a.bias) {
-              lo += __ldg(a.bias + c * 32 + 2 * j);
-              hi += __ldg(a.bias + c * 32 + 2 * j + 1);
-            }
-            pk[j] = ptx::pack_bf16x2(lo, hi);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (a.bias) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < 32; ++j) f[j] += __ldg(a.bias + c * 32 + j);
         }
+        const uint32_t d = stage_s + uint32_t(lane * kPitch + c * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + q * 16),
+                       "r"(ptx::pack_bf16x2(f[8 * q], f[8 * q + 1])), "r"(ptx::pack_bf16x2(f[8 * q + 2], f[8 * q + 3])),
+                       "r"(ptx::pack_bf16x2(f[8 * q + 4], f[8 * q + 5])), "r"(ptx::pack_bf16x2(f[8 * q + 6], f[8 * q + 7]))
+                       : "memory");
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty + buf);
+      ptx::mbar_arrive(tempty + buf);  // TMEM is free once read; the stores below use the staging copy
+      __syncwarp();
+      constexpr int kParts = BN / 8;         // 16-byte pieces per row
+      constexpr int kRowStep = 32 / kParts;  // rows per warp pass
+      const int part = lane % kParts;
+      const int row0 = tile * kBM + warp * 32;
+#pragma unroll 4
+      for (int r = lane / kParts; r < 32; r += kRowStep) {
+        if (row0 + r < a.M) {
+          uint4 val;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                       : "r"(stage_s + uint32_t(r * kPitch + part * 16))
+                       : "memory");
+          *reinterpret_cast<uint4*>(a.out + size_t(row0 + r) * a.Cout + part * 8) = val;
+        }
+      }
+      __syncwarp();
     }
   }
 
@@ -212,7 +232,7 @@ int pick_bn(int64_t cout) {
 }
 
 int stages_for(int bn, int kb_count) {
-  const size_t fixed = size_t(kb_count) * bn * kBK * 2 + 1024 + 8 * (2 * kMaxStages + 8);
+  const size_t fixed = size_t(kb_count) * bn * kBK * 2 + 1024 + 8 * (2 * kMaxStages + 8) + 128 * size_t(bn * 2 + 16);
   if (fixed >= size_t(kSmemLimit)) return 0;
   const int s = int((size_t(kSmemLimit) - fixed) / kATileBytes);
   return std::min(s, kMaxStages);
@@ -220,7 +240,8 @@ int stages_for(int bn, int kb_count) {
 
 template <int BN>
 gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a, int grid, const Launch& l) {
-  const size_t smem = size_t(a.kb_count) * BN * kBK * 2 + size_t(a.stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8);
+  const size_t smem = size_t(a.kb_count) * BN * kBK * 2 + size_t(a.stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8) +
+                      128 * size_t(BN * 2 + 16);
   auto kern = pointwise_gemm_kernel<BN>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device and size.
   static std::atomic<uint64_t> done[64];
