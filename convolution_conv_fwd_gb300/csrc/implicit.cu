@@ -92,6 +92,7 @@ struct Args {
   int n_tiles;
   int a_stage_bytes, b_tile_bytes, sa, sb;
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
+  int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
   int nphase, total_items;
   Phase ph[kMaxPhases];
 };
@@ -218,9 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&maps.b);
       auto load_b = [&](uint8_t* dst, uint64_t* bar, int wt, int kb, int n0) {
         const uint32_t d = ptx::smem_addr(dst);
-        if (DGRAD) {  // MN-major: 64 input channels x 64 output channels per box
+        if (DGRAD) {  // MN-major: BN/64 atoms of [64 output channels][64 input channels]
+          if (a.b4d) {
+            tma_load_4d(d, &maps.b, bar, 0, kb * kKB, n0 / 64, wt);
+          } else {
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) tma_load_3d(d + h * 8192, &maps.b, bar, n0 + h * 64, wt, kb * kKB);
+            for (int h = 0; h < BN / 64; ++h) tma_load_3d(d + h * 8192, &maps.b, bar, n0 + h * 64, wt, kb * kKB);
+          }
         } else {      // K-major: BN output channels x 64 input channels
           tma_load_3d(d, &maps.b, bar, kb * kKB, wt, n0);
         }
@@ -621,6 +626,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
 }
 
 bool encode_maps(Plan& pl, const void* in, const void* w) {
+  pl.a.b4d = 0;
   auto fn = encode_fn();
   if (!fn) return false;
   const Args& a = pl.a;
@@ -636,6 +642,20 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
       return false;
   }
   const int Cout = pl.dgrad ? pl.Ck : a.Cn;
+  if (pl.dgrad) {
+    // The OHWI weight [C_out][T][C_in] viewed as (C_in % 64, C_out, C_in / 64, tap): a box of
+    // (64, 64, BN/64, 1) lands as BN/64 contiguous [64 C_out][64 C_in] atoms, the MN-major operand.
+    cuuint64_t dims[4] = {64, cuuint64_t(Cout), cuuint64_t((pl.Cw + 63) / 64), cuuint64_t(a.T)};
+    cuuint64_t strides[3] = {cuuint64_t(a.T) * pl.Cw * 2, 128, cuuint64_t(pl.Cw) * 2};
+    cuuint32_t box[4] = {64, 64, cuuint32_t(pl.bn / 64), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    // The C_in / 64 split needs whole 64-channel blocks; otherwise 64-wide 3-D boxes below.
+    pl.a.b4d = pl.Cw % 64 == 0 &&
+               fn(&pl.maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (pl.a.b4d) return true;
+  }
   cuuint64_t dims[3] = {cuuint64_t(pl.Cw), cuuint64_t(a.T), cuuint64_t(Cout)};
   cuuint64_t strides[2] = {cuuint64_t(pl.Cw) * 2, cuuint64_t(a.T) * pl.Cw * 2};
   cuuint32_t box[3] = {cuuint32_t(kKB), 1, cuuint32_t(pl.dgrad ? kKB : pl.bn)};
