@@ -288,8 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tiles, which spreads the L2 traffic of the streamed weights.
           const int t_rot = item % ntaps;
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
+            // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
+            // orders the async-proxy writes before the async-proxy MMA reads.
             if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
-            ptx::tc_fence_after();
             const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
             int tc = t_rot;
             int off_c = toff[tc], w_c = tw[tc];
@@ -302,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 b_addr = ptx::smem_addr(b_base + size_t(w_c) * kBTile);
               } else {
                 if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
-                ptx::tc_fence_after();
                 b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
               }
               // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
