@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kThreads) depthwise_fwd_kernel(DwArgs a, const
                                                                  const __nv_bfloat16* __restrict__ w,
                                                                  const float* __restrict__ bias,
                                                                  __nv_bfloat16* __restrict__ y) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   const int KH = KH_ > 0 ? KH_ : a.KH;
   const int KW = KW_ > 0 ? KW_ : a.KW;
   const int taps = KH * KW;
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 2) depthwise3x3_kernel(DwArgs a, con
                                                                   const __nv_bfloat16* __restrict__ w,
                                                                   const float* __restrict__ bias,
                                                                   __nv_bfloat16* __restrict__ y) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   constexpr int kKeep = 3 - S;  // input rows shared by consecutive output rows
   const int cpb = a.cv_per_block * 8;
   const int chunk = blockIdx.x % a.cv_chunks;
@@ -242,6 +246,8 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   // CTAs are split evenly over the channel chunks, so each keeps one chunk's weights.
   const int chunk = blockIdx.x % a.nchunk;
   const int ctas_per_chunk = gridDim.x / a.nchunk;
@@ -380,9 +386,10 @@ gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, cons
   // A multiple of the chunk count, at most one CTA per SM and per tile column of work.
   int grid = std::max(a.nchunk, (l.num_sms / a.nchunk) * a.nchunk);
   grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
-  kern<<<grid, kDwThreads, smem, static_cast<cudaStream_t>(l.stream)>>>(map, a, static_cast<const __nv_bfloat16*>(w));
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  return launch_kernel(kern, dim3(grid), dim3(kDwThreads), smem, l.stream, map, a,
+                       static_cast<const __nv_bfloat16*>(w)) == cudaSuccess
+             ? GBCONV_OK
+             : GBCONV_ECUDA;
 }
 
 }  // namespace
@@ -411,25 +418,24 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
   if (gx > 0x7FFFFFFF || gy > 65535 || p.N > 65535) return GBCONV_EUNSUPPORTED;
   dim3 grid(unsigned(gx), unsigned(gy), unsigned(p.N));
   const size_t smem = size_t(p.KH * p.KW) * cvb * 8 * sizeof(float);
-  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
   auto xb = static_cast<const __nv_bfloat16*>(x);
   auto wb = static_cast<const __nv_bfloat16*>(w);
   auto yb = static_cast<__nv_bfloat16*>(y);
   if (dw_tma_supported(p)) return p.SH == 1 ? launch_dw_tma<1>(p, x, w, bias, y, l) : launch_dw_tma<2>(p, x, w, bias, y, l);
-  if (p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2)) {
+  const bool reg3x3 = p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2);
+  if (reg3x3) {
     a.rows_per_thread = 8;
     grid.y = unsigned((p.OH + a.rows_per_thread - 1) / a.rows_per_thread);
-    if (p.SH == 1)
-      depthwise3x3_kernel<1><<<grid, block, 0, s>>>(a, xb, wb, bias, yb);
-    else
-      depthwise3x3_kernel<2><<<grid, block, 0, s>>>(a, xb, wb, bias, yb);
-  } else if (p.KH == 3 && p.KW == 3) {
-    depthwise_fwd_kernel<3, 3><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
-  } else {
-    depthwise_fwd_kernel<0, 0><<<grid, block, smem, s>>>(a, xb, wb, bias, yb);
   }
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  cudaError_t e;
+  if (reg3x3)
+    e = p.SH == 1 ? launch_kernel(depthwise3x3_kernel<1>, grid, block, 0, l.stream, a, xb, wb, bias, yb)
+                  : launch_kernel(depthwise3x3_kernel<2>, grid, block, 0, l.stream, a, xb, wb, bias, yb);
+  else if (p.KH == 3 && p.KW == 3)
+    e = launch_kernel(depthwise_fwd_kernel<3, 3>, grid, block, smem, l.stream, a, xb, wb, bias, yb);
+  else
+    e = launch_kernel(depthwise_fwd_kernel<0, 0>, grid, block, smem, l.stream, a, xb, wb, bias, yb);
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
 }  // namespace gbconv

@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "problem.h"
+#include "ptx.cuh"
 
 namespace gbconv {
 namespace {
@@ -46,6 +47,8 @@ __device__ __forceinline__ int w_off(const DirectArgs& a, int co, int cl, int kh
 template <typename T>
 __global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T* __restrict__ w,
                                   const float* __restrict__ bias, T* __restrict__ y) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   const int total = a.N * a.Cout * a.OH * a.OW;
   const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -83,6 +86,8 @@ __global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T
 template <typename T>
 __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, const T* __restrict__ w,
                                     T* __restrict__ dx) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   const int total = a.N * a.Cin * a.H * a.W;
   const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -122,6 +127,8 @@ __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, cons
 // [C_out, C_in/G, KH, KW] -> [C_out, KH, KW, C_in/G]; one thread per destination element.
 template <typename T>
 __global__ void pack_ohwi_kernel(int Cout, int cpg, int KH, int KW, const T* __restrict__ src, T* __restrict__ dst) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
   const int total = Cout * cpg * KH * KW;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int cl = i % cpg;
@@ -154,46 +161,36 @@ gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, 
                                 const Launch& l) {
   const DirectArgs a = make_args(p);
   const int threads = 256, blocks = grid_for(p.y_elems(), threads, l.num_sms);
-  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
-  if (p.bf16)
-    direct_fwd_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-        a, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), bias,
-        static_cast<__nv_bfloat16*>(y));
-  else
-    direct_fwd_kernel<float><<<blocks, threads, 0, s>>>(a, static_cast<const float*>(x),
-                                                        static_cast<const float*>(w), bias, static_cast<float*>(y));
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  const cudaError_t e =
+      p.bf16 ? launch_kernel(direct_fwd_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, a,
+                             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), bias,
+                             static_cast<__nv_bfloat16*>(y))
+             : launch_kernel(direct_fwd_kernel<float>, dim3(blocks), dim3(threads), 0, l.stream, a,
+                             static_cast<const float*>(x), static_cast<const float*>(w), bias, static_cast<float*>(y));
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
 gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
   const DirectArgs a = make_args(p);
   const int threads = 256, blocks = grid_for(p.x_elems(), threads, l.num_sms);
-  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
-  if (p.bf16)
-    direct_dgrad_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-        a, static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(w),
-        static_cast<__nv_bfloat16*>(dx));
-  else
-    direct_dgrad_kernel<float><<<blocks, threads, 0, s>>>(a, static_cast<const float*>(dy),
-                                                          static_cast<const float*>(w), static_cast<float*>(dx));
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  const cudaError_t e =
+      p.bf16 ? launch_kernel(direct_dgrad_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, a,
+                             static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(w),
+                             static_cast<__nv_bfloat16*>(dx))
+             : launch_kernel(direct_dgrad_kernel<float>, dim3(blocks), dim3(threads), 0, l.stream, a,
+                             static_cast<const float*>(dy), static_cast<const float*>(w), static_cast<float*>(dx));
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
 gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_ohwi, const Launch& l) {
   const int threads = 256, blocks = grid_for(p.w_elems(), threads, l.num_sms);
-  cudaStream_t s = static_cast<cudaStream_t>(l.stream);
   const int Cout = int(p.Cout), cpg = int(p.cpg()), KH = int(p.KH), KW = int(p.KW);
-  if (p.bf16)
-    pack_ohwi_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(Cout, cpg, KH, KW,
-                                                               static_cast<const __nv_bfloat16*>(w_oihw),
-                                                               static_cast<__nv_bfloat16*>(w_ohwi));
-  else
-    pack_ohwi_kernel<float><<<blocks, threads, 0, s>>>(Cout, cpg, KH, KW, static_cast<const float*>(w_oihw),
-                                                       static_cast<float*>(w_ohwi));
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  const cudaError_t e =
+      p.bf16 ? launch_kernel(pack_ohwi_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, Cout, cpg, KH,
+                             KW, static_cast<const __nv_bfloat16*>(w_oihw), static_cast<__nv_bfloat16*>(w_ohwi))
+             : launch_kernel(pack_ohwi_kernel<float>, dim3(blocks), dim3(threads), 0, l.stream, Cout, cpg, KH, KW,
+                             static_cast<const float*>(w_oihw), static_cast<float*>(w_ohwi));
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
 }  // namespace gbconv

@@ -211,6 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Global memory is touched only after the previous kernel on the stream has finished; the next
+  // kernel may start its prologue now (this CTA already holds its TMEM).
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -677,9 +681,9 @@ gbconv_status run(const Plan& pl, const Launch& l) {
       return GBCONV_ECUDA;
     done[dev].store(uint64_t(kSmemLimit), std::memory_order_release);
   }
-  kern<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(l.stream)>>>(pl.maps, pl.a);
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  return launch_kernel(kern, dim3(pl.grid), dim3(kThreads), pl.smem, l.stream, pl.maps, pl.a) == cudaSuccess
+             ? GBCONV_OK
+             : GBCONV_ECUDA;
 }
 
 template <bool DGRAD>

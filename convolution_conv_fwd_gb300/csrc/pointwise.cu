@@ -88,6 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Global memory is touched only after the previous kernel on the stream has finished; the next
+  // kernel may start its prologue now (this CTA already holds its TMEM).
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   if (warp == 5) {
     // ------------------------------------------------------------ TMA producer
@@ -252,9 +256,8 @@ gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a,
       return GBCONV_ECUDA;
     done[dev].store(uint64_t(smem), std::memory_order_release);
   }
-  kern<<<grid, kThreads, smem, static_cast<cudaStream_t>(l.stream)>>>(ta, tb, a);
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, l.stream, ta, tb, a) == cudaSuccess ? GBCONV_OK
+                                                                                                   : GBCONV_ECUDA;
 }
 
 }  // namespace

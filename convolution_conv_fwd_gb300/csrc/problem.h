@@ -2,7 +2,10 @@
 // launchers.  A 1-D convolution is carried as a 2-D one with H = KH = 1.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
+#include <utility>
 
 #include "../../include/gbconv.h"
 
@@ -57,5 +60,28 @@ gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void
 
 // Counts one enqueued kernel.
 void note_launch();
+
+// Enqueues `kern` with programmatic stream serialization: the launch may begin
+// (prologue: barrier init, TMEM allocation, table staging) while the previous
+// kernel on the stream drains.  Every kernel of this library calls
+// ptx::grid_dep_wait() before its first global-memory access, so results are
+// the same as with plain stream order.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, void* stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  note_launch();
+  return e;
+}
 
 }  // namespace gbconv

@@ -236,5 +236,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running; grid_dep_wait() blocks the calling thread until that kernel has
+// completed and its memory writes are visible, so every thread runs it before
+// its first global-memory access.  grid_dep_launch() lets the next such kernel
+// on the stream start its own prologue early.  Both are no-ops in a kernel
+// launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace ptx
 }  // namespace gbconv
