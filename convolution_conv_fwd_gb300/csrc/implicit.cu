@@ -106,6 +106,15 @@ struct Item {
   int phase, n, m, ntile;
 };
 
+// Item of round r for this CTA.  Items are numbered heaviest phase first; even rounds hand them
+// out in CTA order and odd rounds in reverse, so the CTAs that took the heaviest items in one
+// round take the lightest in the next (-1 once the items run out).
+__device__ __forceinline__ int round_item(int r, int total) {
+  const int g = int(gridDim.x), c = int(blockIdx.x);
+  const int item = r * g + ((r & 1) ? g - 1 - c : c);
+  return item < total ? item : -1;
+}
+
 __device__ __forceinline__ Item decode_item(const PhaseHdr* ph, int nphase, int n_tiles, int item) {
   int p = 0;
   while (p + 1 < nphase && item >= ph[p + 1].item0) ++p;
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
-      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+      for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0; item = round_item(++r, a.total_items)) {
         const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
         const PhaseHdr& ph = phase_s[it.phase];
         if (ph.ntaps == 0) continue;
@@ -274,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, a.status, 2u);
       int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
-      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x, ++iter) {
+      for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0;
+           item = round_item(++r, a.total_items), ++iter) {
         const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
         const PhaseHdr& ph = phase_s[it.phase];
         const int buf = iter & 1;
@@ -360,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage0 = ptx::smem_addr(stage_base + quad * 32 * kPitch);
     int sbuf = 0;  // staging block used next
     int iter = 0;
-    for (int item = blockIdx.x; item < a.total_items; item += gridDim.x, ++iter) {
+    for (int r = 0, item = round_item(0, a.total_items); item >= 0; item = round_item(++r, a.total_items), ++iter) {
       const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
       const PhaseHdr& ph = phase_s[it.phase];
       const int buf = iter & 1;
