@@ -1,17 +1,17 @@
 """Benchmark: the convolution hot path on GB300, one JSON line on stdout.
 
-One step = one pass of the whole hot path: each of the five workloads
-(conv1d fp32 NCL, 1x1 NHWC bf16, dense 3x3 NHWC bf16, depthwise 3x3 stride-2
-NHWC bf16, 3x3 stride-2 dgrad NHWC bf16) is run through the C ABI on inputs
-resident in HBM, as one group of back-to-back launches per workload: one
-launch per copy of its operands.  The copies of a workload together exceed
-2.5x L2, so every launch reads inputs that have been evicted since their last
-use (inputs larger than L2; no flush kernel runs between launches).  CUDA
-events sit between the groups on the launching stream; a kernel's time is its
-group's time over its launch count.  ``value`` is the step's aggregate
-TFLOP/s (algorithmic flops of all launches / step time); per-workload TFLOP/s,
-GB/s and roofline fractions are in ``per_config``; ``roofline`` describes the
-kernel with the longest launch.
+One step = 16 passes of the whole hot path over 16 batches: each of the five
+workloads (conv1d fp32 NCL, 1x1 NHWC bf16, dense 3x3 NHWC bf16, depthwise 3x3
+stride-2 NHWC bf16, 3x3 stride-2 dgrad NHWC bf16) is run through the C ABI on
+each of 16 copies of its operands, resident in HBM, as one group of 16
+back-to-back launches per workload.  The copies of each workload but the tiny
+conv1d one together exceed 2.5x L2, so every launch reads inputs that have been
+evicted since their last use (inputs larger than L2; no flush kernel runs
+between launches).  CUDA events sit between the groups on the launching
+stream; a kernel's time is its group's time over 16.  ``value`` is the step's
+aggregate TFLOP/s (algorithmic flops of all launches / step time);
+per-workload TFLOP/s, GB/s and roofline fractions are in ``per_config``;
+``roofline`` describes the kernel with the largest share of the step.
 
 ``--impl reference`` times the FP64 CPU oracle instead (the reference arm: a
 bounded sample of every workload per step, on the host cores).
@@ -41,8 +41,8 @@ from synth.workloads import WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "conv fwd/dgrad TFLOP/s (or GB/s) per config and % of roofline on 1 GB300"
 UNIT = "TFLOP/s"
-MAX_COPIES = 16  # operand copies per workload (tiny workloads stay L2 resident at this cap)
-WORKLOAD_NAME = "conv hot path: 5 workloads per step (conv1d f32, 1x1, dense 3x3, depthwise 3x3 s2, dgrad 3x3 s2)"
+COPIES = 16  # operand copies per workload = passes over the hot path per step
+WORKLOAD_NAME = "conv hot path: 5 workloads x 16 batches per step (conv1d f32, 1x1, dense 3x3, depthwise 3x3 s2, dgrad 3x3 s2)"
 
 
 def peaks():
@@ -141,19 +141,20 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
-def traffic_record(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+def traffic_record(kernel_file: str, workload: str):
+    """DRAM bytes per launch of a workload's kernel from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     src = os.path.join(ROOT, "convolution_conv_fwd_gb300", "csrc", kernel_file)
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
-        # | kernel file | source sha256[:16] | dram bytes per launch | ...
+        # | workload | kernel file | source sha256[:16] | dram bytes per launch | ...
         parts = [p.strip() for p in line.split("|")]
-        if len(parts) > 4 and parts[1] == kernel_file and parts[2] == digest:
+        if len(parts) > 5 and parts[1] == workload and parts[2] == kernel_file and parts[3] == digest:
             try:
-                return float(parts[3])
+                return float(parts[4])
             except ValueError:
                 return None
     return None
@@ -193,16 +194,17 @@ def run_gpu(args, rank, world, local_rank):
         op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
         family = gb.gbconv_select(d, op)
         flops, nbytes = work(wl)
-        # Copies of every operand that together exceed 2.5x L2: a launch's inputs were last touched
-        # a full rotation earlier, with more than 2x L2 of other traffic in between, so every launch
-        # reads them from HBM with no flush kernel (and no flush write-back) between launches.
+        # COPIES copies of every operand: a launch's inputs were last touched a full rotation
+        # earlier, with more than 2x L2 of other traffic in between (every workload but the tiny
+        # conv1d one has COPIES x its footprint > 2.5x L2), so every launch reads them from HBM
+        # with no flush kernel (and no flush write-back) between launches.
         per_copy = (src.numel() * src.element_size() + w.numel() * w.element_size()
                     + int(np.prod(out_shape)) * src.element_size() + (0 if b is None else b.numel() * 4))
-        reps = int(min(MAX_COPIES, max(2, -(-int(2.5 * l2) // per_copy))))
+        reps = COPIES
         copies = [(src.clone(), w.clone(), None if b is None else b.clone(), torch.empty(out_shape, dtype=dt, device=dev))
                   for _ in range(reps)]
         cases.append(dict(wl=wl, d=d, copies=copies, family=family, flops=flops, bytes=nbytes, host=inp,
-                          l2_resident=reps * per_copy < 2 * l2))
+                          l2_resident=reps * per_copy < int(2.5 * l2)))
 
     def launch(c, k):
         s = stream.cuda_stream
@@ -302,14 +304,14 @@ def run_gpu(args, rank, world, local_rank):
                     "roofline_frac": round(t_roof / (ms * 1e-3), 4),
                     "launches_per_step": len(c["copies"]),
                     "inputs": "L2 resident (too small to exceed L2)" if c["l2_resident"] else "from HBM"})
-    dom = max(range(len(cases)), key=lambda i: per_kernel_ms[i])
+    dom = max(range(len(cases)), key=lambda i: group_ms[i])
     dc, dms = cases[dom], per_kernel_ms[dom]
     if per[dom]["bound"] == "hbm":
         achieved, peak, unit = dc["bytes"] / (dms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = dc["flops"] / (dms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
     roof = {"bound": per[dom]["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic_record(KERNEL_FILE[dc["family"]]),
+            "frac": round(achieved / peak, 4), "traffic": traffic_record(KERNEL_FILE[dc["family"]], dc["wl"].name),
             "kernel": dc["family"], "workload": dc["wl"].name,
             "algorithmic_bytes": dc["bytes"], "algorithmic_flops": dc["flops"],
             "peak_source": pk["source"] + " (burst)"}
