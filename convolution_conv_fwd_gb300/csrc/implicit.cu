@@ -378,6 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int n0 = it.ntile * BN;
       const bool has_bias = a.bias != nullptr;
+      // The phase geometry in registers: read from shared memory inside the store loop, every
+      // field would be re-read after each staging load (those are asm with memory clobbers).
+      const int ph_R = ph.R, ph_OWv = ph.OWv, ph_P = ph.P, ph_ntaps = ph.ntaps;
+      const int row_base = it.n * a.Ho + ph.out_ph, ph_sh = ph.out_sh, ph_sw = ph.out_sw, ph_pw = ph.out_pw;
+      const int Wo = a.Wo, Cn = a.Cn;
+      bf16* const out = a.out;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           constexpr int kChunks = kG / 64;  // 32-column TMEM loads per warp per group
           uint32_t v[kChunks][32];
           const int c0 = g * kG + half * (kG / 2);
-          if (ph.ntaps > 0) {
+          if (ph_ntaps > 0) {
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
               ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * NSUB * BN + s * BN + c0 + ch * 32), v[ch]);
@@ -432,25 +438,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tp = half * 32 + lane;
             const int part = tp % kParts;
             const int co = n0 + g * kG + part * 8;
-            if (co < a.Cn) {
+            if (co < Cn) {
               int row = tp / kParts;
               const int q = qbase + row;
-              int r = q / ph.P, colv = q - r * ph.P;
+              int r = q / ph_P, colv = q - r * ph_P;
+              // All staged pieces are read first, then stored: one shared-memory round trip per
+              // thread instead of one per store.  (The loads need no memory clobber: the pair
+              // barrier above already orders them after the staging writes.)
+              constexpr int kIters = 32 / kRowStep;
+              uint4 val[kIters];
+              int pix[kIters];
 #pragma unroll
-              for (int i = 0; i < 32 / kRowStep; ++i) {
-                if (r < ph.R && colv < ph.OWv) {
-                  uint4 val;
-                  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                               : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                               : "r"(stage_s + uint32_t(row * kPitch + part * 16))
-                               : "memory");
-                  const int pix = (it.n * a.Ho + r * ph.out_sh + ph.out_ph) * a.Wo + colv * ph.out_sw + ph.out_pw;
-                  *reinterpret_cast<uint4*>(a.out + size_t(pix) * a.Cn + co) = val;
-                }
+              for (int i = 0; i < kIters; ++i) {
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
+                             : "r"(stage_s + uint32_t(row * kPitch + part * 16)));
+                pix[i] = (r < ph_R && colv < ph_OWv) ? (row_base + r * ph_sh) * Wo + colv * ph_sw + ph_pw : -1;
                 row += kRowStep;
                 colv += kRowStep;
-                while (colv >= ph.P) { colv -= ph.P; ++r; }
+                while (colv >= ph_P) { colv -= ph_P; ++r; }
               }
+#pragma unroll
+              for (int i = 0; i < kIters; ++i)
+                if (pix[i] >= 0) *reinterpret_cast<uint4*>(out + size_t(pix[i]) * Cn + co) = val[i];
             }
           }
           if (a.stage_bufs == 1) asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");

@@ -182,16 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kRowStep = 32 / kParts;  // rows per warp pass
       const int part = lane % kParts;
       const int row0 = tile * kBM + warp * 32;
-#pragma unroll 4
-      for (int r = lane / kParts; r < 32; r += kRowStep) {
-        if (row0 + r < a.M) {
-          uint4 val;
-          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                       : "r"(stage_s + uint32_t(r * kPitch + part * 16))
-                       : "memory");
-          *reinterpret_cast<uint4*>(a.out + size_t(row0 + r) * a.Cout + part * 8) = val;
-        }
+      // All staged pieces are read first, then stored (the __syncwarp above orders the loads
+      // after this warp's staging writes).
+      constexpr int kIters = 32 / kRowStep;
+      uint4 val[kIters];
+      asm volatile("" ::: "memory");  // keeps the loads below after the __syncwarp
+#pragma unroll
+      for (int i = 0; i < kIters; ++i)
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
+                     : "r"(stage_s + uint32_t((lane / kParts + i * kRowStep) * kPitch + part * 16)));
+#pragma unroll
+      for (int i = 0; i < kIters; ++i) {
+        const int r = lane / kParts + i * kRowStep;
+        if (row0 + r < a.M) *reinterpret_cast<uint4*>(a.out + size_t(row0 + r) * a.Cout + part * 8) = val[i];
       }
       __syncwarp();
     }
