@@ -75,7 +75,6 @@ struct PhaseHdr {
   int a_bytes;  // bytes of one halo box (64 channels x P x bh)
   int tiles;    // m-tiles per image
   int item0;    // first work item of this phase
-  int pitem0;   // first pair item of this phase (CTA-pair mode)
 };
 
 struct Phase : PhaseHdr {
@@ -95,14 +94,12 @@ struct Args {
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
   int nphase, total_items;
-  int total_pitems;   // CTA-pair mode: work items of a CTA pair (two m-tiles sharing every weight tile)
   Phase ph[kMaxPhases];
 };
 
 struct Maps {
   CUtensorMap a[kMaxPhases];  // gathered activations, one box shape per phase
   CUtensorMap b;              // weight viewed as [C_out][KH*KW][C_in]
-  CUtensorMap b_half;         // CTA-pair mode: half a weight tile (each CTA of a pair loads one half for both)
 };
 
 struct Item {
@@ -131,50 +128,6 @@ __device__ __forceinline__ Item decode_item(const PhaseHdr* ph, int nphase, int 
   return it;
 }
 
-// One unit of a CTA's work: an m-tile x n-tile item, or (CTA-pair mode) this CTA's half of a
-// pair item, whose two m-tiles share every weight tile.
-struct Work {
-  int rot;  // sets the k-block / tap rotation; equal on both CTAs of a pair
-  int phase, n, m, ntile;
-  bool real;  // false: pair partner stand-in (no m-tile left): loads and releases its weight halves only
-};
-
-// The work of round r for this CTA; false once there is none.  Without pairs it is round_item's
-// item.  With pairs the rounds deal pair items to clusters the same way (snake order), and CTA
-// rank k of the pair takes m-tile 2*pp + k of the pair item's (phase, n-tile) run.
-template <bool PAIR>
-__device__ __forceinline__ bool next_work(const PhaseHdr* ph, const Args& a, int r, Work& w) {
-  if (!PAIR) {
-    const int item = round_item(r, a.total_items);
-    if (item < 0) return false;
-    const Item it = decode_item(ph, a.nphase, a.n_tiles, item);
-    w.rot = item;
-    w.phase = it.phase;
-    w.n = it.n;
-    w.m = it.m;
-    w.ntile = it.ntile;
-    w.real = true;
-    return true;
-  }
-  const int g = int(gridDim.x) >> 1, c = int(blockIdx.x) >> 1;
-  const int pi = r * g + ((r & 1) ? g - 1 - c : c);
-  if (pi >= a.total_pitems) return false;
-  int p = 0;
-  while (p + 1 < a.nphase && pi >= ph[p + 1].pitem0) ++p;
-  const int npos = a.N * ph[p].tiles, npairs = (npos + 1) >> 1;
-  const int local = pi - ph[p].pitem0;
-  const int ntile = local / npairs;
-  const int pos = 2 * (local - ntile * npairs) + int(blockIdx.x & 1);
-  w.rot = pi;
-  w.phase = p;
-  w.ntile = ntile;
-  w.real = pos < npos;
-  const int posc = w.real ? pos : pos - 1;  // a stand-in keeps an in-range tile (never stored)
-  w.n = posc / ph[p].tiles;
-  w.m = posc - w.n * ph[p].tiles;
-  return true;
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                             int z) {
   asm volatile(
@@ -193,17 +146,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// As tma_load_4d, but the box lands at the same shared-memory offset in every CTA of the cluster
-// named in `cta_mask`, and each of them gets the transaction bytes on its barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_4d_multicast(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                                      int y, int z, int w, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "h"(cta_mask)
-      : "memory");
-}
-
 // K-major operand, 128-byte swizzle, 8-row atoms of 1024 bytes.
 __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) { return ptx::desc_kmajor_sw128(saddr); }
 
@@ -218,15 +160,9 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t saddr, uint32_t 
   return d;
 }
 
-// PAIR: the grid is made of 2-CTA clusters; both CTAs of a pair walk the same weight tiles (one
-// pair item = two m-tiles) and each loads half of every tile for both by TMA multicast, so each
-// SM's TMA engine moves half the weight bytes.  A weight stage is then full once both halves
-// landed (16 KB of transaction bytes on each CTA's barrier) and free once both CTAs' MMAs are
-// done with it (two arrivals, one tcgen05.commit multicast from each CTA).
-template <int BN, int NSUB, bool DGRAD, bool BRES, bool PAIR>
+template <int BN, int NSUB, bool DGRAD, bool BRES>
 __global__ void __launch_bounds__(kThreads, 1)
     implicit_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
-  static_assert(!PAIR || (DGRAD && !BRES && BN % 128 == 0), "pairs split dgrad weight tiles by 64-wide atoms");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Swizzled TMA destinations and operands sit on 1024-byte boundaries.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,13 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.sa; ++i) { ptx::mbar_init(fullA + i, 1); ptx::mbar_init(emptyA + i, 1); }
-    for (int i = 0; i < a.sb; ++i) { ptx::mbar_init(fullB + i, 1); ptx::mbar_init(emptyB + i, PAIR ? 2 : 1); }
+    for (int i = 0; i < a.sb; ++i) { ptx::mbar_init(fullB + i, 1); ptx::mbar_init(emptyB + i, 1); }
     for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, kEpiWarps * 32); }
     ptx::mbar_init(bres, 1);
     ptx::mbar_init(fin, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
-    if (PAIR) ptx::fence_mbar_init_cluster();
   }
   if (warp < kEpiWarps) {
     if (threadIdx.x < a.nphase) phase_s[threadIdx.x] = a.ph[threadIdx.x];
@@ -283,8 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // The partner's barriers must be initialised before a multicast load or commit reaches them.
-  if (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Global memory is touched only after the previous kernel on the stream has finished; the next
@@ -297,14 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int p = 0; p < a.nphase; ++p) ptx::prefetch_tmap(&maps.a[p]);
       ptx::prefetch_tmap(&maps.b);
-      if (PAIR) ptx::prefetch_tmap(&maps.b_half);
       auto load_b = [&](uint8_t* dst, uint64_t* bar, int wt, int kb, int n0) {
         const uint32_t d = ptx::smem_addr(dst);
-        if (PAIR) {  // this CTA's half of the atoms, landing in both CTAs of the pair
-          const int k = int(blockIdx.x & 1);
-          tma_load_4d_multicast(d + k * (BN / 2) * 128, &maps.b_half, bar, 0, kb * kKB, n0 / 64 + k * (BN / 128), wt,
-                                uint16_t(3));
-        } else if (DGRAD) {  // MN-major: BN/64 atoms of [64 output channels][64 input channels]
+        if (DGRAD) {  // MN-major: BN/64 atoms of [64 output channels][64 input channels]
           if (a.b4d) {
             tma_load_4d(d, &maps.b, bar, 0, kb * kKB, n0 / 64, wt);
           } else {
@@ -322,22 +250,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
-      Work it;
-      for (int r = 0; ok && next_work<PAIR>(phase_s, a, r, it); ++r) {
+      for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0; item = round_item(++r, a.total_items)) {
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
         const PhaseHdr& ph = phase_s[it.phase];
         if (ph.ntaps == 0) continue;
         const int ra = (it.m * 128 * NSUB) / ph.P;
-        const int kb_rot = it.rot % a.kb_count, t_rot = it.rot % ph.ntaps;
+        const int kb_rot = item % a.kb_count, t_rot = item % ph.ntaps;
         const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
         for (int kbi = 0; ok && kbi < a.kb_count; ++kbi) {
           const int kb = kbi + kb_rot < a.kb_count ? kbi + kb_rot : kbi + kb_rot - a.kb_count;
-          if (it.real) {  // a pair stand-in loads no activations
-            if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
-            ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
-            tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                        kb * kKB, ph.cmin, ra + ph.rmin, it.n);
-            if (++sa == a.sa) { sa = 0; pa ^= 1; }
-          }
+          if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
+          ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
+          tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                      kb * kKB, ph.cmin, ra + ph.rmin, it.n);
+          if (++sa == a.sa) { sa = 0; pa ^= 1; }
           if (!BRES) {
             for (int ti = 0, t = t_rot; ok && ti < ph.ntaps; ++ti, t = (t + 1 == ph.ntaps ? 0 : t + 1)) {
               if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
@@ -355,21 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, a.status, 2u);
-      int sa = 0, sb = 0, iter = 0;  // iter counts this CTA's accumulators (real work only)
+      int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
-      Work it;
-      for (int r = 0; ok && next_work<PAIR>(phase_s, a, r, it); ++r) {
+      for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0;
+           item = round_item(++r, a.total_items), ++iter) {
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
         const PhaseHdr& ph = phase_s[it.phase];
-        if (PAIR && !it.real) {
-          // Pair stand-in: no m-tile of its own, but the partner needs every weight stage of the
-          // pair item released by both CTAs.
-          for (int k = 0; ok && k < ph.ntaps * a.kb_count; ++k) {
-            if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
-            ptx::mma_commit_multicast(emptyB + sb, uint16_t(3));
-            if (++sb == a.sb) { sb = 0; pb ^= 1; }
-          }
-          continue;
-        }
         const int buf = iter & 1;
         if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, a.status, 2u))) break;
         ptx::tc_fence_after();
@@ -383,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // k-blocks and taps are walked in an order rotated by the item index (the producer
           // walks the same order): CTAs working at the same time then read different weight
           // tiles, which spreads the L2 traffic of the streamed weights.
-          const int t_rot = it.rot % ntaps;
+          const int t_rot = item % ntaps;
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
             // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
             // orders the async-proxy writes before the async-proxy MMA reads.
@@ -418,10 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      b_hi, kIdesc, j == 0 ? first : 1u);
               }
               if (!BRES) {
-                if (PAIR)
-                  ptx::mma_commit_multicast(emptyB + sb, uint16_t(3));
-                else
-                  ptx::mma_commit(emptyB + sb);
+                ptx::mma_commit(emptyB + sb);
                 if (++sb == a.sb) { sb = 0; pb ^= 1; }
               }
               tc = tn;
@@ -433,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ptx::mma_commit(tfull + buf);
-        ++iter;
       }
       ptx::mma_commit(fin);
       ptx::mbar_wait(fin, 0, abort_flag, a.status, 2u);
@@ -457,9 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage0 = ptx::smem_addr(stage_base + quad * 32 * kPitch);
     int sbuf = 0;  // staging block used next
     int iter = 0;
-    Work it;
-    for (int r = 0; next_work<PAIR>(phase_s, a, r, it); ++r) {
-      if (!it.real) continue;
+    for (int r = 0, item = round_item(0, a.total_items); item >= 0; item = round_item(++r, a.total_items), ++iter) {
+      const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
       const PhaseHdr& ph = phase_s[it.phase];
       const int buf = iter & 1;
       if (!ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u)) break;
@@ -556,14 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty + buf);
-      ++iter;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  // Neither CTA of a pair leaves while the other may still multicast into it or commit to it.
-  if (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
@@ -575,7 +484,6 @@ struct Plan {
   Maps maps;
   int bn, nsub;
   bool bres, dgrad;
-  bool pair;  // CTA pairs share the weight tiles (2-CTA clusters, multicast halves)
   size_t smem;
   int grid;
   // geometry kept for the tensor maps
@@ -717,13 +625,6 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   }
   a.nphase = nph;
   a.total_items = item;
-  // Pair items: per phase and n-tile, m-tiles 2j and 2j+1 (an odd last one gets a stand-in partner).
-  int pitem = 0;
-  for (int i = 0; i < nph; ++i) {
-    a.ph[i].pitem0 = pitem;
-    pitem += a.n_tiles * ((a.N * a.ph[i].tiles + 1) / 2);
-  }
-  a.total_pitems = pitem;
   a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
@@ -750,7 +651,6 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
 
 bool encode_maps(Plan& pl, const void* in, const void* w) {
   pl.a.b4d = 0;
-  pl.pair = false;
   auto fn = encode_fn();
   if (!fn) return false;
   const Args& a = pl.a;
@@ -778,16 +678,7 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
                fn(&pl.maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    if (pl.a.b4d) {
-      // CTA pairs: each CTA loads BN/128 of the BN/64 atoms of every weight tile for both.
-      if (!pl.bres && pl.bn % 128 == 0) {
-        cuuint32_t half_box[4] = {64, 64, cuuint32_t(pl.bn / 128), 1};
-        pl.pair = fn(&pl.maps.b_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides,
-                     half_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-      }
-      return true;
-    }
+    if (pl.a.b4d) return true;
   }
   cuuint64_t dims[3] = {cuuint64_t(pl.Cw), cuuint64_t(a.T), cuuint64_t(Cout)};
   cuuint64_t strides[2] = {cuuint64_t(pl.Cw) * 2, cuuint64_t(a.T) * pl.Cw * 2};
@@ -798,39 +689,9 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters of two that fit on the device at once with this shared-memory size (0: none), cached.
-template <typename K>
-int pair_clusters(K kern, size_t smem, int dev) {
-  static std::mutex mu;
-  static int cached_dev = -1, cached_n = 0;
-  static size_t cached_smem = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cached_dev == dev && cached_smem == smem) return cached_n;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  cached_dev = dev;
-  cached_smem = smem;
-  cached_n = n;
-  return n;
-}
-
-template <int BN, int NSUB, bool DGRAD, bool BRES, bool PAIR = false>
+template <int BN, int NSUB, bool DGRAD, bool BRES>
 gbconv_status run(const Plan& pl, const Launch& l) {
-  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES, PAIR>;
+  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES>;
   // The shared-memory opt-in is a per-device function attribute: raise it once per device.
   static std::atomic<uint64_t> done[64];
   int dev = 0;
@@ -839,14 +700,6 @@ gbconv_status run(const Plan& pl, const Launch& l) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemLimit)) != cudaSuccess)
       return GBCONV_ECUDA;
     done[dev].store(uint64_t(kSmemLimit), std::memory_order_release);
-  }
-  if (PAIR) {
-    const int clusters = std::min(pair_clusters(kern, pl.smem, dev), std::min(l.num_sms / 2, pl.a.total_pitems));
-    if (clusters < 1) return run<BN, NSUB, DGRAD, BRES, false>(pl, l);  // no two SMs for a pair
-    return launch_kernel_clustered(kern, dim3(2 * clusters), dim3(kThreads), pl.smem, l.stream, 2, pl.maps, pl.a) ==
-                   cudaSuccess
-               ? GBCONV_OK
-               : GBCONV_ECUDA;
   }
   return launch_kernel(kern, dim3(pl.grid), dim3(kThreads), pl.smem, l.stream, pl.maps, pl.a) == cudaSuccess
              ? GBCONV_OK
@@ -862,10 +715,6 @@ gbconv_status dispatch(const Plan& pl, const Launch& l) {
       case 128: return run<128, 2, false, true>(pl, l);
       default: return run<64, 2, false, true>(pl, l);
     }
-  }
-  if (DGRAD && pl.pair) {
-    if (pl.bn == 256) return run<256, 1, true, false, true>(pl, l);
-    if (pl.bn == 128) return run<128, 2, true, false, true>(pl, l);
   }
   switch (pl.bn) {
     case 256: return run<256, 1, DGRAD, false>(pl, l);

@@ -66,33 +66,22 @@ void note_launch();
 // kernel on the stream drains.  Every kernel of this library calls
 // ptx::grid_dep_wait() before its first global-memory access, so results are
 // the same as with plain stream order.
-// `cluster_x` > 1 launches clusters of that many consecutive CTAs (grid.x a multiple of it).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_clustered(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, void* stream,
-                                    int cluster_x, Args&&... args) {
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, void* stream,
+                          Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = unsigned(cluster_x);
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
   note_launch();
   return e;
-}
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, void* stream,
-                          Args&&... args) {
-  return launch_kernel_clustered(kern, grid, block, smem, stream, 1, std::forward<Args>(args)...);
 }
 
 }  // namespace gbconv

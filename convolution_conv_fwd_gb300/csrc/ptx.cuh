@@ -178,34 +178,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// As mma_commit, but the arrive goes to the barrier at the same shared-memory offset in every
-// CTA of the cluster named in `cta_mask` (bit i = cluster rank i).
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// ------------------------------------------------------------------ clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Makes this CTA's barrier initialisation visible to the other CTAs of the cluster.
-__device__ __forceinline__ void fence_mbar_init_cluster() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Every thread of every CTA of the cluster arrives, then waits for all of them.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
