@@ -108,6 +108,12 @@ SMALL = [
     (shape_kw(n=1, in_size=(7, 7), c_in=96, c_out=48, dil=(2, 2), pad=(1, 1)), "dgrad", "dgrad"),
     (shape_kw(n=2, in_size=(9, 9), c_in=72, c_out=40, stride=(2, 2)), "dgrad", "dgrad"),
     (shape_kw(n=1, in_size=(8, 6), c_in=192, c_out=64), "dgrad", "dgrad"),
+    # wider dgrad: an odd m-tile count per phase, several rounds, BN = 256 with two n-tiles, a ragged
+    # output-channel tail, a 2x2 kernel at stride 2 (four one-tap phases)
+    (shape_kw(n=1, in_size=(11, 13), c_in=128, c_out=64, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=3, in_size=(40, 37), c_in=128, c_out=72, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(12, 12), c_in=512, c_out=64, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=2, in_size=(9, 10), c_in=256, c_out=136, k=(2, 2), pad=(0, 0), stride=(2, 2)), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
