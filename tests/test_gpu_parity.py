@@ -85,6 +85,8 @@ SMALL = [
     (shape_kw(n=1, in_size=(6, 7), c_in=64, c_out=192, bias=True), "fwd", "implicit"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
+    # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
+    (shape_kw(n=2, in_size=(110, 89), c_in=64, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(13, 13), c_in=72, c_out=128, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
     (shape_kw(n=3, in_size=(10, 10), c_in=64, c_out=256, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(5, 9), c_in=8, c_out=32, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
