@@ -161,7 +161,8 @@ def traffic_record(kernel_file: str, workload: str):
 
 
 KERNEL_FILE = {"direct": "direct.cu", "depthwise": "depthwise.cu", "pointwise": "pointwise.cu",
-               "implicit": "implicit.cu", "dgrad": "implicit.cu", "direct_dgrad": "direct.cu"}
+               "implicit": "implicit.cu", "dgrad": "implicit.cu", "direct_dgrad": "direct.cu",
+               "depthwise_dgrad": "depthwise.cu"}
 
 
 def run_gpu(args, rank, world, local_rank):

@@ -24,7 +24,8 @@ GBCONV_NCHW, GBCONV_NHWC = 0, 1
 GBCONV_W_OIHW, GBCONV_W_OHWI = 0, 1
 GBCONV_F32, GBCONV_BF16 = 0, 1
 # kernel families
-KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad"}
+KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad",
+           6: "depthwise_dgrad"}
 GBCONV_OP_FWD, GBCONV_OP_BWD_DATA = 0, 1
 
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",

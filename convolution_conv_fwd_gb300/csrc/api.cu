@@ -106,6 +106,7 @@ int32_t select_fwd(const Problem& p, bool aligned) {
 
 int32_t select_dgrad(const Problem& p, bool aligned) {
   if (aligned && implicit_dgrad_supported(p)) return GBCONV_K_DGRAD;
+  if (aligned && depthwise_dgrad_supported(p)) return GBCONV_K_DEPTHWISE_DGRAD;
   return GBCONV_K_DIRECT_DGRAD;
 }
 
@@ -165,8 +166,11 @@ gbconv_status gbconv_bwd_data(const gbconv_desc* desc, const void* dy, const voi
   Launch l;
   if (!device_context(&l, stream)) return GBCONV_ECUDA;
   const bool aligned = aligned16(dy) && aligned16(w) && aligned16(dx);
-  if (select_dgrad(p, aligned) == GBCONV_K_DGRAD) return launch_implicit_dgrad(p, dy, w, dx, l);
-  return launch_direct_dgrad(p, dy, w, dx, l);
+  switch (select_dgrad(p, aligned)) {
+    case GBCONV_K_DGRAD: return launch_implicit_dgrad(p, dy, w, dx, l);
+    case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(p, dy, w, dx, l);
+    default: return launch_direct_dgrad(p, dy, w, dx, l);
+  }
 }
 
 gbconv_status gbconv_pack_weight(const gbconv_desc* desc, const void* w_oihw, void* w_ohwi, void* stream) {

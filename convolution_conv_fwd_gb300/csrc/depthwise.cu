@@ -126,6 +126,153 @@ __global__ void __launch_bounds__(kThreads) depthwise_fwd_kernel(DwArgs a, const
 }
 
 
+// Depthwise input gradient (gather form, no atomics: every dx element is written once, in a
+// fixed summation order).  The transpose of the forward above, with the same thread layout:
+// each thread owns 8 channels of one dx column and walks a strip of dx rows; for dx (ih, iw) a
+// tap (kh, kw) contributes dy[(ih + PH - kh*DH) / SH, (iw + PW - kw*DW) / SW] * w[c, kh, kw] when
+// both divisions are exact and land inside dy.  teeny-kernels `src/nn/conv/conv2d.rs`,
+// `conv2d_backward` scatters the same products into dx with atomics (G = C case).
+// S_ > 0: compile-time stride S_ in both dims; 0: runtime strides.
+template <int S_>
+__global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, const __nv_bfloat16* __restrict__ dy,
+                                                                   const __nv_bfloat16* __restrict__ w,
+                                                                   __nv_bfloat16* __restrict__ dx) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
+  const int KH = a.KH, KW = a.KW, taps = KH * KW;
+  const int SH = S_ > 0 ? S_ : a.SH, SW = S_ > 0 ? S_ : a.SW;
+  extern __shared__ __align__(16) float ws[];  // [tap][channel] of this block's channels, fp32
+  const int cpb = a.cv_per_block * 8;
+  const int chunk = blockIdx.x % a.cv_chunks;
+  const int c0 = chunk * cpb;
+  for (int i = threadIdx.y * blockDim.x + threadIdx.x; i < taps * cpb; i += kThreads) {
+    const int t = i / cpb, c = i % cpb;
+    ws[t * cpb + c] = __bfloat162float(w[(c0 + c) * taps + t]);
+  }
+  __syncthreads();
+
+  const int iw = (blockIdx.x / a.cv_chunks) * blockDim.y + threadIdx.y;  // dx column
+  const int cv = threadIdx.x;
+  const int n = blockIdx.z;
+  if (iw >= a.W) return;
+  const int ih0 = blockIdx.y * a.rows_per_thread;
+  const int ih1 = min(a.H, ih0 + a.rows_per_thread);
+  const int c = c0 + cv * 8;
+  const uint4* dyv = reinterpret_cast<const uint4*>(dy);
+  uint4* dxv = reinterpret_cast<uint4*>(dx);
+  const int cvec = a.C / 8;
+  for (int ih = ih0; ih < ih1; ++ih) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int kh = 0; kh < KH; ++kh) {
+      const int nh = ih + a.PH - kh * a.DH;
+      if (nh < 0 || nh % SH != 0) continue;
+      const int oh = nh / SH;
+      if (oh >= a.OH) continue;
+      const int row = (n * a.OH + oh) * a.OW;
+      for (int kw = 0; kw < KW; ++kw) {
+        const int nw = iw + a.PW - kw * a.DW;
+        if (nw < 0 || nw % SW != 0) continue;
+        const int ow = nw / SW;
+        if (ow >= a.OW) continue;
+        float g[8];
+        unpack8(__ldg(dyv + (size_t)(row + ow) * cvec + (c >> 3)), g);
+        const float* wt = ws + (kh * KW + kw) * cpb + cv * 8;
+        const float4 w0 = *reinterpret_cast<const float4*>(wt);
+        const float4 w1 = *reinterpret_cast<const float4*>(wt + 4);
+        acc[0] = fmaf(g[0], w0.x, acc[0]);
+        acc[1] = fmaf(g[1], w0.y, acc[1]);
+        acc[2] = fmaf(g[2], w0.z, acc[2]);
+        acc[3] = fmaf(g[3], w0.w, acc[3]);
+        acc[4] = fmaf(g[4], w1.x, acc[4]);
+        acc[5] = fmaf(g[5], w1.y, acc[5]);
+        acc[6] = fmaf(g[6], w1.z, acc[6]);
+        acc[7] = fmaf(g[7], w1.w, acc[7]);
+      }
+    }
+    uint4 o;
+    o.x = pack2(acc[0], acc[1]);
+    o.y = pack2(acc[2], acc[3]);
+    o.z = pack2(acc[4], acc[5]);
+    o.w = pack2(acc[6], acc[7]);
+    dxv[(size_t)((n * a.H + ih) * a.W + iw) * cvec + (c >> 3)] = o;
+  }
+}
+
+// Depthwise dgrad for 3x3, stride 2, pad 1, dilation 1 (the common downsampling layer).  A dx
+// 2x2 block at (2r, 2c) reads exactly the dy 2x2 block at (r, c):
+//   dx[2r  ][2c  ] = dy[r][c] w11
+//   dx[2r  ][2c+1] = dy[r][c] w12 + dy[r][c+1] w10
+//   dx[2r+1][2c  ] = dy[r][c] w21 + dy[r+1][c] w01
+//   dx[2r+1][2c+1] = dy[r][c] w22 + dy[r][c+1] w20 + dy[r+1][c] w02 + dy[r+1][c+1] w00
+// (w[kh][kw]; dy outside [0,OH) x [0,OW) is zero).  Each thread owns 8 channels of one dy column
+// c and walks a strip of dy rows r, keeping row r+1's two vectors for the next step: two 16-byte
+// loads and four 16-byte stores per step, the nine weights of its channels in registers.
+__global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a, const __nv_bfloat16* __restrict__ dy,
+                                                                        const __nv_bfloat16* __restrict__ w,
+                                                                        __nv_bfloat16* __restrict__ dx) {
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
+  const int cpb = a.cv_per_block * 8;
+  const int chunk = blockIdx.x % a.cv_chunks;
+  const int oc = (blockIdx.x / a.cv_chunks) * blockDim.y + threadIdx.y;  // dy column c
+  const int ch = chunk * cpb + threadIdx.x * 8;
+  const int n = blockIdx.z;
+  if (oc >= a.OW) return;
+  float wr[9][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(ch + j) * 9 + t]);
+  const uint4* dyv = reinterpret_cast<const uint4*>(dy);
+  uint4* dxv = reinterpret_cast<uint4*>(dx);
+  const int cvec = a.C / 8, cv = ch >> 3;
+  const bool right = oc + 1 < a.OW;       // dy column c+1 exists
+  const bool col1 = 2 * oc + 1 < a.W;     // dx column 2c+1 exists
+  const int r0 = blockIdx.y * a.rows_per_thread;
+  const int r1 = min(a.OH, r0 + a.rows_per_thread);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  auto load = [&](int r, int c) -> uint4 { return __ldg(dyv + (size_t)((n * a.OH + r) * a.OW + c) * cvec + cv); };
+  uint4 cur0 = load(r0, oc), cur1 = right ? load(r0, oc + 1) : zero;
+  for (int r = r0; r < r1; ++r) {
+    const bool down = r + 1 < a.OH;
+    const uint4 nxt0 = down ? load(r + 1, oc) : zero;
+    const uint4 nxt1 = (down && right) ? load(r + 1, oc + 1) : zero;
+    float a0[8], a1[8], b0[8], b1[8];  // dy[r][c], dy[r][c+1], dy[r+1][c], dy[r+1][c+1]
+    unpack8(cur0, a0);
+    unpack8(cur1, a1);
+    unpack8(nxt0, b0);
+    unpack8(nxt1, b1);
+    float o00[8], o01[8], o10[8], o11[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o00[j] = a0[j] * wr[4][j];
+      o01[j] = fmaf(a1[j], wr[3][j], a0[j] * wr[5][j]);
+      o10[j] = fmaf(b0[j], wr[1][j], a0[j] * wr[7][j]);
+      o11[j] = fmaf(b1[j], wr[0][j], fmaf(b0[j], wr[2][j], fmaf(a1[j], wr[6][j], a0[j] * wr[8][j])));
+    }
+    auto pack = [](const float (&f)[8]) {
+      uint4 o;
+      o.x = pack2(f[0], f[1]);
+      o.y = pack2(f[2], f[3]);
+      o.z = pack2(f[4], f[5]);
+      o.w = pack2(f[6], f[7]);
+      return o;
+    };
+    const size_t row0 = (size_t)(n * a.H + 2 * r) * a.W;
+    dxv[(row0 + 2 * oc) * cvec + cv] = pack(o00);
+    if (col1) dxv[(row0 + 2 * oc + 1) * cvec + cv] = pack(o01);
+    if (2 * r + 1 < a.H) {
+      const size_t row1 = row0 + a.W;
+      dxv[(row1 + 2 * oc) * cvec + cv] = pack(o10);
+      if (col1) dxv[(row1 + 2 * oc + 1) * cvec + cv] = pack(o11);
+    }
+    cur0 = nxt0;
+    cur1 = nxt1;
+  }
+}
+
 // 3x3, dilation 1, stride S in {1, 2}: the nine weights of the thread's 8
 // channels live in registers, and each input row a thread loads is kept in
 // registers for every output row of its strip that reads it (rows overlap by
@@ -435,6 +582,54 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
     e = launch_kernel(depthwise_fwd_kernel<3, 3>, grid, block, smem, l.stream, a, xb, wb, bias, yb);
   else
     e = launch_kernel(depthwise_fwd_kernel<0, 0>, grid, block, smem, l.stream, a, xb, wb, bias, yb);
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+bool depthwise_dgrad_supported(const Problem& p) { return depthwise_supported(p); }
+
+gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
+  if (!depthwise_dgrad_supported(p)) return GBCONV_EUNSUPPORTED;
+  DwArgs a;
+  a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.KH = int(p.KH); a.KW = int(p.KW); a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.DH = int(p.DH); a.DW = int(p.DW);
+  const int cvec = a.C / 8;
+  int cvb = 1;  // largest power-of-two divisor of C/8 up to 32 channel vectors per block row
+  while (cvb < 32 && cvec % (cvb * 2) == 0) cvb *= 2;
+  a.cv_per_block = cvb;
+  a.cv_chunks = cvec / cvb;
+  a.rows_per_thread = 4;
+  const int ty = kThreads / cvb;
+  const int64_t gx = ((p.W + ty - 1) / ty) * a.cv_chunks;
+  const int64_t gy = (p.H + a.rows_per_thread - 1) / a.rows_per_thread;
+  if (gx > 0x7FFFFFFF || gy > 65535 || p.N > 65535) return GBCONV_EUNSUPPORTED;
+  const dim3 grid(unsigned(gx), unsigned(gy), unsigned(p.N)), block(cvb, ty);
+  const size_t smem = size_t(p.KH * p.KW) * cvb * 8 * sizeof(float);
+  auto dyb = static_cast<const __nv_bfloat16*>(dy);
+  auto wb = static_cast<const __nv_bfloat16*>(w);
+  auto dxb = static_cast<__nv_bfloat16*>(dx);
+  if (p.KH == 3 && p.KW == 3 && p.SH == 2 && p.SW == 2 && p.PH == 1 && p.PW == 1 && p.DH == 1 && p.DW == 1 &&
+      p.OH == (p.H + 1) / 2 && p.OW == (p.W + 1) / 2) {
+    // One thread per dy column and 8 channels, walking a strip of dy rows: strips as long as
+    // possible (each strip start re-reads a dy row) while the grid still fills two blocks per SM.
+    // Whole columns measured best for 32x112x112x256 (60.7 us; 8-row strips 68 us, 4-row 83.5 us).
+    const int64_t gx3 = ((p.OW + ty - 1) / ty) * a.cv_chunks;
+    const int64_t strips = std::max<int64_t>(1, (2 * int64_t(l.num_sms)) / std::max<int64_t>(1, gx3 * p.N));
+    a.rows_per_thread = int(std::max<int64_t>(4, (p.OH + strips - 1) / strips));
+    const int64_t gy3 = (p.OH + a.rows_per_thread - 1) / a.rows_per_thread;
+    if (gx3 > 0x7FFFFFFF || gy3 > 65535) return GBCONV_EUNSUPPORTED;
+    return launch_kernel(depthwise3x3s2_dgrad_kernel, dim3(unsigned(gx3), unsigned(gy3), unsigned(p.N)), block, 0,
+                         l.stream, a, dyb, wb, dxb) == cudaSuccess
+               ? GBCONV_OK
+               : GBCONV_ECUDA;
+  }
+  cudaError_t e;
+  if (p.SH == 2 && p.SW == 2)
+    e = launch_kernel(depthwise_dgrad_kernel<2>, grid, block, smem, l.stream, a, dyb, wb, dxb);
+  else if (p.SH == 1 && p.SW == 1)
+    e = launch_kernel(depthwise_dgrad_kernel<1>, grid, block, smem, l.stream, a, dyb, wb, dxb);
+  else
+    e = launch_kernel(depthwise_dgrad_kernel<0>, grid, block, smem, l.stream, a, dyb, wb, dxb);
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 

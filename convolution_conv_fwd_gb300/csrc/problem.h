@@ -47,6 +47,8 @@ gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_o
 bool depthwise_supported(const Problem& p);
 gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                    const Launch& l);
+bool depthwise_dgrad_supported(const Problem& p);
+gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
 
 bool pointwise_supported(const Problem& p);
 gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,

@@ -65,7 +65,8 @@ typedef enum {
   GBCONV_K_POINTWISE = 2,     /* NHWC bf16 1x1: TMA-fed tcgen05 GEMM */
   GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
   GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 */
-  GBCONV_K_DIRECT_DGRAD = 5   /* generic gather dgrad on CUDA cores */
+  GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
+  GBCONV_K_DEPTHWISE_DGRAD = 6 /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
 } gbconv_kernel;
 
 typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1 } gbconv_op;

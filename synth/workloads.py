@@ -64,7 +64,16 @@ WORKLOADS = [
              "conv2d backward-data NHWC bf16, 3x3 stride 2 pad 1, x 16x64x64x128, dy 16x32x32x256"),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Widening beyond the five: the depthwise input gradient, the transpose of the depthwise workload
+# (dy 32x56x56x256 -> dx 32x112x112x256).
+EXTRA_WORKLOADS = [
+    Workload("depthwise3x3_s2_dgrad_nhwc_bf16", 5, "dgrad", "bf16", 2, "nhwc", "ohwi", 32, 256, 256, (112, 112),
+             (3, 3), (2, 2), (1, 1), (1, 1), 256, False, (32, 112, 112, 256), (256, 3, 3, 1), (32, 56, 56, 256),
+             {"g": ("normal", 1.0), "w": ("normal", (2.0 / 9) ** 0.5)},
+             "depthwise 3x3 stride-2 pad-1 backward-data NHWC bf16, dx 32x112x112x256, dy 32x56x56x256"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def _draw(spec, seed, shape):

@@ -11,7 +11,7 @@ import re
 import pytest
 
 import oracle
-from synth.workloads import WORKLOADS
+from synth.workloads import EXTRA_WORKLOADS, WORKLOADS
 from tests.helpers import lib_desc, oracle_conv, shape_kw
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -108,10 +108,11 @@ EXPECTED_FAMILY = {
     "dense3x3_nhwc_bf16": {"implicit"},
     "depthwise3x3_s2_nhwc_bf16": {"depthwise"},
     "dgrad3x3_s2_nhwc_bf16": {"dgrad"},
+    "depthwise3x3_s2_dgrad_nhwc_bf16": {"depthwise_dgrad"},
 }
 
 
-@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+@pytest.mark.parametrize("wl", WORKLOADS + EXTRA_WORKLOADS, ids=[w.name for w in WORKLOADS + EXTRA_WORKLOADS])
 def test_workload_kernel_family(gb, wl):
     d = lib_desc(gb, wl)
     op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
@@ -128,3 +129,6 @@ def test_generic_families_for_other_layouts(gb):
     # channel counts that are not a multiple of 8 break the 16-byte TMA row pitch
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 0) == "direct"
+    # depthwise dgrad (G = C_in = C_out, C a multiple of 8) has its own gather kernel
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=32, c_out=32, groups=32, stride=(2, 2))), 1) == "depthwise_dgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12, groups=12)), 1) == "direct_dgrad"

@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 import synth
-from synth.workloads import WORKLOADS, make_inputs
+from synth.workloads import EXTRA_WORKLOADS, WORKLOADS, make_inputs
 from tests.helpers import (bf16_round, check_bf16, check_f32, draw, lib_desc, oracle_conv, scale_dgrad, scale_fwd,
                            shape_kw, to_device, to_host_f64)
 
@@ -116,6 +116,17 @@ SMALL = [
     (shape_kw(n=3, in_size=(40, 37), c_in=128, c_out=72, stride=(2, 2)), "dgrad", "dgrad"),
     (shape_kw(n=1, in_size=(12, 12), c_in=512, c_out=64, stride=(2, 2)), "dgrad", "dgrad"),
     (shape_kw(n=2, in_size=(9, 10), c_in=256, c_out=136, k=(2, 2), pad=(0, 0), stride=(2, 2)), "dgrad", "dgrad"),
+    # depthwise dgrad gather (G = C): stride 2 (the transpose of the depthwise workload), stride 1,
+    # mixed strides with dilation, a 5x5 kernel, 1x1, many channel chunks
+    (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(9, 13), c_in=40, c_out=40, groups=40), "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(12, 11), c_in=24, c_out=24, groups=24, stride=(2, 1), dil=(2, 1), pad=(2, 1)),
+     "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(10, 10), c_in=16, c_out=16, groups=16, k=(5, 5), pad=(2, 2), stride=(3, 2)),
+     "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=2, in_size=(6, 7), c_in=8, c_out=8, groups=8, k=(1, 1), pad=(0, 0), stride=(2, 2)),
+     "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(8, 9), c_in=512, c_out=512, groups=512, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -210,7 +221,7 @@ def _sample_indices(shape4, seed, count=3000):
     return np.concatenate([idx, np.array(fixed, dtype=np.int64)], axis=0)
 
 
-@pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
+@pytest.mark.parametrize("wl", WORKLOADS + EXTRA_WORKLOADS, ids=[w.name for w in WORKLOADS + EXTRA_WORKLOADS])
 def test_workload_full_size(gb, wl):
     c = oracle_conv(wl)
     inp = make_inputs(wl)
