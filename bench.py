@@ -37,7 +37,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synth.workloads import WORKLOADS, make_inputs  # noqa: E402
+from synth.workloads import EXTRA_WORKLOADS, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "conv fwd/dgrad TFLOP/s (or GB/s) per config and % of roofline on 1 GB300"
 UNIT = "TFLOP/s"
@@ -175,8 +175,7 @@ def run_gpu(args, rank, world, local_rank):
     pk = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    cases = []
-    for wl in WORKLOADS:
+    def make_case(wl):
         inp = make_inputs(wl)
         d = desc_for(gb, wl)
         xs, ws, ys = gb.desc_shapes(d)
@@ -204,8 +203,10 @@ def run_gpu(args, rank, world, local_rank):
         reps = COPIES
         copies = [(src.clone(), w.clone(), None if b is None else b.clone(), torch.empty(out_shape, dtype=dt, device=dev))
                   for _ in range(reps)]
-        cases.append(dict(wl=wl, d=d, copies=copies, family=family, flops=flops, bytes=nbytes, host=inp,
-                          l2_resident=reps * per_copy < int(2.5 * l2)))
+        return dict(wl=wl, d=d, copies=copies, family=family, flops=flops, bytes=nbytes, host=inp,
+                    l2_resident=reps * per_copy < int(2.5 * l2))
+
+    cases = [make_case(wl) for wl in WORKLOADS]
 
     def launch(c, k):
         s = stream.cuda_stream
@@ -261,6 +262,40 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(tt.item())
 
+    def config_line(c, ms):
+        t_f = c["flops"] / (pk["bf16_tflops"] * 1e12)
+        t_b = c["bytes"] / (pk["hbm_gbs"] * 1e9)
+        t_roof = max(t_f, t_b)
+        return {"workload": c["wl"].name, "kernel": c["family"], "us": round(ms * 1e3, 3),
+                "tflops": round(c["flops"] / (ms * 1e-3) / 1e12, 2),
+                "gbs": round(c["bytes"] / (ms * 1e-3) / 1e9, 1),
+                "bound": "tensor" if t_f >= t_b else "hbm", "t_roof_us": round(t_roof * 1e6, 3),
+                "roofline_frac": round(t_roof / (ms * 1e-3), 4),
+                "launches_per_step": len(c["copies"]),
+                "inputs": "L2 resident (too small to exceed L2)" if c["l2_resident"] else "from HBM"}
+
+    # ---------------------------------------------------------------- widened rows, timed the same way
+    # Not part of the step (the step is the five configs above): the same grouped, back-to-back
+    # timing over 16 rotating copies, after the step's timed region.
+    extra = []
+    for wl in EXTRA_WORKLOADS:
+        c = make_case(wl)
+        for k in range(len(c["copies"])):
+            launch(c, k)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        torch.cuda._sleep(int(1e8))
+        ev[0].record(stream)
+        for i in range(args.steps):
+            for k in range(len(c["copies"])):
+                launch(c, k)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)) / len(c["copies"])
+        extra.append(config_line(c, ms))
+        del c
+    gb.device_status()
+
     # ---------------------------------------------------------------- end to end through the public API
     e2e_ms, h2d, d2h = None, 0, 0
     host_cases = []
@@ -293,18 +328,8 @@ def run_gpu(args, rank, world, local_rank):
 
     total_flops = sum(c["flops"] for c in cases)
     step_flops = sum(c["flops"] * len(c["copies"]) for c in cases)
-    per = []
-    for c, ms in zip(cases, per_kernel_ms):
-        t_f = c["flops"] / (pk["bf16_tflops"] * 1e12)
-        t_b = c["bytes"] / (pk["hbm_gbs"] * 1e9)
-        t_roof = max(t_f, t_b)
-        per.append({"workload": c["wl"].name, "kernel": c["family"], "us": round(ms * 1e3, 3),
-                    "tflops": round(c["flops"] / (ms * 1e-3) / 1e12, 2),
-                    "gbs": round(c["bytes"] / (ms * 1e-3) / 1e9, 1),
-                    "bound": "tensor" if t_f >= t_b else "hbm", "t_roof_us": round(t_roof * 1e6, 3),
-                    "roofline_frac": round(t_roof / (ms * 1e-3), 4),
-                    "launches_per_step": len(c["copies"]),
-                    "inputs": "L2 resident (too small to exceed L2)" if c["l2_resident"] else "from HBM"})
+
+    per = [config_line(c, ms) for c, ms in zip(cases, per_kernel_ms)]
     dom = max(range(len(cases)), key=lambda i: group_ms[i])
     dc, dms = cases[dom], per_kernel_ms[dom]
     if per[dom]["bound"] == "hbm":
@@ -329,6 +354,7 @@ def run_gpu(args, rank, world, local_rank):
                    "step_roofline_frac": round(sum(p["t_roof_us"] for p in per) / (step_ms * 1e3), 4),
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "per_config": per,
+        "extra_configs": extra,
         "roofline": roof,
         "e2e": {"value": round(world * total_flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},

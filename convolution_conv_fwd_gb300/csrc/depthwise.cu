@@ -234,11 +234,15 @@ __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a
   const int r1 = min(a.OH, r0 + a.rows_per_thread);
   const uint4 zero = make_uint4(0, 0, 0, 0);
   auto load = [&](int r, int c) -> uint4 { return __ldg(dyv + (size_t)((n * a.OH + r) * a.OW + c) * cvec + cv); };
+  // Rows r and r+1 are in registers when step r starts; the loads of row r+2 are issued first,
+  // so a step's stores overlap the next step's loads.
   uint4 cur0 = load(r0, oc), cur1 = right ? load(r0, oc + 1) : zero;
+  uint4 nxt0 = r0 + 1 < a.OH ? load(r0 + 1, oc) : zero;
+  uint4 nxt1 = (r0 + 1 < a.OH && right) ? load(r0 + 1, oc + 1) : zero;
   for (int r = r0; r < r1; ++r) {
-    const bool down = r + 1 < a.OH;
-    const uint4 nxt0 = down ? load(r + 1, oc) : zero;
-    const uint4 nxt1 = (down && right) ? load(r + 1, oc + 1) : zero;
+    const bool far = r + 2 < a.OH && r + 1 < r1;
+    const uint4 far0 = far ? load(r + 2, oc) : zero;
+    const uint4 far1 = (far && right) ? load(r + 2, oc + 1) : zero;
     float a0[8], a1[8], b0[8], b1[8];  // dy[r][c], dy[r][c+1], dy[r+1][c], dy[r+1][c+1]
     unpack8(cur0, a0);
     unpack8(cur1, a1);
@@ -270,6 +274,8 @@ __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a
     }
     cur0 = nxt0;
     cur1 = nxt1;
+    nxt0 = far0;
+    nxt1 = far1;
   }
 }
 
