@@ -28,8 +28,8 @@ KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad
            6: "depthwise_dgrad"}
 GBCONV_OP_FWD, GBCONV_OP_BWD_DATA = 0, 1
 
-EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
-           "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
+EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
+           "gbconv_pack_weight", "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
 
 
 class Desc(ctypes.Structure):
@@ -58,6 +58,7 @@ def _load():
     lib.gbconv_select.argtypes = [P(Desc), ctypes.c_int32, P(ctypes.c_int32)]
     lib.gbconv_fwd.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_bwd_data.argtypes = [P(Desc), vp, vp, vp, vp]
+    lib.gbconv_conv_transpose.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
     lib.gbconv_device_status.argtypes = [vp]
     for f in ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
@@ -97,6 +98,10 @@ def gbconv_fwd(desc: Desc, x: int, w: int, bias: int | None, y: int, stream: int
 
 def gbconv_bwd_data(desc: Desc, dy: int, w: int, dx: int, stream: int) -> int:
     return _lib.gbconv_bwd_data(ctypes.byref(desc), dy, w, dx, stream or None)
+
+
+def gbconv_conv_transpose(desc: Desc, x: int, w: int, bias: int | None, y: int, stream: int) -> int:
+    return _lib.gbconv_conv_transpose(ctypes.byref(desc), x, w, bias or None, y, stream or None)
 
 
 def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int:
@@ -234,6 +239,41 @@ def conv_bwd_data(d: Desc, dy, w, dx=None):
         raise GbconvError(s, "gbconv_bwd_data")
     if host:
         res = torch.empty(xs, dtype=dt, pin_memory=True) if dx is None else dx
+        res.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return res
+    return out
+
+
+def conv_transpose(d: Desc, x, w, bias=None, y=None):
+    """Transposed convolution forward: the input gradient of the convolution ``d`` applied to x,
+    plus a float32 bias over its C_in output channels, on the current CUDA stream.
+
+    x has d's output shape, w d's weight shape (with OIHW this is the transposed convolution's
+    own [C_in_t, C_out_t/G, KH, KW] weight), the result d's input shape.  Host tensors are staged
+    through the device as in ``conv_fwd``.
+    """
+    torch = _torch()
+    host = not x.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        x = x.to(dev, non_blocking=True)
+        w = w.to(dev, non_blocking=True)
+        bias = None if bias is None else bias.to(dev, non_blocking=True)
+    xs, ws, ys = desc_shapes(d)
+    dt = _dtype(d)
+    _check(x, ys, dt, "x")
+    _check(w, ws, dt, "w")
+    if bias is not None:
+        _check(bias, (d.c_in,), torch.float32, "bias")
+    out = y if (y is not None and not host) else torch.empty(xs, dtype=dt, device=x.device)
+    _check(out, xs, dt, "y")
+    s = gbconv_conv_transpose(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                              out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_conv_transpose")
+    if host:
+        res = torch.empty(xs, dtype=dt, pin_memory=True) if y is None else y
         res.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return res

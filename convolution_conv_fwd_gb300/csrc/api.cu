@@ -110,6 +110,23 @@ int32_t select_dgrad(const Problem& p, bool aligned) {
   return GBCONV_K_DIRECT_DGRAD;
 }
 
+// The gather dgrad, plus the transposed convolution's bias when one is given.
+gbconv_status bwd_data(const gbconv_desc* desc, const void* dy, const void* w, const float* bias, void* dx,
+                       void* stream) {
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (!dy || !w || !dx) return GBCONV_EINVAL;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  const bool aligned = aligned16(dy) && aligned16(w) && aligned16(dx);
+  switch (select_dgrad(p, aligned)) {
+    case GBCONV_K_DGRAD: return launch_implicit_dgrad(p, dy, w, bias, dx, l);
+    case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(p, dy, w, bias, dx, l);
+    default: return launch_direct_dgrad(p, dy, w, bias, dx, l);
+  }
+}
+
 }  // namespace
 }  // namespace gbconv
 
@@ -159,18 +176,12 @@ gbconv_status gbconv_fwd(const gbconv_desc* desc, const void* x, const void* w, 
 }
 
 gbconv_status gbconv_bwd_data(const gbconv_desc* desc, const void* dy, const void* w, void* dx, void* stream) {
-  Problem p;
-  gbconv_status s = resolve(desc, &p);
-  if (s != GBCONV_OK) return s;
-  if (!dy || !w || !dx) return GBCONV_EINVAL;
-  Launch l;
-  if (!device_context(&l, stream)) return GBCONV_ECUDA;
-  const bool aligned = aligned16(dy) && aligned16(w) && aligned16(dx);
-  switch (select_dgrad(p, aligned)) {
-    case GBCONV_K_DGRAD: return launch_implicit_dgrad(p, dy, w, dx, l);
-    case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(p, dy, w, dx, l);
-    default: return launch_direct_dgrad(p, dy, w, dx, l);
-  }
+  return bwd_data(desc, dy, w, nullptr, dx, stream);
+}
+
+gbconv_status gbconv_conv_transpose(const gbconv_desc* desc, const void* x, const void* w, const float* bias, void* y,
+                                    void* stream) {
+  return bwd_data(desc, x, w, bias, y, stream);
 }
 
 gbconv_status gbconv_pack_weight(const gbconv_desc* desc, const void* w_oihw, void* w_ohwi, void* stream) {

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) depthwise_fwd_kernel(DwArgs a, const
 template <int S_>
 __global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, const __nv_bfloat16* __restrict__ dy,
                                                                    const __nv_bfloat16* __restrict__ w,
+                                                                   const float* __restrict__ bias,
                                                                    __nv_bfloat16* __restrict__ dx) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
   ptx::grid_dep_launch();
@@ -161,6 +162,9 @@ __global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, con
   const uint4* dyv = reinterpret_cast<const uint4*>(dy);
   uint4* dxv = reinterpret_cast<uint4*>(dx);
   const int cvec = a.C / 8;
+  float b[8];  // transposed-convolution bias, added after the gather sum
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = bias ? __ldg(bias + c + j) : 0.f;
   for (int ih = ih0; ih < ih1; ++ih) {
     float acc[8];
 #pragma unroll
@@ -192,10 +196,10 @@ __global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, con
       }
     }
     uint4 o;
-    o.x = pack2(acc[0], acc[1]);
-    o.y = pack2(acc[2], acc[3]);
-    o.z = pack2(acc[4], acc[5]);
-    o.w = pack2(acc[6], acc[7]);
+    o.x = pack2(acc[0] + b[0], acc[1] + b[1]);
+    o.y = pack2(acc[2] + b[2], acc[3] + b[3]);
+    o.z = pack2(acc[4] + b[4], acc[5] + b[5]);
+    o.w = pack2(acc[6] + b[6], acc[7] + b[7]);
     dxv[(size_t)((n * a.H + ih) * a.W + iw) * cvec + (c >> 3)] = o;
   }
 }
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, con
 // loads and four 16-byte stores per step, the nine weights of its channels in registers.
 __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a, const __nv_bfloat16* __restrict__ dy,
                                                                         const __nv_bfloat16* __restrict__ w,
+                                                                        const float* __restrict__ bias,
                                                                         __nv_bfloat16* __restrict__ dx) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
   ptx::grid_dep_launch();
@@ -225,6 +230,9 @@ __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(ch + j) * 9 + t]);
+  float bs[8];  // transposed-convolution bias, added after the gather sum
+#pragma unroll
+  for (int j = 0; j < 8; ++j) bs[j] = bias ? __ldg(bias + ch + j) : 0.f;
   const uint4* dyv = reinterpret_cast<const uint4*>(dy);
   uint4* dxv = reinterpret_cast<uint4*>(dx);
   const int cvec = a.C / 8, cv = ch >> 3;
@@ -251,10 +259,10 @@ __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a
     float o00[8], o01[8], o10[8], o11[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      o00[j] = a0[j] * wr[4][j];
-      o01[j] = fmaf(a1[j], wr[3][j], a0[j] * wr[5][j]);
-      o10[j] = fmaf(b0[j], wr[1][j], a0[j] * wr[7][j]);
-      o11[j] = fmaf(b1[j], wr[0][j], fmaf(b0[j], wr[2][j], fmaf(a1[j], wr[6][j], a0[j] * wr[8][j])));
+      o00[j] = a0[j] * wr[4][j] + bs[j];
+      o01[j] = fmaf(a1[j], wr[3][j], a0[j] * wr[5][j]) + bs[j];
+      o10[j] = fmaf(b0[j], wr[1][j], a0[j] * wr[7][j]) + bs[j];
+      o11[j] = fmaf(b1[j], wr[0][j], fmaf(b0[j], wr[2][j], fmaf(a1[j], wr[6][j], a0[j] * wr[8][j]))) + bs[j];
     }
     auto pack = [](const float (&f)[8]) {
       uint4 o;
@@ -593,7 +601,8 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
 
 bool depthwise_dgrad_supported(const Problem& p) { return depthwise_supported(p); }
 
-gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
+gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                     const Launch& l) {
   if (!depthwise_dgrad_supported(p)) return GBCONV_EUNSUPPORTED;
   DwArgs a;
   a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
@@ -625,17 +634,17 @@ gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const voi
     const int64_t gy3 = (p.OH + a.rows_per_thread - 1) / a.rows_per_thread;
     if (gx3 > 0x7FFFFFFF || gy3 > 65535) return GBCONV_EUNSUPPORTED;
     return launch_kernel(depthwise3x3s2_dgrad_kernel, dim3(unsigned(gx3), unsigned(gy3), unsigned(p.N)), block, 0,
-                         l.stream, a, dyb, wb, dxb) == cudaSuccess
+                         l.stream, a, dyb, wb, bias, dxb) == cudaSuccess
                ? GBCONV_OK
                : GBCONV_ECUDA;
   }
   cudaError_t e;
   if (p.SH == 2 && p.SW == 2)
-    e = launch_kernel(depthwise_dgrad_kernel<2>, grid, block, smem, l.stream, a, dyb, wb, dxb);
+    e = launch_kernel(depthwise_dgrad_kernel<2>, grid, block, smem, l.stream, a, dyb, wb, bias, dxb);
   else if (p.SH == 1 && p.SW == 1)
-    e = launch_kernel(depthwise_dgrad_kernel<1>, grid, block, smem, l.stream, a, dyb, wb, dxb);
+    e = launch_kernel(depthwise_dgrad_kernel<1>, grid, block, smem, l.stream, a, dyb, wb, bias, dxb);
   else
-    e = launch_kernel(depthwise_dgrad_kernel<0>, grid, block, smem, l.stream, a, dyb, wb, dxb);
+    e = launch_kernel(depthwise_dgrad_kernel<0>, grid, block, smem, l.stream, a, dyb, wb, bias, dxb);
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 

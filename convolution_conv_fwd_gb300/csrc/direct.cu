@@ -85,7 +85,7 @@ __global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T
 
 template <typename T>
 __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, const T* __restrict__ w,
-                                    T* __restrict__ dx) {
+                                    const float* __restrict__ bias, T* __restrict__ dx) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
   ptx::grid_dep_launch();
   const int total = a.N * a.Cin * a.H * a.W;
@@ -120,6 +120,7 @@ __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, cons
         }
       }
     }
+    if (bias) acc += __ldg(bias + ci);
     dx[act_off(a, a.Cin, a.H, a.W, n, ci, ih, iw)] = cvt<T>(acc);
   }
 }
@@ -170,15 +171,17 @@ gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, 
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
-gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
+gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                  const Launch& l) {
   const DirectArgs a = make_args(p);
   const int threads = 256, blocks = grid_for(p.x_elems(), threads, l.num_sms);
   const cudaError_t e =
       p.bf16 ? launch_kernel(direct_dgrad_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, a,
-                             static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(w),
+                             static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(w), bias,
                              static_cast<__nv_bfloat16*>(dx))
              : launch_kernel(direct_dgrad_kernel<float>, dim3(blocks), dim3(threads), 0, l.stream, a,
-                             static_cast<const float*>(dy), static_cast<const float*>(w), static_cast<float*>(dx));
+                             static_cast<const float*>(dy), static_cast<const float*>(w), bias,
+                             static_cast<float*>(dx));
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 

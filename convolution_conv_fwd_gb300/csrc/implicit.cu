@@ -753,8 +753,9 @@ gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w
   return launch(p, false, x, w, bias, y, l);
 }
 
-gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l) {
-  return launch(p, true, dy, w, nullptr, dx, l);
+gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                    const Launch& l) {
+  return launch(p, true, dy, w, bias, dx, l);
 }
 
 }  // namespace gbconv

@@ -41,14 +41,17 @@ struct Launch {
 
 gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                 const Launch& l);
-gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
+// The dgrad launchers add an optional fp32 bias [C_in] after the gather sum (transposed convolution).
+gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                  const Launch& l);
 gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_ohwi, const Launch& l);
 
 bool depthwise_supported(const Problem& p);
 gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                    const Launch& l);
 bool depthwise_dgrad_supported(const Problem& p);
-gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
+gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                     const Launch& l);
 
 bool pointwise_supported(const Problem& p);
 gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
@@ -58,7 +61,8 @@ bool implicit_fwd_supported(const Problem& p);
 bool implicit_dgrad_supported(const Problem& p);
 gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                   const Launch& l);
-gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, void* dx, const Launch& l);
+gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                    const Launch& l);
 
 // Counts one enqueued kernel.
 void note_launch();

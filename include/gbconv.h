@@ -110,6 +110,19 @@ gbconv_status gbconv_fwd(const gbconv_desc *desc, const void *x, const void *w, 
  * Enqueues exactly one kernel on `stream`.  Deterministic: the same inputs give bitwise-equal dx. */
 gbconv_status gbconv_bwd_data(const gbconv_desc *desc, const void *dy, const void *w, void *dx, void *stream);
 
+/* Transposed convolution forward, y = conv_transpose(x, w) (+ bias): by definition the input gradient
+ * above applied to x, plus a per-channel bias (oarust `conv_transpose_1d` / `conv_transpose_2d`
+ * compute the same scatter with an IOK weight).  desc describes the convolution being transposed:
+ * its input extent is y's extent, which fixes what a framework's output_padding selects.
+ *   x    : device, forward-output shape [N, C_out, out...] / [N, out..., C_out], desc->dtype
+ *   w    : device, the forward weight per desc->wlayout; with GBCONV_W_OIHW this is the transposed
+ *          convolution's own [C_in_t = C_out, C_out_t / G = C_in / G, KH, KW] weight
+ *   bias : device float [C_in] (the transposed convolution's output channels), or NULL
+ *   y    : device, forward-input shape, desc->dtype; fully overwritten
+ * Enqueues exactly one kernel on `stream`.  Deterministic, as gbconv_bwd_data. */
+gbconv_status gbconv_conv_transpose(const gbconv_desc *desc, const void *x, const void *w, const float *bias,
+                                    void *y, void *stream);
+
 /* Re-lays a weight from [C_out, C_in/G, KH, KW] (OIHW) into [C_out, KH, KW, C_in/G] (OHWI), the order the
  * NHWC tensor-core kernels read.  desc->dtype gives the element type; desc->wlayout is ignored.
  * w_oihw and w_ohwi are device pointers that must not overlap.  Enqueues one kernel. */

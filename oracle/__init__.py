@@ -168,6 +168,22 @@ def conv_dgrad(c: Conv, dy, w, scatter: bool = False) -> np.ndarray:
     return dx
 
 
+def conv_transpose(c: Conv, x, w, bias=None) -> np.ndarray:
+    """Transposed convolution forward in fp64, by its definition: the input gradient of the
+    convolution ``c`` applied to ``x``, then ``bias[channel]`` added to every output element of
+    that channel (oarust ``conv_transpose_2d`` runs the same two steps: the transposed scatter,
+    then a separate bias pass).  ``x`` has c's output shape, the result c's input shape, and the
+    bias has ``c.c_in`` entries (the transposed convolution's output channels)."""
+    y = conv_dgrad(c, x, w)
+    if bias is not None:
+        b = _f32(bias, (c.c_in,)).astype(np.float64)
+        axis = y.ndim - 1 if c.nhwc else 1
+        shape = [1] * y.ndim
+        shape[axis] = c.c_in
+        y = y + b.reshape(shape)
+    return y
+
+
 def conv_fwd_points(c: Conv, x, w, bias, idx) -> np.ndarray:
     """Forward outputs at an (count, 4) array of (n, c_out, oh, ow) indices."""
     x, w = _f32(x, c.x_shape()), _f32(w, c.w_shape())

@@ -165,6 +165,43 @@ def test_small_shapes_match_oracle(gb, case):
         check_bf16(got, ref, scale)
 
 
+# Transposed convolution forward (dgrad + a bias over C_in), one case per dgrad kernel family.
+TRANSPOSE = [
+    (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad"),
+    (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(9, 13), c_in=40, c_out=40, groups=40), "depthwise_dgrad"),
+    (shape_kw(n=2, in_size=(7, 9), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
+              stride=(2, 2)), "direct_dgrad"),
+    (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "direct_dgrad"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(TRANSPOSE)), ids=["%s-%d" % (f, i) for i, (_, f) in enumerate(TRANSPOSE)])
+def test_conv_transpose_matches_oracle(gb, case):
+    kw, family = TRANSPOSE[case]
+    d = lib_desc(gb, kw)
+    assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_DATA) == family
+    c = oracle_conv(kw)
+    inp = draw(c, kw["dtype"], 500 + case, op="dgrad")
+    b = synth.normal(600 + case, (c.c_in,)).astype(np.float32)
+    bits = kw["dtype"] == "bf16"
+    x = to_device(torch, inp["g"], inp.get("g_bits") if bits else None)
+    w = to_device(torch, inp["w"], inp.get("w_bits") if bits else None)
+    xs, _, _ = gb.desc_shapes(d)
+    buf, y = _guarded(xs, torch.bfloat16 if bits else torch.float32)
+    gb.conv_transpose(d, x, w, to_device(torch, b), y=y)
+    gb.device_status()
+    assert _guards_intact(buf), "kernel wrote outside y"
+    got = to_host_f64(torch, y)
+    ref = oracle.conv_transpose(c, inp["g"], inp["w"], b)
+    scale = oracle.conv_transpose(c, np.abs(inp["g"]), np.abs(inp["w"]), np.abs(b))
+    assert got.shape == ref.shape
+    if kw["dtype"] == "f32":
+        check_f32(got, ref, scale)
+    else:
+        check_bf16(got, ref, scale)
+
+
 @pytest.mark.parametrize("case", range(len(SMALL)), ids=_ids())
 def test_integer_inputs_bit_exact(gb, case):
     kw, op, _ = SMALL[case]

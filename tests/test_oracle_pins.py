@@ -213,6 +213,32 @@ def test_matches_torch_float64(ci):
     np.testing.assert_allclose(_to_nchw(dx, c), refdx.numpy(), rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_conv_transpose_matches_torch_float64(ci):
+    # The transposed convolution of the forward c: torch's conv_transpose with c's weight as its
+    # [C_in_t = C_out, C_out_t / G, KH, KW] weight, and the output_padding that lands on c's input
+    # extent (the trailing positions no stride reaches).
+    c = CASES[ci]
+    F = torch.nn.functional
+    x = synth.normal(91 + ci, c.y_shape()).astype(np.float32)
+    w = synth.normal(92 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(93 + ci, (c.c_in,)).astype(np.float32)
+    xt = torch.from_numpy(_to_nchw(x, c).astype(np.float64).copy())
+    wt = torch.from_numpy(_w_to_oihw(w, c).astype(np.float64).copy())
+    bt = torch.from_numpy(b.astype(np.float64))
+    oh, ow = c.out_hw()
+    def opad(axis, o):
+        return c.in_hw[axis] - ((o - 1) * c.stride[axis] - 2 * c.pad[axis] + c.dil[axis] * (c.k[axis] - 1) + 1)
+    if c.spatial_dims == 1:
+        ref = F.conv_transpose1d(xt, wt, bt, stride=c.stride[1], padding=c.pad[1], output_padding=opad(1, ow),
+                                 groups=c.groups, dilation=c.dil[1])
+    else:
+        ref = F.conv_transpose2d(xt, wt, bt, stride=c.stride, padding=c.pad, output_padding=(opad(0, oh), opad(1, ow)),
+                                 groups=c.groups, dilation=c.dil)
+    y = oracle.conv_transpose(c, x, w, b)
+    np.testing.assert_allclose(_to_nchw(y, c), ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------- adjoint and scatter == gather
 
 @pytest.mark.parametrize("ci", range(len(CASES)))
