@@ -365,8 +365,16 @@ def run_gpu(args, rank, world, local_rank):
     return res, cases
 
 
-def cpu_sample(target_s: float, cases_host):
-    """Time the FP64 oracle on a bounded, strided sample of every workload's outputs."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_sample(target_s: float, cases_host, threads: int = 1):
+    """Time the FP64 oracle on a bounded, strided sample of every workload's outputs, on `threads`
+    host threads (disjoint slices of the sample; the oracle's C loops run without the GIL)."""
     import oracle
     from tests.helpers import oracle_conv  # the same shape mapping the tests use
     oracle.build()
@@ -385,15 +393,15 @@ def cpu_sample(target_s: float, cases_host):
     # calibrate: a small sample of the heaviest workload
     budget_iters = None
     wl, inp, c, shp, iters = max(per_point, key=lambda p: p[4])
-    probe = 2000
-    t = _time_points(wl, inp, c, shp, probe)
+    probe = 2000 * threads
+    t = _time_points(wl, inp, c, shp, probe, threads)
     rate = probe * iters / max(t, 1e-6)  # inner iterations per second
     budget_iters = rate * target_s
     total_flops, total_s, points = 0.0, 0.0, {}
     for wl, inp, c, shp, iters in per_point:
         outputs = int(np.prod(shp))
         count = int(min(outputs, max(256, budget_iters / len(per_point) / iters)))
-        dt = _time_points(wl, inp, c, shp, count)
+        dt = _time_points(wl, inp, c, shp, count, threads)
         flops, _ = work(wl)
         total_flops += flops * count / outputs
         total_s += dt
@@ -401,30 +409,42 @@ def cpu_sample(target_s: float, cases_host):
     return total_flops, total_s, points
 
 
-def _time_points(wl, inp, c, shp, count):
+def _time_points(wl, inp, c, shp, count, threads=1):
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     n, ch, h, w = shp
     total = n * ch * h * w
     stride = max(1, total // count)
     flat = (np.arange(count, dtype=np.int64) * stride) % total
     idx = np.stack(np.unravel_index(flat, (n, ch, h, w)), axis=1).astype(np.int64)
-    t0 = time.perf_counter()
-    if wl.op == "dgrad":
-        oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
-    else:
-        oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
-    return time.perf_counter() - t0
+
+    def run(part):
+        if wl.op == "dgrad":
+            oracle.conv_dgrad_points(c, inp["g"], inp["w"], part)
+        else:
+            oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), part)
+
+    if threads <= 1:
+        t0 = time.perf_counter()
+        run(idx)
+        return time.perf_counter() - t0
+    parts = np.array_split(idx, threads)
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(run, parts))
+        return time.perf_counter() - t0
 
 
 def run_reference(args):
     """The reference arm: the FP64 oracle on the host cores, one bounded sample per step."""
     cases_host = [(wl, make_inputs(wl)) for wl in WORKLOADS]
+    cores = host_cores()
     for _ in range(args.warmup):
-        cpu_sample(0.5, cases_host)
+        cpu_sample(0.5, cases_host, cores)
     flops, secs = 0.0, 0.0
     points = {}
     for _ in range(args.steps):
-        f, s, points = cpu_sample(args.ref_seconds_per_step, cases_host)
+        f, s, points = cpu_sample(args.ref_seconds_per_step, cases_host, cores)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -434,7 +454,7 @@ def run_reference(args):
         "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME}, "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -497,10 +517,14 @@ def main():
     res, cases = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         host = [(c["wl"], c["host"]) for c in cases]
-        flops, secs, points = cpu_sample(args.cpu_seconds, host)
-        res["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-                               "sample": "strided sample of every workload's outputs, %s points, %.1f s"
-                                         % (json.dumps(points), secs)}
+        cores = host_cores()
+        f1, s1, p1 = cpu_sample(args.cpu_seconds / 2, host, 1)
+        fn, sn, pn = cpu_sample(args.cpu_seconds / 2, host, cores)
+        res["cpu_baseline"] = {"value": fn / sn / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": "strided sample of every workload's outputs split over %d threads, %s points, "
+                                         "%.1f s" % (cores, json.dumps(pn), sn),
+                               "single_core": {"value": f1 / s1 / 1e12, "cores": 1,
+                                               "sample": "%s points, %.1f s" % (json.dumps(p1), s1)}}
         print(json.dumps(res))
     if world > 1:
         import torch
