@@ -75,6 +75,7 @@ struct PhaseHdr {
   int a_bytes;  // bytes of one halo box (64 channels x P x bh)
   int tiles;    // m-tiles per image
   int item0;    // first work item of this phase
+  int row_step;  // input rows per virtual-grid row: the stride of a strided 1x1 forward (else 1)
 };
 
 struct Phase : PhaseHdr {
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* a_base = smem;
   uint8_t* b_base = a_base + size_t(a.sa) * a.a_stage_bytes;
-  const int b_tiles = BRES ? a.T : a.sb;
+  const int b_tiles = BRES ? a.T * a.kb_count : a.sb;  // resident: every (k-block, tap) tile
   // two staging blocks of 128 rows x (staging group * 2 + 16) bytes
   uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;
   constexpr int kStageBlock = 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16);
@@ -244,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = true;
-      if (BRES) {
-        ptx::mbar_arrive_expect_tx(bres, uint32_t(a.T) * kBTile);
-        for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(wt) * kBTile, bres, wt, 0, 0);
+      if (BRES) {  // tile (kb, tap) at index kb * T + tap
+        ptx::mbar_arrive_expect_tx(bres, uint32_t(a.T * a.kb_count) * kBTile);
+        for (int kb = 0; kb < a.kb_count; ++kb)
+          for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(kb * a.T + wt) * kBTile, bres, wt, kb, 0);
       }
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
           ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
           tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                      kb * kKB, ph.cmin, ra + ph.rmin, it.n);
+                      kb * kKB, ph.cmin, (ra + ph.rmin) * ph.row_step, it.n);
           if (++sa == a.sa) { sa = 0; pa ^= 1; }
           if (!BRES) {
             for (int ti = 0, t = t_rot; ok && ti < ph.ntaps; ++ti, t = (t + 1 == ph.ntaps ? 0 : t + 1)) {
@@ -300,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // k-blocks and taps are walked in an order rotated by the item index (the producer
           // walks the same order): CTAs working at the same time then read different weight
           // tiles, which spreads the L2 traffic of the streamed weights.
-          const int t_rot = item % ntaps;
+          const int t_rot = item % ntaps, kb_rot = item % kbn;
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
+            const int kb = kbi + kb_rot < kbn ? kbi + kb_rot : kbi + kb_rot - kbn;  // the producer's order
             // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
             // orders the async-proxy writes before the async-proxy MMA reads.
             if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int off_n = toff[tn], w_n = tw[tn];
               uint32_t b_addr;
               if (BRES) {
-                b_addr = ptx::smem_addr(b_base + size_t(w_c) * kBTile);
+                b_addr = ptx::smem_addr(b_base + size_t(kb * a.T + w_c) * kBTile);
               } else {
                 if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
                 b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
@@ -484,6 +487,7 @@ struct Plan {
   Maps maps;
   int bn, nsub;
   bool bres, dgrad;
+  int row_step = 1, col_step = 1;  // strided view of the activations (strided 1x1 forward)
   size_t smem;
   int grid;
   // geometry kept for the tensor maps
@@ -517,14 +521,18 @@ int pick_bn(int64_t cn) {
 struct PhaseSpec {
   Phase ph;
   int maxoff;
+  int col_step;  // input columns per virtual-grid column (strided 1x1 forward), else 1
 };
 
 // Fills the per-phase box geometry and counts for a tile of 128*nsub positions.
 bool finish_phase(PhaseSpec& s, int nsub, int N) {
   Phase& ph = s.ph;
+  if (ph.row_step == 0) ph.row_step = 1;
+  if (s.col_step == 0) s.col_step = 1;
   const int mt = 128 * nsub;
   ph.bh = (ph.P - 1 + mt + s.maxoff + ph.P - 1) / ph.P;
-  if (ph.P > 256 || ph.bh > 256) return false;  // TMA box extent limit
+  // TMA box extent limit (a strided view spans stride x the loaded extent)
+  if (ph.P * s.col_step > 256 || ph.bh * ph.row_step > 256) return false;
   ph.a_bytes = 128 * ph.P * ph.bh;
   const int64_t per_img = int64_t(ph.R) * ph.P;
   ph.tiles = int((per_img + mt - 1) / mt);
@@ -533,7 +541,10 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
-  if (!dgrad && (p.SH != 1 || p.SW != 1)) return false;
+  // Forward: unit stride, or a strided 1x1 without padding, whose activations are read through a
+  // strided view (TMA element strides): the subsampled pixels land dense, one tap, a plain GEMM.
+  const bool strided_1x1 = !dgrad && p.KH == 1 && p.KW == 1 && p.PH == 0 && p.PW == 0 && p.SH <= 8 && p.SW <= 8;
+  if (!dgrad && (p.SH != 1 || p.SW != 1) && !strided_1x1) return false;
   if (dgrad && p.SH * p.SW > kMaxPhases) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides and vector stores
   if (p.KH * p.KW > kMaxTapsPerPhase) return false;
@@ -569,6 +580,10 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     ph.P = int(p.OW) + (cmax - cmin);
     ph.rmin = rmin; ph.cmin = cmin;
     ph.out_sh = 1; ph.out_sw = 1;
+    ph.row_step = int(p.SH);
+    s.col_step = int(p.SW);
+    pl.col_step = int(p.SW);
+    pl.row_step = int(p.SH);
     for (int kh = 0; kh < p.KH; ++kh)
       for (int kw = 0; kw < p.KW; ++kw) {
         const int t = int(kh * p.KW + kw);
@@ -627,7 +642,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.total_items = item;
   a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
-  pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.b_tile_bytes <= 110 * 1024;
+  pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.kb_count * a.b_tile_bytes <= 110 * 1024;
   const size_t block = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
   for (int bufs = 2; bufs >= 1; --bufs) {
     const size_t fixed = 1024 + bufs * block + size_t(a.n_tiles) * pl.bn * 4 +
@@ -635,7 +650,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
                          8 * (2 * 4 + 2 * 8 + 6) + 16;
     for (int sa = 3; sa >= 2; --sa) {
       for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
-        const size_t total = fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T : sb) * a.b_tile_bytes;
+        const size_t total =
+            fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T * a.kb_count : sb) * a.b_tile_bytes;
         if (total <= size_t(kSmemLimit)) {
           a.sa = sa;
           a.sb = pl.bres ? 1 : sb;
@@ -658,8 +674,10 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
     const Phase& ph = a.ph[i];
     cuuint64_t dims[4] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N)};
     cuuint64_t strides[3] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Wi) * pl.Ck * 2, cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2};
-    cuuint32_t box[4] = {cuuint32_t(kKB), cuuint32_t(ph.P), cuuint32_t(ph.bh), 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
+    // A strided view spans stride x the loaded extent and loads every stride-th element (the
+    // forward of a strided 1x1); otherwise row_step = col_step = 1.
+    cuuint32_t box[4] = {cuuint32_t(kKB), cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1};
+    cuuint32_t estr[4] = {1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1};
     if (fn(&pl.maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(in), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

@@ -129,6 +129,9 @@ def test_generic_families_for_other_layouts(gb):
     # channel counts that are not a multiple of 8 break the 16-byte TMA row pitch
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 0) == "direct"
+    # a strided 1x1 forward reads a strided TMA view: the implicit GEMM with one tap
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(0, 0), stride=(2, 2))), 0) == "implicit"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(1, 1), stride=(2, 2))), 0) == "direct"
     # depthwise dgrad (G = C_in = C_out, C a multiple of 8) has its own gather kernel
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=32, c_out=32, groups=32, stride=(2, 2))), 1) == "depthwise_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12, groups=12)), 1) == "direct_dgrad"

@@ -83,6 +83,8 @@ SMALL = [
     # channel tails: 80 input channels (second 64-block zero-filled by TMA), 72 outputs (masked N columns)
     (shape_kw(n=2, in_size=(7, 9), c_in=80, c_out=72, bias=True), "fwd", "implicit"),
     (shape_kw(n=1, in_size=(6, 7), c_in=64, c_out=192, bias=True), "fwd", "implicit"),
+    # resident weights with two 64-channel k-blocks (every (k-block, tap) tile stays in shared memory)
+    (shape_kw(n=2, in_size=(11, 12), c_in=128, c_out=64, k=(2, 2), pad=(0, 0), bias=True), "fwd", "implicit"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
@@ -102,6 +104,14 @@ SMALL = [
     (shape_kw(n=3, in_size=(19, 35), c_in=64, c_out=64, groups=64, stride=(2, 2), pad=(0, 0)), "fwd", "depthwise"),
     (shape_kw(n=1, in_size=(10, 41), c_in=192, c_out=192, groups=192, stride=(2, 2), pad=(2, 2), bias=True),
      "fwd", "depthwise"),
+    # strided 1x1 forward through a strided TMA view (ResNet-style downsampling): stride 2, uneven
+    # strides with an odd extent, a K tail, several n-tiles
+    (shape_kw(n=2, in_size=(15, 14), c_in=64, c_out=128, k=(1, 1), pad=(0, 0), stride=(2, 2), bias=True),
+     "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(23, 9), c_in=256, c_out=64, k=(1, 1), pad=(0, 0), stride=(2, 3)), "fwd", "implicit"),
+    (shape_kw(n=3, in_size=(8, 8), c_in=72, c_out=40, k=(1, 1), pad=(0, 0), stride=(2, 2)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(28, 28), c_in=128, c_out=512, k=(1, 1), pad=(0, 0), stride=(2, 2), bias=True),
+     "fwd", "implicit"),
     # stride-phase dgrad (tcgen05): one phase, four uneven phases, zero-tap phases, even kernel, N tiles
     (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64), "dgrad", "dgrad"),
     (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad", "dgrad"),
