@@ -63,6 +63,7 @@ constexpr int kTmaWarp = 9;
 constexpr int kThreads = 10 * 32;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kKB = 64;  // channels per k-block: one 128-byte swizzled row
+constexpr int kMaxSrc = 9;  // activation sources of one phase: stride phases of a strided forward
 
 struct PhaseHdr {
   int ntaps;
@@ -75,7 +76,14 @@ struct PhaseHdr {
   int a_bytes;  // bytes of one halo box (64 channels x P x bh)
   int tiles;    // m-tiles per image
   int item0;    // first work item of this phase
-  int row_step;  // input rows per virtual-grid row: the stride of a strided 1x1 forward (else 1)
+  // Activation sources.  A strided forward reads its input as s_h x s_w stride phases: through a
+  // strided view (TMA element strides = the conv strides) each phase is a dense grid, and every
+  // tap reads one of them at a fixed shift.  Source k starts at input offset (src_ah, src_aw)
+  // and owns taps [src_t0[k], src_t0[k+1]).  Unit stride: one source at (0, 0) with every tap.
+  int row_step, col_step;  // input rows / columns per virtual-grid step (the strides; else 1)
+  int nsrc;
+  int src_ah[kMaxSrc], src_aw[kMaxSrc];
+  int src_t0[kMaxSrc + 1];
 };
 
 struct Phase : PhaseHdr {
@@ -257,21 +265,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PhaseHdr& ph = phase_s[it.phase];
         if (ph.ntaps == 0) continue;
         const int ra = (it.m * 128 * NSUB) / ph.P;
-        const int kb_rot = item % a.kb_count, t_rot = item % ph.ntaps;
+        const int kb_rot = item % a.kb_count;
         const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
         for (int kbi = 0; ok && kbi < a.kb_count; ++kbi) {
           const int kb = kbi + kb_rot < a.kb_count ? kbi + kb_rot : kbi + kb_rot - a.kb_count;
-          if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
-          ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
-          tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                      kb * kKB, ph.cmin, (ra + ph.rmin) * ph.row_step, it.n);
-          if (++sa == a.sa) { sa = 0; pa ^= 1; }
-          if (!BRES) {
-            for (int ti = 0, t = t_rot; ok && ti < ph.ntaps; ++ti, t = (t + 1 == ph.ntaps ? 0 : t + 1)) {
-              if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
-              ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
-              load_b(b_base + size_t(sb) * kBTile, fullB + sb, tw[t], kb, it.ntile * BN);
-              if (++sb == a.sb) { sb = 0; pb ^= 1; }
+          for (int src = 0; ok && src < ph.nsrc; ++src) {
+            if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
+            ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
+            tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                        kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src],
+                        it.n);
+            if (++sa == a.sa) { sa = 0; pa ^= 1; }
+            if (!BRES) {
+              const int t0 = ph.src_t0[src], nt = ph.src_t0[src + 1] - t0;
+              for (int ti = 0, t = item % nt; ok && ti < nt; ++ti, t = (t + 1 == nt ? 0 : t + 1)) {
+                if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
+                ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
+                load_b(b_base + size_t(sb) * kBTile, fullB + sb, tw[t0 + t], kb, it.ntile * BN);
+                if (++sb == a.sb) { sb = 0; pb ^= 1; }
+              }
             }
           }
         }
@@ -296,57 +308,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ph.ntaps > 0) {
           const int q0 = it.m * 128 * NSUB;
           const int row0 = q0 - (q0 / ph.P) * ph.P;  // tile start inside the halo block
-          const int ntaps = ph.ntaps, kbn = a.kb_count;
+          const int kbn = a.kb_count;
           const int* toff = taps_s + (it.phase * 2 + 0) * kMaxTapsPerPhase;
           const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
           // k-blocks and taps are walked in an order rotated by the item index (the producer
           // walks the same order): CTAs working at the same time then read different weight
           // tiles, which spreads the L2 traffic of the streamed weights.
-          const int t_rot = item % ntaps, kb_rot = item % kbn;
+          const int kb_rot = item % kbn;
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
             const int kb = kbi + kb_rot < kbn ? kbi + kb_rot : kbi + kb_rot - kbn;  // the producer's order
-            // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
-            // orders the async-proxy writes before the async-proxy MMA reads.
-            if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
-            const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
-            int tc = t_rot;
-            int off_c = toff[tc], w_c = tw[tc];
-            for (int ti = 0; ti < ntaps; ++ti) {
-              // fetch the next tap's table entries before this tap's MMAs are issued
-              const int tn = tc + 1 == ntaps ? 0 : tc + 1;
-              const int off_n = toff[tn], w_n = tw[tn];
-              uint32_t b_addr;
-              if (BRES) {
-                b_addr = ptx::smem_addr(b_base + size_t(kb * a.T + w_c) * kBTile);
-              } else {
-                if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
-                b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
-              }
-              // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
-              // per-MMA operand offsets (K step j, sub-tile s) are compile-time adds on it.
-              const uint64_t ad0 = desc_sw128_kmajor(a_addr + uint32_t(row0 + off_c) * 128);
-              const uint64_t bd0 = DGRAD ? desc_sw128_mnmajor(b_addr, 8192) : desc_sw128_kmajor(b_addr);
-              const uint32_t a_lo = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
-              const uint32_t b_lo = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
-              const uint32_t first = uint32_t(kbi | ti);
+            for (int src = 0; ok && src < ph.nsrc; ++src) {
+              // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
+              // orders the async-proxy writes before the async-proxy MMA reads.
+              if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
+              const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
+              // this source's taps, in the producer's rotated order
+              const int t0 = ph.src_t0[src], nt = ph.src_t0[src + 1] - t0;
+              int tc = item % nt;
+              int off_c = toff[t0 + tc], w_c = tw[t0 + tc];
+              for (int ti = 0; ti < nt; ++ti) {
+                // fetch the next tap's table entries before this tap's MMAs are issued
+                const int tn = tc + 1 == nt ? 0 : tc + 1;
+                const int off_n = toff[t0 + tn], w_n = tw[t0 + tn];
+                uint32_t b_addr;
+                if (BRES) {
+                  b_addr = ptx::smem_addr(b_base + size_t(kb * a.T + w_c) * kBTile);
+                } else {
+                  if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
+                  b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
+                }
+                // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
+                // per-MMA operand offsets (K step j, sub-tile s) are compile-time adds on it.
+                const uint64_t ad0 = desc_sw128_kmajor(a_addr + uint32_t(row0 + off_c) * 128);
+                const uint64_t bd0 = DGRAD ? desc_sw128_mnmajor(b_addr, 8192) : desc_sw128_kmajor(b_addr);
+                const uint32_t a_lo = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
+                const uint32_t b_lo = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+                const uint32_t first = uint32_t(kbi | src | ti);  // 0 only for the item's first MMA
 #pragma unroll
-              for (int j = 0; j < kKB / 16; ++j) {
-                const uint32_t b_off = DGRAD ? uint32_t(j * 2048 >> 4) : uint32_t(j * 32 >> 4);
+                for (int j = 0; j < kKB / 16; ++j) {
+                  const uint32_t b_off = DGRAD ? uint32_t(j * 2048 >> 4) : uint32_t(j * 32 >> 4);
 #pragma unroll
-                for (int s = 0; s < NSUB; ++s)
-                  ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((s * 128 * 128 + j * 32) >> 4), a_hi, b_lo + b_off,
-                                     b_hi, kIdesc, j == 0 ? first : 1u);
+                  for (int s = 0; s < NSUB; ++s)
+                    ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((s * 128 * 128 + j * 32) >> 4), a_hi, b_lo + b_off,
+                                       b_hi, kIdesc, j == 0 ? first : 1u);
+                }
+                if (!BRES) {
+                  ptx::mma_commit(emptyB + sb);
+                  if (++sb == a.sb) { sb = 0; pb ^= 1; }
+                }
+                tc = tn;
+                off_c = off_n;
+                w_c = w_n;
               }
-              if (!BRES) {
-                ptx::mma_commit(emptyB + sb);
-                if (++sb == a.sb) { sb = 0; pb ^= 1; }
-              }
-              tc = tn;
-              off_c = off_n;
-              w_c = w_n;
+              ptx::mma_commit(emptyA + sa);
+              if (++sa == a.sa) { sa = 0; pa ^= 1; }
             }
-            ptx::mma_commit(emptyA + sa);
-            if (++sa == a.sa) { sa = 0; pa ^= 1; }
           }
         }
         ptx::mma_commit(tfull + buf);
@@ -521,18 +537,17 @@ int pick_bn(int64_t cn) {
 struct PhaseSpec {
   Phase ph;
   int maxoff;
-  int col_step;  // input columns per virtual-grid column (strided 1x1 forward), else 1
 };
 
 // Fills the per-phase box geometry and counts for a tile of 128*nsub positions.
 bool finish_phase(PhaseSpec& s, int nsub, int N) {
   Phase& ph = s.ph;
   if (ph.row_step == 0) ph.row_step = 1;
-  if (s.col_step == 0) s.col_step = 1;
+  if (ph.col_step == 0) ph.col_step = 1;
   const int mt = 128 * nsub;
   ph.bh = (ph.P - 1 + mt + s.maxoff + ph.P - 1) / ph.P;
   // TMA box extent limit (a strided view spans stride x the loaded extent)
-  if (ph.P * s.col_step > 256 || ph.bh * ph.row_step > 256) return false;
+  if (ph.P * ph.col_step > 256 || ph.bh * ph.row_step > 256) return false;
   ph.a_bytes = 128 * ph.P * ph.bh;
   const int64_t per_img = int64_t(ph.R) * ph.P;
   ph.tiles = int((per_img + mt - 1) / mt);
@@ -541,10 +556,8 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
-  // Forward: unit stride, or a strided 1x1 without padding, whose activations are read through a
-  // strided view (TMA element strides): the subsampled pixels land dense, one tap, a plain GEMM.
-  const bool strided_1x1 = !dgrad && p.KH == 1 && p.KW == 1 && p.PH == 0 && p.PW == 0 && p.SH <= 8 && p.SW <= 8;
-  if (!dgrad && (p.SH != 1 || p.SW != 1) && !strided_1x1) return false;
+  // A strided forward reads its activations through strided views (TMA element strides <= 8).
+  if (!dgrad && (p.SH > 8 || p.SW > 8)) return false;
   if (dgrad && p.SH * p.SW > kMaxPhases) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides and vector stores
   if (p.KH * p.KW > kMaxTapsPerPhase) return false;
@@ -571,25 +584,56 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   PhaseSpec specs[kMaxPhases];
   int nph = 0;
   if (!dgrad) {
+    // Tap (kh, kw) reads input (oh*SH + rr, ow*SW + cc), rr = kh*DH - PH, cc = kw*DW - PW.  With
+    // rr = SH*dr + ah (0 <= ah < SH) that is row oh + dr of stride phase ah of the input: the
+    // taps of one (ah, aw) phase are shifted windows of that phase's dense grid (its strided view),
+    // so the forward is the shifted-window GEMM once per phase, all into one accumulator.
     PhaseSpec s{};
     Phase& ph = s.ph;
-    const int rmin = -int(p.PH), rmax = int((p.KH - 1) * p.DH - p.PH);
-    const int cmin = -int(p.PW), cmax = int((p.KW - 1) * p.DW - p.PW);
+    int drs[kMaxTapsPerPhase], dcs[kMaxTapsPerPhase], ahs[kMaxTapsPerPhase], aws[kMaxTapsPerPhase];
+    int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
+    for (int kh = 0; kh < p.KH; ++kh)
+      for (int kw = 0; kw < p.KW; ++kw) {
+        const int t = int(kh * p.KW + kw);
+        const int rr = int(kh * p.DH - p.PH), cc = int(kw * p.DW - p.PW);
+        ahs[t] = ((rr % int(p.SH)) + int(p.SH)) % int(p.SH);
+        aws[t] = ((cc % int(p.SW)) + int(p.SW)) % int(p.SW);
+        drs[t] = (rr - ahs[t]) / int(p.SH);
+        dcs[t] = (cc - aws[t]) / int(p.SW);
+        rmin = t ? std::min(rmin, drs[t]) : drs[t];
+        rmax = t ? std::max(rmax, drs[t]) : drs[t];
+        cmin = t ? std::min(cmin, dcs[t]) : dcs[t];
+        cmax = t ? std::max(cmax, dcs[t]) : dcs[t];
+      }
     ph.ntaps = a.T;
     ph.R = int(p.OH); ph.OWv = int(p.OW);
     ph.P = int(p.OW) + (cmax - cmin);
     ph.rmin = rmin; ph.cmin = cmin;
     ph.out_sh = 1; ph.out_sw = 1;
     ph.row_step = int(p.SH);
-    s.col_step = int(p.SW);
-    pl.col_step = int(p.SW);
+    ph.col_step = int(p.SW);
     pl.row_step = int(p.SH);
-    for (int kh = 0; kh < p.KH; ++kh)
-      for (int kw = 0; kw < p.KW; ++kw) {
-        const int t = int(kh * p.KW + kw);
-        ph.tap_off[t] = (int(kh * p.DH - p.PH) - rmin) * ph.P + (int(kw * p.DW - p.PW) - cmin);
-        ph.tap_w[t] = t;
+    pl.col_step = int(p.SW);
+    // taps grouped by source, sources in (ah, aw) order
+    int k = 0;
+    ph.nsrc = 0;
+    for (int ah = 0; ah < p.SH; ++ah)
+      for (int aw = 0; aw < p.SW; ++aw) {
+        const int start = k;
+        for (int t = 0; t < a.T; ++t) {
+          if (ahs[t] != ah || aws[t] != aw) continue;
+          ph.tap_off[k] = (drs[t] - rmin) * ph.P + (dcs[t] - cmin);
+          ph.tap_w[k] = t;
+          ++k;
+        }
+        if (k == start) continue;
+        if (ph.nsrc == kMaxSrc) return false;
+        ph.src_ah[ph.nsrc] = ah;
+        ph.src_aw[ph.nsrc] = aw;
+        ph.src_t0[ph.nsrc] = start;
+        ++ph.nsrc;
       }
+    ph.src_t0[ph.nsrc] = k;
     s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
     specs[nph++] = s;
   } else {
@@ -624,6 +668,11 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
             ph.tap_w[t] = int(khs[i] * p.KW + kws[j]);
           }
         s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+        ph.row_step = ph.col_step = 1;  // dy is read as it is: one source
+        ph.nsrc = 1;
+        ph.src_ah[0] = ph.src_aw[0] = 0;
+        ph.src_t0[0] = 0;
+        ph.src_t0[1] = ph.ntaps;
         specs[nph++] = s;
       }
     // Longest phases first, so the persistent CTAs finish together.

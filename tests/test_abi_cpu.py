@@ -123,7 +123,9 @@ def test_generic_families_for_other_layouts(gb):
     assert gb.gbconv_select(lib_desc(gb, shape_kw(layout="nchw", wlayout="oihw")), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(dtype="f32")), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(groups=2)), 1) == "direct_dgrad"
-    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 0) == "direct"
+    # strided forwards read stride-phase views of x: the implicit GEMM (up to 9 phases, 32 taps)
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 0) == "implicit"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), k=(7, 7), pad=(3, 3))), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), c_in=32, c_out=32)), 1) == "dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2))), 1) == "dgrad"
     # channel counts that are not a multiple of 8 break the 16-byte TMA row pitch
@@ -131,7 +133,7 @@ def test_generic_families_for_other_layouts(gb):
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12)), 0) == "direct"
     # a strided 1x1 forward reads a strided TMA view: the implicit GEMM with one tap
     assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(0, 0), stride=(2, 2))), 0) == "implicit"
-    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(1, 1), stride=(2, 2))), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(1, 1), stride=(2, 2))), 0) == "implicit"
     # depthwise dgrad (G = C_in = C_out, C a multiple of 8) has its own gather kernel
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=32, c_out=32, groups=32, stride=(2, 2))), 1) == "depthwise_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12, groups=12)), 1) == "direct_dgrad"

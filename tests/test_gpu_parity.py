@@ -112,6 +112,16 @@ SMALL = [
     (shape_kw(n=3, in_size=(8, 8), c_in=72, c_out=40, k=(1, 1), pad=(0, 0), stride=(2, 2)), "fwd", "implicit"),
     (shape_kw(n=1, in_size=(28, 28), c_in=128, c_out=512, k=(1, 1), pad=(0, 0), stride=(2, 2), bias=True),
      "fwd", "implicit"),
+    # strided forwards through stride-phase views (several sources per item): 3x3 s2 p1 (ResNet
+    # downsampling), odd extents, dilation, 5x5 s2, 3x3 s3 (nine sources), mixed strides, 4x4 s2,
+    # and a padded strided 1x1
+    (shape_kw(n=2, in_size=(16, 15), c_in=64, c_out=128, stride=(2, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(13, 11), c_in=128, c_out=64, stride=(2, 2), dil=(2, 1), pad=(2, 1)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(17, 14), c_in=32, c_out=64, k=(5, 5), pad=(2, 2), stride=(2, 2)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(14, 13), c_in=64, c_out=64, stride=(3, 3), pad=(1, 1)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(12, 17), c_in=72, c_out=96, stride=(1, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(18, 18), c_in=64, c_out=256, k=(4, 4), pad=(1, 1), stride=(2, 2)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(9, 10), c_in=64, c_out=64, k=(1, 1), pad=(1, 1), stride=(2, 2)), "fwd", "implicit"),
     # stride-phase dgrad (tcgen05): one phase, four uneven phases, zero-tap phases, even kernel, N tiles
     (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64), "dgrad", "dgrad"),
     (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad", "dgrad"),
