@@ -71,6 +71,11 @@ EXTRA_WORKLOADS = [
              (3, 3), (2, 2), (1, 1), (1, 1), 256, False, (32, 112, 112, 256), (256, 3, 3, 1), (32, 56, 56, 256),
              {"g": ("normal", 1.0), "w": ("normal", (2.0 / 9) ** 0.5)},
              "depthwise 3x3 stride-2 pad-1 backward-data NHWC bf16, dx 32x112x112x256, dy 32x56x56x256"),
+    # a strided dense forward (ResNet-style downsampling): four stride-phase sources per tile
+    Workload("dense3x3_s2_nhwc_bf16", 6, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 128, 128, (56, 56), (3, 3), (2, 2),
+             (1, 1), (1, 1), 1, True, (32, 56, 56, 128), (128, 3, 3, 128), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / (128 * 9)) ** 0.5), "b": ("normal", 0.1)},
+             "dense 3x3 conv2d NHWC bf16, N=32, 56x56 -> 28x28, C 128->128, stride 2, pad 1, fp32 bias"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

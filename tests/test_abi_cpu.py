@@ -109,6 +109,7 @@ EXPECTED_FAMILY = {
     "depthwise3x3_s2_nhwc_bf16": {"depthwise"},
     "dgrad3x3_s2_nhwc_bf16": {"dgrad"},
     "depthwise3x3_s2_dgrad_nhwc_bf16": {"depthwise_dgrad"},
+    "dense3x3_s2_nhwc_bf16": {"implicit"},
 }
 
 
