@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kThreads) depthwise_dgrad_kernel(DwArgs a, con
 // (w[kh][kw]; dy outside [0,OH) x [0,OW) is zero).  Each thread owns 8 channels of one dy column
 // c and walks a strip of dy rows r, keeping row r+1's two vectors for the next step: two 16-byte
 // loads and four 16-byte stores per step, the nine weights of its channels in registers.
+template <bool BIAS>
 __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a, const __nv_bfloat16* __restrict__ dy,
                                                                         const __nv_bfloat16* __restrict__ w,
                                                                         const float* __restrict__ bias,
@@ -230,9 +231,9 @@ __global__ void __launch_bounds__(kThreads) depthwise3x3s2_dgrad_kernel(DwArgs a
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(ch + j) * 9 + t]);
-  float bs[8];  // transposed-convolution bias, added after the gather sum
+  float bs[8];  // transposed-convolution bias, added after the gather sum (BIAS only: registers)
 #pragma unroll
-  for (int j = 0; j < 8; ++j) bs[j] = bias ? __ldg(bias + ch + j) : 0.f;
+  for (int j = 0; j < 8; ++j) bs[j] = BIAS ? __ldg(bias + ch + j) : 0.f;
   const uint4* dyv = reinterpret_cast<const uint4*>(dy);
   uint4* dxv = reinterpret_cast<uint4*>(dx);
   const int cvec = a.C / 8, cv = ch >> 3;
@@ -633,8 +634,9 @@ gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const voi
     a.rows_per_thread = int(std::max<int64_t>(4, (p.OH + strips - 1) / strips));
     const int64_t gy3 = (p.OH + a.rows_per_thread - 1) / a.rows_per_thread;
     if (gx3 > 0x7FFFFFFF || gy3 > 65535) return GBCONV_EUNSUPPORTED;
-    return launch_kernel(depthwise3x3s2_dgrad_kernel, dim3(unsigned(gx3), unsigned(gy3), unsigned(p.N)), block, 0,
-                         l.stream, a, dyb, wb, bias, dxb) == cudaSuccess
+    auto kern = bias ? depthwise3x3s2_dgrad_kernel<true> : depthwise3x3s2_dgrad_kernel<false>;
+    return launch_kernel(kern, dim3(unsigned(gx3), unsigned(gy3), unsigned(p.N)), block, 0, l.stream, a, dyb, wb, bias,
+                         dxb) == cudaSuccess
                ? GBCONV_OK
                : GBCONV_ECUDA;
   }

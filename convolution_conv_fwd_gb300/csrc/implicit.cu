@@ -82,8 +82,8 @@ struct PhaseHdr {
   // and owns taps [src_t0[k], src_t0[k+1]).  Unit stride: one source at (0, 0) with every tap.
   int row_step, col_step;  // input rows / columns per virtual-grid step (the strides; else 1)
   int nsrc;
-  int src_ah[kMaxSrc], src_aw[kMaxSrc];
-  int src_t0[kMaxSrc + 1];
+  int8_t src_ah[kMaxSrc], src_aw[kMaxSrc];  // < 8 (TMA element strides are at most 8)
+  int8_t src_t0[kMaxSrc + 1];                // <= kMaxTapsPerPhase
 };
 
 struct Phase : PhaseHdr {
@@ -169,7 +169,9 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t saddr, uint32_t 
   return d;
 }
 
-template <int BN, int NSUB, bool DGRAD, bool BRES>
+// MSRC: phases may have several activation sources (a strided forward); otherwise every phase
+// has exactly one and the source loops fold away at compile time.
+template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC>
 __global__ void __launch_bounds__(kThreads, 1)
     implicit_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int* tw = taps_s + (it.phase * 2 + 1) * kMaxTapsPerPhase;
         for (int kbi = 0; ok && kbi < a.kb_count; ++kbi) {
           const int kb = kbi + kb_rot < a.kb_count ? kbi + kb_rot : kbi + kb_rot - a.kb_count;
-          for (int src = 0; ok && src < ph.nsrc; ++src) {
+          for (int src = 0; ok && src < (MSRC ? ph.nsrc : 1); ++src) {
             if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
             ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
             tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
@@ -315,16 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // walks the same order): CTAs working at the same time then read different weight
           // tiles, which spreads the L2 traffic of the streamed weights.
           const int kb_rot = item % kbn;
+          // Source 0's tap range and rotation, worked out once per item: scalar work between MMA
+          // bursts delays the issue (one source is the common case: unit stride, every dgrad).
+          const int nsrc = MSRC ? ph.nsrc : 1, nt0 = ph.src_t0[1], tc0 = item % nt0;
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
             const int kb = kbi + kb_rot < kbn ? kbi + kb_rot : kbi + kb_rot - kbn;  // the producer's order
-            for (int src = 0; ok && src < ph.nsrc; ++src) {
+            for (int src = 0; ok && src < nsrc; ++src) {
               // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
               // orders the async-proxy writes before the async-proxy MMA reads.
               if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
               const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
               // this source's taps, in the producer's rotated order
-              const int t0 = ph.src_t0[src], nt = ph.src_t0[src + 1] - t0;
-              int tc = item % nt;
+              const int t0 = src == 0 ? 0 : ph.src_t0[src];
+              const int nt = src == 0 ? nt0 : ph.src_t0[src + 1] - t0;
+              int tc = src == 0 ? tc0 : item % nt;
               int off_c = toff[t0 + tc], w_c = tw[t0 + tc];
               for (int ti = 0; ti < nt; ++ti) {
                 // fetch the next tap's table entries before this tap's MMAs are issued
@@ -628,12 +634,12 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         }
         if (k == start) continue;
         if (ph.nsrc == kMaxSrc) return false;
-        ph.src_ah[ph.nsrc] = ah;
-        ph.src_aw[ph.nsrc] = aw;
-        ph.src_t0[ph.nsrc] = start;
+        ph.src_ah[ph.nsrc] = int8_t(ah);
+        ph.src_aw[ph.nsrc] = int8_t(aw);
+        ph.src_t0[ph.nsrc] = int8_t(start);
         ++ph.nsrc;
       }
-    ph.src_t0[ph.nsrc] = k;
+    ph.src_t0[ph.nsrc] = int8_t(k);
     s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
     specs[nph++] = s;
   } else {
@@ -672,7 +678,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         ph.nsrc = 1;
         ph.src_ah[0] = ph.src_aw[0] = 0;
         ph.src_t0[0] = 0;
-        ph.src_t0[1] = ph.ntaps;
+        ph.src_t0[1] = int8_t(ph.ntaps);
         specs[nph++] = s;
       }
     // Longest phases first, so the persistent CTAs finish together.
@@ -756,9 +762,9 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NSUB, bool DGRAD, bool BRES>
+template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC = false>
 gbconv_status run(const Plan& pl, const Launch& l) {
-  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES>;
+  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES, MSRC>;
   // The shared-memory opt-in is a per-device function attribute: raise it once per device.
   static std::atomic<uint64_t> done[64];
   int dev = 0;
@@ -773,22 +779,29 @@ gbconv_status run(const Plan& pl, const Launch& l) {
              : GBCONV_ECUDA;
 }
 
-template <bool DGRAD>
-gbconv_status dispatch(const Plan& pl, const Launch& l) {
+template <bool DGRAD, bool MSRC>
+gbconv_status dispatch_src(const Plan& pl, const Launch& l) {
   if (!DGRAD && pl.bres) {
     switch (pl.bn) {
-      case 256: return run<256, 1, false, true>(pl, l);
-      case 192: return run<192, 1, false, true>(pl, l);
-      case 128: return run<128, 2, false, true>(pl, l);
-      default: return run<64, 2, false, true>(pl, l);
+      case 256: return run<256, 1, false, true, MSRC>(pl, l);
+      case 192: return run<192, 1, false, true, MSRC>(pl, l);
+      case 128: return run<128, 2, false, true, MSRC>(pl, l);
+      default: return run<64, 2, false, true, MSRC>(pl, l);
     }
   }
   switch (pl.bn) {
-    case 256: return run<256, 1, DGRAD, false>(pl, l);
-    case 192: return run<192, 1, DGRAD, false>(pl, l);
-    case 128: return run<128, 2, DGRAD, false>(pl, l);
-    default: return run<64, 2, DGRAD, false>(pl, l);
+    case 256: return run<256, 1, DGRAD, false, MSRC>(pl, l);
+    case 192: return run<192, 1, DGRAD, false, MSRC>(pl, l);
+    case 128: return run<128, 2, DGRAD, false, MSRC>(pl, l);
+    default: return run<64, 2, DGRAD, false, MSRC>(pl, l);
   }
+}
+
+template <bool DGRAD>
+gbconv_status dispatch(const Plan& pl, const Launch& l) {
+  // Only a strided forward has phases with several activation sources.
+  if (!DGRAD && pl.a.ph[0].nsrc > 1) return dispatch_src<false, true>(pl, l);
+  return dispatch_src<DGRAD, false>(pl, l);
 }
 
 gbconv_status launch(const Problem& p, bool dgrad, const void* in, const void* w, const float* bias, void* out,
