@@ -28,7 +28,7 @@ KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad
            6: "depthwise_dgrad"}
 GBCONV_OP_FWD, GBCONV_OP_BWD_DATA = 0, 1
 
-EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
+EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
            "gbconv_pack_weight", "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
 
 
@@ -56,12 +56,13 @@ def _load():
     vp, st = ctypes.c_void_p, ctypes.c_int
     lib.gbconv_out_shape.argtypes = [P(Desc), P(ctypes.c_int64)]
     lib.gbconv_select.argtypes = [P(Desc), ctypes.c_int32, P(ctypes.c_int32)]
+    lib.gbconv_describe.argtypes = [P(Desc), ctypes.c_int32, ctypes.c_char_p, ctypes.c_int64]
     lib.gbconv_fwd.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_bwd_data.argtypes = [P(Desc), vp, vp, vp, vp]
     lib.gbconv_conv_transpose.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
     lib.gbconv_device_status.argtypes = [vp]
-    for f in ("gbconv_out_shape", "gbconv_select", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
+    for f in ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_conv_transpose", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
               "gbconv_device_status"):
         getattr(lib, f).restype = st
     lib.gbconv_kernels_launched.argtypes = []
@@ -90,6 +91,14 @@ def gbconv_select(desc: Desc, op: int) -> str:
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_select")
     return KERNELS[k.value]
+
+
+def gbconv_describe(desc: Desc, op: int) -> str:
+    buf = ctypes.create_string_buffer(256)
+    s = _lib.gbconv_describe(ctypes.byref(desc), op, buf, len(buf))
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_describe")
+    return buf.value.decode()
 
 
 def gbconv_fwd(desc: Desc, x: int, w: int, bias: int | None, y: int, stream: int) -> int:

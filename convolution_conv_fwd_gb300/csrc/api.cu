@@ -1,5 +1,6 @@
 // The C ABI: argument checks, shape resolution, choice of kernel family and
 // the device status word.  Nothing here allocates device memory.
+#include <cstdio>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -155,6 +156,21 @@ gbconv_status gbconv_select(const gbconv_desc* desc, int32_t op, int32_t* kernel
   gbconv_status s = resolve(desc, &p);
   if (s != GBCONV_OK) return s;
   *kernel = op == GBCONV_OP_FWD ? select_fwd(p, true) : select_dgrad(p, true);
+  return GBCONV_OK;
+}
+
+gbconv_status gbconv_describe(const gbconv_desc* desc, int32_t op, char* buf, int64_t len) {
+  if (!buf || len < 1 || (op != GBCONV_OP_FWD && op != GBCONV_OP_BWD_DATA)) return GBCONV_EINVAL;
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  const int32_t k = op == GBCONV_OP_FWD ? select_fwd(p, true) : select_dgrad(p, true);
+  static const char* const names[] = {"direct", "depthwise", "pointwise", "implicit", "dgrad", "direct_dgrad",
+                                      "depthwise_dgrad"};
+  if ((k == GBCONV_K_IMPLICIT || k == GBCONV_K_DGRAD) &&
+      implicit_describe(p, k == GBCONV_K_DGRAD, buf, size_t(len)))
+    return GBCONV_OK;
+  std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_DEPTHWISE_DGRAD) ? names[k] : "unknown");
   return GBCONV_OK;
 }
 

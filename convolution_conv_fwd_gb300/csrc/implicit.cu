@@ -45,6 +45,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "problem.h"
@@ -255,11 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = true;
-      if (BRES) {  // tile (kb, tap) at index kb * T + tap
+      // Resident weights, tile (kb, tap) at index kb * T + tap.  Issued right after the first
+      // activation halo: that box comes from HBM and takes longest, the weights are shared by every
+      // CTA and mostly come from L2.
+      bool b_pending = BRES;
+      auto load_resident_b = [&]() {
         ptx::mbar_arrive_expect_tx(bres, uint32_t(a.T * a.kb_count) * kBTile);
         for (int kb = 0; kb < a.kb_count; ++kb)
           for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(kb * a.T + wt) * kBTile, bres, wt, kb, 0);
-      }
+        b_pending = false;
+      };
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0; item = round_item(++r, a.total_items)) {
@@ -278,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src],
                         it.n);
             if (++sa == a.sa) { sa = 0; pa ^= 1; }
+            if (BRES && b_pending) load_resident_b();
             if (!BRES) {
               const int t0 = ph.src_t0[src], nt = ph.src_t0[src + 1] - t0;
               for (int ti = 0, t = item % nt; ok && ti < nt; ++ti, t = (t + 1 == nt ? 0 : t + 1)) {
@@ -290,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (BRES && b_pending && ok) load_resident_b();  // a CTA that loaded no halo still owes them
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -826,6 +834,20 @@ bool implicit_fwd_supported(const Problem& p) {
 bool implicit_dgrad_supported(const Problem& p) {
   Plan pl;
   return plan_geometry(p, true, pl);
+}
+
+bool implicit_describe(const Problem& p, bool dgrad, char* buf, size_t len) {
+  Plan pl;
+  if (!plan_geometry(p, dgrad, pl)) return false;
+  const Args& a = pl.a;
+  int taps = 0;
+  for (int i = 0; i < a.nphase; ++i) taps = std::max(taps, a.ph[i].ntaps);
+  std::snprintf(buf, len,
+                "implicit_gemm %s bn=%d nsub=%d phases=%d sources=%d taps=%d items=%d kb=%d weights=%s "
+                "a_stages=%d b_stages=%d stage_bufs=%d smem=%zu",
+                dgrad ? "dgrad" : "fwd", pl.bn, pl.nsub, a.nphase, a.ph[0].nsrc, taps, a.total_items, a.kb_count,
+                pl.bres ? "resident" : "streamed", a.sa, pl.bres ? 0 : a.sb, a.stage_bufs, pl.smem);
+  return true;
 }
 
 gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,

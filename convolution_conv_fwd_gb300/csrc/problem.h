@@ -59,6 +59,8 @@ gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* 
 
 bool implicit_fwd_supported(const Problem& p);
 bool implicit_dgrad_supported(const Problem& p);
+// Writes the implicit-GEMM plan for p (forward or dgrad) into buf; false if p has none.
+bool implicit_describe(const Problem& p, bool dgrad, char* buf, size_t len);
 gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                   const Launch& l);
 gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,

@@ -92,6 +92,14 @@ gbconv_status gbconv_out_shape(const gbconv_desc *desc, int64_t out[2]);
  * Launches nothing. */
 gbconv_status gbconv_select(const gbconv_desc *desc, int32_t op, int32_t *kernel);
 
+/* A one-line description of the plan that would serve `op` for this descriptor (pointers assumed
+ * 16-byte aligned): the kernel family, and for the tensor-core implicit GEMM its tile width, work
+ * items, stride phases, activation sources, taps, weight residency, pipeline depth and shared memory.
+ * Writes at most `len` bytes including the terminating NUL into the caller's host buffer `buf`
+ * (truncating if needed).  Launches nothing and needs no GPU.
+ * Returns GBCONV_EINVAL for a NULL argument, len < 1, an unknown op, or a shape the call would reject. */
+gbconv_status gbconv_describe(const gbconv_desc *desc, int32_t op, char *buf, int64_t len);
+
 /* Forward convolution, y = conv(x, w) (+ bias).
  *   x    : device, [N, C_in, in...] or [N, in..., C_in] per desc->layout, desc->dtype
  *   w    : device, per desc->wlayout, desc->dtype

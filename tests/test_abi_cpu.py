@@ -5,13 +5,14 @@ ctypes, and checked for: every function include/gbconv.h declares is
 exported; output sizes agree with the oracle; invalid shapes and arguments are
 rejected before anything is launched; the kernel family chosen per workload.
 """
+import ctypes
 import os
 import re
 
 import pytest
 
 import oracle
-from synth.workloads import EXTRA_WORKLOADS, WORKLOADS
+from synth.workloads import BY_NAME, EXTRA_WORKLOADS, WORKLOADS
 from tests.helpers import lib_desc, oracle_conv, shape_kw
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -138,3 +139,44 @@ def test_generic_families_for_other_layouts(gb):
     # depthwise dgrad (G = C_in = C_out, C a multiple of 8) has its own gather kernel
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=32, c_out=32, groups=32, stride=(2, 2))), 1) == "depthwise_dgrad"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=12, c_out=12, groups=12)), 1) == "direct_dgrad"
+
+
+def _plan(gb, kw_or_wl, op=0):
+    text = gb.gbconv_describe(lib_desc(gb, kw_or_wl), op)
+    fields = dict(f.split("=", 1) for f in text.split()[2:])
+    return text.split()[0], text.split()[1], fields
+
+
+def test_describe_dense_plans(gb):
+    # dense 3x3 at C_out = 64: 64-wide N tiles, two 128-row sub-tiles per item on a virtual grid of
+    # 56 x (56 + 2) positions per image, every (k-block, tap) weight tile resident
+    fam, op, f = _plan(gb, BY_NAME["dense3x3_nhwc_bf16"])
+    assert (fam, op) == ("implicit_gemm", "fwd")
+    assert f["bn"] == "64" and f["nsub"] == "2" and f["taps"] == "9" and f["weights"] == "resident"
+    assert int(f["items"]) == 32 * -(-56 * 58 // 256)
+    assert int(f["smem"]) <= 227 * 1024
+    # 1x2 kernel at dilation 3: the virtual grid pitch is OW + 3
+    _, _, f = _plan(gb, shape_kw(n=1, in_size=(9, 30), c_in=64, c_out=16, k=(1, 2), pad=(0, 1), dil=(1, 3)))
+    assert f["taps"] == "2" and int(f["items"]) == -(-9 * (29 + 3) // 256)
+    # C_out = 192: one 192-wide tile, one sub-tile per item; C_in = 96: two k-blocks
+    _, _, f = _plan(gb, shape_kw(n=2, in_size=(10, 9), c_in=96, c_out=192, k=(3, 2), pad=(1, 0)))
+    assert f["bn"] == "192" and f["nsub"] == "1" and f["kb"] == "2"
+    # weights too large to stay resident stream through a ring
+    _, _, f = _plan(gb, shape_kw(c_in=256, c_out=128))
+    assert f["weights"] == "streamed" and int(f["b_stages"]) >= 3
+
+
+def test_describe_phases_sources_and_families(gb):
+    _, op, f = _plan(gb, BY_NAME["dense3x3_s2_nhwc_bf16"])
+    assert op == "fwd" and f["sources"] == "4" and f["taps"] == "9"
+    _, op, f = _plan(gb, BY_NAME["dgrad3x3_s2_nhwc_bf16"], 1)
+    assert op == "dgrad" and f["phases"] == "4" and f["taps"] == "4" and f["weights"] == "streamed"
+    assert gb.gbconv_describe(lib_desc(gb, BY_NAME["depthwise3x3_s2_nhwc_bf16"]), 0) == "depthwise"
+    assert gb.gbconv_describe(lib_desc(gb, BY_NAME["conv1d_ncl_f32"]), 0) == "direct"
+    d = lib_desc(gb, shape_kw())
+    buf = ctypes.create_string_buffer(8)
+    assert gb._lib.gbconv_describe(ctypes.byref(d), 0, buf, 8) == gb.GBCONV_OK
+    assert buf.value == b"implici"  # truncated to the buffer, NUL-terminated
+    assert gb._lib.gbconv_describe(ctypes.byref(d), 7, buf, 8) == gb.GBCONV_EINVAL
+    assert gb._lib.gbconv_describe(ctypes.byref(d), 0, None, 8) == gb.GBCONV_EINVAL
+    assert gb._lib.gbconv_describe(ctypes.byref(d), 0, buf, 0) == gb.GBCONV_EINVAL

@@ -85,6 +85,13 @@ SMALL = [
     (shape_kw(n=1, in_size=(6, 7), c_in=64, c_out=192, bias=True), "fwd", "implicit"),
     # resident weights with two 64-channel k-blocks (every (k-block, tap) tile stays in shared memory)
     (shape_kw(n=2, in_size=(11, 12), c_in=128, c_out=64, k=(2, 2), pad=(0, 0), bias=True), "fwd", "implicit"),
+    # small C_out at unit stride: dilation 2, a 1x2 kernel at dilation 3, a 3x2 kernel over two
+    # k-blocks, 8 channels, and many items per image with a ragged last one
+    (shape_kw(n=2, in_size=(13, 17), c_in=64, c_out=64, dil=(2, 2), pad=(2, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(9, 30), c_in=64, c_out=16, k=(1, 2), pad=(0, 1), dil=(1, 3)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(10, 9), c_in=96, c_out=48, k=(3, 2), pad=(1, 0), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(12, 7), c_in=8, c_out=8), "fwd", "implicit"),
+    (shape_kw(n=3, in_size=(60, 60), c_in=64, c_out=64, bias=True), "fwd", "implicit"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
