@@ -1,4 +1,4 @@
-"""FP64 CPU oracle for convolution forward and input gradient.
+"""FP64 CPU oracle for convolution forward, input gradient, and weight and bias gradients.
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the package smoke check
 and by the benchmark's CPU-baseline leg, never by the product path.  It shares
@@ -115,6 +115,12 @@ def _load():
         lib.oracle_conv_fwd_points.restype = None
         lib.oracle_conv_dgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_dgrad_points.restype = None
+        lib.oracle_conv_wgrad.argtypes = [P(_Desc), f32p, f32p, f64p]
+        lib.oracle_conv_wgrad.restype = ctypes.c_int
+        lib.oracle_conv_bgrad.argtypes = [P(_Desc), f32p, f64p]
+        lib.oracle_conv_bgrad.restype = ctypes.c_int
+        lib.oracle_conv_wgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_wgrad_points.restype = None
         _lib = lib
     return _lib
 
@@ -202,5 +208,38 @@ def conv_dgrad_points(c: Conv, dy, w, idx) -> np.ndarray:
     idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
     out = np.empty(idx.shape[0], dtype=np.float64)
     _load().oracle_conv_dgrad_points(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(w, ctypes.c_float),
+                                     _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
+    return out
+
+
+def conv_wgrad(c: Conv, x, dy) -> np.ndarray:
+    """Whole weight gradient in fp64, shaped like the weight layout ``c`` names: every
+    (c_out, c_in_local, kh, kw) element is the sum over batch and output positions of the output
+    gradient times the input element the forward multiplied by that weight."""
+    x, dy = _f32(x, c.x_shape()), _f32(dy, c.y_shape())
+    dw = np.empty(c.w_shape(), dtype=np.float64)
+    rc = _load().oracle_conv_wgrad(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(dy, ctypes.c_float),
+                                   _ptr(dw, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return dw
+
+
+def conv_bgrad(c: Conv, dy) -> np.ndarray:
+    """Bias gradient in fp64: the output gradient summed over batch and positions, per channel."""
+    dy = _f32(dy, c.y_shape())
+    db = np.empty((c.c_out,), dtype=np.float64)
+    rc = _load().oracle_conv_bgrad(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(db, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return db
+
+
+def conv_wgrad_points(c: Conv, x, dy, idx) -> np.ndarray:
+    """Weight-gradient elements at an (count, 4) array of (c_out, c_in_local, kh, kw) indices."""
+    x, dy = _f32(x, c.x_shape()), _f32(dy, c.y_shape())
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(idx.shape[0], dtype=np.float64)
+    _load().oracle_conv_wgrad_points(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(dy, ctypes.c_float),
                                      _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
     return out

@@ -1,6 +1,7 @@
 /*
  * Convolution oracle: the plain, slow, FP64 definition of N-D (1-D and 2-D)
- * convolution forward and of its input gradient (dgrad).
+ * convolution forward, of its input gradient (dgrad), and of its weight and
+ * bias gradients (wgrad).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * load this file; only the tests, the package's smoke check and the CPU
@@ -32,6 +33,15 @@
  *  - Data gradient, gather form: oarust `conv_2d_backward` dispatches its
  *    input-gradient pass over input elements; the gather form here is the
  *    exact transpose of the scatter form above.
+ *  - Weight gradient: burn-cubecl `wgrad_im2col` (the weight gradient is the
+ *    contraction of the output gradient with the input's columns over every
+ *    (batch, output position), columns read at out*stride + k*dilation -
+ *    padding and zero outside the image) and teeny-kernels
+ *    `conv2d_backward_dw` (one sum per (c_out, c_in_local, kh, kw) of dy
+ *    times the x element the forward multiplied by that weight).
+ *  - Bias gradient: oarust `conv_2d_backward` returns, beside the input and
+ *    weight gradients, the gradient of the bias: the sum of the output
+ *    gradient over batch and positions, per output channel.
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -217,4 +227,66 @@ void oracle_conv_dgrad_points(const oracle_conv *c, const float *dy, const float
                               const int64_t *idx, int64_t count, double *out) {
   for (int64_t i = 0; i < count; ++i)
     out[i] = oracle_conv_dgrad_at(c, dy, w, idx[4 * i], idx[4 * i + 1], idx[4 * i + 2], idx[4 * i + 3]);
+}
+
+/* One weight-gradient element dw[co, c_local, kh, kw]:
+ *   sum over n < N, oh < OH, ow < OW of
+ *   dy[n, co, oh, ow] * x[n, g*C_in/G + c_local, oh*s_h + kh*d_h - p_h, ow*s_w + kw*d_w - p_w]
+ * with g = co / (C_out/G) and out-of-image x taken as zero (those terms are skipped). */
+double oracle_conv_wgrad_at(const oracle_conv *c, const float *x, const float *dy,
+                            int64_t co, int64_t cl, int64_t kh, int64_t kw) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return 0.0;
+  int64_t cpg = c->c_in / c->groups;
+  int64_t g = co / (c->c_out / c->groups);
+  int64_t ci = g * cpg + cl;
+  double acc = 0.0;
+  for (int64_t n = 0; n < c->n; ++n)
+    for (int64_t oh = 0; oh < OH; ++oh) {
+      int64_t ih = oh * c->s_h + kh * c->d_h - c->p_h;
+      if (ih < 0 || ih >= c->in_h) continue;
+      for (int64_t ow = 0; ow < OW; ++ow) {
+        int64_t iw = ow * c->s_w + kw * c->d_w - c->p_w;
+        if (iw < 0 || iw >= c->in_w) continue;
+        double gv = (double)dy[act_index(c, c->c_out, OH, OW, n, co, oh, ow)];
+        double xv = (double)x[act_index(c, c->c_in, c->in_h, c->in_w, n, ci, ih, iw)];
+        acc += gv * xv;
+      }
+    }
+  return acc;
+}
+
+/* Whole weight gradient, in the descriptor's weight layout. */
+int oracle_conv_wgrad(const oracle_conv *c, const float *x, const float *dy, double *dw) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return ORACLE_EINVAL;
+  int64_t cpg = c->c_in / c->groups;
+  for (int64_t co = 0; co < c->c_out; ++co)
+    for (int64_t cl = 0; cl < cpg; ++cl)
+      for (int64_t kh = 0; kh < c->k_h; ++kh)
+        for (int64_t kw = 0; kw < c->k_w; ++kw)
+          dw[w_index(c, co, cl, kh, kw)] = oracle_conv_wgrad_at(c, x, dy, co, cl, kh, kw);
+  return ORACLE_OK;
+}
+
+/* Bias gradient db[co] = sum over n, oh, ow of dy[n, co, oh, ow]. */
+int oracle_conv_bgrad(const oracle_conv *c, const float *dy, double *db) {
+  int64_t OH, OW;
+  if (oracle_check(c, &OH, &OW) != ORACLE_OK) return ORACLE_EINVAL;
+  for (int64_t co = 0; co < c->c_out; ++co) {
+    double acc = 0.0;
+    for (int64_t n = 0; n < c->n; ++n)
+      for (int64_t oh = 0; oh < OH; ++oh)
+        for (int64_t ow = 0; ow < OW; ++ow) acc += (double)dy[act_index(c, c->c_out, OH, OW, n, co, oh, ow)];
+    db[co] = acc;
+  }
+  return ORACLE_OK;
+}
+
+/* Batched point queries of the weight gradient: out[i] = dw at the i-th
+ * (co, c_local, kh, kw) quadruple of idx. */
+void oracle_conv_wgrad_points(const oracle_conv *c, const float *x, const float *dy,
+                              const int64_t *idx, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_conv_wgrad_at(c, x, dy, idx[4 * i], idx[4 * i + 1], idx[4 * i + 2], idx[4 * i + 3]);
 }

@@ -4,7 +4,8 @@ Each test ties the oracle to a fact the pages or the mathematics fix:
 hand-worked examples (tests/golden), the output-size rule, the 1x1 = matmul
 identity, delta kernels, constant-input closed forms, an independent library
 convolution (PyTorch CPU, float64), the adjoint identity between forward and
-input gradient, scatter == gather, and rejection of degenerate shapes.
+input gradient (and in w, for the weight gradient), scatter == gather, a
+one-hot output gradient, and rejection of degenerate shapes.
 A plausible slip in the oracle (dropped bias, a flipped kernel, a wrong group
 window, a sign or stride error in the gather) fails at least one of them.
 """
@@ -280,3 +281,91 @@ def test_degenerate_shapes_rejected(kw):
     base.update(kw)
     c = Conv(**base)
     assert not oracle.check(c)
+
+
+# ------------------------------------------------------- weight and bias gradients
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_wgrad_matches_torch_float64(ci):
+    # torch's own weight-gradient routine, in float64, on the NCHW / OIHW view of the same case
+    c = CASES[ci]
+    x = synth.normal(101 + ci, c.x_shape()).astype(np.float32)
+    dy = synth.normal(102 + ci, c.y_shape()).astype(np.float32)
+    xt = torch.from_numpy(_to_nchw(x, c).astype(np.float64).copy())
+    dyt = torch.from_numpy(_to_nchw(dy, c).astype(np.float64).copy())
+    w_oihw_shape = (c.c_out, c.c_in // c.groups) + ((c.k[1],) if c.spatial_dims == 1 else tuple(c.k))
+    if c.spatial_dims == 1:
+        ref = torch.nn.grad.conv1d_weight(xt, w_oihw_shape, dyt, stride=c.stride[1], padding=c.pad[1],
+                                          dilation=c.dil[1], groups=c.groups)
+    else:
+        ref = torch.nn.grad.conv2d_weight(xt, w_oihw_shape, dyt, stride=c.stride, padding=c.pad,
+                                          dilation=c.dil, groups=c.groups)
+    dw = oracle.conv_wgrad(c, x, dy)
+    np.testing.assert_allclose(_w_to_oihw(dw, c), ref.numpy(), rtol=1e-12, atol=1e-12)
+    axes = tuple(a for a in range(dyt.ndim) if a != 1)
+    np.testing.assert_allclose(oracle.conv_bgrad(c, dy), dyt.sum(dim=axes).numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_wgrad_adjoint_identity(ci):
+    # The forward is linear in w: <conv(x, w), dy> == <w, wgrad(x, dy)>
+    c = CASES[ci]
+    x = synth.normal(111 + ci, c.x_shape())
+    w = synth.normal(112 + ci, c.w_shape())
+    dy = synth.normal(113 + ci, c.y_shape())
+    lhs = float(np.sum(oracle.conv_fwd(c, x, w) * dy.astype(np.float32)))
+    rhs = float(np.sum(w.astype(np.float32).astype(np.float64) * oracle.conv_wgrad(c, x, dy)))
+    assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs))
+
+
+@pytest.mark.parametrize("nhwc", [False, True])
+def test_pointwise_wgrad_is_matmul(nhwc):
+    # 1x1, stride 1, no padding: dW[co, ci] = sum over pixels m of dy[m, co] * x[m, ci]
+    c = Conv(n=2, c_in=5, c_out=3, in_hw=(4, 3), k=(1, 1), nhwc=nhwc, w_ohwi=nhwc)
+    x = synth.normal(121, c.x_shape())
+    dy = synth.normal(122, c.y_shape())
+    X = x if nhwc else x.transpose(0, 2, 3, 1)
+    G = dy if nhwc else dy.transpose(0, 2, 3, 1)
+    X = X.astype(np.float32).astype(np.float64).reshape(-1, c.c_in)
+    G = G.astype(np.float32).astype(np.float64).reshape(-1, c.c_out)
+    ref = np.zeros((c.c_out, c.c_in))
+    for m in range(X.shape[0]):
+        for co in range(c.c_out):
+            for ci_ in range(c.c_in):
+                ref[co, ci_] += G[m, co] * X[m, ci_]
+    np.testing.assert_allclose(oracle.conv_wgrad(c, x, dy).reshape(c.c_out, c.c_in), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_wgrad_constant_counts():
+    # x = 1, dy = 1: dW[co, cl, kh, kw] = N * (output rows whose tap kh lands in the image) *
+    # (output columns whose tap kw lands in the image); db[co] = N * OH * OW.
+    c = Conv(n=3, c_in=4, c_out=6, in_hw=(7, 6), k=(3, 2), stride=(2, 1), pad=(1, 1), dil=(1, 2), groups=2,
+             nhwc=True, w_ohwi=True)
+    oh_n, ow_n = c.out_hw()
+    dw = oracle.conv_wgrad(c, np.ones(c.x_shape()), np.ones(c.y_shape()))
+    for kh in range(3):
+        rows = sum(1 for oh in range(oh_n) if 0 <= oh * 2 + kh * 1 - 1 < 7)
+        for kw in range(2):
+            cols = sum(1 for ow in range(ow_n) if 0 <= ow * 1 + kw * 2 - 1 < 6)
+            np.testing.assert_array_equal(dw[:, kh, kw, :], 3.0 * rows * cols)
+    np.testing.assert_array_equal(oracle.conv_bgrad(c, np.ones(c.y_shape())), 3.0 * oh_n * ow_n)
+
+
+def test_wgrad_of_one_hot_output_gradient_is_the_input_patch():
+    # dy = 1 at (n0, co0, oh0, ow0) only: dW[co0, cl, kh, kw] is the input element the forward read
+    # for that output with that weight (zero outside the image); every other output channel is 0.
+    c = Conv(n=2, c_in=6, c_out=4, in_hw=(6, 7), k=(3, 3), stride=(2, 1), pad=(1, 2), dil=(1, 2), groups=2)
+    x = synth.normal(131, c.x_shape()).astype(np.float32)
+    n0, co0, oh0, ow0 = 1, 3, 2, 4
+    dy = np.zeros(c.y_shape())
+    dy[n0, co0, oh0, ow0] = 1.0
+    dw = oracle.conv_wgrad(c, x, dy)
+    g = co0 // (c.c_out // c.groups)
+    cpg = c.c_in // c.groups
+    for cl in range(cpg):
+        for kh in range(3):
+            for kw in range(3):
+                ih, iw = oh0 * 2 + kh - 1, ow0 + kw * 2 - 2
+                want = x[n0, g * cpg + cl, ih, iw] if (0 <= ih < 6 and 0 <= iw < 7) else 0.0
+                assert dw[co0, cl, kh, kw] == want
+    assert np.all(np.delete(dw, co0, axis=0) == 0.0)
