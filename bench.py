@@ -162,7 +162,7 @@ def traffic_record(kernel_file: str, workload: str):
 
 KERNEL_FILE = {"direct": "direct.cu", "depthwise": "depthwise.cu", "pointwise": "pointwise.cu",
                "implicit": "implicit.cu", "dgrad": "implicit.cu", "direct_dgrad": "direct.cu",
-               "depthwise_dgrad": "depthwise.cu"}
+               "depthwise_dgrad": "depthwise.cu", "direct_wgrad": "wgrad.cu", "wgrad": "wgrad_tc.cu"}
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -182,16 +182,17 @@ def run_gpu(args, rank, world, local_rank):
         if wl.dtype == "bf16":
             def t(bits):
                 return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+            # operands: (x, w) forward, (dy, w) input gradient, (x, dy) weight gradient
             src = t(inp["g_bits"] if wl.op == "dgrad" else inp["x_bits"])
-            w = t(inp["w_bits"])
+            w = t(inp["g_bits"] if wl.op == "wgrad" else inp["w_bits"])
             dt = torch.bfloat16
         else:
-            src = torch.from_numpy(inp["x"]).to(dev)
-            w = torch.from_numpy(inp["w"]).to(dev)
+            src = torch.from_numpy(inp["g"] if wl.op == "dgrad" else inp["x"]).to(dev)
+            w = torch.from_numpy(inp["g"] if wl.op == "wgrad" else inp["w"]).to(dev)
             dt = torch.float32
         b = torch.from_numpy(inp["b"]).to(dev) if "b" in inp else None
-        out_shape = xs if wl.op == "dgrad" else ys
-        op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
+        out_shape = {"dgrad": xs, "wgrad": ws}.get(wl.op, ys)
+        op = {"fwd": gb.GBCONV_OP_FWD, "dgrad": gb.GBCONV_OP_BWD_DATA, "wgrad": gb.GBCONV_OP_BWD_FILTER}[wl.op]
         family = gb.gbconv_select(d, op)
         flops, nbytes = work(wl)
         # COPIES copies of every operand: a launch's inputs were last touched a full rotation
@@ -203,8 +204,11 @@ def run_gpu(args, rank, world, local_rank):
         reps = COPIES
         copies = [(src.clone(), w.clone(), None if b is None else b.clone(), torch.empty(out_shape, dtype=dt, device=dev))
                   for _ in range(reps)]
+        # the weight gradient's scratch: one buffer serves every copy (launches are stream-ordered)
+        wsp = (torch.empty((gb.gbconv_bwd_filter_workspace(d),), dtype=torch.uint8, device=dev)
+               if wl.op == "wgrad" else None)
         return dict(wl=wl, d=d, copies=copies, family=family, flops=flops, bytes=nbytes, host=inp,
-                    l2_resident=reps * per_copy < int(2.5 * l2))
+                    l2_resident=reps * per_copy < int(2.5 * l2), workspace=wsp)
 
     cases = [make_case(wl) for wl in WORKLOADS]
 
@@ -213,6 +217,10 @@ def run_gpu(args, rank, world, local_rank):
         src, w, b, out = c["copies"][k]
         if c["wl"].op == "dgrad":
             rc = gb.gbconv_bwd_data(c["d"], src.data_ptr(), w.data_ptr(), out.data_ptr(), s)
+        elif c["wl"].op == "wgrad":
+            wsp = c["workspace"]
+            rc = gb.gbconv_bwd_filter(c["d"], src.data_ptr(), w.data_ptr(), out.data_ptr(), None, wsp.data_ptr(),
+                                      wsp.numel(), s)
         else:
             rc = gb.gbconv_fwd(c["d"], src.data_ptr(), w.data_ptr(), None if b is None else b.data_ptr(),
                                out.data_ptr(), s)
@@ -472,8 +480,16 @@ def profile_workload(name: str, reps: int):
         if wl.dtype == "bf16":
             return torch.from_numpy(np.ascontiguousarray(inp[key + "_bits"]).view(np.int16)).cuda().view(torch.bfloat16)
         return torch.from_numpy(inp[key]).cuda()
-    w = dev("w")
     b = torch.from_numpy(inp["b"]).cuda() if "b" in inp else None
+    if wl.op == "wgrad":
+        x, g = dev("x"), dev("g")
+        wsp = torch.empty((gb.gbconv_bwd_filter_workspace(d),), dtype=torch.uint8, device="cuda")
+        for _ in range(reps):
+            gb.conv_bwd_filter(d, x, g, workspace=wsp)
+        gb.device_status()
+        print("ran", name, reps, "times")
+        return
+    w = dev("w")
     src = dev("g" if wl.op == "dgrad" else "x")
     for _ in range(reps):
         if wl.op == "dgrad":

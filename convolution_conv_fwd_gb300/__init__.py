@@ -25,10 +25,11 @@ GBCONV_W_OIHW, GBCONV_W_OHWI = 0, 1
 GBCONV_F32, GBCONV_BF16 = 0, 1
 # kernel families
 KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad",
-           6: "depthwise_dgrad"}
-GBCONV_OP_FWD, GBCONV_OP_BWD_DATA = 0, 1
+           6: "depthwise_dgrad", 7: "direct_wgrad", 8: "wgrad"}
+GBCONV_OP_FWD, GBCONV_OP_BWD_DATA, GBCONV_OP_BWD_FILTER = 0, 1, 2
 
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
+           "gbconv_bwd_filter_workspace", "gbconv_bwd_filter",
            "gbconv_pack_weight", "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
 
 
@@ -60,9 +61,12 @@ def _load():
     lib.gbconv_fwd.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_bwd_data.argtypes = [P(Desc), vp, vp, vp, vp]
     lib.gbconv_conv_transpose.argtypes = [P(Desc), vp, vp, vp, vp, vp]
+    lib.gbconv_bwd_filter_workspace.argtypes = [P(Desc), P(ctypes.c_int64)]
+    lib.gbconv_bwd_filter.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_int64, vp]
     lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
     lib.gbconv_device_status.argtypes = [vp]
-    for f in ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_conv_transpose", "gbconv_fwd", "gbconv_bwd_data", "gbconv_pack_weight",
+    for f in ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_conv_transpose", "gbconv_fwd",
+              "gbconv_bwd_data", "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_pack_weight",
               "gbconv_device_status"):
         getattr(lib, f).restype = st
     lib.gbconv_kernels_launched.argtypes = []
@@ -111,6 +115,20 @@ def gbconv_bwd_data(desc: Desc, dy: int, w: int, dx: int, stream: int) -> int:
 
 def gbconv_conv_transpose(desc: Desc, x: int, w: int, bias: int | None, y: int, stream: int) -> int:
     return _lib.gbconv_conv_transpose(ctypes.byref(desc), x, w, bias or None, y, stream or None)
+
+
+def gbconv_bwd_filter_workspace(desc: Desc) -> int:
+    b = ctypes.c_int64(0)
+    s = _lib.gbconv_bwd_filter_workspace(ctypes.byref(desc), ctypes.byref(b))
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_bwd_filter_workspace")
+    return int(b.value)
+
+
+def gbconv_bwd_filter(desc: Desc, x: int, dy: int, dw: int, db: int | None, workspace: int | None,
+                      workspace_bytes: int, stream: int) -> int:
+    return _lib.gbconv_bwd_filter(ctypes.byref(desc), x, dy, dw, db or None, workspace or None, workspace_bytes,
+                                  stream or None)
 
 
 def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int:
@@ -252,6 +270,38 @@ def conv_bwd_data(d: Desc, dy, w, dx=None):
         torch.cuda.current_stream().synchronize()
         return res
     return out
+
+
+def conv_bwd_filter(d: Desc, x, dy, dw=None, db=None, workspace=None, want_db=False):
+    """Weight gradient (and bias gradient) of the forward convolution ``d`` on the current stream.
+
+    x has the forward input's shape, dy the forward output's; returns ``dw`` (the forward weight's
+    shape and dtype) when no bias gradient is asked for, else ``(dw, db)`` with db float32 [C_out].
+    A bias gradient is asked for by passing ``db`` or ``want_db=True``.  The workspace is a CUDA
+    uint8 tensor of at least ``gbconv_bwd_filter_workspace(d)`` bytes; one is allocated (by torch,
+    not by the library) when none is given.
+    """
+    torch = _torch()
+    xs, ws_, ys = desc_shapes(d)
+    dt = _dtype(d)
+    _check(x, xs, dt, "x")
+    _check(dy, ys, dt, "dy")
+    out = dw if dw is not None else torch.empty(ws_, dtype=dt, device=x.device)
+    _check(out, ws_, dt, "dw")
+    want_db = want_db or db is not None
+    if want_db:
+        db = db if db is not None else torch.empty((d.c_out,), dtype=torch.float32, device=x.device)
+        _check(db, (d.c_out,), torch.float32, "db")
+    need = gbconv_bwd_filter_workspace(d)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
+        raise ValueError("workspace must be a CUDA uint8 tensor of at least %d bytes" % need)
+    s = gbconv_bwd_filter(d, x.data_ptr(), dy.data_ptr(), out.data_ptr(), db.data_ptr() if want_db else None,
+                          workspace.data_ptr(), workspace.numel(), torch.cuda.current_stream().cuda_stream)
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_bwd_filter")
+    return (out, db) if want_db else out
 
 
 def conv_transpose(d: Desc, x, w, bias=None, y=None):

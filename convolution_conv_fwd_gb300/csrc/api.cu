@@ -3,6 +3,7 @@
 #include <cstdio>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -111,6 +112,19 @@ int32_t select_dgrad(const Problem& p, bool aligned) {
   return GBCONV_K_DIRECT_DGRAD;
 }
 
+int32_t select_wgrad(const Problem& p, bool aligned) {
+  if (aligned && wgrad_tc_supported(p)) return GBCONV_K_WGRAD;
+  return GBCONV_K_DIRECT_WGRAD;
+}
+
+int32_t select_op(const Problem& p, int32_t op, bool aligned) {
+  if (op == GBCONV_OP_FWD) return select_fwd(p, aligned);
+  if (op == GBCONV_OP_BWD_DATA) return select_dgrad(p, aligned);
+  return select_wgrad(p, aligned);
+}
+
+bool valid_op(int32_t op) { return op == GBCONV_OP_FWD || op == GBCONV_OP_BWD_DATA || op == GBCONV_OP_BWD_FILTER; }
+
 // The gather dgrad, plus the transposed convolution's bias when one is given.
 gbconv_status bwd_data(const gbconv_desc* desc, const void* dy, const void* w, const float* bias, void* dx,
                        void* stream) {
@@ -151,26 +165,27 @@ gbconv_status gbconv_out_shape(const gbconv_desc* desc, int64_t out[2]) {
 }
 
 gbconv_status gbconv_select(const gbconv_desc* desc, int32_t op, int32_t* kernel) {
-  if (!kernel || (op != GBCONV_OP_FWD && op != GBCONV_OP_BWD_DATA)) return GBCONV_EINVAL;
+  if (!kernel || !valid_op(op)) return GBCONV_EINVAL;
   Problem p;
   gbconv_status s = resolve(desc, &p);
   if (s != GBCONV_OK) return s;
-  *kernel = op == GBCONV_OP_FWD ? select_fwd(p, true) : select_dgrad(p, true);
+  *kernel = select_op(p, op, true);
   return GBCONV_OK;
 }
 
 gbconv_status gbconv_describe(const gbconv_desc* desc, int32_t op, char* buf, int64_t len) {
-  if (!buf || len < 1 || (op != GBCONV_OP_FWD && op != GBCONV_OP_BWD_DATA)) return GBCONV_EINVAL;
+  if (!buf || len < 1 || !valid_op(op)) return GBCONV_EINVAL;
   Problem p;
   gbconv_status s = resolve(desc, &p);
   if (s != GBCONV_OK) return s;
-  const int32_t k = op == GBCONV_OP_FWD ? select_fwd(p, true) : select_dgrad(p, true);
+  const int32_t k = select_op(p, op, true);
   static const char* const names[] = {"direct", "depthwise", "pointwise", "implicit", "dgrad", "direct_dgrad",
-                                      "depthwise_dgrad"};
+                                      "depthwise_dgrad", "direct_wgrad", "wgrad"};
   if ((k == GBCONV_K_IMPLICIT || k == GBCONV_K_DGRAD) &&
       implicit_describe(p, k == GBCONV_K_DGRAD, buf, size_t(len)))
     return GBCONV_OK;
-  std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_DEPTHWISE_DGRAD) ? names[k] : "unknown");
+  if (k == GBCONV_K_WGRAD && wgrad_tc_describe(p, buf, size_t(len))) return GBCONV_OK;
+  std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_WGRAD) ? names[k] : "unknown");
   return GBCONV_OK;
 }
 
@@ -189,6 +204,34 @@ gbconv_status gbconv_fwd(const gbconv_desc* desc, const void* x, const void* w, 
     case GBCONV_K_IMPLICIT: return launch_implicit_fwd(p, x, w, bias, y, l);
     default: return launch_direct_fwd(p, x, w, bias, y, l);
   }
+}
+
+gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc* desc, int64_t* bytes) {
+  if (!bytes) return GBCONV_EINVAL;
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  // Enough for whichever path a call takes (the tensor-core path needs aligned pointers).
+  int64_t b = direct_wgrad_workspace(p);
+  if (wgrad_tc_supported(p)) b = std::max(b, wgrad_tc_workspace(p));
+  *bytes = b;
+  return GBCONV_OK;
+}
+
+gbconv_status gbconv_bwd_filter(const gbconv_desc* desc, const void* x, const void* dy, void* dw, float* db,
+                                void* workspace, int64_t workspace_bytes, void* stream) {
+  Problem p;
+  gbconv_status s = resolve(desc, &p);
+  if (s != GBCONV_OK) return s;
+  if (!x || !dy || !dw) return GBCONV_EINVAL;
+  const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dw) && aligned16(workspace);
+  const int32_t k = select_wgrad(p, aligned);
+  const int64_t need = k == GBCONV_K_WGRAD ? wgrad_tc_workspace(p) : direct_wgrad_workspace(p);
+  if (workspace_bytes < need || (need > 0 && !workspace) || !aligned16(workspace)) return GBCONV_EINVAL;
+  Launch l;
+  if (!device_context(&l, stream)) return GBCONV_ECUDA;
+  if (k == GBCONV_K_WGRAD) return launch_wgrad_tc(p, x, dy, dw, db, workspace, l);
+  return launch_direct_wgrad(p, x, dy, dw, db, workspace, l);
 }
 
 gbconv_status gbconv_bwd_data(const gbconv_desc* desc, const void* dy, const void* w, void* dx, void* stream) {

@@ -66,6 +66,20 @@ gbconv_status launch_implicit_fwd(const Problem& p, const void* x, const void* w
 gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
                                     const Launch& l);
 
+// Weight gradient.  Every path stores fp32 partial sums per position chunk in the caller's workspace,
+// [chunk][element] with elements in OHWI order and then C_out bias-gradient entries, and ends with
+// launch_wgrad_reduce, which adds the chunks in order and writes dw (desc layout and dtype) and db.
+int64_t direct_wgrad_workspace(const Problem& p);
+gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
+                                  const Launch& l);
+gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void* dw, float* db, bool want_db,
+                                  const Launch& l);
+bool wgrad_tc_supported(const Problem& p);
+int64_t wgrad_tc_workspace(const Problem& p);
+gbconv_status launch_wgrad_tc(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
+                              const Launch& l);
+bool wgrad_tc_describe(const Problem& p, char* buf, size_t len);
+
 // Counts one enqueued kernel.
 void note_launch();
 

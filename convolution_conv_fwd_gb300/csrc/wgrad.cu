@@ -1,0 +1,168 @@
+// Weight gradient (and bias gradient) of the convolution, deterministic.
+//
+//   dw[co, cl, kh, kw] = sum over n, oh, ow of dy[n, co, oh, ow] * x[n, g*C_in/G + cl, oh*s_h + kh*d_h - p_h,
+//                                                                    ow*s_w + kw*d_w - p_w]
+//   db[co]             = sum over n, oh, ow of dy[n, co, oh, ow]
+//
+// burn-cubecl `wgrad_im2col` computes dw as one contraction of the output gradient with the input's
+// columns over every (batch, position), and `wgrad_im2col_1x1_split` cuts that contraction into pieces
+// whose partial results are summed afterwards, because the contraction is long and the output small.
+// teeny-kernels `conv2d_backward_dw` instead accumulates every CTA's partial sum into dw with atomics,
+// whose order (and so whose rounding) changes from run to run.  Here the positions are cut into fixed
+// chunks; every partial sum over a chunk is taken in position order by one thread (generic kernel) or
+// by one CTA's tensor-core accumulator (tensor-core kernel) and stored in the caller's workspace; a
+// second kernel adds the chunks in chunk order and rounds once.  The same inputs give the same bits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "problem.h"
+#include "ptx.cuh"
+
+namespace gbconv {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+struct WgArgs {
+  int N, Cin, Cout, H, W, KH, KW, SH, SW, PH, PW, DH, DW, OH, OW;
+  int cpg, opg;
+  int nhwc, ohwi;
+  int E;     // weight-gradient elements, numbered in OHWI order ((co*KH + kh)*KW + kw)*cpg + cl
+  int Etot;  // E plus C_out bias-gradient elements when the bias gradient is wanted
+  int P;     // positions N*OH*OW (the contraction length)
+  int S, L;  // chunks and positions per chunk
+};
+
+__device__ __forceinline__ float ld_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_elem(const bf16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_elem(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elem(bf16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ int64_t act_at(const WgArgs& a, int C, int Hh, int Ww, int n, int c, int h, int w) {
+  return a.nhwc ? ((int64_t(n) * Hh + h) * Ww + w) * C + c : ((int64_t(n) * C + c) * Hh + h) * Ww + w;
+}
+
+// One thread per (weight-gradient element, chunk): the partial sum over the chunk's positions, in
+// position order, with fp32 fused multiply-adds.  Threads of a warp take consecutive c_local, so NHWC
+// x reads are coalesced and the dy read is a broadcast.
+template <typename T>
+__global__ void direct_wgrad_partial_kernel(WgArgs a, const T* __restrict__ x, const T* __restrict__ dy,
+                                            float* __restrict__ ws) {
+  ptx::grid_dep_wait();
+  const int e = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
+  const int s = int(blockIdx.y);
+  if (e >= a.Etot) return;
+  const int p0 = s * a.L, p1 = min(p0 + a.L, a.P);
+  float acc = 0.f;
+  if (p0 < p1) {
+    int ow = p0 % a.OW, q = p0 / a.OW, oh = q % a.OH, n = q / a.OH;
+    if (e < a.E) {
+      int t = e;
+      const int cl = t % a.cpg;
+      t /= a.cpg;
+      const int kw = t % a.KW;
+      t /= a.KW;
+      const int kh = t % a.KH, co = t / a.KH;
+      const int ci = (co / a.opg) * a.cpg + cl;
+      for (int p = p0; p < p1; ++p) {
+        const int ih = oh * a.SH + kh * a.DH - a.PH, iw = ow * a.SW + kw * a.DW - a.PW;
+        if (ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
+          acc = fmaf(ld_elem(dy, act_at(a, a.Cout, a.OH, a.OW, n, co, oh, ow)),
+                     ld_elem(x, act_at(a, a.Cin, a.H, a.W, n, ci, ih, iw)), acc);
+        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; ++n; } }
+      }
+    } else {
+      const int co = e - a.E;
+      for (int p = p0; p < p1; ++p) {
+        acc += ld_elem(dy, act_at(a, a.Cout, a.OH, a.OW, n, co, oh, ow));
+        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; ++n; } }
+      }
+    }
+  }
+  ws[int64_t(s) * a.Etot + e] = acc;
+}
+
+// Adds the S chunk partials of every element in chunk order (in double, so the order is the only
+// thing that fixes the rounding), rounds once, and writes dw in the caller's weight layout and db.
+template <typename T>
+__global__ void wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
+                                    const float* __restrict__ ws, T* __restrict__ dw, float* __restrict__ db) {
+  ptx::grid_dep_wait();
+  const int e = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
+  if (e >= Etot) return;
+  double acc = 0.0;
+  for (int s = 0; s < S; ++s) acc += double(ws[int64_t(s) * Etot + e]);
+  if (e < E) {
+    int t = e;
+    const int cl = t % cpg;
+    t /= cpg;
+    const int kw = t % KW;
+    t /= KW;
+    const int kh = t % KH, co = t / KH;
+    const int64_t o = ohwi ? int64_t(e) : ((int64_t(co) * cpg + cl) * KH + kh) * KW + kw;
+    st_elem(dw, o, float(acc));
+  } else {
+    db[e - E] = float(acc);
+  }
+}
+
+constexpr int kChunkPositions = 256;  // target positions per chunk
+constexpr int kMaxChunks = 64;
+
+WgArgs direct_args(const Problem& p, bool want_db) {
+  WgArgs a{};
+  a.N = int(p.N); a.Cin = int(p.Cin); a.Cout = int(p.Cout);
+  a.H = int(p.H); a.W = int(p.W); a.KH = int(p.KH); a.KW = int(p.KW);
+  a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW); a.DH = int(p.DH); a.DW = int(p.DW);
+  a.OH = int(p.OH); a.OW = int(p.OW);
+  a.cpg = int(p.cpg()); a.opg = int(p.opg());
+  a.nhwc = p.nhwc; a.ohwi = p.ohwi;
+  a.E = int(p.w_elems());
+  a.Etot = a.E + (want_db ? a.Cout : 0);
+  a.P = int(p.N * p.OH * p.OW);
+  a.S = int(std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (int64_t(a.P) + kChunkPositions - 1) / kChunkPositions)));
+  a.L = (a.P + a.S - 1) / a.S;
+  return a;
+}
+
+}  // namespace
+
+int64_t direct_wgrad_workspace(const Problem& p) {
+  const WgArgs a = direct_args(p, true);
+  return ((int64_t(a.S) * a.Etot * 4 + 255) / 256) * 256;
+}
+
+gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void* dw, float* db, bool want_db,
+                                  const Launch& l) {
+  const int E = int(p.w_elems()), Etot = E + (want_db ? int(p.Cout) : 0);
+  const dim3 grid((Etot + 255) / 256), block(256);
+  cudaError_t e;
+  if (p.bf16)
+    e = launch_kernel(wgrad_reduce_kernel<bf16>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                      int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db);
+  else
+    e = launch_kernel(wgrad_reduce_kernel<float>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                      int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db);
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
+                                  const Launch& l) {
+  const WgArgs a = direct_args(p, db != nullptr);
+  float* wsf = static_cast<float*>(ws);
+  const dim3 grid((a.Etot + 255) / 256, a.S), block(256);
+  cudaError_t e;
+  if (p.bf16)
+    e = launch_kernel(direct_wgrad_partial_kernel<bf16>, grid, block, 0, l.stream, a, static_cast<const bf16*>(x),
+                      static_cast<const bf16*>(dy), wsf);
+  else
+    e = launch_kernel(direct_wgrad_partial_kernel<float>, grid, block, 0, l.stream, a, static_cast<const float*>(x),
+                      static_cast<const float*>(dy), wsf);
+  if (e != cudaSuccess) return GBCONV_ECUDA;
+  return launch_wgrad_reduce(p, a.S, wsf, dw, db, db != nullptr, l);
+}
+
+}  // namespace gbconv

@@ -1,6 +1,6 @@
 /*
- * gbconv: convolution forward and input gradient (dgrad) on one NVIDIA GB300
- * (sm_103a), exposed as a plain C ABI.
+ * gbconv: convolution forward, input gradient (dgrad) and weight gradient (wgrad) on one NVIDIA
+ * GB300 (sm_103a), exposed as a plain C ABI.
  *
  * Operations (definitions as the source pages state them):
  *
@@ -18,6 +18,15 @@
  *             Sources: teeny-kernels `conv2d_backward_dx` (the scatter form), oarust `conv_2d_backward`
  *             (an input-gradient pass over input elements, i.e. the gather form).  The library computes the
  *             gather form: every dx element is written once, with no atomics, so results are deterministic.
+ *
+ *   wgrad     dw = the gradient of sum(y * dy) with respect to w:
+ *             dw[co, cl, k] = sum over n and output positions o of dy[n, co, o] * x[n, g*C_in/G + cl, o*stride + k*dil - pad]
+ *             (x zero outside the input), and the bias gradient db[co] = sum over n, o of dy[n, co, o].
+ *             Sources: burn-cubecl `wgrad_im2col` / `wgrad_im2col_1x1` (the contraction of the output gradient
+ *             with the input's columns over every batch position, cut into pieces whose partial sums are added
+ *             afterwards: `wgrad_im2col_1x1_split`), teeny-kernels `conv2d_backward_dw` (one sum per weight
+ *             element, there accumulated with atomics), oarust `conv_2d_backward` (returns the bias gradient
+ *             beside the weight gradient).  The library adds its partial sums in a fixed order, with no atomics.
  *
  *   out size  out = (in + 2*pad - dil*(k - 1) - 1) / stride + 1 (floor), rejected when in + 2*pad < dil*(k-1) + 1.
  *             Source: oarust `Conv1dGeometry::resolve`.
@@ -66,10 +75,12 @@ typedef enum {
   GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
   GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 */
   GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
-  GBCONV_K_DEPTHWISE_DGRAD = 6 /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
+  GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
+  GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
+  GBCONV_K_WGRAD = 8           /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction */
 } gbconv_kernel;
 
-typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1 } gbconv_op;
+typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER = 2 } gbconv_op;
 
 /* One convolution.  For spatial_dims == 1 only index 0 of in/k/stride/pad/dil is read (the length
  * axis); index 1 is ignored.  For spatial_dims == 2 index 0 is height and index 1 is width.
@@ -130,6 +141,25 @@ gbconv_status gbconv_bwd_data(const gbconv_desc *desc, const void *dy, const voi
  * Enqueues exactly one kernel on `stream`.  Deterministic, as gbconv_bwd_data. */
 gbconv_status gbconv_conv_transpose(const gbconv_desc *desc, const void *x, const void *w, const float *bias,
                                     void *y, void *stream);
+
+/* Bytes of device workspace gbconv_bwd_filter needs for this descriptor (a multiple of 256; may be 0).
+ * Launches nothing.  Returns GBCONV_EINVAL for a NULL argument or a shape the forward would reject. */
+gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc *desc, int64_t *bytes);
+
+/* Weight gradient of the forward convolution described by desc, and its bias gradient when db != NULL.
+ *   x         : device, forward input, desc->layout, desc->dtype
+ *   dy        : device, forward-output shape, desc->dtype
+ *   dw        : device, the forward weight's shape per desc->wlayout, desc->dtype; fully overwritten
+ *               (no need to zero it).  Sums are kept in fp32 and rounded once to desc->dtype.
+ *   db        : device float [C_out], fully overwritten, or NULL for no bias gradient
+ *   workspace : device scratch of at least gbconv_bwd_filter_workspace(desc) bytes, 16-byte aligned, owned
+ *               by the caller; its contents are undefined afterwards.  NULL is allowed when 0 bytes are needed.
+ * The sum over batch and positions is cut into fixed chunks; each chunk's partial sums are taken in a
+ * fixed order and the chunks are added in chunk order, so the same inputs give bitwise-equal dw and db.
+ * Enqueues two kernels on `stream` (partial sums, ordered reduction), three when the tensor-core path also
+ * computes db.  Returns GBCONV_EINVAL for NULL tensors or a workspace smaller than required. */
+gbconv_status gbconv_bwd_filter(const gbconv_desc *desc, const void *x, const void *dy, void *dw, float *db,
+                                void *workspace, int64_t workspace_bytes, void *stream);
 
 /* Re-lays a weight from [C_out, C_in/G, KH, KW] (OIHW) into [C_out, KH, KW, C_in/G] (OHWI), the order the
  * NHWC tensor-core kernels read.  desc->dtype gives the element type; desc->wlayout is ignored.

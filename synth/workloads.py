@@ -1,4 +1,4 @@
-"""The five benchmark workloads: tensor shapes and value recipes, nothing else.
+"""The benchmark workloads: tensor shapes and value recipes, nothing else.
 
 Shapes are stated explicitly (including the output-gradient shape of the dgrad
 workload, which its description gives); no convolution arithmetic lives here.
@@ -19,7 +19,7 @@ from . import as_bf16, normal, uniform
 class Workload:
     name: str
     index: int
-    op: str                 # "fwd" or "dgrad"
+    op: str                 # "fwd", "dgrad" or "wgrad"
     dtype: str              # "f32" or "bf16"
     spatial_dims: int
     layout: str             # "ncl" / "nhwc"
@@ -36,7 +36,7 @@ class Workload:
     bias: bool
     x_shape: tuple          # forward input (fwd) -- or dx shape (dgrad)
     w_shape: tuple
-    g_shape: tuple          # output gradient shape (dgrad only)
+    g_shape: tuple          # output gradient shape (dgrad and wgrad)
     recipe: dict = field(default_factory=dict)
     describe: str = ""
 
@@ -76,6 +76,11 @@ EXTRA_WORKLOADS = [
              (1, 1), (1, 1), 1, True, (32, 56, 56, 128), (128, 3, 3, 128), (),
              {"x": ("normal", 1.0), "w": ("normal", (2.0 / (128 * 9)) ** 0.5), "b": ("normal", 0.1)},
              "dense 3x3 conv2d NHWC bf16, N=32, 56x56 -> 28x28, C 128->128, stride 2, pad 1, fp32 bias"),
+    # the weight gradient of the dense 3x3 workload: dW [64, 3, 3, 64] from x and dy, both 32x56x56x64
+    Workload("wgrad3x3_nhwc_bf16", 7, "wgrad", "bf16", 2, "nhwc", "ohwi", 32, 64, 64, (56, 56), (3, 3), (1, 1),
+             (1, 1), (1, 1), 1, False, (32, 56, 56, 64), (64, 3, 3, 64), (32, 56, 56, 64),
+             {"x": ("normal", 1.0), "g": ("normal", 1.0)},
+             "conv2d backward-filter NHWC bf16, 3x3 stride 1 pad 1, x and dy 32x56x56x64 -> dW 64x3x3x64"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
@@ -93,14 +98,19 @@ def _draw(spec, seed, shape):
 def make_inputs(wl: Workload, seed: int | None = None) -> dict:
     """Draw the workload's inputs.
 
-    Returns float32 arrays ``x``/``g`` (input or output gradient), ``w`` and,
-    when the workload has one, float32 ``b``; for bf16 workloads also the
-    uint16 bit patterns ``x_bits``/``g_bits`` and ``w_bits`` of the same values.
+    Returns float32 arrays of the operation's inputs: ``x`` and ``w`` (forward), ``g`` and ``w``
+    (input gradient) or ``x`` and ``g`` (weight gradient), and, when the workload has one, float32
+    ``b``; for bf16 workloads also the uint16 bit patterns (``x_bits``, ``g_bits``, ``w_bits``) of the
+    same values.
     """
     base = 1000 + wl.index if seed is None else seed
     out = {}
-    names = [("g", wl.g_shape)] if wl.op == "dgrad" else [("x", wl.x_shape)]
-    names.append(("w", wl.w_shape))
+    if wl.op == "dgrad":
+        names = [("g", wl.g_shape), ("w", wl.w_shape)]
+    elif wl.op == "wgrad":
+        names = [("x", wl.x_shape), ("g", wl.g_shape)]
+    else:
+        names = [("x", wl.x_shape), ("w", wl.w_shape)]
     for i, (name, shape) in enumerate(names):
         v = _draw(wl.recipe[name], base * 16 + i, shape)
         if wl.dtype == "bf16":

@@ -111,14 +111,16 @@ EXPECTED_FAMILY = {
     "dgrad3x3_s2_nhwc_bf16": {"dgrad"},
     "depthwise3x3_s2_dgrad_nhwc_bf16": {"depthwise_dgrad"},
     "dense3x3_s2_nhwc_bf16": {"implicit"},
+    "wgrad3x3_nhwc_bf16": {"wgrad", "direct_wgrad"},
 }
+
+OPS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
 
 
 @pytest.mark.parametrize("wl", WORKLOADS + EXTRA_WORKLOADS, ids=[w.name for w in WORKLOADS + EXTRA_WORKLOADS])
 def test_workload_kernel_family(gb, wl):
     d = lib_desc(gb, wl)
-    op = gb.GBCONV_OP_BWD_DATA if wl.op == "dgrad" else gb.GBCONV_OP_FWD
-    assert gb.gbconv_select(d, op) in EXPECTED_FAMILY[wl.name]
+    assert gb.gbconv_select(d, OPS[wl.op]) in EXPECTED_FAMILY[wl.name]
 
 
 def test_generic_families_for_other_layouts(gb):
@@ -180,3 +182,28 @@ def test_describe_phases_sources_and_families(gb):
     assert gb._lib.gbconv_describe(ctypes.byref(d), 7, buf, 8) == gb.GBCONV_EINVAL
     assert gb._lib.gbconv_describe(ctypes.byref(d), 0, None, 8) == gb.GBCONV_EINVAL
     assert gb._lib.gbconv_describe(ctypes.byref(d), 0, buf, 0) == gb.GBCONV_EINVAL
+
+
+def test_bwd_filter_workspace_and_argument_checks(gb):
+    d = lib_desc(gb, shape_kw(n=2, in_size=(9, 7), c_in=16, c_out=8))
+    need = gb.gbconv_bwd_filter_workspace(d)
+    assert need > 0 and need % 256 == 0
+    # every family the weight gradient can take, for shapes the forward accepts
+    assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_FILTER) in ("wgrad", "direct_wgrad")
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(layout="nchw", wlayout="oihw", dtype="f32")), 2) == "direct_wgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(groups=2)), 2) == "direct_wgrad"
+    assert gb.gbconv_describe(lib_desc(gb, shape_kw(groups=2)), 2) == "direct_wgrad"
+    # argument errors come back before anything touches a device
+    fake = 1 << 20  # never dereferenced: the calls below fail their checks first
+    assert gb.gbconv_bwd_filter(d, None, fake, fake, None, fake, need, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_filter(d, fake, None, fake, None, fake, need, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_filter(d, fake, fake, None, None, fake, need, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_filter(d, fake, fake, fake, None, fake, need - 256, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_filter(d, fake, fake, fake, None, None, need, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_bwd_filter(d, fake, fake, fake, None, fake + 4, need, None) == gb.GBCONV_EINVAL
+    bad = lib_desc(gb, shape_kw(k=(40, 3)))
+    b = ctypes.c_int64(0)
+    assert gb._lib.gbconv_bwd_filter_workspace(ctypes.byref(bad), ctypes.byref(b)) == gb.GBCONV_EINVAL
+    assert gb._lib.gbconv_bwd_filter_workspace(ctypes.byref(d), None) == gb.GBCONV_EINVAL
+    k = ctypes.c_int32(-1)
+    assert gb._lib.gbconv_select(ctypes.byref(d), 3, ctypes.byref(k)) == gb.GBCONV_EINVAL

@@ -290,6 +290,20 @@ def test_workload_full_size(gb, wl):
     c = oracle_conv(wl)
     inp = make_inputs(wl)
     kw = dict(wl.__dict__)
+    if wl.op == "wgrad":
+        # dW elements (co, c_local, kh, kw): every tap at the channel corners plus a seeded sample; each
+        # oracle element is a full sum over the batch's positions
+        dw, _ = run_wgrad(gb, kw, inp, want_db=wl.bias)
+        idx = _sample_indices((wl.c_out, wl.c_in // wl.groups, wl.k[0], wl.k[1]), 5000 + wl.index, count=160)
+        idx = np.concatenate([idx, np.array([(co, cl, kh, kw_) for co in (0, wl.c_out - 1)
+                                             for cl in (0, wl.c_in // wl.groups - 1)
+                                             for kh in range(wl.k[0]) for kw_ in range(wl.k[1])])], axis=0)
+        ref = oracle.conv_wgrad_points(c, inp["x"], inp["g"], idx)
+        scale = oracle.conv_wgrad_points(c, np.abs(inp["x"]), np.abs(inp["g"]), idx)
+        # dw is OHWI: (co, kh, kw, c_local)
+        check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
+        assert np.isfinite(dw).all()
+        return
     if wl.op == "fwd":
         got = run_fwd(gb, kw, inp)
         oh, ow = c.out_hw()
@@ -315,3 +329,101 @@ def test_workload_full_size(gb, wl):
     check_bf16(sel, ref, scale)
     # global properties: finite everywhere, and nothing left unwritten (the guard fill value is 7.0)
     assert np.isfinite(got).all()
+
+
+# ---------------------------------------------------------------- weight gradient
+
+def draw_wgrad(c, dtype, seed, kind="normal"):
+    """Seeded x and dy for a weight-gradient case (float32 values, and bf16 bits for bf16)."""
+    out = {}
+    for i, (name, shape) in enumerate([("x", c.x_shape()), ("g", c.y_shape())]):
+        v = synth.integers(seed * 16 + i, shape, -3, 3) if kind == "int" else synth.normal(seed * 16 + i, shape, 1.0)
+        if dtype == "bf16":
+            out[name + "_bits"], out[name] = synth.as_bf16(v)
+        else:
+            out[name] = v.astype(np.float32)
+    return out
+
+
+def run_wgrad(gb, kw, inp, want_db=True):
+    d = lib_desc(gb, kw)
+    bits = kw["dtype"] == "bf16"
+    x = to_device(torch, inp["x"], inp.get("x_bits") if bits else None)
+    g = to_device(torch, inp["g"], inp.get("g_bits") if bits else None)
+    _, ws, _ = gb.desc_shapes(d)
+    buf, dw = _guarded(ws, torch.bfloat16 if bits else torch.float32)
+    dbuf, db = _guarded((kw["c_out"],), torch.float32)
+    need = gb.gbconv_bwd_filter_workspace(d)
+    # the workspace starts as garbage: every partial the reduction reads must have been written
+    wsp = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    gb.conv_bwd_filter(d, x, g, dw=dw, db=db if want_db else None, workspace=wsp)
+    gb.device_status()
+    assert _guards_intact(buf), "kernel wrote outside dw"
+    assert _guards_intact(dbuf), "kernel wrote outside db"
+    return to_host_f64(torch, dw), to_host_f64(torch, db)
+
+
+# (shape, expected kernel family)
+WGRAD = [
+    # generic CUDA-core path: fp32 NCL conv1d (the conv1d workload's shape), grouped / strided / dilated
+    # NCHW fp32, NHWC fp32 with OIHW weights, depthwise bf16, NCHW bf16
+    (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
+              layout="ncl", wlayout="oik", dtype="f32"), "direct_wgrad"),
+    (shape_kw(n=2, in_size=(11, 9), c_in=6, c_out=9, groups=3, k=(3, 2), stride=(2, 1), pad=(1, 0), dil=(1, 2),
+              layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
+    (shape_kw(n=3, in_size=(10, 12), c_in=16, c_out=8, wlayout="oihw", dtype="f32", stride=(2, 2)), "direct_wgrad"),
+    (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "direct_wgrad"),
+    (shape_kw(n=1, in_size=(9, 8), c_in=16, c_out=8, layout="nchw", wlayout="oihw", stride=(2, 2)), "direct_wgrad"),
+    # NHWC bf16, dense: 3x3 (several chunks), 1x1 at stride 2, 5x5 with dilation
+    (shape_kw(n=4, in_size=(20, 21), c_in=64, c_out=64, k=(3, 3), pad=(1, 1)), "direct_wgrad"),
+    (shape_kw(n=2, in_size=(15, 14), c_in=32, c_out=48, k=(1, 1), pad=(0, 0), stride=(2, 2)), "direct_wgrad"),
+    (shape_kw(n=1, in_size=(13, 12), c_in=16, c_out=24, k=(5, 5), pad=(2, 2), dil=(1, 2)), "direct_wgrad"),
+]
+
+
+def _wgrad_ids():
+    return ["%s-%d" % (fam, i) for i, (_, fam) in enumerate(WGRAD)]
+
+
+@pytest.mark.parametrize("case", range(len(WGRAD)), ids=_wgrad_ids())
+def test_wgrad_matches_oracle(gb, case):
+    kw, family = WGRAD[case]
+    d = lib_desc(gb, kw)
+    assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_FILTER) == family
+    c = oracle_conv(kw)
+    inp = draw_wgrad(c, kw["dtype"], 700 + case)
+    dw, db = run_wgrad(gb, kw, inp)
+    ref = oracle.conv_wgrad(c, inp["x"], inp["g"])
+    scale = oracle.conv_wgrad(c, np.abs(inp["x"]), np.abs(inp["g"]))
+    assert dw.shape == ref.shape
+    if kw["dtype"] == "f32":
+        check_f32(dw, ref, scale)
+    else:
+        check_bf16(dw, ref, scale)
+    # the bias gradient is always float32
+    check_f32(db, oracle.conv_bgrad(c, inp["g"]), oracle.conv_bgrad(c, np.abs(inp["g"])))
+
+
+@pytest.mark.parametrize("case", range(len(WGRAD)), ids=_wgrad_ids())
+def test_wgrad_integer_inputs_bit_exact(gb, case):
+    kw, _ = WGRAD[case]
+    c = oracle_conv(kw)
+    inp = draw_wgrad(c, kw["dtype"], 800 + case, kind="int")
+    dw, db = run_wgrad(gb, kw, inp)
+    ref = oracle.conv_wgrad(c, inp["x"], inp["g"])
+    if kw["dtype"] == "bf16":
+        ref = bf16_round(ref)
+    np.testing.assert_array_equal(dw, ref)
+    np.testing.assert_array_equal(db, oracle.conv_bgrad(c, inp["g"]))
+
+
+def test_wgrad_is_deterministic_and_db_optional(gb):
+    kw, _ = WGRAD[5]
+    c = oracle_conv(kw)
+    inp = draw_wgrad(c, "bf16", 900)
+    dw1, db1 = run_wgrad(gb, kw, inp)
+    dw2, db2 = run_wgrad(gb, kw, inp)
+    dw3, db3 = run_wgrad(gb, kw, inp, want_db=False)
+    assert np.array_equal(dw1, dw2) and np.array_equal(db1, db2)
+    assert np.array_equal(dw1, dw3)
+    assert np.all(db3 == 7.0)  # not asked for: untouched
