@@ -68,12 +68,14 @@ gbconv_status launch_implicit_dgrad(const Problem& p, const void* dy, const void
 
 // Weight gradient.  Every path stores fp32 partial sums per position chunk in the caller's workspace,
 // [chunk][element] with elements in OHWI order and then C_out bias-gradient entries, and ends with
-// launch_wgrad_reduce, which adds the chunks in order and writes dw (desc layout and dtype) and db.
+// launch_wgrad_reduce, which adds the chunks in a fixed order and writes dw (desc layout and dtype) and db.
 int64_t direct_wgrad_workspace(const Problem& p);
 gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
                                   const Launch& l);
 gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void* dw, float* db, bool want_db,
                                   const Launch& l);
+// Bias-gradient partial sums only, over S equal position chunks, into ws [S][E + C_out] entries E..
+gbconv_status launch_bgrad_partials(const Problem& p, const void* dy, int S, float* ws, const Launch& l);
 bool wgrad_tc_supported(const Problem& p);
 int64_t wgrad_tc_workspace(const Problem& p);
 gbconv_status launch_wgrad_tc(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,

@@ -11,7 +11,7 @@
 // whose order (and so whose rounding) changes from run to run.  Here the positions are cut into fixed
 // chunks; every partial sum over a chunk is taken in position order by one thread (generic kernel) or
 // by one CTA's tensor-core accumulator (tensor-core kernel) and stored in the caller's workspace; a
-// second kernel adds the chunks in chunk order and rounds once.  The same inputs give the same bits.
+// second kernel adds the chunks in a fixed order and rounds once.  The same inputs give the same bits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,6 +32,7 @@ struct WgArgs {
   int nhwc, ohwi;
   int E;     // weight-gradient elements, numbered in OHWI order ((co*KH + kh)*KW + kw)*cpg + cl
   int Etot;  // E plus C_out bias-gradient elements when the bias gradient is wanted
+  int e0;    // first element this launch computes (E: the bias gradient only)
   int P;     // positions N*OH*OW (the contraction length)
   int S, L;  // chunks and positions per chunk
 };
@@ -52,7 +53,7 @@ template <typename T>
 __global__ void direct_wgrad_partial_kernel(WgArgs a, const T* __restrict__ x, const T* __restrict__ dy,
                                             float* __restrict__ ws) {
   ptx::grid_dep_wait();
-  const int e = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
+  const int e = a.e0 + int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
   const int s = int(blockIdx.y);
   if (e >= a.Etot) return;
   const int p0 = s * a.L, p1 = min(p0 + a.L, a.P);
@@ -85,16 +86,42 @@ __global__ void direct_wgrad_partial_kernel(WgArgs a, const T* __restrict__ x, c
   ws[int64_t(s) * a.Etot + e] = acc;
 }
 
-// Adds the S chunk partials of every element in chunk order (in double, so the order is the only
-// thing that fixes the rounding), rounds once, and writes dw in the caller's weight layout and db.
+// Adds the S chunk partials of every element in a fixed order, rounds once, and writes dw in the
+// caller's weight layout and db.  A block takes 32 consecutive elements; warp j sums chunks
+// [j*S/8, (j+1)*S/8) of its lane's element in chunk order, then the eight slice sums are added in
+// slice order.  Every sum is compensated (Kahan): the order fixes the bits, and the compensation
+// keeps the fp32 sum of up to a few hundred partials close to the exact one.
 template <typename T>
-__global__ void wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
-                                    const float* __restrict__ ws, T* __restrict__ dw, float* __restrict__ db) {
+__global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
+                                                           const float* __restrict__ ws, T* __restrict__ dw,
+                                                           float* __restrict__ db) {
   ptx::grid_dep_wait();
-  const int e = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);
-  if (e >= Etot) return;
-  double acc = 0.0;
-  for (int s = 0; s < S; ++s) acc += double(ws[int64_t(s) * Etot + e]);
+  __shared__ float part[8][32];
+  const int lane = int(threadIdx.x) & 31, j = int(threadIdx.x) >> 5;
+  const int e = int(blockIdx.x) * 32 + lane;
+  float acc = 0.f, comp = 0.f;
+  if (e < Etot) {
+    const int s0 = (j * S) / 8, s1 = ((j + 1) * S) / 8;
+#pragma unroll 4
+    for (int s = s0; s < s1; ++s) {
+      const float y = ws[int64_t(s) * Etot + e] - comp;
+      const float t = acc + y;
+      comp = (t - acc) - y;
+      acc = t;
+    }
+  }
+  part[j][lane] = acc - comp;
+  __syncthreads();
+  if (j != 0 || e >= Etot) return;
+  acc = 0.f;
+  comp = 0.f;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    const float y = part[jj][lane] - comp;
+    const float t = acc + y;
+    comp = (t - acc) - y;
+    acc = t;
+  }
   if (e < E) {
     int t = e;
     const int cl = t % cpg;
@@ -103,9 +130,9 @@ __global__ void wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int 
     t /= KW;
     const int kh = t % KH, co = t / KH;
     const int64_t o = ohwi ? int64_t(e) : ((int64_t(co) * cpg + cl) * KH + kh) * KW + kw;
-    st_elem(dw, o, float(acc));
+    st_elem(dw, o, acc);
   } else {
-    db[e - E] = float(acc);
+    db[e - E] = acc;
   }
 }
 
@@ -122,6 +149,7 @@ WgArgs direct_args(const Problem& p, bool want_db) {
   a.nhwc = p.nhwc; a.ohwi = p.ohwi;
   a.E = int(p.w_elems());
   a.Etot = a.E + (want_db ? a.Cout : 0);
+  a.e0 = 0;
   a.P = int(p.N * p.OH * p.OW);
   a.S = int(std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (int64_t(a.P) + kChunkPositions - 1) / kChunkPositions)));
   a.L = (a.P + a.S - 1) / a.S;
@@ -138,7 +166,7 @@ int64_t direct_wgrad_workspace(const Problem& p) {
 gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void* dw, float* db, bool want_db,
                                   const Launch& l) {
   const int E = int(p.w_elems()), Etot = E + (want_db ? int(p.Cout) : 0);
-  const dim3 grid((Etot + 255) / 256), block(256);
+  const dim3 grid((Etot + 31) / 32), block(256);
   cudaError_t e;
   if (p.bf16)
     e = launch_kernel(wgrad_reduce_kernel<bf16>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
@@ -149,11 +177,11 @@ gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 
-gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
-                                  const Launch& l) {
-  const WgArgs a = direct_args(p, db != nullptr);
-  float* wsf = static_cast<float*>(ws);
-  const dim3 grid((a.Etot + 255) / 256, a.S), block(256);
+namespace {
+
+gbconv_status launch_partials(const WgArgs& a, const Problem& p, const void* x, const void* dy, float* wsf,
+                              const Launch& l) {
+  const dim3 grid((a.Etot - a.e0 + 255) / 256, a.S), block(256);
   cudaError_t e;
   if (p.bf16)
     e = launch_kernel(direct_wgrad_partial_kernel<bf16>, grid, block, 0, l.stream, a, static_cast<const bf16*>(x),
@@ -161,8 +189,26 @@ gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* d
   else
     e = launch_kernel(direct_wgrad_partial_kernel<float>, grid, block, 0, l.stream, a, static_cast<const float*>(x),
                       static_cast<const float*>(dy), wsf);
-  if (e != cudaSuccess) return GBCONV_ECUDA;
+  return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+}
+
+}  // namespace
+
+gbconv_status launch_direct_wgrad(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
+                                  const Launch& l) {
+  const WgArgs a = direct_args(p, db != nullptr);
+  float* wsf = static_cast<float*>(ws);
+  const gbconv_status st = launch_partials(a, p, x, dy, wsf, l);
+  if (st != GBCONV_OK) return st;
   return launch_wgrad_reduce(p, a.S, wsf, dw, db, db != nullptr, l);
+}
+
+gbconv_status launch_bgrad_partials(const Problem& p, const void* dy, int S, float* ws, const Launch& l) {
+  WgArgs a = direct_args(p, true);
+  a.e0 = a.E;
+  a.S = S;
+  a.L = (a.P + S - 1) / S;
+  return launch_partials(a, p, nullptr, dy, ws, l);
 }
 
 }  // namespace gbconv

@@ -1,13 +1,533 @@
-// Weight gradient on the tensor cores (NHWC bf16): planned, not yet enabled.
+// Weight gradient on the 5th-generation tensor cores (tcgen05, accumulators in TMEM), NHWC bf16,
+// unit stride, one group.
+//
+// The contraction (burn-cubecl `wgrad_im2col`: [C_out, positions] x [positions, taps * C_in]) runs
+// over positions of the same virtual grid the forward uses: R output rows of P = OW + (KW-1)*DW
+// columns per image.  x is read through the virtual grid (x_v row r = input row r - PH, column
+// c = input column c - PW, zero outside the image) and dy through the same grid (columns past OW
+// are zero), so tap (kh, kw) pairs dy position q with x_v position q + kh*DH*P + kw*DW: every tap is a
+// shifted window, and since every tap's product is a separate output no shifted sums are needed.
+//
+// One MMA covers many taps at once.  Both operands are position-major in shared memory (MN-major,
+// 128-byte swizzle, one 128-byte row of 64 channels per position), and an MN-major operand wider than
+// 64 is a row of 64-wide atoms at a stride the descriptor states (its leading-byte offset):
+//   A (M = 128) = two x atoms DH*P positions apart: kernel rows kh and kh+1 of 64 input channels;
+//   B (N = 64*KW) = KW dy atoms DW positions apart: kernel columns KW-1 .. 0 of 64 output channels.
+// D[(kh, ci), (kw, co)] accumulates the product of x at q + kh*DH*P and dy at q - (KW-1-j)*DW
+// (j = the atom), which is tap (kh, kw = KW-1-j) of the weight gradient.  ceil(KH/2) such MMAs per
+// 16 positions cover every tap (a 3x3: two MMAs of M=128, N=192, the second one half used).
+//
+// Work: one CTA per (64-channel input block, 64-channel output block, chunk of output rows).  A chunk
+// is a run of row blocks (RB rows, with RB*P a multiple of 8 so every TMA box lands on a 1024-byte
+// boundary); it is loaded whole into shared memory as boxes of RB virtual rows (x and dy, one
+// barrier each) and swept by the MMAs as the boxes land.  At the end the accumulators go to the
+// caller's workspace as fp32 partial sums [chunk][co][kh][kw][ci]; launch_wgrad_reduce then adds the
+// chunks in chunk order.  No atomics anywhere: the result is deterministic.
+//
+// Roles: warps 0-7 epilogue (TMEM -> workspace), warp 8 TMEM allocation and MMA issue (lane 0),
+// warp 9 zero fill and TMA loads (lane 0 issues).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
 #include "problem.h"
+#include "ptx.cuh"
 
 namespace gbconv {
+namespace {
 
-bool wgrad_tc_supported(const Problem&) { return false; }
-int64_t wgrad_tc_workspace(const Problem&) { return 0; }
-gbconv_status launch_wgrad_tc(const Problem&, const void*, const void*, void*, float*, void*, const Launch&) {
-  return GBCONV_EUNSUPPORTED;
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kFront = 8;       // zero positions ahead of the dy rows: the dy atoms reach back (KW-1)*DW <= 8
+constexpr int kMaxBoxes = 24;   // per segment, for x and for dy
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kStepBlock = 4;   // 16-position MMA steps issued back to back
+
+struct TcArgs {
+  float* ws;              // [chunk][ws_stride] fp32 partial sums, elements in OHWI order
+  unsigned int* status;
+  int Cin, Cout, KH, KW, DH, DW, PH, PW;
+  int P;                  // virtual grid pitch OW + (KW-1)*DW
+  int RB;                 // virtual rows per TMA box
+  int box_bytes;          // RB * P * 128
+  int cb_in, pairs, chunks, units;
+  int bpi, total_blocks;  // row blocks per image, row blocks in the batch
+  int seg_blocks;         // row blocks one shared-memory load holds
+  int xe;                 // x boxes a segment needs beyond its dy boxes
+  int gm;                 // MMA groups per 16 positions: ceil(KH / 2)
+  int x_bytes;            // x region bytes (the dy region follows)
+  int tail;               // zero positions needed after a segment's dy rows
+  int ws_stride;          // floats per chunk in the workspace
+  uint32_t idesc;
+};
+
+struct TcMaps {
+  CUtensorMap x;   // (C_in, W, H, N), box (64, P, RB, 1)
+  CUtensorMap dy;  // (C_out, OW, OH, N), box (64, P, RB, 1)
+};
+
+struct Segment {
+  int n, rb, nb;  // image, first row block, row blocks
+};
+
+// The segments of a chunk, in order: runs of its row blocks inside one image, at most seg_blocks long.
+struct SegWalk {
+  int b, b1, bpi, cap;
+  __device__ SegWalk(const TcArgs& a, int chunk) {
+    b = int((int64_t(chunk) * a.total_blocks) / a.chunks);
+    b1 = int((int64_t(chunk + 1) * a.total_blocks) / a.chunks);
+    bpi = a.bpi;
+    cap = a.seg_blocks;
+  }
+  __device__ bool next(Segment& s) {
+    if (b >= b1) return false;
+    s.n = b / bpi;
+    s.rb = b - s.n * bpi;
+    s.nb = min(min(b1 - b, bpi - s.rb), cap);
+    b += s.nb;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+      "%6}], [%2];" ::"r"(dst),
+      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
 }
-bool wgrad_tc_describe(const Problem&, char*, size_t) { return false; }
+
+// MN-major operand, 128-byte swizzle: `atom_stride` bytes between 64-element atoms along M (or N),
+// 1024 bytes between 8-position groups along K.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t atom_stride) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// GM: MMA groups per 16 positions (ceil(KH/2)), a template parameter so a block of steps issues its
+// MMAs back to back: scalar work between MMAs in the issuing thread adds directly to their time.
+template <int GM>
+__global__ void __launch_bounds__(kThreads, 1)
+    wgrad_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* xs = smem;
+  uint8_t* ys = smem + a.x_bytes;  // position 0 of the dy region; the dy rows start at kFront
+  const int y_bytes = ((kFront * 128 + a.seg_blocks * a.box_bytes + a.tail * 128) + 1023) & ~1023;
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(ys + y_bytes);
+  uint64_t* ybar = xbar + kMaxBoxes;
+  uint64_t* seg_done = ybar + kMaxBoxes;
+  uint64_t* acc_full = seg_done + 1;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* fin = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t tmem_cols = GM * a.KW * 64 <= 256 ? 256u : 512u;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxBoxes; ++i) { ptx::mbar_init(xbar + i, 1); ptx::mbar_init(ybar + i, 1); }
+    ptx::mbar_init(seg_done, 1);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(acc_empty, kEpiWarps * 32);
+    ptx::mbar_init(fin, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(tmem_slot, tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ zero fill and TMA producer
+    for (int i = lane; i < kFront * 8; i += 32)  // the front pad, never written by TMA
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ptx::smem_addr(ys) + uint32_t(i) * 16u), "r"(0u)
+                   : "memory");
+    if (lane == 0) {
+      ptx::prefetch_tmap(&maps.x);
+      ptx::prefetch_tmap(&maps.dy);
+    }
+    bool ok = true;
+    int seg = 0;  // segments this CTA has loaded: the phase of every box barrier
+    for (int u = int(blockIdx.x); ok && u < a.units; u += int(gridDim.x)) {
+      const int chunk = u / a.pairs, pair = u - chunk * a.pairs;
+      const int cib = pair % a.cb_in, cob = pair / a.cb_in;
+      SegWalk walk(a, chunk);
+      Segment sg;
+      while (ok && walk.next(sg)) {
+        if (seg > 0) {  // the previous segment's MMAs have finished reading shared memory
+          if (lane == 0) ok = ptx::mbar_wait(seg_done, uint32_t(seg - 1) & 1u, abort_flag, a.status, 1u);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+        }
+        // The last MMAs of a segment read up to tail positions past its dy rows: zero them (a
+        // longer earlier segment may have left dy rows there), then order the writes before the
+        // tensor core's reads.
+        const uint32_t tail0 = ptx::smem_addr(ys) + uint32_t(kFront * 128 + sg.nb * a.box_bytes);
+        for (int i = lane; i < a.tail * 8; i += 32)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(tail0 + uint32_t(i) * 16u), "r"(0u)
+                       : "memory");
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int nxb = sg.nb + a.xe;
+          const int row0 = sg.rb * a.RB;  // first virtual row of the segment
+          for (int b = 0; b < kMaxBoxes; ++b) {
+            // Boxes the segment does not need still complete a phase, so every barrier's phase
+            // stays the segment count.
+            if (b < nxb) {
+              ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
+              tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
+                          row0 + b * a.RB - a.PH, sg.n);
+            } else {
+              ptx::mbar_arrive(xbar + b);
+            }
+            if (b < sg.nb) {
+              ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(a.box_bytes));
+              tma_load_4d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
+                          cob * 64, 0, row0 + b * a.RB, sg.n);
+            } else {
+              ptx::mbar_arrive(ybar + b);
+            }
+          }
+        }
+        __syncwarp();
+        ++seg;
+      }
+    }
+    // Leave no copy in flight: wait (bounded, whatever the abort state) for the last segment's boxes.
+    if (lane == 0 && seg > 0) {
+      const uint64_t t0 = ptx::globaltimer();
+      for (int b = 0; b < 2 * kMaxBoxes; ++b) {
+        uint64_t* bar = b < kMaxBoxes ? xbar + b : ybar + (b - kMaxBoxes);
+        while (!ptx::mbar_try_wait(bar, uint32_t(seg - 1) & 1u) && ptx::globaltimer() - t0 < 200000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int seg = 0, it = 0;
+      // Everything the loop needs, in registers: kernel parameters live in memory, and every MMA's
+      // asm statement clobbers memory, so fields read inside the loop would be reloaded per MMA.
+      const int P = a.P, KW = a.KW, xe = a.xe, units = a.units, pairs = a.pairs;
+      const int box_pos = a.RB * a.P;                      // positions per box
+      const int xreach = (2 * GM - 1) * a.DH * P;          // farthest x position an MMA reads past k
+      const uint32_t idesc = a.idesc;
+      const uint32_t ncols = uint32_t(KW * 64);
+      // Descriptor words at k = 0.  A step of 16 positions is 2048 bytes, +128 in the start field;
+      // group g's A starts 2g*DH*P positions on.
+      const uint64_t ad0 = desc_mn_sw128(ptx::smem_addr(xs), uint32_t(a.DH * P) * 128u);
+      const uint64_t bd0 = desc_mn_sw128(ptx::smem_addr(ys) + uint32_t(kFront - (KW - 1) * a.DW) * 128u,
+                                         uint32_t(a.DW) * 128u);
+      const uint32_t a_lo0 = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
+      const uint32_t b_lo0 = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+      const uint32_t g_step = uint32_t(2 * a.DH * P) * 8u;  // (2*DH*P*128) >> 4
+      for (int u = int(blockIdx.x); ok && u < units; u += int(gridDim.x), ++it) {
+        if (it > 0) {  // the epilogue has taken the previous unit's accumulators
+          if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u))) break;
+          ptx::tc_fence_after();
+        }
+        SegWalk walk(a, u / pairs);
+        Segment sg;
+        bool first = true;
+        while (ok && walk.next(sg)) {
+          const int nb = sg.nb, nxb = sg.nb + xe;
+          const int nk = (nb * box_pos + (KW - 1) * a.DW + 15) / 16;
+          const uint32_t ph = uint32_t(seg) & 1u;
+          int xw = 0, yw = 0;  // boxes already waited for
+          // Blocks of kStepBlock steps: the boxes the whole block reads are waited for first, then its
+          // MMAs go out back to back.
+          for (int t0 = 0; ok && t0 < nk; t0 += kStepBlock) {
+            const int tn = min(kStepBlock, nk - t0);
+            const int kend = 16 * (t0 + tn - 1) + 15;  // last position the block reads (before the shifts)
+            while (ok && yw < nb && kend >= yw * box_pos) ok = ptx::mbar_wait(ybar + yw++, ph, abort_flag, a.status, 2u);
+            while (ok && xw < nxb && kend + xreach >= xw * box_pos)
+              ok = ptx::mbar_wait(xbar + xw++, ph, abort_flag, a.status, 2u);
+            if (!ok) break;
+            const uint32_t a_lo = a_lo0 + uint32_t(t0) * 128u, b_lo = b_lo0 + uint32_t(t0) * 128u;
+            const uint32_t acc0 = (first && t0 == 0) ? 0u : 1u;
+            if (tn == kStepBlock) {
+#pragma unroll
+              for (int i = 0; i < kStepBlock; ++i)
+#pragma unroll
+                for (int g = 0; g < GM; ++g)
+                  ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
+                                     b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
+            } else {
+              for (int i = 0; i < tn; ++i)
+#pragma unroll
+                for (int g = 0; g < GM; ++g)
+                  ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
+                                     b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
+            }
+          }
+          ptx::mma_commit(seg_done);
+          first = false;
+          ++seg;
+        }
+        if (ok) ptx::mma_commit(acc_full);
+      }
+      ptx::mma_commit(fin);
+      ptx::mbar_wait(fin, 0, abort_flag, a.status, 2u);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue: TMEM -> workspace
+    // Warps w and w+4 share TMEM lanes 32*(w%4).. and split the 16-column chunks.  Lane m holds
+    // kernel row 2g + m/64 and input channel m%64 of the block; column n holds kernel column
+    // KW-1 - n/64 and output channel n%64.  Consecutive lanes store consecutive input channels.
+    const int q = warp & 3, h = warp >> 2;
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    const int m = q * 32 + lane;
+    const int i_atom = m >> 6, cil = m & 63;
+    const size_t co_stride = size_t(a.KH) * a.KW * a.Cin;
+    int it = 0;
+    for (int u = int(blockIdx.x); u < a.units; u += int(gridDim.x), ++it) {
+      // One thread waits for the accumulators, polling at most every microsecond; the others block
+      // on a hardware barrier.  256 threads polling the mbarrier through the whole MMA phase would
+      // take shared-memory bandwidth from the tensor core's operand reads.
+      if (threadIdx.x == 0) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(acc_full, uint32_t(it) & 1u)) {
+          if (*abort_flag) break;
+          if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(a.status, 4u);
+            break;
+          }
+          __nanosleep(1000);
+        }
+      }
+      // The barrier also makes the give-up decision common to all epilogue threads (the TMEM loads
+      // below are warp-collective).
+      uint32_t stop;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(stop)
+          : "r"(uint32_t(*abort_flag)), "n"(kEpiWarps * 32)
+          : "memory");
+      if (stop) break;
+      ptx::tc_fence_after();
+      const int chunk = u / a.pairs, pair = u - chunk * a.pairs;
+      const int cib = pair % a.cb_in, cob = pair / a.cb_in;
+      const int ci = cib * 64 + cil;
+      float* const wsc = a.ws + size_t(chunk) * a.ws_stride;
+      for (int g = 0; g < a.gm; ++g) {
+        const int kh = 2 * g + i_atom;
+        for (int cc = h; cc < 4 * a.KW; cc += 2) {  // 16-column chunks
+          uint32_t v[16];
+          ptx::tmem_ld_16(tmem + lane_base + uint32_t(g * a.KW * 64 + cc * 16), v);
+          ptx::tmem_ld_wait();
+          const int kw = a.KW - 1 - (cc >> 2);
+          const int co0 = cob * 64 + (cc & 3) * 16;
+          if (kh < a.KH && ci < a.Cin) {
+            float* dst = wsc + ((size_t(co0) * a.KH + kh) * a.KW + kw) * a.Cin + ci;
+            const int nco = min(16, a.Cout - co0);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              if (c < nco) *dst = __uint_as_float(v[c]);
+              dst += co_stride;
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(acc_empty);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, tmem_cols);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// SMs of the current device (the chunk count, and so the workspace size, follow it); 152 when no
+// device can be queried.
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      sms > 0)
+    return sms;
+  cudaGetLastError();
+  return 152;
+}
+
+int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
+
+struct TcPlan {
+  TcArgs a;
+  size_t smem;
+  int grid;
+  int N, H, W, OH, OW;
+};
+
+bool plan(const Problem& p, int sms, TcPlan& pl) {
+  if (!(p.bf16 && p.nhwc && p.G == 1 && p.SH == 1 && p.SW == 1)) return false;
+  if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides
+  if (p.KW > 4 || (p.KW - 1) * p.DW > kFront) return false;
+  const int gm = int((p.KH + 1) / 2);
+  if (gm > 2 || gm * p.KW * 64 > 512) return false;  // the accumulators must fit TMEM
+  const int64_t P = p.OW + (p.KW - 1) * p.DW;
+  if (P > 256) return false;  // TMA box extent
+  if (p.DH * P * 128 >= (int64_t(1) << 18)) return false;  // the A atom stride must fit its descriptor field
+  pl = TcPlan{};
+  TcArgs& a = pl.a;
+  a.Cin = int(p.Cin); a.Cout = int(p.Cout); a.KH = int(p.KH); a.KW = int(p.KW);
+  a.DH = int(p.DH); a.DW = int(p.DW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.P = int(P);
+  a.RB = 8 / gcd(int(P), 8);
+  a.box_bytes = a.RB * a.P * 128;
+  a.gm = gm;
+  // x rows past a segment's dy rows that its last MMAs read: the second atom of the last group
+  // reaches (2*gm - 1)*DH rows down, the dy atoms (KW-1)*DW positions and a 16-position step on.
+  const int64_t reach = int64_t(2 * gm - 1) * p.DH * P + (p.KW - 1) * p.DW + 16;
+  a.xe = int((reach + a.RB * P - 1) / (a.RB * P));
+  a.tail = int((p.KW - 1) * p.DW + 16);
+  a.seg_blocks = 0;
+  for (int sb = kMaxBoxes - a.xe; sb >= 1; --sb) {
+    const int64_t xb = int64_t(sb + a.xe) * a.box_bytes;
+    const int64_t yb = ((int64_t(kFront + a.tail) * 128 + int64_t(sb) * a.box_bytes) + 1023) & ~int64_t(1023);
+    const int64_t total = 1024 + xb + yb + (2 * kMaxBoxes + 4) * 8 + 16;
+    if (total <= kSmemLimit) {
+      a.seg_blocks = sb;
+      a.x_bytes = int(xb);
+      // at least half the SM's shared memory: one CTA per SM, so no second CTA waits for TMEM
+      pl.smem = size_t(std::max<int64_t>(total, kSmemLimit / 2 + 1024));
+      break;
+    }
+  }
+  if (a.seg_blocks == 0) return false;
+  a.bpi = int((p.OH + a.RB - 1) / a.RB);
+  const int64_t tb = p.N * a.bpi;
+  if (tb >= (int64_t(1) << 30)) return false;
+  a.total_blocks = int(tb);
+  a.cb_in = int((p.Cin + 63) / 64);
+  const int cb_out = int((p.Cout + 63) / 64);
+  a.pairs = a.cb_in * cb_out;
+  a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / a.pairs)));
+  a.units = a.pairs * a.chunks;
+  pl.grid = std::max(1, std::min(a.units, sms));
+  // A and B both MN-major (transpose bits 15 and 16), M = 128, N = 64 per kernel column
+  a.idesc = ptx::idesc_bf16_f32(128, 64 * a.KW) | (1u << 15) | (1u << 16);
+  pl.N = int(p.N); pl.H = int(p.H); pl.W = int(p.W); pl.OH = int(p.OH); pl.OW = int(p.OW);
+  return true;
+}
+
+bool encode(const TcPlan& pl, const void* x, const void* dy, TcMaps& maps) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const TcArgs& a = pl.a;
+  const cuuint32_t box[4] = {64, cuuint32_t(a.P), cuuint32_t(a.RB), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  {
+    const cuuint64_t dims[4] = {cuuint64_t(a.Cin), cuuint64_t(pl.W), cuuint64_t(pl.H), cuuint64_t(pl.N)};
+    const cuuint64_t strides[3] = {cuuint64_t(a.Cin) * 2, cuuint64_t(pl.W) * a.Cin * 2,
+                                   cuuint64_t(pl.H) * pl.W * a.Cin * 2};
+    if (fn(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const cuuint64_t dims[4] = {cuuint64_t(a.Cout), cuuint64_t(pl.OW), cuuint64_t(pl.OH), cuuint64_t(pl.N)};
+  const cuuint64_t strides[3] = {cuuint64_t(a.Cout) * 2, cuuint64_t(pl.OW) * a.Cout * 2,
+                                 cuuint64_t(pl.OH) * pl.OW * a.Cout * 2};
+  return fn(&maps.dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool wgrad_tc_supported(const Problem& p) {
+  TcPlan pl;
+  return plan(p, device_sms(), pl);
+}
+
+int64_t wgrad_tc_workspace(const Problem& p) {
+  TcPlan pl;
+  if (!plan(p, device_sms(), pl)) return 0;
+  return ((int64_t(pl.a.chunks) * (p.w_elems() + p.Cout) * 4 + 255) / 256) * 256;
+}
+
+bool wgrad_tc_describe(const Problem& p, char* buf, size_t len) {
+  TcPlan pl;
+  if (!plan(p, device_sms(), pl)) return false;
+  const TcArgs& a = pl.a;
+  std::snprintf(buf, len,
+                "wgrad_tc pairs=%d chunks=%d units=%d grid=%d rows_per_box=%d pitch=%d seg_blocks=%d x_extra=%d "
+                "groups=%d n=%d smem=%zu",
+                a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KW, pl.smem);
+  return true;
+}
+
+gbconv_status launch_wgrad_tc(const Problem& p, const void* x, const void* dy, void* dw, float* db, void* ws,
+                              const Launch& l) {
+  TcPlan pl;
+  if (!plan(p, l.num_sms, pl)) return GBCONV_EUNSUPPORTED;
+  TcArgs& a = pl.a;
+  a.ws = static_cast<float*>(ws);
+  a.status = l.status;
+  a.ws_stride = int(p.w_elems() + (db ? p.Cout : 0));
+  TcMaps maps;
+  if (!encode(pl, x, dy, maps)) return GBCONV_ECUDA;
+  auto kern = a.gm == 1 ? wgrad_tc_kernel<1> : wgrad_tc_kernel<2>;
+  static std::atomic<int> raised[2][64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  if (!raised[a.gm - 1][dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
+      return GBCONV_ECUDA;
+    raised[a.gm - 1][dev].store(1, std::memory_order_release);
+  }
+  if (launch_kernel(kern, dim3(pl.grid), dim3(kThreads), pl.smem, l.stream, maps, a) != cudaSuccess)
+    return GBCONV_ECUDA;
+  float* wsf = static_cast<float*>(ws);
+  if (db) {
+    const gbconv_status s = launch_bgrad_partials(p, dy, a.chunks, wsf, l);
+    if (s != GBCONV_OK) return s;
+  }
+  return launch_wgrad_reduce(p, a.chunks, wsf, dw, db, db != nullptr, l);
+}
 
 }  // namespace gbconv

@@ -155,7 +155,8 @@ gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc *desc, int64_t *byte
  *   workspace : device scratch of at least gbconv_bwd_filter_workspace(desc) bytes, 16-byte aligned, owned
  *               by the caller; its contents are undefined afterwards.  NULL is allowed when 0 bytes are needed.
  * The sum over batch and positions is cut into fixed chunks; each chunk's partial sums are taken in a
- * fixed order and the chunks are added in chunk order, so the same inputs give bitwise-equal dw and db.
+ * fixed order and the chunk sums are added in a fixed order (eight runs of consecutive chunks, each in
+ * chunk order, then the runs in order), so the same inputs give bitwise-equal dw and db.
  * Enqueues two kernels on `stream` (partial sums, ordered reduction), three when the tensor-core path also
  * computes db.  Returns GBCONV_EINVAL for NULL tensors or a workspace smaller than required. */
 gbconv_status gbconv_bwd_filter(const gbconv_desc *desc, const void *x, const void *dy, void *dw, float *db,

@@ -374,10 +374,22 @@ WGRAD = [
     (shape_kw(n=3, in_size=(10, 12), c_in=16, c_out=8, wlayout="oihw", dtype="f32", stride=(2, 2)), "direct_wgrad"),
     (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "direct_wgrad"),
     (shape_kw(n=1, in_size=(9, 8), c_in=16, c_out=8, layout="nchw", wlayout="oihw", stride=(2, 2)), "direct_wgrad"),
-    # NHWC bf16, dense: 3x3 (several chunks), 1x1 at stride 2, 5x5 with dilation
-    (shape_kw(n=4, in_size=(20, 21), c_in=64, c_out=64, k=(3, 3), pad=(1, 1)), "direct_wgrad"),
+    # NHWC bf16 that the tensor-core path declines: 1x1 at stride 2, a 5-wide kernel
     (shape_kw(n=2, in_size=(15, 14), c_in=32, c_out=48, k=(1, 1), pad=(0, 0), stride=(2, 2)), "direct_wgrad"),
     (shape_kw(n=1, in_size=(13, 12), c_in=16, c_out=24, k=(5, 5), pad=(2, 2), dil=(1, 2)), "direct_wgrad"),
+    # tensor-core path: 3x3 over several chunks; channel tails and four block pairs; 2x2 without
+    # padding; 1x1 (one kernel row: the second M atom unused); 3x1; dilation 2; conv1d NLC; 16 channels
+    (shape_kw(n=4, in_size=(20, 21), c_in=64, c_out=64, k=(3, 3), pad=(1, 1)), "wgrad"),
+    (shape_kw(n=2, in_size=(16, 17), c_in=128, c_out=96, k=(3, 3), pad=(1, 1)), "wgrad"),
+    (shape_kw(n=3, in_size=(11, 10), c_in=64, c_out=128, k=(2, 2), pad=(0, 0)), "wgrad"),
+    (shape_kw(n=2, in_size=(9, 13), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "wgrad"),
+    (shape_kw(n=2, in_size=(12, 9), c_in=64, c_out=64, k=(3, 1), pad=(1, 0)), "wgrad"),
+    (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, k=(3, 3), pad=(2, 2), dil=(2, 2)), "wgrad"),
+    (shape_kw(spatial_dims=1, n=3, in_size=(37,), c_in=32, c_out=64, k=(3,), stride=(1,), pad=(2,), dil=(2,),
+              layout="nlc", wlayout="oki"), "wgrad"),
+    (shape_kw(n=2, in_size=(7, 8), c_in=16, c_out=8, k=(3, 3), pad=(1, 1)), "wgrad"),
+    # more block pairs than SMs: CTAs take several units in turn (the accumulators are handed over)
+    (shape_kw(n=1, in_size=(6, 6), c_in=1024, c_out=1024, k=(3, 3), pad=(1, 1)), "wgrad"),
 ]
 
 
@@ -418,7 +430,7 @@ def test_wgrad_integer_inputs_bit_exact(gb, case):
 
 
 def test_wgrad_is_deterministic_and_db_optional(gb):
-    kw, _ = WGRAD[5]
+    kw, _ = WGRAD[7]
     c = oracle_conv(kw)
     inp = draw_wgrad(c, "bf16", 900)
     dw1, db1 = run_wgrad(gb, kw, inp)
@@ -427,3 +439,21 @@ def test_wgrad_is_deterministic_and_db_optional(gb):
     assert np.array_equal(dw1, dw2) and np.array_equal(db1, db2)
     assert np.array_equal(dw1, dw3)
     assert np.all(db3 == 7.0)  # not asked for: untouched
+
+
+def test_wgrad_tc_chunks_longer_than_one_load(gb):
+    # 8 images of 120x120: 64-row-wide boxes hold one block of 4 rows per load, and the row blocks
+    # outnumber the chunks, so CTAs sweep several segments; checked on sampled dW elements
+    kw = shape_kw(n=8, in_size=(120, 120), c_in=64, c_out=64, k=(3, 3), pad=(1, 1))
+    d = lib_desc(gb, kw)
+    assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_FILTER) == "wgrad"
+    plan = dict(f.split("=") for f in gb.gbconv_describe(d, gb.GBCONV_OP_BWD_FILTER).split()[1:])
+    assert int(plan["seg_blocks"]) == 1 and int(plan["chunks"]) < 8 * 30
+    c = oracle_conv(kw)
+    inp = draw_wgrad(c, "bf16", 950)
+    dw, db = run_wgrad(gb, kw, inp)
+    idx = _sample_indices((64, 64, 3, 3), 951, count=120)
+    ref = oracle.conv_wgrad_points(c, inp["x"], inp["g"], idx)
+    scale = oracle.conv_wgrad_points(c, np.abs(inp["x"]), np.abs(inp["g"]), idx)
+    check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
+    check_f32(db, oracle.conv_bgrad(c, inp["g"]), oracle.conv_bgrad(c, np.abs(inp["g"])))
