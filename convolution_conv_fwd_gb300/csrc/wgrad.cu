@@ -86,42 +86,15 @@ __global__ void direct_wgrad_partial_kernel(WgArgs a, const T* __restrict__ x, c
   ws[int64_t(s) * a.Etot + e] = acc;
 }
 
-// Adds the S chunk partials of every element in a fixed order, rounds once, and writes dw in the
-// caller's weight layout and db.  A block takes 32 consecutive elements; warp j sums chunks
-// [j*S/8, (j+1)*S/8) of its lane's element in chunk order, then the eight slice sums are added in
-// slice order.  Every sum is compensated (Kahan): the order fixes the bits, and the compensation
-// keeps the fp32 sum of up to a few hundred partials close to the exact one.
+__device__ __forceinline__ void kahan_add(float& acc, float& comp, float v) {
+  const float y = v - comp;
+  const float t = acc + y;
+  comp = (t - acc) - y;
+  acc = t;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
-                                                           const float* __restrict__ ws, T* __restrict__ dw,
-                                                           float* __restrict__ db) {
-  ptx::grid_dep_wait();
-  __shared__ float part[8][32];
-  const int lane = int(threadIdx.x) & 31, j = int(threadIdx.x) >> 5;
-  const int e = int(blockIdx.x) * 32 + lane;
-  float acc = 0.f, comp = 0.f;
-  if (e < Etot) {
-    const int s0 = (j * S) / 8, s1 = ((j + 1) * S) / 8;
-#pragma unroll 4
-    for (int s = s0; s < s1; ++s) {
-      const float y = ws[int64_t(s) * Etot + e] - comp;
-      const float t = acc + y;
-      comp = (t - acc) - y;
-      acc = t;
-    }
-  }
-  part[j][lane] = acc - comp;
-  __syncthreads();
-  if (j != 0 || e >= Etot) return;
-  acc = 0.f;
-  comp = 0.f;
-#pragma unroll
-  for (int jj = 0; jj < 8; ++jj) {
-    const float y = part[jj][lane] - comp;
-    const float t = acc + y;
-    comp = (t - acc) - y;
-    acc = t;
-  }
+__device__ __forceinline__ void store_grad(int e, float v, int E, int KH, int KW, int cpg, int ohwi, T* dw, float* db) {
   if (e < E) {
     int t = e;
     const int cl = t % cpg;
@@ -130,9 +103,57 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int 
     t /= KW;
     const int kh = t % KH, co = t / KH;
     const int64_t o = ohwi ? int64_t(e) : ((int64_t(co) * cpg + cl) * KH + kh) * KW + kw;
-    st_elem(dw, o, acc);
+    st_elem(dw, o, v);
   } else {
-    db[e - E] = acc;
+    db[e - E] = v;
+  }
+}
+
+// Adds the S chunk partials of every element in a fixed order, rounds once, and writes dw in the
+// caller's weight layout and db.  A block takes 32*V consecutive elements (V per lane, read as one
+// vector when V = 4); warp j sums chunks [j*S/8, (j+1)*S/8) in chunk order, then the eight slice
+// sums are added in slice order.  Every sum is compensated (Kahan): the order fixes the bits, and
+// the compensation keeps the fp32 sum of up to a few hundred partials close to the exact one.
+template <typename T, int V>
+__global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
+                                                           const float* __restrict__ ws, T* __restrict__ dw,
+                                                           float* __restrict__ db) {
+  ptx::grid_dep_wait();
+  __shared__ float part[8][32 * V];
+  const int lane = int(threadIdx.x) & 31, j = int(threadIdx.x) >> 5;
+  const int e0 = (int(blockIdx.x) * 32 + lane) * V;
+  float acc[V], comp[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = comp[v] = 0.f;
+  const int s0 = (j * S) / 8, s1 = ((j + 1) * S) / 8;
+  if (V == 4 && e0 + 3 < Etot) {
+#pragma unroll 4
+    for (int s = s0; s < s1; ++s) {
+      const float4 x = *reinterpret_cast<const float4*>(ws + int64_t(s) * Etot + e0);
+      kahan_add(acc[0], comp[0], x.x);
+      kahan_add(acc[1], comp[1], x.y);
+      kahan_add(acc[2], comp[2], x.z);
+      kahan_add(acc[3], comp[3], x.w);
+    }
+  } else {
+    for (int s = s0; s < s1; ++s)
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (e0 + v < Etot) kahan_add(acc[v], comp[v], ws[int64_t(s) * Etot + e0 + v]);
+  }
+#pragma unroll
+  for (int v = 0; v < V; ++v) part[j][lane * V + v] = acc[v] - comp[v];
+  __syncthreads();
+  // the first warp finishes the block's 32*V elements, V per lane
+  if (j != 0) return;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = e0 + v;
+    if (e >= Etot) continue;
+    float a2 = 0.f, c2 = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) kahan_add(a2, c2, part[jj][lane * V + v]);
+    store_grad(e, a2, E, KH, KW, cpg, ohwi, dw, db);
   }
 }
 
@@ -166,14 +187,20 @@ int64_t direct_wgrad_workspace(const Problem& p) {
 gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void* dw, float* db, bool want_db,
                                   const Launch& l) {
   const int E = int(p.w_elems()), Etot = E + (want_db ? int(p.Cout) : 0);
-  const dim3 grid((Etot + 31) / 32), block(256);
+  // float4 reads need every chunk row to start on 16 bytes (the workspace itself is 16-byte aligned)
+  const bool vec = Etot % 4 == 0;
+  const dim3 grid(vec ? (Etot + 127) / 128 : (Etot + 31) / 32), block(256);
   cudaError_t e;
   if (p.bf16)
-    e = launch_kernel(wgrad_reduce_kernel<bf16>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
-                      int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db);
+    e = vec ? launch_kernel(wgrad_reduce_kernel<bf16, 4>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                            int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db)
+            : launch_kernel(wgrad_reduce_kernel<bf16, 1>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                            int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db);
   else
-    e = launch_kernel(wgrad_reduce_kernel<float>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
-                      int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db);
+    e = vec ? launch_kernel(wgrad_reduce_kernel<float, 4>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                            int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db)
+            : launch_kernel(wgrad_reduce_kernel<float, 1>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+                            int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db);
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 

@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&maps.dy);
     }
     bool ok = true;
-    int seg = 0;  // segments this CTA has loaded: the phase of every box barrier
+    int seg = 0;            // segments this CTA has loaded
+    uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
     for (int u = int(blockIdx.x); ok && u < a.units; u += int(gridDim.x)) {
       const int chunk = u / a.pairs, pair = u - chunk * a.pairs;
       const int cib = pair % a.cb_in, cob = pair / a.cb_in;
@@ -190,38 +191,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : "memory");
         ptx::fence_proxy_async_smem();
         __syncwarp();
+        const int nxb = sg.nb + a.xe;
         if (lane == 0) {
-          const int nxb = sg.nb + a.xe;
           const int row0 = sg.rb * a.RB;  // first virtual row of the segment
-          for (int b = 0; b < kMaxBoxes; ++b) {
-            // Boxes the segment does not need still complete a phase, so every barrier's phase
-            // stays the segment count.
-            if (b < nxb) {
-              ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
-              tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
-                          row0 + b * a.RB - a.PH, sg.n);
-            } else {
-              ptx::mbar_arrive(xbar + b);
-            }
+          for (int b = 0; b < nxb; ++b) {
+            ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
+            tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
+                        row0 + b * a.RB - a.PH, sg.n);
             if (b < sg.nb) {
               ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(a.box_bytes));
               tma_load_4d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
                           cob * 64, 0, row0 + b * a.RB, sg.n);
-            } else {
-              ptx::mbar_arrive(ybar + b);
             }
           }
         }
         __syncwarp();
+        // A segment uses boxes [0, nxb) and [0, nb): each of those barriers completes one phase.
+        xph ^= (1u << nxb) - 1u;
+        yph ^= (1u << sg.nb) - 1u;
         ++seg;
       }
     }
-    // Leave no copy in flight: wait (bounded, whatever the abort state) for the last segment's boxes.
+    // Leave no copy in flight: wait (bounded, whatever the abort state) until every box barrier has
+    // completed the phases armed so far (the parity bits hold the next phase of each).
     if (lane == 0 && seg > 0) {
       const uint64_t t0 = ptx::globaltimer();
       for (int b = 0; b < 2 * kMaxBoxes; ++b) {
         uint64_t* bar = b < kMaxBoxes ? xbar + b : ybar + (b - kMaxBoxes);
-        while (!ptx::mbar_try_wait(bar, uint32_t(seg - 1) & 1u) && ptx::globaltimer() - t0 < 200000000ull) {
+        const uint32_t next = b < kMaxBoxes ? (xph >> b) & 1u : (yph >> (b - kMaxBoxes)) & 1u;
+        while (!ptx::mbar_try_wait(bar, next ^ 1u) && ptx::globaltimer() - t0 < 200000000ull) {
         }
       }
     }
@@ -246,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_lo0 = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
       const uint32_t b_lo0 = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
       const uint32_t g_step = uint32_t(2 * a.DH * P) * 8u;  // (2*DH*P*128) >> 4
+      uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
       for (int u = int(blockIdx.x); ok && u < units; u += int(gridDim.x), ++it) {
         if (it > 0) {  // the epilogue has taken the previous unit's accumulators
           if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u))) break;
@@ -257,16 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && walk.next(sg)) {
           const int nb = sg.nb, nxb = sg.nb + xe;
           const int nk = (nb * box_pos + (KW - 1) * a.DW + 15) / 16;
-          const uint32_t ph = uint32_t(seg) & 1u;
           int xw = 0, yw = 0;  // boxes already waited for
           // Blocks of kStepBlock steps: the boxes the whole block reads are waited for first, then its
           // MMAs go out back to back.
           for (int t0 = 0; ok && t0 < nk; t0 += kStepBlock) {
             const int tn = min(kStepBlock, nk - t0);
             const int kend = 16 * (t0 + tn - 1) + 15;  // last position the block reads (before the shifts)
-            while (ok && yw < nb && kend >= yw * box_pos) ok = ptx::mbar_wait(ybar + yw++, ph, abort_flag, a.status, 2u);
-            while (ok && xw < nxb && kend + xreach >= xw * box_pos)
-              ok = ptx::mbar_wait(xbar + xw++, ph, abort_flag, a.status, 2u);
+            for (; ok && yw < nb && kend >= yw * box_pos; ++yw)
+              ok = ptx::mbar_wait(ybar + yw, (yph >> yw) & 1u, abort_flag, a.status, 2u);
+            for (; ok && xw < nxb && kend + xreach >= xw * box_pos; ++xw)
+              ok = ptx::mbar_wait(xbar + xw, (xph >> xw) & 1u, abort_flag, a.status, 2u);
             if (!ok) break;
             const uint32_t a_lo = a_lo0 + uint32_t(t0) * 128u, b_lo = b_lo0 + uint32_t(t0) * 128u;
             const uint32_t acc0 = (first && t0 == 0) ? 0u : 1u;
@@ -286,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ptx::mma_commit(seg_done);
+          xph ^= (1u << nxb) - 1u;
+          yph ^= (1u << nb) - 1u;
           first = false;
           ++seg;
         }
