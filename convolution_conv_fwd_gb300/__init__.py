@@ -23,6 +23,7 @@ GBCONV_OK, GBCONV_EINVAL, GBCONV_EUNSUPPORTED, GBCONV_ECUDA, GBCONV_ETIMEOUT = r
 GBCONV_NCHW, GBCONV_NHWC = 0, 1
 GBCONV_W_OIHW, GBCONV_W_OHWI = 0, 1
 GBCONV_F32, GBCONV_BF16 = 0, 1
+GBCONV_PAD_SYMMETRIC, GBCONV_PAD_BEGIN_END = 0, 1
 # kernel families
 KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad",
            6: "depthwise_dgrad", 7: "direct_wgrad", 8: "wgrad"}
@@ -39,7 +40,7 @@ class Desc(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("n", ctypes.c_int64), ("c_in", ctypes.c_int64),
                 ("c_out", ctypes.c_int64), ("groups", ctypes.c_int64), ("in_", ctypes.c_int64 * 2),
                 ("k", ctypes.c_int64 * 2), ("stride", ctypes.c_int64 * 2), ("pad", ctypes.c_int64 * 2),
-                ("dil", ctypes.c_int64 * 2)]
+                ("dil", ctypes.c_int64 * 2), ("pad_end", ctypes.c_int64 * 2), ("pad_mode", ctypes.c_int32)]
 
 
 class GbconvError(RuntimeError):
@@ -150,8 +151,9 @@ def status_string(status: int) -> str:
 # ---------------------------------------------------------------- descriptors
 
 def make_desc(n, c_in, c_out, in_size, k, stride=1, pad=0, dil=1, groups=1, *, spatial_dims=2,
-              layout="nhwc", wlayout="ohwi", dtype="bf16") -> Desc:
-    """Build a gbconv_desc.  Sizes are ints (1-D) or pairs (2-D)."""
+              layout="nhwc", wlayout="ohwi", dtype="bf16", pad_end=None) -> Desc:
+    """Build a gbconv_desc.  Sizes are ints (1-D) or pairs (2-D).  ``pad`` is the padding before each
+    axis, and after it too unless ``pad_end`` gives the padding after (begin, end padding)."""
     def pair(v):
         if isinstance(v, (tuple, list)):
             return (int(v[0]), int(v[1]) if len(v) > 1 else 1)
@@ -166,6 +168,9 @@ def make_desc(n, c_in, c_out, in_size, k, stride=1, pad=0, dil=1, groups=1, *, s
         a, b = pair(v)
         getattr(d, name)[0] = a
         getattr(d, name)[1] = b
+    if pad_end is not None:
+        d.pad_mode = GBCONV_PAD_BEGIN_END
+        d.pad_end[0], d.pad_end[1] = pair(pad_end)
     return d
 
 

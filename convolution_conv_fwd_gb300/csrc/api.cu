@@ -56,31 +56,38 @@ gbconv_status resolve(const gbconv_desc* d, Problem* p) {
   if (d->layout != GBCONV_NCHW && d->layout != GBCONV_NHWC) return GBCONV_EINVAL;
   if (d->wlayout != GBCONV_W_OIHW && d->wlayout != GBCONV_W_OHWI) return GBCONV_EINVAL;
   if (d->dtype != GBCONV_F32 && d->dtype != GBCONV_BF16) return GBCONV_EINVAL;
+  if (d->pad_mode != GBCONV_PAD_SYMMETRIC && d->pad_mode != GBCONV_PAD_BEGIN_END) return GBCONV_EINVAL;
+  const bool be = d->pad_mode == GBCONV_PAD_BEGIN_END;
   Problem q{};
   q.N = d->n;
   q.Cin = d->c_in;
   q.Cout = d->c_out;
   q.G = d->groups;
   if (d->spatial_dims == 1) {  // the length axis is carried as the width
-    q.H = 1; q.KH = 1; q.SH = 1; q.PH = 0; q.DH = 1;
+    q.H = 1; q.KH = 1; q.SH = 1; q.PH = 0; q.PHe = 0; q.DH = 1;
     q.W = d->in[0]; q.KW = d->k[0]; q.SW = d->stride[0]; q.PW = d->pad[0]; q.DW = d->dil[0];
+    q.PWe = be ? d->pad_end[0] : q.PW;
   } else {
     q.H = d->in[0]; q.KH = d->k[0]; q.SH = d->stride[0]; q.PH = d->pad[0]; q.DH = d->dil[0];
     q.W = d->in[1]; q.KW = d->k[1]; q.SW = d->stride[1]; q.PW = d->pad[1]; q.DW = d->dil[1];
+    q.PHe = be ? d->pad_end[0] : q.PH;
+    q.PWe = be ? d->pad_end[1] : q.PW;
   }
   if (q.N <= 0 || q.Cin <= 0 || q.Cout <= 0 || q.G <= 0) return GBCONV_EINVAL;
   if (q.H <= 0 || q.W <= 0 || q.KH <= 0 || q.KW <= 0) return GBCONV_EINVAL;
-  if (q.SH <= 0 || q.SW <= 0 || q.DH <= 0 || q.DW <= 0 || q.PH < 0 || q.PW < 0) return GBCONV_EINVAL;
+  if (q.SH <= 0 || q.SW <= 0 || q.DH <= 0 || q.DW <= 0 || q.PH < 0 || q.PW < 0 || q.PHe < 0 || q.PWe < 0)
+    return GBCONV_EINVAL;
   if (q.Cin % q.G != 0 || q.Cout % q.G != 0) return GBCONV_EINVAL;
   // Keep every intermediate well inside int64 before multiplying.
   const int64_t lim = int64_t(1) << 31;
   if (q.N >= lim || q.Cin >= lim || q.Cout >= lim || q.H >= lim || q.W >= lim || q.KH >= lim || q.KW >= lim ||
-      q.SH >= lim || q.SW >= lim || q.PH >= lim || q.PW >= lim || q.DH >= lim || q.DW >= lim)
+      q.SH >= lim || q.SW >= lim || q.PH >= lim || q.PW >= lim || q.PHe >= lim || q.PWe >= lim || q.DH >= lim ||
+      q.DW >= lim)
     return GBCONV_EUNSUPPORTED;
   const int64_t effh = (q.KH - 1) * q.DH + 1, effw = (q.KW - 1) * q.DW + 1;
-  if (q.H + 2 * q.PH < effh || q.W + 2 * q.PW < effw) return GBCONV_EINVAL;
-  q.OH = (q.H + 2 * q.PH - effh) / q.SH + 1;
-  q.OW = (q.W + 2 * q.PW - effw) / q.SW + 1;
+  if (q.H + q.PH + q.PHe < effh || q.W + q.PW + q.PWe < effw) return GBCONV_EINVAL;
+  q.OH = (q.H + q.PH + q.PHe - effh) / q.SH + 1;
+  q.OW = (q.W + q.PW + q.PWe - effw) / q.SW + 1;
   q.nhwc = d->layout == GBCONV_NHWC;
   q.ohwi = d->wlayout == GBCONV_W_OHWI;
   q.bf16 = d->dtype == GBCONV_BF16;

@@ -504,7 +504,8 @@ PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
 }
 
 bool dw_tma_supported(const Problem& p) {
-  return p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2) &&
+  // tiles are laid out for symmetric padding; (begin, end) padding takes the generic kernel
+  return p.sym_pad() && p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2) &&
          p.Cin % 64 == 0;
 }
 
@@ -584,7 +585,8 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
   auto wb = static_cast<const __nv_bfloat16*>(w);
   auto yb = static_cast<__nv_bfloat16*>(y);
   if (dw_tma_supported(p)) return p.SH == 1 ? launch_dw_tma<1>(p, x, w, bias, y, l) : launch_dw_tma<2>(p, x, w, bias, y, l);
-  const bool reg3x3 = p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2);
+  const bool reg3x3 =
+      p.sym_pad() && p.KH == 3 && p.KW == 3 && p.DH == 1 && p.DW == 1 && p.SH == p.SW && (p.SH == 1 || p.SH == 2);
   if (reg3x3) {
     a.rows_per_thread = 8;
     grid.y = unsigned((p.OH + a.rows_per_thread - 1) / a.rows_per_thread);
@@ -624,7 +626,8 @@ gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const voi
   auto dyb = static_cast<const __nv_bfloat16*>(dy);
   auto wb = static_cast<const __nv_bfloat16*>(w);
   auto dxb = static_cast<__nv_bfloat16*>(dx);
-  if (p.KH == 3 && p.KW == 3 && p.SH == 2 && p.SW == 2 && p.PH == 1 && p.PW == 1 && p.DH == 1 && p.DW == 1 &&
+  if (p.KH == 3 && p.KW == 3 && p.SH == 2 && p.SW == 2 && p.PH == 1 && p.PW == 1 && p.PHe == 1 && p.PWe == 1 &&
+      p.DH == 1 && p.DW == 1 &&
       p.OH == (p.H + 1) / 2 && p.OW == (p.W + 1) / 2) {
     // One thread per dy column and 8 channels, walking a strip of dy rows: strips as long as
     // possible (each strip start re-reads a dy row) while the grid still fills two blocks per SM.

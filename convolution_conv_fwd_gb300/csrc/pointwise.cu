@@ -267,7 +267,8 @@ gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a,
 }  // namespace
 
 bool pointwise_supported(const Problem& p) {
-  if (!(p.bf16 && p.nhwc && p.G == 1 && p.KH == 1 && p.KW == 1 && p.SH == 1 && p.SW == 1 && p.PH == 0 && p.PW == 0))
+  if (!(p.bf16 && p.nhwc && p.G == 1 && p.KH == 1 && p.KW == 1 && p.SH == 1 && p.SW == 1 && p.PH == 0 && p.PW == 0 &&
+        p.PHe == 0 && p.PWe == 0))
     return false;
   if (p.Cin % 8 != 0) return false;  // TMA row pitch must be a multiple of 16 bytes
   const int bn = pick_bn(p.Cout);

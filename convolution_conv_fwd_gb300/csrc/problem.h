@@ -14,6 +14,7 @@ namespace gbconv {
 struct Problem {
   int64_t N, Cin, Cout, G;
   int64_t H, W, KH, KW, SH, SW, PH, PW, DH, DW;
+  int64_t PHe, PWe;  // end-side padding (PH, PW are the begin side); equal to PH, PW when symmetric
   int64_t OH, OW;
   bool nhwc;   // activations channels-last
   bool ohwi;   // weight [C_out, KH, KW, C_in/G]
@@ -24,6 +25,7 @@ struct Problem {
   int64_t y_elems() const { return N * Cout * OH * OW; }
   int64_t w_elems() const { return Cout * cpg() * KH * KW; }
   int elem_bytes() const { return bf16 ? 2 : 4; }
+  bool sym_pad() const { return PHe == PH && PWe == PW; }
 };
 
 // Fills `p` from `d` and checks it the way oarust's geometry resolvers do:

@@ -28,8 +28,10 @@
  *             element, there accumulated with atomics), oarust `conv_2d_backward` (returns the bias gradient
  *             beside the weight gradient).  The library adds its partial sums in a fixed order, with no atomics.
  *
- *   out size  out = (in + 2*pad - dil*(k - 1) - 1) / stride + 1 (floor), rejected when in + 2*pad < dil*(k-1) + 1.
- *             Source: oarust `Conv1dGeometry::resolve`.
+ *   out size  out = (in + pad + pad_end - dil*(k - 1) - 1) / stride + 1 (floor), rejected when
+ *             in + pad + pad_end < dil*(k-1) + 1 (pad_end = pad unless the descriptor asks for (begin, end)
+ *             padding).  Source: oarust `Conv1dGeometry::resolve` (symmetric padding); burn-cubecl's
+ *             (begin, end) padding pairs.
  *
  * Conventions shared by every entry point:
  *  - All tensors are dense and contiguous in the layouts named by the descriptor.  Activation layouts:
@@ -82,9 +84,14 @@ typedef enum {
 
 typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER = 2 } gbconv_op;
 
-/* One convolution.  For spatial_dims == 1 only index 0 of in/k/stride/pad/dil is read (the length
- * axis); index 1 is ignored.  For spatial_dims == 2 index 0 is height and index 1 is width.
- * Padding is symmetric: pad[i] zeros on both sides of axis i. */
+typedef enum { GBCONV_PAD_SYMMETRIC = 0, GBCONV_PAD_BEGIN_END = 1 } gbconv_pad_mode;
+
+/* One convolution.  For spatial_dims == 1 only index 0 of in/k/stride/pad/pad_end/dil is read (the
+ * length axis); index 1 is ignored.  For spatial_dims == 2 index 0 is height and index 1 is width.
+ * Padding: with pad_mode GBCONV_PAD_SYMMETRIC (0, what a zero-initialised descriptor holds) axis i has
+ * pad[i] zeros on both sides and pad_end is not read; with GBCONV_PAD_BEGIN_END it has pad[i] zeros
+ * before and pad_end[i] zeros after (burn-cubecl's padding is such a (begin, end) pair per axis).
+ * Output extent per axis: (in + pad + pad_end - dil*(k-1) - 1) / stride + 1, floor. */
 typedef struct {
   int32_t spatial_dims;       /* 1 or 2 */
   int32_t layout;             /* gbconv_layout of x, y, dy, dx */
@@ -92,6 +99,8 @@ typedef struct {
   int32_t dtype;              /* gbconv_dtype of x, w, y, dy, dx */
   int64_t n, c_in, c_out, groups;
   int64_t in[2], k[2], stride[2], pad[2], dil[2];
+  int64_t pad_end[2];         /* end-side padding, read when pad_mode == GBCONV_PAD_BEGIN_END */
+  int32_t pad_mode;           /* gbconv_pad_mode */
 } gbconv_desc;
 
 /* Output spatial extent of the forward convolution (oarust Conv1dGeometry::resolve applied per axis).

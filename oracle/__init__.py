@@ -29,7 +29,7 @@ _lib = None
 class _Desc(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int64) for name in (
         "n", "c_in", "c_out", "groups", "in_h", "in_w", "k_h", "k_w",
-        "s_h", "s_w", "p_h", "p_w", "d_h", "d_w")] + [
+        "s_h", "s_w", "p_h", "p_w", "d_h", "d_w", "p_h_end", "p_w_end")] + [
         ("nhwc", ctypes.c_int32), ("w_ohwi", ctypes.c_int32)]
 
 
@@ -53,15 +53,21 @@ class Conv:
     nhwc: bool = False
     w_ohwi: bool = False
     spatial_dims: int = 2
+    pad_end: tuple = None   # padding after each axis; None: the same as ``pad`` (symmetric)
+
+    def pads_end(self):
+        return tuple(self.pad) if self.pad_end is None else tuple(self.pad_end)
 
     def _c(self) -> _Desc:
+        pe = self.pads_end()
         return _Desc(self.n, self.c_in, self.c_out, self.groups, self.in_hw[0], self.in_hw[1],
                      self.k[0], self.k[1], self.stride[0], self.stride[1], self.pad[0], self.pad[1],
-                     self.dil[0], self.dil[1], int(self.nhwc), int(self.w_ohwi))
+                     self.dil[0], self.dil[1], pe[0], pe[1], int(self.nhwc), int(self.w_ohwi))
 
     def out_hw(self):
-        oh = out_size(self.in_hw[0], self.k[0], self.stride[0], self.pad[0], self.dil[0])
-        ow = out_size(self.in_hw[1], self.k[1], self.stride[1], self.pad[1], self.dil[1])
+        pe = self.pads_end()
+        oh = out_size2(self.in_hw[0], self.k[0], self.stride[0], self.pad[0], pe[0], self.dil[0])
+        ow = out_size2(self.in_hw[1], self.k[1], self.stride[1], self.pad[1], pe[1], self.dil[1])
         return oh, ow
 
     def x_shape(self):
@@ -103,6 +109,8 @@ def _load():
         f32p, f64p, i64p = P(ctypes.c_float), P(ctypes.c_double), P(ctypes.c_int64)
         lib.oracle_out_size.argtypes = [ctypes.c_int64] * 5 + [i64p]
         lib.oracle_out_size.restype = ctypes.c_int
+        lib.oracle_out_size2.argtypes = [ctypes.c_int64] * 6 + [i64p]
+        lib.oracle_out_size2.restype = ctypes.c_int
         lib.oracle_check.argtypes = [P(_Desc), i64p, i64p]
         lib.oracle_check.restype = ctypes.c_int
         for name in ("oracle_conv_fwd",):
@@ -142,6 +150,13 @@ def out_size(in_: int, k: int, s: int, p: int, d: int):
     """Output length along one axis, or None when the shape is rejected."""
     out = ctypes.c_int64(0)
     rc = _load().oracle_out_size(in_, k, s, p, d, ctypes.byref(out))
+    return None if rc != 0 else out.value
+
+
+def out_size2(in_: int, k: int, s: int, p_begin: int, p_end: int, d: int):
+    """Output length along one axis with (begin, end) padding, or None when the shape is rejected."""
+    out = ctypes.c_int64(0)
+    rc = _load().oracle_out_size2(in_, k, s, p_begin, p_end, d, ctypes.byref(out))
     return None if rc != 0 else out.value
 
 

@@ -19,6 +19,8 @@
  *    `Conv1dGeometry::resolve` (effective kernel = (k-1)*dil + 1, reject a
  *    padded input shorter than it, out = (in + 2*pad - eff) / stride + 1 with
  *    integer floor division).  The 2-D rule is the same per spatial axis.
+ *    With burn-cubecl's (begin, end) padding pairs the padded length is
+ *    in + pad_begin + pad_end, and reads use the begin side.
  *  - Index map: burn-cubecl `src/kernel/conv/im2col.rs`, doc of `im2col`
  *    (input position = out*stride + k*dilation - padding, zero outside the
  *    image; no kernel flip: cross-correlation).
@@ -57,6 +59,7 @@ typedef struct {
   int64_t s_h, s_w;
   int64_t p_h, p_w;
   int64_t d_h, d_w;
+  int64_t p_h_end, p_w_end;  /* padding after each axis (p_h, p_w are before it) */
   int32_t nhwc;          /* 0: NCHW / NCL activations, 1: NHWC / NLC activations */
   int32_t w_ohwi;        /* 0: OIHW / OIK weight [C_out, C_in/G, KH, KW], 1: OHWI [C_out, KH, KW, C_in/G] */
 } oracle_conv;
@@ -72,13 +75,23 @@ int oracle_out_size(int64_t in, int64_t k, int64_t s, int64_t p, int64_t d, int6
   return ORACLE_OK;
 }
 
+/* As oracle_out_size, with p_begin zeros before the axis and p_end after it. */
+int oracle_out_size2(int64_t in, int64_t k, int64_t s, int64_t p_begin, int64_t p_end, int64_t d, int64_t *out) {
+  if (in <= 0 || k <= 0 || s <= 0 || d <= 0 || p_begin < 0 || p_end < 0) return ORACLE_EINVAL;
+  int64_t eff = (k - 1) * d + 1;
+  int64_t padded = in + p_begin + p_end;
+  if (padded < eff) return ORACLE_EINVAL;
+  *out = (padded - eff) / s + 1;
+  return ORACLE_OK;
+}
+
 /* Shape checks of oarust Conv1dGeometry / Conv2dGeometry::resolve: nonzero
  * extents, nonzero stride, dilation and groups, channels divisible by groups. */
 int oracle_check(const oracle_conv *c, int64_t *oh, int64_t *ow) {
   if (c->n <= 0 || c->c_in <= 0 || c->c_out <= 0 || c->groups <= 0) return ORACLE_EINVAL;
   if (c->c_in % c->groups != 0 || c->c_out % c->groups != 0) return ORACLE_EINVAL;
-  if (oracle_out_size(c->in_h, c->k_h, c->s_h, c->p_h, c->d_h, oh) != ORACLE_OK) return ORACLE_EINVAL;
-  if (oracle_out_size(c->in_w, c->k_w, c->s_w, c->p_w, c->d_w, ow) != ORACLE_OK) return ORACLE_EINVAL;
+  if (oracle_out_size2(c->in_h, c->k_h, c->s_h, c->p_h, c->p_h_end, c->d_h, oh) != ORACLE_OK) return ORACLE_EINVAL;
+  if (oracle_out_size2(c->in_w, c->k_w, c->s_w, c->p_w, c->p_w_end, c->d_w, ow) != ORACLE_OK) return ORACLE_EINVAL;
   return ORACLE_OK;
 }
 

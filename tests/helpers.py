@@ -27,14 +27,17 @@ def oracle_conv(wl_or_kw) -> oracle.Conv:
     """oracle.Conv from a synth Workload or a dict with the same fields."""
     g = wl_or_kw if isinstance(wl_or_kw, dict) else wl_or_kw.__dict__
     sd = g["spatial_dims"]
+    pe = g.get("pad_end")
     if sd == 1:
         return oracle.Conv(n=g["n"], c_in=g["c_in"], c_out=g["c_out"], in_hw=(1, g["in_size"][0]),
                            k=(1, g["k"][0]), stride=(1, g["stride"][0]), pad=(0, g["pad"][0]),
                            dil=(1, g["dil"][0]), groups=g["groups"], nhwc=g["layout"] in ("nhwc", "nlc"),
-                           w_ohwi=g["wlayout"] in ("ohwi", "oki"), spatial_dims=1)
+                           w_ohwi=g["wlayout"] in ("ohwi", "oki"), spatial_dims=1,
+                           pad_end=None if pe is None else (0, pe[0]))
     return oracle.Conv(n=g["n"], c_in=g["c_in"], c_out=g["c_out"], in_hw=tuple(g["in_size"]), k=tuple(g["k"]),
                        stride=tuple(g["stride"]), pad=tuple(g["pad"]), dil=tuple(g["dil"]), groups=g["groups"],
-                       nhwc=g["layout"] in ("nhwc", "nlc"), w_ohwi=g["wlayout"] in ("ohwi", "oki"), spatial_dims=2)
+                       nhwc=g["layout"] in ("nhwc", "nlc"), w_ohwi=g["wlayout"] in ("ohwi", "oki"), spatial_dims=2,
+                       pad_end=None if pe is None else tuple(pe))
 
 
 def lib_desc(gb, wl_or_kw):
@@ -42,9 +45,10 @@ def lib_desc(gb, wl_or_kw):
     g = wl_or_kw if isinstance(wl_or_kw, dict) else wl_or_kw.__dict__
     sd = g["spatial_dims"]
     one = (lambda t: t[0]) if sd == 1 else (lambda t: tuple(t))
+    pe = g.get("pad_end")
     return gb.make_desc(g["n"], g["c_in"], g["c_out"], one(g["in_size"]), one(g["k"]), one(g["stride"]),
                         one(g["pad"]), one(g["dil"]), g["groups"], spatial_dims=sd, layout=g["layout"],
-                        wlayout=g["wlayout"], dtype=g["dtype"])
+                        wlayout=g["wlayout"], dtype=g["dtype"], pad_end=None if pe is None else one(pe))
 
 
 def shape_kw(**kw):

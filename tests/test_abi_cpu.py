@@ -207,3 +207,35 @@ def test_bwd_filter_workspace_and_argument_checks(gb):
     assert gb._lib.gbconv_bwd_filter_workspace(ctypes.byref(d), None) == gb.GBCONV_EINVAL
     k = ctypes.c_int32(-1)
     assert gb._lib.gbconv_select(ctypes.byref(d), 3, ctypes.byref(k)) == gb.GBCONV_EINVAL
+
+
+def test_begin_end_padding_shapes_and_families(gb):
+    # out = (in + begin + end - eff) // stride + 1 per axis, as the oracle computes it
+    cases = [shape_kw(in_size=(7, 8), k=(3, 3), stride=(2, 2), pad=(0, 1), pad_end=(1, 0)),
+             shape_kw(in_size=(6, 9), k=(2, 3), pad=(1, 0), pad_end=(0, 2)),
+             shape_kw(spatial_dims=1, in_size=(13,), k=(4,), stride=(3,), pad=(2,), pad_end=(0,), dil=(2,),
+                      layout="nlc", wlayout="oki")]
+    for kw in cases:
+        c = oracle_conv(kw)
+        oh, ow = c.out_hw()
+        want = (ow, 1) if kw["spatial_dims"] == 1 else (oh, ow)
+        assert gb.gbconv_out_shape(lib_desc(gb, kw)) == want
+    # a zero-initialised descriptor pads symmetrically: pad_end is read only in (begin, end) mode
+    d = lib_desc(gb, shape_kw(in_size=(8, 8), pad=(1, 1)))
+    d.pad_end[0], d.pad_end[1] = 5, 5
+    assert gb.gbconv_out_shape(d) == (8, 8)
+    d.pad_mode = gb.GBCONV_PAD_BEGIN_END
+    assert gb.gbconv_out_shape(d) == (12, 12)
+    for bad_mode in (2, -1):
+        d.pad_mode = bad_mode
+        with pytest.raises(gb.GbconvError):
+            gb.gbconv_out_shape(d)
+    with pytest.raises(gb.GbconvError):
+        gb.gbconv_out_shape(lib_desc(gb, shape_kw(pad=(1, 1), pad_end=(-1, 0))))
+    with pytest.raises(gb.GbconvError):  # padded input shorter than the kernel
+        gb.gbconv_out_shape(lib_desc(gb, shape_kw(in_size=(2, 8), k=(5, 3), pad=(1, 1), pad_end=(1, 1))))
+    # families: the 1x1 GEMM and the tiled depthwise kernels take symmetric padding only
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(1, 1), pad=(0, 0), pad_end=(1, 1), c_out=64)), 0) == "implicit"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=64, c_out=64, groups=64, stride=(2, 2), pad=(0, 0),
+                                                 pad_end=(1, 1))), 0) == "depthwise"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), pad=(0, 0), pad_end=(1, 1))), 1) == "dgrad"

@@ -154,6 +154,22 @@ SMALL = [
     (shape_kw(n=2, in_size=(6, 7), c_in=8, c_out=8, groups=8, k=(1, 1), pad=(0, 0), stride=(2, 2)),
      "dgrad", "depthwise_dgrad"),
     (shape_kw(n=1, in_size=(8, 9), c_in=512, c_out=512, groups=512, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
+    # (begin, end) padding: implicit forward one-sided, strided with padding after only (the usual
+    # 'same' padding of an even input at stride 2), a 1x1 with padding after, the depthwise
+    # generic kernel, the stride-phase dgrad, the depthwise dgrad, and the generic direct kernels
+    (shape_kw(n=2, in_size=(9, 11), c_in=64, c_out=64, pad=(1, 0), pad_end=(0, 1), bias=True), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(16, 14), c_in=64, c_out=128, stride=(2, 2), pad=(0, 0), pad_end=(1, 1)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(7, 9), c_in=64, c_out=64, k=(1, 1), pad=(0, 0), pad_end=(1, 2), bias=True),
+     "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2), pad=(0, 0), pad_end=(1, 1),
+              bias=True), "fwd", "depthwise"),
+    (shape_kw(n=2, in_size=(16, 13), c_in=128, c_out=64, stride=(2, 2), pad=(0, 1), pad_end=(1, 0)), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(14, 12), c_in=32, c_out=32, groups=32, stride=(2, 2), pad=(0, 0), pad_end=(1, 1)),
+     "dgrad", "depthwise_dgrad"),
+    (shape_kw(n=2, in_size=(9, 8), c_in=6, c_out=4, groups=2, k=(3, 2), stride=(2, 1), pad=(2, 0), pad_end=(0, 1),
+              layout="nchw", wlayout="oihw", dtype="f32", bias=True), "fwd", "direct"),
+    (shape_kw(n=1, in_size=(10, 7), c_in=8, c_out=12, stride=(2, 2), pad=(1, 0), pad_end=(0, 2), layout="nchw",
+              wlayout="oihw", dtype="f32"), "dgrad", "direct_dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -388,6 +404,10 @@ WGRAD = [
     (shape_kw(spatial_dims=1, n=3, in_size=(37,), c_in=32, c_out=64, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="nlc", wlayout="oki"), "wgrad"),
     (shape_kw(n=2, in_size=(7, 8), c_in=16, c_out=8, k=(3, 3), pad=(1, 1)), "wgrad"),
+    # (begin, end) padding on both weight-gradient paths
+    (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "wgrad"),
+    (shape_kw(n=2, in_size=(9, 10), c_in=6, c_out=9, groups=3, stride=(2, 1), pad=(1, 0), pad_end=(0, 1),
+              layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
     # more block pairs than SMs: CTAs take several units in turn (the accumulators are handed over)
     (shape_kw(n=1, in_size=(6, 6), c_in=1024, c_out=1024, k=(3, 3), pad=(1, 1)), "wgrad"),
 ]

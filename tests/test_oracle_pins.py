@@ -369,3 +369,52 @@ def test_wgrad_of_one_hot_output_gradient_is_the_input_patch():
                 want = x[n0, g * cpg + cl, ih, iw] if (0 <= ih < 6 and 0 <= iw < 7) else 0.0
                 assert dw[co0, cl, kh, kw] == want
     assert np.all(np.delete(dw, co0, axis=0) == 0.0)
+
+
+# ------------------------------------------------------- (begin, end) padding
+
+ASYM = [
+    Conv(n=2, c_in=4, c_out=6, in_hw=(7, 8), k=(3, 3), stride=(2, 2), pad=(0, 1), pad_end=(1, 0), groups=2),
+    Conv(n=1, c_in=3, c_out=5, in_hw=(1, 13), k=(1, 4), stride=(1, 3), pad=(0, 2), pad_end=(0, 0), dil=(1, 2),
+         spatial_dims=1, nhwc=True, w_ohwi=True),
+    Conv(n=2, c_in=5, c_out=4, in_hw=(6, 9), k=(2, 3), stride=(1, 1), pad=(1, 0), pad_end=(0, 2), nhwc=True),
+    Conv(n=1, c_in=2, c_out=3, in_hw=(5, 5), k=(1, 1), stride=(1, 1), pad=(0, 0), pad_end=(1, 2), w_ohwi=True),
+]
+
+
+@pytest.mark.parametrize("in_,k,s,pb,pe,d,expect", [
+    (7, 3, 2, 0, 1, 1, 3), (8, 3, 2, 0, 1, 1, 4), (8, 3, 2, 1, 0, 1, 4), (8, 3, 2, 0, 0, 1, 3),
+    (5, 1, 1, 0, 2, 1, 7), (13, 4, 3, 2, 0, 2, 3), (4, 5, 1, 0, 0, 1, None), (4, 5, 1, 0, 1, 1, 1),
+    (4, 5, 1, 1, 1, 1, 2), (5, 3, 1, 0, -1, 1, None),
+])
+def test_out_size_begin_end(in_, k, s, pb, pe, d, expect):
+    # (in + begin + end - (k-1)*d - 1) // s + 1, and rejected when the padded input is shorter
+    # than the effective kernel
+    assert oracle.out_size2(in_, k, s, pb, pe, d) == expect
+
+
+@pytest.mark.parametrize("ci", range(len(ASYM)))
+def test_begin_end_padding_matches_torch_float64(ci):
+    # torch on an explicitly zero-padded input (F.pad), convolution without padding; the input,
+    # weight and bias gradients by autograd through the same graph
+    c = ASYM[ci]
+    F = torch.nn.functional
+    x = synth.normal(141 + ci, c.x_shape()).astype(np.float32)
+    w = synth.normal(142 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(143 + ci, (c.c_out,)).astype(np.float32)
+    dy = synth.normal(144 + ci, c.y_shape()).astype(np.float32)
+    xt = torch.from_numpy(_to_nchw(x, c).astype(np.float64).copy()).requires_grad_(True)
+    wt = torch.from_numpy(_w_to_oihw(w, c).astype(np.float64).copy()).requires_grad_(True)
+    bt = torch.from_numpy(b.astype(np.float64)).requires_grad_(True)
+    pe = c.pads_end()
+    if c.spatial_dims == 1:
+        yt = F.conv1d(F.pad(xt, (c.pad[1], pe[1])), wt, bt, stride=c.stride[1], dilation=c.dil[1], groups=c.groups)
+    else:
+        yt = F.conv2d(F.pad(xt, (c.pad[1], pe[1], c.pad[0], pe[0])), wt, bt, stride=c.stride, dilation=c.dil,
+                      groups=c.groups)
+    np.testing.assert_allclose(_to_nchw(oracle.conv_fwd(c, x, w, b), c), yt.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dyt = torch.from_numpy(_to_nchw(dy, c).astype(np.float64).copy())
+    gx, gw, gb_ = torch.autograd.grad(yt, (xt, wt, bt), dyt)
+    np.testing.assert_allclose(_to_nchw(oracle.conv_dgrad(c, dy, w), c), gx.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(_w_to_oihw(oracle.conv_wgrad(c, x, dy), c), gw.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.conv_bgrad(c, dy), gb_.numpy(), rtol=1e-12, atol=1e-12)
