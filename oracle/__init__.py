@@ -29,7 +29,8 @@ _lib = None
 class _Desc(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int64) for name in (
         "n", "c_in", "c_out", "groups", "in_h", "in_w", "k_h", "k_w",
-        "s_h", "s_w", "p_h", "p_w", "d_h", "d_w", "p_h_end", "p_w_end")] + [
+        "s_h", "s_w", "p_h", "p_w", "d_h", "d_w", "p_h_end", "p_w_end",
+        "in_d", "k_d", "s_d", "p_d", "p_d_end", "d_d")] + [
         ("nhwc", ctypes.c_int32), ("w_ohwi", ctypes.c_int32)]
 
 
@@ -37,9 +38,11 @@ class _Desc(ctypes.Structure):
 class Conv:
     """Shape of one convolution as the oracle sees it.
 
-    ``spatial_dims`` is 1 for conv1d (NCL / NLC; ``in_hw = (1, L)``) and 2 for
-    conv2d.  ``nhwc`` selects channels-last activations, ``w_ohwi`` selects the
-    [C_out, KH, KW, C_in/G] weight order instead of [C_out, C_in/G, KH, KW].
+    ``spatial_dims`` is 1 for conv1d (NCL / NLC; ``in_hw = (1, L)``), 2 for
+    conv2d and 3 for conv3d (then ``in_hw``, ``k``, ``stride``, ``pad``, ``dil`` and
+    ``pad_end`` are (depth, height, width) triples).  ``nhwc`` selects channels-last
+    activations, ``w_ohwi`` selects the [C_out, (KD,) KH, KW, C_in/G] weight order
+    instead of [C_out, C_in/G, (KD,) KH, KW].
     """
     n: int
     c_in: int
@@ -58,17 +61,32 @@ class Conv:
     def pads_end(self):
         return tuple(self.pad) if self.pad_end is None else tuple(self.pad_end)
 
+    def _full(self, t, default):
+        """A per-axis tuple with one entry per axis of ``in_hw`` (defaults, such as stride (1, 1),
+        are pairs: a 3-D shape takes the default for its leading depth entry)."""
+        t = tuple(t)
+        return (default,) * (len(self.in_hw) - len(t)) + t
+
+    def _dhw(self, t, depth_default):
+        """(depth, height, width) of a per-axis tuple; depth_default for 1-D and 2-D shapes."""
+        t = self._full(t, depth_default)
+        return t if self.spatial_dims == 3 else (depth_default,) + t
+
     def _c(self) -> _Desc:
-        pe = self.pads_end()
-        return _Desc(self.n, self.c_in, self.c_out, self.groups, self.in_hw[0], self.in_hw[1],
-                     self.k[0], self.k[1], self.stride[0], self.stride[1], self.pad[0], self.pad[1],
-                     self.dil[0], self.dil[1], pe[0], pe[1], int(self.nhwc), int(self.w_ohwi))
+        ind, inh, inw = self._dhw(self.in_hw, 1)
+        kd, kh, kw = self._dhw(self.k, 1)
+        sd, sh, sw = self._dhw(self.stride, 1)
+        pd, ph, pw = self._dhw(self.pad, 0)
+        dd, dh, dw = self._dhw(self.dil, 1)
+        ped, peh, pew = self._dhw(self.pads_end(), 0)
+        return _Desc(self.n, self.c_in, self.c_out, self.groups, inh, inw, kh, kw, sh, sw, ph, pw, dh, dw,
+                     peh, pew, ind, kd, sd, pd, ped, dd, int(self.nhwc), int(self.w_ohwi))
 
     def out_hw(self):
-        pe = self.pads_end()
-        oh = out_size2(self.in_hw[0], self.k[0], self.stride[0], self.pad[0], pe[0], self.dil[0])
-        ow = out_size2(self.in_hw[1], self.k[1], self.stride[1], self.pad[1], pe[1], self.dil[1])
-        return oh, ow
+        """Output extent per spatial axis: (oh, ow), or (od, oh, ow) for 3-D shapes."""
+        k, s, p, d = self._full(self.k, 1), self._full(self.stride, 1), self._full(self.pad, 0), self._full(self.dil, 1)
+        pe = self._full(self.pads_end(), 0)
+        return tuple(out_size2(self.in_hw[i], k[i], s[i], p[i], pe[i], d[i]) for i in range(len(self.in_hw)))
 
     def x_shape(self):
         return _act_shape(self, self.c_in, self.in_hw)
@@ -81,14 +99,14 @@ class Conv:
         if self.spatial_dims == 1:
             return (self.c_out, self.k[1], cpg) if self.w_ohwi else (self.c_out, cpg, self.k[1])
         if self.w_ohwi:
-            return (self.c_out, self.k[0], self.k[1], cpg)
-        return (self.c_out, cpg, self.k[0], self.k[1])
+            return (self.c_out,) + tuple(self.k) + (cpg,)
+        return (self.c_out, cpg) + tuple(self.k)
 
 
 def _act_shape(c: Conv, ch: int, hw):
     if c.spatial_dims == 1:
         return (c.n, hw[1], ch) if c.nhwc else (c.n, ch, hw[1])
-    return (c.n, hw[0], hw[1], ch) if c.nhwc else (c.n, ch, hw[0], hw[1])
+    return (c.n,) + tuple(hw) + (ch,) if c.nhwc else (c.n, ch) + tuple(hw)
 
 
 def build(force: bool = False) -> str:

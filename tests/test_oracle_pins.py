@@ -418,3 +418,63 @@ def test_begin_end_padding_matches_torch_float64(ci):
     np.testing.assert_allclose(_to_nchw(oracle.conv_dgrad(c, dy, w), c), gx.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(_w_to_oihw(oracle.conv_wgrad(c, x, dy), c), gw.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(oracle.conv_bgrad(c, dy), gb_.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------- 3-D convolution
+
+CASES3 = [
+    Conv(n=2, c_in=4, c_out=6, in_hw=(5, 6, 7), k=(3, 3, 3), stride=(1, 2, 1), pad=(1, 1, 0), dil=(1, 1, 2),
+         groups=2, spatial_dims=3),
+    Conv(n=1, c_in=3, c_out=4, in_hw=(4, 5, 6), k=(2, 3, 1), stride=(2, 1, 1), pad=(0, 1, 0), pad_end=(1, 0, 2),
+         spatial_dims=3, nhwc=True, w_ohwi=True),
+    Conv(n=2, c_in=6, c_out=6, in_hw=(3, 4, 5), k=(3, 3, 3), stride=(1, 1, 1), pad=(1, 1, 1), groups=6,
+         spatial_dims=3, nhwc=True),
+]
+
+
+def _to_ncdhw(a, c):
+    return a.transpose(0, 4, 1, 2, 3) if c.nhwc else a
+
+
+def _w_to_oidhw(w, c):
+    return w.transpose(0, 4, 1, 2, 3) if c.w_ohwi else w
+
+
+@pytest.mark.parametrize("ci", range(len(CASES3)))
+def test_conv3d_matches_torch_float64(ci):
+    # torch conv3d on the explicitly padded input, and its autograd input, weight and bias gradients
+    c = CASES3[ci]
+    F = torch.nn.functional
+    x = synth.normal(151 + ci, c.x_shape()).astype(np.float32)
+    w = synth.normal(152 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(153 + ci, (c.c_out,)).astype(np.float32)
+    dy = synth.normal(154 + ci, c.y_shape()).astype(np.float32)
+    xt = torch.from_numpy(_to_ncdhw(x, c).astype(np.float64).copy()).requires_grad_(True)
+    wt = torch.from_numpy(_w_to_oidhw(w, c).astype(np.float64).copy()).requires_grad_(True)
+    bt = torch.from_numpy(b.astype(np.float64)).requires_grad_(True)
+    pad, pe = c._full(c.pad, 0), c._full(c.pads_end(), 0)
+    xp = F.pad(xt, (pad[2], pe[2], pad[1], pe[1], pad[0], pe[0]))
+    yt = F.conv3d(xp, wt, bt, stride=c._full(c.stride, 1), dilation=c._full(c.dil, 1), groups=c.groups)
+    np.testing.assert_allclose(_to_ncdhw(oracle.conv_fwd(c, x, w, b), c), yt.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dyt = torch.from_numpy(_to_ncdhw(dy, c).astype(np.float64).copy())
+    gx, gw, gb_ = torch.autograd.grad(yt, (xt, wt, bt), dyt)
+    np.testing.assert_allclose(_to_ncdhw(oracle.conv_dgrad(c, dy, w), c), gx.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(_to_ncdhw(oracle.conv_dgrad(c, dy, w, scatter=True), c), gx.numpy(),
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(_w_to_oidhw(oracle.conv_wgrad(c, x, dy), c), gw.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.conv_bgrad(c, dy), gb_.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_conv3d_with_unit_depth_is_conv2d():
+    # depth 1, kernel depth 1: the 3-D sums are the 2-D ones
+    c2 = Conv(n=2, c_in=4, c_out=6, in_hw=(6, 7), k=(3, 2), stride=(2, 1), pad=(1, 0), dil=(1, 2), groups=2, nhwc=True,
+              w_ohwi=True)
+    c3 = Conv(n=2, c_in=4, c_out=6, in_hw=(1, 6, 7), k=(1, 3, 2), stride=(1, 2, 1), pad=(0, 1, 0), dil=(1, 1, 2),
+              groups=2, nhwc=True, w_ohwi=True, spatial_dims=3)
+    x = synth.normal(161, c2.x_shape()).astype(np.float32)
+    w = synth.normal(162, c2.w_shape()).astype(np.float32)
+    dy = synth.normal(163, c2.y_shape()).astype(np.float32)
+    x3, w3, dy3 = x.reshape(c3.x_shape()), w.reshape(c3.w_shape()), dy.reshape(c3.y_shape())
+    np.testing.assert_array_equal(oracle.conv_fwd(c3, x3, w3).reshape(c2.y_shape()), oracle.conv_fwd(c2, x, w))
+    np.testing.assert_array_equal(oracle.conv_dgrad(c3, dy3, w3).reshape(c2.x_shape()), oracle.conv_dgrad(c2, dy, w))
+    np.testing.assert_array_equal(oracle.conv_wgrad(c3, x3, dy3).reshape(c2.w_shape()), oracle.conv_wgrad(c2, x, dy))
