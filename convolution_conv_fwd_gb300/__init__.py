@@ -38,9 +38,9 @@ class Desc(ctypes.Structure):
     """Mirror of gbconv_desc."""
     _fields_ = [("spatial_dims", ctypes.c_int32), ("layout", ctypes.c_int32), ("wlayout", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("n", ctypes.c_int64), ("c_in", ctypes.c_int64),
-                ("c_out", ctypes.c_int64), ("groups", ctypes.c_int64), ("in_", ctypes.c_int64 * 2),
-                ("k", ctypes.c_int64 * 2), ("stride", ctypes.c_int64 * 2), ("pad", ctypes.c_int64 * 2),
-                ("dil", ctypes.c_int64 * 2), ("pad_end", ctypes.c_int64 * 2), ("pad_mode", ctypes.c_int32)]
+                ("c_out", ctypes.c_int64), ("groups", ctypes.c_int64), ("in_", ctypes.c_int64 * 3),
+                ("k", ctypes.c_int64 * 3), ("stride", ctypes.c_int64 * 3), ("pad", ctypes.c_int64 * 3),
+                ("dil", ctypes.c_int64 * 3), ("pad_end", ctypes.c_int64 * 3), ("pad_mode", ctypes.c_int32)]
 
 
 class GbconvError(RuntimeError):
@@ -83,10 +83,13 @@ _lib = _load()
 # ---------------------------------------------------------------- raw C entry points
 
 def gbconv_out_shape(desc: Desc):
-    out = (ctypes.c_int64 * 2)()
+    """(OH, OW) for 2-D, (L_out, 1) for 1-D, (OD, OH, OW) for 3-D descriptors."""
+    out = (ctypes.c_int64 * 3)()
     s = _lib.gbconv_out_shape(ctypes.byref(desc), out)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_out_shape")
+    if desc.spatial_dims == 3:
+        return int(out[0]), int(out[1]), int(out[2])
     return int(out[0]), int(out[1])
 
 
@@ -152,31 +155,39 @@ def status_string(status: int) -> str:
 
 def make_desc(n, c_in, c_out, in_size, k, stride=1, pad=0, dil=1, groups=1, *, spatial_dims=2,
               layout="nhwc", wlayout="ohwi", dtype="bf16", pad_end=None) -> Desc:
-    """Build a gbconv_desc.  Sizes are ints (1-D) or pairs (2-D).  ``pad`` is the padding before each
-    axis, and after it too unless ``pad_end`` gives the padding after (begin, end padding)."""
+    """Build a gbconv_desc.  Sizes are ints (1-D), pairs (2-D: height, width) or triples (3-D: depth,
+    height, width); an int is used on every axis.  ``pad`` is the padding before each axis, and after
+    it too unless ``pad_end`` gives the padding after (begin, end padding)."""
     def pair(v):
         if isinstance(v, (tuple, list)):
-            return (int(v[0]), int(v[1]) if len(v) > 1 else 1)
-        return (int(v), int(v)) if spatial_dims == 2 else (int(v), 1)
+            t = [int(e) for e in v][:3]
+        else:
+            t = [int(v)] * spatial_dims
+        return tuple(t + [1] * (3 - len(t)))
     d = Desc()
     d.spatial_dims = spatial_dims
-    d.layout = {"nchw": GBCONV_NCHW, "ncl": GBCONV_NCHW, "nhwc": GBCONV_NHWC, "nlc": GBCONV_NHWC}[layout]
-    d.wlayout = {"oihw": GBCONV_W_OIHW, "oik": GBCONV_W_OIHW, "ohwi": GBCONV_W_OHWI, "oki": GBCONV_W_OHWI}[wlayout]
+    d.layout = {"nchw": GBCONV_NCHW, "ncl": GBCONV_NCHW, "ncdhw": GBCONV_NCHW, "nhwc": GBCONV_NHWC, "nlc": GBCONV_NHWC,
+                "ndhwc": GBCONV_NHWC}[layout]
+    d.wlayout = {"oihw": GBCONV_W_OIHW, "oik": GBCONV_W_OIHW, "oidhw": GBCONV_W_OIHW, "ohwi": GBCONV_W_OHWI,
+                 "oki": GBCONV_W_OHWI, "odhwi": GBCONV_W_OHWI}[wlayout]
     d.dtype = {"f32": GBCONV_F32, "bf16": GBCONV_BF16}[dtype]
     d.n, d.c_in, d.c_out, d.groups = int(n), int(c_in), int(c_out), int(groups)
     for name, v in (("in_", in_size), ("k", k), ("stride", stride), ("pad", pad), ("dil", dil)):
-        a, b = pair(v)
-        getattr(d, name)[0] = a
-        getattr(d, name)[1] = b
+        t = pair(v)
+        for i in range(3):
+            getattr(d, name)[i] = t[i]
     if pad_end is not None:
         d.pad_mode = GBCONV_PAD_BEGIN_END
-        d.pad_end[0], d.pad_end[1] = pair(pad_end)
+        t = pair(pad_end)
+        for i in range(3):
+            d.pad_end[i] = t[i]
     return d
 
 
 def desc_shapes(d: Desc):
     """(x_shape, w_shape, y_shape) in the layouts the descriptor names."""
-    oh, ow = gbconv_out_shape(d)
+    out = gbconv_out_shape(d)
+    oh, ow = out[0], out[1]
     cpg = d.c_in // d.groups
     if d.spatial_dims == 1:
         L, K = d.in_[0], d.k[0]
@@ -184,10 +195,14 @@ def desc_shapes(d: Desc):
         y = (d.n, oh, d.c_out) if d.layout == GBCONV_NHWC else (d.n, d.c_out, oh)
         w = (d.c_out, K, cpg) if d.wlayout == GBCONV_W_OHWI else (d.c_out, cpg, K)
         return x, w, y
-    H, W, KH, KW = d.in_[0], d.in_[1], d.k[0], d.k[1]
-    x = (d.n, H, W, d.c_in) if d.layout == GBCONV_NHWC else (d.n, d.c_in, H, W)
-    y = (d.n, oh, ow, d.c_out) if d.layout == GBCONV_NHWC else (d.n, d.c_out, oh, ow)
-    w = (d.c_out, KH, KW, cpg) if d.wlayout == GBCONV_W_OHWI else (d.c_out, cpg, KH, KW)
+    if d.spatial_dims == 3:
+        sp_in, sp_k, sp_out = tuple(d.in_[:3]), tuple(d.k[:3]), out
+    else:
+        sp_in, sp_k, sp_out = tuple(d.in_[:2]), tuple(d.k[:2]), (oh, ow)
+    nhwc = d.layout == GBCONV_NHWC
+    x = (d.n,) + sp_in + (d.c_in,) if nhwc else (d.n, d.c_in) + sp_in
+    y = (d.n,) + sp_out + (d.c_out,) if nhwc else (d.n, d.c_out) + sp_out
+    w = (d.c_out,) + sp_k + (cpg,) if d.wlayout == GBCONV_W_OHWI else (d.c_out, cpg) + sp_k
     return x, w, y
 
 

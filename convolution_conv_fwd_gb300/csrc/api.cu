@@ -52,7 +52,7 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 gbconv_status resolve(const gbconv_desc* d, Problem* p) {
   if (!d || !p) return GBCONV_EINVAL;
-  if (d->spatial_dims != 1 && d->spatial_dims != 2) return GBCONV_EINVAL;
+  if (d->spatial_dims < 1 || d->spatial_dims > 3) return GBCONV_EINVAL;
   if (d->layout != GBCONV_NCHW && d->layout != GBCONV_NHWC) return GBCONV_EINVAL;
   if (d->wlayout != GBCONV_W_OIHW && d->wlayout != GBCONV_W_OHWI) return GBCONV_EINVAL;
   if (d->dtype != GBCONV_F32 && d->dtype != GBCONV_BF16) return GBCONV_EINVAL;
@@ -63,42 +63,54 @@ gbconv_status resolve(const gbconv_desc* d, Problem* p) {
   q.Cin = d->c_in;
   q.Cout = d->c_out;
   q.G = d->groups;
+  // axis i of the descriptor -> (extent, kernel, stride, pad, pad_end, dilation)
+  auto axis = [&](int i, int64_t& in, int64_t& k, int64_t& s, int64_t& p, int64_t& pe, int64_t& dl) {
+    in = d->in[i]; k = d->k[i]; s = d->stride[i]; p = d->pad[i]; dl = d->dil[i];
+    pe = be ? d->pad_end[i] : p;
+  };
+  q.D = 1; q.KD = 1; q.SD = 1; q.PD = 0; q.PDe = 0; q.DD = 1;
   if (d->spatial_dims == 1) {  // the length axis is carried as the width
     q.H = 1; q.KH = 1; q.SH = 1; q.PH = 0; q.PHe = 0; q.DH = 1;
-    q.W = d->in[0]; q.KW = d->k[0]; q.SW = d->stride[0]; q.PW = d->pad[0]; q.DW = d->dil[0];
-    q.PWe = be ? d->pad_end[0] : q.PW;
+    axis(0, q.W, q.KW, q.SW, q.PW, q.PWe, q.DW);
+  } else if (d->spatial_dims == 2) {
+    axis(0, q.H, q.KH, q.SH, q.PH, q.PHe, q.DH);
+    axis(1, q.W, q.KW, q.SW, q.PW, q.PWe, q.DW);
   } else {
-    q.H = d->in[0]; q.KH = d->k[0]; q.SH = d->stride[0]; q.PH = d->pad[0]; q.DH = d->dil[0];
-    q.W = d->in[1]; q.KW = d->k[1]; q.SW = d->stride[1]; q.PW = d->pad[1]; q.DW = d->dil[1];
-    q.PHe = be ? d->pad_end[0] : q.PH;
-    q.PWe = be ? d->pad_end[1] : q.PW;
+    axis(0, q.D, q.KD, q.SD, q.PD, q.PDe, q.DD);
+    axis(1, q.H, q.KH, q.SH, q.PH, q.PHe, q.DH);
+    axis(2, q.W, q.KW, q.SW, q.PW, q.PWe, q.DW);
   }
   if (q.N <= 0 || q.Cin <= 0 || q.Cout <= 0 || q.G <= 0) return GBCONV_EINVAL;
-  if (q.H <= 0 || q.W <= 0 || q.KH <= 0 || q.KW <= 0) return GBCONV_EINVAL;
+  if (q.H <= 0 || q.W <= 0 || q.KH <= 0 || q.KW <= 0 || q.D <= 0 || q.KD <= 0) return GBCONV_EINVAL;
   if (q.SH <= 0 || q.SW <= 0 || q.DH <= 0 || q.DW <= 0 || q.PH < 0 || q.PW < 0 || q.PHe < 0 || q.PWe < 0)
     return GBCONV_EINVAL;
+  if (q.SD <= 0 || q.DD <= 0 || q.PD < 0 || q.PDe < 0) return GBCONV_EINVAL;
   if (q.Cin % q.G != 0 || q.Cout % q.G != 0) return GBCONV_EINVAL;
   // Keep every intermediate well inside int64 before multiplying.
   const int64_t lim = int64_t(1) << 31;
   if (q.N >= lim || q.Cin >= lim || q.Cout >= lim || q.H >= lim || q.W >= lim || q.KH >= lim || q.KW >= lim ||
       q.SH >= lim || q.SW >= lim || q.PH >= lim || q.PW >= lim || q.PHe >= lim || q.PWe >= lim || q.DH >= lim ||
-      q.DW >= lim)
+      q.DW >= lim || q.D >= lim || q.KD >= lim || q.SD >= lim || q.PD >= lim || q.PDe >= lim || q.DD >= lim)
     return GBCONV_EUNSUPPORTED;
   const int64_t effh = (q.KH - 1) * q.DH + 1, effw = (q.KW - 1) * q.DW + 1;
-  if (q.H + q.PH + q.PHe < effh || q.W + q.PW + q.PWe < effw) return GBCONV_EINVAL;
+  const int64_t effd = (q.KD - 1) * q.DD + 1;
+  if (q.H + q.PH + q.PHe < effh || q.W + q.PW + q.PWe < effw || q.D + q.PD + q.PDe < effd) return GBCONV_EINVAL;
   q.OH = (q.H + q.PH + q.PHe - effh) / q.SH + 1;
   q.OW = (q.W + q.PW + q.PWe - effw) / q.SW + 1;
+  q.OD = (q.D + q.PD + q.PDe - effd) / q.SD + 1;
   q.nhwc = d->layout == GBCONV_NHWC;
   q.ohwi = d->wlayout == GBCONV_W_OHWI;
   q.bf16 = d->dtype == GBCONV_BF16;
   // 32-bit device indexing: element counts and the farthest coordinate read.
-  auto fits = [](int64_t a, int64_t b, int64_t c, int64_t e) -> bool {
-    __int128 v = static_cast<__int128>(a) * b * c * e;
+  auto fits = [](int64_t a, int64_t b, int64_t c, int64_t e, int64_t f) -> bool {
+    __int128 v = static_cast<__int128>(a) * b * c * e * f;
     return v <= kMax32;
   };
-  if (!fits(q.N, q.Cin, q.H, q.W) || !fits(q.N, q.Cout, q.OH, q.OW) || !fits(q.Cout, q.cpg(), q.KH, q.KW))
+  if (!fits(q.N, q.Cin, q.D, q.H, q.W) || !fits(q.N, q.Cout, q.OD, q.OH, q.OW) ||
+      !fits(q.Cout, q.cpg(), q.KD, q.KH, q.KW))
     return GBCONV_EUNSUPPORTED;
-  if ((q.OH - 1) * q.SH + (q.KH - 1) * q.DH > kMax32 || (q.OW - 1) * q.SW + (q.KW - 1) * q.DW > kMax32)
+  if ((q.OH - 1) * q.SH + (q.KH - 1) * q.DH > kMax32 || (q.OW - 1) * q.SW + (q.KW - 1) * q.DW > kMax32 ||
+      (q.OD - 1) * q.SD + (q.KD - 1) * q.DD > kMax32)
     return GBCONV_EUNSUPPORTED;
   *p = q;
   return GBCONV_OK;
@@ -106,22 +118,52 @@ gbconv_status resolve(const gbconv_desc* d, Problem* p) {
 
 namespace {
 
+// The 2-D view the tensor-core and depthwise families work on: 1-D and 2-D shapes as they are, and
+// channels-last 3-D shapes whose depth axis only repeats the 2-D convolution (kernel depth 1, unit
+// stride, no depth padding) with the depth folded into the batch.  false for every other 3-D shape,
+// which the generic kernels serve.
+bool planar(const Problem& p, Problem* q) {
+  if (!p.depth_trivial()) return false;
+  if (p.D == 1) {
+    *q = p;
+    return true;
+  }
+  if (!p.nhwc) return false;
+  *q = p.fold_depth();
+  return true;
+}
+
 int32_t select_fwd(const Problem& p, bool aligned) {
-  if (aligned && depthwise_supported(p)) return GBCONV_K_DEPTHWISE;
-  if (aligned && pointwise_supported(p)) return GBCONV_K_POINTWISE;
-  if (aligned && implicit_fwd_supported(p)) return GBCONV_K_IMPLICIT;
+  Problem q;
+  if (!aligned || !planar(p, &q)) return GBCONV_K_DIRECT;
+  if (depthwise_supported(q)) return GBCONV_K_DEPTHWISE;
+  if (pointwise_supported(q)) return GBCONV_K_POINTWISE;
+  if (implicit_fwd_supported(q)) return GBCONV_K_IMPLICIT;
   return GBCONV_K_DIRECT;
 }
 
 int32_t select_dgrad(const Problem& p, bool aligned) {
-  if (aligned && implicit_dgrad_supported(p)) return GBCONV_K_DGRAD;
-  if (aligned && depthwise_dgrad_supported(p)) return GBCONV_K_DEPTHWISE_DGRAD;
+  Problem q;
+  if (!aligned || !planar(p, &q)) return GBCONV_K_DIRECT_DGRAD;
+  if (implicit_dgrad_supported(q)) return GBCONV_K_DGRAD;
+  if (depthwise_dgrad_supported(q)) return GBCONV_K_DEPTHWISE_DGRAD;
   return GBCONV_K_DIRECT_DGRAD;
 }
 
 int32_t select_wgrad(const Problem& p, bool aligned) {
-  if (aligned && wgrad_tc_supported(p)) return GBCONV_K_WGRAD;
+  Problem q;
+  if (aligned && planar(p, &q) && wgrad_tc_supported(q)) return GBCONV_K_WGRAD;
   return GBCONV_K_DIRECT_WGRAD;
+}
+
+// The problem a family's launcher takes: the planar view for the 2-D families, the full shape for
+// the generic kernels.
+Problem launch_view(const Problem& p, int32_t family) {
+  Problem q;
+  if (family == GBCONV_K_DIRECT || family == GBCONV_K_DIRECT_DGRAD || family == GBCONV_K_DIRECT_WGRAD ||
+      !planar(p, &q))
+    return p;
+  return q;
 }
 
 int32_t select_op(const Problem& p, int32_t op, bool aligned) {
@@ -142,9 +184,11 @@ gbconv_status bwd_data(const gbconv_desc* desc, const void* dy, const void* w, c
   Launch l;
   if (!device_context(&l, stream)) return GBCONV_ECUDA;
   const bool aligned = aligned16(dy) && aligned16(w) && aligned16(dx);
-  switch (select_dgrad(p, aligned)) {
-    case GBCONV_K_DGRAD: return launch_implicit_dgrad(p, dy, w, bias, dx, l);
-    case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(p, dy, w, bias, dx, l);
+  const int32_t k = select_dgrad(p, aligned);
+  const Problem q = launch_view(p, k);
+  switch (k) {
+    case GBCONV_K_DGRAD: return launch_implicit_dgrad(q, dy, w, bias, dx, l);
+    case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(q, dy, w, bias, dx, l);
     default: return launch_direct_dgrad(p, dy, w, bias, dx, l);
   }
 }
@@ -156,7 +200,7 @@ using namespace gbconv;
 
 extern "C" {
 
-gbconv_status gbconv_out_shape(const gbconv_desc* desc, int64_t out[2]) {
+gbconv_status gbconv_out_shape(const gbconv_desc* desc, int64_t out[3]) {
   if (!out) return GBCONV_EINVAL;
   Problem p;
   gbconv_status s = resolve(desc, &p);
@@ -164,9 +208,15 @@ gbconv_status gbconv_out_shape(const gbconv_desc* desc, int64_t out[2]) {
   if (desc->spatial_dims == 1) {
     out[0] = p.OW;
     out[1] = 1;
-  } else {
+    out[2] = 1;
+  } else if (desc->spatial_dims == 2) {
     out[0] = p.OH;
     out[1] = p.OW;
+    out[2] = 1;
+  } else {
+    out[0] = p.OD;
+    out[1] = p.OH;
+    out[2] = p.OW;
   }
   return GBCONV_OK;
 }
@@ -188,10 +238,11 @@ gbconv_status gbconv_describe(const gbconv_desc* desc, int32_t op, char* buf, in
   const int32_t k = select_op(p, op, true);
   static const char* const names[] = {"direct", "depthwise", "pointwise", "implicit", "dgrad", "direct_dgrad",
                                       "depthwise_dgrad", "direct_wgrad", "wgrad"};
+  const Problem q = launch_view(p, k);
   if ((k == GBCONV_K_IMPLICIT || k == GBCONV_K_DGRAD) &&
-      implicit_describe(p, k == GBCONV_K_DGRAD, buf, size_t(len)))
+      implicit_describe(q, k == GBCONV_K_DGRAD, buf, size_t(len)))
     return GBCONV_OK;
-  if (k == GBCONV_K_WGRAD && wgrad_tc_describe(p, buf, size_t(len))) return GBCONV_OK;
+  if (k == GBCONV_K_WGRAD && wgrad_tc_describe(q, buf, size_t(len))) return GBCONV_OK;
   std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_WGRAD) ? names[k] : "unknown");
   return GBCONV_OK;
 }
@@ -205,10 +256,12 @@ gbconv_status gbconv_fwd(const gbconv_desc* desc, const void* x, const void* w, 
   Launch l;
   if (!device_context(&l, stream)) return GBCONV_ECUDA;
   const bool aligned = aligned16(x) && aligned16(w) && aligned16(y);
-  switch (select_fwd(p, aligned)) {
-    case GBCONV_K_DEPTHWISE: return launch_depthwise_fwd(p, x, w, bias, y, l);
-    case GBCONV_K_POINTWISE: return launch_pointwise_fwd(p, x, w, bias, y, l);
-    case GBCONV_K_IMPLICIT: return launch_implicit_fwd(p, x, w, bias, y, l);
+  const int32_t k = select_fwd(p, aligned);
+  const Problem q = launch_view(p, k);
+  switch (k) {
+    case GBCONV_K_DEPTHWISE: return launch_depthwise_fwd(q, x, w, bias, y, l);
+    case GBCONV_K_POINTWISE: return launch_pointwise_fwd(q, x, w, bias, y, l);
+    case GBCONV_K_IMPLICIT: return launch_implicit_fwd(q, x, w, bias, y, l);
     default: return launch_direct_fwd(p, x, w, bias, y, l);
   }
 }
@@ -220,7 +273,8 @@ gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc* desc, int64_t* byte
   if (s != GBCONV_OK) return s;
   // Enough for whichever path a call takes (the tensor-core path needs aligned pointers).
   int64_t b = direct_wgrad_workspace(p);
-  if (wgrad_tc_supported(p)) b = std::max(b, wgrad_tc_workspace(p));
+  Problem q;
+  if (planar(p, &q) && wgrad_tc_supported(q)) b = std::max(b, wgrad_tc_workspace(q));
   *bytes = b;
   return GBCONV_OK;
 }
@@ -233,11 +287,12 @@ gbconv_status gbconv_bwd_filter(const gbconv_desc* desc, const void* x, const vo
   if (!x || !dy || !dw) return GBCONV_EINVAL;
   const bool aligned = aligned16(x) && aligned16(dy) && aligned16(dw) && aligned16(workspace);
   const int32_t k = select_wgrad(p, aligned);
-  const int64_t need = k == GBCONV_K_WGRAD ? wgrad_tc_workspace(p) : direct_wgrad_workspace(p);
+  const Problem q = launch_view(p, k);
+  const int64_t need = k == GBCONV_K_WGRAD ? wgrad_tc_workspace(q) : direct_wgrad_workspace(p);
   if (workspace_bytes < need || (need > 0 && !workspace) || !aligned16(workspace)) return GBCONV_EINVAL;
   Launch l;
   if (!device_context(&l, stream)) return GBCONV_ECUDA;
-  if (k == GBCONV_K_WGRAD) return launch_wgrad_tc(p, x, dy, dw, db, workspace, l);
+  if (k == GBCONV_K_WGRAD) return launch_wgrad_tc(q, x, dy, dw, db, workspace, l);
   return launch_direct_wgrad(p, x, dy, dw, db, workspace, l);
 }
 

@@ -8,7 +8,9 @@
 // outside, bias after the reduction as in `conv2d_bias_forward`), with
 // dilation per oarust `Conv1dGeometry`.  The input gradient is the gather
 // form: each thread owns one dx element and sums the (dy, w) products whose
-// forward read lands on it, so nothing is accumulated atomically.
+// forward read lands on it, so nothing is accumulated atomically.  Shapes are
+// 3-D (burn-cubecl `ConvOptions<N>`: the same index map on every spatial
+// axis); 1-D and 2-D ones have depth 1.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,6 +25,7 @@ namespace {
 
 struct DirectArgs {
   int N, Cin, Cout, G, H, W, KH, KW, SH, SW, PH, PW, DH, DW, OH, OW;
+  int D, KD, SD, PD, DD, OD;  // depth axis (1, 1, 1, 0, 1, 1 for 1-D and 2-D shapes)
   int nhwc, ohwi;
 };
 
@@ -35,13 +38,15 @@ template <typename T> __device__ __forceinline__ T cvt(float v);
 template <> __device__ __forceinline__ float cvt<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 cvt<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ int act_off(const DirectArgs& a, int C, int H, int W, int n, int c, int h, int w) {
-  return a.nhwc ? ((n * H + h) * W + w) * C + c : ((n * C + c) * H + h) * W + w;
+__device__ __forceinline__ int act_off(const DirectArgs& a, int C, int D, int H, int W, int n, int c, int d, int h,
+                                       int w) {
+  return a.nhwc ? (((n * D + d) * H + h) * W + w) * C + c : (((n * C + c) * D + d) * H + h) * W + w;
 }
 
-__device__ __forceinline__ int w_off(const DirectArgs& a, int co, int cl, int kh, int kw) {
+__device__ __forceinline__ int w_off(const DirectArgs& a, int co, int cl, int kd, int kh, int kw) {
   const int cpg = a.Cin / a.G;
-  return a.ohwi ? ((co * a.KH + kh) * a.KW + kw) * cpg + cl : ((co * cpg + cl) * a.KH + kh) * a.KW + kw;
+  return a.ohwi ? (((co * a.KD + kd) * a.KH + kh) * a.KW + kw) * cpg + cl
+                : (((co * cpg + cl) * a.KD + kd) * a.KH + kh) * a.KW + kw;
 }
 
 template <typename T>
@@ -49,37 +54,44 @@ __global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T
                                   const float* __restrict__ bias, T* __restrict__ y) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
   ptx::grid_dep_launch();
-  const int total = a.N * a.Cout * a.OH * a.OW;
+  const int total = a.N * a.Cout * a.OD * a.OH * a.OW;
   const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    int n, co, oh, ow;
+    int n, co, od, oh, ow;
     if (a.nhwc) {  // channel fastest, so a warp writes contiguous channels
       co = i % a.Cout;
       int r = i / a.Cout;
       ow = r % a.OW; r /= a.OW;
-      oh = r % a.OH; n = r / a.OH;
+      oh = r % a.OH; r /= a.OH;
+      od = r % a.OD; n = r / a.OD;
     } else {
       ow = i % a.OW;
       int r = i / a.OW;
       oh = r % a.OH; r /= a.OH;
+      od = r % a.OD; r /= a.OD;
       co = r % a.Cout; n = r / a.Cout;
     }
     const int g = co / opg;
     float acc = 0.f;
     for (int cl = 0; cl < cpg; ++cl) {
       const int ci = g * cpg + cl;
-      for (int kh = 0; kh < a.KH; ++kh) {
-        const int ih = oh * a.SH + kh * a.DH - a.PH;
-        if (ih < 0 || ih >= a.H) continue;
-        for (int kw = 0; kw < a.KW; ++kw) {
-          const int iw = ow * a.SW + kw * a.DW - a.PW;
-          if (iw < 0 || iw >= a.W) continue;
-          acc = fmaf(ld(x, act_off(a, a.Cin, a.H, a.W, n, ci, ih, iw)), ld(w, w_off(a, co, cl, kh, kw)), acc);
+      for (int kd = 0; kd < a.KD; ++kd) {
+        const int id = od * a.SD + kd * a.DD - a.PD;
+        if (id < 0 || id >= a.D) continue;
+        for (int kh = 0; kh < a.KH; ++kh) {
+          const int ih = oh * a.SH + kh * a.DH - a.PH;
+          if (ih < 0 || ih >= a.H) continue;
+          for (int kw = 0; kw < a.KW; ++kw) {
+            const int iw = ow * a.SW + kw * a.DW - a.PW;
+            if (iw < 0 || iw >= a.W) continue;
+            acc = fmaf(ld(x, act_off(a, a.Cin, a.D, a.H, a.W, n, ci, id, ih, iw)), ld(w, w_off(a, co, cl, kd, kh, kw)),
+                       acc);
+          }
         }
       }
     }
     if (bias) acc += __ldg(bias + co);
-    y[act_off(a, a.Cout, a.OH, a.OW, n, co, oh, ow)] = cvt<T>(acc);
+    y[act_off(a, a.Cout, a.OD, a.OH, a.OW, n, co, od, oh, ow)] = cvt<T>(acc);
   }
 }
 
@@ -88,44 +100,54 @@ __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, cons
                                     const float* __restrict__ bias, T* __restrict__ dx) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
   ptx::grid_dep_launch();
-  const int total = a.N * a.Cin * a.H * a.W;
+  const int total = a.N * a.Cin * a.D * a.H * a.W;
   const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    int n, ci, ih, iw;
+    int n, ci, id, ih, iw;
     if (a.nhwc) {
       ci = i % a.Cin;
       int r = i / a.Cin;
       iw = r % a.W; r /= a.W;
-      ih = r % a.H; n = r / a.H;
+      ih = r % a.H; r /= a.H;
+      id = r % a.D; n = r / a.D;
     } else {
       iw = i % a.W;
       int r = i / a.W;
       ih = r % a.H; r /= a.H;
+      id = r % a.D; r /= a.D;
       ci = r % a.Cin; n = r / a.Cin;
     }
     const int g = ci / cpg, cl = ci - g * cpg;
     float acc = 0.f;
     for (int co = g * opg; co < (g + 1) * opg; ++co) {
-      for (int kh = 0; kh < a.KH; ++kh) {
-        const int th = ih + a.PH - kh * a.DH;
-        if (th < 0 || th % a.SH != 0) continue;
-        const int oh = th / a.SH;
-        if (oh >= a.OH) continue;
-        for (int kw = 0; kw < a.KW; ++kw) {
-          const int tw = iw + a.PW - kw * a.DW;
-          if (tw < 0 || tw % a.SW != 0) continue;
-          const int ow = tw / a.SW;
-          if (ow >= a.OW) continue;
-          acc = fmaf(ld(dy, act_off(a, a.Cout, a.OH, a.OW, n, co, oh, ow)), ld(w, w_off(a, co, cl, kh, kw)), acc);
+      for (int kd = 0; kd < a.KD; ++kd) {
+        const int td = id + a.PD - kd * a.DD;
+        if (td < 0 || td % a.SD != 0) continue;
+        const int od = td / a.SD;
+        if (od >= a.OD) continue;
+        for (int kh = 0; kh < a.KH; ++kh) {
+          const int th = ih + a.PH - kh * a.DH;
+          if (th < 0 || th % a.SH != 0) continue;
+          const int oh = th / a.SH;
+          if (oh >= a.OH) continue;
+          for (int kw = 0; kw < a.KW; ++kw) {
+            const int tw = iw + a.PW - kw * a.DW;
+            if (tw < 0 || tw % a.SW != 0) continue;
+            const int ow = tw / a.SW;
+            if (ow >= a.OW) continue;
+            acc = fmaf(ld(dy, act_off(a, a.Cout, a.OD, a.OH, a.OW, n, co, od, oh, ow)),
+                       ld(w, w_off(a, co, cl, kd, kh, kw)), acc);
+          }
         }
       }
     }
     if (bias) acc += __ldg(bias + ci);
-    dx[act_off(a, a.Cin, a.H, a.W, n, ci, ih, iw)] = cvt<T>(acc);
+    dx[act_off(a, a.Cin, a.D, a.H, a.W, n, ci, id, ih, iw)] = cvt<T>(acc);
   }
 }
 
-// [C_out, C_in/G, KH, KW] -> [C_out, KH, KW, C_in/G]; one thread per destination element.
+// [C_out, C_in/G, KH, KW] -> [C_out, KH, KW, C_in/G]; one thread per destination element.  A 3-D
+// weight is the same re-layout with the kernel's depth and height taken as one axis of KD*KH.
 template <typename T>
 __global__ void pack_ohwi_kernel(int Cout, int cpg, int KH, int KW, const T* __restrict__ src, T* __restrict__ dst) {
   ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
@@ -147,6 +169,7 @@ DirectArgs make_args(const Problem& p) {
   a.H = int(p.H); a.W = int(p.W); a.KH = int(p.KH); a.KW = int(p.KW);
   a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW);
   a.DH = int(p.DH); a.DW = int(p.DW); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.D = int(p.D); a.KD = int(p.KD); a.SD = int(p.SD); a.PD = int(p.PD); a.DD = int(p.DD); a.OD = int(p.OD);
   a.nhwc = p.nhwc; a.ohwi = p.ohwi;
   return a;
 }
@@ -187,7 +210,7 @@ gbconv_status launch_direct_dgrad(const Problem& p, const void* dy, const void* 
 
 gbconv_status launch_pack_weight(const Problem& p, const void* w_oihw, void* w_ohwi, const Launch& l) {
   const int threads = 256, blocks = grid_for(p.w_elems(), threads, l.num_sms);
-  const int Cout = int(p.Cout), cpg = int(p.cpg()), KH = int(p.KH), KW = int(p.KW);
+  const int Cout = int(p.Cout), cpg = int(p.cpg()), KH = int(p.KD * p.KH), KW = int(p.KW);
   const cudaError_t e =
       p.bf16 ? launch_kernel(pack_ohwi_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, Cout, cpg, KH,
                              KW, static_cast<const __nv_bfloat16*>(w_oihw), static_cast<__nv_bfloat16*>(w_ohwi))

@@ -1,5 +1,6 @@
 // Resolved convolution geometry shared by the host dispatcher and the kernel
-// launchers.  A 1-D convolution is carried as a 2-D one with H = KH = 1.
+// launchers.  A 1-D convolution is carried as a 2-D one with H = KH = 1, and
+// 1-D and 2-D ones as 3-D ones with depth 1 (D = KD = SD = DD = OD = 1, PD = 0).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -15,17 +16,28 @@ struct Problem {
   int64_t N, Cin, Cout, G;
   int64_t H, W, KH, KW, SH, SW, PH, PW, DH, DW;
   int64_t PHe, PWe;  // end-side padding (PH, PW are the begin side); equal to PH, PW when symmetric
-  int64_t OH, OW;
+  int64_t D, KD, SD, PD, PDe, DD;  // depth axis
+  int64_t OH, OW, OD;
   bool nhwc;   // activations channels-last
   bool ohwi;   // weight [C_out, KH, KW, C_in/G]
   bool bf16;   // element type bf16 (else f32)
   int64_t cpg() const { return Cin / G; }   // input channels per group
   int64_t opg() const { return Cout / G; }  // output channels per group
-  int64_t x_elems() const { return N * Cin * H * W; }
-  int64_t y_elems() const { return N * Cout * OH * OW; }
-  int64_t w_elems() const { return Cout * cpg() * KH * KW; }
+  int64_t x_elems() const { return N * Cin * D * H * W; }
+  int64_t y_elems() const { return N * Cout * OD * OH * OW; }
+  int64_t w_elems() const { return Cout * cpg() * KD * KH * KW; }
   int elem_bytes() const { return bf16 ? 2 : 4; }
   bool sym_pad() const { return PHe == PH && PWe == PW; }
+  // The depth axis does nothing but repeat a 2-D convolution per depth slice (kernel depth 1, unit
+  // stride, no depth padding): channels-last, the 3-D tensors are then 2-D ones with N*D images.
+  bool depth_trivial() const { return KD == 1 && SD == 1 && PD == 0 && PDe == 0; }
+  Problem fold_depth() const {
+    Problem q = *this;
+    q.N = N * D;
+    q.D = q.OD = 1;
+    q.DD = 1;
+    return q;
+  }
 };
 
 // Fills `p` from `d` and checks it the way oarust's geometry resolvers do:

@@ -28,9 +28,10 @@ using bf16 = __nv_bfloat16;
 
 struct WgArgs {
   int N, Cin, Cout, H, W, KH, KW, SH, SW, PH, PW, DH, DW, OH, OW;
+  int D, KD, SD, PD, DD, OD;  // depth axis (1, 1, 1, 0, 1, 1 for 1-D and 2-D shapes)
   int cpg, opg;
   int nhwc, ohwi;
-  int E;     // weight-gradient elements, numbered in OHWI order ((co*KH + kh)*KW + kw)*cpg + cl
+  int E;     // weight-gradient elements, in O(D)HWI order (((co*KD + kd)*KH + kh)*KW + kw)*cpg + cl
   int Etot;  // E plus C_out bias-gradient elements when the bias gradient is wanted
   int e0;    // first element this launch computes (E: the bias gradient only)
   int P;     // positions N*OH*OW (the contraction length)
@@ -42,8 +43,10 @@ __device__ __forceinline__ float ld_elem(const bf16* p, int64_t i) { return __bf
 __device__ __forceinline__ void st_elem(float* p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st_elem(bf16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ int64_t act_at(const WgArgs& a, int C, int Hh, int Ww, int n, int c, int h, int w) {
-  return a.nhwc ? ((int64_t(n) * Hh + h) * Ww + w) * C + c : ((int64_t(n) * C + c) * Hh + h) * Ww + w;
+__device__ __forceinline__ int64_t act_at(const WgArgs& a, int C, int Dd, int Hh, int Ww, int n, int c, int d, int h,
+                                          int w) {
+  return a.nhwc ? (((int64_t(n) * Dd + d) * Hh + h) * Ww + w) * C + c
+                : (((int64_t(n) * C + c) * Dd + d) * Hh + h) * Ww + w;
 }
 
 // One thread per (weight-gradient element, chunk): the partial sum over the chunk's positions, in
@@ -59,27 +62,33 @@ __global__ void direct_wgrad_partial_kernel(WgArgs a, const T* __restrict__ x, c
   const int p0 = s * a.L, p1 = min(p0 + a.L, a.P);
   float acc = 0.f;
   if (p0 < p1) {
-    int ow = p0 % a.OW, q = p0 / a.OW, oh = q % a.OH, n = q / a.OH;
+    // position p = ((n*OD + od)*OH + oh)*OW + ow, walked in order
+    int ow = p0 % a.OW, q = p0 / a.OW, oh = q % a.OH;
+    q /= a.OH;
+    int od = q % a.OD, n = q / a.OD;
     if (e < a.E) {
       int t = e;
       const int cl = t % a.cpg;
       t /= a.cpg;
       const int kw = t % a.KW;
       t /= a.KW;
-      const int kh = t % a.KH, co = t / a.KH;
+      const int kh = t % a.KH;
+      t /= a.KH;
+      const int kd = t % a.KD, co = t / a.KD;
       const int ci = (co / a.opg) * a.cpg + cl;
       for (int p = p0; p < p1; ++p) {
+        const int id = od * a.SD + kd * a.DD - a.PD;
         const int ih = oh * a.SH + kh * a.DH - a.PH, iw = ow * a.SW + kw * a.DW - a.PW;
-        if (ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
-          acc = fmaf(ld_elem(dy, act_at(a, a.Cout, a.OH, a.OW, n, co, oh, ow)),
-                     ld_elem(x, act_at(a, a.Cin, a.H, a.W, n, ci, ih, iw)), acc);
-        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; ++n; } }
+        if (id >= 0 && id < a.D && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
+          acc = fmaf(ld_elem(dy, act_at(a, a.Cout, a.OD, a.OH, a.OW, n, co, od, oh, ow)),
+                     ld_elem(x, act_at(a, a.Cin, a.D, a.H, a.W, n, ci, id, ih, iw)), acc);
+        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; if (++od == a.OD) { od = 0; ++n; } } }
       }
     } else {
       const int co = e - a.E;
       for (int p = p0; p < p1; ++p) {
-        acc += ld_elem(dy, act_at(a, a.Cout, a.OH, a.OW, n, co, oh, ow));
-        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; ++n; } }
+        acc += ld_elem(dy, act_at(a, a.Cout, a.OD, a.OH, a.OW, n, co, od, oh, ow));
+        if (++ow == a.OW) { ow = 0; if (++oh == a.OH) { oh = 0; if (++od == a.OD) { od = 0; ++n; } } }
       }
     }
   }
@@ -166,12 +175,13 @@ WgArgs direct_args(const Problem& p, bool want_db) {
   a.H = int(p.H); a.W = int(p.W); a.KH = int(p.KH); a.KW = int(p.KW);
   a.SH = int(p.SH); a.SW = int(p.SW); a.PH = int(p.PH); a.PW = int(p.PW); a.DH = int(p.DH); a.DW = int(p.DW);
   a.OH = int(p.OH); a.OW = int(p.OW);
+  a.D = int(p.D); a.KD = int(p.KD); a.SD = int(p.SD); a.PD = int(p.PD); a.DD = int(p.DD); a.OD = int(p.OD);
   a.cpg = int(p.cpg()); a.opg = int(p.opg());
   a.nhwc = p.nhwc; a.ohwi = p.ohwi;
   a.E = int(p.w_elems());
   a.Etot = a.E + (want_db ? a.Cout : 0);
   a.e0 = 0;
-  a.P = int(p.N * p.OH * p.OW);
+  a.P = int(p.N * p.OD * p.OH * p.OW);
   a.S = int(std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (int64_t(a.P) + kChunkPositions - 1) / kChunkPositions)));
   a.L = (a.P + a.S - 1) / a.S;
   return a;
@@ -189,17 +199,19 @@ gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void
   const int E = int(p.w_elems()), Etot = E + (want_db ? int(p.Cout) : 0);
   // float4 reads need every chunk row to start on 16 bytes (the workspace itself is 16-byte aligned)
   const bool vec = Etot % 4 == 0;
+  // both weight layouts order (kd, kh, kw) alike, so the kernel's depth and height are one axis here
+  const int KDH = int(p.KD * p.KH);
   const dim3 grid(vec ? (Etot + 127) / 128 : (Etot + 31) / 32), block(256);
   cudaError_t e;
   if (p.bf16)
-    e = vec ? launch_kernel(wgrad_reduce_kernel<bf16, 4>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+    e = vec ? launch_kernel(wgrad_reduce_kernel<bf16, 4>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
                             int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db)
-            : launch_kernel(wgrad_reduce_kernel<bf16, 1>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+            : launch_kernel(wgrad_reduce_kernel<bf16, 1>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
                             int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db);
   else
-    e = vec ? launch_kernel(wgrad_reduce_kernel<float, 4>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+    e = vec ? launch_kernel(wgrad_reduce_kernel<float, 4>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
                             int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db)
-            : launch_kernel(wgrad_reduce_kernel<float, 1>, grid, block, 0, l.stream, E, Etot, S, int(p.KH), int(p.KW),
+            : launch_kernel(wgrad_reduce_kernel<float, 1>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
                             int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db);
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }

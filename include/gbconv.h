@@ -87,26 +87,31 @@ typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER =
 typedef enum { GBCONV_PAD_SYMMETRIC = 0, GBCONV_PAD_BEGIN_END = 1 } gbconv_pad_mode;
 
 /* One convolution.  For spatial_dims == 1 only index 0 of in/k/stride/pad/pad_end/dil is read (the
- * length axis); index 1 is ignored.  For spatial_dims == 2 index 0 is height and index 1 is width.
+ * length axis).  For spatial_dims == 2 index 0 is height and index 1 is width.  For spatial_dims == 3
+ * index 0 is depth, 1 height and 2 width (burn-cubecl `ConvOptions<N>`: one stride, padding and
+ * dilation per spatial axis, the same index map on each); the activations are then NCDHW or NDHWC
+ * and the weight [C_out, C_in/G, KD, KH, KW] (GBCONV_W_OIHW) or [C_out, KD, KH, KW, C_in/G]
+ * (GBCONV_W_OHWI).  Unread entries are ignored.
  * Padding: with pad_mode GBCONV_PAD_SYMMETRIC (0, what a zero-initialised descriptor holds) axis i has
  * pad[i] zeros on both sides and pad_end is not read; with GBCONV_PAD_BEGIN_END it has pad[i] zeros
  * before and pad_end[i] zeros after (burn-cubecl's padding is such a (begin, end) pair per axis).
  * Output extent per axis: (in + pad + pad_end - dil*(k-1) - 1) / stride + 1, floor. */
 typedef struct {
-  int32_t spatial_dims;       /* 1 or 2 */
+  int32_t spatial_dims;       /* 1, 2 or 3 */
   int32_t layout;             /* gbconv_layout of x, y, dy, dx */
   int32_t wlayout;            /* gbconv_wlayout of w */
   int32_t dtype;              /* gbconv_dtype of x, w, y, dy, dx */
   int64_t n, c_in, c_out, groups;
-  int64_t in[2], k[2], stride[2], pad[2], dil[2];
-  int64_t pad_end[2];         /* end-side padding, read when pad_mode == GBCONV_PAD_BEGIN_END */
+  int64_t in[3], k[3], stride[3], pad[3], dil[3];
+  int64_t pad_end[3];         /* end-side padding, read when pad_mode == GBCONV_PAD_BEGIN_END */
   int32_t pad_mode;           /* gbconv_pad_mode */
 } gbconv_desc;
 
 /* Output spatial extent of the forward convolution (oarust Conv1dGeometry::resolve applied per axis).
- * out[0] = OH (or L_out for 1-D), out[1] = OW (1 for 1-D).  Launches nothing.
+ * out[0] = OH (or L_out for 1-D), out[1] = OW (1 for 1-D); for 3-D out[0] = OD, out[1] = OH,
+ * out[2] = OW.  The caller's array holds 3 entries; entries past the rank are set to 1.  Launches nothing.
  * Returns GBCONV_EINVAL for a NULL argument or any shape the forward would reject. */
-gbconv_status gbconv_out_shape(const gbconv_desc *desc, int64_t out[2]);
+gbconv_status gbconv_out_shape(const gbconv_desc *desc, int64_t out[3]);
 
 /* Which kernel family would serve `op` for this descriptor (pointers assumed 16-byte aligned).
  * Launches nothing. */

@@ -28,6 +28,11 @@ def oracle_conv(wl_or_kw) -> oracle.Conv:
     g = wl_or_kw if isinstance(wl_or_kw, dict) else wl_or_kw.__dict__
     sd = g["spatial_dims"]
     pe = g.get("pad_end")
+    if sd == 3:
+        return oracle.Conv(n=g["n"], c_in=g["c_in"], c_out=g["c_out"], in_hw=tuple(g["in_size"]), k=tuple(g["k"]),
+                           stride=tuple(g["stride"]), pad=tuple(g["pad"]), dil=tuple(g["dil"]), groups=g["groups"],
+                           nhwc=g["layout"] in ("nhwc", "ndhwc"), w_ohwi=g["wlayout"] in ("ohwi", "odhwi"),
+                           spatial_dims=3, pad_end=None if pe is None else tuple(pe))
     if sd == 1:
         return oracle.Conv(n=g["n"], c_in=g["c_in"], c_out=g["c_out"], in_hw=(1, g["in_size"][0]),
                            k=(1, g["k"][0]), stride=(1, g["stride"][0]), pad=(0, g["pad"][0]),

@@ -83,7 +83,7 @@ def test_enum_fields_and_null_pointers_rejected(gb):
     assert gb.gbconv_fwd(d, 16, 16, None, 0, 0) == gb.GBCONV_EINVAL
     assert gb.gbconv_bwd_data(d, 0, 16, 16, 0) == gb.GBCONV_EINVAL
     assert gb.gbconv_pack_weight(d, 0, 16, 0) == gb.GBCONV_EINVAL
-    for field, value in (("spatial_dims", 3), ("layout", 7), ("wlayout", -1), ("dtype", 5)):
+    for field, value in (("spatial_dims", 4), ("spatial_dims", 0), ("layout", 7), ("wlayout", -1), ("dtype", 5)):
         d2 = lib_desc(gb, shape_kw())
         setattr(d2, field, value)
         assert gb.gbconv_fwd(d2, 16, 16, None, 16, 0) == gb.GBCONV_EINVAL
@@ -239,3 +239,37 @@ def test_begin_end_padding_shapes_and_families(gb):
     assert gb.gbconv_select(lib_desc(gb, shape_kw(c_in=64, c_out=64, groups=64, stride=(2, 2), pad=(0, 0),
                                                  pad_end=(1, 1))), 0) == "depthwise"
     assert gb.gbconv_select(lib_desc(gb, shape_kw(stride=(2, 2), pad=(0, 0), pad_end=(1, 1))), 1) == "dgrad"
+
+
+def s3(**kw):
+    """A 3-D shape_kw: triples for every per-axis field."""
+    d = dict(spatial_dims=3, in_size=(4, 6, 5), k=(3, 3, 3), stride=(1, 1, 1), pad=(1, 1, 1), dil=(1, 1, 1),
+             layout="ndhwc", wlayout="odhwi")
+    d.update(kw)
+    return shape_kw(**d)
+
+
+def test_conv3d_shapes_and_families(gb):
+    cases = [s3(), s3(in_size=(5, 7, 6), k=(2, 3, 1), stride=(2, 1, 3), pad=(0, 1, 0), dil=(1, 2, 1)),
+             s3(in_size=(6, 5, 5), pad=(1, 0, 1), pad_end=(0, 2, 1), stride=(2, 2, 1))]
+    for kw in cases:
+        assert gb.gbconv_out_shape(lib_desc(gb, kw)) == oracle_conv(kw).out_hw()
+        xs, ws, ys = gb.desc_shapes(lib_desc(gb, kw))
+        c = oracle_conv(kw)
+        assert (xs, ws, ys) == (c.x_shape(), c.w_shape(), c.y_shape())
+    # a real depth kernel: the generic kernels; depth 1, unit stride, no depth padding: the 2-D
+    # families on N*D images (channels-last only)
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 1) == "direct_dgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 2) == "direct_wgrad"
+    flat = dict(k=(1, 3, 3), pad=(0, 1, 1), c_in=64, c_out=64)
+    assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 0) == "implicit"
+    assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 1) == "dgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 2) == "wgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(**dict(flat, layout="ncdhw", wlayout="oidhw"))), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 1, 1), pad=(0, 0, 0), c_in=64, c_out=64)), 0) == "pointwise"
+    assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 3, 3), pad=(0, 1, 1), c_in=32, c_out=32, groups=32)), 0) == "depthwise"
+    assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 3, 3), pad=(1, 1, 1), c_in=64, c_out=64)), 0) == "direct"
+    # folded: the implicit GEMM's items count N*D images
+    _, _, f = _plan(gb, s3(n=2, in_size=(3, 9, 7), **flat))
+    assert int(f["items"]) == 2 * 3 * -(-9 * (7 + 2) // 256)

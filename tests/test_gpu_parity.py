@@ -170,6 +170,26 @@ SMALL = [
               layout="nchw", wlayout="oihw", dtype="f32", bias=True), "fwd", "direct"),
     (shape_kw(n=1, in_size=(10, 7), c_in=8, c_out=12, stride=(2, 2), pad=(1, 0), pad_end=(0, 2), layout="nchw",
               wlayout="oihw", dtype="f32"), "dgrad", "direct_dgrad"),
+    # 3-D: a depth kernel (generic kernels: fp32 NCDHW with groups, stride, dilation and begin/end
+    # padding; bf16 NDHWC), and depth-1 kernels at unit depth stride, which the 2-D families run
+    # on N*D images (implicit GEMM, 1x1 GEMM, depthwise, stride-phase dgrad)
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
+              pad=(1, 0, 1), pad_end=(0, 1, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32",
+              bias=True), "fwd", "direct"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "direct"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
+              pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "dgrad", "direct_dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(2, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "direct_dgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 9, 11), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 9), c_in=128, c_out=64, k=(1, 1, 1), stride=(1, 1, 1),
+              pad=(0, 0, 0), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "pointwise"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 10, 9), c_in=64, c_out=64, groups=64, k=(1, 3, 3), stride=(1, 2, 2),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "depthwise"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 10, 9), c_in=64, c_out=128, k=(1, 3, 3), stride=(1, 2, 2),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -408,6 +428,14 @@ WGRAD = [
     (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "wgrad"),
     (shape_kw(n=2, in_size=(9, 10), c_in=6, c_out=9, groups=3, stride=(2, 1), pad=(1, 0), pad_end=(0, 1),
               layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
+    # 3-D: a depth kernel on the generic path (fp32 NCDHW with groups, bf16 NDHWC), and a depth-1
+    # kernel on the tensor-core path over N*D images
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
+              pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "direct_wgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "direct_wgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 9, 11), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     # more block pairs than SMs: CTAs take several units in turn (the accumulators are handed over)
     (shape_kw(n=1, in_size=(6, 6), c_in=1024, c_out=1024, k=(3, 3), pad=(1, 1)), "wgrad"),
 ]
