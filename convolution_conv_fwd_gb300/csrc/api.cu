@@ -135,7 +135,9 @@ bool planar(const Problem& p, Problem* q) {
 
 int32_t select_fwd(const Problem& p, bool aligned) {
   Problem q;
-  if (!aligned || !planar(p, &q)) return GBCONV_K_DIRECT;
+  if (!aligned) return GBCONV_K_DIRECT;
+  // a 3-D forward with a real depth axis: the implicit GEMM reads its kernel-depth taps as sources
+  if (!planar(p, &q)) return implicit_fwd_supported(p) ? GBCONV_K_IMPLICIT : GBCONV_K_DIRECT;
   if (depthwise_supported(q)) return GBCONV_K_DEPTHWISE;
   if (pointwise_supported(q)) return GBCONV_K_POINTWISE;
   if (implicit_fwd_supported(q)) return GBCONV_K_IMPLICIT;

@@ -85,6 +85,8 @@ struct PhaseHdr {
   int nsrc;
   int8_t src_ah[kMaxSrc], src_aw[kMaxSrc];  // < 8 (TMA element strides are at most 8)
   int8_t src_t0[kMaxSrc + 1];                // <= kMaxTapsPerPhase
+  // 3-D forward: source k also reads input depth od*SD + src_ad[k] (its kernel-depth tap kd*DD - PD)
+  int src_ad[kMaxSrc];
 };
 
 struct Phase : PhaseHdr {
@@ -104,6 +106,7 @@ struct Args {
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
   int nphase, total_items;
+  int depth_od, depth_sd;  // 3-D forward: output depth and depth stride (items run over N*OD slices); else 0
   Phase ph[kMaxPhases];
 };
 
@@ -144,6 +147,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst),
       "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int v, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+      "%6, %7}], [%2];" ::"r"(dst),
+      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(v), "r"(w)
       : "memory");
 }
 
@@ -280,9 +292,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int src = 0; ok && src < (MSRC ? ph.nsrc : 1); ++src) {
             if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
             ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
-            tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                        kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src],
-                        it.n);
+            if (MSRC && a.depth_od > 0) {  // 3-D: item image it.n is a (batch, output depth) slice
+              const int nn = it.n / a.depth_od, od = it.n - nn * a.depth_od;
+              tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                          kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
+                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], od * a.depth_sd + ph.src_ad[src], nn);
+            } else {
+              tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                          kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
+                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], it.n);
+            }
             if (++sa == a.sa) { sa = 0; pa ^= 1; }
             if (BRES && b_pending) load_resident_b();
             if (!BRES) {
@@ -520,8 +539,8 @@ struct Plan {
   int row_step = 1, col_step = 1;  // strided view of the activations (strided 1x1 forward)
   size_t smem;
   int grid;
-  // geometry kept for the tensor maps
-  int N, Hi, Wi, Ck, Cw;
+  // geometry kept for the tensor maps (Di: input depth of a 3-D forward, else 0)
+  int N, Hi, Wi, Ck, Cw, Di;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -570,26 +589,32 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
+  // A real depth axis (3-D forward): kernel-depth taps are more activation sources (5-D TMA boxes).
+  const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
+  if (deep && dgrad) return false;
   // A strided forward reads its activations through strided views (TMA element strides <= 8).
   if (!dgrad && (p.SH > 8 || p.SW > 8)) return false;
   if (dgrad && p.SH * p.SW > kMaxPhases) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides and vector stores
-  if (p.KH * p.KW > kMaxTapsPerPhase) return false;
+  if (p.KD * p.KH * p.KW > kMaxTapsPerPhase) return false;
   pl = Plan{};
   pl.dgrad = dgrad;
   Args& a = pl.a;
   const int64_t Ck = dgrad ? p.Cout : p.Cin, Cn = dgrad ? p.Cin : p.Cout;
   pl.bn = pick_bn(Cn);
   pl.nsub = pl.bn <= 128 ? 2 : 1;
-  a.N = int(p.N);
+  a.N = int(deep ? p.N * p.OD : p.N);  // items run over (batch, output depth) slices
+  a.depth_od = deep ? int(p.OD) : 0;
+  a.depth_sd = deep ? int(p.SD) : 0;
   a.Cn = int(Cn);
   a.Ho = int(p.H);
   a.Wo = int(p.W);
   if (!dgrad) { a.Ho = int(p.OH); a.Wo = int(p.OW); }
-  a.T = int(p.KH * p.KW);
+  a.T = int(p.KD * p.KH * p.KW);
   a.kb_count = int((Ck + kKB - 1) / kKB);
   a.n_tiles = int((Cn + pl.bn - 1) / pl.bn);
   pl.N = int(p.N);
+  pl.Di = deep ? int(p.D) : 0;
   pl.Hi = int(dgrad ? p.OH : p.H);
   pl.Wi = int(dgrad ? p.OW : p.W);
   pl.Ck = int(Ck);
@@ -605,10 +630,13 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     PhaseSpec s{};
     Phase& ph = s.ph;
     int drs[kMaxTapsPerPhase], dcs[kMaxTapsPerPhase], ahs[kMaxTapsPerPhase], aws[kMaxTapsPerPhase];
+    int kds[kMaxTapsPerPhase];
     int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
+    for (int kd = 0; kd < p.KD; ++kd)
     for (int kh = 0; kh < p.KH; ++kh)
       for (int kw = 0; kw < p.KW; ++kw) {
-        const int t = int(kh * p.KW + kw);
+        const int t = int((kd * p.KH + kh) * p.KW + kw);  // the weight's [KD][KH][KW] tap
+        kds[t] = kd;
         const int rr = int(kh * p.DH - p.PH), cc = int(kw * p.DW - p.PW);
         ahs[t] = ((rr % int(p.SH)) + int(p.SH)) % int(p.SH);
         aws[t] = ((cc % int(p.SW)) + int(p.SW)) % int(p.SW);
@@ -628,14 +656,15 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     ph.col_step = int(p.SW);
     pl.row_step = int(p.SH);
     pl.col_step = int(p.SW);
-    // taps grouped by source, sources in (ah, aw) order
+    // taps grouped by source, sources in (kernel depth, ah, aw) order
     int k = 0;
     ph.nsrc = 0;
+    for (int kd = 0; kd < p.KD; ++kd)
     for (int ah = 0; ah < p.SH; ++ah)
       for (int aw = 0; aw < p.SW; ++aw) {
         const int start = k;
         for (int t = 0; t < a.T; ++t) {
-          if (ahs[t] != ah || aws[t] != aw) continue;
+          if (kds[t] != kd || ahs[t] != ah || aws[t] != aw) continue;
           ph.tap_off[k] = (drs[t] - rmin) * ph.P + (dcs[t] - cmin);
           ph.tap_w[k] = t;
           ++k;
@@ -644,6 +673,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         if (ph.nsrc == kMaxSrc) return false;
         ph.src_ah[ph.nsrc] = int8_t(ah);
         ph.src_aw[ph.nsrc] = int8_t(aw);
+        ph.src_ad[ph.nsrc] = int(kd * p.DD - p.PD);
         ph.src_t0[ph.nsrc] = int8_t(start);
         ++ph.nsrc;
       }
@@ -735,14 +765,22 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
   const Args& a = pl.a;
   for (int i = 0; i < a.nphase; ++i) {
     const Phase& ph = a.ph[i];
-    cuuint64_t dims[4] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N)};
-    cuuint64_t strides[3] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Wi) * pl.Ck * 2, cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2};
     // A strided view spans stride x the loaded extent and loads every stride-th element (the
-    // forward of a strided 1x1); otherwise row_step = col_step = 1.
-    cuuint32_t box[4] = {cuuint32_t(kKB), cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1};
-    cuuint32_t estr[4] = {1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1};
-    if (fn(&pl.maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(in), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    // forward of a strided 1x1); otherwise row_step = col_step = 1.  A 3-D forward adds the input
+    // depth as a fifth dimension, one slice per box.
+    const int rank = pl.Di > 0 ? 5 : 4;
+    const cuuint64_t plane = cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2;
+    cuuint64_t dims[5] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N), 1};
+    cuuint64_t strides[4] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Wi) * pl.Ck * 2, plane, 0};
+    if (rank == 5) {
+      dims[3] = cuuint64_t(pl.Di);
+      dims[4] = cuuint64_t(pl.N);
+      strides[3] = plane * cuuint64_t(pl.Di);
+    }
+    cuuint32_t box[5] = {cuuint32_t(kKB), cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1, 1};
+    cuuint32_t estr[5] = {1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1, 1};
+    if (fn(&pl.maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(in), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
@@ -808,7 +846,7 @@ gbconv_status dispatch_src(const Plan& pl, const Launch& l) {
 template <bool DGRAD>
 gbconv_status dispatch(const Plan& pl, const Launch& l) {
   // Only a strided forward has phases with several activation sources.
-  if (!DGRAD && pl.a.ph[0].nsrc > 1) return dispatch_src<false, true>(pl, l);
+  if (!DGRAD && (pl.a.ph[0].nsrc > 1 || pl.a.depth_od > 0)) return dispatch_src<false, true>(pl, l);
   return dispatch_src<DGRAD, false>(pl, l);
 }
 

@@ -139,6 +139,8 @@ def _load():
             getattr(lib, name).restype = ctypes.c_int
         lib.oracle_conv_fwd_points.argtypes = [P(_Desc), f32p, f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_fwd_points.restype = None
+        lib.oracle_conv_fwd_points3.argtypes = [P(_Desc), f32p, f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_fwd_points3.restype = None
         lib.oracle_conv_dgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_dgrad_points.restype = None
         lib.oracle_conv_wgrad.argtypes = [P(_Desc), f32p, f32p, f64p]
@@ -224,14 +226,16 @@ def conv_transpose(c: Conv, x, w, bias=None) -> np.ndarray:
 
 
 def conv_fwd_points(c: Conv, x, w, bias, idx) -> np.ndarray:
-    """Forward outputs at an (count, 4) array of (n, c_out, oh, ow) indices."""
+    """Forward outputs at an (count, 4) array of (n, c_out, oh, ow) indices, or for a 3-D shape an
+    (count, 5) array of (n, c_out, od, oh, ow) indices."""
     x, w = _f32(x, c.x_shape()), _f32(w, c.w_shape())
     b = None if bias is None else _f32(bias, (c.c_out,))
-    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    k = 5 if c.spatial_dims == 3 else 4
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, k)
     out = np.empty(idx.shape[0], dtype=np.float64)
-    _load().oracle_conv_fwd_points(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float),
-                                   _ptr(b, ctypes.c_float), _ptr(idx, ctypes.c_int64), idx.shape[0],
-                                   _ptr(out, ctypes.c_double))
+    fn = _load().oracle_conv_fwd_points3 if k == 5 else _load().oracle_conv_fwd_points
+    fn(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(b, ctypes.c_float),
+       _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
     return out
 
 

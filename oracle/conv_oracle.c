@@ -364,3 +364,11 @@ void oracle_conv_wgrad_points(const oracle_conv *c, const float *x, const float 
   for (int64_t i = 0; i < count; ++i)
     out[i] = oracle_conv_wgrad_at(c, x, dy, idx[4 * i], idx[4 * i + 1], idx[4 * i + 2], idx[4 * i + 3]);
 }
+
+/* 3-D point queries: out[i] = fwd at the i-th (n, c, d, h, w) quintuple of idx. */
+void oracle_conv_fwd_points3(const oracle_conv *c, const float *x, const float *w, const float *bias,
+                             const int64_t *idx, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_conv_fwd_at3(c, x, w, bias, idx[5 * i], idx[5 * i + 1], idx[5 * i + 2], idx[5 * i + 3],
+                                 idx[5 * i + 4]);
+}

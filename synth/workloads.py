@@ -22,12 +22,12 @@ class Workload:
     op: str                 # "fwd", "dgrad" or "wgrad"
     dtype: str              # "f32" or "bf16"
     spatial_dims: int
-    layout: str             # "ncl" / "nhwc"
-    wlayout: str            # "oik" / "ohwi"
+    layout: str             # "ncl" / "nhwc" / "ndhwc"
+    wlayout: str            # "oik" / "ohwi" / "odhwi"
     n: int
     c_in: int
     c_out: int
-    in_size: tuple          # (L,) or (H, W)
+    in_size: tuple          # (L,), (H, W) or (D, H, W)
     k: tuple
     stride: tuple
     pad: tuple
@@ -81,6 +81,11 @@ EXTRA_WORKLOADS = [
              (1, 1), (1, 1), 1, False, (32, 56, 56, 64), (64, 3, 3, 64), (32, 56, 56, 64),
              {"x": ("normal", 1.0), "g": ("normal", 1.0)},
              "conv2d backward-filter NHWC bf16, 3x3 stride 1 pad 1, x and dy 32x56x56x64 -> dW 64x3x3x64"),
+    # a 3-D convolution layer: 3x3x3, N=2, 16x56x56, C 64->64, pad 1, fp32 bias
+    Workload("dense3x3x3_ndhwc_bf16", 8, "fwd", "bf16", 3, "ndhwc", "odhwi", 2, 64, 64, (16, 56, 56), (3, 3, 3),
+             (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, True, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 27)) ** 0.5), "b": ("normal", 0.1)},
+             "dense 3x3x3 conv3d NDHWC bf16, N=2, 16x56x56, C 64->64, stride 1, pad 1, fp32 bias"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

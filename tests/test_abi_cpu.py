@@ -112,6 +112,7 @@ EXPECTED_FAMILY = {
     "depthwise3x3_s2_dgrad_nhwc_bf16": {"depthwise_dgrad"},
     "dense3x3_s2_nhwc_bf16": {"implicit"},
     "wgrad3x3_nhwc_bf16": {"wgrad", "direct_wgrad"},
+    "dense3x3x3_ndhwc_bf16": {"implicit"},
 }
 
 OPS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
@@ -257,9 +258,15 @@ def test_conv3d_shapes_and_families(gb):
         xs, ws, ys = gb.desc_shapes(lib_desc(gb, kw))
         c = oracle_conv(kw)
         assert (xs, ws, ys) == (c.x_shape(), c.w_shape(), c.y_shape())
-    # a real depth kernel: the generic kernels; depth 1, unit stride, no depth padding: the 2-D
+    # a real depth kernel: the forward on the implicit GEMM with one activation source per kernel-depth
+    # tap, the gradients on the generic kernels; depth 1, unit stride, no depth padding: the 2-D
     # families on N*D images (channels-last only)
-    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 0) == "direct"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 0) == "implicit"
+    _, _, f = _plan(gb, s3(n=2, in_size=(5, 6, 7), c_in=64, c_out=64, stride=(2, 1, 1)))
+    od = (5 + 2 - 3) // 2 + 1
+    assert f["sources"] == "3" and f["taps"] == "27" and int(f["items"]) == 2 * od * -(-6 * (7 + 2) // 256)
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(1, 2, 2))), 0) == "direct"  # 12 sources
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, layout="ncdhw", wlayout="oidhw")), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 2) == "direct_wgrad"
     flat = dict(k=(1, 3, 3), pad=(0, 1, 1), c_in=64, c_out=64)
@@ -269,7 +276,8 @@ def test_conv3d_shapes_and_families(gb):
     assert gb.gbconv_select(lib_desc(gb, s3(**dict(flat, layout="ncdhw", wlayout="oidhw"))), 0) == "direct"
     assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 1, 1), pad=(0, 0, 0), c_in=64, c_out=64)), 0) == "pointwise"
     assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 3, 3), pad=(0, 1, 1), c_in=32, c_out=32, groups=32)), 0) == "depthwise"
-    assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 3, 3), pad=(1, 1, 1), c_in=64, c_out=64)), 0) == "direct"
+    # depth padding with a depth-1 kernel: not a repeated 2-D convolution, one depth source at offset -1
+    assert gb.gbconv_select(lib_desc(gb, s3(k=(1, 3, 3), pad=(1, 1, 1), c_in=64, c_out=64)), 0) == "implicit"
     # folded: the implicit GEMM's items count N*D images
     _, _, f = _plan(gb, s3(n=2, in_size=(3, 9, 7), **flat))
     assert int(f["items"]) == 2 * 3 * -(-9 * (7 + 2) // 256)

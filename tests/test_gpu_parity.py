@@ -177,7 +177,20 @@ SMALL = [
               pad=(1, 0, 1), pad_end=(0, 1, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32",
               bias=True), "fwd", "direct"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
-              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "direct"),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "implicit"),
+    # 3-D forwards on the implicit GEMM (one activation source per kernel-depth tap, 5-D TMA boxes):
+    # depth stride, depth dilation with (begin, end) depth padding, several k-blocks and N tiles,
+    # kernel depth 2 with an H/W stride (two stride phases per depth tap)
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(6, 7, 8), c_in=32, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(2, 1, 1), pad_end=(0, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(3, 6, 7), c_in=128, c_out=192, k=(2, 2, 3), stride=(1, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 9, 10), c_in=64, c_out=64, k=(2, 3, 3), stride=(1, 2, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True), "fwd", "implicit"),
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
               pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "dgrad", "direct_dgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(2, 1, 1),
@@ -339,6 +352,17 @@ def test_workload_full_size(gb, wl):
         # dw is OHWI: (co, kh, kw, c_local)
         check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
         assert np.isfinite(dw).all()
+        return
+    if wl.op == "fwd" and wl.spatial_dims == 3:
+        got = run_fwd(gb, kw, inp)  # NDHWC
+        od, oh, ow = c.out_hw()
+        idx4 = _sample_indices((wl.n * od, wl.c_out, oh, ow), 5000 + wl.index, count=1500)
+        idx = np.stack([idx4[:, 0] // od, idx4[:, 1], idx4[:, 0] % od, idx4[:, 2], idx4[:, 3]], axis=1)
+        ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
+        scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
+                                       None if "b" not in inp else np.abs(inp["b"]), idx)
+        check_bf16(got[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 4], idx[:, 1]], ref, scale)
+        assert np.isfinite(got).all()
         return
     if wl.op == "fwd":
         got = run_fwd(gb, kw, inp)
