@@ -322,8 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Kernel parameters the loop uses, in registers: parameters live in memory, and every MMA's
+      // asm statement clobbers memory, so a field read inside the loop is reloaded after each MMA.
+      unsigned int* const status = a.status;
+      const int n_sa = a.sa, n_sb = a.sb, a_stage = a.a_stage_bytes, T = a.T;
       bool ok = true;
-      if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, a.status, 2u);
+      if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, status, 2u);
       int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
       for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
         const PhaseHdr& ph = phase_s[it.phase];
         const int buf = iter & 1;
-        if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, a.status, 2u))) break;
+        if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, status, 2u))) break;
         ptx::tc_fence_after();
         const uint32_t acc = tmem + uint32_t(buf * NSUB * BN);
         if (ph.ntaps > 0) {
@@ -352,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int src = 0; ok && src < nsrc; ++src) {
               // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
               // orders the async-proxy writes before the async-proxy MMA reads.
-              if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, a.status, 2u))) break;
-              const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes);
+              if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, status, 2u))) break;
+              const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a_stage);
               // this source's taps, in the producer's rotated order
               const int t0 = src == 0 ? 0 : ph.src_t0[src];
               const int nt = src == 0 ? nt0 : ph.src_t0[src + 1] - t0;
@@ -365,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int off_n = toff[t0 + tn], w_n = tw[t0 + tn];
                 uint32_t b_addr;
                 if (BRES) {
-                  b_addr = ptx::smem_addr(b_base + size_t(kb * a.T + w_c) * kBTile);
+                  b_addr = ptx::smem_addr(b_base + size_t(kb * T + w_c) * kBTile);
                 } else {
-                  if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, a.status, 2u))) break;
+                  if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, status, 2u))) break;
                   b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
                 }
                 // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
@@ -387,21 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!BRES) {
                   ptx::mma_commit(emptyB + sb);
-                  if (++sb == a.sb) { sb = 0; pb ^= 1; }
+                  if (++sb == n_sb) { sb = 0; pb ^= 1; }
                 }
                 tc = tn;
                 off_c = off_n;
                 w_c = w_n;
               }
               ptx::mma_commit(emptyA + sa);
-              if (++sa == a.sa) { sa = 0; pa ^= 1; }
+              if (++sa == n_sa) { sa = 0; pa ^= 1; }
             }
           }
         }
         ptx::mma_commit(tfull + buf);
       }
       ptx::mma_commit(fin);
-      ptx::mbar_wait(fin, 0, abort_flag, a.status, 2u);
+      ptx::mbar_wait(fin, 0, abort_flag, status, 2u);
     }
     __syncwarp();
   } else {
