@@ -146,7 +146,9 @@ int32_t select_fwd(const Problem& p, bool aligned) {
 
 int32_t select_dgrad(const Problem& p, bool aligned) {
   Problem q;
-  if (!aligned || !planar(p, &q)) return GBCONV_K_DIRECT_DGRAD;
+  if (!aligned) return GBCONV_K_DIRECT_DGRAD;
+  // a 3-D gradient with a real depth axis at unit depth stride: the kernel-depth taps are dy sources
+  if (!planar(p, &q)) return implicit_dgrad_supported(p) ? GBCONV_K_DGRAD : GBCONV_K_DIRECT_DGRAD;
   if (implicit_dgrad_supported(q)) return GBCONV_K_DGRAD;
   if (depthwise_dgrad_supported(q)) return GBCONV_K_DEPTHWISE_DGRAD;
   return GBCONV_K_DIRECT_DGRAD;

@@ -11,6 +11,11 @@
 //    Each dx element is produced by exactly one accumulator and written once;
 //    there are no atomics and the result is deterministic.
 //
+// A 3-D shape adds a depth axis to both: every kernel-depth tap is one more
+// activation source (a 5-D box at a fixed depth offset from the item's
+// output slice, zero filled outside), and work items run over (batch, depth)
+// output slices.
+//
 // No im2col matrix is materialised (burn-cubecl `im2col.rs` notes that the
 // column matrix holds every pixel once per tap that reads it, nine times for
 // a 3x3).  Positions are laid out on a per-image "virtual grid": R rows of P
@@ -85,7 +90,8 @@ struct PhaseHdr {
   int nsrc;
   int8_t src_ah[kMaxSrc], src_aw[kMaxSrc];  // < 8 (TMA element strides are at most 8)
   int8_t src_t0[kMaxSrc + 1];                // <= kMaxTapsPerPhase
-  // 3-D forward: source k also reads input depth od*SD + src_ad[k] (its kernel-depth tap kd*DD - PD)
+  // 3-D: source k also reads activation depth od*depth_sd + src_ad[k], od the item's output slice:
+  // kd*DD - PD for the forward, PD - kd*DD for the gradient (dy slice id + PD - kd*DD)
   int src_ad[kMaxSrc];
 };
 
@@ -106,7 +112,7 @@ struct Args {
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
   int nphase, total_items;
-  int depth_od, depth_sd;  // 3-D forward: output depth and depth stride (items run over N*OD slices); else 0
+  int depth_od, depth_sd;  // 3-D: output depth and depth stride (items run over N*depth slices); else 0
   Phase ph[kMaxPhases];
 };
 
@@ -543,7 +549,7 @@ struct Plan {
   int row_step = 1, col_step = 1;  // strided view of the activations (strided 1x1 forward)
   size_t smem;
   int grid;
-  // geometry kept for the tensor maps (Di: input depth of a 3-D forward, else 0)
+  // geometry kept for the tensor maps (Di: depth of the activation read, x or dy, when 3-D; else 0)
   int N, Hi, Wi, Ck, Cw, Di;
 };
 
@@ -593,9 +599,11 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
-  // A real depth axis (3-D forward): kernel-depth taps are more activation sources (5-D TMA boxes).
+  // A real depth axis: kernel-depth taps are more activation sources (5-D TMA boxes).  The gradient
+  // takes them only at unit depth stride, where every dx slice meets every kernel-depth tap (a
+  // depth stride would split dx into depth phases with different tap sets).
   const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
-  if (deep && dgrad) return false;
+  if (deep && dgrad && (p.SD != 1 || p.KD > kMaxSrc)) return false;
   // A strided forward reads its activations through strided views (TMA element strides <= 8).
   if (!dgrad && (p.SH > 8 || p.SW > 8)) return false;
   if (dgrad && p.SH * p.SW > kMaxPhases) return false;
@@ -607,9 +615,11 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   const int64_t Ck = dgrad ? p.Cout : p.Cin, Cn = dgrad ? p.Cin : p.Cout;
   pl.bn = pick_bn(Cn);
   pl.nsub = pl.bn <= 128 ? 2 : 1;
-  a.N = int(deep ? p.N * p.OD : p.N);  // items run over (batch, output depth) slices
-  a.depth_od = deep ? int(p.OD) : 0;
-  a.depth_sd = deep ? int(p.SD) : 0;
+  // 3-D: items run over (batch, depth) slices of the output (y, or dx for the gradient)
+  const int64_t out_depth = dgrad ? p.D : p.OD;
+  a.N = int(deep ? p.N * out_depth : p.N);
+  a.depth_od = deep ? int(out_depth) : 0;
+  a.depth_sd = deep ? (dgrad ? 1 : int(p.SD)) : 0;
   a.Cn = int(Cn);
   a.Ho = int(p.H);
   a.Wo = int(p.W);
@@ -618,7 +628,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.kb_count = int((Ck + kKB - 1) / kKB);
   a.n_tiles = int((Cn + pl.bn - 1) / pl.bn);
   pl.N = int(p.N);
-  pl.Di = deep ? int(p.D) : 0;
+  pl.Di = deep ? int(dgrad ? p.OD : p.D) : 0;  // depth of the activation the boxes read (x, or dy)
   pl.Hi = int(dgrad ? p.OH : p.H);
   pl.Wi = int(dgrad ? p.OW : p.W);
   pl.Ck = int(Ck);
@@ -705,22 +715,27 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
         for (int i = 0; i < nkh; ++i) { rmin = i ? std::min(rmin, drs[i]) : drs[i]; rmax = i ? std::max(rmax, drs[i]) : drs[i]; }
         for (int i = 0; i < nkw; ++i) { cmin = i ? std::min(cmin, dcs[i]) : dcs[i]; cmax = i ? std::max(cmax, dcs[i]) : dcs[i]; }
-        ph.ntaps = nkh * nkw;
+        ph.ntaps = int(nkh * nkw * p.KD);
         ph.P = ph.OWv + (cmax - cmin);
         ph.rmin = rmin; ph.cmin = cmin;
         ph.out_sh = int(p.SH); ph.out_sw = int(p.SW); ph.out_ph = ah; ph.out_pw = aw;
-        for (int i = 0; i < nkh; ++i)
-          for (int j = 0; j < nkw; ++j) {
-            const int t = i * nkw + j;
-            ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
-            ph.tap_w[t] = int(khs[i] * p.KW + kws[j]);
-          }
+        // dy is read as it is, one source per kernel-depth tap kd: dx slice id meets dy slice
+        // id + PD - kd*DD (unit depth stride), zero filled outside dy.  2-D: one source.
+        ph.row_step = ph.col_step = 1;
+        ph.nsrc = int(p.KD);
+        for (int kd = 0; kd < p.KD; ++kd) {
+          ph.src_ah[kd] = ph.src_aw[kd] = 0;
+          ph.src_ad[kd] = int(p.PD - kd * p.DD);
+          ph.src_t0[kd] = int8_t(kd * nkh * nkw);
+          for (int i = 0; i < nkh; ++i)
+            for (int j = 0; j < nkw; ++j) {
+              const int t = (kd * nkh + i) * nkw + j;
+              ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
+              ph.tap_w[t] = int((kd * p.KH + khs[i]) * p.KW + kws[j]);
+            }
+        }
+        ph.src_t0[p.KD] = int8_t(ph.ntaps);
         s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
-        ph.row_step = ph.col_step = 1;  // dy is read as it is: one source
-        ph.nsrc = 1;
-        ph.src_ah[0] = ph.src_aw[0] = 0;
-        ph.src_t0[0] = 0;
-        ph.src_t0[1] = int8_t(ph.ntaps);
         specs[nph++] = s;
       }
     // Longest phases first, so the persistent CTAs finish together.
@@ -770,8 +785,8 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
   for (int i = 0; i < a.nphase; ++i) {
     const Phase& ph = a.ph[i];
     // A strided view spans stride x the loaded extent and loads every stride-th element (the
-    // forward of a strided 1x1); otherwise row_step = col_step = 1.  A 3-D forward adds the input
-    // depth as a fifth dimension, one slice per box.
+    // forward of a strided 1x1); otherwise row_step = col_step = 1.  A 3-D problem adds the
+    // activation's depth as a fifth dimension, one slice per box.
     const int rank = pl.Di > 0 ? 5 : 4;
     const cuuint64_t plane = cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2;
     cuuint64_t dims[5] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N), 1};
@@ -849,8 +864,8 @@ gbconv_status dispatch_src(const Plan& pl, const Launch& l) {
 
 template <bool DGRAD>
 gbconv_status dispatch(const Plan& pl, const Launch& l) {
-  // Only a strided forward has phases with several activation sources.
-  if (!DGRAD && (pl.a.ph[0].nsrc > 1 || pl.a.depth_od > 0)) return dispatch_src<false, true>(pl, l);
+  // Several activation sources: a strided forward's stride phases, or a 3-D kernel's depth taps.
+  if (pl.a.depth_od > 0 || pl.a.ph[0].nsrc > 1) return dispatch_src<DGRAD, true>(pl, l);
   return dispatch_src<DGRAD, false>(pl, l);
 }
 

@@ -120,29 +120,41 @@ __device__ __forceinline__ void store_grad(int e, float v, int E, int KH, int KW
 
 // Adds the S chunk partials of every element in a fixed order, rounds once, and writes dw in the
 // caller's weight layout and db.  A block takes 32*V consecutive elements (V per lane, read as one
-// vector when V = 4); warp j sums chunks [j*S/8, (j+1)*S/8) in chunk order, then the eight slice
-// sums are added in slice order.  Every sum is compensated (Kahan): the order fixes the bits, and
-// the compensation keeps the fp32 sum of up to a few hundred partials close to the exact one.
+// vector when V = 4); warp j sums chunks [j*S/16, (j+1)*S/16) in chunk order, then one thread per
+// element adds the sixteen run sums in run order.  Every sum is compensated (Kahan): the order fixes
+// the bits, and the compensation keeps the fp32 sum of up to a few hundred partials close to the
+// exact one.  The partials were just written and are read once: each warp issues up to six chunk
+// loads before it adds any of them, so the reads overlap instead of waiting one round trip each.
+constexpr int kReduceRuns = 16;
+constexpr int kReduceBatch = 6;
+
 template <typename T, int V>
-__global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW, int cpg, int ohwi,
-                                                           const float* __restrict__ ws, T* __restrict__ dw,
-                                                           float* __restrict__ db) {
+__global__ void __launch_bounds__(kReduceRuns * 32, 2) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW,
+                                                                        int cpg, int ohwi,
+                                                                        const float* __restrict__ ws,
+                                                                        T* __restrict__ dw, float* __restrict__ db) {
   ptx::grid_dep_wait();
-  __shared__ float part[8][32 * V];
+  __shared__ float part[kReduceRuns][32 * V];
   const int lane = int(threadIdx.x) & 31, j = int(threadIdx.x) >> 5;
   const int e0 = (int(blockIdx.x) * 32 + lane) * V;
   float acc[V], comp[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = comp[v] = 0.f;
-  const int s0 = (j * S) / 8, s1 = ((j + 1) * S) / 8;
+  const int s0 = (j * S) / kReduceRuns, s1 = ((j + 1) * S) / kReduceRuns;
   if (V == 4 && e0 + 3 < Etot) {
-#pragma unroll 4
-    for (int s = s0; s < s1; ++s) {
-      const float4 x = *reinterpret_cast<const float4*>(ws + int64_t(s) * Etot + e0);
-      kahan_add(acc[0], comp[0], x.x);
-      kahan_add(acc[1], comp[1], x.y);
-      kahan_add(acc[2], comp[2], x.z);
-      kahan_add(acc[3], comp[3], x.w);
+    for (int s = s0; s < s1; s += kReduceBatch) {
+      float4 x[kReduceBatch];
+#pragma unroll
+      for (int u = 0; u < kReduceBatch; ++u)
+        if (s + u < s1) x[u] = __ldcs(reinterpret_cast<const float4*>(ws + int64_t(s + u) * Etot + e0));
+#pragma unroll
+      for (int u = 0; u < kReduceBatch; ++u)
+        if (s + u < s1) {
+          kahan_add(acc[0], comp[0], x[u].x);
+          kahan_add(acc[1], comp[1], x[u].y);
+          kahan_add(acc[2], comp[2], x[u].z);
+          kahan_add(acc[3], comp[3], x[u].w);
+        }
     }
   } else {
     for (int s = s0; s < s1; ++s)
@@ -153,17 +165,15 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(int E, int Etot, int 
 #pragma unroll
   for (int v = 0; v < V; ++v) part[j][lane * V + v] = acc[v] - comp[v];
   __syncthreads();
-  // the first warp finishes the block's 32*V elements, V per lane
-  if (j != 0) return;
+  // one thread per element of the block adds the run sums
+  const int t = int(threadIdx.x);
+  if (t >= 32 * V) return;
+  const int e = int(blockIdx.x) * 32 * V + t;
+  if (e >= Etot) return;
+  float a2 = 0.f, c2 = 0.f;
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
-    const int e = e0 + v;
-    if (e >= Etot) continue;
-    float a2 = 0.f, c2 = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) kahan_add(a2, c2, part[jj][lane * V + v]);
-    store_grad(e, a2, E, KH, KW, cpg, ohwi, dw, db);
-  }
+  for (int jj = 0; jj < kReduceRuns; ++jj) kahan_add(a2, c2, part[jj][t]);
+  store_grad(e, a2, E, KH, KW, cpg, ohwi, dw, db);
 }
 
 constexpr int kChunkPositions = 256;  // target positions per chunk
@@ -201,7 +211,7 @@ gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void
   const bool vec = Etot % 4 == 0;
   // both weight layouts order (kd, kh, kw) alike, so the kernel's depth and height are one axis here
   const int KDH = int(p.KD * p.KH);
-  const dim3 grid(vec ? (Etot + 127) / 128 : (Etot + 31) / 32), block(256);
+  const dim3 grid(vec ? (Etot + 127) / 128 : (Etot + 31) / 32), block(kReduceRuns * 32);
   cudaError_t e;
   if (p.bf16)
     e = vec ? launch_kernel(wgrad_reduce_kernel<bf16, 4>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),

@@ -75,7 +75,7 @@ typedef enum {
   GBCONV_K_DEPTHWISE = 1,     /* NHWC bf16 depthwise direct kernel, bandwidth bound */
   GBCONV_K_POINTWISE = 2,     /* NHWC bf16 1x1: TMA-fed tcgen05 GEMM */
   GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
-  GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 */
+  GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 (3-D: unit depth stride) */
   GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
   GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
   GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
@@ -169,7 +169,7 @@ gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc *desc, int64_t *byte
  *   workspace : device scratch of at least gbconv_bwd_filter_workspace(desc) bytes, 16-byte aligned, owned
  *               by the caller; its contents are undefined afterwards.  NULL is allowed when 0 bytes are needed.
  * The sum over batch and positions is cut into fixed chunks; each chunk's partial sums are taken in a
- * fixed order and the chunk sums are added in a fixed order (eight runs of consecutive chunks, each in
+ * fixed order and the chunk sums are added in a fixed order (sixteen runs of consecutive chunks, each in
  * chunk order, then the runs in order), so the same inputs give bitwise-equal dw and db.
  * Enqueues two kernels on `stream` (partial sums, ordered reduction), three when the tensor-core path also
  * computes db.  Returns GBCONV_EINVAL for NULL tensors or a workspace smaller than required. */

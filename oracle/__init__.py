@@ -141,6 +141,8 @@ def _load():
         lib.oracle_conv_fwd_points.restype = None
         lib.oracle_conv_fwd_points3.argtypes = [P(_Desc), f32p, f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_fwd_points3.restype = None
+        lib.oracle_conv_dgrad_points3.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_dgrad_points3.restype = None
         lib.oracle_conv_dgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_dgrad_points.restype = None
         lib.oracle_conv_wgrad.argtypes = [P(_Desc), f32p, f32p, f64p]
@@ -240,12 +242,15 @@ def conv_fwd_points(c: Conv, x, w, bias, idx) -> np.ndarray:
 
 
 def conv_dgrad_points(c: Conv, dy, w, idx) -> np.ndarray:
-    """Input-gradient elements at an (count, 4) array of (n, c_in, ih, iw) indices."""
+    """Input-gradient elements at an (count, 4) array of (n, c_in, ih, iw) indices, or for a 3-D
+    shape an (count, 5) array of (n, c_in, id, ih, iw) indices."""
     dy, w = _f32(dy, c.y_shape()), _f32(w, c.w_shape())
-    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    k = 5 if c.spatial_dims == 3 else 4
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, k)
     out = np.empty(idx.shape[0], dtype=np.float64)
-    _load().oracle_conv_dgrad_points(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(w, ctypes.c_float),
-                                     _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
+    fn = _load().oracle_conv_dgrad_points3 if k == 5 else _load().oracle_conv_dgrad_points
+    fn(ctypes.byref(c._c()), _ptr(dy, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(idx, ctypes.c_int64),
+       idx.shape[0], _ptr(out, ctypes.c_double))
     return out
 
 

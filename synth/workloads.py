@@ -86,6 +86,11 @@ EXTRA_WORKLOADS = [
              (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, True, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (),
              {"x": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 27)) ** 0.5), "b": ("normal", 0.1)},
              "dense 3x3x3 conv3d NDHWC bf16, N=2, 16x56x56, C 64->64, stride 1, pad 1, fp32 bias"),
+    # the input gradient of that layer: dx 2x16x56x56x64 from dy of the same shape
+    Workload("dgrad3x3x3_ndhwc_bf16", 9, "dgrad", "bf16", 3, "ndhwc", "odhwi", 2, 64, 64, (16, 56, 56), (3, 3, 3),
+             (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, False, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (2, 16, 56, 56, 64),
+             {"g": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 27)) ** 0.5)},
+             "conv3d backward-data NDHWC bf16, 3x3x3 stride 1 pad 1, dx and dy 2x16x56x56x64"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

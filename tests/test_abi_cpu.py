@@ -113,6 +113,7 @@ EXPECTED_FAMILY = {
     "dense3x3_s2_nhwc_bf16": {"implicit"},
     "wgrad3x3_nhwc_bf16": {"wgrad", "direct_wgrad"},
     "dense3x3x3_ndhwc_bf16": {"implicit"},
+    "dgrad3x3x3_ndhwc_bf16": {"dgrad"},
 }
 
 OPS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
@@ -258,16 +259,24 @@ def test_conv3d_shapes_and_families(gb):
         xs, ws, ys = gb.desc_shapes(lib_desc(gb, kw))
         c = oracle_conv(kw)
         assert (xs, ws, ys) == (c.x_shape(), c.w_shape(), c.y_shape())
-    # a real depth kernel: the forward on the implicit GEMM with one activation source per kernel-depth
-    # tap, the gradients on the generic kernels; depth 1, unit stride, no depth padding: the 2-D
-    # families on N*D images (channels-last only)
+    # a real depth kernel: the forward and (at unit depth stride) the input gradient on the implicit
+    # GEMM with one activation source per kernel-depth tap, the weight gradient on the generic
+    # kernel; depth 1, unit stride, no depth padding: the 2-D families on N*D images (channels-last only)
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 0) == "implicit"
     _, _, f = _plan(gb, s3(n=2, in_size=(5, 6, 7), c_in=64, c_out=64, stride=(2, 1, 1)))
     od = (5 + 2 - 3) // 2 + 1
     assert f["sources"] == "3" and f["taps"] == "27" and int(f["items"]) == 2 * od * -(-6 * (7 + 2) // 256)
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(1, 2, 2))), 0) == "direct"  # 12 sources
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, layout="ncdhw", wlayout="oidhw")), 0) == "direct"
-    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 1) == "direct_dgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 1) == "dgrad"
+    # the gradient: items over N*D dx slices, one dy source per kernel-depth tap, each with its phase's taps
+    _, _, f = _plan(gb, s3(n=2, in_size=(5, 6, 7), c_in=64, c_out=64), op=1)
+    assert f["phases"] == "1" and f["sources"] == "3" and f["taps"] == "27"
+    assert int(f["items"]) == 2 * 5 * -(-6 * (7 + 2) // 256)
+    _, _, f = _plan(gb, s3(n=1, in_size=(4, 8, 8), c_in=64, c_out=64, stride=(1, 2, 2)), op=1)
+    assert f["phases"] == "4" and f["sources"] == "3" and f["taps"] == "12"
+    # a depth stride splits dx into depth phases: the generic gradient
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 2) == "direct_wgrad"
     flat = dict(k=(1, 3, 3), pad=(0, 1, 1), c_in=64, c_out=64)
     assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 0) == "implicit"

@@ -203,6 +203,20 @@ SMALL = [
               pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "depthwise"),
     (shape_kw(spatial_dims=3, n=2, in_size=(3, 10, 9), c_in=64, c_out=128, k=(1, 3, 3), stride=(1, 2, 2),
               pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    # 3-D input gradients on the implicit GEMM (unit depth stride: one dy source per kernel-depth tap,
+    # items over N*D dx slices): 3x3x3; H/W stride 2 (four stride phases per depth tap) with depth
+    # dilation and (begin, end) depth padding; several k-blocks and a 128-wide N tile; a 192-wide N
+    # tile; a depth-1 kernel with depth padding (one source at a depth offset)
+    (shape_kw(spatial_dims=3, n=2, in_size=(4, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(6, 10, 9), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 2, 2),
+              pad=(2, 1, 1), pad_end=(0, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(3, 6, 7), c_in=128, c_out=192, k=(2, 2, 3), stride=(1, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(3, 8, 6), c_in=192, c_out=64, k=(2, 3, 3), stride=(1, 2, 2),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -249,6 +263,8 @@ TRANSPOSE = [
     (shape_kw(n=2, in_size=(7, 9), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
               stride=(2, 2)), "direct_dgrad"),
     (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "direct_dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 8, 7), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 2, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
 ]
 
 
@@ -353,14 +369,24 @@ def test_workload_full_size(gb, wl):
         check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
         assert np.isfinite(dw).all()
         return
-    if wl.op == "fwd" and wl.spatial_dims == 3:
-        got = run_fwd(gb, kw, inp)  # NDHWC
-        od, oh, ow = c.out_hw()
-        idx4 = _sample_indices((wl.n * od, wl.c_out, oh, ow), 5000 + wl.index, count=1500)
-        idx = np.stack([idx4[:, 0] // od, idx4[:, 1], idx4[:, 0] % od, idx4[:, 2], idx4[:, 3]], axis=1)
-        ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
-        scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
-                                       None if "b" not in inp else np.abs(inp["b"]), idx)
+    if wl.spatial_dims == 3:
+        # NDHWC; (n*depth, c, h, w) samples cover every depth slice's corners and edges
+        if wl.op == "fwd":
+            got = run_fwd(gb, kw, inp)
+            dd, hh, ww = c.out_hw()
+            ch = wl.c_out
+        else:
+            got = run_dgrad(gb, kw, inp)
+            (dd, hh, ww), ch = wl.in_size, wl.c_in
+        idx4 = _sample_indices((wl.n * dd, ch, hh, ww), 5000 + wl.index, count=1500)
+        idx = np.stack([idx4[:, 0] // dd, idx4[:, 1], idx4[:, 0] % dd, idx4[:, 2], idx4[:, 3]], axis=1)
+        if wl.op == "fwd":
+            ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
+            scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
+                                           None if "b" not in inp else np.abs(inp["b"]), idx)
+        else:
+            ref = oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
+            scale = oracle.conv_dgrad_points(c, np.abs(inp["g"]), np.abs(inp["w"]), idx)
         check_bf16(got[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 4], idx[:, 1]], ref, scale)
         assert np.isfinite(got).all()
         return

@@ -463,6 +463,13 @@ def test_conv3d_matches_torch_float64(ci):
                                rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(_w_to_oidhw(oracle.conv_wgrad(c, x, dy), c), gw.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(oracle.conv_bgrad(c, dy), gb_.numpy(), rtol=1e-12, atol=1e-12)
+    # the point queries the full-size checks use, at every third (n, c, d, h, w) element
+    yi = np.argwhere(np.ones(yt.shape, dtype=bool))[::3]
+    np.testing.assert_allclose(oracle.conv_fwd_points(c, x, w, b, yi), yt.detach().numpy()[tuple(yi.T)],
+                               rtol=1e-12, atol=1e-12)
+    xi = np.argwhere(np.ones(gx.shape, dtype=bool))[::3]
+    np.testing.assert_allclose(oracle.conv_dgrad_points(c, dy, w, xi), gx.numpy()[tuple(xi.T)], rtol=1e-12,
+                               atol=1e-12)
 
 
 def test_conv3d_with_unit_depth_is_conv2d():
