@@ -227,38 +227,121 @@ def _dtype(d: Desc):
     return torch.bfloat16 if d.dtype == GBCONV_BF16 else torch.float32
 
 
+def _check_host(t, shape, dtype, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if t.dtype != dtype or t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous host %s tensor" % (name, dtype))
+    return t
+
+
+# Large host calls are moved through the device in batch slices on three streams: the copy in of
+# slice i+1, the kernels of slice i and the copy out of slice i-1 run at the same time (the two copy
+# directions on their own engines).  Images are independent in every operation sliced here, so a
+# slice is the same call with a smaller batch.  Each slice costs tens of microseconds of host work
+# (descriptor, plan, tensor maps, stream events), so only calls that move at least _PIPE_MIN_BYTES
+# are sliced, into _PIPE_SLICES slices; smaller ones run as one copy in, one call, one copy out.
+_PIPE_SLICES = 4
+_PIPE_MIN_BYTES = 64 << 20
+_copy_streams = {}
+
+
+def _streams(dev):
+    torch = _torch()
+    if dev.index not in _copy_streams:
+        _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    return _copy_streams[dev.index]
+
+
+def _with_batch(d: Desc, n: int) -> Desc:
+    sub = Desc.from_buffer_copy(d)
+    sub.n = n
+    return sub
+
+
+def _host_call(d: Desc, entry, what, src, w, bias, src_shape, out_shape, out=None):
+    """One call on host tensors.  ``entry(desc, src, w, bias, out, stream)`` is the C entry point;
+    src is sliced along the batch (its first axis), w and bias are copied whole.  Pinned host memory
+    lets the copies run asynchronously and overlap; pageable memory still works, without overlap."""
+    torch = _torch()
+    dt = _dtype(d)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    main = torch.cuda.current_stream(dev)
+    res = out if out is not None else torch.empty(out_shape, dtype=dt, pin_memory=True)
+    _check_host(res, out_shape, dt, "result")
+    nbytes = src.numel() * src.element_size() + res.numel() * res.element_size()
+    slices = min(int(d.n), _PIPE_SLICES) if nbytes >= _PIPE_MIN_BYTES else 1
+    if slices <= 1:
+        src_d = src.to(dev, non_blocking=True)
+        w_d = w.to(dev, non_blocking=True)
+        b_d = None if bias is None else bias.to(dev, non_blocking=True)
+        out_d = torch.empty(out_shape, dtype=dt, device=dev)
+        st = entry(d, src_d.data_ptr(), w_d.data_ptr(), None if b_d is None else b_d.data_ptr(), out_d.data_ptr(),
+                   main.cuda_stream)
+        if st != GBCONV_OK:
+            main.synchronize()
+            raise GbconvError(st, what)
+        res.copy_(out_d, non_blocking=True)
+        main.synchronize()
+        return res
+    bounds = [int(d.n) * i // slices for i in range(slices + 1)]
+    s_in, s_out = _streams(dev)
+    src_d = torch.empty(src_shape, dtype=dt, device=dev)
+    out_d = torch.empty(out_shape, dtype=dt, device=dev)
+    # the device buffers come from the current stream's pool: the side streams start after it
+    s_in.wait_stream(main)
+    s_out.wait_stream(main)
+    with torch.cuda.stream(s_in):
+        w_d = w.to(dev, non_blocking=True)
+        b_d = None if bias is None else bias.to(dev, non_blocking=True)
+    for i in range(slices):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi == lo:
+            continue
+        with torch.cuda.stream(s_in):
+            src_d[lo:hi].copy_(src[lo:hi], non_blocking=True)
+        main.wait_stream(s_in)
+        st = entry(_with_batch(d, hi - lo), src_d[lo:hi].data_ptr(), w_d.data_ptr(),
+                   None if b_d is None else b_d.data_ptr(), out_d[lo:hi].data_ptr(), main.cuda_stream)
+        if st != GBCONV_OK:
+            main.synchronize()
+            raise GbconvError(st, what)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_out):
+            res[lo:hi].copy_(out_d[lo:hi], non_blocking=True)
+    main.wait_stream(s_out)
+    main.synchronize()
+    return res
+
+
 def conv_fwd(d: Desc, x, w, bias=None, y=None):
     """y = conv(x, w) (+ bias) on the current CUDA stream.
 
     x, w (and y if given) are contiguous CUDA tensors in the descriptor's
     layouts and dtype; bias is a float32 CUDA tensor [C_out] or None.  Host
     (CPU) tensors are copied to the current device first and the result is
-    copied back, so the same call serves device-resident and host data.
+    copied back, so the same call serves device-resident and host data (in batch slices whose
+    copies overlap the kernels; the result is then a pinned host tensor, or ``y`` if given).
     """
     torch = _torch()
-    host = not x.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        x = x.to(dev, non_blocking=True)
-        w = w.to(dev, non_blocking=True)
-        bias = None if bias is None else bias.to(dev, non_blocking=True)
     xs, ws, ys = desc_shapes(d)
     dt = _dtype(d)
+    if not x.is_cuda:
+        _check_host(x, xs, dt, "x")
+        _check_host(w, ws, dt, "w")
+        if bias is not None:
+            _check_host(bias, (d.c_out,), torch.float32, "bias")
+        return _host_call(d, gbconv_fwd, "gbconv_fwd", x, w, bias, xs, ys, y)
     _check(x, xs, dt, "x")
     _check(w, ws, dt, "w")
     if bias is not None:
         _check(bias, (d.c_out,), torch.float32, "bias")
-    out = y if (y is not None and not host) else torch.empty(ys, dtype=dt, device=x.device)
+    out = y if y is not None else torch.empty(ys, dtype=dt, device=x.device)
     _check(out, ys, dt, "y")
     s = gbconv_fwd(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
                    torch.cuda.current_stream().cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_fwd")
-    if host:
-        res = torch.empty(ys, dtype=dt, pin_memory=True) if y is None else y
-        res.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return res
     return out
 
 
@@ -270,25 +353,20 @@ def conv_bwd_data(d: Desc, dy, w, dx=None):
     staged through the device as in ``conv_fwd``.
     """
     torch = _torch()
-    host = not dy.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        dy = dy.to(dev, non_blocking=True)
-        w = w.to(dev, non_blocking=True)
     xs, ws, ys = desc_shapes(d)
     dt = _dtype(d)
+    if not dy.is_cuda:
+        _check_host(dy, ys, dt, "dy")
+        _check_host(w, ws, dt, "w")
+        return _host_call(d, lambda dd, a, b, _bias, o, st: gbconv_bwd_data(dd, a, b, o, st), "gbconv_bwd_data",
+                          dy, w, None, ys, xs, dx)
     _check(dy, ys, dt, "dy")
     _check(w, ws, dt, "w")
-    out = dx if (dx is not None and not host) else torch.empty(xs, dtype=dt, device=dy.device)
+    out = dx if dx is not None else torch.empty(xs, dtype=dt, device=dy.device)
     _check(out, xs, dt, "dx")
     s = gbconv_bwd_data(d, dy.data_ptr(), w.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_bwd_data")
-    if host:
-        res = torch.empty(xs, dtype=dt, pin_memory=True) if dx is None else dx
-        res.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return res
     return out
 
 
@@ -333,29 +411,24 @@ def conv_transpose(d: Desc, x, w, bias=None, y=None):
     through the device as in ``conv_fwd``.
     """
     torch = _torch()
-    host = not x.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        x = x.to(dev, non_blocking=True)
-        w = w.to(dev, non_blocking=True)
-        bias = None if bias is None else bias.to(dev, non_blocking=True)
     xs, ws, ys = desc_shapes(d)
     dt = _dtype(d)
+    if not x.is_cuda:
+        _check_host(x, ys, dt, "x")
+        _check_host(w, ws, dt, "w")
+        if bias is not None:
+            _check_host(bias, (d.c_in,), torch.float32, "bias")
+        return _host_call(d, gbconv_conv_transpose, "gbconv_conv_transpose", x, w, bias, ys, xs, y)
     _check(x, ys, dt, "x")
     _check(w, ws, dt, "w")
     if bias is not None:
         _check(bias, (d.c_in,), torch.float32, "bias")
-    out = y if (y is not None and not host) else torch.empty(xs, dtype=dt, device=x.device)
+    out = y if y is not None else torch.empty(xs, dtype=dt, device=x.device)
     _check(out, xs, dt, "y")
     s = gbconv_conv_transpose(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
                               out.data_ptr(), torch.cuda.current_stream().cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_conv_transpose")
-    if host:
-        res = torch.empty(xs, dtype=dt, pin_memory=True) if y is None else y
-        res.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return res
     return out
 
 

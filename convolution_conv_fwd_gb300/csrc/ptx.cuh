@@ -254,6 +254,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // its first global-memory access.  grid_dep_launch() lets the next such kernel
 // on the stream start its own prologue early.  Both are no-ops in a kernel
 // launched without the attribute.
+// Invalidates the 128-byte L2 line at p (128-byte aligned) without writing it back: for scratch data
+// that is dead once read.  The line's memory contents become undefined.
+__device__ __forceinline__ void discard_l2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

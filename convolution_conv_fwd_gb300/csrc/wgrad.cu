@@ -125,12 +125,17 @@ __device__ __forceinline__ void store_grad(int e, float v, int E, int KH, int KW
 // the bits, and the compensation keeps the fp32 sum of up to a few hundred partials close to the
 // exact one.  The partials were just written and are read once: each warp issues up to six chunk
 // loads before it adds any of them, so the reads overlap instead of waiting one round trip each.
+// With `discard`, the L2 lines of the partials are dropped once read, so the dead scratch is never
+// written back to HBM (the workspace's contents are undefined after the call).  It needs chunk rows
+// on 128-byte lines (a 128-byte aligned workspace, Etot a multiple of 32), so that every line a
+// block drops holds only elements that block has read.  A block drops lines only when all of its
+// 128 columns are in range.
 constexpr int kReduceRuns = 16;
 constexpr int kReduceBatch = 6;
 
 template <typename T, int V>
 __global__ void __launch_bounds__(kReduceRuns * 32, 2) wgrad_reduce_kernel(int E, int Etot, int S, int KH, int KW,
-                                                                        int cpg, int ohwi,
+                                                                        int cpg, int ohwi, int discard,
                                                                         const float* __restrict__ ws,
                                                                         T* __restrict__ dw, float* __restrict__ db) {
   ptx::grid_dep_wait();
@@ -142,6 +147,8 @@ __global__ void __launch_bounds__(kReduceRuns * 32, 2) wgrad_reduce_kernel(int E
   for (int v = 0; v < V; ++v) acc[v] = comp[v] = 0.f;
   const int s0 = (j * S) / kReduceRuns, s1 = ((j + 1) * S) / kReduceRuns;
   if (V == 4 && e0 + 3 < Etot) {
+    // only blocks whose 128 columns are all in range drop lines (then every lane takes this branch)
+    const bool drop = discard && (int(blockIdx.x) + 1) * 128 <= Etot;
     for (int s = s0; s < s1; s += kReduceBatch) {
       float4 x[kReduceBatch];
 #pragma unroll
@@ -155,6 +162,14 @@ __global__ void __launch_bounds__(kReduceRuns * 32, 2) wgrad_reduce_kernel(int E
           kahan_add(acc[2], comp[2], x[u].z);
           kahan_add(acc[3], comp[3], x[u].w);
         }
+      if (drop) {
+        // the batch's 4 x kReduceBatch lines of this block's 128 columns, one per lane, once every
+        // lane's adds have consumed them
+        __syncwarp();
+        const int u = lane >> 2;
+        if (u < kReduceBatch && s + u < s1)
+          ptx::discard_l2(ws + int64_t(s + u) * Etot + int(blockIdx.x) * 128 + (lane & 3) * 32);
+      }
     }
   } else {
     for (int s = s0; s < s1; ++s)
@@ -211,18 +226,19 @@ gbconv_status launch_wgrad_reduce(const Problem& p, int S, const float* ws, void
   const bool vec = Etot % 4 == 0;
   // both weight layouts order (kd, kh, kw) alike, so the kernel's depth and height are one axis here
   const int KDH = int(p.KD * p.KH);
+  const int discard = vec && Etot % 32 == 0 && reinterpret_cast<uintptr_t>(ws) % 128 == 0;
   const dim3 grid(vec ? (Etot + 127) / 128 : (Etot + 31) / 32), block(kReduceRuns * 32);
   cudaError_t e;
   if (p.bf16)
     e = vec ? launch_kernel(wgrad_reduce_kernel<bf16, 4>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
-                            int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db)
+                            int(p.cpg()), int(p.ohwi), discard, ws, static_cast<bf16*>(dw), db)
             : launch_kernel(wgrad_reduce_kernel<bf16, 1>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
-                            int(p.cpg()), int(p.ohwi), ws, static_cast<bf16*>(dw), db);
+                            int(p.cpg()), int(p.ohwi), discard, ws, static_cast<bf16*>(dw), db);
   else
     e = vec ? launch_kernel(wgrad_reduce_kernel<float, 4>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
-                            int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db)
+                            int(p.cpg()), int(p.ohwi), discard, ws, static_cast<float*>(dw), db)
             : launch_kernel(wgrad_reduce_kernel<float, 1>, grid, block, 0, l.stream, E, Etot, S, KDH, int(p.KW),
-                            int(p.cpg()), int(p.ohwi), ws, static_cast<float*>(dw), db);
+                            int(p.cpg()), int(p.ohwi), discard, ws, static_cast<float*>(dw), db);
   return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
 }
 

@@ -255,6 +255,60 @@ def test_small_shapes_match_oracle(gb, case):
         check_bf16(got, ref, scale)
 
 
+# Host (pinned CPU) tensors through the public calls: batch slices whose copies overlap the kernels
+# (sliced here even at these sizes), uneven slices, each call kind.
+HOST = [
+    (shape_kw(n=5, in_size=(12, 11), c_in=64, c_out=64, bias=True), "fwd"),
+    (shape_kw(n=6, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "fwd"),
+    (shape_kw(n=3, in_size=(16, 13), c_in=128, c_out=64, stride=(2, 2)), "dgrad"),
+    (shape_kw(n=4, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "transpose"),
+    (shape_kw(n=3, in_size=(9, 8), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
+              bias=True), "fwd"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(4, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
+]
+
+
+def _pinned(torch, arr_f32, bits=None):
+    if bits is not None:
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr_f32, dtype=np.float32))
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("case", range(len(HOST)), ids=["%s-%d" % (op, i) for i, (_, op) in enumerate(HOST)])
+def test_host_buffers_match_oracle(gb, case, monkeypatch):
+    monkeypatch.setattr(gb, "_PIPE_MIN_BYTES", 0)
+    kw, op = HOST[case]
+    d = lib_desc(gb, kw)
+    c = oracle_conv(kw)
+    bits = kw["dtype"] == "bf16"
+    inp = draw(c, kw["dtype"], 900 + case, op="dgrad" if op != "fwd" else "fwd", bias=kw["bias"])
+    w = _pinned(torch, inp["w"], inp.get("w_bits") if bits else None)
+    if op == "fwd":
+        x = _pinned(torch, inp["x"], inp.get("x_bits") if bits else None)
+        b = None if "b" not in inp else _pinned(torch, inp["b"])
+        got = gb.conv_fwd(d, x, w, b)
+        ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp.get("b"))
+        scale = scale_fwd(c, inp["x"], inp["w"], inp.get("b"))
+    elif op == "dgrad":
+        g = _pinned(torch, inp["g"], inp.get("g_bits") if bits else None)
+        got = gb.conv_bwd_data(d, g, w)
+        ref = oracle.conv_dgrad(c, inp["g"], inp["w"])
+        scale = scale_dgrad(c, inp["g"], inp["w"])
+    else:
+        g = _pinned(torch, inp["g"], inp.get("g_bits") if bits else None)
+        bias = synth.normal(990 + case, (kw["c_in"],), 0.5).astype(np.float32)
+        got = gb.conv_transpose(d, g, w, _pinned(torch, bias))
+        ref = oracle.conv_transpose(c, inp["g"], inp["w"], bias)
+        scale = oracle.conv_transpose(c, np.abs(inp["g"]), np.abs(inp["w"]), np.abs(bias))
+    assert not got.is_cuda
+    got = to_host_f64(torch, got)
+    assert got.shape == ref.shape
+    (check_bf16 if bits else check_f32)(got, ref, scale)
+
+
 # Transposed convolution forward (dgrad + a bias over C_in), one case per dgrad kernel family.
 TRANSPOSE = [
     (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad"),
