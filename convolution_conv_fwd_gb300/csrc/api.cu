@@ -156,8 +156,10 @@ int32_t select_dgrad(const Problem& p, bool aligned) {
 
 int32_t select_wgrad(const Problem& p, bool aligned) {
   Problem q;
-  if (aligned && planar(p, &q) && wgrad_tc_supported(q)) return GBCONV_K_WGRAD;
-  return GBCONV_K_DIRECT_WGRAD;
+  if (!aligned) return GBCONV_K_DIRECT_WGRAD;
+  // a 3-D weight gradient with a real depth axis at unit depth stride: one kernel-depth tap per unit
+  if (!planar(p, &q)) return wgrad_tc_supported(p) ? GBCONV_K_WGRAD : GBCONV_K_DIRECT_WGRAD;
+  return wgrad_tc_supported(q) ? GBCONV_K_WGRAD : GBCONV_K_DIRECT_WGRAD;
 }
 
 // The problem a family's launcher takes: the planar view for the 2-D families, the full shape for
@@ -278,7 +280,8 @@ gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc* desc, int64_t* byte
   // Enough for whichever path a call takes (the tensor-core path needs aligned pointers).
   int64_t b = direct_wgrad_workspace(p);
   Problem q;
-  if (planar(p, &q) && wgrad_tc_supported(q)) b = std::max(b, wgrad_tc_workspace(q));
+  const Problem& v = planar(p, &q) ? q : p;  // the view the tensor-core path would take
+  if (wgrad_tc_supported(v)) b = std::max(b, wgrad_tc_workspace(v));
   *bytes = b;
   return GBCONV_OK;
 }

@@ -24,6 +24,10 @@
 // caller's workspace as fp32 partial sums [chunk][co][kh][kw][ci]; launch_wgrad_reduce then adds the
 // chunks in chunk order.  No atomics anywhere: the result is deterministic.
 //
+// A 3-D shape (unit depth stride) runs the same sums over (batch, output depth) slices, one
+// kernel-depth tap kd per unit: the unit pairs dy slice od with x slice od + kd*DD - PD (5-D boxes,
+// zero filled outside x) and writes only its kd's taps of the chunk's partial sums.
+//
 // Roles: warps 0-7 epilogue (TMEM -> workspace), warp 8 TMEM allocation and MMA issue (lane 0),
 // warp 9 zero fill and TMA loads (lane 0 issues).
 #include <cuda.h>
@@ -56,11 +60,12 @@ struct TcArgs {
   float* ws;              // [chunk][ws_stride] fp32 partial sums, elements in OHWI order
   unsigned int* status;
   int Cin, Cout, KH, KW, DH, DW, PH, PW;
+  int KD, DD, PD, OD;     // depth: kernel taps, dilation, begin padding, output depth (1, 1, 0, 0 for 2-D)
   int P;                  // virtual grid pitch OW + (KW-1)*DW
   int RB;                 // virtual rows per TMA box
   int box_bytes;          // RB * P * 128
-  int cb_in, pairs, chunks, units;
-  int bpi, total_blocks;  // row blocks per image, row blocks in the batch
+  int cb_in, pairs, chunks, units;  // units: pairs x chunks x KD
+  int bpi, total_blocks;  // row blocks per image (a (batch, depth) slice when 3-D), row blocks in the batch
   int seg_blocks;         // row blocks one shared-memory load holds
   int xe;                 // x boxes a segment needs beyond its dy boxes
   int gm;                 // MMA groups per 16 positions: ceil(KH / 2)
@@ -71,8 +76,19 @@ struct TcArgs {
 };
 
 struct TcMaps {
-  CUtensorMap x;   // (C_in, W, H, N), box (64, P, RB, 1)
-  CUtensorMap dy;  // (C_out, OW, OH, N), box (64, P, RB, 1)
+  CUtensorMap x;   // (C_in, W, H, N), box (64, P, RB, 1); 3-D: (C_in, W, H, D, N), box (64, P, RB, 1, 1)
+  CUtensorMap dy;  // (C_out, OW, OH, N), box (64, P, RB, 1); 3-D: (C_out, OW, OH, OD, N)
+};
+
+// A unit's kernel-depth tap, chunk and (input block, output block) pair.
+struct Unit {
+  int kd, chunk, pair;
+  __device__ Unit(const TcArgs& a, int u) {
+    kd = u % a.KD;
+    const int v = u / a.KD;
+    chunk = v / a.pairs;
+    pair = v - chunk * a.pairs;
+  }
 };
 
 struct Segment {
@@ -97,6 +113,15 @@ struct SegWalk {
     return true;
   }
 };
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int v, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+      "%6, %7}], [%2];" ::"r"(dst),
+      "l"(map), "r"(ptx::smem_addr(bar)), "r"(x), "r"(y), "r"(z), "r"(v), "r"(w)
+      : "memory");
+}
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
                                             int w) {
@@ -172,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int seg = 0;            // segments this CTA has loaded
     uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
     for (int u = int(blockIdx.x); ok && u < a.units; u += int(gridDim.x)) {
-      const int chunk = u / a.pairs, pair = u - chunk * a.pairs;
-      const int cib = pair % a.cb_in, cob = pair / a.cb_in;
-      SegWalk walk(a, chunk);
+      const Unit un(a, u);
+      const int cib = un.pair % a.cb_in, cob = un.pair / a.cb_in;
+      SegWalk walk(a, un.chunk);
       Segment sg;
       while (ok && walk.next(sg)) {
         if (seg > 0) {  // the previous segment's MMAs have finished reading shared memory
@@ -194,14 +219,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nxb = sg.nb + a.xe;
         if (lane == 0) {
           const int row0 = sg.rb * a.RB;  // first virtual row of the segment
+          // 3-D: segment image sg.n is the (batch, output depth) slice (n, od); x is read at depth
+          // od + kd*DD - PD (zero filled outside the input)
+          const int nn = a.OD > 0 ? sg.n / a.OD : sg.n, od = a.OD > 0 ? sg.n - nn * a.OD : 0;
+          const int xd = od + un.kd * a.DD - a.PD;
           for (int b = 0; b < nxb; ++b) {
             ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
-            tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
-                        row0 + b * a.RB - a.PH, sg.n);
+            if (a.OD > 0)
+              tma_load_5d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
+                          row0 + b * a.RB - a.PH, xd, nn);
+            else
+              tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
+                          row0 + b * a.RB - a.PH, sg.n);
             if (b < sg.nb) {
               ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(a.box_bytes));
-              tma_load_4d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
-                          cob * 64, 0, row0 + b * a.RB, sg.n);
+              if (a.OD > 0)
+                tma_load_5d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
+                            cob * 64, 0, row0 + b * a.RB, od, nn);
+              else
+                tma_load_4d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
+                            cob * 64, 0, row0 + b * a.RB, sg.n);
             }
           }
         }
@@ -250,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u))) break;
           ptx::tc_fence_after();
         }
-        SegWalk walk(a, u / pairs);
+        SegWalk walk(a, (u / a.KD) / pairs);
         Segment sg;
         bool first = true;
         while (ok && walk.next(sg)) {
@@ -305,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const int m = q * 32 + lane;
     const int i_atom = m >> 6, cil = m & 63;
-    const size_t co_stride = size_t(a.KH) * a.KW * a.Cin;
+    const size_t co_stride = size_t(a.KD) * a.KH * a.KW * a.Cin;
     int it = 0;
     for (int u = int(blockIdx.x); u < a.units; u += int(gridDim.x), ++it) {
       // One thread waits for the accumulators, polling at most every microsecond; the others block
@@ -334,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           : "memory");
       if (stop) break;
       ptx::tc_fence_after();
-      const int chunk = u / a.pairs, pair = u - chunk * a.pairs;
-      const int cib = pair % a.cb_in, cob = pair / a.cb_in;
+      const Unit un(a, u);
+      const int cib = un.pair % a.cb_in, cob = un.pair / a.cb_in;
       const int ci = cib * 64 + cil;
-      float* const wsc = a.ws + size_t(chunk) * a.ws_stride;
+      float* const wsc = a.ws + size_t(un.chunk) * a.ws_stride;
       for (int g = 0; g < a.gm; ++g) {
         const int kh = 2 * g + i_atom;
         for (int cc = h; cc < 4 * a.KW; cc += 2) {  // 16-column chunks
@@ -347,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kw = a.KW - 1 - (cc >> 2);
           const int co0 = cob * 64 + (cc & 3) * 16;
           if (kh < a.KH && ci < a.Cin) {
-            float* dst = wsc + ((size_t(co0) * a.KH + kh) * a.KW + kw) * a.Cin + ci;
+            float* dst = wsc + (((size_t(co0) * a.KD + un.kd) * a.KH + kh) * a.KW + kw) * a.Cin + ci;
             const int nco = min(16, a.Cout - co0);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -401,10 +438,14 @@ struct TcPlan {
   size_t smem;
   int grid;
   int N, H, W, OH, OW;
+  int D, OD;  // depth of x and dy when 3-D, else 0 (4-D tensor maps)
 };
 
 bool plan(const Problem& p, int sms, TcPlan& pl) {
   if (!(p.bf16 && p.nhwc && p.G == 1 && p.SH == 1 && p.SW == 1)) return false;
+  // a real depth axis: unit depth stride only (every dy slice meets every kernel-depth tap)
+  const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
+  if (deep && p.SD != 1) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides
   if (p.KW > 4 || (p.KW - 1) * p.DW > kFront) return false;
   const int gm = int((p.KH + 1) / 2);
@@ -416,6 +457,10 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   TcArgs& a = pl.a;
   a.Cin = int(p.Cin); a.Cout = int(p.Cout); a.KH = int(p.KH); a.KW = int(p.KW);
   a.DH = int(p.DH); a.DW = int(p.DW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.KD = deep ? int(p.KD) : 1;
+  a.DD = deep ? int(p.DD) : 1;
+  a.PD = deep ? int(p.PD) : 0;
+  a.OD = deep ? int(p.OD) : 0;
   a.P = int(P);
   a.RB = 8 / gcd(int(P), 8);
   a.box_bytes = a.RB * a.P * 128;
@@ -440,42 +485,50 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   }
   if (a.seg_blocks == 0) return false;
   a.bpi = int((p.OH + a.RB - 1) / a.RB);
-  const int64_t tb = p.N * a.bpi;
+  const int64_t tb = p.N * (deep ? p.OD : 1) * a.bpi;  // row blocks over every (batch, depth) slice
   if (tb >= (int64_t(1) << 30)) return false;
   a.total_blocks = int(tb);
   a.cb_in = int((p.Cin + 63) / 64);
   const int cb_out = int((p.Cout + 63) / 64);
   a.pairs = a.cb_in * cb_out;
-  a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / a.pairs)));
-  a.units = a.pairs * a.chunks;
+  // one unit per SM: chunks x pairs x kernel-depth taps (a 3-D chunk is swept once per depth tap)
+  a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / (a.pairs * a.KD))));
+  const int64_t units = int64_t(a.pairs) * a.chunks * a.KD;
+  if (units >= (int64_t(1) << 30)) return false;
+  a.units = int(units);
   pl.grid = std::max(1, std::min(a.units, sms));
   // A and B both MN-major (transpose bits 15 and 16), M = 128, N = 64 per kernel column
   a.idesc = ptx::idesc_bf16_f32(128, 64 * a.KW) | (1u << 15) | (1u << 16);
   pl.N = int(p.N); pl.H = int(p.H); pl.W = int(p.W); pl.OH = int(p.OH); pl.OW = int(p.OW);
+  pl.D = deep ? int(p.D) : 0;
+  pl.OD = deep ? int(p.OD) : 0;
   return true;
 }
 
-bool encode(const TcPlan& pl, const void* x, const void* dy, TcMaps& maps) {
+// One activation map: (C, W, H, N), or (C, W, H, D, N) when depth > 0; boxes of 64 channels x P x RB rows.
+bool encode_one(CUtensorMap* map, const void* base, int C, int W, int H, int depth, int N, const TcArgs& a) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const TcArgs& a = pl.a;
-  const cuuint32_t box[4] = {64, cuuint32_t(a.P), cuuint32_t(a.RB), 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  {
-    const cuuint64_t dims[4] = {cuuint64_t(a.Cin), cuuint64_t(pl.W), cuuint64_t(pl.H), cuuint64_t(pl.N)};
-    const cuuint64_t strides[3] = {cuuint64_t(a.Cin) * 2, cuuint64_t(pl.W) * a.Cin * 2,
-                                   cuuint64_t(pl.H) * pl.W * a.Cin * 2};
-    if (fn(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
+  const cuuint32_t rank = depth > 0 ? 5 : 4;
+  const cuuint64_t plane = cuuint64_t(H) * W * C * 2;
+  cuuint64_t dims[5] = {cuuint64_t(C), cuuint64_t(W), cuuint64_t(H), cuuint64_t(N), 1};
+  cuuint64_t strides[4] = {cuuint64_t(C) * 2, cuuint64_t(W) * C * 2, plane, 0};
+  if (depth > 0) {
+    dims[3] = cuuint64_t(depth);
+    dims[4] = cuuint64_t(N);
+    strides[3] = plane * cuuint64_t(depth);
   }
-  const cuuint64_t dims[4] = {cuuint64_t(a.Cout), cuuint64_t(pl.OW), cuuint64_t(pl.OH), cuuint64_t(pl.N)};
-  const cuuint64_t strides[3] = {cuuint64_t(a.Cout) * 2, cuuint64_t(pl.OW) * a.Cout * 2,
-                                 cuuint64_t(pl.OH) * pl.OW * a.Cout * 2};
-  return fn(&maps.dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, box, estr,
+  const cuuint32_t box[5] = {64, cuuint32_t(a.P), cuuint32_t(a.RB), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode(const TcPlan& pl, const void* x, const void* dy, TcMaps& maps) {
+  const TcArgs& a = pl.a;
+  return encode_one(&maps.x, x, a.Cin, pl.W, pl.H, pl.D, pl.N, a) &&
+         encode_one(&maps.dy, dy, a.Cout, pl.OW, pl.OH, pl.OD, pl.N, a);
 }
 
 }  // namespace
@@ -497,8 +550,8 @@ bool wgrad_tc_describe(const Problem& p, char* buf, size_t len) {
   const TcArgs& a = pl.a;
   std::snprintf(buf, len,
                 "wgrad_tc pairs=%d chunks=%d units=%d grid=%d rows_per_box=%d pitch=%d seg_blocks=%d x_extra=%d "
-                "groups=%d n=%d smem=%zu",
-                a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KW, pl.smem);
+                "groups=%d n=%d depth_taps=%d smem=%zu",
+                a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KW, a.KD, pl.smem);
   return true;
 }
 

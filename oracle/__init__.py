@@ -143,6 +143,8 @@ def _load():
         lib.oracle_conv_fwd_points3.restype = None
         lib.oracle_conv_dgrad_points3.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_dgrad_points3.restype = None
+        lib.oracle_conv_wgrad_points3.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
+        lib.oracle_conv_wgrad_points3.restype = None
         lib.oracle_conv_dgrad_points.argtypes = [P(_Desc), f32p, f32p, i64p, ctypes.c_int64, f64p]
         lib.oracle_conv_dgrad_points.restype = None
         lib.oracle_conv_wgrad.argtypes = [P(_Desc), f32p, f32p, f64p]
@@ -278,10 +280,13 @@ def conv_bgrad(c: Conv, dy) -> np.ndarray:
 
 
 def conv_wgrad_points(c: Conv, x, dy, idx) -> np.ndarray:
-    """Weight-gradient elements at an (count, 4) array of (c_out, c_in_local, kh, kw) indices."""
+    """Weight-gradient elements at an (count, 4) array of (c_out, c_in_local, kh, kw) indices, or for a
+    3-D shape an (count, 5) array of (c_out, c_in_local, kd, kh, kw) indices."""
     x, dy = _f32(x, c.x_shape()), _f32(dy, c.y_shape())
-    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 4)
+    k = 5 if c.spatial_dims == 3 else 4
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, k)
     out = np.empty(idx.shape[0], dtype=np.float64)
-    _load().oracle_conv_wgrad_points(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(dy, ctypes.c_float),
-                                     _ptr(idx, ctypes.c_int64), idx.shape[0], _ptr(out, ctypes.c_double))
+    fn = _load().oracle_conv_wgrad_points3 if k == 5 else _load().oracle_conv_wgrad_points
+    fn(ctypes.byref(c._c()), _ptr(x, ctypes.c_float), _ptr(dy, ctypes.c_float), _ptr(idx, ctypes.c_int64),
+       idx.shape[0], _ptr(out, ctypes.c_double))
     return out

@@ -373,6 +373,15 @@ void oracle_conv_fwd_points3(const oracle_conv *c, const float *x, const float *
                                  idx[5 * i + 4]);
 }
 
+/* 3-D point queries of the weight gradient: out[i] = dw at the i-th (co, c_local, kd, kh, kw)
+ * quintuple of idx. */
+void oracle_conv_wgrad_points3(const oracle_conv *c, const float *x, const float *dy,
+                               const int64_t *idx, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_conv_wgrad_at3(c, x, dy, idx[5 * i], idx[5 * i + 1], idx[5 * i + 2], idx[5 * i + 3],
+                                   idx[5 * i + 4]);
+}
+
 /* 3-D point queries of the input gradient: out[i] = dx at the i-th (n, c, d, h, w) quintuple of idx. */
 void oracle_conv_dgrad_points3(const oracle_conv *c, const float *dy, const float *w,
                                const int64_t *idx, int64_t count, double *out) {

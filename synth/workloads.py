@@ -91,6 +91,11 @@ EXTRA_WORKLOADS = [
              (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, False, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (2, 16, 56, 56, 64),
              {"g": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 27)) ** 0.5)},
              "conv3d backward-data NDHWC bf16, 3x3x3 stride 1 pad 1, dx and dy 2x16x56x56x64"),
+    # and its weight gradient: dW 64x3x3x3x64 from x and dy, both 2x16x56x56x64
+    Workload("wgrad3x3x3_ndhwc_bf16", 10, "wgrad", "bf16", 3, "ndhwc", "odhwi", 2, 64, 64, (16, 56, 56), (3, 3, 3),
+             (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, False, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (2, 16, 56, 56, 64),
+             {"x": ("normal", 1.0), "g": ("normal", 1.0)},
+             "conv3d backward-filter NDHWC bf16, 3x3x3 stride 1 pad 1, x and dy 2x16x56x56x64 -> dW 64x3x3x3x64"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

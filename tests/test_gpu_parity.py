@@ -410,17 +410,19 @@ def test_workload_full_size(gb, wl):
     inp = make_inputs(wl)
     kw = dict(wl.__dict__)
     if wl.op == "wgrad":
-        # dW elements (co, c_local, kh, kw): every tap at the channel corners plus a seeded sample; each
-        # oracle element is a full sum over the batch's positions
+        # dW elements (co, c_local, [kd,] kh, kw): every tap at the channel corners plus a seeded
+        # sample; each oracle element is a full sum over the batch's positions
         dw, _ = run_wgrad(gb, kw, inp, want_db=wl.bias)
-        idx = _sample_indices((wl.c_out, wl.c_in // wl.groups, wl.k[0], wl.k[1]), 5000 + wl.index, count=160)
-        idx = np.concatenate([idx, np.array([(co, cl, kh, kw_) for co in (0, wl.c_out - 1)
-                                             for cl in (0, wl.c_in // wl.groups - 1)
-                                             for kh in range(wl.k[0]) for kw_ in range(wl.k[1])])], axis=0)
+        taps = [tuple(t) for t in np.ndindex(*wl.k)]
+        cpg = wl.c_in // wl.groups
+        rnd = _sample_indices((wl.c_out, cpg, len(taps), 1), 5000 + wl.index, count=160)
+        idx = np.array([(co, cl) + taps[t] for co, cl, t, _ in rnd] +
+                       [(co, cl) + t for co in (0, wl.c_out - 1) for cl in (0, cpg - 1) for t in taps],
+                       dtype=np.int64)
         ref = oracle.conv_wgrad_points(c, inp["x"], inp["g"], idx)
         scale = oracle.conv_wgrad_points(c, np.abs(inp["x"]), np.abs(inp["g"]), idx)
-        # dw is OHWI: (co, kh, kw, c_local)
-        check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
+        # dw is O[D]HWI: (co, [kd,] kh, kw, c_local)
+        check_bf16(dw[(idx[:, 0],) + tuple(idx[:, 2 + i] for i in range(len(wl.k))) + (idx[:, 1],)], ref, scale)
         assert np.isfinite(dw).all()
         return
     if wl.spatial_dims == 3:
@@ -532,12 +534,24 @@ WGRAD = [
     (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "wgrad"),
     (shape_kw(n=2, in_size=(9, 10), c_in=6, c_out=9, groups=3, stride=(2, 1), pad=(1, 0), pad_end=(0, 1),
               layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
-    # 3-D: a depth kernel on the generic path (fp32 NCDHW with groups, bf16 NDHWC), and a depth-1
-    # kernel on the tensor-core path over N*D images
+    # 3-D: the generic path (fp32 NCDHW with groups; a depth stride), and the tensor-core path, one
+    # kernel-depth tap per unit over (batch, depth) slices: 3x3x3; depth dilation with (begin, end)
+    # depth padding and 128 output channels; a depth-2 kernel over six block pairs; a depth-1 kernel
+    # with depth padding; 16 input channels; and a depth-1 kernel over N*D images
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
               pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "direct_wgrad"),
-    (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
+    (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "direct_wgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(4, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(6, 10, 9), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(2, 1, 1), pad_end=(0, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(3, 6, 7), c_in=128, c_out=192, k=(2, 2, 3), stride=(1, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(3, 9, 11), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
               pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     # more block pairs than SMs: CTAs take several units in turn (the accumulators are handed over)

@@ -470,6 +470,9 @@ def test_conv3d_matches_torch_float64(ci):
     xi = np.argwhere(np.ones(gx.shape, dtype=bool))[::3]
     np.testing.assert_allclose(oracle.conv_dgrad_points(c, dy, w, xi), gx.numpy()[tuple(xi.T)], rtol=1e-12,
                                atol=1e-12)
+    wi = np.argwhere(np.ones(gw.shape, dtype=bool))[::3]  # (co, c_local, kd, kh, kw) of the OIDHW gradient
+    np.testing.assert_allclose(oracle.conv_wgrad_points(c, x, dy, wi), gw.numpy()[tuple(wi.T)], rtol=1e-12,
+                               atol=1e-12)
 
 
 def test_conv3d_with_unit_depth_is_conv2d():
