@@ -147,7 +147,7 @@ int32_t select_fwd(const Problem& p, bool aligned) {
 int32_t select_dgrad(const Problem& p, bool aligned) {
   Problem q;
   if (!aligned) return GBCONV_K_DIRECT_DGRAD;
-  // a 3-D gradient with a real depth axis at unit depth stride: the kernel-depth taps are dy sources
+  // a 3-D gradient with a real depth axis: depth phases, whose kernel-depth taps are dy sources
   if (!planar(p, &q)) return implicit_dgrad_supported(p) ? GBCONV_K_DGRAD : GBCONV_K_DIRECT_DGRAD;
   if (implicit_dgrad_supported(q)) return GBCONV_K_DGRAD;
   if (depthwise_dgrad_supported(q)) return GBCONV_K_DEPTHWISE_DGRAD;
@@ -157,7 +157,7 @@ int32_t select_dgrad(const Problem& p, bool aligned) {
 int32_t select_wgrad(const Problem& p, bool aligned) {
   Problem q;
   if (!aligned) return GBCONV_K_DIRECT_WGRAD;
-  // a 3-D weight gradient with a real depth axis at unit depth stride: one kernel-depth tap per unit
+  // a 3-D weight gradient with a real depth axis: one kernel-depth tap per unit
   if (!planar(p, &q)) return wgrad_tc_supported(p) ? GBCONV_K_WGRAD : GBCONV_K_DIRECT_WGRAD;
   return wgrad_tc_supported(q) ? GBCONV_K_WGRAD : GBCONV_K_DIRECT_WGRAD;
 }

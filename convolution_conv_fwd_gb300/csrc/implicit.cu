@@ -61,7 +61,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kMaxPhases = 4;
+constexpr int kMaxPhases = 8;  // stride phases of a gradient: (depth,) row and column phase
 constexpr int kMaxTapsPerPhase = 32;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
@@ -90,9 +90,12 @@ struct PhaseHdr {
   int nsrc;
   int8_t src_ah[kMaxSrc], src_aw[kMaxSrc];  // < 8 (TMA element strides are at most 8)
   int8_t src_t0[kMaxSrc + 1];                // <= kMaxTapsPerPhase
-  // 3-D: source k also reads activation depth od*depth_sd + src_ad[k], od the item's output slice:
-  // kd*DD - PD for the forward, PD - kd*DD for the gradient (dy slice id + PD - kd*DD)
+  // 3-D: source k also reads activation depth j*depth_sd + src_ad[k], j the item's depth slice of
+  // this phase: kd*DD - PD for the forward, (ad + PD - kd*DD) / SD for the gradient (dx slice
+  // id = ad + j*SD meets dy slice (id + PD - kd*DD) / SD when that divides exactly)
   int src_ad[kMaxSrc];
+  int jd;      // 3-D: depth slices of this phase per batch element
+  int out_pd;  // 3-D: output depth of the phase's slice j = 0 (the depth phase ad)
 };
 
 struct Phase : PhaseHdr {
@@ -112,7 +115,8 @@ struct Args {
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
   int nphase, total_items;
-  int depth_od, depth_sd;  // 3-D: output depth and depth stride (items run over N*depth slices); else 0
+  int depth_od, depth_sd;  // 3-D: nonzero, and the activation depth step per slice; else 0
+  int out_d, out_sd;       // 3-D: output depth, and output depth step between a phase's slices
   Phase ph[kMaxPhases];
 };
 
@@ -298,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int src = 0; ok && src < (MSRC ? ph.nsrc : 1); ++src) {
             if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
             ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
-            if (MSRC && a.depth_od > 0) {  // 3-D: item image it.n is a (batch, output depth) slice
-              const int nn = it.n / a.depth_od, od = it.n - nn * a.depth_od;
+            if (MSRC && a.depth_od > 0) {  // 3-D: item image it.n is a (batch, depth slice) pair
+              const int nn = it.n / ph.jd, od = it.n - nn * ph.jd;
               tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
                           kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
                           (ra + ph.rmin) * ph.row_step + ph.src_ah[src], od * a.depth_sd + ph.src_ad[src], nn);
@@ -443,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The phase geometry in registers: read from shared memory inside the store loop, every
       // field would be re-read after each staging load (those are asm with memory clobbers).
       const int ph_R = ph.R, ph_OWv = ph.OWv, ph_P = ph.P, ph_ntaps = ph.ntaps;
-      const int row_base = it.n * a.Ho + ph.out_ph, ph_sh = ph.out_sh, ph_sw = ph.out_sw, ph_pw = ph.out_pw;
+      // 3-D: the item's image is batch element it.n / jd at output depth out_pd + (it.n % jd) * out_sd
+      const int img = a.depth_od > 0 ? (it.n / ph.jd) * a.out_d + ph.out_pd + (it.n % ph.jd) * a.out_sd : it.n;
+      const int row_base = img * a.Ho + ph.out_ph, ph_sh = ph.out_sh, ph_sw = ph.out_sw, ph_pw = ph.out_pw;
       const int Wo = a.Wo, Cn = a.Cn;
       bf16* const out = a.out;
 #pragma unroll 1
@@ -600,13 +606,13 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
   // A real depth axis: kernel-depth taps are more activation sources (5-D TMA boxes).  The gradient
-  // takes them only at unit depth stride, where every dx slice meets every kernel-depth tap (a
-  // depth stride would split dx into depth phases with different tap sets).
+  // also splits dx into depth phases at a depth stride: phase ad holds the slices id = ad + j*SD,
+  // each met by the kernel-depth taps with (ad + PD - kd*DD) divisible by SD.
   const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
-  if (deep && dgrad && (p.SD != 1 || p.KD > kMaxSrc)) return false;
+  if (deep && dgrad && p.KD > kMaxSrc) return false;
   // A strided forward reads its activations through strided views (TMA element strides <= 8).
   if (!dgrad && (p.SH > 8 || p.SW > 8)) return false;
-  if (dgrad && p.SH * p.SW > kMaxPhases) return false;
+  if (dgrad && (deep ? p.SD : 1) * p.SH * p.SW > kMaxPhases) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides and vector stores
   if (p.KD * p.KH * p.KW > kMaxTapsPerPhase) return false;
   pl = Plan{};
@@ -615,11 +621,12 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   const int64_t Ck = dgrad ? p.Cout : p.Cin, Cn = dgrad ? p.Cin : p.Cout;
   pl.bn = pick_bn(Cn);
   pl.nsub = pl.bn <= 128 ? 2 : 1;
-  // 3-D: items run over (batch, depth) slices of the output (y, or dx for the gradient)
-  const int64_t out_depth = dgrad ? p.D : p.OD;
-  a.N = int(deep ? p.N * out_depth : p.N);
-  a.depth_od = deep ? int(out_depth) : 0;
+  // 3-D: items run over (batch, depth slice) pairs of each phase (its jd slices of y, or of dx)
+  a.N = int(p.N);
+  a.depth_od = deep ? 1 : 0;
   a.depth_sd = deep ? (dgrad ? 1 : int(p.SD)) : 0;
+  a.out_d = deep ? int(dgrad ? p.D : p.OD) : 0;
+  a.out_sd = deep && dgrad ? int(p.SD) : 1;
   a.Cn = int(Cn);
   a.Ho = int(p.H);
   a.Wo = int(p.W);
@@ -693,12 +700,25 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
       }
     ph.src_t0[ph.nsrc] = int8_t(k);
     s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+    ph.jd = deep ? int(p.OD) : 1;
+    ph.out_pd = 0;
     specs[nph++] = s;
   } else {
+    const int SD = deep ? int(p.SD) : 1;
+    for (int ad = 0; ad < SD; ++ad)
     for (int ah = 0; ah < p.SH; ++ah)
       for (int aw = 0; aw < p.SW; ++aw) {
         PhaseSpec s{};
         Phase& ph = s.ph;
+        ph.jd = deep ? int((p.D - ad + SD - 1) / SD) : 1;
+        ph.out_pd = ad;
+        if (ph.jd <= 0) continue;
+        // the kernel-depth taps that reach depth phase ad, and their dy slice offsets
+        int kds[kMaxSrc], nkd = 0;
+        for (int kd = 0; kd < (deep ? p.KD : 1); ++kd) {
+          const int num = deep ? int(ad + p.PD - kd * p.DD) : 0;
+          if (((num % SD) + SD) % SD == 0) { ph.src_ad[nkd] = num / SD; kds[nkd++] = kd; }
+        }
         ph.R = int((p.H - ah + p.SH - 1) / p.SH);
         ph.OWv = int((p.W - aw + p.SW - 1) / p.SW);
         if (ph.R <= 0 || ph.OWv <= 0) continue;
@@ -715,26 +735,25 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         int rmin = 0, rmax = 0, cmin = 0, cmax = 0;
         for (int i = 0; i < nkh; ++i) { rmin = i ? std::min(rmin, drs[i]) : drs[i]; rmax = i ? std::max(rmax, drs[i]) : drs[i]; }
         for (int i = 0; i < nkw; ++i) { cmin = i ? std::min(cmin, dcs[i]) : dcs[i]; cmax = i ? std::max(cmax, dcs[i]) : dcs[i]; }
-        ph.ntaps = int(nkh * nkw * p.KD);
+        ph.ntaps = nkh * nkw * nkd;
         ph.P = ph.OWv + (cmax - cmin);
         ph.rmin = rmin; ph.cmin = cmin;
         ph.out_sh = int(p.SH); ph.out_sw = int(p.SW); ph.out_ph = ah; ph.out_pw = aw;
-        // dy is read as it is, one source per kernel-depth tap kd: dx slice id meets dy slice
-        // id + PD - kd*DD (unit depth stride), zero filled outside dy.  2-D: one source.
+        // dy is read as it is, one source per kernel-depth tap kd that reaches the phase (zero
+        // filled outside dy).  2-D: one source.
         ph.row_step = ph.col_step = 1;
-        ph.nsrc = int(p.KD);
-        for (int kd = 0; kd < p.KD; ++kd) {
-          ph.src_ah[kd] = ph.src_aw[kd] = 0;
-          ph.src_ad[kd] = int(p.PD - kd * p.DD);
-          ph.src_t0[kd] = int8_t(kd * nkh * nkw);
+        ph.nsrc = nkd;
+        for (int k = 0; k < nkd; ++k) {
+          ph.src_ah[k] = ph.src_aw[k] = 0;
+          ph.src_t0[k] = int8_t(k * nkh * nkw);
           for (int i = 0; i < nkh; ++i)
             for (int j = 0; j < nkw; ++j) {
-              const int t = (kd * nkh + i) * nkw + j;
+              const int t = (k * nkh + i) * nkw + j;
               ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
-              ph.tap_w[t] = int((kd * p.KH + khs[i]) * p.KW + kws[j]);
+              ph.tap_w[t] = int((kds[k] * p.KH + khs[i]) * p.KW + kws[j]);
             }
         }
-        ph.src_t0[p.KD] = int8_t(ph.ntaps);
+        ph.src_t0[nkd] = int8_t(ph.ntaps);
         s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
         specs[nph++] = s;
       }
@@ -744,9 +763,11 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   if (nph == 0) return false;
   int item = 0, a_max = 0;
   for (int i = 0; i < nph; ++i) {
-    if (!finish_phase(specs[i], pl.nsub, a.N)) return false;
+    const int imgs = a.N * specs[i].ph.jd;  // (batch, depth slice) pairs; 2-D: the batch
+    if (!finish_phase(specs[i], pl.nsub, imgs)) return false;
     specs[i].ph.item0 = item;
-    item += a.N * specs[i].ph.tiles * a.n_tiles;
+    if (int64_t(item) + int64_t(imgs) * specs[i].ph.tiles * a.n_tiles >= (int64_t(1) << 30)) return false;
+    item += imgs * specs[i].ph.tiles * a.n_tiles;
     a.ph[i] = specs[i].ph;
     a_max = std::max(a_max, specs[i].ph.a_bytes);
   }

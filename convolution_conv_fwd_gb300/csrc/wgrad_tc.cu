@@ -24,9 +24,9 @@
 // caller's workspace as fp32 partial sums [chunk][co][kh][kw][ci]; launch_wgrad_reduce then adds the
 // chunks in chunk order.  No atomics anywhere: the result is deterministic.
 //
-// A 3-D shape (unit depth stride) runs the same sums over (batch, output depth) slices, one
-// kernel-depth tap kd per unit: the unit pairs dy slice od with x slice od + kd*DD - PD (5-D boxes,
-// zero filled outside x) and writes only its kd's taps of the chunk's partial sums.
+// A 3-D shape runs the same sums over (batch, output depth) slices, one kernel-depth tap kd per
+// unit: the unit pairs dy slice od with x slice od*SD + kd*DD - PD (5-D boxes, zero filled outside
+// x) and writes only its kd's taps of the chunk's partial sums.
 //
 // Roles: warps 0-7 epilogue (TMEM -> workspace), warp 8 TMEM allocation and MMA issue (lane 0),
 // warp 9 zero fill and TMA loads (lane 0 issues).
@@ -60,7 +60,7 @@ struct TcArgs {
   float* ws;              // [chunk][ws_stride] fp32 partial sums, elements in OHWI order
   unsigned int* status;
   int Cin, Cout, KH, KW, DH, DW, PH, PW;
-  int KD, DD, PD, OD;     // depth: kernel taps, dilation, begin padding, output depth (1, 1, 0, 0 for 2-D)
+  int KD, SD, DD, PD, OD;  // depth: kernel taps, stride, dilation, begin padding, output depth (2-D: 1, 1, 1, 0, 0)
   int P;                  // virtual grid pitch OW + (KW-1)*DW
   int RB;                 // virtual rows per TMA box
   int box_bytes;          // RB * P * 128
@@ -220,9 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const int row0 = sg.rb * a.RB;  // first virtual row of the segment
           // 3-D: segment image sg.n is the (batch, output depth) slice (n, od); x is read at depth
-          // od + kd*DD - PD (zero filled outside the input)
+          // od*SD + kd*DD - PD (zero filled outside the input)
           const int nn = a.OD > 0 ? sg.n / a.OD : sg.n, od = a.OD > 0 ? sg.n - nn * a.OD : 0;
-          const int xd = od + un.kd * a.DD - a.PD;
+          const int xd = od * a.SD + un.kd * a.DD - a.PD;
           for (int b = 0; b < nxb; ++b) {
             ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
             if (a.OD > 0)
@@ -443,9 +443,8 @@ struct TcPlan {
 
 bool plan(const Problem& p, int sms, TcPlan& pl) {
   if (!(p.bf16 && p.nhwc && p.G == 1 && p.SH == 1 && p.SW == 1)) return false;
-  // a real depth axis: unit depth stride only (every dy slice meets every kernel-depth tap)
+  // a real depth axis: any depth stride (a unit's x slice is a fixed function of the dy slice)
   const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
-  if (deep && p.SD != 1) return false;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides
   if (p.KW > 4 || (p.KW - 1) * p.DW > kFront) return false;
   const int gm = int((p.KH + 1) / 2);
@@ -458,6 +457,7 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   a.Cin = int(p.Cin); a.Cout = int(p.Cout); a.KH = int(p.KH); a.KW = int(p.KW);
   a.DH = int(p.DH); a.DW = int(p.DW); a.PH = int(p.PH); a.PW = int(p.PW);
   a.KD = deep ? int(p.KD) : 1;
+  a.SD = deep ? int(p.SD) : 1;
   a.DD = deep ? int(p.DD) : 1;
   a.PD = deep ? int(p.PD) : 0;
   a.OD = deep ? int(p.OD) : 0;

@@ -75,12 +75,12 @@ typedef enum {
   GBCONV_K_DEPTHWISE = 1,     /* NHWC bf16 depthwise direct kernel, bandwidth bound */
   GBCONV_K_POINTWISE = 2,     /* NHWC bf16 1x1: TMA-fed tcgen05 GEMM */
   GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
-  GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 (3-D: unit depth stride) */
+  GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 (3-D: depth phases at a depth stride) */
   GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
   GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
   GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
   GBCONV_K_WGRAD = 8           /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction
-                                  (3-D: unit depth stride, one kernel-depth tap per work unit) */
+                                  (3-D: one kernel-depth tap per work unit) */
 } gbconv_kernel;
 
 typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER = 2 } gbconv_op;

@@ -260,10 +260,9 @@ def test_conv3d_shapes_and_families(gb):
         xs, ws, ys = gb.desc_shapes(lib_desc(gb, kw))
         c = oracle_conv(kw)
         assert (xs, ws, ys) == (c.x_shape(), c.w_shape(), c.y_shape())
-    # a real depth kernel: the forward and (at unit depth stride) the input gradient on the implicit
-    # GEMM with one activation source per kernel-depth tap, the weight gradient (unit depth stride)
-    # on the tensor-core kernel one kernel-depth tap per unit; depth 1, unit stride, no depth
-    # padding: the 2-D families on N*D images (channels-last only)
+    # a real depth kernel: the forward and the input gradient on the implicit GEMM with one activation
+    # source per kernel-depth tap, the weight gradient on the tensor-core kernel one kernel-depth tap
+    # per unit; depth 1, unit stride, no depth padding: the 2-D families on N*D images (channels-last only)
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 0) == "implicit"
     _, _, f = _plan(gb, s3(n=2, in_size=(5, 6, 7), c_in=64, c_out=64, stride=(2, 1, 1)))
     od = (5 + 2 - 3) // 2 + 1
@@ -277,13 +276,20 @@ def test_conv3d_shapes_and_families(gb):
     assert int(f["items"]) == 2 * 5 * -(-6 * (7 + 2) // 256)
     _, _, f = _plan(gb, s3(n=1, in_size=(4, 8, 8), c_in=64, c_out=64, stride=(1, 2, 2)), op=1)
     assert f["phases"] == "4" and f["sources"] == "3" and f["taps"] == "12"
-    # a depth stride splits dx into depth phases: the generic gradient
-    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 1) == "direct_dgrad"
+    # a depth stride splits dx into depth phases (2 x 2 x 2 strides: eight), each with the kernel-depth
+    # taps that reach it
+    _, _, f = _plan(gb, s3(n=1, in_size=(5, 8, 9), c_in=64, c_out=64, stride=(2, 2, 2)), op=1)
+    assert f["phases"] == "8" and f["taps"] == "8"
+    _, _, f = _plan(gb, s3(n=1, in_size=(7, 6, 7), c_in=64, c_out=64, stride=(3, 1, 1)), op=1)
+    assert f["phases"] == "3" and f["sources"] in ("1",) and f["taps"] == "9"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 1) == "dgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, layout="ncdhw", wlayout="oidhw")), 1) == "direct_dgrad"
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64)), 2) == "wgrad"
     # the weight gradient: one unit per (chunk, block pair, kernel-depth tap), about one unit per SM
     _, _, f = _plan(gb, s3(n=2, in_size=(16, 56, 56), c_in=64, c_out=64), op=2)
     assert f["depth_taps"] == "3" and int(f["units"]) == 3 * int(f["chunks"]) and int(f["units"]) <= 152
-    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 2) == "direct_wgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 2) == "wgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(1, 2, 2))), 2) == "direct_wgrad"
     flat = dict(k=(1, 3, 3), pad=(0, 1, 1), c_in=64, c_out=64)
     assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 0) == "implicit"
     assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 1) == "dgrad"

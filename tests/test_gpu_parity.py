@@ -194,7 +194,7 @@ SMALL = [
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
               pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "dgrad", "direct_dgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(2, 1, 1),
-              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "direct_dgrad"),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(3, 9, 11), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
               pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True), "fwd", "implicit"),
     (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 9), c_in=128, c_out=64, k=(1, 1, 1), stride=(1, 1, 1),
@@ -217,6 +217,17 @@ SMALL = [
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(3, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(1, 1, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    # depth strides: dx split into depth phases, each met by the kernel-depth taps that divide
+    # evenly: 2x2x2 strides (eight phases, an odd depth); depth stride 3; depth stride 2 with depth
+    # dilation and (begin, end) depth padding; a depth-1 kernel, whose odd depth phase no tap reaches
+    (shape_kw(spatial_dims=3, n=1, in_size=(5, 8, 9), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 2, 2),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(7, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(3, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(7, 6, 5), c_in=64, c_out=128, k=(3, 3, 3), stride=(2, 1, 1),
+              pad=(2, 1, 1), pad_end=(1, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(2, 1, 1),
+              pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -318,6 +329,8 @@ TRANSPOSE = [
               stride=(2, 2)), "direct_dgrad"),
     (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "direct_dgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 8, 7), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 2, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 8), c_in=128, c_out=64, k=(3, 3, 3), stride=(2, 2, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
 ]
 
@@ -534,14 +547,19 @@ WGRAD = [
     (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "wgrad"),
     (shape_kw(n=2, in_size=(9, 10), c_in=6, c_out=9, groups=3, stride=(2, 1), pad=(1, 0), pad_end=(0, 1),
               layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
-    # 3-D: the generic path (fp32 NCDHW with groups; a depth stride), and the tensor-core path, one
-    # kernel-depth tap per unit over (batch, depth) slices: 3x3x3; depth dilation with (begin, end)
-    # depth padding and 128 output channels; a depth-2 kernel over six block pairs; a depth-1 kernel
-    # with depth padding; 16 input channels; and a depth-1 kernel over N*D images
+    # 3-D: the generic path (fp32 NCDHW with groups; an H/W stride), and the tensor-core path, one
+    # kernel-depth tap per unit over (batch, depth) slices: depth strides (with depth dilation and
+    # (begin, end) depth padding); 3x3x3; depth dilation with (begin, end) depth padding and 128
+    # output channels; a depth-2 kernel over six block pairs; a depth-1 kernel with depth padding;
+    # 16 input channels; and a depth-1 kernel over N*D images
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
               pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "direct_wgrad"),
-    (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
+    (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 2, 2),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "direct_wgrad"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
+    (shape_kw(spatial_dims=3, n=2, in_size=(7, 6, 5), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
+              pad=(2, 1, 1), pad_end=(1, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 6, 5), c_in=16, c_out=8, k=(3, 3, 3), stride=(1, 1, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(4, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
