@@ -45,6 +45,23 @@ COPIES = 16  # operand copies per workload = passes over the hot path per step
 WORKLOAD_NAME = "conv hot path: 5 workloads x 16 batches per step (conv1d f32, 1x1, dense 3x3, depthwise 3x3 s2, dgrad 3x3 s2)"
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of every rank's value (a job's time is its slowest rank's); the value itself when
+    no process group is running or it has one rank."""
+    import torch
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's algorithmic flops over the slowest rank's time (weak scaling)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def peaks():
     p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -264,11 +281,7 @@ def run_gpu(args, rank, world, local_rank):
     group_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                 for i in range(len(cases))]
     per_kernel_ms = [g / len(c["copies"]) for g, c in zip(group_ms, cases)]
-    step_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps))
-    if world > 1:
-        tt = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(statistics.mean(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)), dev)
 
     def config_line(c, ms):
         t_f = c["flops"] / (pk["bf16_tflops"] * 1e12)
@@ -328,11 +341,7 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(args.steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dev)
 
     total_flops = sum(c["flops"] for c in cases)
     step_flops = sum(c["flops"] * len(c["copies"]) for c in cases)
@@ -349,7 +358,7 @@ def run_gpu(args, rank, world, local_rank):
             "kernel": dc["family"], "workload": dc["wl"].name,
             "algorithmic_bytes": dc["bytes"], "algorithmic_flops": dc["flops"],
             "peak_source": pk["source"] + " (burst)"}
-    value = world * step_flops / (step_ms * 1e-3) / 1e12
+    value = job_rate(world, step_flops, step_ms)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -364,7 +373,7 @@ def run_gpu(args, rank, world, local_rank):
         "per_config": per,
         "extra_configs": extra,
         "roofline": roof,
-        "e2e": {"value": round(world * total_flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": UNIT,
+        "e2e": {"value": round(job_rate(world, total_flops, e2e_ms), 4), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
