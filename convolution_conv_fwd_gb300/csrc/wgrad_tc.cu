@@ -55,24 +55,34 @@ constexpr int kFront = 8;       // zero positions ahead of the dy rows: the dy a
 constexpr int kMaxBoxes = 24;   // per segment, for x and for dy
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kStepBlock = 4;   // 16-position MMA steps issued back to back
+constexpr int kMaxWgPhases = 16;  // H/W stride phases (strides up to 4 x 4)
 
 struct TcArgs {
   float* ws;              // [chunk][ws_stride] fp32 partial sums, elements in OHWI order
   unsigned int* status;
   int Cin, Cout, KH, KW, DH, DW, PH, PW;
+  int SH, SW;             // H/W strides: x is read through a strided view (TMA element strides)
+  int ddr, ddc;           // phase-grid rows / columns between a stride phase's consecutive kernel rows / columns
   int KD, SD, DD, PD, OD;  // depth: kernel taps, stride, dilation, begin padding, output depth (2-D: 1, 1, 1, 0, 0)
-  int P;                  // virtual grid pitch OW + (KW-1)*DW
+  int nph;                // stride phases that hold taps (1 at unit stride)
+  int KWP;                // most kernel columns in one phase: a group's TMEM columns are KWP * 64
+  int P;                  // virtual grid pitch OW + (KWP-1)*ddc
   int RB;                 // virtual rows per TMA box
   int box_bytes;          // RB * P * 128
-  int cb_in, pairs, chunks, units;  // units: pairs x chunks x KD
+  int cb_in, pairs, chunks, units;  // units: pairs x chunks x KD x nph
   int bpi, total_blocks;  // row blocks per image (a (batch, depth) slice when 3-D), row blocks in the batch
   int seg_blocks;         // row blocks one shared-memory load holds
   int xe;                 // x boxes a segment needs beyond its dy boxes
-  int gm;                 // MMA groups per 16 positions: ceil(KH / 2)
+  int gm;                 // MMA groups per 16 positions: ceil(kernel rows of a phase / 2), at most
   int x_bytes;            // x region bytes (the dy region follows)
   int tail;               // zero positions needed after a segment's dy rows
   int ws_stride;          // floats per chunk in the workspace
-  uint32_t idesc;
+  // Stride phase q: its kernel rows (A atom 2g+i is row ph_kh[q][2g+i]) and kernel columns (B atom j is
+  // column ph_kw[q][nkw-1-j]), the x row and column of its virtual (0, 0) (x row = r * SH + ph_r0), and
+  // its MMA instruction descriptor (N = 64 * nkw).
+  int8_t ph_kh[kMaxWgPhases][4], ph_kw[kMaxWgPhases][4], ph_nkh[kMaxWgPhases], ph_nkw[kMaxWgPhases];
+  int ph_r0[kMaxWgPhases], ph_c0[kMaxWgPhases];
+  uint32_t ph_idesc[kMaxWgPhases];
 };
 
 struct TcMaps {
@@ -80,12 +90,15 @@ struct TcMaps {
   CUtensorMap dy;  // (C_out, OW, OH, N), box (64, P, RB, 1); 3-D: (C_out, OW, OH, OD, N)
 };
 
-// A unit's kernel-depth tap, chunk and (input block, output block) pair.
+// A unit's kernel-depth tap, stride phase, chunk and (input block, output block) pair.
 struct Unit {
-  int kd, chunk, pair;
+  int kd, ph, chunk, pair;
   __device__ Unit(const TcArgs& a, int u) {
-    kd = u % a.KD;
-    const int v = u / a.KD;
+    const int classes = a.KD * a.nph;
+    const int cls = u % classes;
+    kd = cls / a.nph;
+    ph = cls - kd * a.nph;
+    const int v = u / classes;
     chunk = v / a.pairs;
     pair = v - chunk * a.pairs;
   }
@@ -143,6 +156,27 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t atom_
   return d;
 }
 
+// One block of tn 16-position steps (kStepBlock when full), G MMA groups per step, issued back to back.
+template <int G>
+__device__ __forceinline__ void issue_steps(int tn, uint32_t tmem, uint32_t ncols, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t g_step, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t acc0) {
+  if (tn == kStepBlock) {
+#pragma unroll
+    for (int i = 0; i < kStepBlock; ++i)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
+                           b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
+  } else {
+    for (int i = 0; i < tn; ++i)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
+                           b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
+  }
+}
+
 // GM: MMA groups per 16 positions (ceil(KH/2)), a template parameter so a block of steps issues its
 // MMAs back to back: scalar work between MMAs in the issuing thread adds directly to their time.
 template <int GM>
@@ -161,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* fin = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t tmem_cols = GM * a.KW * 64 <= 256 ? 256u : 512u;
+  const uint32_t tmem_cols = GM * a.KWP * 64 <= 256 ? 256u : 512u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -223,14 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // od*SD + kd*DD - PD (zero filled outside the input)
           const int nn = a.OD > 0 ? sg.n / a.OD : sg.n, od = a.OD > 0 ? sg.n - nn * a.OD : 0;
           const int xd = od * a.SD + un.kd * a.DD - a.PD;
+          // the unit's stride phase: virtual row r, column c read x row r*SH + r0, column c*SW + c0
+          const int xr0 = a.ph_r0[un.ph], xc0 = a.ph_c0[un.ph];
           for (int b = 0; b < nxb; ++b) {
             ptx::mbar_arrive_expect_tx(xbar + b, uint32_t(a.box_bytes));
+            const int xrow = (row0 + b * a.RB) * a.SH + xr0;
             if (a.OD > 0)
-              tma_load_5d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
-                          row0 + b * a.RB - a.PH, xd, nn);
+              tma_load_5d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, xc0, xrow, xd,
+                          nn);
             else
-              tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, -a.PW,
-                          row0 + b * a.RB - a.PH, sg.n);
+              tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, xc0, xrow,
+                          sg.n);
             if (b < sg.nb) {
               ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(a.box_bytes));
               if (a.OD > 0)
@@ -268,31 +305,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg = 0, it = 0;
       // Everything the loop needs, in registers: kernel parameters live in memory, and every MMA's
       // asm statement clobbers memory, so fields read inside the loop would be reloaded per MMA.
-      const int P = a.P, KW = a.KW, xe = a.xe, units = a.units, pairs = a.pairs;
+      const int P = a.P, xe = a.xe, units = a.units, ddr = a.ddr, ddc = a.ddc;
       const int box_pos = a.RB * a.P;                      // positions per box
-      const int xreach = (2 * GM - 1) * a.DH * P;          // farthest x position an MMA reads past k
-      const uint32_t idesc = a.idesc;
-      const uint32_t ncols = uint32_t(KW * 64);
-      // Descriptor words at k = 0.  A step of 16 positions is 2048 bytes, +128 in the start field;
-      // group g's A starts 2g*DH*P positions on.
-      const uint64_t ad0 = desc_mn_sw128(ptx::smem_addr(xs), uint32_t(a.DH * P) * 128u);
-      const uint64_t bd0 = desc_mn_sw128(ptx::smem_addr(ys) + uint32_t(kFront - (KW - 1) * a.DW) * 128u,
-                                         uint32_t(a.DW) * 128u);
+      const uint32_t ncols = uint32_t(a.KWP * 64);         // TMEM columns between groups
+      // A descriptor words at k = 0.  A step of 16 positions is 2048 bytes, +128 in the start field;
+      // group g's A starts 2g*ddr*P positions on.
+      const uint64_t ad0 = desc_mn_sw128(ptx::smem_addr(xs), uint32_t(ddr * P) * 128u);
       const uint32_t a_lo0 = uint32_t(ad0), a_hi = uint32_t(ad0 >> 32);
-      const uint32_t b_lo0 = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
-      const uint32_t g_step = uint32_t(2 * a.DH * P) * 8u;  // (2*DH*P*128) >> 4
+      const uint32_t g_step = uint32_t(2 * ddr * P) * 8u;  // (2*ddr*P*128) >> 4
       uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
       for (int u = int(blockIdx.x); ok && u < units; u += int(gridDim.x), ++it) {
         if (it > 0) {  // the epilogue has taken the previous unit's accumulators
           if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u))) break;
           ptx::tc_fence_after();
         }
-        SegWalk walk(a, (u / a.KD) / pairs);
+        // the unit's stride phase: its groups, its N (its kernel columns) and its B atoms
+        const Unit un(a, u);
+        const int nkw = a.ph_nkw[un.ph], gmu = (a.ph_nkh[un.ph] + 1) / 2;
+        const uint32_t idesc = a.ph_idesc[un.ph];
+        const int xreach = (2 * gmu - 1) * ddr * P;  // farthest x position an MMA reads past k
+        const uint64_t bd0 = desc_mn_sw128(ptx::smem_addr(ys) + uint32_t(kFront - (nkw - 1) * ddc) * 128u,
+                                           uint32_t(ddc) * 128u);
+        const uint32_t b_lo0 = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+        SegWalk walk(a, un.chunk);
         Segment sg;
         bool first = true;
         while (ok && walk.next(sg)) {
           const int nb = sg.nb, nxb = sg.nb + xe;
-          const int nk = (nb * box_pos + (KW - 1) * a.DW + 15) / 16;
+          const int nk = (nb * box_pos + (nkw - 1) * ddc + 15) / 16;
           int xw = 0, yw = 0;  // boxes already waited for
           // Blocks of kStepBlock steps: the boxes the whole block reads are waited for first, then its
           // MMAs go out back to back.
@@ -306,20 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const uint32_t a_lo = a_lo0 + uint32_t(t0) * 128u, b_lo = b_lo0 + uint32_t(t0) * 128u;
             const uint32_t acc0 = (first && t0 == 0) ? 0u : 1u;
-            if (tn == kStepBlock) {
-#pragma unroll
-              for (int i = 0; i < kStepBlock; ++i)
-#pragma unroll
-                for (int g = 0; g < GM; ++g)
-                  ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
-                                     b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
-            } else {
-              for (int i = 0; i < tn; ++i)
-#pragma unroll
-                for (int g = 0; g < GM; ++g)
-                  ptx::mma_bf16_lohi(tmem + uint32_t(g) * ncols, a_lo + uint32_t(i) * 128u + uint32_t(g) * g_step, a_hi,
-                                     b_lo + uint32_t(i) * 128u, b_hi, idesc, i == 0 ? acc0 : 1u);
-            }
+            // every group of the kernel (the unit-stride case), or a stride phase's fewer ones
+            if (gmu == GM)
+              issue_steps<GM>(tn, tmem, ncols, a_lo, a_hi, g_step, b_lo, b_hi, idesc, acc0);
+            else
+              issue_steps<1>(tn, tmem, ncols, a_lo, a_hi, g_step, b_lo, b_hi, idesc, acc0);
           }
           ptx::mma_commit(seg_done);
           xph ^= (1u << nxb) - 1u;
@@ -335,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue: TMEM -> workspace
-    // Warps w and w+4 share TMEM lanes 32*(w%4).. and split the 16-column chunks.  Lane m holds
-    // kernel row 2g + m/64 and input channel m%64 of the block; column n holds kernel column
-    // KW-1 - n/64 and output channel n%64.  Consecutive lanes store consecutive input channels.
+    // Warps w and w+4 share TMEM lanes 32*(w%4).. and split the 16-column chunks.  Lane m holds the
+    // phase's kernel row 2g + m/64 and input channel m%64 of the block; column n of a group holds the
+    // phase's kernel column nkw-1 - n/64 and output channel n%64.  Consecutive lanes store consecutive
+    // input channels.
     const int q = warp & 3, h = warp >> 2;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const int m = q * 32 + lane;
@@ -375,15 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cib = un.pair % a.cb_in, cob = un.pair / a.cb_in;
       const int ci = cib * 64 + cil;
       float* const wsc = a.ws + size_t(un.chunk) * a.ws_stride;
-      for (int g = 0; g < a.gm; ++g) {
-        const int kh = 2 * g + i_atom;
-        for (int cc = h; cc < 4 * a.KW; cc += 2) {  // 16-column chunks
+      const int nkh = a.ph_nkh[un.ph], nkw = a.ph_nkw[un.ph];
+      for (int g = 0; g < (nkh + 1) / 2; ++g) {
+        const int ri = 2 * g + i_atom;
+        const int kh = ri < nkh ? a.ph_kh[un.ph][ri] : -1;
+        for (int cc = h; cc < 4 * nkw; cc += 2) {  // 16-column chunks
           uint32_t v[16];
-          ptx::tmem_ld_16(tmem + lane_base + uint32_t(g * a.KW * 64 + cc * 16), v);
+          ptx::tmem_ld_16(tmem + lane_base + uint32_t(g * a.KWP * 64 + cc * 16), v);
           ptx::tmem_ld_wait();
-          const int kw = a.KW - 1 - (cc >> 2);
+          const int kw = a.ph_kw[un.ph][nkw - 1 - (cc >> 2)];
           const int co0 = cob * 64 + (cc & 3) * 16;
-          if (kh < a.KH && ci < a.Cin) {
+          if (kh >= 0 && ci < a.Cin) {
             float* dst = wsc + (((size_t(co0) * a.KD + un.kd) * a.KH + kh) * a.KW + kw) * a.Cin + ci;
             const int nco = min(16, a.Cout - co0);
 #pragma unroll
@@ -442,20 +476,60 @@ struct TcPlan {
 };
 
 bool plan(const Problem& p, int sms, TcPlan& pl) {
-  if (!(p.bf16 && p.nhwc && p.G == 1 && p.SH == 1 && p.SW == 1)) return false;
+  if (!(p.bf16 && p.nhwc && p.G == 1)) return false;
+  // An H/W stride splits x into stride phases: phase (ah, aw) is the strided view of x rows
+  // ah (mod SH), columns aw (mod SW), and the kernel rows kh with kh*DH - PH = ah (mod SH) (columns
+  // alike) reach it, DH / gcd(DH, SH) phase rows apart.  Each phase is a unit-stride weight gradient
+  // over its own taps; strides up to 4 (the x view's element strides).
+  if (p.SH > 4 || p.SW > 4) return false;
   // a real depth axis: any depth stride (a unit's x slice is a fixed function of the dy slice)
   const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
   if (p.Cin % 8 != 0 || p.Cout % 8 != 0) return false;  // 16-byte TMA strides
-  if (p.KW > 4 || (p.KW - 1) * p.DW > kFront) return false;
-  const int gm = int((p.KH + 1) / 2);
-  if (gm > 2 || gm * p.KW * 64 > 512) return false;  // the accumulators must fit TMEM
-  const int64_t P = p.OW + (p.KW - 1) * p.DW;
-  if (P > 256) return false;  // TMA box extent
-  if (p.DH * P * 128 >= (int64_t(1) << 18)) return false;  // the A atom stride must fit its descriptor field
+  const int SH = int(p.SH), SW = int(p.SW);
+  const int ddr = int(p.DH) / gcd(int(p.DH), SH), ddc = int(p.DW) / gcd(int(p.DW), SW);
   pl = TcPlan{};
   TcArgs& a = pl.a;
+  int nph = 0, kwp = 0, gm = 0;
+  for (int ah = 0; ah < SH; ++ah)
+    for (int aw = 0; aw < SW; ++aw) {
+      int khs[4], kws[4], nkh = 0, nkw = 0;
+      for (int kh = 0; kh < p.KH; ++kh)
+        if (((int(kh * p.DH - p.PH) - ah) % SH + SH) % SH == 0) {
+          if (nkh == 4) return false;  // at most two MMA groups of two kernel rows
+          khs[nkh++] = kh;
+        }
+      for (int kw = 0; kw < p.KW; ++kw)
+        if (((int(kw * p.DW - p.PW) - aw) % SW + SW) % SW == 0) {
+          if (nkw == 4) return false;  // at most four 64-wide kernel-column atoms in N
+          kws[nkw++] = kw;
+        }
+      if (nkh == 0 || nkw == 0) continue;  // no tap reads this phase
+      for (int i = 0; i < 4; ++i) {
+        a.ph_kh[nph][i] = int8_t(i < nkh ? khs[i] : -1);
+        a.ph_kw[nph][i] = int8_t(i < nkw ? kws[i] : -1);
+      }
+      a.ph_nkh[nph] = int8_t(nkh);
+      a.ph_nkw[nph] = int8_t(nkw);
+      // virtual (0, 0) of the phase grid: the x position its first kernel row and column read
+      a.ph_r0[nph] = int(khs[0] * p.DH - p.PH);
+      a.ph_c0[nph] = int(kws[0] * p.DW - p.PW);
+      // A and B both MN-major (transpose bits 15 and 16), M = 128, N = 64 per kernel column
+      a.ph_idesc[nph] = ptx::idesc_bf16_f32(128, 64 * nkw) | (1u << 15) | (1u << 16);
+      kwp = std::max(kwp, nkw);
+      gm = std::max(gm, (nkh + 1) / 2);
+      ++nph;
+    }
+  if (nph == 0) return false;
+  if ((kwp - 1) * ddc > kFront) return false;        // the dy atoms reach back at most kFront positions
+  if (gm * kwp * 64 > 512) return false;             // the accumulators must fit TMEM
+  const int64_t P = p.OW + (kwp - 1) * ddc;
+  if (P * SW > 256) return false;                    // TMA box extent (a strided view spans SW x P columns)
+  if (int64_t(ddr) * P * 128 >= (int64_t(1) << 18)) return false;  // the A atom stride must fit its field
   a.Cin = int(p.Cin); a.Cout = int(p.Cout); a.KH = int(p.KH); a.KW = int(p.KW);
   a.DH = int(p.DH); a.DW = int(p.DW); a.PH = int(p.PH); a.PW = int(p.PW);
+  a.SH = SH; a.SW = SW; a.ddr = ddr; a.ddc = ddc;
+  a.nph = nph;
+  a.KWP = kwp;
   a.KD = deep ? int(p.KD) : 1;
   a.SD = deep ? int(p.SD) : 1;
   a.DD = deep ? int(p.DD) : 1;
@@ -463,13 +537,14 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   a.OD = deep ? int(p.OD) : 0;
   a.P = int(P);
   a.RB = 8 / gcd(int(P), 8);
+  if (a.RB * SH > 256) return false;  // TMA box extent of the strided x rows
   a.box_bytes = a.RB * a.P * 128;
   a.gm = gm;
   // x rows past a segment's dy rows that its last MMAs read: the second atom of the last group
-  // reaches (2*gm - 1)*DH rows down, the dy atoms (KW-1)*DW positions and a 16-position step on.
-  const int64_t reach = int64_t(2 * gm - 1) * p.DH * P + (p.KW - 1) * p.DW + 16;
+  // reaches (2*gm - 1)*ddr rows down, the dy atoms (KWP-1)*ddc positions and a 16-position step on.
+  const int64_t reach = int64_t(2 * gm - 1) * ddr * P + (kwp - 1) * ddc + 16;
   a.xe = int((reach + a.RB * P - 1) / (a.RB * P));
-  a.tail = int((p.KW - 1) * p.DW + 16);
+  a.tail = int((kwp - 1) * ddc + 16);
   a.seg_blocks = 0;
   for (int sb = kMaxBoxes - a.xe; sb >= 1; --sb) {
     const int64_t xb = int64_t(sb + a.xe) * a.box_bytes;
@@ -491,22 +566,23 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   a.cb_in = int((p.Cin + 63) / 64);
   const int cb_out = int((p.Cout + 63) / 64);
   a.pairs = a.cb_in * cb_out;
-  // one unit per SM: chunks x pairs x kernel-depth taps (a 3-D chunk is swept once per depth tap)
-  a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / (a.pairs * a.KD))));
-  const int64_t units = int64_t(a.pairs) * a.chunks * a.KD;
+  // one unit per SM: chunks x pairs x kernel-depth taps x stride phases (a chunk is swept once per
+  // depth tap and phase)
+  a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / (a.pairs * a.KD * nph))));
+  const int64_t units = int64_t(a.pairs) * a.chunks * a.KD * nph;
   if (units >= (int64_t(1) << 30)) return false;
   a.units = int(units);
   pl.grid = std::max(1, std::min(a.units, sms));
-  // A and B both MN-major (transpose bits 15 and 16), M = 128, N = 64 per kernel column
-  a.idesc = ptx::idesc_bf16_f32(128, 64 * a.KW) | (1u << 15) | (1u << 16);
   pl.N = int(p.N); pl.H = int(p.H); pl.W = int(p.W); pl.OH = int(p.OH); pl.OW = int(p.OW);
   pl.D = deep ? int(p.D) : 0;
   pl.OD = deep ? int(p.OD) : 0;
   return true;
 }
 
-// One activation map: (C, W, H, N), or (C, W, H, D, N) when depth > 0; boxes of 64 channels x P x RB rows.
-bool encode_one(CUtensorMap* map, const void* base, int C, int W, int H, int depth, int N, const TcArgs& a) {
+// One activation map: (C, W, H, N), or (C, W, H, D, N) when depth > 0; boxes of 64 channels x P x RB
+// rows, read every sw-th column and sh-th row (element strides: the box spans sw*P columns, sh*RB rows).
+bool encode_one(CUtensorMap* map, const void* base, int C, int W, int H, int depth, int N, int sw, int sh,
+                const TcArgs& a) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t rank = depth > 0 ? 5 : 4;
@@ -518,8 +594,8 @@ bool encode_one(CUtensorMap* map, const void* base, int C, int W, int H, int dep
     dims[4] = cuuint64_t(N);
     strides[3] = plane * cuuint64_t(depth);
   }
-  const cuuint32_t box[5] = {64, cuuint32_t(a.P), cuuint32_t(a.RB), 1, 1};
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const cuuint32_t box[5] = {64, cuuint32_t(a.P * sw), cuuint32_t(a.RB * sh), 1, 1};
+  const cuuint32_t estr[5] = {1, cuuint32_t(sw), cuuint32_t(sh), 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -527,8 +603,8 @@ bool encode_one(CUtensorMap* map, const void* base, int C, int W, int H, int dep
 
 bool encode(const TcPlan& pl, const void* x, const void* dy, TcMaps& maps) {
   const TcArgs& a = pl.a;
-  return encode_one(&maps.x, x, a.Cin, pl.W, pl.H, pl.D, pl.N, a) &&
-         encode_one(&maps.dy, dy, a.Cout, pl.OW, pl.OH, pl.OD, pl.N, a);
+  return encode_one(&maps.x, x, a.Cin, pl.W, pl.H, pl.D, pl.N, a.SW, a.SH, a) &&
+         encode_one(&maps.dy, dy, a.Cout, pl.OW, pl.OH, pl.OD, pl.N, 1, 1, a);
 }
 
 }  // namespace
@@ -550,8 +626,9 @@ bool wgrad_tc_describe(const Problem& p, char* buf, size_t len) {
   const TcArgs& a = pl.a;
   std::snprintf(buf, len,
                 "wgrad_tc pairs=%d chunks=%d units=%d grid=%d rows_per_box=%d pitch=%d seg_blocks=%d x_extra=%d "
-                "groups=%d n=%d depth_taps=%d smem=%zu",
-                a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KW, a.KD, pl.smem);
+                "groups=%d n=%d depth_taps=%d phases=%d smem=%zu",
+                a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KWP, a.KD, a.nph,
+                pl.smem);
   return true;
 }
 

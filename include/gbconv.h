@@ -80,7 +80,7 @@ typedef enum {
   GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
   GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
   GBCONV_K_WGRAD = 8           /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction
-                                  (3-D: one kernel-depth tap per work unit) */
+                                  (H/W strides: one stride phase per work unit; 3-D: one kernel-depth tap per unit) */
 } gbconv_kernel;
 
 typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER = 2 } gbconv_op;

@@ -96,6 +96,12 @@ EXTRA_WORKLOADS = [
              (1, 1, 1), (1, 1, 1), (1, 1, 1), 1, False, (2, 16, 56, 56, 64), (64, 3, 3, 3, 64), (2, 16, 56, 56, 64),
              {"x": ("normal", 1.0), "g": ("normal", 1.0)},
              "conv3d backward-filter NDHWC bf16, 3x3x3 stride 1 pad 1, x and dy 2x16x56x56x64 -> dW 64x3x3x3x64"),
+    # the weight gradient of the strided dense workload (ResNet-style downsampling): dW [128, 3, 3, 128]
+    # from x 32x56x56x128 and dy 32x28x28x128
+    Workload("wgrad3x3_s2_nhwc_bf16", 11, "wgrad", "bf16", 2, "nhwc", "ohwi", 32, 128, 128, (56, 56), (3, 3), (2, 2),
+             (1, 1), (1, 1), 1, False, (32, 56, 56, 128), (128, 3, 3, 128), (32, 28, 28, 128),
+             {"x": ("normal", 1.0), "g": ("normal", 1.0)},
+             "conv2d backward-filter NHWC bf16, 3x3 stride 2 pad 1, x 32x56x56x128, dy 32x28x28x128 -> dW 128x3x3x128"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

@@ -115,6 +115,7 @@ EXPECTED_FAMILY = {
     "dense3x3x3_ndhwc_bf16": {"implicit"},
     "dgrad3x3x3_ndhwc_bf16": {"dgrad"},
     "wgrad3x3x3_ndhwc_bf16": {"wgrad"},
+    "wgrad3x3_s2_nhwc_bf16": {"wgrad"},
 }
 
 OPS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
@@ -289,7 +290,8 @@ def test_conv3d_shapes_and_families(gb):
     _, _, f = _plan(gb, s3(n=2, in_size=(16, 56, 56), c_in=64, c_out=64), op=2)
     assert f["depth_taps"] == "3" and int(f["units"]) == 3 * int(f["chunks"]) and int(f["units"]) <= 152
     assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(2, 1, 1))), 2) == "wgrad"
-    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(1, 2, 2))), 2) == "direct_wgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, stride=(1, 2, 2))), 2) == "wgrad"
+    assert gb.gbconv_select(lib_desc(gb, s3(c_in=64, c_out=64, layout="ncdhw", wlayout="oidhw")), 2) == "direct_wgrad"
     flat = dict(k=(1, 3, 3), pad=(0, 1, 1), c_in=64, c_out=64)
     assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 0) == "implicit"
     assert gb.gbconv_select(lib_desc(gb, s3(**flat)), 1) == "dgrad"

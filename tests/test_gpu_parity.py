@@ -529,9 +529,22 @@ WGRAD = [
     (shape_kw(n=3, in_size=(10, 12), c_in=16, c_out=8, wlayout="oihw", dtype="f32", stride=(2, 2)), "direct_wgrad"),
     (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "direct_wgrad"),
     (shape_kw(n=1, in_size=(9, 8), c_in=16, c_out=8, layout="nchw", wlayout="oihw", stride=(2, 2)), "direct_wgrad"),
-    # NHWC bf16 that the tensor-core path declines: 1x1 at stride 2, a 5-wide kernel
-    (shape_kw(n=2, in_size=(15, 14), c_in=32, c_out=48, k=(1, 1), pad=(0, 0), stride=(2, 2)), "direct_wgrad"),
+    # NHWC bf16 that the tensor-core path declines: a 5-wide kernel, five kernel rows in one stride phase
     (shape_kw(n=1, in_size=(13, 12), c_in=16, c_out=24, k=(5, 5), pad=(2, 2), dil=(1, 2)), "direct_wgrad"),
+    (shape_kw(n=1, in_size=(15, 14), c_in=16, c_out=24, k=(5, 3), pad=(4, 1), dil=(2, 1), stride=(2, 1)),
+     "direct_wgrad"),
+    # tensor-core path at H/W strides: one unit per stride phase, x through a strided view.  1x1 s2;
+    # 3x3 s2 with odd extents; 7x7 s2 (four phases of up to four kernel rows, input-channel tail);
+    # (2, 1) strides; stride 3 (nine one-tap phases); dilation 2 at stride 2 (every kernel row in one
+    # phase); (begin, end) padding at stride 2; 3-D at H/W stride 2
+    (shape_kw(n=2, in_size=(15, 14), c_in=32, c_out=48, k=(1, 1), pad=(0, 0), stride=(2, 2)), "wgrad"),
+    (shape_kw(n=2, in_size=(15, 14), c_in=64, c_out=128, k=(3, 3), pad=(1, 1), stride=(2, 2)), "wgrad"),
+    (shape_kw(n=1, in_size=(21, 20), c_in=24, c_out=64, k=(7, 7), pad=(3, 3), stride=(2, 2)), "wgrad"),
+    (shape_kw(n=2, in_size=(12, 11), c_in=64, c_out=64, k=(3, 3), pad=(1, 1), stride=(2, 1)), "wgrad"),
+    (shape_kw(n=2, in_size=(13, 14), c_in=64, c_out=64, k=(3, 3), pad=(1, 1), stride=(3, 3)), "wgrad"),
+    (shape_kw(n=2, in_size=(16, 15), c_in=64, c_out=64, k=(3, 3), pad=(2, 2), dil=(2, 2), stride=(2, 2)), "wgrad"),
+    (shape_kw(n=2, in_size=(14, 13), c_in=64, c_out=64, k=(3, 3), pad=(1, 0), pad_end=(0, 1), stride=(2, 2)),
+     "wgrad"),
     # tensor-core path: 3x3 over several chunks; channel tails and four block pairs; 2x2 without
     # padding; 1x1 (one kernel row: the second M atom unused); 3x1; dilation 2; conv1d NLC; 16 channels
     (shape_kw(n=4, in_size=(20, 21), c_in=64, c_out=64, k=(3, 3), pad=(1, 1)), "wgrad"),
@@ -547,7 +560,7 @@ WGRAD = [
     (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "wgrad"),
     (shape_kw(n=2, in_size=(9, 10), c_in=6, c_out=9, groups=3, stride=(2, 1), pad=(1, 0), pad_end=(0, 1),
               layout="nchw", wlayout="oihw", dtype="f32"), "direct_wgrad"),
-    # 3-D: the generic path (fp32 NCDHW with groups; an H/W stride), and the tensor-core path, one
+    # 3-D: the generic path (fp32 NCDHW with groups), and the tensor-core path (an H/W stride too), one
     # kernel-depth tap per unit over (batch, depth) slices: depth strides (with depth dilation and
     # (begin, end) depth padding); 3x3x3; depth dilation with (begin, end) depth padding and 128
     # output channels; a depth-2 kernel over six block pairs; a depth-1 kernel with depth padding;
@@ -555,7 +568,7 @@ WGRAD = [
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 7), c_in=4, c_out=6, groups=2, k=(3, 2, 3), stride=(2, 1, 2),
               pad=(1, 0, 1), dil=(1, 2, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "direct_wgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 2, 2),
-              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "direct_wgrad"),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(5, 6, 7), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "wgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(7, 6, 5), c_in=64, c_out=64, k=(3, 3, 3), stride=(2, 1, 1),
