@@ -1,5 +1,5 @@
 // Weight gradient on the 5th-generation tensor cores (tcgen05, accumulators in TMEM), NHWC bf16,
-// unit stride, one group.
+// one group, H/W strides up to 4 (described below at unit stride first).
 //
 // The contraction (burn-cubecl `wgrad_im2col`: [C_out, positions] x [positions, taps * C_in]) runs
 // over positions of the same virtual grid the forward uses: R output rows of P = OW + (KW-1)*DW
@@ -23,6 +23,12 @@
 // barrier each) and swept by the MMAs as the boxes land.  At the end the accumulators go to the
 // caller's workspace as fp32 partial sums [chunk][co][kh][kw][ci]; launch_wgrad_reduce then adds the
 // chunks in chunk order.  No atomics anywhere: the result is deterministic.
+//
+// An H/W stride (SH, SW) splits x into stride phases: phase (ah, aw) is x at rows ah (mod SH) and
+// columns aw (mod SW), read as a dense grid through a strided TMA view.  Tap (kh, kw) reads phase
+// ((kh*DH - PH) mod SH, (kw*DW - PW) mod SW), and the taps of one phase sit DH / gcd(DH, SH) phase
+// rows (and DW / gcd(DW, SW) phase columns) apart, so each phase is the unit-stride sum above over
+// its own taps, with its own N.  A work unit takes one phase and writes only that phase's taps.
 //
 // A 3-D shape runs the same sums over (batch, output depth) slices, one kernel-depth tap kd per
 // unit: the unit pairs dy slice od with x slice od*SD + kd*DD - PD (5-D boxes, zero filled outside
