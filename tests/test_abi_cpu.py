@@ -213,6 +213,34 @@ def test_bwd_filter_workspace_and_argument_checks(gb):
     assert gb._lib.gbconv_select(ctypes.byref(d), 3, ctypes.byref(k)) == gb.GBCONV_EINVAL
 
 
+def test_describe_weight_gradient_stride_phases(gb):
+    # a unit per (chunk, block pair, stride phase); each phase the unit-stride sum over its own taps
+    _, _, f = _plan(gb, shape_kw(n=32, in_size=(56, 56), c_in=64, c_out=64), op=2)
+    assert f["phases"] == "1" and f["groups"] == "2" and f["n"] == "192" and f["pitch"] == "58"
+    # 3x3 stride 2: phases {1} x {1}, {1} x {0, 2}, {0, 2} x {1}, {0, 2} x {0, 2}; the pitch is OW + 1
+    _, _, f = _plan(gb, shape_kw(n=32, in_size=(56, 56), c_in=128, c_out=128, stride=(2, 2)), op=2)
+    assert f["phases"] == "4" and f["groups"] == "1" and f["n"] == "128" and f["pitch"] == "29"
+    assert int(f["units"]) == 4 * 4 * int(f["chunks"]) and int(f["units"]) <= 152
+    # 7x7 stride 2: four kernel rows and columns in the (0, 0) phase -> two groups, N = 256
+    _, _, f = _plan(gb, shape_kw(n=8, in_size=(112, 112), c_in=64, c_out=64, k=(7, 7), pad=(3, 3), stride=(2, 2)), op=2)
+    assert f["phases"] == "4" and f["groups"] == "2" and f["n"] == "256"
+    # 1x1 stride 2: one phase, one tap
+    _, _, f = _plan(gb, shape_kw(n=4, in_size=(28, 28), c_in=64, c_out=64, k=(1, 1), pad=(0, 0), stride=(2, 2)), op=2)
+    assert f["phases"] == "1" and f["groups"] == "1" and f["n"] == "64"
+    # 3x3 stride 3: nine one-tap phases; 2x2 stride 4: a phase per tap, twelve phases empty
+    _, _, f = _plan(gb, shape_kw(n=4, in_size=(30, 30), c_in=64, c_out=64, stride=(3, 3)), op=2)
+    assert f["phases"] == "9" and f["n"] == "64"
+    _, _, f = _plan(gb, shape_kw(n=4, in_size=(32, 32), c_in=64, c_out=64, k=(2, 2), pad=(0, 0), stride=(4, 4)), op=2)
+    assert f["phases"] == "4"
+    # dilation 2 at stride 2: every kernel row in one phase, consecutive phase rows
+    _, _, f = _plan(gb, shape_kw(n=4, in_size=(30, 30), c_in=64, c_out=64, pad=(2, 2), dil=(2, 2), stride=(2, 2)), op=2)
+    assert f["phases"] == "1" and f["groups"] == "2" and f["n"] == "192"
+    # five kernel rows in one phase, or a stride above 4: the generic kernel
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(k=(5, 3), pad=(4, 1), dil=(2, 1), stride=(2, 1),
+                                                  c_in=64, c_out=64)), 2) == "direct_wgrad"
+    assert gb.gbconv_select(lib_desc(gb, shape_kw(in_size=(30, 30), stride=(5, 5), c_in=64, c_out=64)), 2) == "direct_wgrad"
+
+
 def test_begin_end_padding_shapes_and_families(gb):
     # out = (in + begin + end - eff) // stride + 1 per axis, as the oracle computes it
     cases = [shape_kw(in_size=(7, 8), k=(3, 3), stride=(2, 2), pad=(0, 1), pad_end=(1, 0)),
