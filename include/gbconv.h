@@ -120,7 +120,9 @@ gbconv_status gbconv_select(const gbconv_desc *desc, int32_t op, int32_t *kernel
 
 /* A one-line description of the plan that would serve `op` for this descriptor (pointers assumed
  * 16-byte aligned): the kernel family, and for the tensor-core implicit GEMM its tile width, work
- * items, stride phases, activation sources, taps, weight residency, pipeline depth and shared memory.
+ * items, stride phases, activation sources, taps, weight residency, pipeline depth and shared memory;
+ * for the tensor-core weight gradient its block pairs, chunks, work units, box rows, pitch, MMA groups
+ * and width, kernel-depth taps, stride phases and shared memory.
  * Writes at most `len` bytes including the terminating NUL into the caller's host buffer `buf`
  * (truncating if needed).  Launches nothing and needs no GPU.
  * Returns GBCONV_EINVAL for a NULL argument, len < 1, an unknown op, or a shape the call would reject. */
