@@ -30,7 +30,7 @@ KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad
 GBCONV_OP_FWD, GBCONV_OP_BWD_DATA, GBCONV_OP_BWD_FILTER = 0, 1, 2
 
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
-           "gbconv_bwd_filter_workspace", "gbconv_bwd_filter",
+           "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_bwd_filter_noalloc",
            "gbconv_pack_weight", "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
 
 
@@ -64,10 +64,12 @@ def _load():
     lib.gbconv_conv_transpose.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_bwd_filter_workspace.argtypes = [P(Desc), P(ctypes.c_int64)]
     lib.gbconv_bwd_filter.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_int64, vp]
+    lib.gbconv_bwd_filter_noalloc.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
     lib.gbconv_device_status.argtypes = [vp]
     for f in ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_conv_transpose", "gbconv_fwd",
-              "gbconv_bwd_data", "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_pack_weight",
+              "gbconv_bwd_data", "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_bwd_filter_noalloc",
+              "gbconv_pack_weight",
               "gbconv_device_status"):
         getattr(lib, f).restype = st
     lib.gbconv_kernels_launched.argtypes = []
@@ -133,6 +135,16 @@ def gbconv_bwd_filter(desc: Desc, x: int, dy: int, dw: int, db: int | None, work
                       workspace_bytes: int, stream: int) -> int:
     return _lib.gbconv_bwd_filter(ctypes.byref(desc), x, dy, dw, db or None, workspace or None, workspace_bytes,
                                   stream or None)
+
+
+# Size of the library's static scratch array (GBCONV_NOALLOC_WORKSPACE_BYTES in include/gbconv.h).
+NOALLOC_WORKSPACE_BYTES = 32 << 20
+
+
+def gbconv_bwd_filter_noalloc(desc: Desc, x: int, dy: int, dw: int, db: int | None, stream: int) -> int:
+    """The weight gradient on the library's own static scratch array, for callers that cannot
+    allocate device memory (no workspace argument; see include/gbconv.h)."""
+    return _lib.gbconv_bwd_filter_noalloc(ctypes.byref(desc), x, dy, dw, db or None, stream or None)
 
 
 def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int:

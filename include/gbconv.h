@@ -179,6 +179,32 @@ gbconv_status gbconv_bwd_filter_workspace(const gbconv_desc *desc, int64_t *byte
 gbconv_status gbconv_bwd_filter(const gbconv_desc *desc, const void *x, const void *dy, void *dw, float *db,
                                 void *workspace, int64_t workspace_bytes, void *stream);
 
+/* Size of the scratch array gbconv_bwd_filter_noalloc uses: 32 MiB. */
+#define GBCONV_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+/* Weight gradient without any device allocation, for callers that cannot allocate device memory
+ * (for example code that runs inside an allocator's own callbacks, a plugin that is handed only its
+ * tensors, or an application that reserves all device memory up front and forbids further
+ * allocations), and so cannot supply the workspace gbconv_bwd_filter asks for.  The source pages have
+ * no counterpart: their weight gradients either accumulate with atomics or allocate their own buffers.
+ *
+ * Same arguments, results and determinism as gbconv_bwd_filter, minus the workspace: the partial sums
+ * go to a fixed array of GBCONV_NOALLOC_WORKSPACE_BYTES in device global memory that the library
+ * declares statically.  Every GPU that loads the library holds that array until the process exits.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Returns GBCONV_EUNSUPPORTED when gbconv_bwd_filter_workspace(desc) exceeds
+ *    GBCONV_NOALLOC_WORKSPACE_BYTES (use gbconv_bwd_filter with your own workspace then), and
+ *    GBCONV_EINVAL for NULL tensors or a shape the forward would reject.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ *    that device current) and caches it; make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's contents (nothing has
+ *    to start at zero: each call writes every partial sum before reading it).  Calls whose kernels
+ *    overlap on the GPU (other streams, other host threads) race on the array and give wrong results:
+ *    order them on one stream or synchronise between them.
+ * Enqueues the same kernels as gbconv_bwd_filter on `stream`. */
+gbconv_status gbconv_bwd_filter_noalloc(const gbconv_desc *desc, const void *x, const void *dy, void *dw, float *db,
+                                        void *stream);
+
 /* Re-lays a weight from [C_out, C_in/G, KH, KW] (OIHW) into [C_out, KH, KW, C_in/G] (OHWI), the order the
  * NHWC tensor-core kernels read.  desc->dtype gives the element type; desc->wlayout is ignored.
  * w_oihw and w_ohwi are device pointers that must not overlap.  Enqueues one kernel. */
