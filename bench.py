@@ -158,23 +158,72 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
-def traffic_record(kernel_file: str, workload: str):
-    """DRAM bytes per launch of a workload's kernel from the committed ncu summary, if the kernel
-    source is unchanged since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def source_digest(kernel_file: str) -> str:
     src = os.path.join(ROOT, "convolution_conv_fwd_gb300", "csrc", kernel_file)
-    if not (os.path.exists(path) and os.path.exists(src)):
-        return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    for line in open(path):
-        # | workload | kernel file | source sha256[:16] | dram bytes per launch | ...
-        parts = [p.strip() for p in line.split("|")]
-        if len(parts) > 5 and parts[1] == workload and parts[2] == kernel_file and parts[3] == digest:
-            try:
-                return float(parts[4])
-            except ValueError:
-                return None
-    return None
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def traffic_record(kernel_file: str, workload: str):
+    """(DRAM bytes per launch, note) of a workload's kernel from profiles/traffic.json, which only
+    ``--record-traffic`` writes (from an ncu capture).  The bytes are None, with the reason in the
+    note, when there is no record or the kernel source changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_JSON):
+        return None, "no ncu traffic record"
+    rec = json.load(open(TRAFFIC_JSON)).get(workload)
+    if rec is None or rec.get("kernel_file") != kernel_file:
+        return None, "no ncu traffic record for this workload"
+    if rec.get("source_sha16") != source_digest(kernel_file):
+        return None, "kernel source changed since the ncu capture (%s)" % rec.get("source_sha16")
+    return float(rec["dram_bytes_per_launch"]), "ncu capture at source %s" % rec["source_sha16"]
+
+
+_NCU_UNITS = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+
+
+def ncu_dram_bytes(csv_path: str, kernel_regex: str):
+    """Mean dram__bytes_read.sum + dram__bytes_write.sum per captured launch of kernels matching
+    kernel_regex, from an ``ncu --metrics ... --csv --log-file`` file."""
+    import csv
+    import re
+    per = {}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        name = row.get("Metric Name", "")
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        if not re.search(kernel_regex, row.get("Kernel Name", "")):
+            continue
+        scale = _NCU_UNITS.get(row.get("Metric Unit", "byte").strip().lower())
+        if scale is None:
+            raise ValueError("unknown ncu unit %r" % row.get("Metric Unit"))
+        val = float(row["Metric Value"].replace(",", "")) * scale
+        per[row["ID"]] = per.get(row["ID"], 0.0) + val
+    if not per:
+        raise ValueError("no DRAM byte counters for kernels matching %r in %s" % (kernel_regex, csv_path))
+    return sum(per.values()) / len(per), len(per)
+
+
+def record_traffic(csv_path: str, workload: str, kernel_regex: str, command: str):
+    """Write one workload's DRAM traffic per launch into profiles/traffic.json (machine-written;
+    keyed by the workload and the hash of its kernel's source at the time of the capture)."""
+    from synth.workloads import BY_NAME
+    import convolution_conv_fwd_gb300 as gb
+    wl = BY_NAME[workload]
+    op = {"fwd": gb.GBCONV_OP_FWD, "dgrad": gb.GBCONV_OP_BWD_DATA, "wgrad": gb.GBCONV_OP_BWD_FILTER}[wl.op]
+    kfile = KERNEL_FILE[gb.gbconv_select(desc_for(gb, wl), op)]
+    nbytes, launches = ncu_dram_bytes(csv_path, kernel_regex)
+    data = json.load(open(TRAFFIC_JSON)) if os.path.exists(TRAFFIC_JSON) else {}
+    data[workload] = {"kernel_file": kfile, "source_sha16": source_digest(kfile), "kernel_regex": kernel_regex,
+                      "dram_bytes_per_launch": round(nbytes), "launches_captured": launches,
+                      "algorithmic_bytes": work(wl)[1], "command": command}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({workload: data[workload]}))
 
 
 KERNEL_FILE = {"direct": "direct.cu", "depthwise": "depthwise.cu", "pointwise": "pointwise.cu",
@@ -353,8 +402,9 @@ def run_gpu(args, rank, world, local_rank):
         achieved, peak, unit = dc["bytes"] / (dms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = dc["flops"] / (dms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    traffic, traffic_note = traffic_record(KERNEL_FILE[dc["family"]], dc["wl"].name)
     roof = {"bound": per[dom]["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic_record(KERNEL_FILE[dc["family"]], dc["wl"].name),
+            "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
             "kernel": dc["family"], "workload": dc["wl"].name,
             "algorithmic_bytes": dc["bytes"], "algorithmic_flops": dc["flops"],
             "peak_source": pk["source"] + " (burst)"}
@@ -368,7 +418,9 @@ def run_gpu(args, rank, world, local_rank):
                          "> 2.5x L2, so every launch reads its inputs from HBM",
                    "launch": "back-to-back on one stream, programmatic dependent launch; events between workload groups",
                    "inputs": "seeded SplitMix64/Box-Muller, bf16 RNE; conv1d workload fp32",
-                   "step_roofline_frac": round(sum(p["t_roof_us"] for p in per) / (step_ms * 1e3), 4),
+                   # every launch of the step at its roofline time, over the measured step time
+                   "step_roofline_frac": round(sum(p["t_roof_us"] * p["launches_per_step"] for p in per)
+                                               / (step_ms * 1e3), 4),
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "per_config": per,
         "extra_configs": extra,
@@ -519,7 +571,13 @@ def main():
     ap.add_argument("--ref-seconds-per-step", type=float, default=3.0)
     ap.add_argument("--profile-workload", default=None,
                     help="run only this workload --steps times through the C ABI and exit (for ncu captures)")
+    ap.add_argument("--record-traffic", nargs=4, metavar=("NCU_CSV", "WORKLOAD", "KERNEL_REGEX", "COMMAND"),
+                    help="write the workload's DRAM bytes per launch from an ncu --metrics "
+                         "dram__bytes_read.sum,dram__bytes_write.sum --csv log into profiles/traffic.json")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+        return
     if args.profile_workload:
         profile_workload(args.profile_workload, args.steps)
         return

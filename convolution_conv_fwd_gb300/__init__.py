@@ -26,7 +26,7 @@ GBCONV_F32, GBCONV_BF16 = 0, 1
 GBCONV_PAD_SYMMETRIC, GBCONV_PAD_BEGIN_END = 0, 1
 # kernel families
 KERNELS = {0: "direct", 1: "depthwise", 2: "pointwise", 3: "implicit", 4: "dgrad", 5: "direct_dgrad",
-           6: "depthwise_dgrad", 7: "direct_wgrad", 8: "wgrad"}
+           6: "depthwise_dgrad", 7: "direct_wgrad", 8: "wgrad", 9: "smallgroup", 10: "smallgroup_dgrad"}
 GBCONV_OP_FWD, GBCONV_OP_BWD_DATA, GBCONV_OP_BWD_FILTER = 0, 1, 2
 
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
@@ -226,12 +226,27 @@ def _torch():
 
 
 def _check(t, shape, dtype, name):
-    torch = _torch()
     if tuple(t.shape) != tuple(shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
     if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
     return t
+
+
+def _one_device(**tensors):
+    """The one CUDA device every given tensor (None entries skipped) lives on.  The C ABI launches on
+    the current device with device pointers, so tensors on different GPUs are refused here and the
+    wrappers make this device current for the call."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("%s is on %s, but the other tensors are on %s: one call takes one device"
+                             % (name, t.device, dev))
+    return dev
 
 
 def _dtype(d: Desc):
@@ -350,8 +365,10 @@ def conv_fwd(d: Desc, x, w, bias=None, y=None):
         _check(bias, (d.c_out,), torch.float32, "bias")
     out = y if y is not None else torch.empty(ys, dtype=dt, device=x.device)
     _check(out, ys, dt, "y")
-    s = gbconv_fwd(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
-                   torch.cuda.current_stream().cuda_stream)
+    dev = _one_device(x=x, w=w, bias=bias, y=out)
+    with torch.cuda.device(dev):
+        s = gbconv_fwd(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
+                       torch.cuda.current_stream(dev).cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_fwd")
     return out
@@ -376,7 +393,9 @@ def conv_bwd_data(d: Desc, dy, w, dx=None):
     _check(w, ws, dt, "w")
     out = dx if dx is not None else torch.empty(xs, dtype=dt, device=dy.device)
     _check(out, xs, dt, "dx")
-    s = gbconv_bwd_data(d, dy.data_ptr(), w.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    dev = _one_device(dy=dy, w=w, dx=out)
+    with torch.cuda.device(dev):
+        s = gbconv_bwd_data(d, dy.data_ptr(), w.data_ptr(), out.data_ptr(), torch.cuda.current_stream(dev).cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_bwd_data")
     return out
@@ -402,13 +421,16 @@ def conv_bwd_filter(d: Desc, x, dy, dw=None, db=None, workspace=None, want_db=Fa
     if want_db:
         db = db if db is not None else torch.empty((d.c_out,), dtype=torch.float32, device=x.device)
         _check(db, (d.c_out,), torch.float32, "db")
-    need = gbconv_bwd_filter_workspace(d)
-    if workspace is None:
-        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
-    if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
-        raise ValueError("workspace must be a CUDA uint8 tensor of at least %d bytes" % need)
-    s = gbconv_bwd_filter(d, x.data_ptr(), dy.data_ptr(), out.data_ptr(), db.data_ptr() if want_db else None,
-                          workspace.data_ptr(), workspace.numel(), torch.cuda.current_stream().cuda_stream)
+    dev = _one_device(x=x, dy=dy, dw=out, db=db if want_db else None, workspace=workspace)
+    with torch.cuda.device(dev):
+        # the workspace size follows the SM count of the device the call runs on
+        need = gbconv_bwd_filter_workspace(d)
+        if workspace is None:
+            workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
+            raise ValueError("workspace must be a CUDA uint8 tensor of at least %d bytes" % need)
+        s = gbconv_bwd_filter(d, x.data_ptr(), dy.data_ptr(), out.data_ptr(), db.data_ptr() if want_db else None,
+                              workspace.data_ptr(), workspace.numel(), torch.cuda.current_stream(dev).cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_bwd_filter")
     return (out, db) if want_db else out
@@ -437,25 +459,27 @@ def conv_transpose(d: Desc, x, w, bias=None, y=None):
         _check(bias, (d.c_in,), torch.float32, "bias")
     out = y if y is not None else torch.empty(xs, dtype=dt, device=x.device)
     _check(out, xs, dt, "y")
-    s = gbconv_conv_transpose(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
-                              out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    dev = _one_device(x=x, w=w, bias=bias, y=out)
+    with torch.cuda.device(dev):
+        s = gbconv_conv_transpose(d, x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                  out.data_ptr(), torch.cuda.current_stream(dev).cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_conv_transpose")
     return out
 
 
 def pack_weight(d: Desc, w_oihw):
-    """OIHW -> OHWI copy of a weight, on the device."""
+    """OIHW -> OHWI copy of a weight, on the device ([C_out, C_in/G, K...] -> [C_out, K..., C_in/G] for
+    1-D, 2-D and 3-D descriptors)."""
     torch = _torch()
     dt = _dtype(d)
     cpg = d.c_in // d.groups
-    if d.spatial_dims == 1:
-        src_shape, dst_shape = (d.c_out, cpg, d.k[0]), (d.c_out, d.k[0], cpg)
-    else:
-        src_shape, dst_shape = (d.c_out, cpg, d.k[0], d.k[1]), (d.c_out, d.k[0], d.k[1], cpg)
+    k = tuple(int(v) for v in d.k[:d.spatial_dims])
+    src_shape, dst_shape = (d.c_out, cpg) + k, (d.c_out,) + k + (cpg,)
     _check(w_oihw, src_shape, dt, "w_oihw")
     out = torch.empty(dst_shape, dtype=dt, device=w_oihw.device)
-    s = gbconv_pack_weight(d, w_oihw.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    with torch.cuda.device(w_oihw.device):
+        s = gbconv_pack_weight(d, w_oihw.data_ptr(), out.data_ptr(), torch.cuda.current_stream(w_oihw.device).cuda_stream)
     if s != GBCONV_OK:
         raise GbconvError(s, "gbconv_pack_weight")
     return out

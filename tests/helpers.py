@@ -6,6 +6,10 @@ values from ``synth`` are shared.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import dataclasses
+import os
+
 import numpy as np
 
 import oracle
@@ -126,3 +130,75 @@ def check_bf16(got, ref, scale):
 def bf16_round(a):
     """Exact bf16 RNE rounding of float64 values that are exact in float32."""
     return synth.bf16_to_f32(synth.bf16_bits(np.asarray(a, dtype=np.float32))).astype(np.float64)
+
+
+# ---------------------------------------------------------------- whole oracle outputs on every host core
+
+def host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _pool_map(fn, items):
+    with cf.ThreadPoolExecutor(max_workers=min(len(items), host_threads())) as ex:
+        return list(ex.map(fn, items))
+
+
+def _batch_bounds(n, parts):
+    parts = max(1, min(n, parts))
+    b = [n * i // parts for i in range(parts + 1)]
+    return [(lo, hi) for lo, hi in zip(b[:-1], b[1:]) if hi > lo]
+
+
+def _points_whole(c, shape, query, parts):
+    """Every element of an NC... shaped result by point queries, the flat index range split in parts."""
+    total = int(np.prod(shape))
+    bounds = [(total * i // parts, total * (i + 1) // parts) for i in range(parts)]
+
+    def run(lohi):
+        lo, hi = lohi
+        idx = np.stack(np.unravel_index(np.arange(lo, hi, dtype=np.int64), shape), axis=1).astype(np.int64)
+        return query(idx)
+
+    return np.concatenate(_pool_map(run, bounds)).reshape(shape)
+
+
+def oracle_whole(c: oracle.Conv, op: str, a, b, bias=None):
+    """The oracle's whole result for ``op`` on the host's cores.
+
+    op 'fwd' (a = x, b = w), 'dgrad' (a = dy, b = w) or 'wgrad' (a = x, b = dy).  Images are
+    independent in the forward and input gradient, so 1-D and 2-D shapes split over batch slices
+    (each slice one oracle call); the weight gradient is the fp64 sum of its batch slices' weight
+    gradients.  3-D shapes have small batches, so they run as point queries over slices of the
+    flat output index.  Returns the array in ``c``'s layout (fwd: y, dgrad: dx, wgrad: dw)."""
+    t = host_threads()
+    if c.spatial_dims == 3:
+        parts = 4 * t
+        if op == "fwd":
+            shape = (c.n, c.c_out) + tuple(c.out_hw())
+            r = _points_whole(c, shape, lambda i: oracle.conv_fwd_points(c, a, b, bias, i), parts)
+        elif op == "dgrad":
+            shape = (c.n, c.c_in) + tuple(c.in_hw)
+            r = _points_whole(c, shape, lambda i: oracle.conv_dgrad_points(c, a, b, i), parts)
+        else:
+            shape = (c.c_out, c.c_in // c.groups) + tuple(c.k)
+            r = _points_whole(c, shape, lambda i: oracle.conv_wgrad_points(c, a, b, i), parts)
+            return r.transpose(0, 2, 3, 4, 1) if c.w_ohwi else r
+        return r.transpose(0, 2, 3, 4, 1) if c.nhwc else r
+    slices = _batch_bounds(c.n, t)
+
+    def run(lohi):
+        lo, hi = lohi
+        cs = dataclasses.replace(c, n=hi - lo)
+        if op == "fwd":
+            return oracle.conv_fwd(cs, a[lo:hi], b, bias)
+        if op == "dgrad":
+            return oracle.conv_dgrad(cs, a[lo:hi], b)
+        return oracle.conv_wgrad(cs, a[lo:hi], b[lo:hi])
+
+    parts = _pool_map(run, slices)
+    if op == "wgrad":
+        return np.sum(np.stack(parts), axis=0)
+    return np.concatenate(parts, axis=0)

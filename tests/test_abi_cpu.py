@@ -332,3 +332,14 @@ def test_conv3d_shapes_and_families(gb):
     # folded: the implicit GEMM's items count N*D images
     _, _, f = _plan(gb, s3(n=2, in_size=(3, 9, 7), **flat))
     assert int(f["items"]) == 2 * 3 * -(-9 * (7 + 2) // 256)
+
+
+def test_tensors_on_different_devices_are_refused(gb):
+    # the C ABI takes device pointers on the current device: one call, one device
+    import types
+    torch = pytest.importorskip("torch")
+    a = types.SimpleNamespace(device=torch.device("cuda", 0))
+    b = types.SimpleNamespace(device=torch.device("cuda", 1))
+    assert gb._one_device(x=a, w=a, bias=None) == torch.device("cuda", 0)
+    with pytest.raises(ValueError, match="one device"):
+        gb._one_device(x=a, w=a, y=b)

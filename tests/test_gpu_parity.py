@@ -1,12 +1,12 @@
 """GPU parity: every kernel family, through the C ABI, against the FP64 oracle.
 
 Small shapes (several tiles, ragged tails, odd extents, zero-tap phases) are
-compared element by element with the whole oracle output.  The five benchmark
+compared element by element with the whole oracle output.  The benchmark
 workloads run at full size in the launch configuration the benchmark times
-and are compared on sampled outputs the oracle computes one by one (borders,
-corners, the last elements and a seeded random sample).  Integer-valued
-inputs make every product and partial sum exact, so those runs must match the
-oracle bit for bit (after the one bf16 rounding of the output).
+and are compared element by element with the whole oracle output too (the
+oracle split over the host's cores).  Integer-valued inputs make every
+product and partial sum exact, so those runs, small and full size, must match
+the oracle bit for bit (after the one bf16 rounding of the output).
 """
 import numpy as np
 import pytest
@@ -14,8 +14,8 @@ import pytest
 import oracle
 import synth
 from synth.workloads import EXTRA_WORKLOADS, WORKLOADS, make_inputs
-from tests.helpers import (bf16_round, check_bf16, check_f32, draw, lib_desc, oracle_conv, scale_dgrad, scale_fwd,
-                           shape_kw, to_device, to_host_f64)
+from tests.helpers import (bf16_round, check_bf16, check_f32, draw, lib_desc, oracle_conv, oracle_whole, scale_dgrad,
+                           scale_fwd, shape_kw, to_device, to_host_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -402,88 +402,98 @@ def test_pack_weight_then_fast_path(gb):
     check_bf16(got, ref, scale_fwd(c_oihw, inp["x"], inp["w"], None))
 
 
+@pytest.mark.parametrize("kw", [
+    shape_kw(spatial_dims=1, n=1, in_size=(9,), c_in=16, c_out=24, k=(5,), stride=(1,), pad=(2,), dil=(1,),
+             layout="nlc", wlayout="oik"),
+    shape_kw(n=1, in_size=(6, 7), c_in=32, c_out=16, groups=2, k=(3, 2), pad=(1, 0), wlayout="oihw"),
+    shape_kw(spatial_dims=3, n=1, in_size=(4, 5, 6), c_in=16, c_out=8, k=(3, 2, 3), stride=(1, 1, 1),
+             pad=(1, 0, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="oidhw", dtype="f32"),
+], ids=["1d", "2d-grouped", "3d-f32"])
+def test_pack_weight_shapes(gb, kw):
+    # [C_out, C_in/G, K...] -> [C_out, K..., C_in/G] on the device, 1-D, 2-D and 3-D
+    d = lib_desc(gb, kw)
+    c = oracle_conv(kw)
+    w = synth.integers(93, c.w_shape(), -100, 100).astype(np.float32)
+    dt = torch.bfloat16 if kw["dtype"] == "bf16" else torch.float32
+    got = gb.pack_weight(d, torch.from_numpy(w).to("cuda").to(dt))
+    torch.cuda.synchronize()
+    nd = w.ndim
+    np.testing.assert_array_equal(to_host_f64(torch, got), np.moveaxis(w, 1, nd - 1).astype(np.float64))
+
+
 # ------------------------------------------------------------ full-size workloads
 
-def _sample_indices(shape4, seed, count=3000):
-    """(n, c, h, w) indices: every corner/edge class plus a seeded random sample."""
-    n, c, h, w = shape4
-    rng = synth.uniform01(seed, count * 4).reshape(count, 4)
-    idx = np.stack([np.floor(rng[:, i] * m) for i, m in enumerate((n, c, h, w))], axis=1).astype(np.int64)
-    fixed = []
-    for hh in sorted({0, 1, h // 2, h - 2, h - 1}):
-        for ww in sorted({0, 1, w // 2, w - 2, w - 1}):
-            for cc in sorted({0, c - 1}):
-                fixed.append((n - 1, cc, max(hh, 0), max(ww, 0)))
-    return np.concatenate([idx, np.array(fixed, dtype=np.int64)], axis=0)
+def _run_workload(gb, wl, inp):
+    kw = dict(wl.__dict__)
+    if wl.op == "wgrad":
+        return run_wgrad(gb, kw, inp, want_db=wl.bias)
+    if wl.op == "fwd":
+        return run_fwd(gb, kw, inp), None
+    return run_dgrad(gb, kw, inp), None
+
+
+def _oracle_workload(c, wl, inp, absolute=False):
+    """The oracle's whole result for the workload (on the host's cores), or with ``absolute`` the
+    per-element scale (the same sums over absolute values, |bias| included)."""
+    f = np.abs if absolute else (lambda v: v)
+    if wl.op == "wgrad":
+        return oracle_whole(c, "wgrad", f(inp["x"]), f(inp["g"]))
+    if wl.op == "fwd":
+        b = inp.get("b")
+        return oracle_whole(c, "fwd", f(inp["x"]), f(inp["w"]), None if b is None else f(b))
+    return oracle_whole(c, "dgrad", f(inp["g"]), f(inp["w"]))
 
 
 @pytest.mark.parametrize("wl", WORKLOADS + EXTRA_WORKLOADS, ids=[w.name for w in WORKLOADS + EXTRA_WORKLOADS])
 def test_workload_full_size(gb, wl):
+    # every output element of the workload, in the launch configuration the benchmark times, against
+    # the whole oracle result: the normwise bar and the per-element bound
     c = oracle_conv(wl)
     inp = make_inputs(wl)
-    kw = dict(wl.__dict__)
-    if wl.op == "wgrad":
-        # dW elements (co, c_local, [kd,] kh, kw): every tap at the channel corners plus a seeded
-        # sample; each oracle element is a full sum over the batch's positions
-        dw, _ = run_wgrad(gb, kw, inp, want_db=wl.bias)
-        taps = [tuple(t) for t in np.ndindex(*wl.k)]
-        cpg = wl.c_in // wl.groups
-        rnd = _sample_indices((wl.c_out, cpg, len(taps), 1), 5000 + wl.index, count=160)
-        idx = np.array([(co, cl) + taps[t] for co, cl, t, _ in rnd] +
-                       [(co, cl) + t for co in (0, wl.c_out - 1) for cl in (0, cpg - 1) for t in taps],
-                       dtype=np.int64)
-        ref = oracle.conv_wgrad_points(c, inp["x"], inp["g"], idx)
-        scale = oracle.conv_wgrad_points(c, np.abs(inp["x"]), np.abs(inp["g"]), idx)
-        # dw is O[D]HWI: (co, [kd,] kh, kw, c_local)
-        check_bf16(dw[(idx[:, 0],) + tuple(idx[:, 2 + i] for i in range(len(wl.k))) + (idx[:, 1],)], ref, scale)
-        assert np.isfinite(dw).all()
-        return
-    if wl.spatial_dims == 3:
-        # NDHWC; (n*depth, c, h, w) samples cover every depth slice's corners and edges
-        if wl.op == "fwd":
-            got = run_fwd(gb, kw, inp)
-            dd, hh, ww = c.out_hw()
-            ch = wl.c_out
-        else:
-            got = run_dgrad(gb, kw, inp)
-            (dd, hh, ww), ch = wl.in_size, wl.c_in
-        idx4 = _sample_indices((wl.n * dd, ch, hh, ww), 5000 + wl.index, count=1500)
-        idx = np.stack([idx4[:, 0] // dd, idx4[:, 1], idx4[:, 0] % dd, idx4[:, 2], idx4[:, 3]], axis=1)
-        if wl.op == "fwd":
-            ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
-            scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
-                                           None if "b" not in inp else np.abs(inp["b"]), idx)
-        else:
-            ref = oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
-            scale = oracle.conv_dgrad_points(c, np.abs(inp["g"]), np.abs(inp["w"]), idx)
-        check_bf16(got[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 4], idx[:, 1]], ref, scale)
-        assert np.isfinite(got).all()
-        return
-    if wl.op == "fwd":
-        got = run_fwd(gb, kw, inp)
-        oh, ow = c.out_hw()
-        shape4 = (wl.n, wl.c_out, oh, ow)
+    got, db = _run_workload(gb, wl, inp)
+    ref = _oracle_workload(c, wl, inp)
+    scale = _oracle_workload(c, wl, inp, absolute=True)
+    assert got.shape == ref.shape
+    if wl.dtype == "f32":
+        check_f32(got, ref, scale)
     else:
-        got = run_dgrad(gb, kw, inp)
-        shape4 = (wl.n, wl.c_in, c.in_hw[0], c.in_hw[1])
-    if wl.spatial_dims == 1:
-        # NCL: compare everything (it is tiny)
-        ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp.get("b"))
-        check_f32(got, ref, scale_fwd(c, inp["x"], inp["w"], inp.get("b")))
-        return
-    idx = _sample_indices(shape4, 5000 + wl.index)
-    if wl.op == "fwd":
-        ref = oracle.conv_fwd_points(c, inp["x"], inp["w"], inp.get("b"), idx)
-        scale = oracle.conv_fwd_points(c, np.abs(inp["x"]), np.abs(inp["w"]),
-                                       None if "b" not in inp else np.abs(inp["b"]), idx)
-    else:
-        ref = oracle.conv_dgrad_points(c, inp["g"], inp["w"], idx)
-        scale = oracle.conv_dgrad_points(c, np.abs(inp["g"]), np.abs(inp["w"]), idx)
-    # got is NHWC: (n, h, w, c)
-    sel = got[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]]
-    check_bf16(sel, ref, scale)
-    # global properties: finite everywhere, and nothing left unwritten (the guard fill value is 7.0)
-    assert np.isfinite(got).all()
+        check_bf16(got, ref, scale)
+    if db is not None and wl.bias:
+        check_bf16(db, oracle.conv_bgrad(c, inp["g"]), oracle.conv_bgrad(c, np.abs(inp["g"])))
+
+
+def _integer_inputs(wl):
+    """Integer-valued inputs of the workload's shapes (activations and output gradients in [-3, 3],
+    weights in [-2, 2], bias in [-4, 4]): every bf16 product and every fp32 partial sum is exact."""
+    base = 6000 + wl.index
+    out = {}
+    shapes = {"fwd": (("x", wl.x_shape), ("w", wl.w_shape)), "dgrad": (("g", wl.g_shape), ("w", wl.w_shape)),
+              "wgrad": (("x", wl.x_shape), ("g", wl.g_shape))}[wl.op]
+    for i, (name, shape) in enumerate(shapes):
+        lo, hi = (-2, 2) if name == "w" else (-3, 3)
+        out[name + "_bits"], out[name] = synth.as_bf16(synth.integers(base * 16 + i, shape, lo, hi))
+    if wl.bias and wl.op == "fwd":
+        out["b"] = synth.integers(base * 16 + 7, (wl.c_out,), -4, 4).astype(np.float32)
+    return out
+
+
+BF16_WORKLOADS = [w for w in WORKLOADS + EXTRA_WORKLOADS if w.dtype == "bf16"]
+
+
+@pytest.mark.parametrize("wl", BF16_WORKLOADS, ids=[w.name for w in BF16_WORKLOADS])
+def test_workload_full_size_integer_bit_exact(gb, wl):
+    # the full-size launch configurations (wide tiles, several persistent rounds, every stride phase,
+    # chunked weight-gradient sums) on integer inputs: the largest sum stays below 2^24, so fp32 holds
+    # every partial sum exactly and the output must equal the oracle rounded once to bf16, bit for bit
+    c = oracle_conv(wl)
+    inp = _integer_inputs(wl)
+    got, db = _run_workload(gb, wl, inp)
+    ref = _oracle_workload(c, wl, inp)
+    scale = _oracle_workload(c, wl, inp, absolute=True)
+    assert float(scale.max()) < 2.0 ** 24
+    np.testing.assert_array_equal(got, bf16_round(ref))
+    if db is not None and wl.bias:
+        np.testing.assert_array_equal(db, oracle.conv_bgrad(c, inp["g"]))
 
 
 # ---------------------------------------------------------------- weight gradient
@@ -640,7 +650,7 @@ def test_wgrad_is_deterministic_and_db_optional(gb):
 
 def test_wgrad_tc_chunks_longer_than_one_load(gb):
     # 8 images of 120x120: 64-row-wide boxes hold one block of 4 rows per load, and the row blocks
-    # outnumber the chunks, so CTAs sweep several segments; checked on sampled dW elements
+    # outnumber the chunks, so CTAs sweep several segments; checked on every dW element
     kw = shape_kw(n=8, in_size=(120, 120), c_in=64, c_out=64, k=(3, 3), pad=(1, 1))
     d = lib_desc(gb, kw)
     assert gb.gbconv_select(d, gb.GBCONV_OP_BWD_FILTER) == "wgrad"
@@ -649,8 +659,7 @@ def test_wgrad_tc_chunks_longer_than_one_load(gb):
     c = oracle_conv(kw)
     inp = draw_wgrad(c, "bf16", 950)
     dw, db = run_wgrad(gb, kw, inp)
-    idx = _sample_indices((64, 64, 3, 3), 951, count=120)
-    ref = oracle.conv_wgrad_points(c, inp["x"], inp["g"], idx)
-    scale = oracle.conv_wgrad_points(c, np.abs(inp["x"]), np.abs(inp["g"]), idx)
-    check_bf16(dw[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]], ref, scale)
+    ref = oracle_whole(c, "wgrad", inp["x"], inp["g"])
+    scale = oracle_whole(c, "wgrad", np.abs(inp["x"]), np.abs(inp["g"]))
+    check_bf16(dw, ref, scale)
     check_f32(db, oracle.conv_bgrad(c, inp["g"]), oracle.conv_bgrad(c, np.abs(inp["g"])))

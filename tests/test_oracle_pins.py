@@ -9,6 +9,7 @@ one-hot output gradient, and rejection of degenerate shapes.
 A plausible slip in the oracle (dropped bias, a flipped kernel, a wrong group
 window, a sign or stride error in the gather) fails at least one of them.
 """
+import dataclasses
 import json
 import os
 
@@ -488,3 +489,74 @@ def test_conv3d_with_unit_depth_is_conv2d():
     np.testing.assert_array_equal(oracle.conv_fwd(c3, x3, w3).reshape(c2.y_shape()), oracle.conv_fwd(c2, x, w))
     np.testing.assert_array_equal(oracle.conv_dgrad(c3, dy3, w3).reshape(c2.x_shape()), oracle.conv_dgrad(c2, dy, w))
     np.testing.assert_array_equal(oracle.conv_wgrad(c3, x3, dy3).reshape(c2.w_shape()), oracle.conv_wgrad(c2, x, dy))
+
+
+# ------------------------------------------------- 2-D and 1-D point queries
+
+def _torch_fwd_and_grads(c, x, w, b, dy):
+    """torch float64 forward on the explicitly padded NCHW / NCL view, and its autograd input, weight
+    and bias gradients (all in the NCHW / OIHW view)."""
+    F = torch.nn.functional
+    xt = torch.from_numpy(_to_nchw(x, c).astype(np.float64).copy()).requires_grad_(True)
+    wt = torch.from_numpy(_w_to_oihw(w, c).astype(np.float64).copy()).requires_grad_(True)
+    bt = torch.from_numpy(b.astype(np.float64)).requires_grad_(True)
+    pe = c.pads_end()
+    if c.spatial_dims == 1:
+        yt = F.conv1d(F.pad(xt, (c.pad[1], pe[1])), wt, bt, stride=c.stride[1], dilation=c.dil[1], groups=c.groups)
+    else:
+        yt = F.conv2d(F.pad(xt, (c.pad[1], pe[1], c.pad[0], pe[0])), wt, bt, stride=c.stride, dilation=c.dil,
+                      groups=c.groups)
+    dyt = torch.from_numpy(_to_nchw(dy, c).astype(np.float64).copy())
+    gx, gw, _ = torch.autograd.grad(yt, (xt, wt, bt), dyt)
+    return yt.detach().numpy(), gx.numpy(), gw.numpy()
+
+
+def _as4(idx, c):
+    """Indices of an NCL / OIK tensor as the 4-index (n, c, 0, l) / (co, cl, 0, k) form the 2-D point
+    queries take; 2-D indices unchanged."""
+    if c.spatial_dims == 1:
+        return np.stack([idx[:, 0], idx[:, 1], np.zeros_like(idx[:, 0]), idx[:, 2]], axis=1)
+    return idx
+
+
+@pytest.mark.parametrize("ci", range(len(CASES) + len(ASYM)))
+def test_points_2d_match_torch_float64(ci):
+    # The batched 4-index point queries (forward, input gradient, weight gradient) that the full-size
+    # checks of 2-D workloads use, against torch at every third element: grouped, strided, dilated,
+    # symmetric and (begin, end) padded, both activation layouts and both weight orders, 1-D and 2-D.
+    # Indices are (n, c, h, w) of the NCHW view and (co, c_local, kh, kw) of the OIHW view whatever
+    # the layout, so a swapped index order or layout slip fails here.
+    c = (CASES + ASYM)[ci]
+    x = synth.normal(171 + ci, c.x_shape()).astype(np.float32)
+    w = synth.normal(172 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(173 + ci, (c.c_out,)).astype(np.float32)
+    dy = synth.normal(174 + ci, c.y_shape()).astype(np.float32)
+    y_ref, gx_ref, gw_ref = _torch_fwd_and_grads(c, x, w, b, dy)
+    for ref, query in ((y_ref, lambda i: oracle.conv_fwd_points(c, x, w, b, i)),
+                       (gx_ref, lambda i: oracle.conv_dgrad_points(c, dy, w, i)),
+                       (gw_ref, lambda i: oracle.conv_wgrad_points(c, x, dy, i))):
+        idx = np.argwhere(np.ones(ref.shape, dtype=bool))[ci % 3::3]
+        np.testing.assert_allclose(query(_as4(idx, c)), ref[tuple(idx.T)], rtol=1e-12, atol=1e-12)
+    # and without a bias the forward points are the bias-free sums
+    idx = np.argwhere(np.ones(y_ref.shape, dtype=bool))[::5]
+    got = oracle.conv_fwd_points(c, x, w, None, _as4(idx, c))
+    bias_at = b.astype(np.float64)[idx[:, 1]]
+    np.testing.assert_allclose(got, y_ref[tuple(idx.T)] - bias_at, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------- the tests' whole-output oracle on many cores
+
+@pytest.mark.parametrize("ci", range(len(CASES) + len(CASES3)))
+def test_whole_on_host_threads_equals_one_call(ci):
+    # the full-size parity tests split the oracle over batch slices (1-D / 2-D) or flat index ranges
+    # of point queries (3-D) on every host core; the pieces must put back the one-call result
+    from tests.helpers import oracle_whole
+    c = (CASES + CASES3)[ci]
+    c = dataclasses.replace(c, n=3)
+    x = synth.normal(181 + ci, c.x_shape()).astype(np.float32)
+    w = synth.normal(182 + ci, c.w_shape()).astype(np.float32)
+    b = synth.normal(183 + ci, (c.c_out,)).astype(np.float32)
+    dy = synth.normal(184 + ci, c.y_shape()).astype(np.float32)
+    np.testing.assert_allclose(oracle_whole(c, "fwd", x, w, b), oracle.conv_fwd(c, x, w, b), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle_whole(c, "dgrad", dy, w), oracle.conv_dgrad(c, dy, w), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle_whole(c, "wgrad", x, dy), oracle.conv_wgrad(c, x, dy), rtol=1e-13, atol=1e-13)
