@@ -68,7 +68,7 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             m = json.load(f)
-        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "sm_max_mhz") if k in m})
         p["source"] = "measured"
     return p
 
@@ -228,7 +228,17 @@ def record_traffic(csv_path: str, workload: str, kernel_regex: str, command: str
 
 KERNEL_FILE = {"direct": "direct.cu", "depthwise": "depthwise.cu", "pointwise": "pointwise.cu",
                "implicit": "implicit.cu", "dgrad": "implicit.cu", "direct_dgrad": "direct.cu",
-               "depthwise_dgrad": "depthwise.cu", "direct_wgrad": "wgrad.cu", "wgrad": "wgrad_tc.cu"}
+               "depthwise_dgrad": "depthwise.cu", "direct_wgrad": "wgrad.cu", "wgrad": "wgrad_tc.cu",
+               "smallgroup": "smallgroup.cu", "smallgroup_dgrad": "smallgroup.cu"}
+
+# Families whose arithmetic runs on the CUDA cores (fp32 FMA), not the tensor cores.
+CUDA_CORE_FAMILIES = {"direct", "direct_dgrad", "direct_wgrad", "depthwise", "depthwise_dgrad", "smallgroup",
+                      "smallgroup_dgrad"}
+
+
+def fp32_peak_tflops(sms: int, sm_mhz: float) -> float:
+    """FP32 FMA peak from unit counts: 128 fp32 lanes per SM, one FMA (2 flops) per lane per clock."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -239,7 +249,9 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
     pk = peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    pk["fp32_tflops"] = fp32_peak_tflops(props.multi_processor_count, pk.get("sm_max_mhz", 2070.0))
 
     def make_case(wl):
         inp = make_inputs(wl)
@@ -333,16 +345,23 @@ def run_gpu(args, rank, world, local_rank):
     step_ms = max_over_ranks(statistics.mean(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)), dev)
 
     def config_line(c, ms):
+        # the slower of the flops at the dense bf16 tensor peak and the bytes at the copy bandwidth;
+        # for a family that runs on the CUDA cores, also the flops at the fp32 FMA peak
         t_f = c["flops"] / (pk["bf16_tflops"] * 1e12)
         t_b = c["bytes"] / (pk["hbm_gbs"] * 1e9)
-        t_roof = max(t_f, t_b)
-        return {"workload": c["wl"].name, "kernel": c["family"], "us": round(ms * 1e3, 3),
+        t_a = c["flops"] / (pk["fp32_tflops"] * 1e12) if c["family"] in CUDA_CORE_FAMILIES else 0.0
+        t_roof = max(t_f, t_b, t_a)
+        bound = "alu" if t_a >= max(t_f, t_b) else ("tensor" if t_f >= t_b else "hbm")
+        line = {"workload": c["wl"].name, "kernel": c["family"], "us": round(ms * 1e3, 3),
                 "tflops": round(c["flops"] / (ms * 1e-3) / 1e12, 2),
                 "gbs": round(c["bytes"] / (ms * 1e-3) / 1e9, 1),
-                "bound": "tensor" if t_f >= t_b else "hbm", "t_roof_us": round(t_roof * 1e6, 3),
+                "bound": bound, "t_roof_us": round(t_roof * 1e6, 3),
                 "roofline_frac": round(t_roof / (ms * 1e-3), 4),
                 "launches_per_step": len(c["copies"]),
                 "inputs": "L2 resident (too small to exceed L2)" if c["l2_resident"] else "from HBM"}
+        if bound == "alu":
+            line["roofline_frac_tensor_hbm"] = round(max(t_f, t_b) / (ms * 1e-3), 4)
+        return line
 
     # ---------------------------------------------------------------- widened rows, timed the same way
     # Not part of the step (the step is the five configs above): the same grouped, back-to-back
@@ -400,6 +419,8 @@ def run_gpu(args, rank, world, local_rank):
     dc, dms = cases[dom], per_kernel_ms[dom]
     if per[dom]["bound"] == "hbm":
         achieved, peak, unit = dc["bytes"] / (dms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+    elif per[dom]["bound"] == "alu":
+        achieved, peak, unit = dc["flops"] / (dms * 1e-3) / 1e12, pk["fp32_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = dc["flops"] / (dms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
     traffic, traffic_note = traffic_record(KERNEL_FILE[dc["family"]], dc["wl"].name)
@@ -407,7 +428,8 @@ def run_gpu(args, rank, world, local_rank):
             "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
             "kernel": dc["family"], "workload": dc["wl"].name,
             "algorithmic_bytes": dc["bytes"], "algorithmic_flops": dc["flops"],
-            "peak_source": pk["source"] + " (burst)"}
+            "peak_source": (pk["source"] + " (burst)") if per[dom]["bound"] != "alu" else
+                           "fp32 FMA from unit counts: SMs x 128 lanes x 2 flops x max SM clock"}
     value = job_rate(world, step_flops, step_ms)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,

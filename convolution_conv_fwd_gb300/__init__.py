@@ -31,7 +31,8 @@ GBCONV_OP_FWD, GBCONV_OP_BWD_DATA, GBCONV_OP_BWD_FILTER = 0, 1, 2
 
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
            "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_bwd_filter_noalloc",
-           "gbconv_pack_weight", "gbconv_device_status", "gbconv_kernels_launched", "gbconv_status_string")
+           "gbconv_pack_weight", "gbconv_device_status", "gbconv_set_wait_limit_ns", "gbconv_kernels_launched",
+           "gbconv_status_string")
 
 
 class Desc(ctypes.Structure):
@@ -72,6 +73,8 @@ def _load():
               "gbconv_pack_weight",
               "gbconv_device_status"):
         getattr(lib, f).restype = st
+    lib.gbconv_set_wait_limit_ns.argtypes = [ctypes.c_int64]
+    lib.gbconv_set_wait_limit_ns.restype = ctypes.c_int64
     lib.gbconv_kernels_launched.argtypes = []
     lib.gbconv_kernels_launched.restype = ctypes.c_uint64
     lib.gbconv_status_string.argtypes = [st]
@@ -153,6 +156,12 @@ def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int
 
 def gbconv_device_status(stream: int) -> int:
     return _lib.gbconv_device_status(stream or None)
+
+
+def gbconv_set_wait_limit_ns(ns: int) -> int:
+    """Bound of the kernels' internal waits for later launches (<= 0: the 2 s default); returns the
+    previous bound."""
+    return int(_lib.gbconv_set_wait_limit_ns(int(ns)))
 
 
 def gbconv_kernels_launched() -> int:

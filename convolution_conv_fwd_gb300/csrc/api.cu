@@ -19,6 +19,9 @@ __device__ unsigned int g_status_word;
 
 std::atomic<uint64_t> g_launches{0};
 
+constexpr int64_t kDefaultWaitNs = 2000000000;  // 2 s
+std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
+
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
@@ -39,6 +42,7 @@ bool device_context(Launch* l, void* stream) {
   l->stream = stream;
   l->status = g_status_ptr[dev];
   l->num_sms = g_num_sms[dev];
+  l->wait_ns = uint64_t(g_wait_ns.load(std::memory_order_relaxed));
   return true;
 }
 
@@ -139,6 +143,7 @@ int32_t select_fwd(const Problem& p, bool aligned) {
   // a 3-D forward with a real depth axis: the implicit GEMM reads its kernel-depth taps as sources
   if (!planar(p, &q)) return implicit_fwd_supported(p) ? GBCONV_K_IMPLICIT : GBCONV_K_DIRECT;
   if (depthwise_supported(q)) return GBCONV_K_DEPTHWISE;
+  if (smallgroup_supported(q)) return GBCONV_K_SMALLGROUP;
   if (pointwise_supported(q)) return GBCONV_K_POINTWISE;
   if (implicit_fwd_supported(q)) return GBCONV_K_IMPLICIT;
   return GBCONV_K_DIRECT;
@@ -149,8 +154,9 @@ int32_t select_dgrad(const Problem& p, bool aligned) {
   if (!aligned) return GBCONV_K_DIRECT_DGRAD;
   // a 3-D gradient with a real depth axis: depth phases, whose kernel-depth taps are dy sources
   if (!planar(p, &q)) return implicit_dgrad_supported(p) ? GBCONV_K_DGRAD : GBCONV_K_DIRECT_DGRAD;
-  if (implicit_dgrad_supported(q)) return GBCONV_K_DGRAD;
   if (depthwise_dgrad_supported(q)) return GBCONV_K_DEPTHWISE_DGRAD;
+  if (smallgroup_dgrad_supported(q)) return GBCONV_K_SMALLGROUP_DGRAD;
+  if (implicit_dgrad_supported(q)) return GBCONV_K_DGRAD;
   return GBCONV_K_DIRECT_DGRAD;
 }
 
@@ -195,6 +201,7 @@ gbconv_status bwd_data(const gbconv_desc* desc, const void* dy, const void* w, c
   switch (k) {
     case GBCONV_K_DGRAD: return launch_implicit_dgrad(q, dy, w, bias, dx, l);
     case GBCONV_K_DEPTHWISE_DGRAD: return launch_depthwise_dgrad(q, dy, w, bias, dx, l);
+    case GBCONV_K_SMALLGROUP_DGRAD: return launch_smallgroup_dgrad(q, dy, w, bias, dx, l);
     default: return launch_direct_dgrad(p, dy, w, bias, dx, l);
   }
 }
@@ -242,14 +249,18 @@ gbconv_status gbconv_describe(const gbconv_desc* desc, int32_t op, char* buf, in
   gbconv_status s = resolve(desc, &p);
   if (s != GBCONV_OK) return s;
   const int32_t k = select_op(p, op, true);
-  static const char* const names[] = {"direct", "depthwise", "pointwise", "implicit", "dgrad", "direct_dgrad",
-                                      "depthwise_dgrad", "direct_wgrad", "wgrad"};
+  static const char* const names[] = {"direct",       "depthwise",    "pointwise",  "implicit",
+                                      "dgrad",        "direct_dgrad", "depthwise_dgrad", "direct_wgrad",
+                                      "wgrad",        "smallgroup",   "smallgroup_dgrad"};
   const Problem q = launch_view(p, k);
   if ((k == GBCONV_K_IMPLICIT || k == GBCONV_K_DGRAD) &&
       implicit_describe(q, k == GBCONV_K_DGRAD, buf, size_t(len)))
     return GBCONV_OK;
   if (k == GBCONV_K_WGRAD && wgrad_tc_describe(q, buf, size_t(len))) return GBCONV_OK;
-  std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_WGRAD) ? names[k] : "unknown");
+  if ((k == GBCONV_K_SMALLGROUP || k == GBCONV_K_SMALLGROUP_DGRAD) &&
+      smallgroup_describe(q, k == GBCONV_K_SMALLGROUP_DGRAD, buf, size_t(len)))
+    return GBCONV_OK;
+  std::snprintf(buf, size_t(len), "%s", (k >= 0 && k <= GBCONV_K_SMALLGROUP_DGRAD) ? names[k] : "unknown");
   return GBCONV_OK;
 }
 
@@ -266,6 +277,7 @@ gbconv_status gbconv_fwd(const gbconv_desc* desc, const void* x, const void* w, 
   const Problem q = launch_view(p, k);
   switch (k) {
     case GBCONV_K_DEPTHWISE: return launch_depthwise_fwd(q, x, w, bias, y, l);
+    case GBCONV_K_SMALLGROUP: return launch_smallgroup_fwd(q, x, w, bias, y, l);
     case GBCONV_K_POINTWISE: return launch_pointwise_fwd(q, x, w, bias, y, l);
     case GBCONV_K_IMPLICIT: return launch_implicit_fwd(q, x, w, bias, y, l);
     default: return launch_direct_fwd(p, x, w, bias, y, l);
@@ -333,6 +345,10 @@ gbconv_status gbconv_device_status(void* stream) {
 }
 
 uint64_t gbconv_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int64_t gbconv_set_wait_limit_ns(int64_t ns) {
+  return g_wait_ns.exchange(ns > 0 ? ns : kDefaultWaitNs, std::memory_order_relaxed);
+}
 
 const char* gbconv_status_string(gbconv_status status) {
   switch (status) {

@@ -388,6 +388,7 @@ struct DwTmaArgs {
   const float* bias;
   __nv_bfloat16* y;
   unsigned int* status;
+  uint64_t wait_ns;   // bound of every barrier wait (the host sets it; 2 s by default)
   int N, C, H, W, OH, OW, PH, PW;
   int nchunk, tiles_h, tiles_w, tiles_per_chunk;
   int ir, ic, stage_bytes;
@@ -417,11 +418,12 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   if (warp == kDwCompute / 32) {
     if ((threadIdx.x & 31) == 0) {
       ptx::prefetch_tmap(&xmap);
-      int st = 0;
+      int st = 0, issued = 0;
       uint32_t ph = 0;
       for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
         const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
-        if (!ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 16u)) break;
+        if (!ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 16u, a.wait_ns)) break;
+        ++issued;
         ptx::mbar_arrive_expect_tx(full + st, uint32_t(a.stage_bytes));
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
@@ -431,6 +433,10 @@ __global__ void __launch_bounds__(kDwThreads, 1)
             : "memory");
         if (++st == kDwStages) { st = 0; ph ^= 1; }
       }
+      // Drain: copies still in flight write this CTA's shared memory and must land before it leaves
+      // (after an abort the compute threads no longer consume them).
+      for (int k = max(0, issued - kDwStages); k < issued; ++k)
+        ptx::mbar_wait_drain(full + k % kDwStages, uint32_t((k / kDwStages) & 1));
     }
     __syncwarp();
     return;
@@ -453,7 +459,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   uint32_t ph = 0;
   for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
     const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
-    if (!ptx::mbar_wait(full + st, ph, abort_flag, a.status, 16u)) break;
+    if (!ptx::mbar_wait(full + st, ph, abort_flag, a.status, 16u, a.wait_ns)) break;
     const uint32_t base = ptx::smem_addr(smem + st * a.stage_bytes) + cv * 16;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -518,6 +524,7 @@ gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, cons
   a.bias = bias;
   a.y = static_cast<__nv_bfloat16*>(y);
   a.status = l.status;
+  a.wait_ns = l.wait_ns;
   a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
   a.PH = int(p.PH); a.PW = int(p.PW);
   a.nchunk = a.C / 64;

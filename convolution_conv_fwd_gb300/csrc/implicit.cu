@@ -109,8 +109,14 @@ struct Args {
   unsigned int* status;
   int N, Cn, Ho, Wo;
   int T;              // KH*KW
-  int kb_count;       // 64-channel k-blocks of the reduction
-  int n_tiles;
+  int kb_count;       // 64-channel k-blocks of the reduction (of one group)
+  int n_tiles;        // BN-wide output tiles of one group
+  // Groups: every group is its own GEMM.  G groups of cg_k reduction channels and cg_n output
+  // channels; the activations are read through a view with the group as a dimension of its own, so
+  // each group's k-blocks end at the group's last channel (TMA zero fill past it).
+  int G, cg_k, cg_n;
+  int bias_n;         // bias entries staged in shared memory
+  uint64_t wait_ns;   // bound of every barrier wait (the host sets it; 2 s by default)
   int a_stage_bytes, b_tile_bytes, sa, sb;
   int stage_bufs;     // epilogue staging blocks (2: copies of one overlap the next sub-tile)
   int b4d;            // gradient weight tiles come as one 4-D box (C_in a multiple of 64), else 64-wide boxes
@@ -126,7 +132,7 @@ struct Maps {
 };
 
 struct Item {
-  int phase, n, m, ntile;
+  int phase, n, m, ntile, g;
 };
 
 // Item of round r for this CTA.  Items are numbered heaviest phase first; even rounds hand them
@@ -138,14 +144,16 @@ __device__ __forceinline__ int round_item(int r, int total) {
   return item < total ? item : -1;
 }
 
-__device__ __forceinline__ Item decode_item(const PhaseHdr* ph, int nphase, int n_tiles, int item) {
+__device__ __forceinline__ Item decode_item(const PhaseHdr* ph, int nphase, int n_tiles, int G, int item) {
   int p = 0;
   while (p + 1 < nphase && item >= ph[p + 1].item0) ++p;
   Item it;
   it.phase = p;
   int local = item - ph[p].item0;
-  it.ntile = local % n_tiles;
-  local /= n_tiles;
+  const int t2 = local % (n_tiles * G);  // (group, output tile) of the item
+  it.g = t2 / n_tiles;
+  it.ntile = t2 - it.g * n_tiles;
+  local /= n_tiles * G;
   it.n = local / ph[p].tiles;
   it.m = local - it.n * ph[p].tiles;
   return it;
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* bias_s = reinterpret_cast<float*>(stage_base + a.stage_bufs * kStageBlock);
   // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
   // parameter reads are slow next to shared-memory reads in the MMA loop.
-  int* taps_s = reinterpret_cast<int*>(bias_s + a.n_tiles * BN);  // [phase][off, w][kMaxTapsPerPhase]
+  int* taps_s = reinterpret_cast<int*>(bias_s + a.bias_n);  // [phase][off, w][kMaxTapsPerPhase]
   PhaseHdr* phase_s = reinterpret_cast<PhaseHdr*>(taps_s + kMaxPhases * 2 * kMaxTapsPerPhase);
   uint64_t* bars = reinterpret_cast<uint64_t*>(phase_s + kMaxPhases);
   uint64_t* fullA = bars;
@@ -264,17 +272,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int p = 0; p < a.nphase; ++p) ptx::prefetch_tmap(&maps.a[p]);
       ptx::prefetch_tmap(&maps.b);
-      auto load_b = [&](uint8_t* dst, uint64_t* bar, int wt, int kb, int n0) {
+      // n0: first output channel of the tile inside group g (the weight's C_out rows of group g
+      // start at g*cg_n in the forward; the gradient's reduction runs over them, from g*cg_k)
+      auto load_b = [&](uint8_t* dst, uint64_t* bar, int wt, int kb, int n0, int g) {
         const uint32_t d = ptx::smem_addr(dst);
         if (DGRAD) {  // MN-major: BN/64 atoms of [64 output channels][64 input channels]
+          const int co = g * a.cg_k + kb * kKB;
           if (a.b4d) {
-            tma_load_4d(d, &maps.b, bar, 0, kb * kKB, n0 / 64, wt);
+            tma_load_4d(d, &maps.b, bar, 0, co, n0 / 64, wt);
           } else {
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) tma_load_3d(d + h * 8192, &maps.b, bar, n0 + h * 64, wt, kb * kKB);
+            for (int h = 0; h < BN / 64; ++h) tma_load_3d(d + h * 8192, &maps.b, bar, n0 + h * 64, wt, co);
           }
         } else {      // K-major: BN output channels x 64 input channels
-          tma_load_3d(d, &maps.b, bar, kb * kKB, wt, n0);
+          tma_load_3d(d, &maps.b, bar, kb * kKB, wt, g * a.cg_n + n0);
         }
       };
       bool ok = true;
@@ -282,16 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // activation halo: that box comes from HBM and takes longest, the weights are shared by every
       // CTA and mostly come from L2.
       bool b_pending = BRES;
+      int issued_a = 0, issued_b = 0;  // loads issued into the A and B rings (for the drain below)
       auto load_resident_b = [&]() {
         ptx::mbar_arrive_expect_tx(bres, uint32_t(a.T * a.kb_count) * kBTile);
         for (int kb = 0; kb < a.kb_count; ++kb)
-          for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(kb * a.T + wt) * kBTile, bres, wt, kb, 0);
+          for (int wt = 0; wt < a.T; ++wt) load_b(b_base + size_t(kb * a.T + wt) * kBTile, bres, wt, kb, 0, 0);
         b_pending = false;
       };
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0; item = round_item(++r, a.total_items)) {
-        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, a.G, item);
         const PhaseHdr& ph = phase_s[it.phase];
         if (ph.ntaps == 0) continue;
         const int ra = (it.m * 128 * NSUB) / ph.P;
@@ -300,26 +312,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kbi = 0; ok && kbi < a.kb_count; ++kbi) {
           const int kb = kbi + kb_rot < a.kb_count ? kbi + kb_rot : kbi + kb_rot - a.kb_count;
           for (int src = 0; ok && src < (MSRC ? ph.nsrc : 1); ++src) {
-            if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u))) break;
+            if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u, a.wait_ns))) break;
             ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
             if (MSRC && a.depth_od > 0) {  // 3-D: item image it.n is a (batch, depth slice) pair
               const int nn = it.n / ph.jd, od = it.n - nn * ph.jd;
               tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
                           kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
                           (ra + ph.rmin) * ph.row_step + ph.src_ah[src], od * a.depth_sd + ph.src_ad[src], nn);
+            } else if (a.G > 1) {  // (channel in group, group, column, row, image)
+              tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
+                          kb * kKB, it.g, ph.cmin * ph.col_step + ph.src_aw[src],
+                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], it.n);
             } else {
               tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
                           kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
                           (ra + ph.rmin) * ph.row_step + ph.src_ah[src], it.n);
             }
+            ++issued_a;
             if (++sa == a.sa) { sa = 0; pa ^= 1; }
             if (BRES && b_pending) load_resident_b();
             if (!BRES) {
               const int t0 = ph.src_t0[src], nt = ph.src_t0[src + 1] - t0;
               for (int ti = 0, t = item % nt; ok && ti < nt; ++ti, t = (t + 1 == nt ? 0 : t + 1)) {
-                if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u))) break;
+                if (!(ok = ptx::mbar_wait(emptyB + sb, pb ^ 1, abort_flag, a.status, 1u, a.wait_ns))) break;
                 ptx::mbar_arrive_expect_tx(fullB + sb, uint32_t(kBTile));
-                load_b(b_base + size_t(sb) * kBTile, fullB + sb, tw[t0 + t], kb, it.ntile * BN);
+                load_b(b_base + size_t(sb) * kBTile, fullB + sb, tw[t0 + t], kb, it.ntile * BN, it.g);
+                ++issued_b;
                 if (++sb == a.sb) { sb = 0; pb ^= 1; }
               }
             }
@@ -327,6 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (BRES && b_pending && ok) load_resident_b();  // a CTA that loaded no halo still owes them
+      // Drain: after an abort the MMA thread no longer consumes the stages, but copies still in
+      // flight write this CTA's shared memory, so they must land before the CTA leaves.  The k-th
+      // load into a ring completes phase k / stages of barrier k % stages.
+      for (int k = max(0, issued_a - a.sa); k < issued_a; ++k)
+        ptx::mbar_wait_drain(fullA + k % a.sa, uint32_t((k / a.sa) & 1));
+      for (int k = max(0, issued_b - a.sb); k < issued_b; ++k)
+        ptx::mbar_wait_drain(fullB + k % a.sb, uint32_t((k / a.sb) & 1));
+      if (BRES && !b_pending) ptx::mbar_wait_drain(bres, 0);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -335,17 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Kernel parameters the loop uses, in registers: parameters live in memory, and every MMA's
       // asm statement clobbers memory, so a field read inside the loop is reloaded after each MMA.
       unsigned int* const status = a.status;
+      const uint64_t wait_ns = a.wait_ns;
       const int n_sa = a.sa, n_sb = a.sb, a_stage = a.a_stage_bytes, T = a.T;
       bool ok = true;
-      if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, status, 2u);
+      if (BRES) ok = ptx::mbar_wait(bres, 0, abort_flag, status, 2u, wait_ns);
       int sa = 0, sb = 0, iter = 0;
       uint32_t pa = 0, pb = 0;
       for (int r = 0, item = round_item(0, a.total_items); ok && item >= 0;
            item = round_item(++r, a.total_items), ++iter) {
-        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+        const Item it = decode_item(phase_s, a.nphase, a.n_tiles, a.G, item);
         const PhaseHdr& ph = phase_s[it.phase];
         const int buf = iter & 1;
-        if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, status, 2u))) break;
+        if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, status, 2u, wait_ns))) break;
         ptx::tc_fence_after();
         const uint32_t acc = tmem + uint32_t(buf * NSUB * BN);
         if (ph.ntaps > 0) {
@@ -366,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int src = 0; ok && src < nsrc; ++src) {
               // TMA-filled stages need no tcgen05 fence: the barrier's transaction count already
               // orders the async-proxy writes before the async-proxy MMA reads.
-              if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, status, 2u))) break;
+              if (!(ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, status, 2u, wait_ns))) break;
               const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a_stage);
               // this source's taps, in the producer's rotated order
               const int t0 = src == 0 ? 0 : ph.src_t0[src];
@@ -381,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (BRES) {
                   b_addr = ptx::smem_addr(b_base + size_t(kb * T + w_c) * kBTile);
                 } else {
-                  if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, status, 2u))) break;
+                  if (!(ok = ptx::mbar_wait(fullB + sb, pb, abort_flag, status, 2u, wait_ns))) break;
                   b_addr = ptx::smem_addr(b_base + size_t(sb) * kBTile);
                 }
                 // Descriptor halves: the low word is (address >> 4) plus the leading-offset field, so
@@ -415,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(tfull + buf);
       }
       ptx::mma_commit(fin);
-      ptx::mbar_wait(fin, 0, abort_flag, status, 2u);
+      // Even after an abort, every MMA issued so far must complete before TMEM is freed and the CTA
+      // leaves: this wait ignores the abort flag.
+      ptx::mbar_wait_drain(fin, 0);
     }
     __syncwarp();
   } else {
@@ -431,18 +460,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
     // The bias comes from global memory: copied here, after the block-wide barrier, so the
     // producer and MMA warps start without waiting for it.
-    for (int i = threadIdx.x; i < a.n_tiles * BN; i += kEpiWarps * 32) bias_s[i] = (a.bias && i < a.Cn) ? a.bias[i] : 0.f;
+    for (int i = threadIdx.x; i < a.bias_n; i += kEpiWarps * 32) bias_s[i] = (a.bias && i < a.Cn) ? a.bias[i] : 0.f;
     asm volatile("bar.sync 5, %0;" ::"n"(kEpiWarps * 32) : "memory");
     const uint32_t stage0 = ptx::smem_addr(stage_base + quad * 32 * kPitch);
     int sbuf = 0;  // staging block used next
     int iter = 0;
     for (int r = 0, item = round_item(0, a.total_items); item >= 0; item = round_item(++r, a.total_items), ++iter) {
-      const Item it = decode_item(phase_s, a.nphase, a.n_tiles, item);
+      const Item it = decode_item(phase_s, a.nphase, a.n_tiles, a.G, item);
       const PhaseHdr& ph = phase_s[it.phase];
       const int buf = iter & 1;
-      if (!ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u)) break;
+      const bool got = ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u, a.wait_ns);
+      // Every thread times its own wait, so after an expired wait the 64 threads of a warp pair could
+      // disagree, and a thread that carried on would block at the pair barrier below for good: the
+      // pair takes one decision (leave if any of its threads gave up).
+      uint32_t stop;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 64, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(stop)
+          : "r"(uint32_t(got)), "r"(1 + quad)
+          : "memory");
+      if (stop) break;
       ptx::tc_fence_after();
-      const int n0 = it.ntile * BN;
+      const int n0 = it.g * a.cg_n + it.ntile * BN;  // first output channel of the tile
+      const int n_end = (it.g + 1) * a.cg_n;         // the group's last output channel + 1
       const bool has_bias = a.bias != nullptr;
       // The phase geometry in registers: read from shared memory inside the store loop, every
       // field would be re-read after each staging load (those are asm with memory clobbers).
@@ -506,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tp = half * 32 + lane;
             const int part = tp % kParts;
             const int co = n0 + g * kG + part * 8;
-            if (co < Cn) {
+            if (co < n_end) {
               int row = tp / kParts;
               const int q = qbase + row;
               int r = q / ph_P, colv = q - r * ph_P;
@@ -557,6 +598,7 @@ struct Plan {
   int grid;
   // geometry kept for the tensor maps (Di: depth of the activation read, x or dy, when 3-D; else 0)
   int N, Hi, Wi, Ck, Cw, Di;
+  int G, Ctot;  // groups, and the activation's channel count (Ck is one group's)
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -604,11 +646,18 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
 }
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
-  if (!(p.bf16 && p.nhwc && p.ohwi && p.G == 1)) return false;
+  if (!(p.bf16 && p.nhwc && p.ohwi)) return false;
   // A real depth axis: kernel-depth taps are more activation sources (5-D TMA boxes).  The gradient
   // also splits dx into depth phases at a depth stride: phase ad holds the slices id = ad + j*SD,
   // each met by the kernel-depth taps with (ad + PD - kd*DD) divisible by SD.
   const bool deep = p.D > 1 || p.KD > 1 || p.OD > 1;
+  // Groups: one GEMM per group, the group a dimension of the activation view (5-D boxes, so not
+  // with a depth axis as well).
+  if (p.G > 1 && deep) return false;
+  // At C_in/G <= 8 a group's reduction fills at most an eighth of a 64-channel k-block: the direct
+  // (CUDA-core) families take those shapes.
+  if (p.G > 1 && p.cpg() <= 8) return false;
+  if (p.cpg() % 8 != 0 || p.opg() % 8 != 0) return false;  // 16-byte TMA strides of the group views
   if (deep && dgrad && p.KD > kMaxSrc) return false;
   // A strided forward reads its activations through strided views (TMA element strides <= 8).
   if (!dgrad && (p.SH > 8 || p.SW > 8)) return false;
@@ -618,8 +667,9 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   pl = Plan{};
   pl.dgrad = dgrad;
   Args& a = pl.a;
-  const int64_t Ck = dgrad ? p.Cout : p.Cin, Cn = dgrad ? p.Cin : p.Cout;
-  pl.bn = pick_bn(Cn);
+  const int64_t Ck = dgrad ? p.opg() : p.cpg(), Cn = dgrad ? p.Cin : p.Cout;  // Ck: one group's reduction
+  const int64_t Cg = dgrad ? p.cpg() : p.opg();                                 // one group's output channels
+  pl.bn = pick_bn(Cg);
   pl.nsub = pl.bn <= 128 ? 2 : 1;
   // 3-D: items run over (batch, depth slice) pairs of each phase (its jd slices of y, or of dx)
   a.N = int(p.N);
@@ -628,18 +678,24 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.out_d = deep ? int(dgrad ? p.D : p.OD) : 0;
   a.out_sd = deep && dgrad ? int(p.SD) : 1;
   a.Cn = int(Cn);
+  a.G = int(p.G);
+  a.cg_k = int(Ck);
+  a.cg_n = int(Cg);
   a.Ho = int(p.H);
   a.Wo = int(p.W);
   if (!dgrad) { a.Ho = int(p.OH); a.Wo = int(p.OW); }
   a.T = int(p.KD * p.KH * p.KW);
   a.kb_count = int((Ck + kKB - 1) / kKB);
-  a.n_tiles = int((Cn + pl.bn - 1) / pl.bn);
+  a.n_tiles = int((Cg + pl.bn - 1) / pl.bn);
+  a.bias_n = int((p.G - 1) * Cg + int64_t(a.n_tiles) * pl.bn);  // covers the last group's last tile
   pl.N = int(p.N);
+  pl.G = int(p.G);
+  pl.Ctot = int(dgrad ? p.Cout : p.Cin);
   pl.Di = deep ? int(dgrad ? p.OD : p.D) : 0;  // depth of the activation the boxes read (x, or dy)
   pl.Hi = int(dgrad ? p.OH : p.H);
   pl.Wi = int(dgrad ? p.OW : p.W);
   pl.Ck = int(Ck);
-  pl.Cw = int(p.Cin);
+  pl.Cw = int(p.cpg());  // the weight's innermost extent [C_out][T][C_in/G]
 
   PhaseSpec specs[kMaxPhases];
   int nph = 0;
@@ -766,8 +822,9 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     const int imgs = a.N * specs[i].ph.jd;  // (batch, depth slice) pairs; 2-D: the batch
     if (!finish_phase(specs[i], pl.nsub, imgs)) return false;
     specs[i].ph.item0 = item;
-    if (int64_t(item) + int64_t(imgs) * specs[i].ph.tiles * a.n_tiles >= (int64_t(1) << 30)) return false;
-    item += imgs * specs[i].ph.tiles * a.n_tiles;
+    const int64_t n_all = int64_t(a.n_tiles) * a.G;  // (group, output tile) pairs
+    if (int64_t(item) + int64_t(imgs) * specs[i].ph.tiles * n_all >= (int64_t(1) << 30)) return false;
+    item += int(imgs * specs[i].ph.tiles * n_all);
     a.ph[i] = specs[i].ph;
     a_max = std::max(a_max, specs[i].ph.a_bytes);
   }
@@ -775,10 +832,10 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   a.total_items = item;
   a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
-  pl.bres = !dgrad && a.n_tiles == 1 && a.T * a.kb_count * a.b_tile_bytes <= 110 * 1024;
+  pl.bres = !dgrad && a.G == 1 && a.n_tiles == 1 && a.T * a.kb_count * a.b_tile_bytes <= 110 * 1024;
   const size_t block = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
   for (int bufs = 2; bufs >= 1; --bufs) {
-    const size_t fixed = 1024 + bufs * block + size_t(a.n_tiles) * pl.bn * 4 +
+    const size_t fixed = 1024 + bufs * block + size_t(a.bias_n) * 4 +
                          size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
                          8 * (2 * 4 + 2 * 8 + 6) + 16;
     for (int sa = 3; sa >= 2; --sa) {
@@ -808,23 +865,32 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
     // A strided view spans stride x the loaded extent and loads every stride-th element (the
     // forward of a strided 1x1); otherwise row_step = col_step = 1.  A 3-D problem adds the
     // activation's depth as a fifth dimension, one slice per box.
-    const int rank = pl.Di > 0 ? 5 : 4;
-    const cuuint64_t plane = cuuint64_t(pl.Hi) * pl.Wi * pl.Ck * 2;
+    const int rank = (pl.Di > 0 || pl.G > 1) ? 5 : 4;
+    const cuuint64_t plane = cuuint64_t(pl.Hi) * pl.Wi * pl.Ctot * 2;
     cuuint64_t dims[5] = {cuuint64_t(pl.Ck), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi), cuuint64_t(pl.N), 1};
-    cuuint64_t strides[4] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Wi) * pl.Ck * 2, plane, 0};
-    if (rank == 5) {
+    cuuint64_t strides[4] = {cuuint64_t(pl.Ctot) * 2, cuuint64_t(pl.Wi) * pl.Ctot * 2, plane, 0};
+    cuuint32_t box[5] = {cuuint32_t(kKB), cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1, 1};
+    cuuint32_t estr[5] = {1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1, 1};
+    if (pl.Di > 0) {
       dims[3] = cuuint64_t(pl.Di);
       dims[4] = cuuint64_t(pl.N);
       strides[3] = plane * cuuint64_t(pl.Di);
+    } else if (pl.G > 1) {
+      // (channel in group, group, column, row, image): each box stays inside one group's channels
+      const cuuint64_t d5[5] = {cuuint64_t(pl.Ck), cuuint64_t(pl.G), cuuint64_t(pl.Wi), cuuint64_t(pl.Hi),
+                                cuuint64_t(pl.N)};
+      const cuuint64_t s4[4] = {cuuint64_t(pl.Ck) * 2, cuuint64_t(pl.Ctot) * 2, cuuint64_t(pl.Wi) * pl.Ctot * 2, plane};
+      const cuuint32_t b5[5] = {cuuint32_t(kKB), 1, cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1};
+      const cuuint32_t e5[5] = {1, 1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1};
+      for (int k = 0; k < 5; ++k) { dims[k] = d5[k]; box[k] = b5[k]; estr[k] = e5[k]; }
+      for (int k = 0; k < 4; ++k) strides[k] = s4[k];
     }
-    cuuint32_t box[5] = {cuuint32_t(kKB), cuuint32_t(ph.P * pl.col_step), cuuint32_t(ph.bh * pl.row_step), 1, 1};
-    cuuint32_t estr[5] = {1, cuuint32_t(pl.col_step), cuuint32_t(pl.row_step), 1, 1};
     if (fn(&pl.maps.a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(in), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
-  const int Cout = pl.dgrad ? pl.Ck : a.Cn;
+  const int Cout = pl.dgrad ? pl.Ctot : a.Cn;  // the weight's C_out extent (all groups)
   if (pl.dgrad) {
     // The OHWI weight [C_out][T][C_in] viewed as (C_in % 64, C_out, C_in / 64, tap): a box of
     // (64, 64, BN/64, 1) lands as BN/64 contiguous [64 C_out][64 C_in] atoms, the MN-major operand.
@@ -897,6 +963,7 @@ gbconv_status launch(const Problem& p, bool dgrad, const void* in, const void* w
   pl.a.bias = bias;
   pl.a.out = static_cast<bf16*>(out);
   pl.a.status = l.status;
+  pl.a.wait_ns = l.wait_ns;
   pl.grid = std::max(1, std::min(pl.a.total_items, l.num_sms));
   if (!encode_maps(pl, in, w)) return GBCONV_ECUDA;
   return dgrad ? dispatch<true>(pl, l) : dispatch<false>(pl, l);

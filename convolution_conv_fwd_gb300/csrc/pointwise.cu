@@ -41,6 +41,7 @@ struct PwArgs {
   const float* bias;
   bf16* out;
   unsigned int* status;
+  uint64_t wait_ns;   // bound of every barrier wait (the host sets it; 2 s by default)
   int M, Cout, K;
   int kb_count, m_tiles, stages;
 };
@@ -101,33 +102,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive_expect_tx(bfull, uint32_t(a.kb_count) * kBTileBytes);
       for (int kb = 0; kb < a.kb_count; ++kb)
         ptx::tma_load_2d(ptx::smem_addr(b_base + size_t(kb) * kBTileBytes), &tmap_b, bfull, kb * kBK, 0);
-      int st = 0;
+      int st = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < a.m_tiles; tile += gridDim.x) {
         for (int kb = 0; kb < a.kb_count; ++kb) {
-          if (!(ok = ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 8u))) break;
+          if (!(ok = ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 8u, a.wait_ns))) break;
           ptx::mbar_arrive_expect_tx(full + st, kATileBytes);
           ptx::tma_load_2d(ptx::smem_addr(a_base + size_t(st) * kATileBytes), &tmap_a, full + st, kb * kBK,
                            tile * kBM);
+          ++issued;
           if (++st == a.stages) { st = 0; ph ^= 1; }
         }
       }
+      // Drain: copies still in flight write this CTA's shared memory and must land before it leaves
+      // (after an abort the MMA thread no longer consumes them).  Load k completes phase
+      // k / stages of barrier k % stages; the resident weights complete bfull's first phase.
+      for (int k = max(0, issued - a.stages); k < issued; ++k)
+        ptx::mbar_wait_drain(full + k % a.stages, uint32_t((k / a.stages) & 1));
+      ptx::mbar_wait_drain(bfull, 0);
     }
     __syncwarp();
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = ptx::mbar_wait(bfull, 0, abort_flag, a.status, 8u);
+      bool ok = ptx::mbar_wait(bfull, 0, abort_flag, a.status, 8u, a.wait_ns);
       int st = 0, it = 0;
       uint32_t ph = 0;
       for (int tile = blockIdx.x; ok && tile < a.m_tiles; tile += gridDim.x, ++it) {
         const int buf = it & 1;
-        if (!(ok = ptx::mbar_wait(tempty + buf, ((it >> 1) & 1) ^ 1, abort_flag, a.status, 8u))) break;
+        if (!(ok = ptx::mbar_wait(tempty + buf, ((it >> 1) & 1) ^ 1, abort_flag, a.status, 8u, a.wait_ns))) break;
         ptx::tc_fence_after();
         const uint32_t acc = tmem + uint32_t(buf * BN);
         for (int kb = 0; kb < a.kb_count; ++kb) {
-          if (!(ok = ptx::mbar_wait(full + st, ph, abort_flag, a.status, 8u))) break;
+          if (!(ok = ptx::mbar_wait(full + st, ph, abort_flag, a.status, 8u, a.wait_ns))) break;
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_addr(a_base + size_t(st) * kATileBytes);
           const uint32_t b_addr = ptx::smem_addr(b_base + size_t(kb) * kBTileBytes);
@@ -141,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(tfull + buf);
       }
       ptx::mma_commit(fin);
-      ptx::mbar_wait(fin, 0, abort_flag, a.status, 8u);
+      // every MMA issued so far completes before TMEM is freed, abort or not
+      ptx::mbar_wait_drain(fin, 0);
     }
     __syncwarp();
   } else {
@@ -150,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     for (int tile = blockIdx.x; tile < a.m_tiles; tile += gridDim.x, ++it) {
       const int buf = it & 1;
-      if (!ptx::mbar_wait(tfull + buf, (it >> 1) & 1, abort_flag, a.status, 8u)) break;
+      const bool got = ptx::mbar_wait(tfull + buf, (it >> 1) & 1, abort_flag, a.status, 8u, a.wait_ns);
+      // the TMEM loads below are warp-collective: the warp leaves together if any lane gave up
+      if (__any_sync(0xffffffffu, !got)) break;
       ptx::tc_fence_after();
       // TMEM -> (+ bias) -> bf16 -> this warp's staging rows, then whole-row coalesced stores:
       // consecutive lanes write consecutive 16-byte pieces of the same output pixel.
@@ -284,6 +295,7 @@ gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* 
   a.bias = bias;
   a.out = static_cast<bf16*>(y);
   a.status = l.status;
+  a.wait_ns = l.wait_ns;
   a.M = int(p.N * p.H * p.W);
   a.Cout = int(p.Cout);
   a.K = int(p.Cin);

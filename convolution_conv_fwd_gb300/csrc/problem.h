@@ -51,6 +51,7 @@ struct Launch {
   void* stream;
   unsigned int* status;  // device status word for bounded-wait failures
   int num_sms;
+  uint64_t wait_ns;      // bound of the kernels' barrier waits (gbconv_set_wait_limit_ns)
 };
 
 gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
@@ -66,6 +67,16 @@ gbconv_status launch_depthwise_fwd(const Problem& p, const void* x, const void* 
 bool depthwise_dgrad_supported(const Problem& p);
 gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
                                      const Launch& l);
+
+// Small groups (1 < G < C, C_in/G = C_out/G in {2, 4, 8}): tiled forward and stride-1 input
+// gradient on CUDA cores, gather input gradient at other strides.
+bool smallgroup_supported(const Problem& p);
+bool smallgroup_dgrad_supported(const Problem& p);
+bool smallgroup_describe(const Problem& p, bool dgrad, char* buf, size_t len);
+gbconv_status launch_smallgroup_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
+                                    const Launch& l);
+gbconv_status launch_smallgroup_dgrad(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                      const Launch& l);
 
 bool pointwise_supported(const Problem& p);
 gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,

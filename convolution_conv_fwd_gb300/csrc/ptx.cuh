@@ -9,8 +9,9 @@
 namespace gbconv {
 namespace ptx {
 
-// A wait that has not completed after this long is treated as a hang: the
-// waiting role records it in the status word and leaves its loop.
+// A wait that has not completed after this long is treated as a hang: the waiting role records it
+// in the status word and leaves its loop.  This is the default of the host-set limit every kernel
+// receives as an argument, and the bound of the drain waits below.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -73,20 +74,35 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitNs, or as soon as another role of the CTA has given up
+// after limit_ns, or as soon as another role of the CTA has given up
 // (*abort != 0); on giving up it records bit `why` in *status and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status, unsigned int why) {
+                                          unsigned int* status, unsigned int why, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  // the suspend hint stays below the limit, so a short limit is checked in time
+  const uint32_t hint = limit_ns < 20000u ? uint32_t(limit_ns) : 20000u;
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
       atomicOr(status, why);
       return false;
     }
+  }
+}
+
+// Waits for a phase that this thread's own bulk copy will complete (a TMA load it issued), ignoring
+// the CTA abort flag: a CTA must not leave while copies into its shared memory are in flight, so a
+// role that gives up still drains what it issued.  Bounded by kWaitLimitNs all the same; returns
+// false if the phase did not complete in time.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 

@@ -66,6 +66,7 @@ constexpr int kMaxWgPhases = 16;  // H/W stride phases (strides up to 4 x 4)
 struct TcArgs {
   float* ws;              // [chunk][ws_stride] fp32 partial sums, elements in OHWI order
   unsigned int* status;
+  uint64_t wait_ns;       // bound of every barrier wait (the host sets it; 2 s by default)
   int Cin, Cout, KH, KW, DH, DW, PH, PW;
   int SH, SW;             // H/W strides: x is read through a strided view (TMA element strides)
   int ddr, ddc;           // phase-grid rows / columns between a stride phase's consecutive kernel rows / columns
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Segment sg;
       while (ok && walk.next(sg)) {
         if (seg > 0) {  // the previous segment's MMAs have finished reading shared memory
-          if (lane == 0) ok = ptx::mbar_wait(seg_done, uint32_t(seg - 1) & 1u, abort_flag, a.status, 1u);
+          if (lane == 0) ok = ptx::mbar_wait(seg_done, uint32_t(seg - 1) & 1u, abort_flag, a.status, 1u, a.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
         }
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
       for (int u = int(blockIdx.x); ok && u < units; u += int(gridDim.x), ++it) {
         if (it > 0) {  // the epilogue has taken the previous unit's accumulators
-          if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u))) break;
+          if (!(ok = ptx::mbar_wait(acc_empty, uint32_t(it - 1) & 1u, abort_flag, a.status, 2u, a.wait_ns))) break;
           ptx::tc_fence_after();
         }
         // the unit's stride phase: its groups, its N (its kernel columns) and its B atoms
@@ -346,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tn = min(kStepBlock, nk - t0);
             const int kend = 16 * (t0 + tn - 1) + 15;  // last position the block reads (before the shifts)
             for (; ok && yw < nb && kend >= yw * box_pos; ++yw)
-              ok = ptx::mbar_wait(ybar + yw, (yph >> yw) & 1u, abort_flag, a.status, 2u);
+              ok = ptx::mbar_wait(ybar + yw, (yph >> yw) & 1u, abort_flag, a.status, 2u, a.wait_ns);
             for (; ok && xw < nxb && kend + xreach >= xw * box_pos; ++xw)
-              ok = ptx::mbar_wait(xbar + xw, (xph >> xw) & 1u, abort_flag, a.status, 2u);
+              ok = ptx::mbar_wait(xbar + xw, (xph >> xw) & 1u, abort_flag, a.status, 2u, a.wait_ns);
             if (!ok) break;
             const uint32_t a_lo = a_lo0 + uint32_t(t0) * 128u, b_lo = b_lo0 + uint32_t(t0) * 128u;
             const uint32_t acc0 = (first && t0 == 0) ? 0u : 1u;
@@ -367,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ptx::mma_commit(acc_full);
       }
       ptx::mma_commit(fin);
-      ptx::mbar_wait(fin, 0, abort_flag, a.status, 2u);
+      // every MMA issued so far completes before TMEM is freed, abort or not
+      ptx::mbar_wait_drain(fin, 0);
     }
     __syncwarp();
   } else {
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t t0 = ptx::globaltimer();
         while (!ptx::mbar_try_wait(acc_full, uint32_t(it) & 1u)) {
           if (*abort_flag) break;
-          if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+          if (ptx::globaltimer() - t0 > a.wait_ns) {
             *abort_flag = 1;
             atomicOr(a.status, 4u);
             break;
@@ -645,6 +647,7 @@ gbconv_status launch_wgrad_tc(const Problem& p, const void* x, const void* dy, v
   TcArgs& a = pl.a;
   a.ws = static_cast<float*>(ws);
   a.status = l.status;
+  a.wait_ns = l.wait_ns;
   a.ws_stride = int(p.w_elems() + (db ? p.Cout : 0));
   TcMaps maps;
   if (!encode(pl, x, dy, maps)) return GBCONV_ECUDA;

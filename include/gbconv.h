@@ -79,8 +79,11 @@ typedef enum {
   GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
   GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
   GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
-  GBCONV_K_WGRAD = 8           /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction
+  GBCONV_K_WGRAD = 8,          /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction
                                   (H/W strides: one stride phase per work unit; 3-D: one kernel-depth tap per unit) */
+  GBCONV_K_SMALLGROUP = 9,     /* NHWC bf16 small groups (1 < G < C, C_in/G = C_out/G in {2, 4, 8}): TMA-fed halo
+                                  tiles on CUDA cores */
+  GBCONV_K_SMALLGROUP_DGRAD = 10 /* their dgrad: the same tiled kernel at stride 1, a vectorised gather otherwise */
 } gbconv_kernel;
 
 typedef enum { GBCONV_OP_FWD = 0, GBCONV_OP_BWD_DATA = 1, GBCONV_OP_BWD_FILTER = 2 } gbconv_op;
@@ -214,6 +217,14 @@ gbconv_status gbconv_pack_weight(const gbconv_desc *desc, const void *w_oihw, vo
  * device recorded an expired internal wait since the last call (and clears the record), else GBCONV_OK
  * (or GBCONV_ECUDA if the synchronisation itself failed). */
 gbconv_status gbconv_device_status(void *stream);
+
+/* Sets how long any internal barrier wait of the library's kernels may take before the kernel gives
+ * up (records GBCONV_ETIMEOUT for gbconv_device_status, drains its copies and tensor-core work in
+ * flight, frees its tensor memory and returns), for kernels enqueued from now on, in this process.
+ * ns <= 0 restores the default, 2 s.  No correct launch comes near the default; a short limit is
+ * for exercising the failure path.  Returns the previous limit.  The source pages have no
+ * counterpart (their kernels have no bounded waits).  Launches nothing. */
+int64_t gbconv_set_wait_limit_ns(int64_t ns);
 
 /* Number of kernels this library has enqueued in this process (all devices, all streams). */
 uint64_t gbconv_kernels_launched(void);

@@ -102,6 +102,23 @@ EXTRA_WORKLOADS = [
              (1, 1), (1, 1), 1, False, (32, 56, 56, 128), (128, 3, 3, 128), (32, 28, 28, 128),
              {"x": ("normal", 1.0), "g": ("normal", 1.0)},
              "conv2d backward-filter NHWC bf16, 3x3 stride 2 pad 1, x 32x56x56x128, dy 32x28x28x128 -> dW 128x3x3x128"),
+    # a small-group layer (ResNeXt-style grouped 3x3): C 256 in 64 groups of 4 channels, 56x56, fp32 bias
+    Workload("smallgroup3x3_g64_nhwc_bf16", 12, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 256, 256, (56, 56), (3, 3),
+             (1, 1), (1, 1), (1, 1), 64, True, (32, 56, 56, 256), (256, 3, 3, 4), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / (4 * 9)) ** 0.5), "b": ("normal", 0.1)},
+             "grouped 3x3 conv2d NHWC bf16, N=32, 56x56, C 256->256, G=64 (4 channels per group), stride 1, pad 1, "
+             "fp32 bias"),
+    # its input gradient: dx 32x56x56x256 from dy of the same shape
+    Workload("smallgroup3x3_g64_dgrad_nhwc_bf16", 13, "dgrad", "bf16", 2, "nhwc", "ohwi", 32, 256, 256, (56, 56),
+             (3, 3), (1, 1), (1, 1), (1, 1), 64, False, (32, 56, 56, 256), (256, 3, 3, 4), (32, 56, 56, 256),
+             {"g": ("normal", 1.0), "w": ("normal", (2.0 / (4 * 9)) ** 0.5)},
+             "grouped 3x3 conv2d backward-data NHWC bf16, G=64 (4 channels per group), dx and dy 32x56x56x256"),
+    # a grouped dense layer on the tensor cores: C 128 in 2 groups of 64 channels, 56x56, fp32 bias
+    Workload("grouped3x3_g2_nhwc_bf16", 14, "fwd", "bf16", 2, "nhwc", "ohwi", 32, 128, 128, (56, 56), (3, 3),
+             (1, 1), (1, 1), (1, 1), 2, True, (32, 56, 56, 128), (128, 3, 3, 64), (),
+             {"x": ("normal", 1.0), "w": ("normal", (2.0 / (64 * 9)) ** 0.5), "b": ("normal", 0.1)},
+             "grouped 3x3 conv2d NHWC bf16, N=32, 56x56, C 128->128, G=2 (64 channels per group), stride 1, pad 1, "
+             "fp32 bias"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}

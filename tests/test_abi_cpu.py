@@ -116,6 +116,9 @@ EXPECTED_FAMILY = {
     "dgrad3x3x3_ndhwc_bf16": {"dgrad"},
     "wgrad3x3x3_ndhwc_bf16": {"wgrad"},
     "wgrad3x3_s2_nhwc_bf16": {"wgrad"},
+    "smallgroup3x3_g64_nhwc_bf16": {"smallgroup"},
+    "smallgroup3x3_g64_dgrad_nhwc_bf16": {"smallgroup_dgrad"},
+    "grouped3x3_g2_nhwc_bf16": {"implicit"},
 }
 
 OPS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
@@ -343,3 +346,24 @@ def test_tensors_on_different_devices_are_refused(gb):
     assert gb._one_device(x=a, w=a, bias=None) == torch.device("cuda", 0)
     with pytest.raises(ValueError, match="one device"):
         gb._one_device(x=a, w=a, y=b)
+
+
+@pytest.mark.parametrize("kw,fam_fwd,fam_dgrad", [
+    # the small-group regime: 1 < G < C with C_in/G = C_out/G in {2, 4, 8} and whole 64-channel chunks
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=128, groups=32), "smallgroup", "smallgroup_dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=128, groups=16, stride=(2, 2)), "smallgroup", "smallgroup_dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=128, groups=64), "smallgroup", "smallgroup_dgrad"),
+    # outside it: 16 channels per group and C_out/G != C_in/G (multiples of 8) are grouped implicit GEMMs
+    # on the tensor cores; 4 -> 8 channels per group, channels not in whole 64-channel chunks, and fp32
+    # take the generic kernels
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=128, groups=8), "implicit", "dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=256, c_out=512, groups=16), "implicit", "dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=256, c_out=512, groups=32), "direct", "direct_dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=256, groups=32), "direct", "direct_dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=96, c_out=96, groups=24), "direct", "direct_dgrad"),
+    (shape_kw(in_size=(16, 16), c_in=128, c_out=128, groups=32, dtype="f32"), "direct", "direct_dgrad"),
+])
+def test_small_group_regime_selection(gb, kw, fam_fwd, fam_dgrad):
+    d = lib_desc(gb, kw)
+    assert gb.gbconv_select(d, 0) == fam_fwd
+    assert gb.gbconv_select(d, 1) == fam_dgrad

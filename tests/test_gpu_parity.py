@@ -228,6 +228,47 @@ SMALL = [
               pad=(2, 1, 1), pad_end=(1, 1, 1), dil=(2, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 7, 6), c_in=64, c_out=64, k=(1, 3, 3), stride=(2, 1, 1),
               pad=(0, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad", "dgrad"),
+    # small groups (1 < G < C, C_in/G = C_out/G in {2, 4, 8}): TMA halo tiles on CUDA cores; ragged
+    # tile rows and columns, strides, dilation, (begin, end) padding, 1-D, OIHW weights, a 1x1 kernel
+    (shape_kw(n=2, in_size=(13, 37), c_in=64, c_out=64, groups=16, bias=True), "fwd", "smallgroup"),
+    (shape_kw(n=1, in_size=(15, 14), c_in=128, c_out=128, groups=64, stride=(2, 2), bias=True), "fwd", "smallgroup"),
+    (shape_kw(n=2, in_size=(10, 9), c_in=128, c_out=128, groups=16, k=(5, 3), pad=(2, 1), dil=(1, 2)), "fwd",
+     "smallgroup"),
+    (shape_kw(n=1, in_size=(9, 40), c_in=64, c_out=64, groups=32, k=(1, 1), pad=(0, 0)), "fwd", "smallgroup"),
+    (shape_kw(n=2, in_size=(11, 12), c_in=64, c_out=64, groups=8, pad=(0, 1), pad_end=(2, 0), bias=True), "fwd",
+     "smallgroup"),
+    (shape_kw(spatial_dims=1, n=2, in_size=(70,), c_in=64, c_out=64, groups=16, k=(5,), stride=(1,), pad=(2,),
+              dil=(1,), layout="nlc", wlayout="oki"), "fwd", "smallgroup"),
+    (shape_kw(n=1, in_size=(8, 8), c_in=64, c_out=64, groups=16, wlayout="oihw"), "fwd", "smallgroup"),
+    (shape_kw(n=1, in_size=(20, 66), c_in=192, c_out=192, groups=48, stride=(1, 2), pad=(1, 1)), "fwd", "smallgroup"),
+    # their input gradients: the tiled kernel at stride 1 (transposed, flipped weights), the gather otherwise
+    (shape_kw(n=2, in_size=(13, 37), c_in=64, c_out=64, groups=16), "dgrad", "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(12, 11), c_in=128, c_out=128, groups=16, dil=(2, 2), pad=(2, 2)), "dgrad",
+     "smallgroup_dgrad"),
+    (shape_kw(n=2, in_size=(9, 10), c_in=64, c_out=64, groups=32, pad=(0, 0)), "dgrad", "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(8, 8), c_in=64, c_out=64, groups=16, pad=(3, 3)), "dgrad", "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(9, 9), c_in=64, c_out=64, groups=8, pad=(1, 0), pad_end=(0, 2), wlayout="oihw"),
+     "dgrad", "smallgroup_dgrad"),
+    (shape_kw(n=2, in_size=(15, 13), c_in=64, c_out=64, groups=16, stride=(2, 2)), "dgrad", "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(14, 11), c_in=128, c_out=128, groups=16, k=(3, 2), stride=(2, 1), pad=(1, 0)), "dgrad",
+     "smallgroup_dgrad"),
+    (shape_kw(n=2, in_size=(12, 13), c_in=64, c_out=64, groups=32, stride=(3, 2), wlayout="oihw"), "dgrad",
+     "smallgroup_dgrad"),
+    # grouped dense convolutions on the tensor cores: one implicit GEMM per group (group views of the
+    # activations, group offsets into the weight and the output); whole and partial 64-channel k-blocks
+    # per group, C_out/G != C_in/G, strides (stride-phase sources / phases), 1x1, tiles wider than a group
+    (shape_kw(n=2, in_size=(9, 11), c_in=128, c_out=128, groups=2, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(10, 9), c_in=128, c_out=128, groups=4), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(8, 13), c_in=128, c_out=256, groups=8, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(13, 12), c_in=192, c_out=96, groups=3, stride=(2, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(7, 9), c_in=96, c_out=48, groups=2, k=(1, 1), pad=(0, 0)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(11, 10), c_in=64, c_out=64, groups=4, dil=(2, 1), pad=(2, 1), pad_end=(0, 1)), "fwd",
+     "implicit"),
+    (shape_kw(n=2, in_size=(9, 11), c_in=128, c_out=128, groups=2), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(12, 10), c_in=128, c_out=256, groups=4, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=2, in_size=(10, 9), c_in=96, c_out=192, groups=6, stride=(2, 1), k=(3, 2), pad=(1, 0)), "dgrad",
+     "dgrad"),
+    (shape_kw(n=1, in_size=(8, 8), c_in=256, c_out=128, groups=2, k=(1, 1), pad=(0, 0)), "dgrad", "dgrad"),
     # generic direct kernels (CUDA cores)
     (shape_kw(spatial_dims=1, n=2, in_size=(32,), c_in=4, c_out=8, k=(3,), stride=(1,), pad=(2,), dil=(2,),
               layout="ncl", wlayout="oik", dtype="f32", bias=True), "fwd", "direct"),
@@ -328,6 +369,9 @@ TRANSPOSE = [
     (shape_kw(n=2, in_size=(7, 9), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
               stride=(2, 2)), "direct_dgrad"),
     (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "direct_dgrad"),
+    (shape_kw(n=2, in_size=(11, 9), c_in=64, c_out=64, groups=16), "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(10, 12), c_in=128, c_out=64, groups=2, stride=(2, 2)), "dgrad"),
+    (shape_kw(n=1, in_size=(12, 10), c_in=128, c_out=128, groups=32, stride=(2, 2)), "smallgroup_dgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 8, 7), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 2, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 8), c_in=128, c_out=64, k=(3, 3, 3), stride=(2, 2, 1),
