@@ -99,9 +99,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&tmap_a);
       ptx::prefetch_tmap(&tmap_b);
-      ptx::mbar_arrive_expect_tx(bfull, uint32_t(a.kb_count) * kBTileBytes);
-      for (int kb = 0; kb < a.kb_count; ++kb)
-        ptx::tma_load_2d(ptx::smem_addr(b_base + size_t(kb) * kBTileBytes), &tmap_b, bfull, kb * kBK, 0);
+      // The resident weights are issued right after the first activation tile: that tile comes from
+      // HBM and takes longest, the weights are shared by every CTA and mostly come from L2.
+      auto load_weights = [&]() {
+        ptx::mbar_arrive_expect_tx(bfull, uint32_t(a.kb_count) * kBTileBytes);
+        for (int kb = 0; kb < a.kb_count; ++kb)
+          ptx::tma_load_2d(ptx::smem_addr(b_base + size_t(kb) * kBTileBytes), &tmap_b, bfull, kb * kBK, 0);
+      };
       int st = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -111,10 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(full + st, kATileBytes);
           ptx::tma_load_2d(ptx::smem_addr(a_base + size_t(st) * kATileBytes), &tmap_a, full + st, kb * kBK,
                            tile * kBM);
-          ++issued;
+          if (issued++ == 0) load_weights();
           if (++st == a.stages) { st = 0; ph ^= 1; }
         }
       }
+      if (issued == 0) load_weights();  // a CTA without tiles still completes the weight barrier
       // Drain: copies still in flight write this CTA's shared memory and must land before it leaves
       // (after an abort the MMA thread no longer consumes them).  Load k completes phase
       // k / stages of barrier k % stages; the resident weights complete bfull's first phase.

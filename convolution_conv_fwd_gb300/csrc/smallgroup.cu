@@ -9,11 +9,14 @@
 // [C_OUT, C_IN/G, KH, KW]); oarust `src/rs/ml/matrix/conv.rs`, `conv_2d` (groups).
 //
 // Forward (and the stride-1 input gradient): a persistent kernel.  A producer lane streams halo
-// tiles of the input (the rows and columns a 4 x 32 output tile reads, 64 channels, zero fill for the
-// padding) into a ring of shared-memory stages with TMA, 128-byte swizzled.  Each of 8 compute warps
-// owns one 8-channel vector of the 64-channel chunk, each lane one output column, and each thread
-// walks the tile's 4 rows: the weights of a warp's channels are then the same for all its lanes
-// (shared-memory broadcasts), and the swizzle spreads the lanes' 16-byte reads over all banks.
+// tiles of the input (the rows and columns a TR x 32 output tile reads, 64 channels, zero fill for
+// the padding) into a ring of shared-memory stages with TMA, 128-byte swizzled.  Each of 16 compute
+// warps owns four output channels of the 64-channel chunk, each lane one output column, and each
+// thread walks the tile's TR rows (8 at unit stride): a warp's weights are the same for all its lanes
+// (shared-memory broadcasts, each loaded once per tile), each lane reads its pixels as 8-byte pieces
+// that the swizzle spreads over all banks, and at unit stride a 3x3 kernel's input pixel is loaded
+// once per kernel column and feeds every output row it reaches.  The tile's outputs go through a
+// double-buffered, swizzled shared-memory tile to one TMA tensor store per tile.
 // The stride-1 input gradient is the same correlation read the other way round: dx = dy correlated
 // with the kernel flipped in both axes, begin padding (K-1)*dil - pad, and the weight transposed
 // inside each group (the dgrad's output channel ci takes dy channel g*CPG + o through w[g*CPG + o,
@@ -41,27 +44,35 @@
 namespace gbconv {
 namespace {
 
-constexpr int kTR = 4;                      // output rows per tile (a thread's row loop)
 constexpr int kTC = 32;                     // output columns per tile (one per lane)
-constexpr int kWarps = 8;                   // compute warps, one 8-channel vector of the chunk each
+constexpr int kWarps = 16;                  // compute warps, four output channels of the chunk each
 constexpr int kCompute = kWarps * 32;
-constexpr int kThreads = kCompute + 32;     // + the producer warp
+constexpr int kThreads = kCompute;          // thread 0 also issues the loads (no producer warp: at 512
+                                            // threads a thread may hold 128 registers)
 constexpr int kMaxStages = 4;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxTapTerms = 200;           // taps * CPG: the chunk's weights as fp32 in shared memory
 
 struct SgArgs {
   const float* bias;      // [C] fp32 or null (added once after the sum)
-  __nv_bfloat16* y;       // output: y (forward) or dx (input gradient)
   unsigned int* status;
   uint64_t wait_ns;       // bound of every barrier wait (the host sets it; 2 s by default)
   int N, C;               // batch, channels (C_in == C_out)
   int Hi, Wi, Ho, Wo;     // extents read (x or dy) and written (y or dx)
   int KH, KW, SH, SW, DH, DW, PH, PW;  // the read map: in = out*S + k*D - P (begin-side P)
+  int tr;                 // output rows per tile
   int nchunk, tiles_h, tiles_w, tiles_per_chunk;
   int ir, ic;             // halo rows and columns of a tile
   int box_bytes, stage_bytes, stages;
+  int out_bytes;          // one output staging tile (tr x 32 pixels x 64 channels, bf16)
   int wbytes;             // the chunk's fp32 weights
+};
+
+// Input channels a warp reads per pixel: its four output channels' groups (the same four channels
+// for CPG <= 4, the group's eight for CPG = 8).
+template <int CPG>
+struct In {
+  static constexpr int n = CPG <= 4 ? 4 : 8;
 };
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -92,60 +103,98 @@ __device__ __forceinline__ float weight_at(const __nv_bfloat16* __restrict__ w, 
   return __bfloat162float(w[idx]);
 }
 
-// The tap's weights of one warp's 8 channels ([8][CPG] fp32, the same address in every lane: a
+// Two fp32 lanes in one 64-bit register, and the paired FMA: fma.rn.f32x2 is two independent
+// round-to-nearest fp32 FMAs, the same results as two fmaf, in one instruction.
+__device__ __forceinline__ uint64_t pack2f(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2f(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// The tap's weights of one warp's 4 channels, laid out [k][channel] in shared memory: for input k, the
+// channel pairs (0, 1) and (2, 3) as two packed registers (the same address in every lane: a
 // shared-memory broadcast).
 template <int CPG>
-__device__ __forceinline__ void load_tap_weights(const float4* wp, float (&wt)[8][CPG]) {
+__device__ __forceinline__ void load_tap_weights(uint32_t wp, uint64_t (&wt)[CPG][2]) {
 #pragma unroll
-  for (int q = 0; q < 2 * CPG; ++q) {
-    const float4 v = wp[q];
-    const int e = 4 * q;
-    wt[e / CPG][e % CPG] = v.x;
-    wt[(e + 1) / CPG][(e + 1) % CPG] = v.y;
-    wt[(e + 2) / CPG][(e + 2) % CPG] = v.z;
-    wt[(e + 3) / CPG][(e + 3) % CPG] = v.w;
+  for (int k = 0; k < CPG; ++k)
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(wt[k][0]), "=l"(wt[k][1]) : "r"(wp + uint32_t(k * 16)));
+}
+
+// The warp's input piece of halo pixel `line` (128 bytes per pixel; 128-byte swizzle: the 16-byte
+// piece c of line l sits at piece c ^ (l & 7)), as fp32.
+template <int CPG>
+__device__ __forceinline__ void load_pixel(uint32_t base, int line, int piece, int half, float (&xf)[In<CPG>::n]) {
+  const uint32_t addr = base + uint32_t(line * 128 + ((piece ^ (line & 7)) << 4));
+  if constexpr (In<CPG>::n == 4) {
+    uint32_t u0, u1;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(u0), "=r"(u1) : "r"(addr + uint32_t(half * 8)));
+    xf[0] = __uint_as_float(u0 << 16);
+    xf[1] = __uint_as_float(u0 & 0xFFFF0000u);
+    xf[2] = __uint_as_float(u1 << 16);
+    xf[3] = __uint_as_float(u1 & 0xFFFF0000u);
+  } else {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    unpack8(v, xf);
   }
 }
 
-// This warp's 8-channel vector of halo pixel `line` (128 bytes per pixel, 128-byte swizzle: the
-// 16-byte piece c of line l sits at piece c ^ (l & 7)), as fp32.
-__device__ __forceinline__ void load_pixel(uint32_t base, int line, int warp, float (&xf)[8]) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(base + uint32_t(line * 128 + ((warp ^ (line & 7)) << 4))));
-  unpack8(v, xf);
-}
-
-// acc[j] += sum over the group's CPG inputs of x * w: output channel j of the vector reads the
-// vector's channels (j / CPG) * CPG .. + CPG - 1.
+// The warp's input values as duplicated pairs {x, x}, one per input of the groups it reads.
 template <int CPG>
-__device__ __forceinline__ void group_fma(float (&acc)[8], const float (&xf)[8], const float (&wt)[8][CPG]) {
+__device__ __forceinline__ void dup_pairs(const float (&xf)[In<CPG>::n], uint64_t (&xd)[In<CPG>::n]) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int k = 0; k < CPG; ++k) acc[j] = fmaf(xf[(j / CPG) * CPG + k], wt[j][k], acc[j]);
+  for (int i = 0; i < In<CPG>::n; ++i) xd[i] = pack2f(xf[i], xf[i]);
 }
 
-// K3: 3x3 kernel at unit stride and dilation, the halo geometry known at compile time; otherwise
-// any kernel, stride and dilation from the arguments.
-template <int CPG, int K3>
+// acc pair p (channels 2p, 2p+1, one group) += sum over the group's CPG inputs of x * w, input k
+// outermost (each accumulator takes its terms in the order k = 0, 1, ...).
+template <int CPG>
+__device__ __forceinline__ void group_fma(uint64_t (&acc)[2], const uint64_t (&xd)[In<CPG>::n],
+                                          const uint64_t (&wt)[CPG][2]) {
+#pragma unroll
+  for (int k = 0; k < CPG; ++k)
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) acc[pp] = fma2(xd[(CPG <= 4 ? ((2 * pp) / CPG) * CPG : 0) + k], wt[k][pp], acc[pp]);
+}
+
+__device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// waits until at most N committed bulk groups of this thread still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// TR: output rows per tile.  K3: 3x3 kernel at unit stride and dilation, the halo geometry known at
+// compile time (CPG <= 4); otherwise any kernel, stride and dilation from the arguments.
+template <int CPG, int TR, int K3>
 __global__ void __launch_bounds__(kThreads, 1)
-    smallgroup_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ SgArgs a,
-                          const __nv_bfloat16* __restrict__ w, int ohwi, int transposed) {
+    smallgroup_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+                          const __grid_constant__ SgArgs a, const __nv_bfloat16* __restrict__ w, int ohwi,
+                          int transposed) {
+  constexpr int IN = In<CPG>::n;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* wsm = reinterpret_cast<float*>(smem + a.stages * a.stage_bytes);  // [tap][64][CPG]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.stages * a.stage_bytes + a.wbytes);
-  uint64_t* empty = full + kMaxStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxStages);
+  uint8_t* out_s = smem + a.stages * a.stage_bytes;                     // 2 output staging tiles
+  float* wsm = reinterpret_cast<float*>(out_s + 2 * a.out_bytes);       // [tap][64][CPG]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(wsm) + a.wbytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kMaxStages);
   const int KH = K3 ? 3 : a.KH, KW = K3 ? 3 : a.KW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.stages; ++i) {
-      ptx::mbar_init(full + i, 1);
-      ptx::mbar_init(empty + i, kCompute);
-    }
+    for (int i = 0; i < a.stages; ++i) ptx::mbar_init(full + i, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -156,111 +205,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ctas_per_chunk = gridDim.x / a.nchunk;
   const int first = blockIdx.x / a.nchunk;
   const int taps = KH * KW;
+  // Thread 0 issues the halo loads: the k-th tile of this CTA goes to stage k % stages and completes
+  // phase k / stages of that stage's barrier.  Stage s is reloaded only after the block-wide barrier
+  // that follows the reads of the tile it held.
+  int issued = 0;
+  auto issue = [&](int k) {
+    const int t = first + k * ctas_per_chunk;
+    if (t >= a.tiles_per_chunk) return;
+    const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
+    const int s = k % a.stages;
+    ptx::mbar_arrive_expect_tx(full + s, uint32_t(a.box_bytes));
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+        "%6}], [%2];" ::"r"(ptx::smem_addr(smem + s * a.stage_bytes)),
+        "l"(&xmap), "r"(ptx::smem_addr(full + s)), "r"(chunk * 64), "r"(tw * kTC * a.SW - a.PW),
+        "r"(th * TR * a.SH - a.PH), "r"(n)
+        : "memory");
+    issued = k + 1;
+  };
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tmap(&xmap);
+    for (int k = 0; k < a.stages; ++k) issue(k);  // the first halos first: they come from HBM
+  }
+  // weights [tap][warp][k][4 channels] (a warp's channels for one input are one 16-byte piece)
   for (int e = threadIdx.x; e < taps * 64 * CPG; e += kThreads) {
-    const int k = e % CPG, j = (e / CPG) % 64, t = e / (64 * CPG);
-    wsm[e] = weight_at<CPG>(w, ohwi != 0, transposed != 0, KH, KW, chunk * 64 + j, k, t / KW, t % KW);
+    const int j = e & 3, k = (e >> 2) % CPG, wq = (e / (4 * CPG)) % 16, t = e / (64 * CPG);
+    wsm[e] = weight_at<CPG>(w, ohwi != 0, transposed != 0, KH, KW, chunk * 64 + wq * 4 + j, k, t / KW, t % KW);
   }
   __syncthreads();
 
-  if (warp == kWarps) {  // ---------------------------------------------------- producer
-    if (lane == 0) {
-      ptx::prefetch_tmap(&xmap);
-      int st = 0, issued = 0;
-      uint32_t ph = 0;
-      for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
-        const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
-        if (!ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 64u, a.wait_ns)) break;
-        ptx::mbar_arrive_expect_tx(full + st, uint32_t(a.box_bytes));
-        asm volatile(
-            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
-            "%6}], [%2];" ::"r"(ptx::smem_addr(smem + st * a.stage_bytes)),
-            "l"(&xmap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC * a.SW - a.PW),
-            "r"(th * kTR * a.SH - a.PH), "r"(n)
-            : "memory");
-        ++issued;
-        if (++st == a.stages) { st = 0; ph ^= 1; }
-      }
-      // Drain: the loads still in flight target this CTA's shared memory, so they must land before
-      // the CTA may leave (after an abort the compute warps no longer consume them).
-      for (int k = max(0, issued - a.stages); k < issued; ++k)
-        ptx::mbar_wait_drain(full + (k % a.stages), uint32_t((k / a.stages) & 1));
-    }
-    __syncwarp();
-    return;
-  }
-
-  // ------------------------------------------------------------------ compute warps
-  const int c = chunk * 64 + warp * 8;  // this warp's 8 output channels
-  float b[8];
+  const int c = chunk * 64 + warp * 4;  // this warp's 4 output channels
+  const int piece = warp >> 1;          // its 16-byte piece of a pixel's 64 channels
+  const int half = warp & 1;            // and the 8-byte half of it (CPG <= 4)
+  float b[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = a.bias ? __ldg(a.bias + c + j) : 0.f;
-  const float4* wv = reinterpret_cast<const float4*>(wsm) + warp * 2 * CPG;  // tap 0, this warp's channels
-  uint4* yv = reinterpret_cast<uint4*>(a.y);
-  const int cvec = a.C / 8;
-  int st = 0;
-  uint32_t ph = 0;
-  for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
+  for (int j = 0; j < 4; ++j) b[j] = a.bias ? __ldg(a.bias + c + j) : 0.f;
+  const uint32_t wv = ptx::smem_addr(wsm) + uint32_t(warp * CPG * 16);  // tap 0, this warp's weights
+  for (int k = 0;; ++k) {
+    const int t = first + k * ctas_per_chunk;
+    if (t >= a.tiles_per_chunk) break;
     const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
-    if (!ptx::mbar_wait(full + st, ph, abort_flag, a.status, 64u, a.wait_ns)) break;
+    const int st = k % a.stages;
+    const bool got = ptx::mbar_wait(full + st, uint32_t((k / a.stages) & 1), abort_flag, a.status, 64u, a.wait_ns);
     const uint32_t base = ptx::smem_addr(smem + st * a.stage_bytes);
-    float acc[kTR][8];
+    uint64_t acc[TR][2];  // channel pairs (0, 1) and (2, 3) of each row
 #pragma unroll
-    for (int r = 0; r < kTR; ++r)
+    for (int r = 0; r < TR; ++r) {
+      acc[r][0] = pack2f(b[0], b[1]);
+      acc[r][1] = pack2f(b[2], b[3]);
+    }
+    if (got) {
+      if constexpr (K3 && CPG <= 4) {
+        // Each of the (TR + 2) x 3 halo pixels a thread reads is loaded and converted once and feeds
+        // every output row that reads it through its kernel row; the weights of one kernel column
+        // (three taps) stay in registers meanwhile.
+        constexpr int IC = kTC + 2;
+#pragma unroll 1
+        for (int kw = 0; kw < 3; ++kw) {
+          uint64_t wt[3][CPG][2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[r][j] = b[j];
-    if constexpr (K3 && CPG <= 4) {
-      // Each of the (4 + 2) x 3 halo pixels a thread reads is loaded and converted once and feeds
-      // every output row that reads it through its kernel row; the weights of one kernel column
-      // (three taps) stay in registers meanwhile.
-      constexpr int IC = kTC + 2;
+          for (int kh = 0; kh < 3; ++kh) load_tap_weights<CPG>(wv + uint32_t((kh * 3 + kw) * 64 * CPG * 4), wt[kh]);
 #pragma unroll
-      for (int kw = 0; kw < 3; ++kw) {
-        float wt[3][8][CPG];
+          for (int rho = 0; rho < TR + 2; ++rho) {
+            float xf[IN];
+            uint64_t xd[IN];
+            load_pixel<CPG>(base, rho * IC + lane + kw, piece, half, xf);
+            dup_pairs<CPG>(xf, xd);
 #pragma unroll
-        for (int kh = 0; kh < 3; ++kh) load_tap_weights<CPG>(wv + (kh * 3 + kw) * (64 * CPG / 4), wt[kh]);
-#pragma unroll
-        for (int rho = 0; rho < kTR + 2; ++rho) {
-          float xf[8];
-          load_pixel(base, rho * IC + lane + kw, warp, xf);
-#pragma unroll
-          for (int kh = 0; kh < 3; ++kh)
-            if (rho - kh >= 0 && rho - kh < kTR) group_fma<CPG>(acc[rho - kh], xf, wt[kh]);
+            for (int kh = 0; kh < 3; ++kh)
+              if (rho - kh >= 0 && rho - kh < TR) group_fma<CPG>(acc[rho - kh], xd, wt[kh]);
+          }
         }
-      }
-    } else {
-      const int SH = K3 ? 1 : a.SH, SW = K3 ? 1 : a.SW, DH = K3 ? 1 : a.DH, DW = K3 ? 1 : a.DW;
-      const int IC = K3 ? kTC + 2 : a.ic;
+      } else {
+        const int SH = K3 ? 1 : a.SH, SW = K3 ? 1 : a.SW, DH = K3 ? 1 : a.DH, DW = K3 ? 1 : a.DW;
+        const int IC = K3 ? kTC + 2 : a.ic;
+#pragma unroll 1
+        for (int kh = 0; kh < KH; ++kh) {
+#pragma unroll 1
+          for (int kw = 0; kw < KW; ++kw) {
+            uint64_t wt[CPG][2];
+            load_tap_weights<CPG>(wv + uint32_t((kh * KW + kw) * 64 * CPG * 4), wt);
+            const int col = lane * SW + kw * DW;
 #pragma unroll
-      for (int kh = 0; kh < KH; ++kh) {
-#pragma unroll
-        for (int kw = 0; kw < KW; ++kw) {
-          float wt[8][CPG];  // the tap's weights of this warp's 8 channels (the same for every lane)
-          load_tap_weights<CPG>(wv + (kh * KW + kw) * (64 * CPG / 4), wt);
-          const int col = lane * SW + kw * DW;
-#pragma unroll
-          for (int r = 0; r < kTR; ++r) {
-            float xf[8];
-            load_pixel(base, (r * SH + kh * DH) * IC + col, warp, xf);
-            group_fma<CPG>(acc[r], xf, wt);
+            for (int r = 0; r < TR; ++r) {
+              float xf[IN];
+              uint64_t xd[IN];
+              load_pixel<CPG>(base, (r * SH + kh * DH) * IC + col, piece, half, xf);
+              dup_pairs<CPG>(xf, xd);
+              group_fma<CPG>(acc[r], xd, wt);
+            }
           }
         }
       }
     }
-    ptx::mbar_arrive(empty + st);
-    if (++st == a.stages) { st = 0; ph ^= 1; }
-    const int ow = tw * kTC + lane;
+    // The output tile: the store that last used this staging buffer must have read it, and all
+    // threads must agree to go on (leave together if any of them gave up: the barriers below count
+    // every thread).  Past this barrier every thread has finished reading input stage st.
+    const int ob = k & 1;
+    if (threadIdx.x == 0) bulk_wait_read<1>();
+    uint32_t stop;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(stop)
+        : "r"(uint32_t(got)), "n"(kThreads)
+        : "memory");
+    if (stop) break;
+    if (threadIdx.x == 0) issue(k + a.stages);  // refill the stage just read
+    const uint32_t ob_s = ptx::smem_addr(out_s + ob * a.out_bytes);
 #pragma unroll
-    for (int r = 0; r < kTR; ++r) {
-      const int oh = th * kTR + r;
-      if (oh < a.Ho && ow < a.Wo) {
-        uint4 o;
-        o.x = ptx::pack_bf16x2(acc[r][0], acc[r][1]);
-        o.y = ptx::pack_bf16x2(acc[r][2], acc[r][3]);
-        o.z = ptx::pack_bf16x2(acc[r][4], acc[r][5]);
-        o.w = ptx::pack_bf16x2(acc[r][6], acc[r][7]);
-        yv[(size_t(n * a.Ho + oh) * a.Wo + ow) * cvec + (c >> 3)] = o;
-      }
+    for (int r = 0; r < TR; ++r) {
+      const int line = r * kTC + lane;  // the staging tile is (row, column, 64 channels), swizzled
+      float y0, y1, y2, y3;
+      unpack2f(acc[r][0], y0, y1);
+      unpack2f(acc[r][1], y2, y3);
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ob_s + uint32_t(line * 128 + ((piece ^ (line & 7)) << 4) +
+                                                                            half * 8)),
+                   "r"(ptx::pack_bf16x2(y0, y1)), "r"(ptx::pack_bf16x2(y2, y3))
+                   : "memory");
     }
+    ptx::fence_proxy_async_smem();  // the tile's writes before the tensor store reads it
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+    if (threadIdx.x == 0) {  // rows and columns past the output are clipped by the store
+      tma_store_4d(&ymap, ob_s, chunk * 64, tw * kTC, th * TR, n);
+      bulk_commit();
+    }
+  }
+  if (threadIdx.x == 0) {
+    // Drain: loads still in flight (after an abort) write this CTA's shared memory; the last `stages`
+    // issued are the only ones that can be.
+    for (int k = max(0, issued - a.stages); k < issued; ++k)
+      ptx::mbar_wait_drain(full + (k % a.stages), uint32_t((k / a.stages) & 1));
+    bulk_wait_all();  // every tensor store has completed before the CTA leaves
   }
 }
 
@@ -322,9 +398,9 @@ __global__ void __launch_bounds__(256) smallgroup_dgrad_kernel(SgDgArgs a, const
         unpack8(__ldg(dyv + (size_t(n * a.OH + oh) * a.OW + ow) * cvec + (c >> 3)), g);
         const float* wt = wsg + ((kh * KW + kw) * cpb + cv * 8) * CPG;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int o = 0; o < CPG; ++o)
 #pragma unroll
-          for (int o = 0; o < CPG; ++o) acc[j] = fmaf(g[(j / CPG) * CPG + o], wt[j * CPG + o], acc[j]);
+          for (int j = 0; j < 8; ++j) acc[j] = fmaf(g[(j / CPG) * CPG + o], wt[j * CPG + o], acc[j]);
       }
     }
     uint4 o;
@@ -377,19 +453,27 @@ bool plan(const Problem& p, bool dgrad, SgArgs& a, size_t& smem) {
     a.PW = int((p.KW - 1) * p.DW - p.PW);
   }
   if (a.SH > 2 || a.SW > 2) return false;
-  const int64_t ir = int64_t(kTR - 1) * a.SH + int64_t(a.KH - 1) * a.DH + 1;
-  const int64_t ic = int64_t(kTC - 1) * a.SW + int64_t(a.KW - 1) * a.DW + 1;
-  if (ir > 256 || ic > 256) return false;  // TMA box extents
-  a.ir = int(ir);
-  a.ic = int(ic);
-  a.box_bytes = a.ir * a.ic * 128;
-  a.stage_bytes = (a.box_bytes + 1023) & ~1023;
+  // 8 output rows per tile at unit row stride, else (or when the halo leaves room for fewer than two
+  // stages) 4
   a.wbytes = int(p.KH * p.KW) * 64 * int(p.Cin / p.G) * 4;
-  const int fixed = 1024 + a.wbytes + 2 * kMaxStages * 8 + 16;
-  a.stages = std::min(kMaxStages, (kSmemLimit - fixed) / a.stage_bytes);
+  int fixed = 0;
+  a.stages = 0;
+  for (int tr = (a.SH == 1 ? 8 : 4); tr >= 4 && a.stages < 2; tr -= 4) {
+    a.tr = tr;
+    const int64_t ir = int64_t(a.tr - 1) * a.SH + int64_t(a.KH - 1) * a.DH + 1;
+    const int64_t ic = int64_t(kTC - 1) * a.SW + int64_t(a.KW - 1) * a.DW + 1;
+    if (ir > 256 || ic > 256) return false;  // TMA box extents
+    a.ir = int(ir);
+    a.ic = int(ic);
+    a.box_bytes = a.ir * a.ic * 128;
+    a.stage_bytes = (a.box_bytes + 1023) & ~1023;
+    a.out_bytes = a.tr * kTC * 128;
+    fixed = 1024 + 2 * a.out_bytes + a.wbytes + kMaxStages * 8 + 16;
+    a.stages = std::max(0, std::min(kMaxStages, (kSmemLimit - fixed) / a.stage_bytes));
+  }
   if (a.stages < 2) return false;
   a.nchunk = a.C / 64;
-  a.tiles_h = (a.Ho + kTR - 1) / kTR;
+  a.tiles_h = (a.Ho + a.tr - 1) / a.tr;
   a.tiles_w = (a.Wo + kTC - 1) / kTC;
   const int64_t tpc = int64_t(a.N) * a.tiles_h * a.tiles_w;
   if (tpc >= (int64_t(1) << 30)) return false;
@@ -398,50 +482,63 @@ bool plan(const Problem& p, bool dgrad, SgArgs& a, size_t& smem) {
   return true;
 }
 
+// (C, W, H, N) map of an NHWC bf16 tensor with boxes of 64 channels x bw columns x bh rows, 128-byte
+// swizzle (zero fill on loads past the edges; stores past them are clipped).
+bool encode_act(CUtensorMap* map, const void* base, int C, int W, int H, int N, int bw, int bh) {
+  auto fn = sg_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {cuuint64_t(C), cuuint64_t(W), cuuint64_t(H), cuuint64_t(N)};
+  cuuint64_t strides[3] = {cuuint64_t(C) * 2, cuuint64_t(W) * C * 2, cuuint64_t(H) * W * C * 2};
+  cuuint32_t box[4] = {64, cuuint32_t(bw), cuuint32_t(bh), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int CPG, int TR, int K3>
+gbconv_status run_tiled(const CUtensorMap& xmap, const CUtensorMap& ymap, const SgArgs& a, size_t smem,
+                        const void* w, int ohwi, int dgrad, const Launch& l) {
+  auto kern = smallgroup_tma_kernel<CPG, TR, K3>;
+  static std::atomic<int> raised[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  if (!raised[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
+      return GBCONV_ECUDA;
+    raised[dev].store(1, std::memory_order_release);
+  }
+  // a multiple of the chunk count, at most one CTA per SM and per tile
+  int64_t grid = std::max<int64_t>(a.nchunk, (int64_t(l.num_sms) / a.nchunk) * a.nchunk);
+  grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
+  return launch_kernel(kern, dim3(unsigned(grid)), dim3(kThreads), smem, l.stream, xmap, ymap, a,
+                       static_cast<const __nv_bfloat16*>(w), ohwi, dgrad) == cudaSuccess
+             ? GBCONV_OK
+             : GBCONV_ECUDA;
+}
+
 template <int CPG>
 gbconv_status launch_tiled(const Problem& p, bool dgrad, const void* src, const void* w, const float* bias, void* dst,
                            const Launch& l) {
   SgArgs a;
   size_t smem = 0;
   if (!plan(p, dgrad, a, smem)) return GBCONV_EUNSUPPORTED;
-  auto fn = sg_encode_fn();
-  if (!fn) return GBCONV_ECUDA;
   a.bias = bias;
-  a.y = static_cast<__nv_bfloat16*>(dst);
   a.status = l.status;
   a.wait_ns = l.wait_ns;
-  CUtensorMap map;
-  cuuint64_t dims[4] = {cuuint64_t(a.C), cuuint64_t(a.Wi), cuuint64_t(a.Hi), cuuint64_t(a.N)};
-  cuuint64_t strides[3] = {cuuint64_t(a.C) * 2, cuuint64_t(a.Wi) * a.C * 2, cuuint64_t(a.Hi) * a.Wi * a.C * 2};
-  cuuint32_t box[4] = {64, cuuint32_t(a.ic), cuuint32_t(a.ir), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(src), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return GBCONV_ECUDA;
-  // the read map's stride and dilation (the stride-1 input gradient reads at unit stride)
-  // (the compile-time 3x3 variant only up to 4 channels per group: at 8 its weights and
-  // accumulators no longer fit the registers)
+  CUtensorMap xmap, ymap;
+  if (!encode_act(&xmap, src, a.C, a.Wi, a.Hi, a.N, a.ic, a.ir)) return GBCONV_ECUDA;
+  if (!encode_act(&ymap, dst, a.C, a.Wo, a.Ho, a.N, kTC, a.tr)) return GBCONV_ECUDA;
+  const int ohwi = p.ohwi ? 1 : 0;
+  // the compile-time 3x3 variant up to 4 channels per group (at 8 its weights no longer fit the
+  // registers next to the accumulators); the read map's stride and dilation decide (the stride-1
+  // input gradient reads at unit stride)
   const bool k3 = CPG <= 4 && a.KH == 3 && a.KW == 3 && a.SH == 1 && a.SW == 1 && a.DH == 1 && a.DW == 1;
-  auto kern = smallgroup_tma_kernel<CPG, 0>;
   if constexpr (CPG <= 4) {
-    if (k3) kern = smallgroup_tma_kernel<CPG, 1>;
+    if (k3) return run_tiled<CPG, 8, 1>(xmap, ymap, a, smem, w, ohwi, int(dgrad), l);
   }
-  static std::atomic<int> raised[2][64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
-  if (!raised[k3][dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
-      return GBCONV_ECUDA;
-    raised[k3][dev].store(1, std::memory_order_release);
-  }
-  // a multiple of the chunk count, at most one CTA per SM and per tile
-  int64_t grid = std::max<int64_t>(a.nchunk, (int64_t(l.num_sms) / a.nchunk) * a.nchunk);
-  grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
-  return launch_kernel(kern, dim3(unsigned(grid)), dim3(kThreads), smem, l.stream, map, a,
-                       static_cast<const __nv_bfloat16*>(w), int(p.ohwi), int(dgrad)) == cudaSuccess
-             ? GBCONV_OK
-             : GBCONV_ECUDA;
+  if (a.tr == 8) return run_tiled<CPG, 8, 0>(xmap, ymap, a, smem, w, ohwi, int(dgrad), l);
+  return run_tiled<CPG, 4, 0>(xmap, ymap, a, smem, w, ohwi, int(dgrad), l);
 }
 
 template <int CPG>
@@ -514,7 +611,7 @@ bool smallgroup_describe(const Problem& p, bool dgrad, char* buf, size_t len) {
   size_t smem = 0;
   if (!plan(p, dgrad, a, smem)) return false;
   std::snprintf(buf, len, "smallgroup%s cpg=%d tile=%dx%d halo=%dx%d stages=%d chunks=%d tiles=%d smem=%zu",
-                dgrad ? "_dgrad" : "", int(p.Cin / p.G), kTR, kTC, a.ir, a.ic, a.stages, a.nchunk,
+                dgrad ? "_dgrad" : "", int(p.Cin / p.G), a.tr, kTC, a.ir, a.ic, a.stages, a.nchunk,
                 a.nchunk * a.tiles_per_chunk, smem);
   return true;
 }

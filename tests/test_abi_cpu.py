@@ -367,3 +367,16 @@ def test_small_group_regime_selection(gb, kw, fam_fwd, fam_dgrad):
     d = lib_desc(gb, kw)
     assert gb.gbconv_select(d, 0) == fam_fwd
     assert gb.gbconv_select(d, 1) == fam_dgrad
+
+
+def test_gpu_parity_cases_select_their_families(gb):
+    # every GPU parity case asserts the kernel family it exercises; the choice is made on the host,
+    # so a plan that no longer fits (and would silently fall back) is caught here without a GPU
+    pytest.importorskip("torch")
+    from tests import test_gpu_parity as t
+    for kw, op, fam in t.SMALL:
+        assert gb.gbconv_select(lib_desc(gb, kw), 1 if op == "dgrad" else 0) == fam, (kw, op)
+    for kw, fam in t.TRANSPOSE:
+        assert gb.gbconv_select(lib_desc(gb, kw), 1) == fam, kw
+    for kw, fam in t.WGRAD:
+        assert gb.gbconv_select(lib_desc(gb, kw), 2) == fam, kw

@@ -92,6 +92,14 @@ SMALL = [
     (shape_kw(n=2, in_size=(10, 9), c_in=96, c_out=48, k=(3, 2), pad=(1, 0), bias=True), "fwd", "implicit"),
     (shape_kw(n=1, in_size=(12, 7), c_in=8, c_out=8), "fwd", "implicit"),
     (shape_kw(n=3, in_size=(60, 60), c_in=64, c_out=64, bias=True), "fwd", "implicit"),
+    # C_out = 64 (64-wide N tiles): odd output widths, KW = 2 and 5, a row stride, two k-blocks, a
+    # k-block tail, (begin, end) padding, row dilation
+    (shape_kw(n=2, in_size=(9, 13), c_in=64, c_out=64, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(10, 12), c_in=64, c_out=64, k=(2, 2), pad=(0, 0)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(11, 15), c_in=128, c_out=64, k=(3, 5), pad=(1, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(17, 14), c_in=72, c_out=64, stride=(2, 1), bias=True), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(12, 11), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(30, 25), c_in=64, c_out=64, k=(3, 3), pad=(2, 1), dil=(2, 1)), "fwd", "implicit"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
