@@ -96,6 +96,10 @@ struct PhaseHdr {
   int src_ad[kMaxSrc];
   int jd;      // 3-D: depth slices of this phase per batch element
   int out_pd;  // 3-D: output depth of the phase's slice j = 0 (the depth phase ad)
+  // Column strips: an image wider than one halo box allows is cut into nstrips vertical strips of
+  // strip_w valid columns (the last one may be narrower), each with its own virtual grid of pitch
+  // P = strip_w + the horizontal reach.  Work items run over (image, strip) pairs.
+  int strip_w, nstrips;
 };
 
 struct Phase : PhaseHdr {
@@ -314,19 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int src = 0; ok && src < (MSRC ? ph.nsrc : 1); ++src) {
             if (!(ok = ptx::mbar_wait(emptyA + sa, pa ^ 1, abort_flag, a.status, 1u, a.wait_ns))) break;
             ptx::mbar_arrive_expect_tx(fullA + sa, uint32_t(ph.a_bytes));
-            if (MSRC && a.depth_od > 0) {  // 3-D: item image it.n is a (batch, depth slice) pair
-              const int nn = it.n / ph.jd, od = it.n - nn * ph.jd;
+            // the item's (image, column strip): the strip's virtual column 0 is phase-grid column
+            // strip * strip_w
+            const int img = it.n / ph.nstrips, col = (ph.cmin + (it.n - img * ph.nstrips) * ph.strip_w) * ph.col_step;
+            if (MSRC && a.depth_od > 0) {  // 3-D: image img is a (batch, depth slice) pair
+              const int nn = img / ph.jd, od = img - nn * ph.jd;
               tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                          kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
-                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], od * a.depth_sd + ph.src_ad[src], nn);
+                          kb * kKB, col + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src],
+                          od * a.depth_sd + ph.src_ad[src], nn);
             } else if (a.G > 1) {  // (channel in group, group, column, row, image)
               tma_load_5d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                          kb * kKB, it.g, ph.cmin * ph.col_step + ph.src_aw[src],
-                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], it.n);
+                          kb * kKB, it.g, col + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src], img);
             } else {
               tma_load_4d(ptx::smem_addr(a_base + size_t(sa) * a.a_stage_bytes), &maps.a[it.phase], fullA + sa,
-                          kb * kKB, ph.cmin * ph.col_step + ph.src_aw[src],
-                          (ra + ph.rmin) * ph.row_step + ph.src_ah[src], it.n);
+                          kb * kKB, col + ph.src_aw[src], (ra + ph.rmin) * ph.row_step + ph.src_ah[src], img);
             }
             ++issued_a;
             if (++sa == a.sa) { sa = 0; pa ^= 1; }
@@ -487,9 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has_bias = a.bias != nullptr;
       // The phase geometry in registers: read from shared memory inside the store loop, every
       // field would be re-read after each staging load (those are asm with memory clobbers).
-      const int ph_R = ph.R, ph_OWv = ph.OWv, ph_P = ph.P, ph_ntaps = ph.ntaps;
-      // 3-D: the item's image is batch element it.n / jd at output depth out_pd + (it.n % jd) * out_sd
-      const int img = a.depth_od > 0 ? (it.n / ph.jd) * a.out_d + ph.out_pd + (it.n % ph.jd) * a.out_sd : it.n;
+      const int ph_R = ph.R, ph_P = ph.P, ph_ntaps = ph.ntaps;
+      // the item's (image, column strip); the strip's valid columns
+      const int nimg = it.n / ph.nstrips, col0 = (it.n - nimg * ph.nstrips) * ph.strip_w;
+      const int ph_OWv = min(ph.strip_w, ph.OWv - col0);
+      // 3-D: the item's image is batch element nimg / jd at output depth out_pd + (nimg % jd) * out_sd
+      const int img = a.depth_od > 0 ? (nimg / ph.jd) * a.out_d + ph.out_pd + (nimg % ph.jd) * a.out_sd : nimg;
       const int row_base = img * a.Ho + ph.out_ph, ph_sh = ph.out_sh, ph_sw = ph.out_sw, ph_pw = ph.out_pw;
       const int Wo = a.Wo, Cn = a.Cn;
       bf16* const out = a.out;
@@ -562,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
                              : "r"(stage_s + uint32_t(row * kPitch + part * 16)));
-                pix[i] = (r < ph_R && colv < ph_OWv) ? (row_base + r * ph_sh) * Wo + colv * ph_sw + ph_pw : -1;
+                pix[i] = (r < ph_R && colv < ph_OWv) ? (row_base + r * ph_sh) * Wo + (col0 + colv) * ph_sw + ph_pw : -1;
                 row += kRowStep;
                 colv += kRowStep;
                 while (colv >= ph_P) { colv -= ph_P; ++r; }
@@ -628,7 +636,21 @@ int pick_bn(int64_t cn) {
 struct PhaseSpec {
   Phase ph;
   int maxoff;
+  // tap t reads the halo at (tdr[t], tdc[t]) rows / columns past virtual (0, 0); the offsets span
+  // rspan rows and cspan columns (the horizontal reach)
+  int tdr[kMaxTapsPerPhase], tdc[kMaxTapsPerPhase];
+  int rspan, cspan;
 };
+
+// Lays a phase out on strips of strip_w valid columns: pitch, tap offsets and the largest offset.
+void layout_strips(PhaseSpec& s, int strip_w) {
+  Phase& ph = s.ph;
+  ph.strip_w = strip_w;
+  ph.nstrips = (ph.OWv + strip_w - 1) / strip_w;
+  ph.P = strip_w + s.cspan;
+  for (int t = 0; t < ph.ntaps; ++t) ph.tap_off[t] = s.tdr[t] * ph.P + s.tdc[t];
+  s.maxoff = s.rspan * ph.P + s.cspan;
+}
 
 // Fills the per-phase box geometry and counts for a tile of 128*nsub positions.
 bool finish_phase(PhaseSpec& s, int nsub, int N) {
@@ -642,7 +664,7 @@ bool finish_phase(PhaseSpec& s, int nsub, int N) {
   ph.a_bytes = 128 * ph.P * ph.bh;
   const int64_t per_img = int64_t(ph.R) * ph.P;
   ph.tiles = int((per_img + mt - 1) / mt);
-  return int64_t(N) * ph.tiles < (int64_t(1) << 30);
+  return int64_t(N) * ph.nstrips * ph.tiles < (int64_t(1) << 30);
 }
 
 bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
@@ -742,7 +764,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         const int start = k;
         for (int t = 0; t < a.T; ++t) {
           if (kds[t] != kd || ahs[t] != ah || aws[t] != aw) continue;
-          ph.tap_off[k] = (drs[t] - rmin) * ph.P + (dcs[t] - cmin);
+          s.tdr[k] = drs[t] - rmin;
+          s.tdc[k] = dcs[t] - cmin;
           ph.tap_w[k] = t;
           ++k;
         }
@@ -755,7 +778,8 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
         ++ph.nsrc;
       }
     ph.src_t0[ph.nsrc] = int8_t(k);
-    s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+    s.rspan = rmax - rmin;
+    s.cspan = cmax - cmin;
     ph.jd = deep ? int(p.OD) : 1;
     ph.out_pd = 0;
     specs[nph++] = s;
@@ -805,49 +829,61 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
           for (int i = 0; i < nkh; ++i)
             for (int j = 0; j < nkw; ++j) {
               const int t = (k * nkh + i) * nkw + j;
-              ph.tap_off[t] = (drs[i] - rmin) * ph.P + (dcs[j] - cmin);
+              s.tdr[t] = drs[i] - rmin;
+              s.tdc[t] = dcs[j] - cmin;
               ph.tap_w[t] = int((kds[k] * p.KH + khs[i]) * p.KW + kws[j]);
             }
         }
         ph.src_t0[nkd] = int8_t(ph.ntaps);
-        s.maxoff = (rmax - rmin) * ph.P + (cmax - cmin);
+        s.rspan = rmax - rmin;
+        s.cspan = cmax - cmin;
         specs[nph++] = s;
       }
     // Longest phases first, so the persistent CTAs finish together.
     std::stable_sort(specs, specs + nph, [](const PhaseSpec& x, const PhaseSpec& y) { return x.ph.ntaps > y.ph.ntaps; });
   }
   if (nph == 0) return false;
-  int item = 0, a_max = 0;
-  for (int i = 0; i < nph; ++i) {
-    const int imgs = a.N * specs[i].ph.jd;  // (batch, depth slice) pairs; 2-D: the batch
-    if (!finish_phase(specs[i], pl.nsub, imgs)) return false;
-    specs[i].ph.item0 = item;
-    const int64_t n_all = int64_t(a.n_tiles) * a.G;  // (group, output tile) pairs
-    if (int64_t(item) + int64_t(imgs) * specs[i].ph.tiles * n_all >= (int64_t(1) << 30)) return false;
-    item += int(imgs * specs[i].ph.tiles * n_all);
-    a.ph[i] = specs[i].ph;
-    a_max = std::max(a_max, specs[i].ph.a_bytes);
-  }
   a.nphase = nph;
-  a.total_items = item;
-  a.a_stage_bytes = (a_max + 1023) & ~1023;
   a.b_tile_bytes = pl.bn * kKB * 2;
   pl.bres = !dgrad && a.G == 1 && a.n_tiles == 1 && a.T * a.kb_count * a.b_tile_bytes <= 110 * 1024;
   const size_t block = size_t(128) * ((pl.bn % 128 == 0 ? 128 : 64) * 2 + 16);
-  for (int bufs = 2; bufs >= 1; --bufs) {
-    const size_t fixed = 1024 + bufs * block + size_t(a.bias_n) * 4 +
-                         size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
-                         8 * (2 * 4 + 2 * 8 + 6) + 16;
-    for (int sa = 3; sa >= 2; --sa) {
-      for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
-        const size_t total =
-            fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T * a.kb_count : sb) * a.b_tile_bytes;
-        if (total <= size_t(kSmemLimit)) {
-          a.sa = sa;
-          a.sb = pl.bres ? 1 : sb;
-          a.stage_bufs = bufs;
-          pl.smem = total;
-          return true;
+  // The fewest column strips per image whose halo boxes fit a box and the shared memory (one strip:
+  // whole image rows).
+  int max_w = 1;
+  for (int i = 0; i < nph; ++i) max_w = std::max(max_w, specs[i].ph.OWv);
+  for (int k = 1; k <= max_w; ++k) {
+    int item = 0, a_max = 0;
+    bool fits = true;
+    for (int i = 0; fits && i < nph; ++i) {
+      const int imgs = a.N * specs[i].ph.jd;  // (batch, depth slice) pairs; 2-D: the batch
+      layout_strips(specs[i], (specs[i].ph.OWv + k - 1) / k);
+      if (!finish_phase(specs[i], pl.nsub, imgs)) { fits = false; break; }
+      specs[i].ph.item0 = item;
+      const int64_t n_all = int64_t(a.n_tiles) * a.G;  // (group, output tile) pairs
+      const int64_t n_items = int64_t(imgs) * specs[i].ph.nstrips * specs[i].ph.tiles * n_all;
+      if (int64_t(item) + n_items >= (int64_t(1) << 30)) return false;
+      item += int(n_items);
+      a.ph[i] = specs[i].ph;
+      a_max = std::max(a_max, specs[i].ph.a_bytes);
+    }
+    if (!fits) continue;
+    a.total_items = item;
+    a.a_stage_bytes = (a_max + 1023) & ~1023;
+    for (int bufs = 2; bufs >= 1; --bufs) {
+      const size_t fixed = 1024 + bufs * block + size_t(a.bias_n) * 4 +
+                           size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
+                           8 * (2 * 4 + 2 * 8 + 6) + 16;
+      for (int sa = 3; sa >= 2; --sa) {
+        for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
+          const size_t total =
+              fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T * a.kb_count : sb) * a.b_tile_bytes;
+          if (total <= size_t(kSmemLimit)) {
+            a.sa = sa;
+            a.sb = pl.bres ? 1 : sb;
+            a.stage_bufs = bufs;
+            pl.smem = total;
+            return true;
+          }
         }
       }
     }
@@ -989,9 +1025,9 @@ bool implicit_describe(const Problem& p, bool dgrad, char* buf, size_t len) {
   for (int i = 0; i < a.nphase; ++i) taps = std::max(taps, a.ph[i].ntaps);
   std::snprintf(buf, len,
                 "implicit_gemm %s bn=%d nsub=%d phases=%d sources=%d taps=%d items=%d kb=%d weights=%s "
-                "a_stages=%d b_stages=%d stage_bufs=%d smem=%zu",
+                "a_stages=%d b_stages=%d stage_bufs=%d strips=%d smem=%zu",
                 dgrad ? "dgrad" : "fwd", pl.bn, pl.nsub, a.nphase, a.ph[0].nsrc, taps, a.total_items, a.kb_count,
-                pl.bres ? "resident" : "streamed", a.sa, pl.bres ? 0 : a.sb, a.stage_bufs, pl.smem);
+                pl.bres ? "resident" : "streamed", a.sa, pl.bres ? 0 : a.sb, a.stage_bufs, a.ph[0].nstrips, pl.smem);
   return true;
 }
 

@@ -100,6 +100,18 @@ SMALL = [
     (shape_kw(n=1, in_size=(17, 14), c_in=72, c_out=64, stride=(2, 1), bias=True), "fwd", "implicit"),
     (shape_kw(n=2, in_size=(12, 11), c_in=64, c_out=64, pad=(0, 1), pad_end=(2, 0)), "fwd", "implicit"),
     (shape_kw(n=2, in_size=(30, 25), c_in=64, c_out=64, k=(3, 3), pad=(2, 1), dil=(2, 1)), "fwd", "implicit"),
+    # images wider than one halo box: column strips (each with its own virtual grid), the last strip
+    # narrower; strided forward, grouped, 3-D, dilation, C_out tails
+    (shape_kw(n=1, in_size=(9, 150), c_in=64, c_out=64, bias=True), "fwd", "implicit"),
+    (shape_kw(n=2, in_size=(6, 113), c_in=128, c_out=96, k=(3, 5), pad=(1, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(11, 230), c_in=64, c_out=128, stride=(2, 2), bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(7, 171), c_in=64, c_out=64, dil=(1, 2), pad=(1, 2)), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(6, 140), c_in=128, c_out=128, groups=2, bias=True), "fwd", "implicit"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(3, 5, 130), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+              pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(10, 150), c_in=128, c_out=128, stride=(2, 2)), "dgrad", "dgrad"),
+    (shape_kw(n=2, in_size=(5, 121), c_in=64, c_out=128), "dgrad", "dgrad"),
+    (shape_kw(n=1, in_size=(9, 233), c_in=64, c_out=64, stride=(2, 1), k=(3, 2), pad=(1, 0)), "dgrad", "dgrad"),
     # pointwise TMA GEMM: ragged M, K tail inside a 64-wide block, every N tile width
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
@@ -380,6 +392,7 @@ TRANSPOSE = [
     (shape_kw(n=2, in_size=(11, 9), c_in=64, c_out=64, groups=16), "smallgroup_dgrad"),
     (shape_kw(n=1, in_size=(10, 12), c_in=128, c_out=64, groups=2, stride=(2, 2)), "dgrad"),
     (shape_kw(n=1, in_size=(12, 10), c_in=128, c_out=128, groups=32, stride=(2, 2)), "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(8, 140), c_in=64, c_out=128, stride=(2, 2)), "dgrad"),
     (shape_kw(spatial_dims=3, n=1, in_size=(4, 8, 7), c_in=64, c_out=128, k=(3, 3, 3), stride=(1, 2, 1),
               pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi"), "dgrad"),
     (shape_kw(spatial_dims=3, n=2, in_size=(5, 6, 8), c_in=128, c_out=64, k=(3, 3, 3), stride=(2, 2, 1),
