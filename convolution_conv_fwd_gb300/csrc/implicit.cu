@@ -70,6 +70,10 @@ constexpr int kThreads = 10 * 32;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kKB = 64;  // channels per k-block: one 128-byte swizzled row
 constexpr int kMaxSrc = 9;  // activation sources of one phase: stride phases of a strided forward
+// Transposed-form staging: per epilogue half, two blocks of 32 positions x 128 channels, rows
+// padded to 320 bytes (80 words: rows r and r+1 fall 16 banks apart).
+constexpr int kTposPitch = 320;
+constexpr int kTposStage = 2 * 2 * 32 * kTposPitch;
 
 struct PhaseHdr {
   int ntaps;
@@ -206,15 +210,26 @@ __device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t saddr, uint32_t 
 
 // MSRC: phases may have several activation sources (a strided forward); otherwise every phase
 // has exactly one and the source loops fold away at compile time.
-template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC>
+//
+// TPOS (BN = 128, NSUB = 2): the product is formed transposed, D^T = W * X^T, with the tile's 128
+// output channels on the MMA's M side and its 256 positions on N.  One 128x256x16 MMA then does the
+// work of the two 128x128x16 ones and reads 12 KB of operands from shared memory instead of 16 KB
+// (the weight slice once, not once per sub-tile): shared-memory bandwidth, not the tensor pipe, is
+// what limits the 128x128 form once the TMA writes are added.  The accumulator then holds one
+// channel per TMEM lane, so the epilogue writes channel pairs straight from registers.
+template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC, bool TPOS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     implicit_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
+  static_assert(!TPOS || (BN == 128 && NSUB == 2), "the transposed form is a 128-channel x 256-position tile");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Swizzled TMA destinations and operands sit on 1024-byte boundaries.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr uint32_t kCols = 2 * NSUB * BN;
   constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BN) | (DGRAD ? (1u << 16) : 0u);
+  // The weight operand is MN-major in the gradient (C_in, the GEMM's output dimension, is
+  // contiguous): the transpose bit of B, or of A in the transposed form.
+  constexpr uint32_t kIdesc = TPOS ? ptx::idesc_bf16_f32(128, 128 * NSUB) | (DGRAD ? (1u << 15) : 0u)
+                                   : ptx::idesc_bf16_f32(128, BN) | (DGRAD ? (1u << 16) : 0u);
   constexpr int kBTile = BN * kKB * 2;
 
   uint8_t* a_base = smem;
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // two staging blocks of 128 rows x (staging group * 2 + 16) bytes
   uint8_t* stage_base = b_base + size_t(b_tiles) * kBTile;
   constexpr int kStageBlock = 128 * ((BN % 128 == 0 ? 128 : 64) * 2 + 16);
-  float* bias_s = reinterpret_cast<float*>(stage_base + a.stage_bufs * kStageBlock);
+  float* bias_s = reinterpret_cast<float*>(stage_base + (TPOS ? kTposStage : a.stage_bufs * kStageBlock));
   // Per-phase tap tables, copied from the kernel parameters: runtime-indexed
   // parameter reads are slow next to shared-memory reads in the MMA loop.
   int* taps_s = reinterpret_cast<int*>(bias_s + a.bias_n);  // [phase][off, w][kMaxTapsPerPhase]
@@ -426,10 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kKB / 16; ++j) {
                   const uint32_t b_off = DGRAD ? uint32_t(j * 2048 >> 4) : uint32_t(j * 32 >> 4);
+                  if (TPOS) {  // weights as A (128 channels), the 256 halo rows as B
+                    ptx::mma_bf16_lohi(acc, b_lo + b_off, b_hi, a_lo + uint32_t((j * 32) >> 4), a_hi, kIdesc,
+                                       j == 0 ? first : 1u);
+                  } else {
 #pragma unroll
-                  for (int s = 0; s < NSUB; ++s)
-                    ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((s * 128 * 128 + j * 32) >> 4), a_hi, b_lo + b_off,
-                                       b_hi, kIdesc, j == 0 ? first : 1u);
+                    for (int s = 0; s < NSUB; ++s)
+                      ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((s * 128 * 128 + j * 32) >> 4), a_hi,
+                                         b_lo + b_off, b_hi, kIdesc, j == 0 ? first : 1u);
+                  }
                 }
                 if (!BRES) {
                   ptx::mma_commit(emptyB + sb);
@@ -478,12 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every thread times its own wait, so after an expired wait the 64 threads of a warp pair could
       // disagree, and a thread that carried on would block at the pair barrier below for good: the
       // pair takes one decision (leave if any of its threads gave up).
+      // (In the transposed form the four warps of a half work together: the half decides.)
       uint32_t stop;
       asm volatile(
-          "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 64, p;\n\t"
+          "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
           "selp.u32 %0, 1, 0, q;\n\t}"
           : "=r"(stop)
-          : "r"(uint32_t(got)), "r"(1 + quad)
+          : "r"(uint32_t(got)), "r"(TPOS ? 6 + half : 1 + quad), "r"(TPOS ? 128 : 64)
           : "memory");
       if (stop) break;
       ptx::tc_fence_after();
@@ -501,6 +522,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_base = img * a.Ho + ph.out_ph, ph_sh = ph.out_sh, ph_sw = ph.out_sw, ph_pw = ph.out_pw;
       const int Wo = a.Wo, Cn = a.Cn;
       bf16* const out = a.out;
+      if constexpr (TPOS) {
+        // TMEM lane = output channel, column = tile position; warps w and w+4 take 128 positions
+        // each, in chunks of 32.  Lanes 2i and 2i+1 (channels c, c+1) swap one value per pair of
+        // positions, so that each lane holds both channels of one position as a 4-byte word; the
+        // four warps of a half write their words into a staged [32 positions][128 channels] block
+        // (each warp instruction fills two rows, 16 banks each), then store it as whole pixels:
+        // consecutive threads write consecutive 16-byte pieces, 256 bytes per pixel.
+        const int odd = lane & 1;
+        const float bv = has_bias ? bias_s[n0 + quad * 32 + lane] : 0.f;
+        const uint32_t stage_h = ptx::smem_addr(stage_base) + uint32_t(half * 2 * 32 * kTposPitch);
+        const uint32_t word_off = uint32_t(odd * kTposPitch + (quad * 16 + (lane >> 1)) * 4);
+        const int tp = quad * 32 + lane, part = tp & 15, row0 = tp >> 4;  // store role: piece, first row
+        const int co = n0 + part * 8;
+        const bool live = co < n_end;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          const int col = half * 128 + ch * 32;
+          const uint32_t blk = stage_h + uint32_t(sbuf * 32 * kTposPitch);
+          sbuf ^= 1;
+          uint32_t v[32];
+          if (ph_ntaps > 0) {
+            ptx::tmem_ld_32(tmem + lane_base + uint32_t(buf * 256 + col), v);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float f0 = __uint_as_float(v[2 * k]) + bv, f1 = __uint_as_float(v[2 * k + 1]) + bv;
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? f0 : f1, 1);
+            const uint32_t wd = odd ? ptx::pack_bf16x2(other, f1) : ptx::pack_bf16x2(f0, other);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(blk + uint32_t(2 * k * kTposPitch) + word_off), "r"(wd)
+                         : "memory");
+          }
+          // With two blocks per half this barrier also proves that the half finished reading the
+          // block it is about to overwrite (two chunks ago).
+          asm volatile("bar.sync %0, 128;" ::"r"(6 + half) : "memory");
+          if (live) {
+            uint4 val[4];
+            int pix[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int row = row0 + 8 * i;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
+                           : "r"(blk + uint32_t(row * kTposPitch + part * 16)));
+              const int q = it.m * 256 + col + row;
+              const int r = q / ph_P, colv = q - r * ph_P;
+              pix[i] = (r < ph_R && colv < ph_OWv) ? (row_base + r * ph_sh) * Wo + (col0 + colv) * ph_sw + ph_pw : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (pix[i] >= 0) *reinterpret_cast<uint4*>(out + size_t(pix[i]) * Cn + co) = val[i];
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
@@ -583,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.stage_bufs == 1) asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
       }
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty + buf);
     }
@@ -601,6 +680,7 @@ struct Plan {
   Maps maps;
   int bn, nsub;
   bool bres, dgrad;
+  bool tpos;  // channels on M, positions on N (the 128-channel tile)
   int row_step = 1, col_step = 1;  // strided view of the activations (strided 1x1 forward)
   size_t smem;
   int grid;
@@ -693,6 +773,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
   const int64_t Cg = dgrad ? p.cpg() : p.opg();                                 // one group's output channels
   pl.bn = pick_bn(Cg);
   pl.nsub = pl.bn <= 128 ? 2 : 1;
+  pl.tpos = pl.bn == 128;
   // 3-D: items run over (batch, depth slice) pairs of each phase (its jd slices of y, or of dx)
   a.N = int(p.N);
   a.depth_od = deep ? 1 : 0;
@@ -869,12 +950,15 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     if (!fits) continue;
     a.total_items = item;
     a.a_stage_bytes = (a_max + 1023) & ~1023;
-    for (int bufs = 2; bufs >= 1; --bufs) {
-      const size_t fixed = 1024 + bufs * block + size_t(a.bias_n) * 4 +
+    // (the transposed form has its own staging layout, of fixed size)
+    for (int bufs = pl.tpos ? 1 : 2; bufs >= 1; --bufs) {
+      const size_t fixed = 1024 + (pl.tpos ? size_t(kTposStage) : bufs * block) + size_t(a.bias_n) * 4 +
                            size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
                            8 * (2 * 4 + 2 * 8 + 6) + 16;
+      // streamed weights: at least four weight stages before a third activation stage
+      for (int min_sb = pl.bres ? 1 : 4; min_sb >= (pl.bres ? 1 : 3); --min_sb)
       for (int sa = 3; sa >= 2; --sa) {
-        for (int sb = pl.bres ? 1 : 8; sb >= (pl.bres ? 1 : 3); --sb) {
+        for (int sb = pl.bres ? 1 : 8; sb >= min_sb; --sb) {
           const size_t total =
               fixed + size_t(sa) * a.a_stage_bytes + size_t(pl.bres ? a.T * a.kb_count : sb) * a.b_tile_bytes;
           if (total <= size_t(kSmemLimit)) {
@@ -950,9 +1034,9 @@ bool encode_maps(Plan& pl, const void* in, const void* w) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC = false>
+template <int BN, int NSUB, bool DGRAD, bool BRES, bool MSRC = false, bool TPOS = false>
 gbconv_status run(const Plan& pl, const Launch& l) {
-  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES, MSRC>;
+  auto kern = implicit_gemm_kernel<BN, NSUB, DGRAD, BRES, MSRC, TPOS>;
   // The shared-memory opt-in is a per-device function attribute: raise it once per device.
   static std::atomic<uint64_t> done[64];
   int dev = 0;
@@ -973,14 +1057,14 @@ gbconv_status dispatch_src(const Plan& pl, const Launch& l) {
     switch (pl.bn) {
       case 256: return run<256, 1, false, true, MSRC>(pl, l);
       case 192: return run<192, 1, false, true, MSRC>(pl, l);
-      case 128: return run<128, 2, false, true, MSRC>(pl, l);
+      case 128: return run<128, 2, false, true, MSRC, true>(pl, l);
       default: return run<64, 2, false, true, MSRC>(pl, l);
     }
   }
   switch (pl.bn) {
     case 256: return run<256, 1, DGRAD, false, MSRC>(pl, l);
     case 192: return run<192, 1, DGRAD, false, MSRC>(pl, l);
-    case 128: return run<128, 2, DGRAD, false, MSRC>(pl, l);
+    case 128: return run<128, 2, DGRAD, false, MSRC, true>(pl, l);
     default: return run<64, 2, DGRAD, false, MSRC>(pl, l);
   }
 }
@@ -1024,9 +1108,9 @@ bool implicit_describe(const Problem& p, bool dgrad, char* buf, size_t len) {
   int taps = 0;
   for (int i = 0; i < a.nphase; ++i) taps = std::max(taps, a.ph[i].ntaps);
   std::snprintf(buf, len,
-                "implicit_gemm %s bn=%d nsub=%d phases=%d sources=%d taps=%d items=%d kb=%d weights=%s "
+                "implicit_gemm %s m_side=%s bn=%d nsub=%d phases=%d sources=%d taps=%d items=%d kb=%d weights=%s "
                 "a_stages=%d b_stages=%d stage_bufs=%d strips=%d smem=%zu",
-                dgrad ? "dgrad" : "fwd", pl.bn, pl.nsub, a.nphase, a.ph[0].nsrc, taps, a.total_items, a.kb_count,
+                dgrad ? "dgrad" : "fwd", pl.tpos ? "channels" : "positions", pl.bn, pl.nsub, a.nphase, a.ph[0].nsrc, taps, a.total_items, a.kb_count,
                 pl.bres ? "resident" : "streamed", a.sa, pl.bres ? 0 : a.sb, a.stage_bufs, a.ph[0].nstrips, pl.smem);
   return true;
 }

@@ -28,9 +28,12 @@ def gb():
 
 @pytest.mark.parametrize("op", ["fwd", "dgrad"])
 def test_expired_wait_reports_timeout_and_the_next_call_is_correct(gb, op):
-    kw = shape_kw(n=8, in_size=(56, 56), c_in=64, c_out=64, bias=(op == "fwd"))
+    # Long reductions (a 256- or 1024-channel k loop per tap): one work item's MMAs take well over
+    # 10 us, so the epilogue's first wait, for the item's accumulator, outlasts the bound however
+    # quickly the operands arrive (an L2-warm halo can land within a microsecond).
+    kw = shape_kw(n=4, in_size=(56, 56), c_in=256, c_out=64, bias=(op == "fwd"))
     if op == "dgrad":
-        kw = shape_kw(n=8, in_size=(48, 48), c_in=128, c_out=256, stride=(2, 2))
+        kw = shape_kw(n=4, in_size=(48, 48), c_in=128, c_out=1024, stride=(2, 2))
     d = lib_desc(gb, kw)
     assert gb.gbconv_select(d, gb.GBCONV_OP_FWD if op == "fwd" else gb.GBCONV_OP_BWD_DATA) == (
         "implicit" if op == "fwd" else "dgrad")
@@ -50,7 +53,7 @@ def test_expired_wait_reports_timeout_and_the_next_call_is_correct(gb, op):
         return gb.gbconv_bwd_data(d, src.data_ptr(), w.data_ptr(), out.data_ptr(), stream)
 
     assert gb.gbconv_device_status(stream) == gb.GBCONV_OK  # nothing pending from earlier tests
-    prev = gb.gbconv_set_wait_limit_ns(1000)  # 1 us: the first halo alone takes longer to arrive
+    prev = gb.gbconv_set_wait_limit_ns(1000)  # 1 us
     try:
         assert call() == gb.GBCONV_OK  # the launch itself succeeds
         assert gb.gbconv_device_status(stream) == gb.GBCONV_ETIMEOUT
