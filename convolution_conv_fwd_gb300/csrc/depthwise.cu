@@ -496,6 +496,128 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   }
 }
 
+// The same persistent TMA design for the input gradient of the 3x3 / stride 2 / pad 1 / dilation 1
+// layer, whose dx 2x2 block at (2R, 2C) reads exactly the dy 2x2 block at (R, C) (the gather
+// written out above depthwise3x3s2_dgrad_kernel).  A tile is kTR x kTC dy positions, which need
+// (kTR+1) x (kTC+1) dy pixels (zero fill past the last row and column) and produce 2kTR x 2kTC dx
+// pixels.  Every SM takes an equal share of the tiles; the register-streaming kernel above ran one
+// block per (image, column group), which left some SMs two blocks' work and others one.
+template <bool BIAS>
+__global__ void __launch_bounds__(kDwThreads, 1)
+    depthwise3x3s2_dgrad_tma_kernel(const __grid_constant__ CUtensorMap dymap, const __grid_constant__ DwTmaArgs a,
+                                    const __nv_bfloat16* __restrict__ w) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDwStages * a.stage_bytes);
+  uint64_t* empty = full + kDwStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDwStages);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDwStages; ++i) { ptx::mbar_init(full + i, 1); ptx::mbar_init(empty + i, kDwCompute); }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
+  const int chunk = blockIdx.x % a.nchunk;
+  const int ctas_per_chunk = gridDim.x / a.nchunk;
+  const int first = blockIdx.x / a.nchunk;
+  if (warp == kDwCompute / 32) {
+    if ((threadIdx.x & 31) == 0) {
+      ptx::prefetch_tmap(&dymap);
+      int st = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
+        const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
+        if (!ptx::mbar_wait(empty + st, ph ^ 1, abort_flag, a.status, 16u, a.wait_ns)) break;
+        ++issued;
+        ptx::mbar_arrive_expect_tx(full + st, uint32_t(a.stage_bytes));
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+            "%6}], [%2];" ::"r"(ptx::smem_addr(smem + st * a.stage_bytes)),
+            "l"(&dymap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC), "r"(th * kTR), "r"(n)
+            : "memory");
+        if (++st == kDwStages) { st = 0; ph ^= 1; }
+      }
+      for (int k = max(0, issued - kDwStages); k < issued; ++k)
+        ptx::mbar_wait_drain(full + k % kDwStages, uint32_t((k / kDwStages) & 1));
+    }
+    __syncwarp();
+    return;
+  }
+  // ------------------------------------------------------------ compute threads
+  // A warp covers 4 consecutive dy positions x 8 channel vectors: its shared-memory reads are 512
+  // contiguous bytes, and each of its stores writes four whole 128-byte lines.
+  const int cv = threadIdx.x & 7;
+  const int pos = threadIdx.x >> 3;  // dy positions pos and pos + 32 of the tile
+  const int c = chunk * 64 + cv * 8;
+  float wr[9][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int t = 0; t < 9; ++t) wr[t][j] = __bfloat162float(w[(c + j) * 9 + t]);
+  float bs[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) bs[j] = BIAS ? __ldg(a.bias + c + j) : 0.f;
+  uint4* dxv = reinterpret_cast<uint4*>(a.y);
+  const int cvec = a.C / 8;
+  int st = 0;
+  uint32_t ph = 0;
+  for (int t = first; t < a.tiles_per_chunk; t += ctas_per_chunk) {
+    const int tw = t % a.tiles_w, th = (t / a.tiles_w) % a.tiles_h, n = t / (a.tiles_w * a.tiles_h);
+    if (!ptx::mbar_wait(full + st, ph, abort_flag, a.status, 16u, a.wait_ns)) break;
+    const uint32_t base = ptx::smem_addr(smem + st * a.stage_bytes) + cv * 16;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int p = pos + half * 32;
+      const int r = p / kTC, col = p % kTC;
+      const int R = th * kTR + r, C = tw * kTC + col;  // dy position
+      if (R < a.OH && C < a.OW) {
+        uint4 v00, v01, v10, v11;  // dy[R][C], dy[R][C+1], dy[R+1][C], dy[R+1][C+1]
+        const uint32_t q = base + uint32_t((r * a.ic + col) * 128);
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v00.x), "=r"(v00.y), "=r"(v00.z), "=r"(v00.w) : "r"(q));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v01.x), "=r"(v01.y), "=r"(v01.z), "=r"(v01.w) : "r"(q + 128));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v10.x), "=r"(v10.y), "=r"(v10.z), "=r"(v10.w) : "r"(q + uint32_t(a.ic * 128)));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v11.x), "=r"(v11.y), "=r"(v11.z), "=r"(v11.w) : "r"(q + uint32_t(a.ic * 128 + 128)));
+        float a0[8], a1[8], b0[8], b1[8];
+        unpack8(v00, a0);
+        unpack8(v01, a1);
+        unpack8(v10, b0);
+        unpack8(v11, b1);
+        float o00[8], o01[8], o10[8], o11[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o00[j] = a0[j] * wr[4][j] + bs[j];
+          o01[j] = fmaf(a1[j], wr[3][j], a0[j] * wr[5][j]) + bs[j];
+          o10[j] = fmaf(b0[j], wr[1][j], a0[j] * wr[7][j]) + bs[j];
+          o11[j] = fmaf(b1[j], wr[0][j], fmaf(b0[j], wr[2][j], fmaf(a1[j], wr[6][j], a0[j] * wr[8][j]))) + bs[j];
+        }
+        auto pack = [](const float (&f)[8]) {
+          uint4 o;
+          o.x = pack2(f[0], f[1]);
+          o.y = pack2(f[2], f[3]);
+          o.z = pack2(f[4], f[5]);
+          o.w = pack2(f[6], f[7]);
+          return o;
+        };
+        const bool col1 = 2 * C + 1 < a.W;
+        const size_t row0 = size_t(n * a.H + 2 * R) * a.W;
+        dxv[(row0 + 2 * C) * cvec + (c >> 3)] = pack(o00);
+        if (col1) dxv[(row0 + 2 * C + 1) * cvec + (c >> 3)] = pack(o01);
+        if (2 * R + 1 < a.H) {
+          const size_t row1 = row0 + a.W;
+          dxv[(row1 + 2 * C) * cvec + (c >> 3)] = pack(o10);
+          if (col1) dxv[(row1 + 2 * C + 1) * cvec + (c >> 3)] = pack(o11);
+        }
+      }
+    }
+    ptx::mbar_arrive(empty + st);
+    if (++st == kDwStages) { st = 0; ph ^= 1; }
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -554,6 +676,52 @@ gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, cons
     done[dev].store(1, std::memory_order_release);
   }
   // A multiple of the chunk count, at most one CTA per SM and per tile column of work.
+  int grid = std::max(a.nchunk, (l.num_sms / a.nchunk) * a.nchunk);
+  grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
+  return launch_kernel(kern, dim3(grid), dim3(kDwThreads), smem, l.stream, map, a,
+                       static_cast<const __nv_bfloat16*>(w)) == cudaSuccess
+             ? GBCONV_OK
+             : GBCONV_ECUDA;
+}
+
+gbconv_status launch_dw_dgrad_tma(const Problem& p, const void* dy, const void* w, const float* bias, void* dx,
+                                  const Launch& l) {
+  auto fn = dw_encode_fn();
+  if (!fn) return GBCONV_ECUDA;
+  DwTmaArgs a{};
+  a.bias = bias;
+  a.y = static_cast<__nv_bfloat16*>(dx);
+  a.status = l.status;
+  a.wait_ns = l.wait_ns;
+  a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
+  a.nchunk = a.C / 64;
+  a.tiles_h = (a.OH + kTR - 1) / kTR;
+  a.tiles_w = (a.OW + kTC - 1) / kTC;
+  a.tiles_per_chunk = a.N * a.tiles_h * a.tiles_w;
+  a.ir = kTR + 1;
+  a.ic = kTC + 1;
+  a.stage_bytes = a.ir * a.ic * 128;
+  CUtensorMap map;
+  cuuint64_t dims[4] = {cuuint64_t(a.C), cuuint64_t(a.OW), cuuint64_t(a.OH), cuuint64_t(a.N)};
+  cuuint64_t strides[3] = {cuuint64_t(a.C) * 2, cuuint64_t(a.OW) * a.C * 2, cuuint64_t(a.OH) * a.OW * a.C * 2};
+  cuuint32_t box[4] = {64, cuuint32_t(a.ic), cuuint32_t(a.ir), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return GBCONV_ECUDA;
+  const size_t smem = size_t(kDwStages) * a.stage_bytes + 8 * 2 * kDwStages + 16;
+  auto kern = bias ? depthwise3x3s2_dgrad_tma_kernel<true> : depthwise3x3s2_dgrad_tma_kernel<false>;
+  static std::atomic<uint64_t> done[64];  // bit 0: without bias, bit 1: with bias
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
+  const uint64_t bit = bias ? 2u : 1u;
+  if ((done[dev].load(std::memory_order_acquire) & bit) == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+      return GBCONV_ECUDA;
+    done[dev].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  // A multiple of the chunk count, at most one CTA per SM and per tile of work.
   int grid = std::max(a.nchunk, (l.num_sms / a.nchunk) * a.nchunk);
   grid = std::min<int64_t>(grid, int64_t(a.nchunk) * a.tiles_per_chunk);
   return launch_kernel(kern, dim3(grid), dim3(kDwThreads), smem, l.stream, map, a,
@@ -636,6 +804,7 @@ gbconv_status launch_depthwise_dgrad(const Problem& p, const void* dy, const voi
   if (p.KH == 3 && p.KW == 3 && p.SH == 2 && p.SW == 2 && p.PH == 1 && p.PW == 1 && p.PHe == 1 && p.PWe == 1 &&
       p.DH == 1 && p.DW == 1 &&
       p.OH == (p.H + 1) / 2 && p.OW == (p.W + 1) / 2) {
+    if (p.Cin % 64 == 0) return launch_dw_dgrad_tma(p, dy, w, bias, dx, l);
     // One thread per dy column and 8 channels, walking a strip of dy rows: strips as long as
     // possible (each strip start re-reads a dy row) while the grid still fills two blocks per SM.
     // Whole columns measured best for 32x112x112x256 (60.7 us; 8-row strips 68 us, 4-row 83.5 us).
