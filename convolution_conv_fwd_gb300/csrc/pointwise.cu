@@ -311,7 +311,12 @@ gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* 
   CUtensorMap ta, tb;
   if (!make_map(&ta, x, uint64_t(a.M), uint64_t(a.K), kBM)) return GBCONV_ECUDA;
   if (!make_map(&tb, w, uint64_t(p.Cout), uint64_t(a.K), uint32_t(bn))) return GBCONV_ECUDA;
-  const int grid = std::max(1, std::min(a.m_tiles, l.num_sms));
+  // The fewest rounds the SMs allow, over as many CTAs as that many rounds needs: every CTA then
+  // takes the same number of tiles (give or take one in the last round) instead of a last round in
+  // which a few CTAs work while the rest are done (784 tiles: 131 CTAs of 6 tiles, not 152 CTAs of
+  // which 24 take a 6th).
+  const int rounds = (a.m_tiles + l.num_sms - 1) / std::max(1, l.num_sms);
+  const int grid = std::max(1, std::min(a.m_tiles, (a.m_tiles + rounds - 1) / std::max(1, rounds)));
   switch (bn) {
     case 256: return run<256>(ta, tb, a, grid, l);
     case 128: return run<128>(ta, tb, a, grid, l);

@@ -116,6 +116,8 @@ SMALL = [
     (shape_kw(n=2, in_size=(9, 7), c_in=256, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
     (shape_kw(n=2, in_size=(110, 89), c_in=64, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
+    # 252 tiles: two tiles on each of 126 CTAs (the grid is sized for equal rounds), ragged last tile
+    (shape_kw(n=2, in_size=(126, 128), c_in=64, c_out=32, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(13, 13), c_in=72, c_out=128, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
     (shape_kw(n=3, in_size=(10, 10), c_in=64, c_out=256, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(5, 9), c_in=8, c_out=32, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
@@ -174,6 +176,8 @@ SMALL = [
     (shape_kw(n=2, in_size=(6, 7), c_in=8, c_out=8, groups=8, k=(1, 1), pad=(0, 0), stride=(2, 2)),
      "dgrad", "depthwise_dgrad"),
     (shape_kw(n=1, in_size=(8, 9), c_in=512, c_out=512, groups=512, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
+    # the TMA-fed stride-2 gather: several 4x16 dy tiles each way, ragged in both, odd H
+    (shape_kw(n=3, in_size=(37, 70), c_in=128, c_out=128, groups=128, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
     # (begin, end) padding: implicit forward one-sided, strided with padding after only (the usual
     # 'same' padding of an even input at stride 2), a 1x1 with padding after, the depthwise
     # generic kernel, the stride-phase dgrad, the depthwise dgrad, and the generic direct kernels
@@ -386,6 +390,7 @@ TRANSPOSE = [
     (shape_kw(n=2, in_size=(13, 10), c_in=128, c_out=256, stride=(2, 2)), "dgrad"),
     (shape_kw(n=2, in_size=(14, 15), c_in=64, c_out=64, groups=64, stride=(2, 2)), "depthwise_dgrad"),
     (shape_kw(n=1, in_size=(9, 13), c_in=40, c_out=40, groups=40), "depthwise_dgrad"),
+    (shape_kw(n=1, in_size=(37, 70), c_in=128, c_out=128, groups=128, stride=(2, 2)), "depthwise_dgrad"),
     (shape_kw(n=2, in_size=(7, 9), c_in=6, c_out=4, groups=2, layout="nchw", wlayout="oihw", dtype="f32",
               stride=(2, 2)), "direct_dgrad"),
     (shape_kw(n=1, in_size=(10, 6), c_in=16, c_out=16, groups=2, stride=(2, 1)), "direct_dgrad"),
