@@ -373,13 +373,15 @@ __global__ void __launch_bounds__(kThreads, 2) depthwise3x3_kernel(DwArgs a, con
 
 // ---------------------------------------------------------------- TMA-fed 3x3
 // Persistent kernel for the 3x3 / stride 1 or 2 / dilation 1 case with 64-channel
-// chunks.  A producer lane streams halo tiles (kTR x kTC outputs need
-// ((kTR-1)S+3) x ((kTC-1)S+3) input pixels x 64 channels, zero fill supplying the
+// chunks.  A producer lane streams halo tiles (TR x TC outputs need
+// ((TR-1)S+3) x ((TC-1)S+3) input pixels x 64 channels, zero fill supplying the
 // padding) through a ring of shared-memory stages with TMA; 256 compute threads
 // each own 8 channels of two output pixels per tile, keep their 72 weights in
 // registers, and read the taps from shared memory.  DRAM sees each input byte
 // once per tile (halo overlap between tiles comes from L2).
-constexpr int kTR = 4, kTC = 16;            // output tile: rows x columns
+// Output tiles are TR x TC = 64 pixels: 4 x 16, or 8 x 8 where that cuts fewer partial tiles (a
+// 56-wide output is 3.5 tiles of 16 columns but 7 of 8; a partial tile costs a whole tile's time).
+constexpr int kTilePix = 64;
 constexpr int kDwStages = 4;
 constexpr int kDwCompute = 256;             // compute threads (8 warps)
 constexpr int kDwThreads = kDwCompute + 32; // + one producer warp
@@ -394,10 +396,11 @@ struct DwTmaArgs {
   int ir, ic, stage_bytes;
 };
 
-template <int S>
+template <int S, int TR>
 __global__ void __launch_bounds__(kDwThreads, 1)
     depthwise3x3_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ DwTmaArgs a,
                             const __nv_bfloat16* __restrict__ w) {
+  constexpr int kTC = kTilePix / TR;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDwStages * a.stage_bytes);
   uint64_t* empty = full + kDwStages;
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
             "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
             "%6}], [%2];" ::"r"(ptx::smem_addr(smem + st * a.stage_bytes)),
             "l"(&xmap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC * S - a.PW),
-            "r"(th * kTR * S - a.PH), "r"(n)
+            "r"(th * TR * S - a.PH), "r"(n)
             : "memory");
         if (++st == kDwStages) { st = 0; ph ^= 1; }
       }
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[j] = fmaf(xf[j], wr[kh * 3 + kw][j], acc[j]);
         }
-      const int oh = th * kTR + r, ow = tw * kTC + col;
+      const int oh = th * TR + r, ow = tw * kTC + col;
       if (oh < a.OH && ow < a.OW) {
         uint4 o;
         o.x = pack2(acc[0], acc[1]);
@@ -498,14 +501,15 @@ __global__ void __launch_bounds__(kDwThreads, 1)
 
 // The same persistent TMA design for the input gradient of the 3x3 / stride 2 / pad 1 / dilation 1
 // layer, whose dx 2x2 block at (2R, 2C) reads exactly the dy 2x2 block at (R, C) (the gather
-// written out above depthwise3x3s2_dgrad_kernel).  A tile is kTR x kTC dy positions, which need
-// (kTR+1) x (kTC+1) dy pixels (zero fill past the last row and column) and produce 2kTR x 2kTC dx
+// written out above depthwise3x3s2_dgrad_kernel).  A tile is TR x TC dy positions, which need
+// (TR+1) x (TC+1) dy pixels (zero fill past the last row and column) and produce 2TR x 2TC dx
 // pixels.  Every SM takes an equal share of the tiles; the register-streaming kernel above ran one
 // block per (image, column group), which left some SMs two blocks' work and others one.
-template <bool BIAS>
+template <bool BIAS, int TR>
 __global__ void __launch_bounds__(kDwThreads, 1)
     depthwise3x3s2_dgrad_tma_kernel(const __grid_constant__ CUtensorMap dymap, const __grid_constant__ DwTmaArgs a,
                                     const __nv_bfloat16* __restrict__ w) {
+  constexpr int kTC = kTilePix / TR;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDwStages * a.stage_bytes);
   uint64_t* empty = full + kDwStages;
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
             "%6}], [%2];" ::"r"(ptx::smem_addr(smem + st * a.stage_bytes)),
-            "l"(&dymap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC), "r"(th * kTR), "r"(n)
+            "l"(&dymap), "r"(ptx::smem_addr(full + st)), "r"(chunk * 64), "r"(tw * kTC), "r"(th * TR), "r"(n)
             : "memory");
         if (++st == kDwStages) { st = 0; ph ^= 1; }
       }
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     for (int half = 0; half < 2; ++half) {
       const int p = pos + half * 32;
       const int r = p / kTC, col = p % kTC;
-      const int R = th * kTR + r, C = tw * kTC + col;  // dy position
+      const int R = th * TR + r, C = tw * kTC + col;  // dy position
       if (R < a.OH && C < a.OW) {
         uint4 v00, v01, v10, v11;  // dy[R][C], dy[R][C+1], dy[R+1][C], dy[R+1][C+1]
         const uint32_t q = base + uint32_t((r * a.ic + col) * 128);
@@ -618,6 +622,12 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   }
 }
 
+// Output tile rows of the TMA-fed kernels: 8 (8 x 8 tiles) when that gives fewer tiles than 4 x 16.
+int tile_rows(int oh, int ow) {
+  const int64_t t4 = int64_t((oh + 3) / 4) * ((ow + 15) / 16), t8 = int64_t((oh + 7) / 8) * ((ow + 7) / 8);
+  return t8 < t4 ? 8 : 4;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -650,11 +660,12 @@ gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, cons
   a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
   a.PH = int(p.PH); a.PW = int(p.PW);
   a.nchunk = a.C / 64;
-  a.tiles_h = (a.OH + kTR - 1) / kTR;
-  a.tiles_w = (a.OW + kTC - 1) / kTC;
+  const int TR = tile_rows(a.OH, a.OW), TC = kTilePix / TR;
+  a.tiles_h = (a.OH + TR - 1) / TR;
+  a.tiles_w = (a.OW + TC - 1) / TC;
   a.tiles_per_chunk = a.N * a.tiles_h * a.tiles_w;
-  a.ir = (kTR - 1) * S + 3;
-  a.ic = (kTC - 1) * S + 3;
+  a.ir = (TR - 1) * S + 3;
+  a.ic = (TC - 1) * S + 3;
   a.stage_bytes = a.ir * a.ic * 128;
   CUtensorMap map;
   cuuint64_t dims[4] = {cuuint64_t(a.C), cuuint64_t(a.W), cuuint64_t(a.H), cuuint64_t(a.N)};
@@ -666,14 +677,15 @@ gbconv_status launch_dw_tma(const Problem& p, const void* x, const void* w, cons
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return GBCONV_ECUDA;
   const size_t smem = size_t(kDwStages) * a.stage_bytes + 8 * 2 * kDwStages + 16;
-  auto kern = depthwise3x3_tma_kernel<S>;
-  static std::atomic<uint64_t> done[64];
+  auto kern = TR == 8 ? depthwise3x3_tma_kernel<S, 8> : depthwise3x3_tma_kernel<S, 4>;
+  static std::atomic<uint64_t> done[64];  // bit per tile shape
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
-  if (done[dev].load(std::memory_order_acquire) == 0) {
+  const uint64_t bit = TR == 8 ? 2u : 1u;
+  if ((done[dev].load(std::memory_order_acquire) & bit) == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return GBCONV_ECUDA;
-    done[dev].store(1, std::memory_order_release);
+    done[dev].fetch_or(bit, std::memory_order_acq_rel);
   }
   // A multiple of the chunk count, at most one CTA per SM and per tile column of work.
   int grid = std::max(a.nchunk, (l.num_sms / a.nchunk) * a.nchunk);
@@ -695,11 +707,12 @@ gbconv_status launch_dw_dgrad_tma(const Problem& p, const void* dy, const void* 
   a.wait_ns = l.wait_ns;
   a.N = int(p.N); a.C = int(p.Cin); a.H = int(p.H); a.W = int(p.W); a.OH = int(p.OH); a.OW = int(p.OW);
   a.nchunk = a.C / 64;
-  a.tiles_h = (a.OH + kTR - 1) / kTR;
-  a.tiles_w = (a.OW + kTC - 1) / kTC;
+  const int TR = tile_rows(a.OH, a.OW), TC = kTilePix / TR;
+  a.tiles_h = (a.OH + TR - 1) / TR;
+  a.tiles_w = (a.OW + TC - 1) / TC;
   a.tiles_per_chunk = a.N * a.tiles_h * a.tiles_w;
-  a.ir = kTR + 1;
-  a.ic = kTC + 1;
+  a.ir = TR + 1;
+  a.ic = TC + 1;
   a.stage_bytes = a.ir * a.ic * 128;
   CUtensorMap map;
   cuuint64_t dims[4] = {cuuint64_t(a.C), cuuint64_t(a.OW), cuuint64_t(a.OH), cuuint64_t(a.N)};
@@ -711,11 +724,12 @@ gbconv_status launch_dw_dgrad_tma(const Problem& p, const void* dy, const void* 
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return GBCONV_ECUDA;
   const size_t smem = size_t(kDwStages) * a.stage_bytes + 8 * 2 * kDwStages + 16;
-  auto kern = bias ? depthwise3x3s2_dgrad_tma_kernel<true> : depthwise3x3s2_dgrad_tma_kernel<false>;
-  static std::atomic<uint64_t> done[64];  // bit 0: without bias, bit 1: with bias
+  auto kern = TR == 8 ? (bias ? depthwise3x3s2_dgrad_tma_kernel<true, 8> : depthwise3x3s2_dgrad_tma_kernel<false, 8>)
+                      : (bias ? depthwise3x3s2_dgrad_tma_kernel<true, 4> : depthwise3x3s2_dgrad_tma_kernel<false, 4>);
+  static std::atomic<uint64_t> done[64];  // bit per (bias, tile shape)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
-  const uint64_t bit = bias ? 2u : 1u;
+  const uint64_t bit = uint64_t(1) << ((bias ? 2 : 0) + (TR == 8 ? 1 : 0));
   if ((done[dev].load(std::memory_order_acquire) & bit) == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
       return GBCONV_ECUDA;

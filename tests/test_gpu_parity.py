@@ -117,6 +117,10 @@ SMALL = [
     # more 128-row tiles than SMs (a second round on a few CTAs) and a ragged last tile
     (shape_kw(n=2, in_size=(110, 89), c_in=64, c_out=64, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
     # 252 tiles: two tiles on each of 126 CTAs (the grid is sized for equal rounds), ragged last tile
+    # 128-channel tiles with channels on M: a grouped forward (128 channels per group, bias) and five
+    # output tiles of one plan
+    (shape_kw(n=2, in_size=(9, 11), c_in=256, c_out=256, groups=2, bias=True), "fwd", "implicit"),
+    (shape_kw(n=1, in_size=(7, 6), c_in=64, c_out=640, bias=True), "fwd", "implicit"),
     (shape_kw(n=2, in_size=(126, 128), c_in=64, c_out=32, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
     (shape_kw(n=1, in_size=(13, 13), c_in=72, c_out=128, k=(1, 1), pad=(0, 0), bias=True), "fwd", "pointwise"),
     (shape_kw(n=3, in_size=(10, 10), c_in=64, c_out=256, k=(1, 1), pad=(0, 0)), "fwd", "pointwise"),
@@ -176,6 +180,8 @@ SMALL = [
     (shape_kw(n=2, in_size=(6, 7), c_in=8, c_out=8, groups=8, k=(1, 1), pad=(0, 0), stride=(2, 2)),
      "dgrad", "depthwise_dgrad"),
     (shape_kw(n=1, in_size=(8, 9), c_in=512, c_out=512, groups=512, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
+    # the TMA-fed depthwise forward at unit stride with 4 x 16 output tiles (4 rows: one tile row)
+    (shape_kw(n=2, in_size=(4, 30), c_in=64, c_out=64, groups=64), "fwd", "depthwise"),
     # the TMA-fed stride-2 gather: several 4x16 dy tiles each way, ragged in both, odd H
     (shape_kw(n=3, in_size=(37, 70), c_in=128, c_out=128, groups=128, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
     # (begin, end) padding: implicit forward one-sided, strided with padding after only (the usual
