@@ -74,10 +74,12 @@ typedef enum {
   GBCONV_K_DIRECT = 0,        /* generic direct kernel on CUDA cores (any layout, dtype, groups, stride, dilation) */
   GBCONV_K_DEPTHWISE = 1,     /* NHWC bf16 depthwise direct kernel, bandwidth bound */
   GBCONV_K_POINTWISE = 2,     /* NHWC bf16 1x1: TMA-fed tcgen05 GEMM */
-  GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense: implicit GEMM on tcgen05, halo tile in shared memory */
+  GBCONV_K_IMPLICIT = 3,      /* NHWC bf16 dense and grouped (C_in/G > 8): implicit GEMM on tcgen05, halo tile in
+                                 shared memory (wide images in column strips) */
   GBCONV_K_DGRAD = 4,         /* NHWC bf16 dgrad: stride-phase gather implicit GEMM on tcgen05 (3-D: depth phases at a depth stride) */
   GBCONV_K_DIRECT_DGRAD = 5,  /* generic gather dgrad on CUDA cores */
-  GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: vectorised gather on CUDA cores, bandwidth bound */
+  GBCONV_K_DEPTHWISE_DGRAD = 6, /* NHWC bf16 depthwise dgrad: gather on CUDA cores, bandwidth bound (3x3 stride 2:
+                                    TMA-fed dy tiles, each dy 2x2 block giving a dx 2x2 block) */
   GBCONV_K_DIRECT_WGRAD = 7,   /* generic wgrad on CUDA cores: per-chunk partial sums, then an ordered reduction */
   GBCONV_K_WGRAD = 8,          /* NHWC bf16 wgrad on tcgen05: taps packed into M and N, then an ordered reduction
                                   (H/W strides: one stride phase per work unit; 3-D: one kernel-depth tap per unit) */
