@@ -95,6 +95,67 @@ __global__ void direct_fwd_kernel(DirectArgs a, const T* __restrict__ x, const T
   }
 }
 
+// Small problems: when the whole input and weight fit in shared memory and every output fits one
+// block, the block first stages both as fp32, all its threads loading at once, and then each output's
+// taps read shared memory.  A launch-latency-bound shape (the fp32 conv1d workload: 12 kFLOP) then
+// pays one round trip to memory instead of one dependent global load per tap.
+constexpr int kSmallFloats = 8192;   // staged x + w, 32 KB
+constexpr int kSmallThreads = 1024;  // one block; each thread takes up to kSmallOutPerThread outputs
+constexpr int kSmallOutPerThread = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kSmallThreads) direct_fwd_small_kernel(DirectArgs a, const T* __restrict__ x,
+                                                                         const T* __restrict__ w,
+                                                                         const float* __restrict__ bias,
+                                                                         T* __restrict__ y, int nx, int nw) {
+  extern __shared__ float stage[];
+  float* xs = stage;
+  float* ws = stage + nx;
+  ptx::grid_dep_wait();  // inputs may come from the previous kernel on the stream
+  ptx::grid_dep_launch();
+  for (int i = threadIdx.x; i < nx; i += blockDim.x) xs[i] = ld(x, i);
+  for (int i = threadIdx.x; i < nw; i += blockDim.x) ws[i] = ld(w, i);
+  __syncthreads();
+  const int total = a.N * a.Cout * a.OD * a.OH * a.OW;
+  const int cpg = a.Cin / a.G, opg = a.Cout / a.G;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    int n, co, od, oh, ow;
+    if (a.nhwc) {
+      co = i % a.Cout;
+      int r = i / a.Cout;
+      ow = r % a.OW; r /= a.OW;
+      oh = r % a.OH; r /= a.OH;
+      od = r % a.OD; n = r / a.OD;
+    } else {
+      ow = i % a.OW;
+      int r = i / a.OW;
+      oh = r % a.OH; r /= a.OH;
+      od = r % a.OD; r /= a.OD;
+      co = r % a.Cout; n = r / a.Cout;
+    }
+    const int g = co / opg;
+    float acc = 0.f;  // the same terms in the same order as direct_fwd_kernel
+    for (int cl = 0; cl < cpg; ++cl) {
+      const int ci = g * cpg + cl;
+      for (int kd = 0; kd < a.KD; ++kd) {
+        const int id = od * a.SD + kd * a.DD - a.PD;
+        if (id < 0 || id >= a.D) continue;
+        for (int kh = 0; kh < a.KH; ++kh) {
+          const int ih = oh * a.SH + kh * a.DH - a.PH;
+          if (ih < 0 || ih >= a.H) continue;
+          for (int kw = 0; kw < a.KW; ++kw) {
+            const int iw = ow * a.SW + kw * a.DW - a.PW;
+            if (iw < 0 || iw >= a.W) continue;
+            acc = fmaf(xs[act_off(a, a.Cin, a.D, a.H, a.W, n, ci, id, ih, iw)], ws[w_off(a, co, cl, kd, kh, kw)], acc);
+          }
+        }
+      }
+    }
+    if (bias) acc += __ldg(bias + co);
+    y[act_off(a, a.Cout, a.OD, a.OH, a.OW, n, co, od, oh, ow)] = cvt<T>(acc);
+  }
+}
+
 template <typename T>
 __global__ void direct_dgrad_kernel(DirectArgs a, const T* __restrict__ dy, const T* __restrict__ w,
                                     const float* __restrict__ bias, T* __restrict__ dx) {
@@ -184,6 +245,19 @@ int grid_for(int64_t total, int threads, int num_sms) {
 gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                 const Launch& l) {
   const DirectArgs a = make_args(p);
+  if (p.x_elems() + p.w_elems() <= kSmallFloats && p.y_elems() <= int64_t(kSmallThreads) * kSmallOutPerThread) {
+    const int nx = int(p.x_elems()), nw = int(p.w_elems());
+    const int threads = int(std::min<int64_t>(kSmallThreads, (p.y_elems() + 31) / 32 * 32));
+    const size_t smem = size_t(nx + nw) * sizeof(float);
+    const cudaError_t e =
+        p.bf16 ? launch_kernel(direct_fwd_small_kernel<__nv_bfloat16>, dim3(1), dim3(threads), smem, l.stream, a,
+                               static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), bias,
+                               static_cast<__nv_bfloat16*>(y), nx, nw)
+               : launch_kernel(direct_fwd_small_kernel<float>, dim3(1), dim3(threads), smem, l.stream, a,
+                               static_cast<const float*>(x), static_cast<const float*>(w), bias,
+                               static_cast<float*>(y), nx, nw);
+    return e == cudaSuccess ? GBCONV_OK : GBCONV_ECUDA;
+  }
   const int threads = 256, blocks = grid_for(p.y_elems(), threads, l.num_sms);
   const cudaError_t e =
       p.bf16 ? launch_kernel(direct_fwd_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, l.stream, a,

@@ -180,6 +180,13 @@ SMALL = [
     (shape_kw(n=2, in_size=(6, 7), c_in=8, c_out=8, groups=8, k=(1, 1), pad=(0, 0), stride=(2, 2)),
      "dgrad", "depthwise_dgrad"),
     (shape_kw(n=1, in_size=(8, 9), c_in=512, c_out=512, groups=512, stride=(2, 2)), "dgrad", "depthwise_dgrad"),
+    # the generic direct forward beyond the shared-memory-staged small path (x + w above 8192
+    # elements): fp32 NCHW grouped, strided, dilated; bf16 NCHW; fp32 3-D
+    (shape_kw(n=2, in_size=(40, 37), c_in=6, c_out=9, groups=3, k=(3, 2), stride=(2, 1), pad=(1, 1), dil=(1, 2),
+              layout="nchw", wlayout="oihw", dtype="f32", bias=True), "fwd", "direct"),
+    (shape_kw(n=2, in_size=(30, 29), c_in=16, c_out=8, layout="nchw", wlayout="oihw"), "fwd", "direct"),
+    (shape_kw(spatial_dims=3, n=1, in_size=(6, 20, 21), c_in=8, c_out=4, k=(3, 3, 3), stride=(1, 1, 1), pad=(1, 1, 1),
+              dil=(1, 1, 1), layout="ncdhw", wlayout="oidhw", dtype="f32"), "fwd", "direct"),
     # the TMA-fed depthwise forward at unit stride with 4 x 16 output tiles (4 rows: one tile row)
     (shape_kw(n=2, in_size=(4, 30), c_in=64, c_out=64, groups=64), "fwd", "depthwise"),
     # the TMA-fed stride-2 gather: several 4x16 dy tiles each way, ragged in both, odd H
