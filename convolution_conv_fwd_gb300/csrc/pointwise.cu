@@ -255,17 +255,27 @@ int pick_bn(int64_t cout) {
   return 0;
 }
 
+size_t smem_for(int bn, int kb_count, int stages) {
+  return size_t(kb_count) * bn * kBK * 2 + size_t(stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8) +
+         128 * size_t(bn * 2 + 16);
+}
+
 int stages_for(int bn, int kb_count) {
-  const size_t fixed = size_t(kb_count) * bn * kBK * 2 + 1024 + 8 * (2 * kMaxStages + 8) + 128 * size_t(bn * 2 + 16);
+  const size_t fixed = smem_for(bn, kb_count, 0);
   if (fixed >= size_t(kSmemLimit)) return 0;
   const int s = int((size_t(kSmemLimit) - fixed) / kATileBytes);
   return std::min(s, kMaxStages);
 }
 
+// Two CTAs per SM, each with a 3-stage ring, when both fit one SM's shared memory: two CTAs streaming
+// side by side move more bytes per SM than one with a deeper ring (the 1x1 workload: 12.86 us against
+// 13.70 with 8 stages on one CTA per SM).
+constexpr int kPairStages = 3;
+bool two_per_sm(int bn, int kb_count) { return 2 * smem_for(bn, kb_count, kPairStages) <= size_t(kSmemLimit); }
+
 template <int BN>
 gbconv_status run(const CUtensorMap& ta, const CUtensorMap& tb, const PwArgs& a, int grid, const Launch& l) {
-  const size_t smem = size_t(a.kb_count) * BN * kBK * 2 + size_t(a.stages) * kATileBytes + 1024 + 8 * (2 * kMaxStages + 8) +
-                      128 * size_t(BN * 2 + 16);
+  const size_t smem = smem_for(BN, a.kb_count, a.stages);
   auto kern = pointwise_gemm_kernel<BN>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device and size.
   static std::atomic<uint64_t> done[64];
@@ -307,15 +317,17 @@ gbconv_status launch_pointwise_fwd(const Problem& p, const void* x, const void* 
   a.kb_count = int((p.Cin + kBK - 1) / kBK);
   a.m_tiles = (a.M + kBM - 1) / kBM;
   const int bn = pick_bn(p.Cout);
-  a.stages = stages_for(bn, a.kb_count);
+  const int per_sm = two_per_sm(bn, a.kb_count) ? 2 : 1;
+  a.stages = per_sm == 2 ? kPairStages : stages_for(bn, a.kb_count);
   CUtensorMap ta, tb;
   if (!make_map(&ta, x, uint64_t(a.M), uint64_t(a.K), kBM)) return GBCONV_ECUDA;
   if (!make_map(&tb, w, uint64_t(p.Cout), uint64_t(a.K), uint32_t(bn))) return GBCONV_ECUDA;
-  // The fewest rounds the SMs allow, over as many CTAs as that many rounds needs: every CTA then
+  // The fewest rounds the CTA slots allow, over as many CTAs as that many rounds needs: every CTA then
   // takes the same number of tiles (give or take one in the last round) instead of a last round in
-  // which a few CTAs work while the rest are done (784 tiles: 131 CTAs of 6 tiles, not 152 CTAs of
-  // which 24 take a 6th).
-  const int rounds = (a.m_tiles + l.num_sms - 1) / std::max(1, l.num_sms);
+  // which a few CTAs work while the rest are done (784 tiles on 2 x 152 slots: 262 CTAs of 3 tiles;
+  // with one CTA per SM it was 131 CTAs of 6, not 152 of which 24 take a 6th).
+  const int slots = std::max(1, per_sm * l.num_sms);
+  const int rounds = (a.m_tiles + slots - 1) / slots;
   const int grid = std::max(1, std::min(a.m_tiles, (a.m_tiles + rounds - 1) / std::max(1, rounds)));
   switch (bn) {
     case 256: return run<256>(ta, tb, a, grid, l);
