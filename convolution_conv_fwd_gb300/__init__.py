@@ -32,7 +32,8 @@ GBCONV_OP_FWD, GBCONV_OP_BWD_DATA, GBCONV_OP_BWD_FILTER = 0, 1, 2
 EXPORTS = ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_fwd", "gbconv_bwd_data", "gbconv_conv_transpose",
            "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_bwd_filter_noalloc",
            "gbconv_pack_weight", "gbconv_device_status", "gbconv_set_wait_limit_ns", "gbconv_kernels_launched",
-           "gbconv_status_string")
+           "gbconv_status_string", "gbconv_host_staging_bytes", "gbconv_fwd_host", "gbconv_bwd_data_host",
+           "gbconv_conv_transpose_host")
 
 
 class Desc(ctypes.Structure):
@@ -68,10 +69,14 @@ def _load():
     lib.gbconv_bwd_filter_noalloc.argtypes = [P(Desc), vp, vp, vp, vp, vp]
     lib.gbconv_pack_weight.argtypes = [P(Desc), vp, vp, vp]
     lib.gbconv_device_status.argtypes = [vp]
+    lib.gbconv_host_staging_bytes.argtypes = [P(Desc), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_int64)]
+    lib.gbconv_fwd_host.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
+    lib.gbconv_bwd_data_host.argtypes = [P(Desc), vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
+    lib.gbconv_conv_transpose_host.argtypes = [P(Desc), vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
     for f in ("gbconv_out_shape", "gbconv_select", "gbconv_describe", "gbconv_conv_transpose", "gbconv_fwd",
               "gbconv_bwd_data", "gbconv_bwd_filter_workspace", "gbconv_bwd_filter", "gbconv_bwd_filter_noalloc",
-              "gbconv_pack_weight",
-              "gbconv_device_status"):
+              "gbconv_pack_weight", "gbconv_device_status", "gbconv_host_staging_bytes", "gbconv_fwd_host",
+              "gbconv_bwd_data_host", "gbconv_conv_transpose_host"):
         getattr(lib, f).restype = st
     lib.gbconv_set_wait_limit_ns.argtypes = [ctypes.c_int64]
     lib.gbconv_set_wait_limit_ns.restype = ctypes.c_int64
@@ -154,6 +159,34 @@ def gbconv_pack_weight(desc: Desc, w_oihw: int, w_ohwi: int, stream: int) -> int
     return _lib.gbconv_pack_weight(ctypes.byref(desc), w_oihw, w_ohwi, stream or None)
 
 
+def gbconv_host_staging_bytes(desc: Desc, op: int, with_bias: bool = False) -> int:
+    b = ctypes.c_int64(0)
+    s = _lib.gbconv_host_staging_bytes(ctypes.byref(desc), op, int(bool(with_bias)), ctypes.byref(b))
+    if s != GBCONV_OK:
+        raise GbconvError(s, "gbconv_host_staging_bytes")
+    return int(b.value)
+
+
+def gbconv_fwd_host(desc: Desc, x: int, w: int, bias: int | None, y: int, staging: int, staging_bytes: int,
+                    slices: int, stream: int, done_event: int | None = None) -> int:
+    """gbconv_fwd on host buffers (x, w, bias, y host addresses), pipelined in batch slices through the
+    device staging buffer: synchronous, or recording ``done_event`` (a raw cudaEvent_t) at the end."""
+    return _lib.gbconv_fwd_host(ctypes.byref(desc), x, w, bias or None, y, staging, staging_bytes, slices,
+                                stream or None, done_event or None)
+
+
+def gbconv_bwd_data_host(desc: Desc, dy: int, w: int, dx: int, staging: int, staging_bytes: int, slices: int,
+                         stream: int, done_event: int | None = None) -> int:
+    return _lib.gbconv_bwd_data_host(ctypes.byref(desc), dy, w, dx, staging, staging_bytes, slices, stream or None,
+                                     done_event or None)
+
+
+def gbconv_conv_transpose_host(desc: Desc, x: int, w: int, bias: int | None, y: int, staging: int,
+                               staging_bytes: int, slices: int, stream: int, done_event: int | None = None) -> int:
+    return _lib.gbconv_conv_transpose_host(ctypes.byref(desc), x, w, bias or None, y, staging, staging_bytes, slices,
+                                           stream or None, done_event or None)
+
+
 def gbconv_device_status(stream: int) -> int:
     return _lib.gbconv_device_status(stream or None)
 
@@ -205,8 +238,21 @@ def make_desc(n, c_in, c_out, in_size, k, stride=1, pad=0, dil=1, groups=1, *, s
     return d
 
 
+_shape_cache = {}
+
+
 def desc_shapes(d: Desc):
-    """(x_shape, w_shape, y_shape) in the layouts the descriptor names."""
+    """(x_shape, w_shape, y_shape) in the layouts the descriptor names (kept per descriptor value)."""
+    key = bytes(d)
+    hit = _shape_cache.get(key)
+    if hit is None:
+        if len(_shape_cache) > 4096:
+            _shape_cache.clear()
+        hit = _shape_cache[key] = _desc_shapes(d)
+    return hit
+
+
+def _desc_shapes(d: Desc):
     out = gbconv_out_shape(d)
     oh, ow = out[0], out[1]
     cpg = d.c_in // d.groups
@@ -271,83 +317,112 @@ def _check_host(t, shape, dtype, name):
     return t
 
 
-# Large host calls are moved through the device in batch slices on three streams: the copy in of
-# slice i+1, the kernels of slice i and the copy out of slice i-1 run at the same time (the two copy
-# directions on their own engines).  Images are independent in every operation sliced here, so a
-# slice is the same call with a smaller batch.  Each slice costs tens of microseconds of host work
-# (descriptor, plan, tensor maps, stream events), so only calls that move at least _PIPE_MIN_BYTES
-# are sliced, into _PIPE_SLICES slices; smaller ones run as one copy in, one call, one copy out.
-_PIPE_SLICES = 8  # measured: 8 slices 2.08 ms per bench e2e pass, 4 slices 2.12 ms
-_PIPE_MIN_BYTES = 64 << 20
-_copy_streams = {}
+# Calls on host tensors go to the library's host entry points (gbconv_fwd_host, gbconv_bwd_data_host),
+# which pipeline the batch through a device staging buffer in slices: the copy in of slice i+1, the
+# kernel of slice i and the copy out of slice i-1 run at the same time.  The staging buffer comes from
+# torch's caching allocator; the library allocates nothing.  HOST_SLICES = 0 lets the library choose
+# (about 4 MiB of copies per slice).
+HOST_SLICES = 0
+_staging_cache = {}
 
 
-def _streams(dev):
-    torch = _torch()
-    if dev.index not in _copy_streams:
-        _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
-    return _copy_streams[dev.index]
+class HostCall:
+    """A host-buffer call in flight (``conv_fwd_async`` and the like).  ``wait()`` blocks until the
+    result is in host memory and returns it; until then the call holds its host tensors and device
+    staging buffer, which must not be modified."""
+
+    def __init__(self, result, keep, event):
+        self._result, self._keep, self._event = result, keep, event
+
+    def done(self) -> bool:
+        return self._event is None or self._event.query()
+
+    def wait(self):
+        if self._event is not None:
+            self._event.synchronize()
+            self._event = self._keep = None
+        return self._result
+
+    def __del__(self):
+        # the copies still read and write the tensors this object holds
+        if getattr(self, "_event", None) is not None:
+            self._event.synchronize()
 
 
-def _with_batch(d: Desc, n: int) -> Desc:
-    sub = Desc.from_buffer_copy(d)
-    sub.n = n
-    return sub
-
-
-def _host_call(d: Desc, entry, what, src, w, bias, src_shape, out_shape, out=None):
-    """One call on host tensors.  ``entry(desc, src, w, bias, out, stream)`` is the C entry point;
-    src is sliced along the batch (its first axis), w and bias are copied whole.  Pinned host memory
-    lets the copies run asynchronously and overlap; pageable memory still works, without overlap."""
+def _host_call(d: Desc, op: int, src, w, bias, out_shape, out=None, wait=True):
+    """One call on host tensors.  Synchronous (wait=True): returns the result as a pinned host tensor
+    (or ``out``).  Else returns a HostCall whose completion event the library records.  op
+    GBCONV_OP_BWD_DATA with a bias is the transposed convolution."""
     torch = _torch()
     dt = _dtype(d)
     dev = torch.device("cuda", torch.cuda.current_device())
-    main = torch.cuda.current_stream(dev)
     res = out if out is not None else torch.empty(out_shape, dtype=dt, pin_memory=True)
     _check_host(res, out_shape, dt, "result")
-    nbytes = src.numel() * src.element_size() + res.numel() * res.element_size()
-    slices = min(int(d.n), _PIPE_SLICES) if nbytes >= _PIPE_MIN_BYTES else 1
-    if slices <= 1:
-        src_d = src.to(dev, non_blocking=True)
-        w_d = w.to(dev, non_blocking=True)
-        b_d = None if bias is None else bias.to(dev, non_blocking=True)
-        out_d = torch.empty(out_shape, dtype=dt, device=dev)
-        st = entry(d, src_d.data_ptr(), w_d.data_ptr(), None if b_d is None else b_d.data_ptr(), out_d.data_ptr(),
-                   main.cuda_stream)
-        if st != GBCONV_OK:
-            main.synchronize()
-            raise GbconvError(st, what)
-        res.copy_(out_d, non_blocking=True)
-        main.synchronize()
+    key = (bytes(d), op, bias is not None)
+    nbytes = _staging_cache.get(key)
+    if nbytes is None:
+        if len(_staging_cache) > 4096:
+            _staging_cache.clear()
+        nbytes = _staging_cache[key] = gbconv_host_staging_bytes(d, op, bias is not None)
+    staging = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream(dev)
+    event = None
+    if not wait:
+        event = torch.cuda.Event()
+        event.record(cur)  # creates the event; the library records it again at the call's end
+    done = None if event is None else event.cuda_event
+    stream = cur.cuda_stream
+    if op == GBCONV_OP_FWD:
+        st = gbconv_fwd_host(d, src.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                             res.data_ptr(), staging.data_ptr(), nbytes, HOST_SLICES, stream, done)
+        what = "gbconv_fwd_host"
+    elif bias is not None:
+        st = gbconv_conv_transpose_host(d, src.data_ptr(), w.data_ptr(), bias.data_ptr(), res.data_ptr(),
+                                        staging.data_ptr(), nbytes, HOST_SLICES, stream, done)
+        what = "gbconv_conv_transpose_host"
+    else:
+        st = gbconv_bwd_data_host(d, src.data_ptr(), w.data_ptr(), res.data_ptr(), staging.data_ptr(), nbytes,
+                                  HOST_SLICES, stream, done)
+        what = "gbconv_bwd_data_host"
+    if st != GBCONV_OK:
+        if event is not None:
+            event.synchronize()  # recorded after whatever was enqueued
+        raise GbconvError(st, what)
+    if wait:
         return res
-    bounds = [int(d.n) * i // slices for i in range(slices + 1)]
-    s_in, s_out = _streams(dev)
-    src_d = torch.empty(src_shape, dtype=dt, device=dev)
-    out_d = torch.empty(out_shape, dtype=dt, device=dev)
-    # the device buffers come from the current stream's pool: the side streams start after it
-    s_in.wait_stream(main)
-    s_out.wait_stream(main)
-    with torch.cuda.stream(s_in):
-        w_d = w.to(dev, non_blocking=True)
-        b_d = None if bias is None else bias.to(dev, non_blocking=True)
-    for i in range(slices):
-        lo, hi = bounds[i], bounds[i + 1]
-        if hi == lo:
-            continue
-        with torch.cuda.stream(s_in):
-            src_d[lo:hi].copy_(src[lo:hi], non_blocking=True)
-        main.wait_stream(s_in)
-        st = entry(_with_batch(d, hi - lo), src_d[lo:hi].data_ptr(), w_d.data_ptr(),
-                   None if b_d is None else b_d.data_ptr(), out_d[lo:hi].data_ptr(), main.cuda_stream)
-        if st != GBCONV_OK:
-            main.synchronize()
-            raise GbconvError(st, what)
-        s_out.wait_stream(main)
-        with torch.cuda.stream(s_out):
-            res[lo:hi].copy_(out_d[lo:hi], non_blocking=True)
-    main.wait_stream(s_out)
-    main.synchronize()
-    return res
+    return HostCall(res, (src, w, bias, staging), event)
+
+
+def _host_args(d: Desc, op: int, src, w, bias):
+    """Checks host tensors against the descriptor; returns the result's shape."""
+    torch = _torch()
+    xs, ws, ys = desc_shapes(d)
+    dt = _dtype(d)
+    _check_host(src, xs if op == GBCONV_OP_FWD else ys, dt, "x" if op == GBCONV_OP_FWD else "dy")
+    _check_host(w, ws, dt, "w")
+    if bias is not None:
+        _check_host(bias, (d.c_out if op == GBCONV_OP_FWD else d.c_in,), torch.float32, "bias")
+    return ys if op == GBCONV_OP_FWD else xs
+
+
+def conv_fwd_async(d: Desc, x, w, bias=None, y=None) -> HostCall:
+    """``conv_fwd`` on host tensors without waiting: the copies and kernels are enqueued and a HostCall
+    is returned at once.  Independent calls made this way keep the host link busy back to back (one
+    call's last copy out overlaps the next call's copies in); ``wait()`` returns the result."""
+    ys = _host_args(d, GBCONV_OP_FWD, x, w, bias)
+    return _host_call(d, GBCONV_OP_FWD, x, w, bias, ys, y, wait=False)
+
+
+def conv_bwd_data_async(d: Desc, dy, w, dx=None) -> HostCall:
+    """``conv_bwd_data`` on host tensors without waiting (see ``conv_fwd_async``)."""
+    xs = _host_args(d, GBCONV_OP_BWD_DATA, dy, w, None)
+    return _host_call(d, GBCONV_OP_BWD_DATA, dy, w, None, xs, dx, wait=False)
+
+
+def conv_transpose_async(d: Desc, x, w, bias=None, y=None) -> HostCall:
+    """``conv_transpose`` on host tensors without waiting (see ``conv_fwd_async``)."""
+    xs = _host_args(d, GBCONV_OP_BWD_DATA, x, w, bias)
+    return _host_call(d, GBCONV_OP_BWD_DATA, x, w, bias, xs, y, wait=False)
 
 
 def conv_fwd(d: Desc, x, w, bias=None, y=None):
@@ -367,7 +442,7 @@ def conv_fwd(d: Desc, x, w, bias=None, y=None):
         _check_host(w, ws, dt, "w")
         if bias is not None:
             _check_host(bias, (d.c_out,), torch.float32, "bias")
-        return _host_call(d, gbconv_fwd, "gbconv_fwd", x, w, bias, xs, ys, y)
+        return _host_call(d, GBCONV_OP_FWD, x, w, bias, ys, y)
     _check(x, xs, dt, "x")
     _check(w, ws, dt, "w")
     if bias is not None:
@@ -396,8 +471,7 @@ def conv_bwd_data(d: Desc, dy, w, dx=None):
     if not dy.is_cuda:
         _check_host(dy, ys, dt, "dy")
         _check_host(w, ws, dt, "w")
-        return _host_call(d, lambda dd, a, b, _bias, o, st: gbconv_bwd_data(dd, a, b, o, st), "gbconv_bwd_data",
-                          dy, w, None, ys, xs, dx)
+        return _host_call(d, GBCONV_OP_BWD_DATA, dy, w, None, xs, dx)
     _check(dy, ys, dt, "dy")
     _check(w, ws, dt, "w")
     out = dx if dx is not None else torch.empty(xs, dtype=dt, device=dy.device)
@@ -461,7 +535,7 @@ def conv_transpose(d: Desc, x, w, bias=None, y=None):
         _check_host(w, ws, dt, "w")
         if bias is not None:
             _check_host(bias, (d.c_in,), torch.float32, "bias")
-        return _host_call(d, gbconv_conv_transpose, "gbconv_conv_transpose", x, w, bias, ys, xs, y)
+        return _host_call(d, GBCONV_OP_BWD_DATA, x, w, bias, xs, y)
     _check(x, ys, dt, "x")
     _check(w, ws, dt, "w")
     if bias is not None:

@@ -52,6 +52,8 @@ constexpr int64_t kMax32 = 2147483647;
 
 }  // namespace
 
+bool launch_context(Launch* l, void* stream) { return device_context(l, stream); }
+
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 gbconv_status resolve(const gbconv_desc* d, Problem* p) {

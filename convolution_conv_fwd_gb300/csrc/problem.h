@@ -54,6 +54,9 @@ struct Launch {
   uint64_t wait_ns;      // bound of the kernels' barrier waits (gbconv_set_wait_limit_ns)
 };
 
+// The launch context of the current device for `stream` (false if a CUDA query failed).
+bool launch_context(Launch* l, void* stream);
+
 gbconv_status launch_direct_fwd(const Problem& p, const void* x, const void* w, const float* bias, void* y,
                                 const Launch& l);
 // The dgrad launchers add an optional fp32 bias [C_in] after the gather sum (transposed convolution).

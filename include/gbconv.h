@@ -151,6 +151,59 @@ gbconv_status gbconv_fwd(const gbconv_desc *desc, const void *x, const void *w, 
  * Enqueues exactly one kernel on `stream`.  Deterministic: the same inputs give bitwise-equal dx. */
 gbconv_status gbconv_bwd_data(const gbconv_desc *desc, const void *dy, const void *w, void *dx, void *stream);
 
+/* Bytes of device staging buffer that gbconv_fwd_host (op GBCONV_OP_FWD; with_bias nonzero when a bias
+ * is passed), gbconv_bwd_data_host or gbconv_conv_transpose_host (op GBCONV_OP_BWD_DATA) needs for this descriptor: the weight,
+ * the bias, the whole source batch and the whole result batch, each rounded up to 256 bytes.
+ * Launches nothing.  Returns GBCONV_EINVAL for a NULL argument, another op, or a shape the call would
+ * reject. */
+gbconv_status gbconv_host_staging_bytes(const gbconv_desc *desc, int32_t op, int32_t with_bias, int64_t *bytes);
+
+/* gbconv_fwd on HOST buffers: synchronous (done_event NULL), or enqueued with a completion event.
+ *   x, w, bias, y : host memory in the layouts gbconv_fwd takes (bias float [C_out] or NULL).
+ *                   Page-locked (pinned) memory lets the copies overlap the kernels; pageable memory
+ *                   works too, without the overlap.
+ *   staging       : device, at least gbconv_host_staging_bytes(desc, GBCONV_OP_FWD, bias != NULL) bytes,
+ *                   256-byte aligned, owned by the caller; its contents are undefined afterwards.
+ *   slices        : batch slices to pipeline (clamped to [1, min(N, 16)]), or 0 for the library's
+ *                   choice, about sqrt(result bytes / 512 KiB) slices.  One slice runs every step on
+ *                   `stream` itself.
+ *   stream        : the call's copies and kernels start after the work already enqueued there.  A
+ *                   call of one slice without a completion event runs on `stream` itself; otherwise
+ *                   the copies in, the kernels and the copies out run on three streams the library
+ *                   creates per device on first use.
+ *   done_event    : NULL: the call returns once y holds the result, and `stream` also waits for every
+ *                   copy of the call.  Else a cudaEvent_t (as void*) of the current device that the
+ *                   call records when y holds the result, returning as soon as everything is
+ *                   enqueued: x, w, bias, y and the staging buffer must then stay valid and untouched
+ *                   until the event completes (also after an error return, when it is recorded after
+ *                   whatever was enqueued).  Independent calls made this way overlap one call's last
+ *                   copy out with the next call's copies in.
+ * The batch is cut into slices of consecutive images.  The copy in of slice i+1 (host to device), the
+ * kernel of slice i and the copy out of slice i-1 (device to host) run at the same time.  Each slice
+ * is one gbconv_fwd call on the staging buffer, so the results are those of gbconv_fwd on the same
+ * batch slices (and equal to one call on the whole batch: images are independent).  The enqueueing of host calls on one device is
+ * serialised; their copies run in call order.
+ * Returns the first failing slice's status, GBCONV_EINVAL for NULL buffers or a staging buffer that is
+ * too small or misaligned (nothing enqueued then), GBCONV_ECUDA for a failed copy, and, synchronous
+ * only, GBCONV_ETIMEOUT (clearing the record) when a kernel of the library on this device recorded an
+ * expired internal wait by the end of the call; with a completion event gbconv_device_status reports
+ * that, as for the device-pointer calls. */
+gbconv_status gbconv_fwd_host(const gbconv_desc *desc, const void *x, const void *w, const float *bias, void *y,
+                              void *staging, int64_t staging_bytes, int32_t slices, void *stream, void *done_event);
+
+/* gbconv_bwd_data on HOST buffers (dy, w and dx in host memory), pipelined, synchronous or with a
+ * completion event, as gbconv_fwd_host; staging of at least
+ * gbconv_host_staging_bytes(desc, GBCONV_OP_BWD_DATA, 0) bytes. */
+gbconv_status gbconv_bwd_data_host(const gbconv_desc *desc, const void *dy, const void *w, void *dx, void *staging,
+                                   int64_t staging_bytes, int32_t slices, void *stream, void *done_event);
+
+/* gbconv_conv_transpose on HOST buffers (x, w, bias float [C_in] or NULL, y in host memory), pipelined,
+ * synchronous or with a completion event, as gbconv_fwd_host; staging of at least
+ * gbconv_host_staging_bytes(desc, GBCONV_OP_BWD_DATA, bias != NULL) bytes. */
+gbconv_status gbconv_conv_transpose_host(const gbconv_desc *desc, const void *x, const void *w, const float *bias,
+                                         void *y, void *staging, int64_t staging_bytes, int32_t slices, void *stream,
+                                         void *done_event);
+
 /* Transposed convolution forward, y = conv_transpose(x, w) (+ bias): by definition the input gradient
  * above applied to x, plus a per-channel bias (oarust `conv_transpose_1d` / `conv_transpose_2d`
  * compute the same scatter with an IOK weight).  desc describes the convolution being transposed:

@@ -9,6 +9,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -214,6 +215,42 @@ def test_bwd_filter_workspace_and_argument_checks(gb):
     assert gb._lib.gbconv_bwd_filter_workspace(ctypes.byref(d), None) == gb.GBCONV_EINVAL
     k = ctypes.c_int32(-1)
     assert gb._lib.gbconv_select(ctypes.byref(d), 3, ctypes.byref(k)) == gb.GBCONV_EINVAL
+
+
+def test_host_staging_bytes_and_argument_checks(gb):
+    """The host-buffer calls' staging buffer holds the weight, the bias, the whole source batch and the
+    whole result batch, each rounded up to 256 bytes; argument errors come back before any CUDA call."""
+    kw = shape_kw(n=2, in_size=(9, 7), c_in=16, c_out=8)
+    d = lib_desc(gb, kw)
+    c = oracle_conv(kw)
+    r256 = lambda b: (b + 255) // 256 * 256
+    nbytes = lambda shape: 2 * int(np.prod(shape))
+    x_b, y_b, w_b = nbytes(c.x_shape()), nbytes(c.y_shape()), nbytes(c.w_shape())
+    assert gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_FWD) == r256(w_b) + r256(x_b) + r256(y_b)
+    assert gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_FWD, True) == r256(w_b) + r256(4 * 8) + r256(x_b) + r256(y_b)
+    assert gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_BWD_DATA) == r256(w_b) + r256(y_b) + r256(x_b)
+    assert gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_BWD_DATA, True) == (r256(w_b) + r256(4 * 16) + r256(y_b) +
+                                                                           r256(x_b))
+    b = ctypes.c_int64(0)
+    assert gb._lib.gbconv_host_staging_bytes(ctypes.byref(d), gb.GBCONV_OP_BWD_FILTER, 0,
+                                             ctypes.byref(b)) == gb.GBCONV_EINVAL
+    assert gb._lib.gbconv_host_staging_bytes(ctypes.byref(d), gb.GBCONV_OP_FWD, 0, None) == gb.GBCONV_EINVAL
+    bad = lib_desc(gb, shape_kw(k=(40, 3)))
+    assert gb._lib.gbconv_host_staging_bytes(ctypes.byref(bad), gb.GBCONV_OP_FWD, 0, ctypes.byref(b)) == gb.GBCONV_EINVAL
+    need = gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_FWD)
+    fake = 1 << 20  # never dereferenced: the calls below fail their checks first
+    assert gb.gbconv_fwd_host(d, None, fake, None, fake, fake, need, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, fake, None, None, fake, fake, need, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, fake, fake, None, None, fake, need, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, fake, fake, None, fake, None, need, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, fake, fake, None, fake, fake, need - 1, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, fake, fake, None, fake, fake + 16, need, 0, None) == gb.GBCONV_EINVAL
+    # with a bias the staging buffer must also hold it
+    assert gb.gbconv_fwd_host(d, fake, fake, fake, fake, fake, need, 0, None) == gb.GBCONV_EINVAL
+    need_dg = gb.gbconv_host_staging_bytes(d, gb.GBCONV_OP_BWD_DATA)
+    assert gb.gbconv_bwd_data_host(d, fake, fake, fake, fake, need_dg - 256, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_conv_transpose_host(d, fake, fake, fake, fake, fake, need_dg, 0, None) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(bad, fake, fake, None, fake, fake, need, 0, None) == gb.GBCONV_EINVAL
 
 
 def test_describe_weight_gradient_stride_phases(gb):

@@ -368,8 +368,7 @@ def _pinned(torch, arr_f32, bits=None):
 
 @pytest.mark.parametrize("case", range(len(HOST)), ids=["%s-%d" % (op, i) for i, (_, op) in enumerate(HOST)])
 def test_host_buffers_match_oracle(gb, case, monkeypatch):
-    monkeypatch.setattr(gb, "_PIPE_MIN_BYTES", 0)
-    monkeypatch.setattr(gb, "_PIPE_SLICES", 4)  # batches of 3-6 in 4 slices: uneven slices
+    monkeypatch.setattr(gb, "HOST_SLICES", 4)  # batches of 3-6 in 4 slices: uneven slices
     kw, op = HOST[case]
     d = lib_desc(gb, kw)
     c = oracle_conv(kw)
