@@ -278,6 +278,10 @@ SMALL = [
               dil=(1,), layout="nlc", wlayout="oki"), "fwd", "smallgroup"),
     (shape_kw(n=1, in_size=(8, 8), c_in=64, c_out=64, groups=16, wlayout="oihw"), "fwd", "smallgroup"),
     (shape_kw(n=1, in_size=(20, 66), c_in=192, c_out=192, groups=48, stride=(1, 2), pad=(1, 1)), "fwd", "smallgroup"),
+    # outputs 56 and 112 wide, partial and whole 32-column tiles (8 channels per group: the generic
+    # path; 2 per group: the compile-time 3x3)
+    (shape_kw(n=1, in_size=(10, 112), c_in=128, c_out=128, groups=16, bias=True), "fwd", "smallgroup"),
+    (shape_kw(n=2, in_size=(9, 56), c_in=64, c_out=64, groups=32, bias=True), "fwd", "smallgroup"),
     # their input gradients: the tiled kernel at stride 1 (transposed, flipped weights), the gather otherwise
     (shape_kw(n=2, in_size=(13, 37), c_in=64, c_out=64, groups=16), "dgrad", "smallgroup_dgrad"),
     (shape_kw(n=1, in_size=(12, 11), c_in=128, c_out=128, groups=16, dil=(2, 2), pad=(2, 2)), "dgrad",
@@ -291,6 +295,7 @@ SMALL = [
      "smallgroup_dgrad"),
     (shape_kw(n=2, in_size=(12, 13), c_in=64, c_out=64, groups=32, stride=(3, 2), wlayout="oihw"), "dgrad",
      "smallgroup_dgrad"),
+    (shape_kw(n=1, in_size=(10, 56), c_in=128, c_out=128, groups=16), "dgrad", "smallgroup_dgrad"),
     # grouped dense convolutions on the tensor cores: one implicit GEMM per group (group views of the
     # activations, group offsets into the weight and the output); whole and partial 64-channel k-blocks
     # per group, C_out/G != C_in/G, strides (stride-phase sources / phases), 1x1, tiles wider than a group
