@@ -23,6 +23,7 @@ ranks and ``value`` the work of all ranks over that time.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -396,10 +397,13 @@ def run_gpu(args, rank, world, local_rank):
         host_cases.append((c, hs, hw, hb))
         h2d += hs.numel() * hs.element_size() + hw.numel() * hw.element_size() + (0 if hb is None else hb.numel() * 4)
         d2h += out.numel() * out.element_size()
-    # The five calls are independent: enqueued back to back, largest host-to-device transfer first (while
-    # it streams, the host enqueues the rest, so the link never waits for the host), then every result
-    # is waited on.
-    host_cases.sort(key=lambda hc: -(hc[1].numel() * hc[1].element_size()))
+    # The five calls are independent: enqueued back to back, then every result is waited on.  The
+    # largest host-to-device transfer goes first (while it streams, the host enqueues the rest, so the
+    # link never waits for the host), the others by result size (a long copy back overlaps the later
+    # calls' copies in instead of ending the step).
+    nbytes = lambda t: t.numel() * t.element_size()
+    biggest_in = max(nbytes(hc[1]) for hc in host_cases)
+    host_cases.sort(key=lambda hc: (nbytes(hc[1]) < biggest_in, -nbytes(hc[0]["copies"][0][3])))
 
     def e2e_step():
         calls = [gb.conv_bwd_data_async(c["d"], hs, hw) if c["wl"].op == "dgrad" else
@@ -409,11 +413,18 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dev)
+    # Host-timed: as timeit does, Python's cyclic garbage collector is run before the timed steps and
+    # kept off during them (a full collection of this process's objects takes tens of ms).
+    gc.collect()
+    gc.disable()
+    try:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dev)
+    finally:
+        gc.enable()
 
     total_flops = sum(c["flops"] for c in cases)
     step_flops = sum(c["flops"] * len(c["copies"]) for c in cases)
@@ -456,7 +467,7 @@ def run_gpu(args, rank, world, local_rank):
                 "path": "one batch of each workload per step from pinned host tensors through the public host "
                         "calls (conv_fwd_async / conv_bwd_data_async: batch slices pipelined through a device "
                         "staging buffer), the five calls enqueued back to back and every result waited on inside "
-                        "the timed region, largest transfer first"},
+                        "the timed region; largest transfer in first, then by result size"},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
