@@ -158,3 +158,59 @@ def test_async_calls_in_flight_together(gb):
         assert call.done() and not got.is_cuda
         check_bf16(to_host_f64(torch, got), ref, scale)
     assert gb.gbconv_device_status(torch.cuda.current_stream().cuda_stream) == gb.GBCONV_OK
+
+
+def test_pageable_buffers_given_output_and_3d(gb):
+    """Host tensors that are not page-locked (the copies then do not overlap, but the results are the
+    same), a caller-given result tensor, and a 3-D shape, through the public calls."""
+    kw = shape_kw(spatial_dims=3, n=3, in_size=(4, 9, 11), c_in=64, c_out=64, k=(3, 3, 3), stride=(1, 1, 1),
+                  pad=(1, 1, 1), dil=(1, 1, 1), layout="ndhwc", wlayout="odhwi", bias=True)
+    d = lib_desc(gb, kw)
+    c = oracle_conv(kw)
+    inp = draw(c, "bf16", 4900, op="fwd", bias=True)
+    x = torch.from_numpy(np.ascontiguousarray(inp["x_bits"]).view(np.int16)).view(torch.bfloat16)  # pageable
+    w = torch.from_numpy(np.ascontiguousarray(inp["w_bits"]).view(np.int16)).view(torch.bfloat16)
+    b = torch.from_numpy(inp["b"].astype(np.float32))
+    _, _, ys = gb.desc_shapes(d)
+    y = torch.full(ys, 7.0, dtype=torch.bfloat16)  # pageable, given by the caller
+    assert not x.is_pinned() and not y.is_pinned()
+    ref = oracle.conv_fwd(c, inp["x"], inp["w"], inp["b"])
+    scale = scale_fwd(c, inp["x"], inp["w"], inp["b"])
+    got = gb.conv_fwd(d, x, w, b, y)
+    assert got is y
+    check_bf16(to_host_f64(torch, y), ref, scale)
+    y.fill_(7.0)
+    call = gb.conv_fwd_async(d, x, w, b, y)
+    assert call.wait() is y
+    check_bf16(to_host_f64(torch, y), ref, scale)
+    # its input gradient through the synchronous host call, four slices of three images
+    g = draw(c, "bf16", 4901, op="dgrad")
+    dy = torch.from_numpy(np.ascontiguousarray(g["g_bits"]).view(np.int16)).view(torch.bfloat16)
+    xs, _, _ = gb.desc_shapes(d)
+    dx = torch.empty(xs, dtype=torch.bfloat16)
+    stg, n = _staging(gb, d, gb.GBCONV_OP_BWD_DATA, False)
+    w2 = torch.from_numpy(np.ascontiguousarray(g["w_bits"]).view(np.int16)).view(torch.bfloat16)
+    assert gb.gbconv_bwd_data_host(d, dy.data_ptr(), w2.data_ptr(), dx.data_ptr(), stg.data_ptr(), n, 4,
+                                   torch.cuda.current_stream().cuda_stream) == gb.GBCONV_OK
+    check_bf16(to_host_f64(torch, dx), oracle.conv_dgrad(c, g["g"], g["w"]), scale_dgrad(c, g["g"], g["w"]))
+
+
+def test_host_call_errors_raise(gb):
+    """Argument errors of the host calls come back as exceptions before anything is enqueued."""
+    kw = shape_kw(n=2, in_size=(9, 7), c_in=64, c_out=64)
+    d = lib_desc(gb, kw)
+    xs, ws, ys = gb.desc_shapes(d)
+    x = torch.zeros(xs, dtype=torch.bfloat16).pin_memory()
+    w = torch.zeros(ws, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(ValueError):
+        gb.conv_fwd_async(d, torch.zeros((1, 2, 3, 4), dtype=torch.bfloat16), w)  # wrong shape
+    with pytest.raises(ValueError):
+        gb.conv_fwd_async(d, x, w, y=torch.zeros((1,), dtype=torch.bfloat16))  # wrong result shape
+    stg, n = _staging(gb, d, gb.GBCONV_OP_FWD, False)
+    st = torch.cuda.current_stream().cuda_stream
+    y = torch.empty(ys, dtype=torch.bfloat16).pin_memory()
+    assert gb.gbconv_fwd_host(d, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), stg.data_ptr(), n - 256, 0,
+                              st) == gb.GBCONV_EINVAL
+    assert gb.gbconv_fwd_host(d, x.data_ptr(), w.data_ptr(), None, y.data_ptr(), stg.data_ptr() + 128, n, 0,
+                              st) == gb.GBCONV_EINVAL
+    assert gb.gbconv_device_status(st) == gb.GBCONV_OK
