@@ -346,7 +346,10 @@ class HostCall:
     def __del__(self):
         # the copies still read and write the tensors this object holds
         if getattr(self, "_event", None) is not None:
-            self._event.synchronize()
+            try:
+                self._event.synchronize()
+            except Exception:  # interpreter shutdown: the CUDA context may already be gone
+                pass
 
 
 def _host_call(d: Desc, op: int, src, w, bias, out_shape, out=None, wait=True):
