@@ -17,7 +17,9 @@
 // (j = the atom), which is tap (kh, kw = KW-1-j) of the weight gradient.  ceil(KH/2) such MMAs per
 // 16 positions cover every tap (a 3x3: two MMAs of M=128, N=192, the second one half used).
 //
-// Work: one CTA per (64-channel input block, 64-channel output block, chunk of output rows).  A chunk
+// Work: one CTA per (64-channel input block, group of nco 64-channel output blocks, chunk of output
+// rows); nco = 2 where the accumulators fit TMEM twice, so that x is loaded once for two output blocks
+// (each output block has its own dy region and its own MMAs, into its own TMEM columns).  A chunk
 // is a run of row blocks (RB rows, with RB*P a multiple of 8 so every TMA box lands on a 1024-byte
 // boundary); it is loaded whole into shared memory as boxes of RB virtual rows (x and dy, one
 // barrier each) and swept by the MMAs as the boxes land.  At the end the accumulators go to the
@@ -76,7 +78,9 @@ struct TcArgs {
   int P;                  // virtual grid pitch OW + (KWP-1)*ddc
   int RB;                 // virtual rows per TMA box
   int box_bytes;          // RB * P * 128
-  int cb_in, pairs, chunks, units;  // units: pairs x chunks x KD x nph
+  int cb_in, pairs, chunks, units;  // pairs: (input block, output block group); units: pairs x chunks x KD x nph
+  int nco;                // output blocks per unit (1 or 2)
+  int y_bytes;            // one output block's dy region: front pad, a segment's boxes, tail
   int bpi, total_blocks;  // row blocks per image (a (batch, depth) slice when 3-D), row blocks in the batch
   int seg_blocks;         // row blocks one shared-memory load holds
   int xe;                 // x boxes a segment needs beyond its dy boxes
@@ -184,17 +188,18 @@ __device__ __forceinline__ void issue_steps(int tn, uint32_t tmem, uint32_t ncol
   }
 }
 
-// GM: MMA groups per 16 positions (ceil(KH/2)), a template parameter so a block of steps issues its
-// MMAs back to back: scalar work between MMAs in the issuing thread adds directly to their time.
-template <int GM>
+// GM: MMA groups per 16 positions (ceil(KH/2)), and NCO: output blocks per unit (a.nco), template
+// parameters so a block of steps issues its MMAs back to back: scalar work between MMAs in the issuing
+// thread adds directly to their time.
+template <int GM, int NCO>
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xs = smem;
-  uint8_t* ys = smem + a.x_bytes;  // position 0 of the dy region; the dy rows start at kFront
-  const int y_bytes = ((kFront * 128 + a.seg_blocks * a.box_bytes + a.tail * 128) + 1023) & ~1023;
-  uint64_t* xbar = reinterpret_cast<uint64_t*>(ys + y_bytes);
+  uint8_t* ys = smem + a.x_bytes;  // position 0 of output block 0's dy region; the dy rows start at kFront
+  const int y_bytes = a.y_bytes;   // output block c's region starts c * y_bytes later
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(ys + NCO * y_bytes);
   uint64_t* ybar = xbar + kMaxBoxes;
   uint64_t* seg_done = ybar + kMaxBoxes;
   uint64_t* acc_full = seg_done + 1;
@@ -202,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* fin = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t tmem_cols = GM * a.KWP * 64 <= 256 ? 256u : 512u;
+  const uint32_t acc_cols = uint32_t(GM * a.KWP * 64);  // TMEM columns of one output block's accumulators
+  const uint32_t tmem_cols = NCO * acc_cols <= 256 ? 256u : 512u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -227,9 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ zero fill and TMA producer
-    for (int i = lane; i < kFront * 8; i += 32)  // the front pad, never written by TMA
-      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ptx::smem_addr(ys) + uint32_t(i) * 16u), "r"(0u)
-                   : "memory");
+#pragma unroll
+    for (int c = 0; c < NCO; ++c)  // the front pads, never written by TMA
+      for (int i = lane; i < kFront * 8; i += 32)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ptx::smem_addr(ys) + uint32_t(c * y_bytes + i * 16)),
+                     "r"(0u)
+                     : "memory");
     if (lane == 0) {
       ptx::prefetch_tmap(&maps.x);
       ptx::prefetch_tmap(&maps.dy);
@@ -239,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t xph = 0, yph = 0;  // bit b: the phase parity box barrier b completes next
     for (int u = int(blockIdx.x); ok && u < a.units; u += int(gridDim.x)) {
       const Unit un(a, u);
-      const int cib = un.pair % a.cb_in, cob = un.pair / a.cb_in;
+      const int cib = un.pair % a.cb_in, cob = (un.pair / a.cb_in) * NCO;  // the group's first output block
       SegWalk walk(a, un.chunk);
       Segment sg;
       while (ok && walk.next(sg)) {
@@ -252,9 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // longer earlier segment may have left dy rows there), then order the writes before the
         // tensor core's reads.
         const uint32_t tail0 = ptx::smem_addr(ys) + uint32_t(kFront * 128 + sg.nb * a.box_bytes);
-        for (int i = lane; i < a.tail * 8; i += 32)
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(tail0 + uint32_t(i) * 16u), "r"(0u)
-                       : "memory");
+#pragma unroll
+        for (int c = 0; c < NCO; ++c)
+          for (int i = lane; i < a.tail * 8; i += 32)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(tail0 + uint32_t(c * y_bytes + i * 16)), "r"(0u)
+                         : "memory");
         ptx::fence_proxy_async_smem();
         __syncwarp();
         const int nxb = sg.nb + a.xe;
@@ -275,14 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tma_load_4d(ptx::smem_addr(xs) + uint32_t(b * a.box_bytes), &maps.x, xbar + b, cib * 64, xc0, xrow,
                           sg.n);
-            if (b < sg.nb) {
-              ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(a.box_bytes));
-              if (a.OD > 0)
-                tma_load_5d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
-                            cob * 64, 0, row0 + b * a.RB, od, nn);
-              else
-                tma_load_4d(ptx::smem_addr(ys) + uint32_t(kFront * 128 + b * a.box_bytes), &maps.dy, ybar + b,
-                            cob * 64, 0, row0 + b * a.RB, sg.n);
+            if (b < sg.nb) {  // box b of every output block of the group, on one barrier
+              ptx::mbar_arrive_expect_tx(ybar + b, uint32_t(NCO * a.box_bytes));
+              for (int c = 0; c < NCO; ++c) {
+                const uint32_t dst = ptx::smem_addr(ys) + uint32_t(c * y_bytes + kFront * 128 + b * a.box_bytes);
+                if (a.OD > 0)
+                  tma_load_5d(dst, &maps.dy, ybar + b, (cob + c) * 64, 0, row0 + b * a.RB, od, nn);
+                else
+                  tma_load_4d(dst, &maps.dy, ybar + b, (cob + c) * 64, 0, row0 + b * a.RB, sg.n);
+              }
             }
           }
         }
@@ -334,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd0 = desc_mn_sw128(ptx::smem_addr(ys) + uint32_t(kFront - (nkw - 1) * ddc) * 128u,
                                            uint32_t(ddc) * 128u);
         const uint32_t b_lo0 = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+        const uint32_t b_next = uint32_t(y_bytes) >> 4;  // the next output block's dy region, in the start field
         SegWalk walk(a, un.chunk);
         Segment sg;
         bool first = true;
@@ -353,11 +366,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const uint32_t a_lo = a_lo0 + uint32_t(t0) * 128u, b_lo = b_lo0 + uint32_t(t0) * 128u;
             const uint32_t acc0 = (first && t0 == 0) ? 0u : 1u;
-            // every group of the kernel (the unit-stride case), or a stride phase's fewer ones
-            if (gmu == GM)
-              issue_steps<GM>(tn, tmem, ncols, a_lo, a_hi, g_step, b_lo, b_hi, idesc, acc0);
-            else
-              issue_steps<1>(tn, tmem, ncols, a_lo, a_hi, g_step, b_lo, b_hi, idesc, acc0);
+            // every group of the kernel (the unit-stride case), or a stride phase's fewer ones; each
+            // output block of the unit into its own accumulators
+#pragma unroll
+            for (int c = 0; c < NCO; ++c) {
+              if (gmu == GM)
+                issue_steps<GM>(tn, tmem + uint32_t(c) * acc_cols, ncols, a_lo, a_hi, g_step, b_lo + uint32_t(c) * b_next,
+                                b_hi, idesc, acc0);
+              else
+                issue_steps<1>(tn, tmem + uint32_t(c) * acc_cols, ncols, a_lo, a_hi, g_step, b_lo + uint32_t(c) * b_next,
+                               b_hi, idesc, acc0);
+            }
           }
           ptx::mma_commit(seg_done);
           xph ^= (1u << nxb) - 1u;
@@ -412,19 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (stop) break;
       ptx::tc_fence_after();
       const Unit un(a, u);
-      const int cib = un.pair % a.cb_in, cob = un.pair / a.cb_in;
+      const int cib = un.pair % a.cb_in, cob0 = (un.pair / a.cb_in) * NCO;
       const int ci = cib * 64 + cil;
       float* const wsc = a.ws + size_t(un.chunk) * a.ws_stride;
       const int nkh = a.ph_nkh[un.ph], nkw = a.ph_nkw[un.ph];
+      for (int ob = 0; ob < NCO; ++ob)  // the unit's output blocks, each with its own accumulators
       for (int g = 0; g < (nkh + 1) / 2; ++g) {
         const int ri = 2 * g + i_atom;
         const int kh = ri < nkh ? a.ph_kh[un.ph][ri] : -1;
         for (int cc = h; cc < 4 * nkw; cc += 2) {  // 16-column chunks
           uint32_t v[16];
-          ptx::tmem_ld_16(tmem + lane_base + uint32_t(g * a.KWP * 64 + cc * 16), v);
+          ptx::tmem_ld_16(tmem + lane_base + uint32_t(ob) * acc_cols + uint32_t(g * a.KWP * 64 + cc * 16), v);
           ptx::tmem_ld_wait();
           const int kw = a.ph_kw[un.ph][nkw - 1 - (cc >> 2)];
-          const int co0 = cob * 64 + (cc & 3) * 16;
+          const int co0 = (cob0 + ob) * 64 + (cc & 3) * 16;
           if (kh >= 0 && ci < a.Cin) {
             float* dst = wsc + (((size_t(co0) * a.KD + un.kd) * a.KH + kh) * a.KW + kw) * a.Cin + ci;
             const int nco = min(16, a.Cout - co0);
@@ -553,27 +573,33 @@ bool plan(const Problem& p, int sms, TcPlan& pl) {
   const int64_t reach = int64_t(2 * gm - 1) * ddr * P + (kwp - 1) * ddc + 16;
   a.xe = int((reach + a.RB * P - 1) / (a.RB * P));
   a.tail = int((kwp - 1) * ddc + 16);
+  // Two output blocks per unit where the output has an even number of them, both accumulator sets fit
+  // TMEM, and a segment of at least two row blocks still fits the shared memory (x is then loaded
+  // once for both); else one.
+  const int cb_out = int((p.Cout + 63) / 64);
   a.seg_blocks = 0;
-  for (int sb = kMaxBoxes - a.xe; sb >= 1; --sb) {
-    const int64_t xb = int64_t(sb + a.xe) * a.box_bytes;
-    const int64_t yb = ((int64_t(kFront + a.tail) * 128 + int64_t(sb) * a.box_bytes) + 1023) & ~int64_t(1023);
-    const int64_t total = 1024 + xb + yb + (2 * kMaxBoxes + 4) * 8 + 16;
-    if (total <= kSmemLimit) {
-      a.seg_blocks = sb;
-      a.x_bytes = int(xb);
-      // at least half the SM's shared memory: one CTA per SM, so no second CTA waits for TMEM
-      pl.smem = size_t(std::max<int64_t>(total, kSmemLimit / 2 + 1024));
-      break;
+  for (int nco = (cb_out % 2 == 0 && 2 * gm * kwp * 64 <= 512) ? 2 : 1; nco >= 1 && a.seg_blocks == 0; --nco)
+    for (int sb = kMaxBoxes - a.xe; sb >= (nco == 2 ? 2 : 1); --sb) {
+      const int64_t xb = int64_t(sb + a.xe) * a.box_bytes;
+      const int64_t yb = ((int64_t(kFront + a.tail) * 128 + int64_t(sb) * a.box_bytes) + 1023) & ~int64_t(1023);
+      const int64_t total = 1024 + xb + nco * yb + (2 * kMaxBoxes + 4) * 8 + 16;
+      if (total <= kSmemLimit) {
+        a.seg_blocks = sb;
+        a.nco = nco;
+        a.x_bytes = int(xb);
+        a.y_bytes = int(yb);
+        // at least half the SM's shared memory: one CTA per SM, so no second CTA waits for TMEM
+        pl.smem = size_t(std::max<int64_t>(total, kSmemLimit / 2 + 1024));
+        break;
+      }
     }
-  }
   if (a.seg_blocks == 0) return false;
   a.bpi = int((p.OH + a.RB - 1) / a.RB);
   const int64_t tb = p.N * (deep ? p.OD : 1) * a.bpi;  // row blocks over every (batch, depth) slice
   if (tb >= (int64_t(1) << 30)) return false;
   a.total_blocks = int(tb);
   a.cb_in = int((p.Cin + 63) / 64);
-  const int cb_out = int((p.Cout + 63) / 64);
-  a.pairs = a.cb_in * cb_out;
+  a.pairs = a.cb_in * (cb_out / a.nco);
   // one unit per SM: chunks x pairs x kernel-depth taps x stride phases (a chunk is swept once per
   // depth tap and phase)
   a.chunks = int(std::max<int64_t>(1, std::min<int64_t>(tb, sms / (a.pairs * a.KD * nph))));
@@ -634,9 +660,9 @@ bool wgrad_tc_describe(const Problem& p, char* buf, size_t len) {
   const TcArgs& a = pl.a;
   std::snprintf(buf, len,
                 "wgrad_tc pairs=%d chunks=%d units=%d grid=%d rows_per_box=%d pitch=%d seg_blocks=%d x_extra=%d "
-                "groups=%d n=%d depth_taps=%d phases=%d smem=%zu",
+                "groups=%d n=%d depth_taps=%d phases=%d out_blocks=%d smem=%zu",
                 a.pairs, a.chunks, a.units, pl.grid, a.RB, a.P, a.seg_blocks, a.xe, a.gm, 64 * a.KWP, a.KD, a.nph,
-                pl.smem);
+                a.nco, pl.smem);
   return true;
 }
 
@@ -651,14 +677,16 @@ gbconv_status launch_wgrad_tc(const Problem& p, const void* x, const void* dy, v
   a.ws_stride = int(p.w_elems() + (db ? p.Cout : 0));
   TcMaps maps;
   if (!encode(pl, x, dy, maps)) return GBCONV_ECUDA;
-  auto kern = a.gm == 1 ? wgrad_tc_kernel<1> : wgrad_tc_kernel<2>;
-  static std::atomic<int> raised[2][64];
+  auto kern = a.gm == 1 ? (a.nco == 2 ? wgrad_tc_kernel<1, 2> : wgrad_tc_kernel<1, 1>)
+                        : (a.nco == 2 ? wgrad_tc_kernel<2, 2> : wgrad_tc_kernel<2, 1>);
+  static std::atomic<int> raised[4][64];
+  const int variant = (a.gm - 1) * 2 + (a.nco - 1);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBCONV_ECUDA;
-  if (!raised[a.gm - 1][dev].load(std::memory_order_acquire)) {
+  if (!raised[variant][dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
       return GBCONV_ECUDA;
-    raised[a.gm - 1][dev].store(1, std::memory_order_release);
+    raised[variant][dev].store(1, std::memory_order_release);
   }
   if (launch_kernel(kern, dim3(pl.grid), dim3(kThreads), pl.smem, l.stream, maps, a) != cudaSuccess)
     return GBCONV_ECUDA;

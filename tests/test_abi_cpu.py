@@ -257,10 +257,13 @@ def test_describe_weight_gradient_stride_phases(gb):
     # a unit per (chunk, block pair, stride phase); each phase the unit-stride sum over its own taps
     _, _, f = _plan(gb, shape_kw(n=32, in_size=(56, 56), c_in=64, c_out=64), op=2)
     assert f["phases"] == "1" and f["groups"] == "2" and f["n"] == "192" and f["pitch"] == "58"
+    assert f["out_blocks"] == "1"  # one 64-channel output block
     # 3x3 stride 2: phases {1} x {1}, {1} x {0, 2}, {0, 2} x {1}, {0, 2} x {0, 2}; the pitch is OW + 1
     _, _, f = _plan(gb, shape_kw(n=32, in_size=(56, 56), c_in=128, c_out=128, stride=(2, 2)), op=2)
     assert f["phases"] == "4" and f["groups"] == "1" and f["n"] == "128" and f["pitch"] == "29"
-    assert int(f["units"]) == 4 * 4 * int(f["chunks"]) and int(f["units"]) <= 152
+    # two output blocks per unit (x loaded once for both): 2 input blocks x 1 output-block pair x 4 phases
+    assert f["out_blocks"] == "2"
+    assert int(f["units"]) == 2 * 4 * int(f["chunks"]) and int(f["units"]) <= 152
     # 7x7 stride 2: four kernel rows and columns in the (0, 0) phase -> two groups, N = 256
     _, _, f = _plan(gb, shape_kw(n=8, in_size=(112, 112), c_in=64, c_out=64, k=(7, 7), pad=(3, 3), stride=(2, 2)), op=2)
     assert f["phases"] == "4" and f["groups"] == "2" and f["n"] == "256"

@@ -637,6 +637,8 @@ WGRAD = [
     # phase); (begin, end) padding at stride 2; 3-D at H/W stride 2
     (shape_kw(n=2, in_size=(15, 14), c_in=32, c_out=48, k=(1, 1), pad=(0, 0), stride=(2, 2)), "wgrad"),
     (shape_kw(n=2, in_size=(15, 14), c_in=64, c_out=128, k=(3, 3), pad=(1, 1), stride=(2, 2)), "wgrad"),
+    # two output blocks per unit (x loaded once for both), the second block 32 channels wide, two input blocks
+    (shape_kw(n=3, in_size=(30, 29), c_in=128, c_out=96, k=(3, 3), pad=(1, 1), stride=(2, 2)), "wgrad"),
     (shape_kw(n=1, in_size=(21, 20), c_in=24, c_out=64, k=(7, 7), pad=(3, 3), stride=(2, 2)), "wgrad"),
     (shape_kw(n=2, in_size=(12, 11), c_in=64, c_out=64, k=(3, 3), pad=(1, 1), stride=(2, 1)), "wgrad"),
     (shape_kw(n=2, in_size=(13, 14), c_in=64, c_out=64, k=(3, 3), pad=(1, 1), stride=(3, 3)), "wgrad"),
