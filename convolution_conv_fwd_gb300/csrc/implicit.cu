@@ -248,8 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* emptyA = fullA + a.sa;
   uint64_t* fullB = emptyA + a.sa;
   uint64_t* emptyB = fullB + a.sb;
+  // One k-block, resident weights and one source: an item's halo stage and every weight tile stay in
+  // shared memory for all of its MMAs, so its sub-tiles can be issued one after the other, each
+  // committed to its own barrier, and the epilogue starts on sub-tile 0 while sub-tile 1's MMAs run
+  // (for a CTA's last item nothing else overlaps its epilogue).
+  constexpr bool kSubMajor = !TPOS && !DGRAD && BRES && !MSRC && NSUB > 1;
+  // Accumulator-full barriers: one per TMEM buffer, or one per buffer and sub-tile where the
+  // sub-tiles may be issued one after the other.
+  constexpr int kTf = kSubMajor ? NSUB : 1;
   uint64_t* tfull = emptyB + a.sb;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* tempty = tfull + 2 * kTf;
   uint64_t* bres = tempty + 2;
   uint64_t* fin = bres + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
@@ -259,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.sa; ++i) { ptx::mbar_init(fullA + i, 1); ptx::mbar_init(emptyA + i, 1); }
     for (int i = 0; i < a.sb; ++i) { ptx::mbar_init(fullB + i, 1); ptx::mbar_init(emptyB + i, 1); }
-    for (int i = 0; i < 2; ++i) { ptx::mbar_init(tfull + i, 1); ptx::mbar_init(tempty + i, kEpiWarps * 32); }
+    for (int i = 0; i < 2 * kTf; ++i) ptx::mbar_init(tfull + i, 1);
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(tempty + i, kEpiWarps * 32);
     ptx::mbar_init(bres, 1);
     ptx::mbar_init(fin, 1);
     *abort_flag = 0;
@@ -395,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ptx::mbar_wait(tempty + buf, ((iter >> 1) & 1) ^ 1, abort_flag, status, 2u, wait_ns))) break;
         ptx::tc_fence_after();
         const uint32_t acc = tmem + uint32_t(buf * NSUB * BN);
+        bool sub_committed = false;  // the sub-tile-major path commits each sub-tile itself
         if (ph.ntaps > 0) {
           const int q0 = it.m * 128 * NSUB;
           const int row0 = q0 - (q0 / ph.P) * ph.P;  // tile start inside the halo block
@@ -408,6 +418,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Source 0's tap range and rotation, worked out once per item: scalar work between MMA
           // bursts delays the issue (one source is the common case: unit stride, every dgrad).
           const int nsrc = MSRC ? ph.nsrc : 1, nt0 = ph.src_t0[1], tc0 = item % nt0;
+          if (kSubMajor && kbn == 1) {
+            if ((ok = ptx::mbar_wait(fullA + sa, pa, abort_flag, status, 2u, wait_ns))) {
+              const uint32_t a_addr = ptx::smem_addr(a_base + size_t(sa) * a_stage);
+#pragma unroll 1
+              for (int s = 0; s < NSUB; ++s) {
+                int tc = tc0, off_c = toff[tc], w_c = tw[tc];
+                for (int ti = 0; ti < nt0; ++ti) {
+                  const int tn = tc + 1 == nt0 ? 0 : tc + 1;
+                  const int off_n = toff[tn], w_n = tw[tn];
+                  const uint64_t ad0 = desc_sw128_kmajor(a_addr + uint32_t(row0 + off_c) * 128);
+                  const uint64_t bd0 = desc_sw128_kmajor(ptx::smem_addr(b_base + size_t(w_c) * kBTile));
+                  const uint32_t a_lo = uint32_t(ad0) + uint32_t((s * 128 * 128) >> 4), a_hi = uint32_t(ad0 >> 32);
+                  const uint32_t b_lo = uint32_t(bd0), b_hi = uint32_t(bd0 >> 32);
+#pragma unroll
+                  for (int j = 0; j < kKB / 16; ++j)
+                    ptx::mma_bf16_lohi(acc + s * BN, a_lo + uint32_t((j * 32) >> 4), a_hi, b_lo + uint32_t((j * 32) >> 4),
+                                       b_hi, kIdesc, (ti | j) == 0 ? 0u : 1u);
+                  tc = tn;
+                  off_c = off_n;
+                  w_c = w_n;
+                }
+                ptx::mma_commit(tfull + buf * kTf + s);
+              }
+              ptx::mma_commit(emptyA + sa);
+              if (++sa == n_sa) { sa = 0; pa ^= 1; }
+              sub_committed = true;
+            }
+          } else
           for (int kbi = 0; ok && kbi < kbn; ++kbi) {
             const int kb = kbi + kb_rot < kbn ? kbi + kb_rot : kbi + kb_rot - kbn;  // the producer's order
             for (int src = 0; ok && src < nsrc; ++src) {
@@ -464,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        ptx::mma_commit(tfull + buf);
+        if (!sub_committed)
+          for (int s = 0; s < kTf; ++s) ptx::mma_commit(tfull + buf * kTf + s);
       }
       ptx::mma_commit(fin);
       // Even after an abort, every MMA issued so far must complete before TMEM is freed and the CTA
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode_item(phase_s, a.nphase, a.n_tiles, a.G, item);
       const PhaseHdr& ph = phase_s[it.phase];
       const int buf = iter & 1;
-      const bool got = ptx::mbar_wait(tfull + buf, (iter >> 1) & 1, abort_flag, a.status, 4u, a.wait_ns);
+      const bool got = ptx::mbar_wait(tfull + buf * kTf, (iter >> 1) & 1, abort_flag, a.status, 4u, a.wait_ns);
       // Every thread times its own wait, so after an expired wait the 64 threads of a warp pair could
       // disagree, and a thread that carried on would block at the pair barrier below for good: the
       // pair takes one decision (leave if any of its threads gave up).
@@ -579,8 +618,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+      bool stopped = false;
 #pragma unroll 1
       for (int s = 0; s < NSUB; ++s) {
+        if (kTf > 1 && s > 0) {
+          // Sub-tile s's accumulators have their own barrier (the MMAs may run sub-tile by sub-tile);
+          // the warp pair again takes one decision.
+          const bool got_s = ptx::mbar_wait(tfull + buf * kTf + s, (iter >> 1) & 1, abort_flag, a.status, 4u, a.wait_ns);
+          uint32_t stop_s;
+          asm volatile(
+              "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 64, p;\n\t"
+              "selp.u32 %0, 1, 0, q;\n\t}"
+              : "=r"(stop_s)
+              : "r"(uint32_t(got_s)), "r"(1 + quad)
+              : "memory");
+          if (stop_s) { stopped = true; break; }
+          ptx::tc_fence_after();
+        }
         const int qbase = it.m * 128 * NSUB + s * 128 + quad * 32;
 #pragma unroll 1
         for (int g = 0; g < BN / kG; ++g) {
@@ -661,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.stage_bufs == 1) asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
         }
       }
+      if (stopped) break;
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty + buf);
@@ -954,7 +1009,7 @@ bool plan_geometry(const Problem& p, bool dgrad, Plan& pl) {
     for (int bufs = pl.tpos ? 1 : 2; bufs >= 1; --bufs) {
       const size_t fixed = 1024 + (pl.tpos ? size_t(kTposStage) : bufs * block) + size_t(a.bias_n) * 4 +
                            size_t(kMaxPhases) * 2 * kMaxTapsPerPhase * 4 + kMaxPhases * sizeof(PhaseHdr) +
-                           8 * (2 * 4 + 2 * 8 + 6) + 16;
+                           8 * (2 * 4 + 2 * 8 + 8) + 16;
       // streamed weights: at least four weight stages before a third activation stage
       for (int min_sb = pl.bres ? 1 : 4; min_sb >= (pl.bres ? 1 : 3); --min_sb)
       for (int sa = 3; sa >= 2; --sa) {
