@@ -417,12 +417,18 @@ def run_gpu(args, rank, world, local_rank):
     # kept off during them (a full collection of this process's objects takes tens of ms).
     gc.collect()
     gc.disable()
+    e2e_steps = []  # each step ends with every result waited on, so the host clock brackets it
+    # At least 100 steps (about 0.17 s): the mean of a host-timed loop of 20 steps (33 ms) moved by
+    # tens of percent with one pause of the host.
+    e2e_n = max(args.steps, 100)
     try:
         t0 = time.perf_counter()
-        for _ in range(args.steps):
+        for _ in range(e2e_n):
+            ts = time.perf_counter()
             e2e_step()
+            e2e_steps.append((time.perf_counter() - ts) * 1e3)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dev)
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_n, dev)
     finally:
         gc.enable()
 
@@ -464,6 +470,9 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": round(job_rate(world, total_flops, e2e_ms), 4), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "steps": e2e_n,
+                "step_ms": {"min": round(min(e2e_steps), 3), "median": round(statistics.median(e2e_steps), 3),
+                            "max": round(max(e2e_steps), 3)},
                 "path": "one batch of each workload per step from pinned host tensors through the public host "
                         "calls (conv_fwd_async / conv_bwd_data_async: batch slices pipelined through a device "
                         "staging buffer), the five calls enqueued back to back and every result waited on inside "
